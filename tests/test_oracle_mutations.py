@@ -1,0 +1,113 @@
+"""The pins have teeth: plant a plausible mistake in the oracle (on the CPU, by
+monkeypatching one function) and check that at least one pin then fails."""
+import numpy as np
+import pytest
+
+from oracle import msa_oracle as O
+from tests import test_oracle_pins as P
+
+
+def _rope_adjacent_pairs(x, pos, rope_dim=64, base=1.0e7):
+    x = np.asarray(x, dtype=np.float64)
+    ang = np.asarray(pos, dtype=np.float64)[:, None] * O.rope_inv_freq(rope_dim, base)[None, :]
+    shape = (x.shape[0],) + (1,) * (x.ndim - 2) + (rope_dim // 2,)
+    c, s = np.cos(ang).reshape(shape), np.sin(ang).reshape(shape)
+    y = x.copy()
+    y[..., 0:rope_dim:2] = x[..., 0:rope_dim:2] * c - x[..., 1:rope_dim:2] * s
+    y[..., 1:rope_dim:2] = x[..., 1:rope_dim:2] * c + x[..., 0:rope_dim:2] * s
+    return y
+
+
+def _norm_without_one(x, w, eps=1e-6):
+    x = np.asarray(x, dtype=np.float64)
+    return x / np.sqrt(np.mean(x * x, axis=-1, keepdims=True) + eps) * w
+
+
+def _norm_eps_outside(x, w, eps=1e-6):
+    x = np.asarray(x, dtype=np.float64)
+    return x / (np.sqrt(np.mean(x * x, axis=-1, keepdims=True)) + 1e-2) * (1 + w)
+
+
+def _select_higher_id_on_tie(scores, own, topk=O.TOPK):
+    s = scores.copy()
+    n = s.shape[1]
+    s = s + 1e-12 * np.arange(n)[None, :]      # breaks ties towards the higher id
+    return _ORIG["select_from_scores"](s, own, topk)
+
+
+def _select_own_not_forced(scores, own, topk=O.TOPK):
+    n = scores.shape[0]
+    sel = np.full((n, topk), -1, dtype=np.int64)
+    for r in range(n):
+        cand = np.arange(int(own[r]) + 1)
+        order = cand[np.argsort(-scores[r, :len(cand)], kind="stable")]
+        ids = np.sort(order[:topk])
+        sel[r, :len(ids)] = ids
+    return sel, np.full(n, np.inf)
+
+
+def _keys_one_past_causal(sel_row, p, block=O.BLOCK):
+    # off by one: lets the key right after the query through (j <= p + 1)
+    parts = [np.arange(b * block, min((b + 1) * block, p + 2)) for b in sel_row if b >= 0]
+    return np.concatenate(parts)
+
+
+def _keys_ignore_selection(sel_row, p, block=O.BLOCK):
+    return np.arange(p + 1)
+
+
+def _grads_without_delta(qt, do_t, kJ, vJ, scale):
+    logits = scale * (qt @ kJ.T)
+    e = np.exp(logits - logits.max(axis=1, keepdims=True))
+    P_ = e / e.sum(axis=1, keepdims=True)
+    return P_, P_ * (do_t @ vJ.T)
+
+
+def _grads_transposed_dp(qt, do_t, kJ, vJ, scale):
+    logits = scale * (qt @ kJ.T)
+    e = np.exp(logits - logits.max(axis=1, keepdims=True))
+    P_ = e / e.sum(axis=1, keepdims=True)
+    o = P_ @ vJ
+    dP = do_t @ kJ.T                        # wrong operand: K instead of V
+    return P_, P_ * (dP - np.sum(do_t * o, axis=1, keepdims=True))
+
+
+def _scores_no_causal(qi, ki, rows=None, block=O.BLOCK):
+    L = qi.shape[0]
+    nb = (L + block - 1) // block
+    rows = np.arange(L) if rows is None else np.asarray(rows)
+    s = qi[rows] @ ki.T
+    out = np.stack([s[:, b * block:(b + 1) * block].max(axis=1) for b in range(nb)], axis=1)
+    out[np.arange(nb)[None, :] > (rows // block)[:, None]] = -np.inf
+    return out
+
+
+_ORIG = {"select_from_scores": O.select_from_scores}
+
+MUTATIONS = [
+    ("partial_rope", _rope_adjacent_pairs, [P.test_rope_matches_complex_rotation]),
+    ("gemma_rmsnorm", _norm_without_one, [P.test_gemma_rmsnorm_matches_torch_rms_norm]),
+    ("gemma_rmsnorm", _norm_eps_outside, [P.test_gemma_rmsnorm_zero_weight_gives_unit_rms]),
+    ("select_from_scores", _select_higher_id_on_tie, [P.test_selection_tie_prefers_lower_block]),
+    ("select_from_scores", _select_own_not_forced, [P.test_selection_invariants]),
+    ("_keys_of", _keys_one_past_causal,
+     [P.test_sparse_forward_and_backward_match_masked_library_attention]),
+    ("_keys_of", _keys_ignore_selection,
+     [P.test_sparse_forward_and_backward_match_masked_library_attention]),
+    ("_row_grads", _grads_without_delta, [P.test_backward_finite_differences]),
+    ("_row_grads", _grads_transposed_dp, [P.test_backward_finite_differences]),
+    ("block_scores_seq", _scores_no_causal, [P.test_block_scores_brute_force]),
+]
+
+
+@pytest.mark.parametrize("name,fn,pins", MUTATIONS,
+                         ids=[f"{m[0]}-{m[1].__name__}" for m in MUTATIONS])
+def test_planted_mistake_is_caught(monkeypatch, name, fn, pins):
+    monkeypatch.setattr(O, name, fn)
+    caught = False
+    for pin in pins:
+        try:
+            pin()
+        except (AssertionError, ValueError, IndexError):
+            caught = True
+    assert caught, f"no pin caught the planted mistake in {name}"

@@ -1,0 +1,402 @@
+"""Pins for the CPU oracle: library routines, closed forms, invariants, brute force
+on tiny inputs and the facts the pages state.  None of these calls the CUDA path."""
+import itertools
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+import torch.nn.functional as F
+
+from oracle import msa_oracle as O
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+FACTS = json.load(open(os.path.join(HERE, "golden", "msa_page_facts.json")))
+
+
+def rng(seed=0):
+    return np.random.default_rng(seed)
+
+
+# ------------------------------------------------------------------ bf16 rounding
+
+def test_bf16_round_matches_torch_on_float32_values():
+    r = rng(1)
+    x = np.concatenate([
+        r.standard_normal(20000) * 10.0 ** r.integers(-40, 38, 20000),
+        r.standard_normal(2000) * 1e-39,                 # bf16 subnormals
+        np.array([0.0, -0.0, 1.0, -2.5, 3.0e38, -3.3e38]),
+    ]).astype(np.float32)
+    # exact halfway points between neighbouring bf16 values
+    base = torch.randn(4000, dtype=torch.float32).to(torch.bfloat16).float().numpy()
+    half = (base.view(np.uint32) | np.uint32(0x8000)).view(np.float32)
+    x = np.concatenate([x, half])
+    want = torch.from_numpy(x).to(torch.bfloat16).double().numpy()
+    got = O.bf16_round(x.astype(np.float64))
+    np.testing.assert_array_equal(got, want)
+
+
+def test_bf16_round_from_float64_is_single_rounding():
+    # 1 + 2^-8 is halfway between 1 and 1 + 2^-7: ties go to the even value 1.
+    assert O.bf16_round(1.0 + 2.0 ** -8) == 1.0
+    # slightly above halfway (not representable in float32) must round up.
+    assert O.bf16_round(1.0 + 2.0 ** -8 + 2.0 ** -40) == 1.0 + 2.0 ** -7
+    # 1 + 3*2^-8 is halfway between 1+2^-7 and 1+2^-6: even is 1+2^-6.
+    assert O.bf16_round(1.0 + 3 * 2.0 ** -8) == 1.0 + 2.0 ** -6
+    assert O.bf16_round(2.0 ** -133) == 2.0 ** -133
+    assert O.bf16_round(0.49 * 2.0 ** -133) == 0.0
+    assert np.isinf(O.bf16_round(3.4e38))
+
+
+# ------------------------------------------------------------------ prologue
+
+def test_gemma_rmsnorm_matches_torch_rms_norm():
+    r = rng(2)
+    x = r.standard_normal((7, 3, 128)) * 3.0
+    w = r.standard_normal(128) * 0.1
+    want = F.rms_norm(torch.from_numpy(x), (128,), weight=torch.from_numpy(1.0 + w),
+                      eps=1e-6).numpy()
+    np.testing.assert_allclose(O.gemma_rmsnorm(x, w, 1e-6), want, rtol=1e-12, atol=1e-12)
+
+
+def test_gemma_rmsnorm_zero_weight_gives_unit_rms():
+    x = rng(3).standard_normal((50, 128)) * 7.0
+    y = O.gemma_rmsnorm(x, np.zeros(128), eps=0.0)
+    np.testing.assert_allclose(np.sqrt(np.mean(y * y, axis=-1)), 1.0, rtol=1e-12)
+
+
+def test_rope_matches_complex_rotation():
+    # channel i and i+32 form the complex number x_i + i*x_{i+32}; RoPE multiplies
+    # it by exp(i * p * base^(-2i/64)); channels 64..127 pass through.
+    r = rng(4)
+    T, H = 9, 2
+    x = r.standard_normal((T, H, 128))
+    pos = r.integers(0, 40000, T)
+    base = FACTS["rope_base"]["value"]
+    y = O.partial_rope(x, pos, 64, base)
+    theta = base ** (-np.arange(32) * 2.0 / 64.0)
+    z = (x[..., :32] + 1j * x[..., 32:64]) * np.exp(1j * pos[:, None, None] * theta)
+    np.testing.assert_allclose(y[..., :32], z.real, rtol=1e-9, atol=1e-9)
+    np.testing.assert_allclose(y[..., 32:64], z.imag, rtol=1e-9, atol=1e-9)
+    np.testing.assert_array_equal(y[..., 64:], x[..., 64:])
+
+
+def test_rope_closed_form_values():
+    x = np.zeros((2, 1, 128))
+    x[:, 0, 0] = 1.0     # pair (0, 32) has frequency 1
+    x[:, 0, 31] = 1.0    # pair (31, 63) has frequency base^(-62/64)
+    y = O.partial_rope(x, np.array([0, 1]), 64, 1e7)
+    np.testing.assert_allclose(y[0, 0], x[0, 0], atol=0)          # p = 0 is the identity
+    assert y[1, 0, 0] == pytest.approx(math.cos(1.0), abs=1e-15)
+    assert y[1, 0, 32] == pytest.approx(math.sin(1.0), abs=1e-15)
+    f = 1e7 ** (-62.0 / 64.0)
+    assert y[1, 0, 31] == pytest.approx(math.cos(f), abs=1e-15)
+    assert y[1, 0, 63] == pytest.approx(math.sin(f), abs=1e-15)
+
+
+def test_rope_relative_position_and_norm():
+    r = rng(5)
+    q = r.standard_normal((1, 1, 128))
+    k = r.standard_normal((1, 1, 128))
+    def dot(p1, p2):
+        a = O.partial_rope(q, np.array([p1]), 64, 1e7)
+        b = O.partial_rope(k, np.array([p2]), 64, 1e7)
+        return float(np.sum(a * b))
+    assert dot(100, 37) == pytest.approx(dot(1100, 1037), rel=1e-9)
+    assert dot(5, 5) == pytest.approx(float(np.sum(q * k)), rel=1e-9)
+    y = O.partial_rope(q, np.array([12345]), 64, 1e7)
+    assert np.linalg.norm(y[..., :64]) == pytest.approx(np.linalg.norm(q[..., :64]), rel=1e-12)
+
+
+def test_positions_restart_per_sequence():
+    np.testing.assert_array_equal(O.positions([0, 3, 5, 5, 9]),
+                                  [0, 1, 2, 0, 1, 0, 1, 2, 3])
+
+
+def test_prologue_is_norm_then_rope_then_bf16():
+    r = rng(6)
+    cu = [0, 130, 300]
+    x = r.standard_normal((300, 2, 128))
+    w = r.standard_normal(128) * 0.1
+    y = O.qk_norm_rope(x, w, cu)
+    xt = torch.from_numpy(x)
+    n = F.rms_norm(xt, (128,), weight=torch.from_numpy(1.0 + w), eps=1e-6).numpy()
+    pos = np.concatenate([np.arange(130), np.arange(170)])
+    ref = O.partial_rope(n, pos, 64, 1e7)
+    np.testing.assert_array_equal(y, O.bf16_round(ref))
+    assert np.all(O.bf16_round(y) == y)
+
+
+# ------------------------------------------------------------------ indexer
+
+def _brute_scores(qi, ki, block):
+    L = qi.shape[0]
+    nb = (L + block - 1) // block
+    out = np.full((L, nb), -np.inf)
+    for t in range(L):
+        for b in range(nb):
+            for j in range(b * block, min((b + 1) * block, t + 1)):
+                out[t, b] = max(out[t, b], float(np.dot(qi[t], ki[j])))
+    return out
+
+
+def test_block_scores_brute_force():
+    r = rng(7)
+    qi = r.standard_normal((23, 8))
+    ki = r.standard_normal((23, 8))
+    np.testing.assert_array_equal(O.block_scores_seq(qi, ki, block=4), _brute_scores(qi, ki, 4))
+
+
+def test_selection_is_best_subset_by_enumeration():
+    # the top-(k-1) earlier blocks are the subset of that size with the largest
+    # total score; check against enumeration of all subsets on tiny inputs.
+    r = rng(8)
+    block, topk = 4, 3
+    for trial in range(20):
+        L = int(r.integers(1, 40))
+        qi = r.standard_normal((L, 6))
+        ki = r.standard_normal((L, 6))
+        sc = _brute_scores(qi, ki, block)
+        own = np.arange(L) // block
+        sel, _ = O.select_from_scores(sc, own, topk)
+        for t in range(L):
+            o = own[t]
+            m = min(topk - 1, o)
+            best = max(itertools.combinations(range(o), m), key=lambda c: sum(sc[t, list(c)]))
+            want = sorted(list(best) + [o]) + [-1] * (topk - 1 - m)
+            assert list(sel[t]) == want
+
+
+def test_selection_tie_prefers_lower_block():
+    sc = np.array([[5.0, 7.0, 5.0, 5.0, 1.0, 0.0]])
+    sel, gap = O.select_from_scores(sc, np.array([5]), topk=3)
+    assert list(sel[0]) == [0, 1, 5]
+    assert gap[0] == 0.0
+
+
+def _small_pack(seed, seqlens, hi=2, d=32):
+    r = rng(seed)
+    T = sum(seqlens)
+    cu = np.concatenate([[0], np.cumsum(seqlens)])
+    return r.standard_normal((T, hi, d)), r.standard_normal((T, hi, d)), cu
+
+
+def test_selection_invariants():
+    qi, ki, cu = _small_pack(9, [2500, 100, 3000, 1])
+    sel, gap = O.index_select(qi, ki, cu)
+    pos = O.positions(cu)
+    for t in range(len(pos)):
+        own = pos[t] // 128
+        for h in range(qi.shape[1]):
+            ids = sel[t, h][sel[t, h] >= 0]
+            assert own in ids
+            assert ids.max() == own
+            assert len(ids) == min(16, own + 1) == len(set(ids))
+            assert np.all(np.diff(ids) > 0)
+            assert np.all(sel[t, h][len(ids):] == -1)
+    # the result does not depend on the logit scale
+    sel2, _ = O.index_select(qi * 0.37, ki, cu)
+    np.testing.assert_array_equal(sel, sel2)
+
+
+def test_selection_keeps_every_block_up_to_2048_tokens():
+    n = FACTS["dense_equivalent_tokens"]["value"]
+    assert n == FACTS["topk_blocks"]["value"] * FACTS["block"]["value"]
+    qi, ki, cu = _small_pack(10, [n + 1], hi=1)
+    sel, gap = O.index_select(qi, ki, cu)
+    for t in range(n):
+        assert list(sel[t, 0]) == list(range(t // 128 + 1)) + [-1] * (15 - t // 128)
+        assert gap[t, 0] == np.inf
+    # token 2048 (17 causal blocks) is the first that drops one
+    assert len(set(sel[n, 0])) == 16 and np.isfinite(gap[n, 0])
+
+
+# ------------------------------------------------------------------ attention
+
+def _sdpa_masked(q, k, v, mask, scale):
+    """Library attention (fp64, torch CPU) with a boolean allow-mask per head."""
+    qt = torch.from_numpy(q).requires_grad_(True)
+    kt = torch.from_numpy(k).requires_grad_(True)
+    vt = torch.from_numpy(v).requires_grad_(True)
+    out = F.scaled_dot_product_attention(qt, kt, vt, attn_mask=torch.from_numpy(mask), scale=scale)
+    return qt, kt, vt, out
+
+
+def _allow_mask(sel_g, cu, block):
+    """allow[t, j]: j is in t's sequence, in one of t's selected blocks, and j <= t."""
+    T = sel_g.shape[0]
+    pos = O.positions(cu)
+    seq = np.searchsorted(cu, np.arange(T), side="right") - 1
+    allow = np.zeros((T, T), dtype=bool)
+    for t in range(T):
+        for j in range(T):
+            if seq[j] == seq[t] and pos[j] <= pos[t] and (pos[j] // block) in set(sel_g[t]):
+                allow[t, j] = True
+    return allow
+
+
+def _gqa_reference(q, k, v, do, sel, cu, scale, block):
+    """Dense library attention per KV group with the selection as a mask; returns
+    o, lse, dq, dk, dv from torch autograd in fp64."""
+    T, Hq, D = q.shape
+    Hkv = k.shape[1]
+    G = Hq // Hkv
+    o = np.zeros_like(q); lse = np.zeros((T, Hq))
+    dq = np.zeros_like(q); dk = np.zeros_like(k); dv = np.zeros_like(v)
+    for g in range(Hkv):
+        mask = _allow_mask(sel[:, g], cu, block)
+        qg = np.ascontiguousarray(q[:, g * G:(g + 1) * G].transpose(1, 0, 2))
+        kg = np.repeat(k[None, :, g], G, axis=0)
+        vg = np.repeat(v[None, :, g], G, axis=0)
+        qt, kt, vt, out = _sdpa_masked(qg, kg, vg, mask[None], scale)
+        out.backward(torch.from_numpy(np.ascontiguousarray(do[:, g * G:(g + 1) * G].transpose(1, 0, 2))))
+        o[:, g * G:(g + 1) * G] = out.detach().numpy().transpose(1, 0, 2)
+        logits = torch.from_numpy(qg) @ torch.from_numpy(kg).transpose(1, 2) * scale
+        logits = logits.masked_fill(~torch.from_numpy(mask)[None], float("-inf"))
+        lse[:, g * G:(g + 1) * G] = torch.logsumexp(logits, dim=-1).numpy().T
+        dq[:, g * G:(g + 1) * G] = qt.grad.numpy().transpose(1, 0, 2)
+        dk[:, g] = kt.grad.numpy().sum(0)
+        dv[:, g] = vt.grad.numpy().sum(0)
+    return o, lse, dq, dk, dv
+
+
+def test_dense_equivalence_up_to_2048_tokens():
+    """Every causal block is selected for sequences of <= 2048 tokens, so the
+    block-sparse forward equals plain causal attention (Megatron-Bridge MiniMax-M3
+    page, Known Limitations)."""
+    r = rng(11)
+    seqlens = [300, 700, 2048]
+    cu = np.concatenate([[0], np.cumsum(seqlens)])
+    T, Hq, Hkv, D = sum(seqlens), 4, 2, 16
+    q, k, v = (r.standard_normal((T, h, D)) for h in (Hq, Hkv, Hkv))
+    qi, ki = r.standard_normal((T, Hkv, D)), r.standard_normal((T, Hkv, D))
+    sel, _ = O.index_select(qi, ki, cu)
+    scale = 1 / math.sqrt(D)
+    o, lse = O.sparse_attn_fwd(q, k, v, sel, cu, scale)
+    G = Hq // Hkv
+    for s in range(len(seqlens)):
+        a, b = cu[s], cu[s + 1]
+        qq = torch.from_numpy(q[a:b].transpose(1, 0, 2).copy())
+        kk = torch.from_numpy(np.repeat(k[a:b], G, axis=1).transpose(1, 0, 2).copy())
+        vv = torch.from_numpy(np.repeat(v[a:b], G, axis=1).transpose(1, 0, 2).copy())
+        want = F.scaled_dot_product_attention(qq, kk, vv, is_causal=True, scale=scale)
+        np.testing.assert_allclose(o[a:b], want.numpy().transpose(1, 0, 2), rtol=1e-10, atol=1e-12)
+
+
+def test_sparse_forward_and_backward_match_masked_library_attention():
+    block, topk = 4, 3
+    r = rng(12)
+    seqlens = [13, 30, 1, 21]
+    cu = np.concatenate([[0], np.cumsum(seqlens)])
+    T, Hq, Hkv, D = sum(seqlens), 6, 2, 8
+    q, k, v, do = (r.standard_normal((T, h, D)) for h in (Hq, Hkv, Hkv, Hq))
+    qi, ki = r.standard_normal((T, Hkv, D)), r.standard_normal((T, Hkv, D))
+    sel, _ = O.index_select(qi, ki, cu, topk=topk, block=block)
+    assert np.any(sel[:, :, -1] >= 0) and np.any(O.positions(cu) // block >= topk)
+    scale = 0.3
+    o, lse = O.sparse_attn_fwd(q, k, v, sel, cu, scale, block=block)
+    ro, rlse, rdq, rdk, rdv = _gqa_reference(q, k, v, do, sel, cu, scale, block)
+    np.testing.assert_allclose(o, ro, rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(lse, rlse, rtol=1e-10, atol=1e-12)
+    dq, dk, dv = O.sparse_attn_bwd(q, k, v, do, sel, cu, scale, block=block)
+    np.testing.assert_allclose(dq, rdq, rtol=1e-9, atol=1e-11)
+    np.testing.assert_allclose(dk, rdk, rtol=1e-9, atol=1e-11)
+    np.testing.assert_allclose(dv, rdv, rtol=1e-9, atol=1e-11)
+    # sampled mode agrees with full mode
+    out = O.sparse_attn_bwd(q, k, v, do, sel, cu, scale, dq_tokens=[0, 20, 63],
+                            dkv_blocks=[(1, 0, 2), (3, 1, 0)], block=block)
+    np.testing.assert_allclose(out["dq"], dq[[0, 20, 63]], rtol=1e-12, atol=1e-13)
+    (dkb, dvb), (dkb2, dvb2) = out["dkv"]
+    np.testing.assert_allclose(dkb, dk[cu[1] + 8:cu[1] + 12, 0], rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(dvb2, dv[cu[3]:cu[3] + 4, 1], rtol=1e-12, atol=1e-13)
+
+
+def test_backward_finite_differences():
+    block, topk = 4, 2
+    r = rng(13)
+    cu = np.array([0, 11, 19])
+    T, Hq, Hkv, D = 19, 2, 1, 4
+    q, k, v, do = (r.standard_normal((T, h, D)) for h in (Hq, Hkv, Hkv, Hq))
+    sel, _ = O.index_select(r.standard_normal((T, 1, D)), r.standard_normal((T, 1, D)), cu,
+                            topk=topk, block=block)
+    scale = 0.7
+    loss = lambda q_, k_, v_: float(np.sum(O.sparse_attn_fwd(q_, k_, v_, sel, cu, scale, block=block)[0] * do))
+    dq, dk, dv = O.sparse_attn_bwd(q, k, v, do, sel, cu, scale, block=block)
+    h = 1e-6
+    for name, x, g in (("q", q, dq), ("k", k, dk), ("v", v, dv)):
+        for idx in [(0, 0, 0), (10, 0, 3), (15, 0, 1), (18, 0, 2)]:
+            if idx[1] >= x.shape[1]:
+                continue
+            xp = x.copy(); xp[idx] += h
+            xm = x.copy(); xm[idx] -= h
+            args_p = {"q": (xp, k, v), "k": (q, xp, v), "v": (q, k, xp)}[name]
+            args_m = {"q": (xm, k, v), "k": (q, xm, v), "v": (q, k, xm)}[name]
+            fd = (loss(*args_p) - loss(*args_m)) / (2 * h)
+            assert fd == pytest.approx(g[idx], rel=1e-6, abs=1e-8), (name, idx)
+
+
+def test_lse_and_normalisation():
+    r = rng(14)
+    cu = np.array([0, 2600])
+    q, k, v = r.standard_normal((2600, 2, 16)), r.standard_normal((2600, 1, 16)), np.ones((2600, 1, 16))
+    sel, _ = O.index_select(r.standard_normal((2600, 1, 16)), r.standard_normal((2600, 1, 16)), cu)
+    toks = [0, 5, 2047, 2048, 2599]
+    o, lse = O.sparse_attn_fwd(q, k, v, sel, cu, 0.25, tokens=toks)
+    np.testing.assert_allclose(o, 1.0, rtol=1e-12)    # softmax weights sum to one
+    for n, t in enumerate(toks):
+        own0 = (t // 128) * 128            # the own block is always attended
+        assert lse[n, 0] >= 0.25 * float(np.max(k[own0:t + 1, 0] @ q[t, 0])) - 1e-12
+        if t < 2048:                       # dense region: every key attended
+            lg = 0.25 * (k[:t + 1, 0] @ q[t, 0])
+            assert lse[n, 0] == pytest.approx(float(np.log(np.sum(np.exp(lg)))), rel=1e-12)
+
+
+# ------------------------------------------------------------------ decode
+
+def test_decode_equals_prefill_at_last_token():
+    r = rng(15)
+    lens = [2100, 130, 2560, 1]
+    Hq, Hkv, D = 4, 2, 16
+    pages_per = [(L + 127) // 128 for L in lens]
+    P = sum(pages_per)
+    perm = r.permutation(P)
+    maxp = max(pages_per)
+    table = np.full((len(lens), maxp), -1)
+    kc = np.zeros((P, Hkv, 128, D)); vc = np.zeros((P, Hkv, 128, D)); ic = np.zeros((P, Hkv, 128, D))
+    qd = r.standard_normal((len(lens), Hq, D)); qid = r.standard_normal((len(lens), Hkv, D))
+    pos = 0
+    for b, L in enumerate(lens):
+        kk, vv, ii = (r.standard_normal((L, Hkv, D)) for _ in range(3))
+        pg = perm[pos:pos + pages_per[b]]; pos += pages_per[b]
+        table[b, :len(pg)] = pg
+        for c, p in enumerate(pg):
+            n = min(128, L - 128 * c)
+            kc[p, :, :n] = kk[128 * c:128 * c + n].transpose(1, 0, 2)
+            vc[p, :, :n] = vv[128 * c:128 * c + n].transpose(1, 0, 2)
+            ic[p, :, :n] = ii[128 * c:128 * c + n].transpose(1, 0, 2)
+        # prefill view of the same sequence: the new token is the last one
+        qf = np.zeros((L, Hq, D)); qf[-1] = qd[b]
+        qif = np.zeros((L, Hkv, D)); qif[-1] = qid[b]
+        cu = np.array([0, L])
+        sel_p, gap_p = O.index_select(qif, ii, cu, tokens=[L - 1])
+        o_p, _ = O.sparse_attn_fwd(qf, kk, vv, _expand(sel_p, L), cu, 0.2, tokens=[L - 1])
+        o_d, sel_d, gap_d = O.decode_step(qd, qid, kc, vc, ic, table, lens, 0.2, batch=[b])
+        np.testing.assert_array_equal(sel_d[0], sel_p[0])
+        np.testing.assert_allclose(o_d[0], o_p[0], rtol=1e-11, atol=1e-12)
+
+
+def _expand(sel_last, L):
+    s = np.full((L,) + sel_last.shape[1:], -1, dtype=np.int64)
+    s[-1] = sel_last[0]
+    return s
+
+
+# ------------------------------------------------------------------ page facts
+
+def test_page_facts_fixture():
+    assert FACTS["hq"]["value"] // FACTS["hkv"]["value"] == 16
+    assert FACTS["index_heads"]["value"] == FACTS["hkv"]["value"]
+    assert FACTS["rope_dims"]["value"] * 2 == FACTS["d_head"]["value"]
+    assert O.BLOCK == FACTS["block"]["value"] and O.TOPK == FACTS["topk_blocks"]["value"]
