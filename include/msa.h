@@ -1,0 +1,197 @@
+/*
+ * msa.h -- C ABI of libmsa.so: MiniMax-M3 MSA block-sparse attention on one
+ * NVIDIA GB300 (sm_103a).
+ *
+ * What the library computes is defined on these pages:
+ *   "MiniMax-M3.1-Flash" (miles docs), section 1 "Model Introduction":
+ *       a 4-head indexer (dim 128, its own gemma q/k norm and RoPE) scores every
+ *       causal 128-token key block by its maximum logit; each query attends to
+ *       the 16 best blocks, its own block always included; index head h picks
+ *       the blocks of KV head h.  Attention is GQA, 64 query / 4 KV heads of
+ *       dim 128, with per-head gemma q/k norm and RoPE on the first 64 dims
+ *       (base 1e7).
+ *   same page, section 5.1 "Parallelism": the sparse attention runs on
+ *       THD-packed sequences (cu_seqlens).
+ *   same page, section 5.4 "Notable quirks": the indexer is frozen, so the
+ *       block selection gets no gradient.
+ *   "[1/4] Add MiniMax-M3 support - #4581" (radixark/miles), "Kernel tuning":
+ *       per-block max-logit scores, top-k select, forward and dQ/dK/dV
+ *       backward of the block-sparse attention kernel.
+ *   "MiniMax-M3" (Megatron-Bridge docs), "Architecture Notes": Gemma-style
+ *       RMSNorm x * (1 + w); "Known Limitations": 16 x 128 = 2048 keys per
+ *       query, so the method equals full causal attention up to that length.
+ *
+ * Conventions shared by every call
+ *   - Every pointer argument is a DEVICE pointer (cudaMalloc / torch CUDA
+ *     tensor memory), 16-byte aligned, contiguous in the stated layout, on
+ *     the device that is current when the call is made.
+ *   - bf16 means IEEE bfloat16 (2 bytes); compute is fp32 inside the kernels.
+ *   - D (head dim) is 128, the key block is 128 tokens, top-k is 16, the
+ *     rotated part is the first 64 channels: the library rejects other values.
+ *   - Packed (THD) inputs: token t of the pack belongs to sequence s with
+ *     cu_seqlens[s] <= t < cu_seqlens[s+1]; its position is t - cu_seqlens[s].
+ *     Key block b of sequence s covers positions [128 b, 128 b + 128); the last
+ *     block of a sequence may be partial.  cu_seqlens is int32 [S + 1] on the
+ *     device, cu_seqlens[0] = 0, non-decreasing, cu_seqlens[S] = T, and no
+ *     sequence longer than max_seqlen.  The library does not read device
+ *     memory on the host, so it cannot verify these contents: kernels clamp
+ *     indices and set MSA_STATUS_BOUNDS in the device status word instead of
+ *     reading or writing out of range.
+ *   - Selected block ids (sel) are int32 [T, H, 16], relative to the start of
+ *     the token's sequence, sorted ascending, padded with -1.
+ *   - GQA: query head i uses KV head i / (Hq / Hkv).
+ *   - Ownership: the caller allocates every buffer, including the workspace
+ *     (size from the matching *_workspace_size call, 256-byte aligned).  The
+ *     library never allocates or frees device memory and never synchronizes
+ *     the stream.  Outputs are fully overwritten.  Two calls that may run at
+ *     the same time need distinct workspaces.
+ *   - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default).
+ *   - Errors: argument checks run on the host before any launch and return
+ *     MSA_ERR_INVALID_ARG / MSA_ERR_UNSUPPORTED with nothing enqueued; a
+ *     failed launch returns MSA_ERR_CUDA.  msa_last_error() gives the message
+ *     of the calling thread's last failure.  Kernels never trap: a wait that
+ *     runs out or an index out of range sets a bit in the device status word,
+ *     read (and cleared) by msa_check_status().
+ */
+#ifndef MSA_H_
+#define MSA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define MSA_API __attribute__((visibility("default")))
+#else
+#define MSA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MSA_OK = 0,
+  MSA_ERR_INVALID_ARG = 1,  /* bad pointer, size, alignment or workspace */
+  MSA_ERR_UNSUPPORTED = 2,  /* a shape the library does not implement */
+  MSA_ERR_CUDA = 3,         /* a CUDA runtime call or launch failed */
+  MSA_ERR_TIMEOUT = 4,      /* msa_check_status: a kernel wait ran out */
+  MSA_ERR_BOUNDS = 5        /* msa_check_status: an index was out of range */
+} msa_status_t;
+
+/* A cudaStream_t passed through as an opaque handle. */
+typedef void* msa_stream_t;
+
+#define MSA_ABI_VERSION 1
+
+MSA_API int msa_abi_version(void);
+
+/* Message of the calling thread's most recent failed call ("" if none). */
+MSA_API const char* msa_last_error(void);
+
+/* Synchronizes `stream`, then reads and clears the device status word of the
+ * current device.  MSA_OK if no kernel reported a problem since the last
+ * check, MSA_ERR_TIMEOUT or MSA_ERR_BOUNDS otherwise.  Meant for tests and
+ * debugging; it blocks the host. */
+MSA_API msa_status_t msa_check_status(msa_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Prologue ("MiniMax-M3.1-Flash", 1 "Model Introduction"; "MiniMax-M3",
+ * "Architecture Notes").  In place on x, bf16 [T, H, 128]:
+ *   y = x / sqrt(mean(x^2) + eps) * (1 + w)        per (token, head), w bf16 [128]
+ *   then channels i and i + rope_dim/2 (i < rope_dim/2) are rotated by the
+ *   angle pos * rope_base^(-2 i / rope_dim), pos = the token's in-sequence
+ *   position; channels >= rope_dim pass through.  rope_dim must be 64.
+ * The four-tensor form runs q [T,Hq,128], k [T,Hkv,128], q_idx and k_idx
+ * [T,Hi,128] with their own weights in one launch; same result as four calls.
+ */
+MSA_API msa_status_t msa_qk_norm_rope(void* x, int T, int H, const void* w,
+                              const int32_t* cu_seqlens, int S, int rope_dim,
+                              float rope_base, float eps, msa_stream_t stream);
+
+MSA_API msa_status_t msa_qk_norm_rope4(void* q, int Hq, void* k, int Hkv, void* q_idx,
+                               void* k_idx, int Hi, const void* w_q, const void* w_k,
+                               const void* w_qi, const void* w_ki,
+                               const int32_t* cu_seqlens, int S, int T, int rope_dim,
+                               float rope_base, float eps, msa_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Index select ("MiniMax-M3.1-Flash", 1 "Model Introduction"; "#4581",
+ * "Kernel tuning").  q_idx, k_idx: post-prologue bf16 [T, Hi, 128].
+ * For token t at position p and index head h the own block is p / 128; every
+ * earlier block b of the sequence is scored by max_j q_idx[t,h] . k_idx[j,h]
+ * over its keys (fp32 accumulation); the own block plus the best
+ * min(15, own) earlier blocks (equal scores: lower id) are written to
+ * sel [T, Hi, 16] (ascending, -1 padded).  topk must be 16.
+ */
+MSA_API size_t msa_index_select_workspace_size(int T, int S, int Hi, int max_seqlen);
+
+MSA_API msa_status_t msa_index_select(const void* q_idx, const void* k_idx,
+                              const int32_t* cu_seqlens, int S, int T, int Hi,
+                              int max_seqlen, int topk, int32_t* sel, void* workspace,
+                              size_t workspace_bytes, msa_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Block-sparse attention forward ("MiniMax-M3.1-Flash", 1; "#4581").
+ * q bf16 [T, Hq, 128]; k, v bf16 [T, Hkv, 128]; sel int32 [T, Hkv, 16].
+ * For query head i of token t (KV head g = i / (Hq/Hkv)) the keys are those
+ * of the blocks in sel[t, g] at positions <= the query's position:
+ *   o[t, i]   = softmax(scale * q k_j) v_j            bf16 [T, Hq, 128]
+ *   lse[t, i] = log sum_j exp(scale * q k_j)         fp32 [T, Hq] (natural log)
+ * Hq / Hkv must divide 128.
+ */
+MSA_API size_t msa_sparse_attn_fwd_workspace_size(int T, int S, int Hq, int Hkv, int max_seqlen);
+
+MSA_API msa_status_t msa_sparse_attn_fwd(const void* q, const void* k, const void* v,
+                                 const int32_t* sel, const int32_t* cu_seqlens, int S,
+                                 int T, int Hq, int Hkv, int max_seqlen, float scale,
+                                 void* o, float* lse, void* workspace,
+                                 size_t workspace_bytes, msa_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Block-sparse attention backward ("#4581", "Kernel tuning"; the selection
+ * is constant: "MiniMax-M3.1-Flash", 5.4 "Notable quirks").
+ * Inputs as for the forward plus o (bf16, the forward's output), dout (bf16
+ * [T, Hq, 128], gradient of the loss w.r.t. o) and lse (fp32 [T, Hq]).
+ * With P = exp(scale q k^T - lse) over the attended keys, dP = dout v^T and
+ * Delta = rowsum(dout * o):  dS = P * (dP - Delta);
+ *   dq = scale dS k  (bf16 [T,Hq,128]),  dk = scale dS^T q,  dv = P^T dout
+ *   (bf16 [T,Hkv,128]; sums over all query heads and tokens using the key).
+ */
+MSA_API size_t msa_sparse_attn_bwd_workspace_size(int T, int S, int Hq, int Hkv, int max_seqlen);
+
+MSA_API msa_status_t msa_sparse_attn_bwd(const void* q, const void* k, const void* v,
+                                 const void* o, const void* dout, const float* lse,
+                                 const int32_t* sel, const int32_t* cu_seqlens, int S,
+                                 int T, int Hq, int Hkv, int max_seqlen, float scale,
+                                 void* dq, void* dk, void* dv, void* workspace,
+                                 size_t workspace_bytes, msa_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Decode step against a paged cache (scoring and selection rule of
+ * "MiniMax-M3.1-Flash", 1 "Model Introduction", applied to one new token).
+ * A page holds one 128-token block: k_cache, v_cache bf16 [num_pages, Hkv,
+ * 128, 128] and kidx_cache bf16 [num_pages, Hkv, 128, 128] (index head h =
+ * KV head h), post-prologue values.  block_table int32 [B, max_pages] maps
+ * block c of sequence b to a page; cache_lens int32 [B] counts the cached
+ * tokens INCLUDING the new one, whose position is cache_lens[b] - 1.
+ * q bf16 [B, Hq, 128] and q_idx bf16 [B, Hkv, 128] are the new token's
+ * post-prologue query and index query.  Per (b, h): every block up to the
+ * own block is scored by its max logit, the own block plus the best 15
+ * earlier ones are selected (sel_out int32 [B, Hkv, 16], may be NULL), and
+ * o bf16 [B, Hq, 128] is the attention of the 16 query heads of KV head h
+ * over the selected keys.
+ */
+MSA_API size_t msa_decode_step_workspace_size(int B, int Hq, int Hkv, int max_pages);
+
+MSA_API msa_status_t msa_decode_step(const void* q, const void* q_idx, const void* k_cache,
+                             const void* v_cache, const void* kidx_cache,
+                             const int32_t* block_table, const int32_t* cache_lens, int B,
+                             int Hq, int Hkv, int num_pages, int max_pages, float scale,
+                             void* o, int32_t* sel_out, void* workspace,
+                             size_t workspace_bytes, msa_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MSA_H_ */

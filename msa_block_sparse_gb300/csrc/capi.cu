@@ -1,0 +1,413 @@
+// C ABI of libmsa: argument validation, workspace layout, error reporting and
+// the per-call tile plan.  The compute kernels live in the other .cu files.
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <cudaTypedefs.h>
+
+#include "common.cuh"
+#include "kernels.cuh"
+
+namespace msa {
+
+// ------------------------------------------------------------------ errors
+
+static thread_local char g_last_error[512] = "";
+
+void set_error(const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_last_error, sizeof(g_last_error), fmt, ap);
+  va_end(ap);
+}
+
+msa_status_t fail(msa_status_t code, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_last_error, sizeof(g_last_error), fmt, ap);
+  va_end(ap);
+  return code;
+}
+
+msa_status_t check_launch(const char* what) {
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return fail(MSA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+  return MSA_OK;
+}
+
+// ------------------------------------------------------------------ status word
+
+__device__ uint32_t g_device_status;
+
+uint32_t* status_word() {
+  static uint32_t* ptrs[64] = {nullptr};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  if (!ptrs[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_device_status) != cudaSuccess) return nullptr;
+    ptrs[dev] = static_cast<uint32_t*>(p);
+  }
+  return ptrs[dev];
+}
+
+// ------------------------------------------------------------------ tensor maps
+
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+bool make_tmap_bf16(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
+                    const uint32_t* box) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t gdim[3], gstride[2];
+  cuuint32_t bdim[3], estr[3] = {1, 1, 1};
+  uint64_t stride = 2;
+  for (int i = 0; i < rank; ++i) {
+    gdim[i] = dims[i];
+    bdim[i] = box[i];
+    if (i > 0) gstride[i - 1] = stride;
+    stride *= dims[i];
+  }
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), gdim,
+                  gstride, bdim, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// ------------------------------------------------------------------ tile plan
+
+// One CTA.  nb(s) = ceil(len_s / 128) tiles per sequence; tiles are listed with
+// qb descending, s ascending.  cnt[q] = #{s : nb(s) > q}; start[q] = sum of
+// cnt[q'] for q' > q; thread q then appends (s, q) for every qualifying s in
+// order, so the list is deterministic.
+__global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ cu, int S,
+                                                    int max_nb, int2* __restrict__ tiles,
+                                                    int* __restrict__ num_tiles, int max_tiles,
+                                                    uint32_t* status) {
+  extern __shared__ int sh[];
+  int* cnt = sh;                // [max_nb + 1]
+  int* start = sh + max_nb + 1; // [max_nb + 1]
+  const int tid = threadIdx.x;
+  for (int q = tid; q <= max_nb; q += blockDim.x) cnt[q] = 0;
+  __syncthreads();
+  for (int s = tid; s < S; s += blockDim.x) {
+    int len = cu[s + 1] - cu[s];
+    int nb = (len + kBlock - 1) / kBlock;
+    if (len < 0 || nb > max_nb) {
+      atomicOr(status, kStatusBounds);
+      nb = len < 0 ? 0 : max_nb;
+    }
+    if (nb > 0) atomicAdd(&cnt[nb - 1], 1);   // histogram of nb - 1
+  }
+  __syncthreads();
+  // cnt[q] <- #{s : nb(s) - 1 >= q} (suffix sum), start[q] <- sum_{q' > q} cnt[q'].
+  if (tid == 0) {
+    int run = 0;
+    for (int q = max_nb - 1; q >= 0; --q) {
+      run += cnt[q];
+      cnt[q] = run;
+    }
+    int acc = 0;
+    for (int q = max_nb - 1; q >= 0; --q) {
+      start[q] = acc;
+      acc += cnt[q];
+    }
+    *num_tiles = acc < max_tiles ? acc : max_tiles;
+    if (acc > max_tiles) atomicOr(status, kStatusBounds);
+  }
+  __syncthreads();
+  for (int q = tid; q < max_nb; q += blockDim.x) {
+    int pos = start[q];
+    for (int s = 0; s < S; ++s) {
+      int len = cu[s + 1] - cu[s];
+      int nb = (len + kBlock - 1) / kBlock;
+      if (nb > max_nb) nb = max_nb;
+      if (nb > q && pos < max_tiles) tiles[pos++] = make_int2(s, q);
+    }
+  }
+}
+
+Plan carve_plan(WsCursor& ws, int T, int S) {
+  Plan p;
+  p.max_tiles = plan_max_tiles(T, S);
+  p.tiles = ws.take<int2>(p.max_tiles);
+  p.num_tiles = ws.take<int>(1);
+  return p;
+}
+
+msa_status_t launch_plan(const Plan& plan, const int32_t* cu_seqlens, int S, int max_seqlen,
+                         cudaStream_t stream) {
+  int max_nb = (max_seqlen + kBlock - 1) / kBlock;
+  size_t smem = 2 * (max_nb + 1) * sizeof(int);
+  plan_kernel<<<1, 1024, smem, stream>>>(cu_seqlens, S, max_nb, plan.tiles, plan.num_tiles,
+                                         plan.max_tiles, status_word());
+  return check_launch("plan_kernel");
+}
+
+}  // namespace msa
+
+using namespace msa;
+
+// ====================================================================== C ABI
+
+static msa_status_t check_pack(const int32_t* cu, int S, int T, int max_seqlen) {
+  if (!cu || !aligned16(cu)) return fail(MSA_ERR_INVALID_ARG, "cu_seqlens null or misaligned");
+  if (S < 1) return fail(MSA_ERR_INVALID_ARG, "S must be >= 1 (got %d)", S);
+  if (T < 1) return fail(MSA_ERR_INVALID_ARG, "T must be >= 1 (got %d)", T);
+  if (max_seqlen < 1 || max_seqlen > T)
+    return fail(MSA_ERR_INVALID_ARG, "max_seqlen %d outside [1, T=%d]", max_seqlen, T);
+  if (max_seqlen > kMaxSeqlen)
+    return fail(MSA_ERR_UNSUPPORTED, "max_seqlen %d above the supported %d", max_seqlen,
+                kMaxSeqlen);
+  return MSA_OK;
+}
+
+#define MSA_REQUIRE_PTR(p)                                                            \
+  do {                                                                                \
+    if (!(p) || !aligned16(p))                                                        \
+      return fail(MSA_ERR_INVALID_ARG, "%s is null or not 16-byte aligned", #p);      \
+  } while (0)
+
+#define MSA_TRY(expr)                 \
+  do {                                \
+    msa_status_t _s = (expr);         \
+    if (_s != MSA_OK) return _s;      \
+  } while (0)
+
+extern "C" {
+
+int msa_abi_version(void) { return MSA_ABI_VERSION; }
+
+const char* msa_last_error(void) { return g_last_error; }
+
+msa_status_t msa_check_status(msa_stream_t stream) {
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(MSA_ERR_CUDA, "stream sync: %s", cudaGetErrorString(e));
+  uint32_t* sw = status_word();
+  if (!sw) return fail(MSA_ERR_CUDA, "status word unavailable");
+  uint32_t v = 0;
+  e = cudaMemcpy(&v, sw, sizeof(v), cudaMemcpyDeviceToHost);
+  if (e == cudaSuccess) e = cudaMemset(sw, 0, sizeof(v));
+  if (e != cudaSuccess) return fail(MSA_ERR_CUDA, "status read: %s", cudaGetErrorString(e));
+  if (v & kStatusTimeout) return fail(MSA_ERR_TIMEOUT, "a kernel wait ran out (status %u)", v);
+  if (v & kStatusBounds) return fail(MSA_ERR_BOUNDS, "an index was out of range (status %u)", v);
+  return MSA_OK;
+}
+
+// ---------------------------------------------------------------- prologue
+
+static msa_status_t check_rope(int rope_dim, float rope_base, float eps) {
+  if (rope_dim != kRopeDim)
+    return fail(MSA_ERR_UNSUPPORTED, "rope_dim must be %d (got %d)", kRopeDim, rope_dim);
+  if (!(rope_base > 1.0f)) return fail(MSA_ERR_INVALID_ARG, "rope_base must be > 1");
+  if (!(eps >= 0.0f)) return fail(MSA_ERR_INVALID_ARG, "eps must be >= 0");
+  return MSA_OK;
+}
+
+msa_status_t msa_qk_norm_rope(void* x, int T, int H, const void* w, const int32_t* cu_seqlens,
+                              int S, int rope_dim, float rope_base, float eps,
+                              msa_stream_t stream) {
+  MSA_REQUIRE_PTR(x);
+  MSA_REQUIRE_PTR(w);
+  MSA_TRY(check_pack(cu_seqlens, S, T, T));
+  MSA_TRY(check_rope(rope_dim, rope_base, eps));
+  if (H < 1) return fail(MSA_ERR_INVALID_ARG, "H must be >= 1");
+  PrologueJob job{static_cast<__nv_bfloat16*>(x), static_cast<const __nv_bfloat16*>(w), H};
+  return launch_prologue(&job, 1, cu_seqlens, S, T, rope_base, eps,
+                         static_cast<cudaStream_t>(stream));
+}
+
+msa_status_t msa_qk_norm_rope4(void* q, int Hq, void* k, int Hkv, void* q_idx, void* k_idx,
+                               int Hi, const void* w_q, const void* w_k, const void* w_qi,
+                               const void* w_ki, const int32_t* cu_seqlens, int S, int T,
+                               int rope_dim, float rope_base, float eps, msa_stream_t stream) {
+  MSA_REQUIRE_PTR(q);
+  MSA_REQUIRE_PTR(k);
+  MSA_REQUIRE_PTR(q_idx);
+  MSA_REQUIRE_PTR(k_idx);
+  MSA_REQUIRE_PTR(w_q);
+  MSA_REQUIRE_PTR(w_k);
+  MSA_REQUIRE_PTR(w_qi);
+  MSA_REQUIRE_PTR(w_ki);
+  MSA_TRY(check_pack(cu_seqlens, S, T, T));
+  MSA_TRY(check_rope(rope_dim, rope_base, eps));
+  if (Hq < 1 || Hkv < 1 || Hi < 1) return fail(MSA_ERR_INVALID_ARG, "head counts must be >= 1");
+  PrologueJob jobs[4] = {
+      {static_cast<__nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(w_q), Hq},
+      {static_cast<__nv_bfloat16*>(k), static_cast<const __nv_bfloat16*>(w_k), Hkv},
+      {static_cast<__nv_bfloat16*>(q_idx), static_cast<const __nv_bfloat16*>(w_qi), Hi},
+      {static_cast<__nv_bfloat16*>(k_idx), static_cast<const __nv_bfloat16*>(w_ki), Hi}};
+  return launch_prologue(jobs, 4, cu_seqlens, S, T, rope_base, eps,
+                         static_cast<cudaStream_t>(stream));
+}
+
+// ---------------------------------------------------------------- index select
+
+size_t msa_index_select_workspace_size(int T, int S, int Hi, int max_seqlen) {
+  (void)Hi;
+  (void)max_seqlen;
+  if (T < 1 || S < 1) return 0;
+  WsCursor ws(nullptr);
+  carve_plan(ws, T, S);
+  return ws.used + 256;
+}
+
+msa_status_t msa_index_select(const void* q_idx, const void* k_idx, const int32_t* cu_seqlens,
+                              int S, int T, int Hi, int max_seqlen, int topk, int32_t* sel,
+                              void* workspace, size_t workspace_bytes, msa_stream_t stream) {
+  MSA_REQUIRE_PTR(q_idx);
+  MSA_REQUIRE_PTR(k_idx);
+  MSA_REQUIRE_PTR(sel);
+  MSA_REQUIRE_PTR(workspace);
+  MSA_TRY(check_pack(cu_seqlens, S, T, max_seqlen));
+  if (topk != kTopK) return fail(MSA_ERR_UNSUPPORTED, "topk must be %d (got %d)", kTopK, topk);
+  if (Hi < 1) return fail(MSA_ERR_INVALID_ARG, "Hi must be >= 1");
+  if (workspace_bytes < msa_index_select_workspace_size(T, S, Hi, max_seqlen))
+    return fail(MSA_ERR_INVALID_ARG, "workspace too small");
+  WsCursor ws(workspace);
+  Plan plan = carve_plan(ws, T, S);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  MSA_TRY(launch_plan(plan, cu_seqlens, S, max_seqlen, st));
+  return launch_index_select(q_idx, k_idx, cu_seqlens, S, T, Hi, plan, sel, st);
+}
+
+// ---------------------------------------------------------------- sparse forward
+
+static msa_status_t check_heads(int Hq, int Hkv) {
+  if (Hq < 1 || Hkv < 1 || Hq % Hkv != 0)
+    return fail(MSA_ERR_INVALID_ARG, "Hq (%d) must be a positive multiple of Hkv (%d)", Hq, Hkv);
+  int G = Hq / Hkv;
+  if (G > 128 || (128 % G) != 0)
+    return fail(MSA_ERR_UNSUPPORTED, "Hq/Hkv = %d must divide 128", G);
+  return MSA_OK;
+}
+
+size_t msa_sparse_attn_fwd_workspace_size(int T, int S, int Hq, int Hkv, int max_seqlen) {
+  (void)Hq;
+  (void)Hkv;
+  (void)max_seqlen;
+  if (T < 1 || S < 1) return 0;
+  WsCursor ws(nullptr);
+  carve_plan(ws, T, S);
+  return ws.used + 256;
+}
+
+msa_status_t msa_sparse_attn_fwd(const void* q, const void* k, const void* v, const int32_t* sel,
+                                 const int32_t* cu_seqlens, int S, int T, int Hq, int Hkv,
+                                 int max_seqlen, float scale, void* o, float* lse,
+                                 void* workspace, size_t workspace_bytes, msa_stream_t stream) {
+  MSA_REQUIRE_PTR(q);
+  MSA_REQUIRE_PTR(k);
+  MSA_REQUIRE_PTR(v);
+  MSA_REQUIRE_PTR(sel);
+  MSA_REQUIRE_PTR(o);
+  MSA_REQUIRE_PTR(lse);
+  MSA_REQUIRE_PTR(workspace);
+  MSA_TRY(check_pack(cu_seqlens, S, T, max_seqlen));
+  MSA_TRY(check_heads(Hq, Hkv));
+  if (!(scale > 0.0f)) return fail(MSA_ERR_INVALID_ARG, "scale must be > 0");
+  if (workspace_bytes < msa_sparse_attn_fwd_workspace_size(T, S, Hq, Hkv, max_seqlen))
+    return fail(MSA_ERR_INVALID_ARG, "workspace too small");
+  WsCursor ws(workspace);
+  Plan plan = carve_plan(ws, T, S);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  MSA_TRY(launch_plan(plan, cu_seqlens, S, max_seqlen, st));
+  return launch_sparse_fwd(q, k, v, sel, cu_seqlens, S, T, Hq, Hkv, max_seqlen, scale, plan, o,
+                           lse, st);
+}
+
+// ---------------------------------------------------------------- sparse backward
+
+size_t msa_sparse_attn_bwd_workspace_size(int T, int S, int Hq, int Hkv, int max_seqlen) {
+  if (T < 1 || S < 1 || Hq < 1 || Hkv < 1 || max_seqlen < 1) return 0;
+  WsCursor ws(nullptr);
+  carve_bwd_workspace(ws, T, S, Hq, Hkv, max_seqlen);
+  return ws.used + 256;
+}
+
+msa_status_t msa_sparse_attn_bwd(const void* q, const void* k, const void* v, const void* o,
+                                 const void* dout, const float* lse, const int32_t* sel,
+                                 const int32_t* cu_seqlens, int S, int T, int Hq, int Hkv,
+                                 int max_seqlen, float scale, void* dq, void* dk, void* dv,
+                                 void* workspace, size_t workspace_bytes, msa_stream_t stream) {
+  MSA_REQUIRE_PTR(q);
+  MSA_REQUIRE_PTR(k);
+  MSA_REQUIRE_PTR(v);
+  MSA_REQUIRE_PTR(o);
+  MSA_REQUIRE_PTR(dout);
+  MSA_REQUIRE_PTR(lse);
+  MSA_REQUIRE_PTR(sel);
+  MSA_REQUIRE_PTR(dq);
+  MSA_REQUIRE_PTR(dk);
+  MSA_REQUIRE_PTR(dv);
+  MSA_REQUIRE_PTR(workspace);
+  MSA_TRY(check_pack(cu_seqlens, S, T, max_seqlen));
+  MSA_TRY(check_heads(Hq, Hkv));
+  if (!(scale > 0.0f)) return fail(MSA_ERR_INVALID_ARG, "scale must be > 0");
+  if (workspace_bytes < msa_sparse_attn_bwd_workspace_size(T, S, Hq, Hkv, max_seqlen))
+    return fail(MSA_ERR_INVALID_ARG, "workspace too small");
+  WsCursor ws(workspace);
+  BwdWorkspace bw = carve_bwd_workspace(ws, T, S, Hq, Hkv, max_seqlen);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  MSA_TRY(launch_plan(bw.plan, cu_seqlens, S, max_seqlen, st));
+  return launch_sparse_bwd(q, k, v, o, dout, lse, sel, cu_seqlens, S, T, Hq, Hkv, max_seqlen,
+                           scale, bw, dq, dk, dv, st);
+}
+
+// ---------------------------------------------------------------- decode
+
+size_t msa_decode_step_workspace_size(int B, int Hq, int Hkv, int max_pages) {
+  if (B < 1 || Hq < 1 || Hkv < 1 || max_pages < 1) return 0;
+  WsCursor ws(nullptr);
+  carve_decode_workspace(ws, B, Hq, Hkv, max_pages);
+  return ws.used + 256;
+}
+
+msa_status_t msa_decode_step(const void* q, const void* q_idx, const void* k_cache,
+                             const void* v_cache, const void* kidx_cache,
+                             const int32_t* block_table, const int32_t* cache_lens, int B, int Hq,
+                             int Hkv, int num_pages, int max_pages, float scale, void* o,
+                             int32_t* sel_out, void* workspace, size_t workspace_bytes,
+                             msa_stream_t stream) {
+  MSA_REQUIRE_PTR(q);
+  MSA_REQUIRE_PTR(q_idx);
+  MSA_REQUIRE_PTR(k_cache);
+  MSA_REQUIRE_PTR(v_cache);
+  MSA_REQUIRE_PTR(kidx_cache);
+  MSA_REQUIRE_PTR(block_table);
+  MSA_REQUIRE_PTR(cache_lens);
+  MSA_REQUIRE_PTR(o);
+  MSA_REQUIRE_PTR(workspace);
+  if (sel_out && !aligned16(sel_out))
+    return fail(MSA_ERR_INVALID_ARG, "sel_out is not 16-byte aligned");
+  if (B < 1 || num_pages < 1 || max_pages < 1)
+    return fail(MSA_ERR_INVALID_ARG, "B, num_pages and max_pages must be >= 1");
+  if (max_pages > kMaxSeqlen / kBlock)
+    return fail(MSA_ERR_UNSUPPORTED, "max_pages %d above the supported %d", max_pages,
+                kMaxSeqlen / kBlock);
+  MSA_TRY(check_heads(Hq, Hkv));
+  if (Hq / Hkv != 16) return fail(MSA_ERR_UNSUPPORTED, "decode needs Hq/Hkv = 16");
+  if (!(scale > 0.0f)) return fail(MSA_ERR_INVALID_ARG, "scale must be > 0");
+  if (workspace_bytes < msa_decode_step_workspace_size(B, Hq, Hkv, max_pages))
+    return fail(MSA_ERR_INVALID_ARG, "workspace too small");
+  WsCursor ws(workspace);
+  DecodeWorkspace dw = carve_decode_workspace(ws, B, Hq, Hkv, max_pages);
+  return launch_decode(q, q_idx, k_cache, v_cache, kidx_cache, block_table, cache_lens, B, Hq, Hkv,
+                       num_pages, max_pages, scale, o, sel_out, dw,
+                       static_cast<cudaStream_t>(stream));
+}
+
+}  // extern "C"

@@ -1,0 +1,67 @@
+// Shared host/device plumbing of libmsa: error reporting, tensor-map encoding,
+// per-call tile plans and launch helpers.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <cstdint>
+#include <cstddef>
+#include <string>
+
+#include "../../include/msa.h"
+
+namespace msa {
+
+constexpr int kD = 128;         // head dim
+constexpr int kBlock = 128;     // key block (tokens)
+constexpr int kTopK = 16;       // selected blocks per query
+constexpr int kRopeDim = 64;    // rotated channels
+
+// ------------------------------------------------------------------ host errors
+
+void set_error(const char* fmt, ...);
+msa_status_t fail(msa_status_t code, const char* fmt, ...);
+msa_status_t check_launch(const char* what);
+
+// Address of the device status word on the current device.
+uint32_t* status_word();
+
+// ------------------------------------------------------------------ tensor maps
+
+// bf16 tensor with up to 3 dims (dims[0] innermost, contiguous), 128B swizzle.
+bool make_tmap_bf16(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
+                    const uint32_t* box);
+
+// ------------------------------------------------------------------ workspace
+
+// Bump allocator over the caller's workspace (256-byte aligned pieces).
+struct WsCursor {
+  uint8_t* base;
+  size_t used = 0;
+  explicit WsCursor(void* b) : base(static_cast<uint8_t*>(b)) {}
+  template <typename T>
+  T* take(size_t count) {
+    size_t off = (used + 255) & ~size_t(255);
+    used = off + count * sizeof(T);
+    return base ? reinterpret_cast<T*>(base + off) : nullptr;
+  }
+};
+
+// ------------------------------------------------------------------ tile plan
+// The 128-token tiles (sequence s, block qb) of a pack, ordered by qb
+// descending (heaviest causal work first), then s ascending.  Built on the
+// device from cu_seqlens by `launch_plan`.
+struct Plan {
+  int2* tiles;      // [max_tiles] (s, qb)
+  int* num_tiles;   // [1]
+  int max_tiles;    // host-side upper bound: T/128 + S
+};
+
+inline int plan_max_tiles(int T, int S) { return T / kBlock + S; }
+Plan carve_plan(WsCursor& ws, int T, int S);
+msa_status_t launch_plan(const Plan& plan, const int32_t* cu_seqlens, int S, int max_seqlen,
+                         cudaStream_t stream);
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace msa

@@ -1,0 +1,69 @@
+// Launchers of the compute kernels (one .cu file each) and the workspace
+// layouts of the calls that need scratch memory.
+#pragma once
+#include "common.cuh"
+#include "sm100_ptx.cuh"
+
+namespace msa {
+
+// Longest supported sequence: the per-tile block bitmaps hold 1024 blocks.
+constexpr int kMaxSeqlen = 1024 * kBlock;
+
+// ---------------------------------------------------------------- prologue
+struct PrologueJob {
+  __nv_bfloat16* x;          // [T, H, 128], in place
+  const __nv_bfloat16* w;    // [128]
+  int H;
+};
+msa_status_t launch_prologue(const PrologueJob* jobs, int njobs, const int32_t* cu, int S,
+                             int T, float rope_base, float eps, cudaStream_t stream);
+
+// ---------------------------------------------------------------- index select
+msa_status_t launch_index_select(const void* q_idx, const void* k_idx, const int32_t* cu, int S,
+                                 int T, int Hi, const Plan& plan, int32_t* sel,
+                                 cudaStream_t stream);
+
+// ---------------------------------------------------------------- sparse forward
+msa_status_t launch_sparse_fwd(const void* q, const void* k, const void* v, const int32_t* sel,
+                               const int32_t* cu, int S, int T, int Hq, int Hkv, int max_seqlen,
+                               float scale, const Plan& plan, void* o, float* lse,
+                               cudaStream_t stream);
+
+// ---------------------------------------------------------------- sparse backward
+// Work items of the KV-major backward: (sequence, key block, segment of
+// candidate query tokens), listed key block ascending.
+constexpr int kBwdSegment = 1024;   // candidate query tokens per work item
+
+struct BwdWorkspace {
+  Plan plan;
+  int4* items;         // [max_items] (s, b, token_begin, token_end) in sequence positions
+  int* num_items;      // [1]
+  int max_items;
+  float* delta;        // [T, Hq]  rowsum(dout * o)
+  float* dq_acc;       // [T, Hq, 128] fp32
+  float* dk_acc;       // [T, Hkv, 128] fp32
+  float* dv_acc;       // [T, Hkv, 128] fp32
+};
+BwdWorkspace carve_bwd_workspace(WsCursor& ws, int T, int S, int Hq, int Hkv, int max_seqlen);
+msa_status_t launch_sparse_bwd(const void* q, const void* k, const void* v, const void* o,
+                               const void* dout, const float* lse, const int32_t* sel,
+                               const int32_t* cu, int S, int T, int Hq, int Hkv, int max_seqlen,
+                               float scale, const BwdWorkspace& ws, void* dq, void* dk, void* dv,
+                               cudaStream_t stream);
+
+// ---------------------------------------------------------------- decode
+struct DecodeWorkspace {
+  float* scores;       // [B, Hkv, max_pages] per-block max logits
+  float* part_o;       // [B, Hkv, kDecodeSplits, 16, 128] partial outputs
+  float* part_ml;      // [B, Hkv, kDecodeSplits, 16, 2] partial (max, sum)
+  int max_pages;
+};
+constexpr int kDecodeSplits = 4;     // selected blocks are attended in 4 groups of 4
+DecodeWorkspace carve_decode_workspace(WsCursor& ws, int B, int Hq, int Hkv, int max_pages);
+msa_status_t launch_decode(const void* q, const void* q_idx, const void* k_cache,
+                           const void* v_cache, const void* kidx_cache,
+                           const int32_t* block_table, const int32_t* cache_lens, int B, int Hq,
+                           int Hkv, int num_pages, int max_pages, float scale, void* o,
+                           int32_t* sel_out, const DecodeWorkspace& ws, cudaStream_t stream);
+
+}  // namespace msa
