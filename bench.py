@@ -1,0 +1,449 @@
+#!/usr/bin/env python
+"""Benchmark: ms per 16k-token THD pack of MiniMax-M3 MSA block-sparse attention
+(prologue + index select + sparse attention forward + backward) on one GB300.
+
+Workload: one KV group on a 16,384-token pack of 4 sequences (seeded lengths,
+multiples of 128, each >= 1024), 16 query / 1 KV / 1 index head, D 128, block
+128, top-16; synthetic N(0,1) bf16 inputs with per-block index-key offsets.
+A step = msa_qk_norm_rope4 -> msa_index_select -> msa_sparse_attn_fwd ->
+msa_sparse_attn_bwd over one pack.  Each step reads its own copy of the
+inputs from a pool larger than L2, so every step starts L2-cold.
+
+Prints one JSON line.  Also measured in the same run: the decode step on the
+paged-cache workload (B = 64, 64 q / 4 kv heads), the end-to-end time through
+the public API with host buffers, the CPU oracle on a bounded sample, and
+per-kernel CUDA-event timings (library tracing) for the roofline.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+"""
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "ms per 16k-token pack (index select + sparse attn fwd/bwd); TFLOP/s, % BF16 peak"
+PAGES_CONTEXT = {
+    "note": "the pages' own GB300 Triton timings (16k pack, 16 q / 1 kv head, D 128, block 128; "
+            "pack composition unstated): attention fwd+bwd 6.7 ms, indexer select 0.62 ms",
+    "fwd_bwd_ms": 6.7, "select_ms": 0.62,
+}
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--pool", type=int, default=8, help="input copies cycled through")
+    ap.add_argument("--cpu-sample-tokens", type=int, default=2048)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d, "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    """nvidia-smi samples (SM clock, throttle reasons) while the timed region runs."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.gpu = gpu_index
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(gpu_index), f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        sm.sort()
+        return {"sm_mhz": sm[len(sm) // 2], "sm_max_mhz": smax, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ reference arm
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    from oracle import cpu_sample
+    import workloads as W
+    n_tok = 128
+    sampler = cpu_sample.Sampler(1, args.seed)
+    vals = []
+    for i in range(args.warmup + args.steps):
+        r = sampler.sample(n_tok, sample_seed=i)
+        if i >= args.warmup:
+            vals.append(r["ms_per_pack"])
+    ms = sum(vals) / len(vals)
+    shape = W.config(1, args.seed)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": ms, "unit": "ms", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": shape.name, "tokens": shape.T, "seqlens": list(shape.seqlens),
+                   "hq": shape.hq, "hkv": shape.hkv, "hi": shape.hi},
+        "cpu_baseline": {"value": ms, "unit": "ms", "cores": 1, "kind": "oracle",
+                         "sample": f"prologue + select + fwd + bwd of {n_tok} random query "
+                                   f"tokens per step (all heads), scaled by T/{n_tok}"},
+        "e2e": {"value": ms, "unit": "ms", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ our arm
+
+def kernel_source_hash(name: str) -> str:
+    files = {"sparse_bwd_kernel": "sparse_bwd.cu", "sparse_fwd_kernel": "sparse_fwd.cu",
+             "index_select_kernel": "index_select.cu", "prologue_kernel": "prologue.cu",
+             "decode_score_kernel": "decode.cu"}
+    f = files.get(name)
+    if f is None:
+        return ""
+    h = hashlib.sha256()
+    for p in (os.path.join(ROOT, "msa_block_sparse_gb300", "csrc", f),
+              os.path.join(ROOT, "msa_block_sparse_gb300", "csrc", "sm100_ptx.cuh")):
+        h.update(open(p, "rb").read())
+    return h.hexdigest()[:16]
+
+
+def traffic_for(name: str):
+    """dram bytes per launch from the committed ncu summary, if it was taken on
+    the current source of the kernel (else None)."""
+    p = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p)).get(name)
+    if not d or d.get("source_hash") != kernel_source_hash(name):
+        return None
+    return d.get("bytes_per_launch")
+
+
+def run_ours(args):
+    import torch
+
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend)
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    import __graft_entry__ as ge
+    ge.build()
+    import msa_block_sparse_gb300 as m
+    from msa_block_sparse_gb300 import workmodel
+    import workloads as W
+
+    peaks, peak_src = load_peaks()
+    shape = W.config(1, args.seed)
+    T, S = shape.T, shape.S
+    hq, hkv, hi, maxL = shape.hq, shape.hkv, shape.hi, shape.max_seqlen
+
+    # ---- input pool (each rank draws its own pack: weak scaling)
+    pool = []
+    for j in range(args.pool):
+        pool.append(W.make_prefill(shape, seed=args.seed + 1000 * rank + j, device=dev,
+                                   with_grad_out=True))
+    cu = pool[0]["cu_seqlens"]
+    bf = torch.bfloat16
+    work = {
+        "q": torch.empty((T, hq, 128), dtype=bf, device=dev),
+        "k": torch.empty((T, hkv, 128), dtype=bf, device=dev),
+        "qi": torch.empty((T, hi, 128), dtype=bf, device=dev),
+        "ki": torch.empty((T, hi, 128), dtype=bf, device=dev),
+        "sel": torch.empty((T, hi, 16), dtype=torch.int32, device=dev),
+        "o": torch.empty((T, hq, 128), dtype=bf, device=dev),
+        "lse": torch.empty((T, hq), dtype=torch.float32, device=dev),
+        "dq": torch.empty((T, hq, 128), dtype=bf, device=dev),
+        "dk": torch.empty((T, hkv, 128), dtype=bf, device=dev),
+        "dv": torch.empty((T, hkv, 128), dtype=bf, device=dev),
+    }
+    ws = {c: torch.empty(max(256, m.workspace_bytes(*a)), dtype=torch.uint8, device=dev)
+          for c, a in (("index_select", ("index_select", T, S, hi, maxL)),
+                       ("fwd", ("sparse_attn_fwd", T, S, hq, hkv, maxL)),
+                       ("bwd", ("sparse_attn_bwd", T, S, hq, hkv, maxL)))}
+
+    def step(x):
+        m.msa_qk_norm_rope4(x["q"], x["k"], x["q_idx"], x["k_idx"], x["w_q"], x["w_k"],
+                            x["w_qi"], x["w_ki"], x["cu_seqlens"],
+                            outs=(work["q"], work["k"], work["qi"], work["ki"]))
+        m.msa_index_select(work["qi"], work["ki"], x["cu_seqlens"], maxL, out=work["sel"],
+                           workspace=ws["index_select"])
+        m.msa_sparse_attn_fwd(work["q"], work["k"], x["v"], work["sel"], x["cu_seqlens"], maxL,
+                              out=work["o"], lse=work["lse"], workspace=ws["fwd"])
+        m.msa_sparse_attn_bwd(work["q"], work["k"], x["v"], work["o"], x["do"], work["lse"],
+                              work["sel"], x["cu_seqlens"], maxL, dq=work["dq"], dk=work["dk"],
+                              dv=work["dv"], workspace=ws["bwd"])
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    stream = torch.cuda.current_stream(dev)
+    for i in range(args.warmup):
+        step(pool[i % args.pool])
+    torch.cuda.synchronize(dev)
+    m.msa_check_status(dev)
+
+    sampler = ClockSampler(local)
+    time.sleep(0.3)
+    barrier()
+    torch.cuda.synchronize(dev)
+    m.msa_trace_begin()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for i in range(args.steps):
+        step(pool[i % args.pool])
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    trace = m.msa_trace_end()
+    barrier()
+    clocks = sampler.stop()
+    m.msa_check_status(dev)
+    ms_step = ev0.elapsed_time(ev1) / args.steps
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([ms_step], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_step = float(t.item())
+
+    wk = workmodel.prefill_work(shape.seqlens, hq, hkv, hi)
+    total_flops = wk["fwd_flops"] + wk["bwd_flops"] + wk["select_flops"]
+    kernels = {n: {"launches": v["launches"] // args.steps if v["launches"] >= args.steps else v["launches"],
+                   "ms_per_launch": v["ms"] / max(1, v["launches"]),
+                   "share": None}
+               for n, v in trace.items()}
+    tot_ms = sum(v["ms"] for v in trace.values())
+    for n, v in trace.items():
+        kernels[n]["share"] = v["ms"] / tot_ms if tot_ms > 0 else None
+    gpu_launches = int(sum(v["launches"] for v in trace.values()))
+
+    flops_of = {"sparse_bwd_kernel": wk["bwd_flops"], "sparse_fwd_kernel": wk["fwd_flops"],
+                "index_select_kernel": wk["select_flops"]}
+    dom = max(trace.items(), key=lambda kv: kv[1]["ms"])[0]
+    roofline = None
+    if dom in flops_of:
+        ms_launch = trace[dom]["ms"] / trace[dom]["launches"]
+        ach = flops_of[dom] / (ms_launch * 1e-3) / 1e12
+        peak = peaks.get("bf16_tflops_sustained", 1700.0)
+        roofline = {"kernel": dom, "bound": "tensor", "achieved": ach, "peak": peak,
+                    "unit": "TFLOP/s", "frac": ach / peak, "traffic": traffic_for(dom),
+                    "peak_source": f"{peak_src} bf16 dense sustained (kernel timed inside a long step)",
+                    "frac_of_burst": ach / peaks.get("bf16_tflops", 1900.0),
+                    "flops_per_launch": flops_of[dom], "ms_per_launch": ms_launch}
+    per_kernel_roofline = {}
+    for n, f in flops_of.items():
+        if n in trace:
+            msl = trace[n]["ms"] / trace[n]["launches"]
+            per_kernel_roofline[n] = {"tflops": f / (msl * 1e-3) / 1e12, "ms": msl,
+                                      "frac": f / (msl * 1e-3) / 1e12 / peaks.get("bf16_tflops_sustained", 1700.0)}
+    if "prologue_kernel" in trace:
+        msl = trace["prologue_kernel"]["ms"] / trace["prologue_kernel"]["launches"]
+        per_kernel_roofline["prologue_kernel"] = {
+            "gbs": wk["prologue_bytes"] / (msl * 1e-3) / 1e9, "ms": msl,
+            "frac": wk["prologue_bytes"] / (msl * 1e-3) / 1e9 / peaks.get("hbm_gbs", 6800.0)}
+
+    out = {
+        "metric": METRIC,
+        "value": ms_step / world,
+        "unit": "ms",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms_step,
+        "higher_is_better": False,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": shape.name, "tokens": T, "seqlens": list(shape.seqlens),
+                   "hq": hq, "hkv": hkv, "hi": hi, "d": 128, "block": 128, "topk": 16,
+                   "step": "qk_norm_rope4 + index_select + sparse_attn_fwd + sparse_attn_bwd",
+                   "l2": f"inputs larger than L2: each step reads its own input copy from a "
+                         f"pool of {args.pool} packs ({args.pool * 144} MB)",
+                   "parallelism": f"replicas x{world} (one pack per GPU, no collective)"},
+        "tflops": total_flops / (ms_step * 1e-3) / 1e12,
+        "tokens_per_s": T * world / (ms_step * 1e-3),
+        "work": wk,
+        "roofline": roofline,
+        "kernels": kernels,
+        "kernel_roofline": per_kernel_roofline,
+        "gpu_launches": gpu_launches,
+        "clocks": clocks,
+        "pages_context": PAGES_CONTEXT,
+    }
+
+    # ---- end to end through the public API with host buffers
+    if not args.no_e2e:
+        host_in = {k: v.cpu().pin_memory() for k, v in pool[0].items()}
+        dev_in = {k: torch.empty_like(v) for k, v in pool[0].items()}
+        host_out = {n: torch.empty(work[n].shape, dtype=work[n].dtype).pin_memory()
+                    for n in ("o", "dq", "dk", "dv")}
+        h2d = sum(v.numel() * v.element_size() for v in host_in.values())
+        d2h = sum(v.numel() * v.element_size() for v in host_out.values())
+
+        def e2e_step():
+            for k in host_in:
+                dev_in[k].copy_(host_in[k], non_blocking=True)
+            step(dev_in)
+            for n in host_out:
+                host_out[n].copy_(work[n], non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize(dev)
+        n_e2e = max(5, args.steps // 4)
+        barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(n_e2e):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        barrier()
+        e2e_ms = e0.elapsed_time(e1) / n_e2e
+        out["e2e"] = {"value": e2e_ms / world, "unit": "ms", "h2d_bytes_per_step": h2d,
+                      "d2h_bytes_per_step": d2h, "steps": n_e2e}
+
+    # ---- decode step on the paged-cache workload
+    if not args.no_decode:
+        dshape = W.config(3, args.seed)
+        dx = W.make_decode(dshape, seed=args.seed + 1000 * rank, device=dev)
+        B, maxp = dshape.B, dx["block_table"].shape[1]
+        dws = torch.empty(m.workspace_bytes("decode_step", B, dshape.hq, dshape.hkv, maxp),
+                          dtype=torch.uint8, device=dev)
+        od = torch.empty_like(dx["q"])
+        sd = torch.empty((B, dshape.hkv, 16), dtype=torch.int32, device=dev)
+
+        def dstep():
+            m.msa_decode_step(dx["q"], dx["q_idx"], dx["k_cache"], dx["v_cache"], dx["kidx_cache"],
+                              dx["block_table"], dx["cache_lens"], out=od, sel_out=sd,
+                              workspace=dws)
+
+        for _ in range(3):
+            dstep()
+        torch.cuda.synchronize(dev)
+        nd = max(10, args.steps)
+        m.msa_trace_begin()
+        d0, d1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        d0.record(stream)
+        for _ in range(nd):
+            dstep()
+        d1.record(stream)
+        torch.cuda.synchronize(dev)
+        dtrace = m.msa_trace_end()
+        m.msa_check_status(dev)
+        dms = d0.elapsed_time(d1) / nd
+        dbytes = workmodel.decode_bytes(dshape.cache_lens, dshape.hq, dshape.hkv)
+        gbs = dbytes / (dms * 1e-3) / 1e9
+        out["decode"] = {
+            "workload": dshape.name, "batch": B, "ms_per_step": dms,
+            "gbs": gbs, "bytes_per_step": dbytes,
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks.get("hbm_gbs", 6800.0),
+                         "unit": "GB/s", "frac": gbs / peaks.get("hbm_gbs", 6800.0),
+                         "traffic": traffic_for("decode_score_kernel"),
+                         "peak_source": f"{peak_src} HBM copy"},
+            "kernels": {n: {"launches": v["launches"] // nd, "ms_per_launch": v["ms"] / v["launches"]}
+                        for n, v in dtrace.items()},
+            "l2": "the index-key cache (%.2f GB) is larger than L2" %
+                  (dx["kidx_cache"].numel() * 2 / 1e9),
+        }
+        del dx
+
+    # ---- CPU oracle on a bounded sample (rank 0, N = 1 only)
+    if not args.no_cpu_baseline and rank == 0 and world == 1:
+        env = dict(os.environ)
+        from oracle.cpu_sample import THREAD_VARS
+        for v in THREAD_VARS:
+            env[v] = "1"
+        r = subprocess.run([sys.executable, "-m", "oracle.cpu_sample", "--config", "1",
+                            "--tokens", str(args.cpu_sample_tokens), "--seed", str(args.seed)],
+                           cwd=ROOT, env=env, capture_output=True, text=True, timeout=900)
+        if r.returncode == 0:
+            cs = json.loads(r.stdout.strip().splitlines()[-1])
+            out["cpu_baseline"] = {
+                "value": cs["ms_per_pack"], "unit": "ms", "cores": 1, "kind": "oracle",
+                "sample": f"prologue + select + fwd + bwd of {cs['sample_tokens']} random "
+                          f"query tokens (all heads) of the same pack, scaled by "
+                          f"T/{cs['sample_tokens']}",
+                "seconds": {k: cs[k] for k in ("prologue_s", "select_s", "fwd_s", "bwd_s")}}
+        else:
+            out["cpu_baseline"] = {"value": None, "error": r.stderr[-500:]}
+
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        # the oracle runs on one host core; set before numpy loads
+        for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS",
+                    "NUMEXPR_NUM_THREADS", "BLIS_NUM_THREADS"):
+            os.environ[var] = "1"
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -96,7 +96,8 @@ MSA_API msa_status_t msa_check_status(msa_stream_t stream);
 
 /* ------------------------------------------------------------------------
  * Prologue ("MiniMax-M3.1-Flash", 1 "Model Introduction"; "MiniMax-M3",
- * "Architecture Notes").  In place on x, bf16 [T, H, 128]:
+ * "Architecture Notes").  x bf16 [T, H, 128] -> y bf16 [T, H, 128] (y may be
+ * x itself, for an in-place update):
  *   y = x / sqrt(mean(x^2) + eps) * (1 + w)        per (token, head), w bf16 [128]
  *   then channels i and i + rope_dim/2 (i < rope_dim/2) are rotated by the
  *   angle pos * rope_base^(-2 i / rope_dim), pos = the token's in-sequence
@@ -104,15 +105,17 @@ MSA_API msa_status_t msa_check_status(msa_stream_t stream);
  * The four-tensor form runs q [T,Hq,128], k [T,Hkv,128], q_idx and k_idx
  * [T,Hi,128] with their own weights in one launch; same result as four calls.
  */
-MSA_API msa_status_t msa_qk_norm_rope(void* x, int T, int H, const void* w,
-                              const int32_t* cu_seqlens, int S, int rope_dim,
-                              float rope_base, float eps, msa_stream_t stream);
+MSA_API msa_status_t msa_qk_norm_rope(const void* x, void* y, int T, int H, const void* w,
+                                      const int32_t* cu_seqlens, int S, int rope_dim,
+                                      float rope_base, float eps, msa_stream_t stream);
 
-MSA_API msa_status_t msa_qk_norm_rope4(void* q, int Hq, void* k, int Hkv, void* q_idx,
-                               void* k_idx, int Hi, const void* w_q, const void* w_k,
-                               const void* w_qi, const void* w_ki,
-                               const int32_t* cu_seqlens, int S, int T, int rope_dim,
-                               float rope_base, float eps, msa_stream_t stream);
+MSA_API msa_status_t msa_qk_norm_rope4(const void* q, void* q_out, int Hq, const void* k,
+                                       void* k_out, int Hkv, const void* q_idx,
+                                       void* q_idx_out, const void* k_idx, void* k_idx_out,
+                                       int Hi, const void* w_q, const void* w_k,
+                                       const void* w_qi, const void* w_ki,
+                                       const int32_t* cu_seqlens, int S, int T, int rope_dim,
+                                       float rope_base, float eps, msa_stream_t stream);
 
 /* ------------------------------------------------------------------------
  * Index select ("MiniMax-M3.1-Flash", 1 "Model Introduction"; "#4581",
@@ -189,6 +192,19 @@ MSA_API msa_status_t msa_decode_step(const void* q, const void* q_idx, const voi
                              int Hq, int Hkv, int num_pages, int max_pages, float scale,
                              void* o, int32_t* sel_out, void* workspace,
                              size_t workspace_bytes, msa_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Launch tracing (no counterpart on the pages: measurement plumbing).
+ * msa_trace_begin() clears the record and turns tracing on: from then on the
+ * library brackets each of its kernel launches with a pair of CUDA events on
+ * the launch stream (host-side objects, created on first use and kept).
+ * msa_trace_end() waits for the recorded events, turns tracing off and writes
+ * a JSON object {"<kernel>": {"launches": n, "ms": total}, ...} (NUL
+ * terminated, truncated to `cap` bytes) into `json`.  Not for use inside
+ * stream capture.  Tracing is process-wide and off by default.
+ */
+MSA_API msa_status_t msa_trace_begin(void);
+MSA_API msa_status_t msa_trace_end(char* json, size_t cap);
 
 #ifdef __cplusplus
 }

@@ -26,10 +26,13 @@ _SIGNATURES = {
     "msa_abi_version": (_c_int, []),
     "msa_last_error": (ctypes.c_char_p, []),
     "msa_check_status": (_c_int, [_vp]),
-    "msa_qk_norm_rope": (_c_int, [_vp, _c_int, _c_int, _vp, _vp, _c_int, _c_int, _c_float,
+    "msa_trace_begin": (_c_int, []),
+    "msa_trace_end": (_c_int, [ctypes.c_char_p, _c_size]),
+    "msa_qk_norm_rope": (_c_int, [_vp, _vp, _c_int, _c_int, _vp, _vp, _c_int, _c_int, _c_float,
                                   _c_float, _vp]),
-    "msa_qk_norm_rope4": (_c_int, [_vp, _c_int, _vp, _c_int, _vp, _vp, _c_int, _vp, _vp, _vp,
-                                   _vp, _vp, _c_int, _c_int, _c_int, _c_float, _c_float, _vp]),
+    "msa_qk_norm_rope4": (_c_int, [_vp, _vp, _c_int, _vp, _vp, _c_int, _vp, _vp, _vp, _vp,
+                                   _c_int, _vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int,
+                                   _c_float, _c_float, _vp]),
     "msa_index_select_workspace_size": (_c_size, [_c_int, _c_int, _c_int, _c_int]),
     "msa_index_select": (_c_int, [_vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_int, _vp,
                                   _vp, _c_size, _vp]),
@@ -114,23 +117,40 @@ def msa_check_status(device=None) -> None:
 
 # ------------------------------------------------------------------ prologue
 
-def msa_qk_norm_rope(x, w, cu_seqlens, rope_dim: int = 64, rope_base: float = 1.0e7,
-                     eps: float = 1.0e-6):
-    """In place on x (bf16 [T, H, 128]): gemma RMSNorm with weight w (bf16 [128])
-    then partial RoPE at each token's position in its sequence."""
+def msa_trace_begin() -> None:
+    """Start recording CUDA-event timings around every library kernel launch."""
+    _check(lib().msa_trace_begin())
+
+
+def msa_trace_end() -> dict:
+    """Stop recording; {kernel: {"launches": n, "ms": total}} since msa_trace_begin."""
+    buf = ctypes.create_string_buffer(1 << 16)
+    _check(lib().msa_trace_end(buf, len(buf)))
+    import json
+    return json.loads(buf.value.decode())
+
+
+def msa_qk_norm_rope(x, w, cu_seqlens, out: Optional[torch.Tensor] = None, rope_dim: int = 64,
+                     rope_base: float = 1.0e7, eps: float = 1.0e-6):
+    """x bf16 [T, H, 128] -> out (default: a new tensor; pass out=x for in place):
+    gemma RMSNorm with weight w (bf16 [128]) then partial RoPE at each token's
+    position in its sequence."""
     T, H = x.shape[0], x.shape[1]
     _req(x, "x", torch.bfloat16, (T, H, D))
     _req(w, "w", torch.bfloat16, (D,))
     _req(cu_seqlens, "cu_seqlens", torch.int32)
+    out = torch.empty_like(x) if out is None else out
+    _req(out, "out", torch.bfloat16, (T, H, D))
     S = cu_seqlens.numel() - 1
-    _check(lib().msa_qk_norm_rope(_ptr(x), T, H, _ptr(w), _ptr(cu_seqlens), S, rope_dim,
-                                  rope_base, eps, _stream(x)))
-    return x
+    _check(lib().msa_qk_norm_rope(_ptr(x), _ptr(out), T, H, _ptr(w), _ptr(cu_seqlens), S,
+                                  rope_dim, rope_base, eps, _stream(x)))
+    return out
 
 
-def msa_qk_norm_rope4(q, k, q_idx, k_idx, w_q, w_k, w_qi, w_ki, cu_seqlens,
+def msa_qk_norm_rope4(q, k, q_idx, k_idx, w_q, w_k, w_qi, w_ki, cu_seqlens, outs=None,
                       rope_dim: int = 64, rope_base: float = 1.0e7, eps: float = 1.0e-6):
-    """The prologue of q, k, index-q and index-k in one launch (in place)."""
+    """The prologue of q, k, index-q and index-k in one launch.  `outs` is a
+    4-tuple of output tensors (default: new tensors; pass the inputs for in place)."""
     T = q.shape[0]
     Hq, Hkv, Hi = q.shape[1], k.shape[1], q_idx.shape[1]
     _req(q, "q", torch.bfloat16, (T, Hq, D))
@@ -140,12 +160,17 @@ def msa_qk_norm_rope4(q, k, q_idx, k_idx, w_q, w_k, w_qi, w_ki, cu_seqlens,
     for n, w in (("w_q", w_q), ("w_k", w_k), ("w_qi", w_qi), ("w_ki", w_ki)):
         _req(w, n, torch.bfloat16, (D,))
     _req(cu_seqlens, "cu_seqlens", torch.int32)
+    if outs is None:
+        outs = tuple(torch.empty_like(t) for t in (q, k, q_idx, k_idx))
+    for o_, t, n in zip(outs, (q, k, q_idx, k_idx), ("q_out", "k_out", "q_idx_out", "k_idx_out")):
+        _req(o_, n, torch.bfloat16, tuple(t.shape))
     S = cu_seqlens.numel() - 1
-    _check(lib().msa_qk_norm_rope4(_ptr(q), Hq, _ptr(k), Hkv, _ptr(q_idx), _ptr(k_idx), Hi,
+    _check(lib().msa_qk_norm_rope4(_ptr(q), _ptr(outs[0]), Hq, _ptr(k), _ptr(outs[1]), Hkv,
+                                   _ptr(q_idx), _ptr(outs[2]), _ptr(k_idx), _ptr(outs[3]), Hi,
                                    _ptr(w_q), _ptr(w_k), _ptr(w_qi), _ptr(w_ki),
                                    _ptr(cu_seqlens), S, T, rope_dim, rope_base, eps,
                                    _stream(q)))
-    return q, k, q_idx, k_idx
+    return tuple(outs)
 
 
 # ------------------------------------------------------------------ index select

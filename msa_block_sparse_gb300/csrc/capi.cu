@@ -3,7 +3,10 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <map>
 #include <mutex>
+#include <string>
+#include <vector>
 #include <cudaTypedefs.h>
 
 #include "common.cuh"
@@ -50,6 +53,39 @@ uint32_t* status_word() {
     ptrs[dev] = static_cast<uint32_t*>(p);
   }
   return ptrs[dev];
+}
+
+// ------------------------------------------------------------------ tracing
+
+namespace {
+struct TraceRec {
+  const char* name;
+  cudaEvent_t start, stop;
+};
+std::mutex g_trace_mu;
+bool g_trace_on = false;
+std::vector<TraceRec> g_trace_pool;   // events are created once and reused
+size_t g_trace_used = 0;
+}  // namespace
+
+TraceScope::TraceScope(const char* kernel, cudaStream_t stream) : stream_(stream) {
+  std::lock_guard<std::mutex> lk(g_trace_mu);
+  if (!g_trace_on) return;
+  if (g_trace_used == g_trace_pool.size()) {
+    TraceRec r{nullptr, nullptr, nullptr};
+    if (cudaEventCreate(&r.start) != cudaSuccess || cudaEventCreate(&r.stop) != cudaSuccess)
+      return;
+    g_trace_pool.push_back(r);
+  }
+  slot_ = static_cast<int>(g_trace_used++);
+  g_trace_pool[slot_].name = kernel;
+  cudaEventRecord(g_trace_pool[slot_].start, stream_);
+}
+
+TraceScope::~TraceScope() {
+  if (slot_ < 0) return;
+  std::lock_guard<std::mutex> lk(g_trace_mu);
+  cudaEventRecord(g_trace_pool[slot_].stop, stream_);
 }
 
 // ------------------------------------------------------------------ tensor maps
@@ -152,8 +188,11 @@ msa_status_t launch_plan(const Plan& plan, const int32_t* cu_seqlens, int S, int
                          cudaStream_t stream) {
   int max_nb = (max_seqlen + kBlock - 1) / kBlock;
   size_t smem = 2 * (max_nb + 1) * sizeof(int);
-  plan_kernel<<<1, 1024, smem, stream>>>(cu_seqlens, S, max_nb, plan.tiles, plan.num_tiles,
+  {
+    TraceScope trace_("plan_kernel", stream);
+    plan_kernel<<<1, 1024, smem, stream>>>(cu_seqlens, S, max_nb, plan.tiles, plan.num_tiles,
                                          plan.max_tiles, status_word());
+  }
   return check_launch("plan_kernel");
 }
 
@@ -191,6 +230,51 @@ extern "C" {
 
 int msa_abi_version(void) { return MSA_ABI_VERSION; }
 
+msa_status_t msa_trace_begin(void) {
+  std::lock_guard<std::mutex> lk(g_trace_mu);
+  g_trace_used = 0;
+  g_trace_on = true;
+  return MSA_OK;
+}
+
+msa_status_t msa_trace_end(char* json, size_t cap) {
+  std::lock_guard<std::mutex> lk(g_trace_mu);
+  g_trace_on = false;
+  std::map<std::string, std::pair<long, double>> agg;
+  std::vector<std::string> order;
+  for (size_t i = 0; i < g_trace_used; ++i) {
+    const TraceRec& r = g_trace_pool[i];
+    float ms = 0.f;
+    if (cudaEventSynchronize(r.stop) != cudaSuccess ||
+        cudaEventElapsedTime(&ms, r.start, r.stop) != cudaSuccess)
+      return fail(MSA_ERR_CUDA, "trace: event timing failed");
+    auto it = agg.find(r.name);
+    if (it == agg.end()) {
+      order.push_back(r.name);
+      agg[r.name] = {1, ms};
+    } else {
+      it->second.first += 1;
+      it->second.second += ms;
+    }
+  }
+  std::string out = "{";
+  for (size_t i = 0; i < order.size(); ++i) {
+    char buf[256];
+    const auto& v = agg[order[i]];
+    snprintf(buf, sizeof(buf), "%s\"%s\": {\"launches\": %ld, \"ms\": %.6f}", i ? ", " : "",
+             order[i].c_str(), v.first, v.second);
+    out += buf;
+  }
+  out += "}";
+  g_trace_used = 0;
+  if (json && cap > 0) {
+    const size_t n = out.size() < cap - 1 ? out.size() : cap - 1;
+    memcpy(json, out.data(), n);
+    json[n] = '\0';
+  }
+  return MSA_OK;
+}
+
 const char* msa_last_error(void) { return g_last_error; }
 
 msa_status_t msa_check_status(msa_stream_t stream) {
@@ -217,27 +301,35 @@ static msa_status_t check_rope(int rope_dim, float rope_base, float eps) {
   return MSA_OK;
 }
 
-msa_status_t msa_qk_norm_rope(void* x, int T, int H, const void* w, const int32_t* cu_seqlens,
-                              int S, int rope_dim, float rope_base, float eps,
-                              msa_stream_t stream) {
+msa_status_t msa_qk_norm_rope(const void* x, void* y, int T, int H, const void* w,
+                              const int32_t* cu_seqlens, int S, int rope_dim, float rope_base,
+                              float eps, msa_stream_t stream) {
   MSA_REQUIRE_PTR(x);
+  MSA_REQUIRE_PTR(y);
   MSA_REQUIRE_PTR(w);
   MSA_TRY(check_pack(cu_seqlens, S, T, T));
   MSA_TRY(check_rope(rope_dim, rope_base, eps));
   if (H < 1) return fail(MSA_ERR_INVALID_ARG, "H must be >= 1");
-  PrologueJob job{static_cast<__nv_bfloat16*>(x), static_cast<const __nv_bfloat16*>(w), H};
+  PrologueJob job{static_cast<const __nv_bfloat16*>(x), static_cast<__nv_bfloat16*>(y),
+                  static_cast<const __nv_bfloat16*>(w), H};
   return launch_prologue(&job, 1, cu_seqlens, S, T, rope_base, eps,
                          static_cast<cudaStream_t>(stream));
 }
 
-msa_status_t msa_qk_norm_rope4(void* q, int Hq, void* k, int Hkv, void* q_idx, void* k_idx,
-                               int Hi, const void* w_q, const void* w_k, const void* w_qi,
-                               const void* w_ki, const int32_t* cu_seqlens, int S, int T,
-                               int rope_dim, float rope_base, float eps, msa_stream_t stream) {
+msa_status_t msa_qk_norm_rope4(const void* q, void* q_out, int Hq, const void* k, void* k_out,
+                               int Hkv, const void* q_idx, void* q_idx_out, const void* k_idx,
+                               void* k_idx_out, int Hi, const void* w_q, const void* w_k,
+                               const void* w_qi, const void* w_ki, const int32_t* cu_seqlens,
+                               int S, int T, int rope_dim, float rope_base, float eps,
+                               msa_stream_t stream) {
   MSA_REQUIRE_PTR(q);
   MSA_REQUIRE_PTR(k);
   MSA_REQUIRE_PTR(q_idx);
   MSA_REQUIRE_PTR(k_idx);
+  MSA_REQUIRE_PTR(q_out);
+  MSA_REQUIRE_PTR(k_out);
+  MSA_REQUIRE_PTR(q_idx_out);
+  MSA_REQUIRE_PTR(k_idx_out);
   MSA_REQUIRE_PTR(w_q);
   MSA_REQUIRE_PTR(w_k);
   MSA_REQUIRE_PTR(w_qi);
@@ -245,11 +337,14 @@ msa_status_t msa_qk_norm_rope4(void* q, int Hq, void* k, int Hkv, void* q_idx, v
   MSA_TRY(check_pack(cu_seqlens, S, T, T));
   MSA_TRY(check_rope(rope_dim, rope_base, eps));
   if (Hq < 1 || Hkv < 1 || Hi < 1) return fail(MSA_ERR_INVALID_ARG, "head counts must be >= 1");
+  using bf = __nv_bfloat16;
   PrologueJob jobs[4] = {
-      {static_cast<__nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(w_q), Hq},
-      {static_cast<__nv_bfloat16*>(k), static_cast<const __nv_bfloat16*>(w_k), Hkv},
-      {static_cast<__nv_bfloat16*>(q_idx), static_cast<const __nv_bfloat16*>(w_qi), Hi},
-      {static_cast<__nv_bfloat16*>(k_idx), static_cast<const __nv_bfloat16*>(w_ki), Hi}};
+      {static_cast<const bf*>(q), static_cast<bf*>(q_out), static_cast<const bf*>(w_q), Hq},
+      {static_cast<const bf*>(k), static_cast<bf*>(k_out), static_cast<const bf*>(w_k), Hkv},
+      {static_cast<const bf*>(q_idx), static_cast<bf*>(q_idx_out), static_cast<const bf*>(w_qi),
+       Hi},
+      {static_cast<const bf*>(k_idx), static_cast<bf*>(k_idx_out), static_cast<const bf*>(w_ki),
+       Hi}};
   return launch_prologue(jobs, 4, cu_seqlens, S, T, rope_base, eps,
                          static_cast<cudaStream_t>(stream));
 }

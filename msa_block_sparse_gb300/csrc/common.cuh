@@ -26,6 +26,20 @@ msa_status_t check_launch(const char* what);
 // Address of the device status word on the current device.
 uint32_t* status_word();
 
+// Brackets one kernel launch with CUDA events on `stream` while tracing is on
+// (msa_trace_begin / msa_trace_end); does nothing otherwise.
+class TraceScope {
+ public:
+  TraceScope(const char* kernel, cudaStream_t stream);
+  ~TraceScope();
+  TraceScope(const TraceScope&) = delete;
+  TraceScope& operator=(const TraceScope&) = delete;
+
+ private:
+  int slot_ = -1;
+  cudaStream_t stream_;
+};
+
 // ------------------------------------------------------------------ tensor maps
 
 // bf16 tensor with up to 3 dims (dims[0] innermost, contiguous), 128B swizzle.

@@ -454,9 +454,12 @@ msa_status_t launch_decode(const void* q, const void* q_idx, const void* k_cache
                            int32_t* sel_out, const DecodeWorkspace& ws, cudaStream_t stream) {
   uint32_t* st = status_word();
   dim3 g1((max_pages + kPagesPerCta - 1) / kPagesPerCta, B);
-  decode_score_kernel<<<g1, 256, 0, stream>>>(
+  {
+    TraceScope trace_("decode_score_kernel", stream);
+    decode_score_kernel<<<g1, 256, 0, stream>>>(
       static_cast<const __nv_bfloat16*>(q_idx), static_cast<const __nv_bfloat16*>(kidx_cache),
       block_table, cache_lens, Hkv, num_pages, max_pages, ws.scores, st);
+  }
   msa_status_t e = check_launch("decode_score_kernel");
   if (e != MSA_OK) return e;
   const size_t smem = sizeof(AttendSmem) + 128;
@@ -467,14 +470,20 @@ msa_status_t launch_decode(const void* q, const void* q_idx, const void* k_cache
     attr_set = true;
   }
   dim3 g2(B, Hkv, kDecodeSplits);
-  decode_attend_kernel<<<g2, 128, smem, stream>>>(
+  {
+    TraceScope trace_("decode_attend_kernel", stream);
+    decode_attend_kernel<<<g2, 128, smem, stream>>>(
       static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k_cache),
       static_cast<const __nv_bfloat16*>(v_cache), block_table, cache_lens, Hq, Hkv, num_pages,
       max_pages, scale, ws.scores, sel_out, ws.part_o, ws.part_ml, st);
+  }
   e = check_launch("decode_attend_kernel");
   if (e != MSA_OK) return e;
-  decode_merge_kernel<<<B * Hkv, 128, 0, stream>>>(ws.part_o, ws.part_ml, Hq, Hkv,
+  {
+    TraceScope trace_("decode_merge_kernel", stream);
+    decode_merge_kernel<<<B * Hkv, 128, 0, stream>>>(ws.part_o, ws.part_ml, Hq, Hkv,
                                                    static_cast<__nv_bfloat16*>(o));
+  }
   return check_launch("decode_merge_kernel");
 }
 

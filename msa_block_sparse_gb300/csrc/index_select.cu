@@ -226,9 +226,12 @@ msa_status_t launch_index_select(const void* q_idx, const void* k_idx, const int
     attr_set = true;
   }
   dim3 grid(plan.max_tiles, Hi);
-  index_select_kernel<<<grid, kSelThreads, smem, stream>>>(tq, tk, cu, plan.tiles,
+  {
+    TraceScope trace_("index_select_kernel", stream);
+    index_select_kernel<<<grid, kSelThreads, smem, stream>>>(tq, tk, cu, plan.tiles,
                                                            plan.num_tiles, Hi, sel,
                                                            status_word());
+  }
   return check_launch("index_select_kernel");
 }
 

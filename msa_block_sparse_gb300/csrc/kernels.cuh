@@ -11,7 +11,8 @@ constexpr int kMaxSeqlen = 1024 * kBlock;
 
 // ---------------------------------------------------------------- prologue
 struct PrologueJob {
-  __nv_bfloat16* x;          // [T, H, 128], in place
+  const __nv_bfloat16* x;    // [T, H, 128] input
+  __nv_bfloat16* y;          // [T, H, 128] output (may equal x)
   const __nv_bfloat16* w;    // [128]
   int H;
 };

@@ -2,7 +2,7 @@
 // followed by partial RoPE on the first 64 of 128 channels (channel i pairs
 // with i + 32; angle = position * base^(-2i/64)).  ("MiniMax-M3.1-Flash",
 // 1 "Model Introduction"; "MiniMax-M3" Megatron-Bridge page, "Architecture
-// Notes".)  In place on bf16 [T, H, 128]; HBM-bound.
+// Notes".)  bf16 [T, H, 128] -> bf16 [T, H, 128] (in place allowed); HBM-bound.
 //
 // Layout of the work: a CTA takes 8 consecutive tokens of one tensor.  Its 256
 // threads first compute the 8 x 32 (cos, sin) pairs of those tokens once, then
@@ -78,9 +78,10 @@ __global__ void __launch_bounds__(256) prologue_kernel(const PrologueArgs args,
     const bool valid = r < rows;
     const int tl = valid ? r / H : 0;
     const size_t row = static_cast<size_t>(t0) * H + (valid ? r : 0);
-    uint4* ptr = reinterpret_cast<uint4*>(job.x + row * kD) + chunk;
+    const uint4* src = reinterpret_cast<const uint4*>(job.x + row * kD) + chunk;
+    uint4* dst = reinterpret_cast<uint4*>(job.y + row * kD) + chunk;
     float x[8];
-    uint4 xv = valid ? *ptr : make_uint4(0, 0, 0, 0);
+    uint4 xv = valid ? *src : make_uint4(0, 0, 0, 0);
     {
       const __nv_bfloat162* xp = reinterpret_cast<const __nv_bfloat162*>(&xv);
 #pragma unroll
@@ -116,7 +117,7 @@ __global__ void __launch_bounds__(256) prologue_kernel(const PrologueArgs args,
       out.y = pack_bf16x2(x[2], x[3]);
       out.z = pack_bf16x2(x[4], x[5]);
       out.w = pack_bf16x2(x[6], x[7]);
-      *ptr = out;
+      *dst = out;
     }
   }
 }
@@ -133,7 +134,10 @@ msa_status_t launch_prologue(const PrologueJob* jobs, int njobs, const int32_t* 
     turns.f[i] = static_cast<unsigned long long>(f / two_pi * 18446744073709551616.0);
   }
   dim3 grid(args.ctas_per_job * njobs);
-  prologue_kernel<<<grid, 256, 0, stream>>>(args, turns, cu, S, T, eps, status_word());
+  {
+    TraceScope trace_("prologue_kernel", stream);
+    prologue_kernel<<<grid, 256, 0, stream>>>(args, turns, cu, S, T, eps, status_word());
+  }
   return check_launch("prologue_kernel");
 }
 

@@ -499,11 +499,17 @@ msa_status_t launch_sparse_bwd(const void* q, const void* k, const void* v, cons
     return fail(MSA_ERR_CUDA, "workspace clear failed");
 
   const size_t rows = static_cast<size_t>(T) * Hq;
-  bwd_delta_kernel<<<static_cast<unsigned>((rows * 32 + 255) / 256), 256, 0, stream>>>(
+  {
+    TraceScope trace_("bwd_delta_kernel", stream);
+    bwd_delta_kernel<<<static_cast<unsigned>((rows * 32 + 255) / 256), 256, 0, stream>>>(
       static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dout), ws.delta,
       rows);
-  bwd_items_kernel<<<1, 1024, 0, stream>>>(cu, ws.plan.tiles, ws.plan.num_tiles, ws.items,
+  }
+  {
+    TraceScope trace_("bwd_items_kernel", stream);
+    bwd_items_kernel<<<1, 1024, 0, stream>>>(cu, ws.plan.tiles, ws.plan.num_tiles, ws.items,
                                            ws.num_items, ws.max_items, st);
+  }
   msa_status_t e = check_launch("bwd_delta/items");
   if (e != MSA_OK) return e;
 
@@ -515,18 +521,30 @@ msa_status_t launch_sparse_bwd(const void* q, const void* k, const void* v, cons
     attr_set = true;
   }
   dim3 grid(ws.max_items, Hkv);
-  sparse_bwd_kernel<<<grid, kBwdThreads, smem, stream>>>(
+  {
+    TraceScope trace_("sparse_bwd_kernel", stream);
+    sparse_bwd_kernel<<<grid, kBwdThreads, smem, stream>>>(
       tq, tk, tv, tdo, sel, cu, lse, ws.delta, ws.items, ws.num_items, Hq, Hkv, G, scale,
       ws.dq_acc, ws.dk_acc, ws.dv_acc, st);
+  }
   e = check_launch("sparse_bwd_kernel");
   if (e != MSA_OK) return e;
 
-  bwd_convert_kernel<<<static_cast<unsigned>((nq / 8 + 255) / 256), 256, 0, stream>>>(
+  {
+    TraceScope trace_("bwd_convert_kernel", stream);
+    bwd_convert_kernel<<<static_cast<unsigned>((nq / 8 + 255) / 256), 256, 0, stream>>>(
       ws.dq_acc, static_cast<__nv_bfloat16*>(dq), nq / 8, scale);
-  bwd_convert_kernel<<<static_cast<unsigned>((nkv / 8 + 255) / 256), 256, 0, stream>>>(
+  }
+  {
+    TraceScope trace_("bwd_convert_kernel", stream);
+    bwd_convert_kernel<<<static_cast<unsigned>((nkv / 8 + 255) / 256), 256, 0, stream>>>(
       ws.dk_acc, static_cast<__nv_bfloat16*>(dk), nkv / 8, scale);
-  bwd_convert_kernel<<<static_cast<unsigned>((nkv / 8 + 255) / 256), 256, 0, stream>>>(
+  }
+  {
+    TraceScope trace_("bwd_convert_kernel", stream);
+    bwd_convert_kernel<<<static_cast<unsigned>((nkv / 8 + 255) / 256), 256, 0, stream>>>(
       ws.dv_acc, static_cast<__nv_bfloat16*>(dv), nkv / 8, 1.0f);
+  }
   return check_launch("bwd_convert_kernel");
 }
 

@@ -344,9 +344,12 @@ msa_status_t launch_sparse_fwd(const void* q, const void* k, const void* v, cons
     attr_set = true;
   }
   dim3 grid(plan.max_tiles * G, Hkv);
-  sparse_fwd_kernel<<<grid, kFwdThreads, smem, stream>>>(
+  {
+    TraceScope trace_("sparse_fwd_kernel", stream);
+    sparse_fwd_kernel<<<grid, kFwdThreads, smem, stream>>>(
       tq, tk, tv, sel, cu, plan.tiles, plan.num_tiles, Hq, Hkv, G, scale,
       static_cast<__nv_bfloat16*>(o), lse, status_word());
+  }
   return check_launch("sparse_fwd_kernel");
 }
 

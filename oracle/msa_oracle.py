@@ -249,7 +249,8 @@ def _row_grads(qt, do_t, kJ, vJ, scale):
 
 def sparse_attn_bwd(q, k, v, do, sel, cu_seqlens, scale: float,
                     dq_tokens: Optional[Iterable[int]] = None,
-                    dkv_blocks: Optional[Iterable[tuple]] = None, block: int = BLOCK):
+                    dkv_blocks: Optional[Iterable[tuple]] = None, block: int = BLOCK,
+                    only_tokens: Optional[Iterable[int]] = None):
     """Gradients of sum(o * do) w.r.t. q, k, v for the block-sparse attention;
     the selection is a constant (frozen indexer) [M31q, PR].
 
@@ -258,7 +259,8 @@ def sparse_attn_bwd(q, k, v, do, sel, cu_seqlens, scale: float,
     dk = scale dS^T q,  dv = P^T do, the sums running over every query row that
     attends to the key.
 
-    Full mode (both selectors None) returns dq [T,Hq,D], dk, dv [T,Hkv,D].
+    Full mode (both selectors None) returns dq [T,Hq,D], dk, dv [T,Hkv,D];
+    with `only_tokens` it sums the contributions of those query tokens only.
     Sampled mode returns dq for `dq_tokens` and, for every (s, g, b) in
     `dkv_blocks`, dk/dv of the keys of block b of sequence s, KV head g."""
     q = np.asarray(q, dtype=np.float64)
@@ -276,7 +278,7 @@ def sparse_attn_bwd(q, k, v, do, sel, cu_seqlens, scale: float,
         dq = np.zeros_like(q)
         dk = np.zeros_like(k)
         dv = np.zeros_like(v)
-        for t in range(T):
+        for t in (range(T) if only_tokens is None else only_tokens):
             s = int(seq_of[t])
             p = int(t - cu[s])
             for g in range(Hkv):

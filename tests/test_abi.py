@@ -28,7 +28,7 @@ def declared_functions():
 def test_header_declares_the_five_calls():
     names = declared_functions()
     for call in ("msa_qk_norm_rope", "msa_index_select", "msa_sparse_attn_fwd",
-                 "msa_sparse_attn_bwd", "msa_decode_step"):
+                 "msa_sparse_attn_bwd", "msa_decode_step", "msa_trace_begin", "msa_trace_end"):
         assert call in names
 
 
@@ -57,15 +57,15 @@ def _err(lib):
 
 
 def test_null_and_misaligned_pointers_are_rejected(lib):
-    rc = lib.msa_qk_norm_rope(None, 10, 1, FAKE, FAKE, 1, 64, 1e7, 1e-6, None)
+    rc = lib.msa_qk_norm_rope(None, FAKE, 10, 1, FAKE, FAKE, 1, 64, 1e7, 1e-6, None)
     assert rc == 1 and "x" in _err(lib)
-    rc = lib.msa_qk_norm_rope(ctypes.c_void_p((1 << 20) + 2), 10, 1, FAKE, FAKE, 1, 64, 1e7,
+    rc = lib.msa_qk_norm_rope(ctypes.c_void_p((1 << 20) + 2), FAKE, 10, 1, FAKE, FAKE, 1, 64, 1e7,
                               1e-6, None)
     assert rc == 1
 
 
 def test_unsupported_shapes_are_rejected(lib):
-    rc = lib.msa_qk_norm_rope(FAKE, 10, 1, FAKE, FAKE, 1, 32, 1e7, 1e-6, None)
+    rc = lib.msa_qk_norm_rope(FAKE, FAKE, 10, 1, FAKE, FAKE, 1, 32, 1e7, 1e-6, None)
     assert rc == 2 and "rope_dim" in _err(lib)
     rc = lib.msa_index_select(FAKE, FAKE, FAKE, 1, 100, 1, 100, 8, FAKE, FAKE, 1 << 20, None)
     assert rc == 2 and "topk" in _err(lib)
@@ -95,3 +95,10 @@ def test_python_binding_refuses_cpu_tensors():
     with pytest.raises(ValueError):
         api.msa_qk_norm_rope(x, torch.zeros(128, dtype=torch.bfloat16),
                              torch.tensor([0, 4], dtype=torch.int32))
+
+
+def test_trace_without_gpu_work_is_empty(lib):
+    assert lib.msa_trace_begin() == 0
+    buf = ctypes.create_string_buffer(256)
+    assert lib.msa_trace_end(buf, 256) == 0
+    assert buf.value == b"{}"

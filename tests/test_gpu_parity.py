@@ -118,12 +118,13 @@ def test_prologue_matches_oracle(m, name):
     shape = SMALL[name]
     cpu, gpu = inputs(name, shape)
     cu = gpu["cu_seqlens"]
-    q, k, qi, ki = (gpu[n].clone() for n in ("q", "k", "q_idx", "k_idx"))
-    m.msa_qk_norm_rope4(q, k, qi, ki, gpu["w_q"], gpu["w_k"], gpu["w_qi"], gpu["w_ki"], cu)
-    q1 = gpu["q"].clone()
-    m.msa_qk_norm_rope(q1, gpu["w_q"], cu)
+    q, k, qi, ki = m.msa_qk_norm_rope4(gpu["q"], gpu["k"], gpu["q_idx"], gpu["k_idx"],
+                                       gpu["w_q"], gpu["w_k"], gpu["w_qi"], gpu["w_ki"], cu)
+    q1 = m.msa_qk_norm_rope(gpu["q"], gpu["w_q"], cu)
+    k2 = gpu["k"].clone()
+    m.msa_qk_norm_rope(k2, gpu["w_k"], cu, out=k2)          # in place
     m.msa_check_status()
-    assert torch.equal(q1, q)
+    assert torch.equal(q1, q) and torch.equal(k2, k)
     cun = cpu["cu_seqlens"].numpy()
     for got, n, wn in ((q, "q", "w_q"), (k, "k", "w_k"), (qi, "q_idx", "w_qi"), (ki, "k_idx", "w_ki")):
         want = O.qk_norm_rope(f64(cpu[n]), f64(cpu[wn]), cun)
@@ -303,8 +304,8 @@ def test_prefill_pipeline_tiny(m):
     shape = W.config(0)
     cpu, gpu = inputs("tiny", shape)
     cu = gpu["cu_seqlens"]
-    q, k, qi, ki = (gpu[n].clone() for n in ("q", "k", "q_idx", "k_idx"))
-    m.msa_qk_norm_rope4(q, k, qi, ki, gpu["w_q"], gpu["w_k"], gpu["w_qi"], gpu["w_ki"], cu)
+    q, k, qi, ki = m.msa_qk_norm_rope4(gpu["q"], gpu["k"], gpu["q_idx"], gpu["k_idx"],
+                                       gpu["w_q"], gpu["w_k"], gpu["w_qi"], gpu["w_ki"], cu)
     sel = m.msa_index_select(qi, ki, cu, shape.max_seqlen)
     o, lse = m.msa_sparse_attn_fwd(q, k, gpu["v"], sel, cu, shape.max_seqlen)
     m.msa_check_status()
