@@ -194,6 +194,38 @@ MSA_API msa_status_t msa_decode_step(const void* q, const void* q_idx, const voi
                              size_t workspace_bytes, msa_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * msa_decode_step_static: the decode step above for callers that cannot
+ * allocate device memory.  The pages have no counterpart of this call; it
+ * exists for integration.  Some callers of a decode step own no allocator:
+ * a serving engine that hands out a fixed pool of GPU memory at start-up and
+ * forbids later cudaMalloc / cudaFree (which synchronize the device and
+ * fragment the pool), or a plugin whose host framework gives it only the
+ * tensors it computes on.  Such a caller cannot provide the workspace that
+ * msa_decode_step needs.
+ *
+ * Same arguments, layouts and results as msa_decode_step, minus the
+ * workspace: the scratch (per-block scores and per-split partial outputs)
+ * lives in one fixed array in the library's device memory, sized for
+ *   B * Hkv <= 256   and   max_pages <= 1024   (128K cached tokens),
+ * about 9.2 MB, which every GPU that loads the library keeps until the
+ * process exits.  Larger calls return MSA_ERR_UNSUPPORTED and enqueue nothing.
+ * The call allocates nothing: no cudaMalloc, no cudaFree, no allocating
+ * library routine.  Its first call on a device looks up that device's copy
+ * of the array (a host-side query, done with the device current); make that
+ * first call before any stream capture.  All calls share the one array, so
+ * two calls whose kernels may overlap on the GPU (different streams, no
+ * ordering between them) race and corrupt each other's results; calls on one
+ * stream are safe.  Every scratch element a call reads is written earlier in
+ * the same call, so leftovers of a previous call do not matter.
+ */
+MSA_API msa_status_t msa_decode_step_static(const void* q, const void* q_idx,
+                                            const void* k_cache, const void* v_cache,
+                                            const void* kidx_cache, const int32_t* block_table,
+                                            const int32_t* cache_lens, int B, int Hq, int Hkv,
+                                            int num_pages, int max_pages, float scale, void* o,
+                                            int32_t* sel_out, msa_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * Launch tracing (no counterpart on the pages: measurement plumbing).
  * msa_trace_begin() clears the record and turns tracing on: from then on the
  * library brackets each of its kernel launches with a pair of CUDA events on

@@ -46,6 +46,8 @@ _SIGNATURES = {
     "msa_decode_step_workspace_size": (_c_size, [_c_int, _c_int, _c_int, _c_int]),
     "msa_decode_step": (_c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int,
                                  _c_int, _c_int, _c_float, _vp, _vp, _vp, _c_size, _vp]),
+    "msa_decode_step_static": (_c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _c_int, _c_int,
+                                        _c_int, _c_int, _c_int, _c_float, _vp, _vp, _vp]),
 }
 
 STATUS = {0: "MSA_OK", 1: "MSA_ERR_INVALID_ARG", 2: "MSA_ERR_UNSUPPORTED", 3: "MSA_ERR_CUDA",

@@ -488,3 +488,99 @@ msa_status_t launch_decode(const void* q, const void* q_idx, const void* k_cache
 }
 
 }  // namespace msa
+
+// ==================================================================== no-alloc variant
+//
+// msa_decode_step_static: the decode step for callers that own no device
+// allocator (see msa.h).  Its scratch is the fixed array below instead of a
+// caller workspace; the kernels and their launch sequence are those of
+// msa_decode_step.
+
+#include <mutex>
+
+namespace msa {
+namespace {
+
+constexpr int kStaticMaxRows = 256;     // B * Hkv
+constexpr int kStaticMaxPages = 1024;   // pages (128-token blocks) per sequence
+constexpr size_t kStaticScores = static_cast<size_t>(kStaticMaxRows) * kStaticMaxPages;
+constexpr size_t kStaticPartO = static_cast<size_t>(kStaticMaxRows) * kDecodeSplits * 16 * kD;
+constexpr size_t kStaticPartMl = static_cast<size_t>(kStaticMaxRows) * kDecodeSplits * 16 * 2;
+
+// One copy per GPU that loads the library, kept until the process exits
+// (about 9.2 MB).  In host code this name is only a host-side stand-in for
+// the symbol: kernels must be given the device address that
+// cudaGetSymbolAddress returns for the current device.
+static __device__ __align__(256) float g_decode_scratch[kStaticScores + kStaticPartO +
+                                                        kStaticPartMl];
+
+std::mutex g_static_mu;
+float* g_static_ptr[64] = {nullptr};
+
+// Device address of g_decode_scratch on the current device, looked up once
+// per device (with that device current) and cached.
+msa_status_t static_scratch(float** out) {
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail(MSA_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+  if (dev < 0 || dev >= 64) return fail(MSA_ERR_UNSUPPORTED, "device index %d above 63", dev);
+  std::lock_guard<std::mutex> lk(g_static_mu);
+  if (!g_static_ptr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_decode_scratch);
+    if (e != cudaSuccess || p == nullptr)
+      return fail(MSA_ERR_CUDA, "cudaGetSymbolAddress(decode scratch): %s",
+                  cudaGetErrorString(e));
+    g_static_ptr[dev] = static_cast<float*>(p);
+  }
+  *out = g_static_ptr[dev];
+  return MSA_OK;
+}
+
+}  // namespace
+}  // namespace msa
+
+extern "C" msa_status_t msa_decode_step_static(const void* q, const void* q_idx,
+                                               const void* k_cache, const void* v_cache,
+                                               const void* kidx_cache,
+                                               const int32_t* block_table,
+                                               const int32_t* cache_lens, int B, int Hq,
+                                               int Hkv, int num_pages, int max_pages,
+                                               float scale, void* o, int32_t* sel_out,
+                                               msa_stream_t stream) {
+  using namespace msa;
+  const void* ptrs[] = {q, q_idx, k_cache, v_cache, kidx_cache, block_table, cache_lens, o};
+  const char* names[] = {"q", "q_idx", "k_cache", "v_cache", "kidx_cache", "block_table",
+                         "cache_lens", "o"};
+  for (int i = 0; i < 8; ++i)
+    if (!ptrs[i] || !aligned16(ptrs[i]))
+      return fail(MSA_ERR_INVALID_ARG, "%s is null or not 16-byte aligned", names[i]);
+  if (sel_out && !aligned16(sel_out))
+    return fail(MSA_ERR_INVALID_ARG, "sel_out is not 16-byte aligned");
+  if (B < 1 || num_pages < 1 || max_pages < 1)
+    return fail(MSA_ERR_INVALID_ARG, "B, num_pages and max_pages must be >= 1");
+  if (Hq < 1 || Hkv < 1 || Hq != 16 * Hkv)
+    return fail(MSA_ERR_UNSUPPORTED, "decode needs Hq = 16 * Hkv (got Hq %d, Hkv %d)", Hq, Hkv);
+  if (!(scale > 0.0f)) return fail(MSA_ERR_INVALID_ARG, "scale must be > 0");
+  if (static_cast<long long>(B) * Hkv > kStaticMaxRows)
+    return fail(MSA_ERR_UNSUPPORTED,
+                "msa_decode_step_static holds scratch for B * Hkv <= %d (got %d x %d); "
+                "use msa_decode_step with a workspace",
+                kStaticMaxRows, B, Hkv);
+  if (max_pages > kStaticMaxPages)
+    return fail(MSA_ERR_UNSUPPORTED,
+                "msa_decode_step_static holds scratch for max_pages <= %d (got %d); "
+                "use msa_decode_step with a workspace",
+                kStaticMaxPages, max_pages);
+  float* base = nullptr;
+  msa_status_t st = static_scratch(&base);
+  if (st != MSA_OK) return st;
+  DecodeWorkspace ws;
+  ws.max_pages = max_pages;
+  ws.scores = base;                                   // [B, Hkv, max_pages]
+  ws.part_o = base + kStaticScores;                   // [B, Hkv, splits, 16, 128]
+  ws.part_ml = base + kStaticScores + kStaticPartO;   // [B, Hkv, splits, 16, 2]
+  return launch_decode(q, q_idx, k_cache, v_cache, kidx_cache, block_table, cache_lens, B, Hq,
+                       Hkv, num_pages, max_pages, scale, o, sel_out, ws,
+                       static_cast<cudaStream_t>(stream));
+}
