@@ -3,7 +3,7 @@ inputs.  Small packs (several tiles, ragged tails, an empty sequence) compare
 every output element; the full workload sizes compare sampled outputs that the
 oracle computes one by one.
 
-Tolerances (the benchmark spec of the method's statement): selected block sets are
+Tolerances (from the statement of the method's acceptance): selected block sets are
 bit-exact except on rows the oracle marks as near-ties (relative gap between
 the 15th and 16th earlier block below 1e-3), which are counted; given the same
 selection, o is within max-abs 2e-2 and rel-L2 1e-2 (bf16 I/O, fp32
