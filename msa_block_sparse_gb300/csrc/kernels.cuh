@@ -33,7 +33,7 @@ msa_status_t launch_sparse_fwd(const void* q, const void* k, const void* v, cons
 // ---------------------------------------------------------------- sparse backward
 // Work items of the KV-major backward: (sequence, key block, segment of
 // candidate query tokens), listed key block ascending.
-constexpr int kBwdSegment = 1024;   // candidate query tokens per work item
+constexpr int kBwdSegment = 256;    // window of candidate query positions per work item
 
 struct BwdWorkspace {
   Plan plan;

@@ -3,96 +3,114 @@
 // indexer is frozen, so the selection is a constant here).
 //
 // KV-major schedule.  A work item is (KV head g, key block b of sequence s, a
-// segment of candidate query positions).  Its CTA keeps K_b and V_b in shared
-// memory and streams the query tokens of the segment that selected b, in
+// 256-position window of candidate query positions).  Items are listed window
+// by window, so the items running at any moment add into dQ rows of a few
+// windows only and the fp32 dQ accumulator lines stay in L2.  Persistent CTAs
+// (one per SM) stride over the items.  Per item the CTA holds K_b and V_b in
+// shared memory and streams the query tokens of the window that selected b, in
 // ascending order, in chunks of 128/G tokens x G heads = 128 columns:
-//   scanner  : warp 0 reads each candidate's 16 selected ids, compacts the
-//              matches with a ballot, loads the chunk's Q and dO rows by TMA
-//              and its lse / Delta values into shared memory
-//   MMA      : S^T = K_b Q^T and dP^T = V_b dO^T (M = keys, N = columns)
-//   compute  : thread = key; P^T = exp2(S^T log2e scale - lse log2e) masked
-//              causally, dS^T = P^T (dP^T - Delta); both as bf16 in shared
-//              memory (one buffer serves as K-major and MN-major operand)
-//   MMA      : dV += P^T dO, dK += dS^T Q (TMEM accumulators over the whole
-//              item), dQ^T = K_b^T dS^T (M = head dim, N = columns)
-//   compute  : dQ^T drained from TMEM into the fp32 dQ accumulator with
-//              coalesced atomics (a warp covers 32 consecutive channels)
-// At the end of the item dK and dV are added to fp32 accumulators (segments
-// of one block add up there); a last kernel scales and converts to bf16.
+//   scanner (warp 0): reads each candidate's 16 selected ids, compacts the
+//            matches with a ballot, loads the chunk's Q and dO rows by TMA
+//            (one box per token) and its lse / Delta into a 2-stage ring
+//   MMA (warp 1): S^T = K_b Q^T -> TMEM, dP^T = V_b dO^T -> TMEM,
+//            dV += P^T dO (P^T read from TMEM), dK += dS^T Q,
+//            dQ = dS K_b (dS^T in shared memory read as an MN-major operand)
+//   compute (warps 2..9, thread = key row x 64 columns):
+//            P^T = exp2(S^T scale log2e - lse log2e), causally masked, packed
+//            to bf16 into TMEM; dS^T = P^T (dP^T - Delta) to shared memory;
+//            then dQ rows (lane = column) added to the fp32 accumulator with
+//            16-byte atomics; at the end of an item dK, dV likewise.
+// A last kernel scales and converts the accumulators to bf16.
 #include "kernels.cuh"
 
 namespace msa {
 
 namespace {
 
-constexpr int kBwdThreads = 192;            // warp 0 scan + TMA, warp 1 MMA, warps 2..5 compute
+constexpr int kBwdThreads = 320;            // warp 0 scan + TMA, warp 1 MMA, warps 2..9 compute
+constexpr int kComputeThreads = 256;
 constexpr int kTile = 128 * 128 * 2;
 constexpr int kHalf = kTile / 2;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr uint32_t kIdescKK = idesc_bf16(128, 128, false, false);   // both K-major
 constexpr uint32_t kIdescKM = idesc_bf16(128, 128, false, true);    // B MN-major
 constexpr uint32_t kIdescMM = idesc_bf16(128, 128, true, true);     // both MN-major
+// TMEM columns
+constexpr uint32_t kColDV = 0, kColDK = 128, kColS = 256, kColDP = 384;
 
 struct BwdSmem {
   uint8_t k[kTile];
   uint8_t v[kTile];
-  uint8_t q[kTile];
-  uint8_t dout[kTile];
-  uint8_t pt[kTile];
+  uint8_t q[2][kTile];
+  uint8_t dout[2][kTile];
   uint8_t dst[kTile];
-  float lse2[128];
-  float delta[128];
-  int tok[16];
-  int ntok;
-  uint64_t kv_full;
-  uint64_t ld_full;
-  uint64_t ld_empty;
-  uint64_t st_full;
-  uint64_t ds_full;
-  uint64_t mm_done;
-  uint64_t dq_free;
+  float lse2[2][128];
+  float delta[2][128];
+  int tok[2][16];
+  int ntok[2];
+  uint64_t kv_full, kv_empty;
+  uint64_t ld_full[2], ld_empty[2];
+  uint64_t s_full, dp_full, p_full, ds_full, dv_done, dq_full, dq_free;
   uint32_t tmem_base;
 };
+static_assert(sizeof(BwdSmem) <= 232448, "backward shared memory above the 227 KB limit");
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ void umma_bf16_tmem_a(uint32_t d_tmem, uint32_t a_tmem,
+                                                 uint64_t b_desc, uint32_t idesc,
+                                                 uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
 
 }  // namespace
 
 // ---------------------------------------------------------------- items
 
-// One CTA: turns the tile plan (qb descending) into work items with the key
-// block ascending, each block split into segments of kBwdSegment candidate
-// query positions [128 b, len).
-__global__ void __launch_bounds__(1024) bwd_items_kernel(const int32_t* __restrict__ cu,
-                                                         const int2* __restrict__ tiles,
-                                                         const int* __restrict__ num_tiles,
+// One CTA.  Pairs (window w, sequence s) in w-major order; pair (w, s) holds the
+// key blocks b that some query of window w can select: 128 b < min(len, (w+1) W).
+// Each becomes an item (s, b, first position, end position) of that window.
+__global__ void __launch_bounds__(1024) bwd_items_kernel(const int32_t* __restrict__ cu, int S,
+                                                         int num_windows,
                                                          int4* __restrict__ items,
                                                          int* __restrict__ num_items,
                                                          int max_items, uint32_t* status) {
   __shared__ int warp_sums[32];
   __shared__ int carry;
-  const int n = *num_tiles;
   if (threadIdx.x == 0) carry = 0;
   __syncthreads();
-  for (int base = 0; base < n; base += blockDim.x) {
-    const int j = base + threadIdx.x;
-    int s = 0, b = 0, len = 0, nseg = 0;
-    if (j < n) {
-      const int2 t = tiles[n - 1 - j];
-      s = t.x;
-      b = t.y;
+  const long long npairs = static_cast<long long>(num_windows) * S;
+  for (long long base = 0; base < npairs; base += blockDim.x) {
+    const long long pi = base + threadIdx.x;
+    int s = 0, w = 0, len = 0, cnt = 0;
+    if (pi < npairs) {
+      w = static_cast<int>(pi / S);
+      s = static_cast<int>(pi % S);
       len = cu[s + 1] - cu[s];
-      nseg = (len - b * kBlock + kBwdSegment - 1) / kBwdSegment;
+      const int w0 = w * kBwdSegment;
+      if (len > w0) {
+        const int hi = min(len, w0 + kBwdSegment);
+        cnt = (hi + kBlock - 1) / kBlock;
+      }
     }
-    // block-wide exclusive scan of nseg
-    int incl = nseg;
-    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    int incl = cnt;
+    const int lane = threadIdx.x & 31, wp = threadIdx.x >> 5;
 #pragma unroll
     for (int d = 1; d < 32; d <<= 1) {
       const int x = __shfl_up_sync(0xffffffffu, incl, d);
       if (lane >= d) incl += x;
     }
-    if (lane == 31) warp_sums[w] = incl;
+    if (lane == 31) warp_sums[wp] = incl;
     __syncthreads();
-    if (w == 0) {
+    if (wp == 0) {
       int ws = (lane < static_cast<int>(blockDim.x >> 5)) ? warp_sums[lane] : 0;
 #pragma unroll
       for (int d = 1; d < 32; d <<= 1) {
@@ -102,15 +120,17 @@ __global__ void __launch_bounds__(1024) bwd_items_kernel(const int32_t* __restri
       warp_sums[lane] = ws;
     }
     __syncthreads();
-    const int off = carry + (w > 0 ? warp_sums[w - 1] : 0) + incl - nseg;
-    for (int k = 0; k < nseg; ++k) {
-      const int idx = off + k;
-      const int p0 = b * kBlock + k * kBwdSegment;
-      if (idx < max_items) items[idx] = make_int4(s, b, p0, min(len, p0 + kBwdSegment));
-      else atomicOr(status, kStatusBounds);
+    const int off = carry + (wp > 0 ? warp_sums[wp - 1] : 0) + incl - cnt;
+    const int w0 = w * kBwdSegment;
+    for (int b = 0; b < cnt; ++b) {
+      const int idx = off + b;
+      if (idx < max_items)
+        items[idx] = make_int4(s, b, max(b * kBlock, w0), min(len, w0 + kBwdSegment));
+      else
+        atomicOr(status, kStatusBounds);
     }
     __syncthreads();
-    if (threadIdx.x == blockDim.x - 1) carry = off + nseg;
+    if (threadIdx.x == blockDim.x - 1) carry = off + cnt;
     __syncthreads();
   }
   if (threadIdx.x == 0) *num_items = min(carry, max_items);
@@ -166,32 +186,37 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                       const __grid_constant__ CUtensorMap tm_do, const int32_t* __restrict__ sel,
                       const int32_t* __restrict__ cu, const float* __restrict__ lse,
                       const float* __restrict__ delta, const int4* __restrict__ items,
-                      const int* __restrict__ num_items, int Hq, int Hkv, int G, float scale,
+                      const int* __restrict__ num_items, int Hq, int Hkv, float scale,
                       float* __restrict__ dq_acc, float* __restrict__ dk_acc,
                       float* __restrict__ dv_acc, uint32_t* status) {
-  if (static_cast<int>(blockIdx.x) >= *num_items) return;
-  const int4 item = items[blockIdx.x];
-  const int s = item.x, b = item.y, pbeg = item.z, pend = item.w;
+  constexpr int G = 16, tpt = 8;    // heads per KV group, tokens per chunk
+  const int n_items = *num_items;
+  if (static_cast<int>(blockIdx.x) >= n_items) return;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  if (smem_u32(smem_raw) & 1023u) {   // the tiles need 1024-byte alignment
+    if (threadIdx.x == 0) atomicOr(status, kStatusBounds);
+    return;
+  }
+  BwdSmem& sm = *reinterpret_cast<BwdSmem*>(smem_raw);
   const int g = blockIdx.y;
-  const int seq0 = cu[s];
-  const int len = cu[s + 1] - seq0;
-  const int tpt = 128 / G;
-
-  extern __shared__ uint8_t smem_raw[];
-  BwdSmem& sm = *reinterpret_cast<BwdSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                            ~static_cast<uintptr_t>(1023));
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
 
   if (tid == 0) {
     mbar_init(&sm.kv_full, 1);
-    mbar_init(&sm.ld_full, 1);
-    mbar_init(&sm.ld_empty, 1);
-    mbar_init(&sm.st_full, 1);
-    mbar_init(&sm.ds_full, 128);
-    mbar_init(&sm.mm_done, 1);
-    mbar_init(&sm.dq_free, 128);
+    mbar_init(&sm.kv_empty, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&sm.ld_full[i], 1);
+      mbar_init(&sm.ld_empty[i], 1 + kComputeThreads);
+    }
+    mbar_init(&sm.s_full, 1);
+    mbar_init(&sm.dp_full, 1);
+    mbar_init(&sm.p_full, kComputeThreads);
+    mbar_init(&sm.ds_full, kComputeThreads);
+    mbar_init(&sm.dv_done, 1);
+    mbar_init(&sm.dq_full, 1);
+    mbar_init(&sm.dq_free, kComputeThreads);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -202,241 +227,322 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = sm.tmem_base;
-  const uint32_t t_dv = tmem, t_dk = tmem + 128, t_s = tmem + 256, t_dp = tmem + 384;
 
   if (warp == 0) {
     // ------------------------------------------------------------ scanner / TMA
     if (lane == 0) {
       prefetch_tmap(&tm_q);
       prefetch_tmap(&tm_do);
-      mbar_arrive_expect_tx(&sm.kv_full, 2 * kTile);
-      const int row = seq0 + b * kBlock;
-      tma_load_3d(sm.k, &tm_k, &sm.kv_full, 0, g, row);
-      tma_load_3d(sm.k + kHalf, &tm_k, &sm.kv_full, 64, g, row);
-      tma_load_3d(sm.v, &tm_v, &sm.kv_full, 0, g, row);
-      tma_load_3d(sm.v + kHalf, &tm_v, &sm.kv_full, 64, g, row);
+      prefetch_tmap(&tm_k);
+      prefetch_tmap(&tm_v);
     }
-    int chunk = 0, cnt = 0, my_pos = -1;
+    uint32_t cg = 0;
     bool alive = true;
-    auto emit = [&](int n) {
-      // wait until the previous chunk's MMAs have released the Q/dO buffer
-      if (lane == 0) alive = mbar_wait(&sm.ld_empty, (chunk & 1) ^ 1, status);
-      alive = __shfl_sync(0xffffffffu, alive ? 1 : 0, 0) != 0;
-      if (!alive) return;
-      const int first = __shfl_sync(0xffffffffu, my_pos, 0);
-      const int pos = (lane < n) ? my_pos : first;
-      if (lane < tpt) {
-        sm.tok[lane] = (lane < n) ? pos : -1;
-        const size_t base = static_cast<size_t>(seq0 + pos) * Hq + g * G;
-        for (int h = 0; h < G; ++h) {
-          sm.lse2[lane * G + h] = __ldg(lse + base + h) * kLog2e;
-          sm.delta[lane * G + h] = __ldg(delta + base + h);
+    int itl = 0;
+    for (int it = blockIdx.x; alive && it < n_items; it += gridDim.x, ++itl) {
+      const int4 item = items[it];
+      const int s = item.x, b = item.y, pbeg = item.z, pend = item.w;
+      const int seq0 = cu[s];
+      if (lane == 0) {
+        alive = mbar_wait(&sm.kv_empty, (itl & 1) ^ 1, status);
+        if (alive) {
+          mbar_arrive_expect_tx(&sm.kv_full, 2 * kTile);
+          const int row = seq0 + b * kBlock;
+          tma_load_3d(sm.k, &tm_k, &sm.kv_full, 0, g, row);
+          tma_load_3d(sm.k + kHalf, &tm_k, &sm.kv_full, 64, g, row);
+          tma_load_3d(sm.v, &tm_v, &sm.kv_full, 0, g, row);
+          tma_load_3d(sm.v + kHalf, &tm_v, &sm.kv_full, 64, g, row);
         }
       }
-      if (lane == 0) sm.ntok = n;
-      __syncwarp();
-      if (n > 0) {
-        int slot_pos[16];
+      alive = __shfl_sync(0xffffffffu, alive ? 1 : 0, 0) != 0;
+      int cnt = 0, my_pos = -1;
+      auto emit = [&](int n) {
+        const int st = cg & 1;
+        if (lane == 0) alive = mbar_wait(&sm.ld_empty[st], ((cg >> 1) & 1) ^ 1, status);
+        alive = __shfl_sync(0xffffffffu, alive ? 1 : 0, 0) != 0;
+        if (!alive) return;
+        const int first = __shfl_sync(0xffffffffu, my_pos, 0);
+        const int pos = (lane < n) ? my_pos : first;
+        if (lane < tpt && n > 0) {
+          sm.tok[st][lane] = (lane < n) ? pos : -1;
+          const size_t base = static_cast<size_t>(seq0 + pos) * Hq + g * G;
+          const float4* l4 = reinterpret_cast<const float4*>(lse + base);
+          const float4* d4 = reinterpret_cast<const float4*>(delta + base);
 #pragma unroll
-        for (int i = 0; i < 16; ++i) slot_pos[i] = __shfl_sync(0xffffffffu, pos, i);
-        if (lane == 0) {
-          mbar_arrive_expect_tx(&sm.ld_full, 2 * kTile);
-          for (int i = 0; i < tpt; ++i) {
-            const int t = seq0 + slot_pos[i];
-            const uint32_t off = i * G * 128;
-            tma_load_3d(sm.q + off, &tm_q, &sm.ld_full, 0, g * G, t);
-            tma_load_3d(sm.q + kHalf + off, &tm_q, &sm.ld_full, 64, g * G, t);
-            tma_load_3d(sm.dout + off, &tm_do, &sm.ld_full, 0, g * G, t);
-            tma_load_3d(sm.dout + kHalf + off, &tm_do, &sm.ld_full, 64, g * G, t);
+          for (int q4 = 0; q4 < G / 4; ++q4) {
+            float4 lv = __ldg(l4 + q4);
+            lv.x *= kLog2e; lv.y *= kLog2e; lv.z *= kLog2e; lv.w *= kLog2e;
+            reinterpret_cast<float4*>(&sm.lse2[st][lane * G])[q4] = lv;
+            reinterpret_cast<float4*>(&sm.delta[st][lane * G])[q4] = __ldg(d4 + q4);
           }
         }
-      } else if (lane == 0) {
-        mbar_arrive(&sm.ld_full);   // end marker: no data
-      }
-      ++chunk;
-    };
-    for (int base = pbeg; alive && base < pend; base += 32) {
-      const int p = base + lane;
-      bool hit = false;
-      if (p < pend) {
-        const int4* row = reinterpret_cast<const int4*>(
-            sel + (static_cast<size_t>(seq0 + p) * Hkv + g) * kTopK);
+        if (lane == 0) sm.ntok[st] = n;
+        __syncwarp();
+        if (n > 0) {
+          int slot_pos[tpt];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const int4 v = __ldg(row + c);
-          hit |= (v.x == b) | (v.y == b) | (v.z == b) | (v.w == b);
+          for (int i = 0; i < tpt; ++i) slot_pos[i] = __shfl_sync(0xffffffffu, pos, i);
+          if (lane == 0) {
+            mbar_arrive_expect_tx(&sm.ld_full[st], 2 * kTile);
+#pragma unroll
+            for (int i = 0; i < tpt; ++i) {
+              const int t = seq0 + slot_pos[i];
+              const uint32_t off = i * G * 128;
+              tma_load_3d(sm.q[st] + off, &tm_q, &sm.ld_full[st], 0, g * G, t);
+              tma_load_3d(sm.q[st] + kHalf + off, &tm_q, &sm.ld_full[st], 64, g * G, t);
+              tma_load_3d(sm.dout[st] + off, &tm_do, &sm.ld_full[st], 0, g * G, t);
+              tma_load_3d(sm.dout[st] + kHalf + off, &tm_do, &sm.ld_full[st], 64, g * G, t);
+            }
+          }
+        } else if (lane == 0) {
+          mbar_arrive(&sm.ld_full[st]);   // end of the item: no data
+        }
+        ++cg;
+      };
+      for (int base = pbeg; alive && base < pend; base += 32) {
+        const int p = base + lane;
+        bool hit = false;
+        if (p < pend) {
+          const int4* row = reinterpret_cast<const int4*>(
+              sel + (static_cast<size_t>(seq0 + p) * Hkv + g) * kTopK);
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const int4 v = __ldg(row + c);
+            hit |= (v.x == b) | (v.y == b) | (v.z == b) | (v.w == b);
+          }
+        }
+        uint32_t mask = __ballot_sync(0xffffffffu, hit);
+        while (mask) {
+          const int bit = __ffs(mask) - 1;
+          mask &= mask - 1;
+          if (lane == cnt) my_pos = base + bit;
+          if (++cnt == tpt) {
+            emit(tpt);
+            cnt = 0;
+            if (!alive) break;
+          }
         }
       }
-      uint32_t mask = __ballot_sync(0xffffffffu, hit);
-      while (mask) {
-        const int bit = __ffs(mask) - 1;
-        mask &= mask - 1;
-        if (lane == cnt) my_pos = base + bit;
-        if (++cnt == tpt) {
-          emit(tpt);
-          cnt = 0;
-          if (!alive) break;
-        }
-      }
+      if (alive && cnt > 0) emit(cnt);
+      if (alive) emit(0);
     }
-    if (alive && cnt > 0) emit(cnt);
-    if (alive) emit(0);
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (elect_one()) {
-      bool ok = mbar_wait(&sm.kv_full, 0, status);
-      const uint32_t ka = smem_u32(sm.k), va = smem_u32(sm.v);
-      const uint32_t qa = smem_u32(sm.q), da = smem_u32(sm.dout);
-      const uint32_t pa = smem_u32(sm.pt), sa = smem_u32(sm.dst);
-      for (int c = 0; ok; ++c) {
-        ok = mbar_wait(&sm.ld_full, c & 1, status);
-        if (!ok || sm.ntok == 0) break;
-        tc_fence_after();
-        // dP^T = V dO^T -> t_dp (free: the compute warps read it before ds_full of c-1)
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
-          umma_bf16(t_dp, sdesc_sw128(va + off, 16, 1024), sdesc_sw128(da + off, 16, 1024),
-                    kIdescKK, kk > 0);
-        }
-        // S^T = K Q^T -> t_s, once dQ^T of the previous chunk has been drained
-        if (c > 0) {
-          ok = mbar_wait(&sm.dq_free, (c - 1) & 1, status);
+      const uint32_t ka = smem_u32(sm.k), va = smem_u32(sm.v), sa = smem_u32(sm.dst);
+      uint32_t cg = 0, cm = 0;
+      bool ok = true;
+      int itl = 0;
+      for (int it = blockIdx.x; ok && it < n_items; it += gridDim.x, ++itl) {
+        ok = mbar_wait(&sm.kv_full, itl & 1, status);
+        bool first = true;
+        while (ok) {
+          const int st = cg & 1;
+          ok = mbar_wait(&sm.ld_full[st], (cg >> 1) & 1, status);
+          ++cg;
           if (!ok) break;
+          if (sm.ntok[st] == 0) {
+            mbar_arrive(&sm.ld_empty[st]);
+            break;
+          }
           tc_fence_after();
-        }
+          const uint32_t qa = smem_u32(sm.q[st]), da = smem_u32(sm.dout[st]);
+          // S^T = K Q^T (needs P^T of the previous chunk consumed by its dV)
+          if (cm > 0 && !(ok = mbar_wait(&sm.dv_done, (cm - 1) & 1, status))) break;
+          tc_fence_after();
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
-          umma_bf16(t_s, sdesc_sw128(ka + off, 16, 1024), sdesc_sw128(qa + off, 16, 1024),
-                    kIdescKK, kk > 0);
-        }
-        umma_commit(&sm.st_full);
-        ok = mbar_wait(&sm.ds_full, c & 1, status);
-        if (!ok) break;
-        tc_fence_after();
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
+            umma_bf16(tmem + kColS, sdesc_sw128(ka + off, 16, 1024),
+                      sdesc_sw128(qa + off, 16, 1024), kIdescKK, kk > 0);
+          }
+          umma_commit(&sm.s_full);
+          // dP^T = V dO^T (needs dQ of the previous chunk drained)
+          if (cm > 0 && !(ok = mbar_wait(&sm.dq_free, (cm - 1) & 1, status))) break;
+          tc_fence_after();
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {   // K dimension = the 128 columns
-          const uint32_t aoff = (kk >> 2) * kHalf + (kk & 3) * 32;
-          const uint32_t boff = kk * 2048;
-          // dV += P^T dO      (A = P^T K-major, B = dO as MN-major [col][d])
-          umma_bf16(t_dv, sdesc_sw128(pa + aoff, 16, 1024), sdesc_sw128(da + boff, kHalf, 1024),
-                    kIdescKM, (c > 0 || kk > 0));
-          // dK += dS^T Q      (A = dS^T K-major, B = Q as MN-major)
-          umma_bf16(t_dk, sdesc_sw128(sa + aoff, 16, 1024), sdesc_sw128(qa + boff, kHalf, 1024),
-                    kIdescKM, (c > 0 || kk > 0));
-        }
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
+            umma_bf16(tmem + kColDP, sdesc_sw128(va + off, 16, 1024),
+                      sdesc_sw128(da + off, 16, 1024), kIdescKK, kk > 0);
+          }
+          umma_commit(&sm.dp_full);
+          // dV += P^T dO, P^T packed in TMEM: columns [64h, 64h+64) of the chunk
+          // at TMEM kColS + 64h .. + 32
+          if (!(ok = mbar_wait(&sm.p_full, cm & 1, status))) break;
+          tc_fence_after();
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {   // K dimension = the 128 keys
-          const uint32_t off = kk * 2048;
-          // dQ^T = K^T dS^T   (A = K as MN-major [key][d], B = dS^T as MN-major [key][col])
-          umma_bf16(t_s, sdesc_sw128(ka + off, kHalf, 1024), sdesc_sw128(sa + off, kHalf, 1024),
-                    kIdescMM, kk > 0);
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint32_t a_t = tmem + kColS + (kk >> 2) * 64 + (kk & 3) * 8;
+            umma_bf16_tmem_a(tmem + kColDV, a_t, sdesc_sw128(da + kk * 2048, kHalf, 1024),
+                             kIdescKM, (!first || kk > 0));
+          }
+          umma_commit(&sm.dv_done);
+          // dK += dS^T Q and dQ = dS K
+          if (!(ok = mbar_wait(&sm.ds_full, cm & 1, status))) break;
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint32_t aoff = (kk >> 2) * kHalf + (kk & 3) * 32;
+            umma_bf16(tmem + kColDK, sdesc_sw128(sa + aoff, 16, 1024),
+                      sdesc_sw128(qa + kk * 2048, kHalf, 1024), kIdescKM, (!first || kk > 0));
+          }
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint32_t off = kk * 2048;
+            umma_bf16(tmem + kColDP, sdesc_sw128(sa + off, kHalf, 1024),
+                      sdesc_sw128(ka + off, kHalf, 1024), kIdescMM, kk > 0);
+          }
+          umma_commit(&sm.dq_full);
+          umma_commit(&sm.ld_empty[st]);
+          first = false;
+          ++cm;
         }
-        umma_commit(&sm.mm_done);
-        umma_commit(&sm.ld_empty);
+        umma_commit(&sm.kv_empty);   // K_b / V_b free once this item's MMAs are done
       }
     }
   } else {
     // ------------------------------------------------------------ compute
-    const int subp = warp & 3;
-    const int r = subp * 32 + lane;           // key row (and head-dim row for dQ^T)
+    const int cw = warp - 2;                // 0..7
+    const int subp = warp & 3;              // TMEM sub-partition (lanes 32 subp ..)
+    const int h = cw >> 2;                  // column half: chunk columns [64h, 64h + 64)
+    const int r = subp * 32 + lane;         // key row; also the dQ column (token, head)
     const uint32_t trow = static_cast<uint32_t>(subp * 32) << 16;
-    const int kp = b * kBlock + r;            // key position in the sequence
     const float sl2 = scale * kLog2e;
-    int nchunks = 0;
+    uint32_t cg = 0, cm = 0;
     bool ok = true;
-    for (int c = 0; ok; ++c) {
-      if (!mbar_wait(&sm.ld_full, c & 1, status)) { ok = false; break; }
-      const int ntok = sm.ntok;
-      if (ntok == 0) break;
-      int tokp[16];
-#pragma unroll
-      for (int i = 0; i < 16; ++i) tokp[i] = (i < tpt) ? sm.tok[i] : -1;
-      if (!mbar_wait(&sm.st_full, c & 1, status)) { ok = false; break; }
-      __syncwarp();
-      tc_fence_after();
-#pragma unroll 1
-      for (int cc = 0; cc < 4; ++cc) {
-        uint32_t sv[32], dv[32];
-        tmem_ld32(t_s + trow + cc * 32, sv);
-        tmem_ld32(t_dp + trow + cc * 32, dv);
-        tmem_ld_wait();
-        float pv[32], dsv[32];
-#pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const int col = cc * 32 + j;
-          const int tpos = tokp[col / G];
-          const bool valid = tpos >= 0 && kp <= tpos;
-          const float p = valid ? exp2f(fmaf(__uint_as_float(sv[j]), sl2, -sm.lse2[col])) : 0.f;
-          pv[j] = p;
-          dsv[j] = p * (__uint_as_float(dv[j]) - sm.delta[col]);
+    for (int it = blockIdx.x; ok && it < n_items; it += gridDim.x) {
+      const int4 item = items[it];
+      const int s = item.x, b = item.y;
+      const int seq0 = cu[s];
+      const int len = cu[s + 1] - seq0;
+      const int kp = b * kBlock + r;        // key position of this row
+      int nch = 0;
+      while (true) {
+        const int st = cg & 1;
+        if (!(ok = mbar_wait(&sm.ld_full[st], (cg >> 1) & 1, status))) break;
+        ++cg;
+        const int n = sm.ntok[st];
+        if (n == 0) {
+          mbar_arrive(&sm.ld_empty[st]);
+          break;
         }
+        int tokp[4];
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-          const int chunk16 = cc * 4 + q4;   // 8 columns per 16-byte chunk
-          const uint32_t off = (chunk16 >> 3) * kHalf + sw128_offset(r, chunk16 & 7);
-          uint4 a, d;
-          a.x = pack_bf16x2(pv[8 * q4 + 0], pv[8 * q4 + 1]);
-          a.y = pack_bf16x2(pv[8 * q4 + 2], pv[8 * q4 + 3]);
-          a.z = pack_bf16x2(pv[8 * q4 + 4], pv[8 * q4 + 5]);
-          a.w = pack_bf16x2(pv[8 * q4 + 6], pv[8 * q4 + 7]);
-          d.x = pack_bf16x2(dsv[8 * q4 + 0], dsv[8 * q4 + 1]);
-          d.y = pack_bf16x2(dsv[8 * q4 + 2], dsv[8 * q4 + 3]);
-          d.z = pack_bf16x2(dsv[8 * q4 + 4], dsv[8 * q4 + 5]);
-          d.w = pack_bf16x2(dsv[8 * q4 + 6], dsv[8 * q4 + 7]);
-          *reinterpret_cast<uint4*>(sm.pt + off) = a;
-          *reinterpret_cast<uint4*>(sm.dst + off) = d;
+        for (int i = 0; i < 4; ++i) tokp[i] = sm.tok[st][4 * h + i];
+        const int tokd = sm.tok[st][r >> 4];     // token of this thread's dQ column
+        const float* lse2 = sm.lse2[st] + 64 * h;
+        const float* dlt = sm.delta[st] + 64 * h;
+
+        // ---- P^T = exp2(S^T * scale log2e - lse log2e), causally masked
+        if (!(ok = mbar_wait(&sm.s_full, cm & 1, status))) break;
+        __syncwarp();
+        tc_fence_after();
+        float p[64];
+        {
+          uint32_t sv[64];
+          tmem_ld32(tmem + kColS + trow + 64 * h, sv);
+          tmem_ld32(tmem + kColS + trow + 64 * h + 32, sv + 32);
+          tmem_ld_wait();
+#pragma unroll
+          for (int j4 = 0; j4 < 16; ++j4) {
+            const float4 l4 = reinterpret_cast<const float4*>(lse2)[j4];
+            const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+            const bool valid = kp <= tokp[j4 >> 2];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int j = 4 * j4 + e;
+              p[j] = valid ? ex2(fmaf(__uint_as_float(sv[j]), sl2, -lv[e])) : 0.f;
+            }
+          }
+          uint32_t pk[32];
+#pragma unroll
+          for (int j = 0; j < 32; ++j) pk[j] = pack_bf16x2(p[2 * j], p[2 * j + 1]);
+          tmem_st16(tmem + kColS + trow + 64 * h, pk);
+          tmem_st16(tmem + kColS + trow + 64 * h + 16, pk + 16);
+          tmem_st_wait();
         }
-      }
-      fence_proxy_async_smem();
-      tc_fence_before();
-      mbar_arrive(&sm.ds_full);
-      // drain dQ^T (lane = head-dim channel r, column = (token, head))
-      if (!mbar_wait(&sm.mm_done, c & 1, status)) { ok = false; break; }
-      __syncwarp();
-      tc_fence_after();
-#pragma unroll 1
-      for (int cc = 0; cc < 4; ++cc) {
-        uint32_t qv[32];
-        tmem_ld32(t_s + trow + cc * 32, qv);
-        tmem_ld_wait();
+        tc_fence_before();
+        mbar_arrive(&sm.p_full);
+
+        // ---- dS^T = P^T (dP^T - Delta) -> shared memory (K-major rows = keys)
+        if (!(ok = mbar_wait(&sm.dp_full, cm & 1, status))) break;
+        __syncwarp();
+        tc_fence_after();
+        {
+          uint32_t dv[64];
+          tmem_ld32(tmem + kColDP + trow + 64 * h, dv);
+          tmem_ld32(tmem + kColDP + trow + 64 * h + 32, dv + 32);
+          tmem_ld_wait();
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const int col = cc * 32 + j;
-          const int ti = col / G;
-          if (ti < ntok) {
-            const size_t rowq = static_cast<size_t>(seq0 + tokp[ti]) * Hq + g * G + (col % G);
-            atomicAdd(dq_acc + rowq * kD + r, __uint_as_float(qv[j]));
+          for (int c = 0; c < 8; ++c) {
+            const float4 d0 = reinterpret_cast<const float4*>(dlt)[2 * c];
+            const float4 d1 = reinterpret_cast<const float4*>(dlt)[2 * c + 1];
+            const float dd[8] = {d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, d1.z, d1.w};
+            float x[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+              x[e] = p[8 * c + e] * (__uint_as_float(dv[8 * c + e]) - dd[e]);
+            uint4 pk;
+            pk.x = pack_bf16x2(x[0], x[1]);
+            pk.y = pack_bf16x2(x[2], x[3]);
+            pk.z = pack_bf16x2(x[4], x[5]);
+            pk.w = pack_bf16x2(x[6], x[7]);
+            *reinterpret_cast<uint4*>(sm.dst + h * kHalf + sw128_offset(r, c)) = pk;
           }
         }
-      }
-      tc_fence_before();
-      mbar_arrive(&sm.dq_free);
-      ++nchunks;
-    }
-    // dK, dV of this item -> fp32 accumulators
-    if (ok && nchunks > 0) {
-      __syncwarp();
-      const bool key_valid = kp < len;
-      const size_t krow = (static_cast<size_t>(seq0 + kp) * Hkv + g) * kD;
-#pragma unroll 1
-      for (int cc = 0; cc < 4; ++cc) {
-        uint32_t a[32], d[32];
-        tmem_ld32(t_dk + trow + cc * 32, a);
-        tmem_ld32(t_dv + trow + cc * 32, d);
-        tmem_ld_wait();
-        if (key_valid) {
+        fence_proxy_async_smem();
+        tc_fence_before();
+        mbar_arrive(&sm.ds_full);
+        mbar_arrive(&sm.ld_empty[st]);     // done with this stage's metadata
+
+        // ---- dQ rows (lane = chunk column) -> fp32 accumulator
+        if (!(ok = mbar_wait(&sm.dq_full, cm & 1, status))) break;
+        __syncwarp();
+        tc_fence_after();
+        {
+          uint32_t qv[64];
+          tmem_ld32(tmem + kColDP + trow + 64 * h, qv);
+          tmem_ld32(tmem + kColDP + trow + 64 * h + 32, qv + 32);
+          tmem_ld_wait();
+          if (tokd >= 0) {
+            float4* dst = reinterpret_cast<float4*>(
+                dq_acc + (static_cast<size_t>(seq0 + tokd) * Hq + g * G + (r & 15)) * kD + 64 * h);
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            atomicAdd(reinterpret_cast<float4*>(dk_acc + krow + cc * 32) + j,
-                      make_float4(__uint_as_float(a[4 * j]), __uint_as_float(a[4 * j + 1]),
-                                  __uint_as_float(a[4 * j + 2]), __uint_as_float(a[4 * j + 3])));
-            atomicAdd(reinterpret_cast<float4*>(dv_acc + krow + cc * 32) + j,
-                      make_float4(__uint_as_float(d[4 * j]), __uint_as_float(d[4 * j + 1]),
-                                  __uint_as_float(d[4 * j + 2]), __uint_as_float(d[4 * j + 3])));
+            for (int j = 0; j < 16; ++j)
+              atomicAdd(dst + j, make_float4(__uint_as_float(qv[4 * j]),
+                                             __uint_as_float(qv[4 * j + 1]),
+                                             __uint_as_float(qv[4 * j + 2]),
+                                             __uint_as_float(qv[4 * j + 3])));
           }
         }
+        tc_fence_before();
+        mbar_arrive(&sm.dq_free);
+        ++cm;
+        ++nch;
+      }
+      // ---- dK, dV of this item (all its MMAs completed before the last dq_full)
+      if (ok && nch > 0) {
+        __syncwarp();
+        const bool key_valid = kp < len;
+        const size_t krow = (static_cast<size_t>(seq0 + kp) * Hkv + g) * kD + 64 * h;
+#pragma unroll
+        for (int which = 0; which < 2; ++which) {
+          uint32_t a[64];
+          const uint32_t col = (which == 0 ? kColDK : kColDV) + 64 * h;
+          tmem_ld32(tmem + col + trow, a);
+          tmem_ld32(tmem + col + trow + 32, a + 32);
+          tmem_ld_wait();
+          if (key_valid) {
+            float4* dst = reinterpret_cast<float4*>((which == 0 ? dk_acc : dv_acc) + krow);
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+              atomicAdd(dst + j, make_float4(__uint_as_float(a[4 * j]), __uint_as_float(a[4 * j + 1]),
+                                             __uint_as_float(a[4 * j + 2]),
+                                             __uint_as_float(a[4 * j + 3])));
+          }
+        }
+        tc_fence_before();
       }
     }
   }
@@ -448,12 +554,26 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
 // ---------------------------------------------------------------- host
 
+static int bwd_windows(int max_seqlen) { return (max_seqlen + kBwdSegment - 1) / kBwdSegment; }
+
 static int bwd_max_items(int T, int S, int max_seqlen) {
+  // items of sequence s <= (windows of s) x (blocks of s) <= (T / W + S) x max_nb
   const long long max_nb = (max_seqlen + kBlock - 1) / kBlock;
-  const long long tiles = plan_max_tiles(T, S);
-  const long long extra = (static_cast<long long>(T) * (max_nb + 1) + 2 * kBwdSegment - 1) /
-                          (2 * kBwdSegment);
-  return static_cast<int>(2 * tiles + extra + 1);
+  const long long n = (static_cast<long long>(T) / kBwdSegment + S) * max_nb;
+  return static_cast<int>(n < (1LL << 30) ? n : (1LL << 30));
+}
+
+static int sm_count() {
+  static int cached[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) return 148;
+  if (!cached[dev]) {
+    int n = 0;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    cached[dev] = n > 0 ? n : 148;
+  }
+  return cached[dev];
 }
 
 BwdWorkspace carve_bwd_workspace(WsCursor& ws, int T, int S, int Hq, int Hkv, int max_seqlen) {
@@ -474,11 +594,9 @@ msa_status_t launch_sparse_bwd(const void* q, const void* k, const void* v, cons
                                const int32_t* cu, int S, int T, int Hq, int Hkv, int max_seqlen,
                                float scale, const BwdWorkspace& ws, void* dq, void* dk, void* dv,
                                cudaStream_t stream) {
-  (void)S;
-  (void)max_seqlen;
   const int G = Hq / Hkv;
-  if (G != 16 && G != 8)
-    return fail(MSA_ERR_UNSUPPORTED, "backward supports Hq/Hkv of 8 or 16 (got %d)", G);
+  if (G != 16)
+    return fail(MSA_ERR_UNSUPPORTED, "backward supports Hq/Hkv = 16 (got %d)", G);
   CUtensorMap tq, tk, tv, tdo;
   const uint64_t dq3[3] = {static_cast<uint64_t>(kD), static_cast<uint64_t>(Hq),
                            static_cast<uint64_t>(T)};
@@ -502,30 +620,31 @@ msa_status_t launch_sparse_bwd(const void* q, const void* k, const void* v, cons
   {
     TraceScope trace_("bwd_delta_kernel", stream);
     bwd_delta_kernel<<<static_cast<unsigned>((rows * 32 + 255) / 256), 256, 0, stream>>>(
-      static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dout), ws.delta,
-      rows);
+        static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dout), ws.delta,
+        rows);
   }
   {
     TraceScope trace_("bwd_items_kernel", stream);
-    bwd_items_kernel<<<1, 1024, 0, stream>>>(cu, ws.plan.tiles, ws.plan.num_tiles, ws.items,
-                                           ws.num_items, ws.max_items, st);
+    bwd_items_kernel<<<1, 1024, 0, stream>>>(cu, S, bwd_windows(max_seqlen), ws.items,
+                                             ws.num_items, ws.max_items, st);
   }
   msa_status_t e = check_launch("bwd_delta/items");
   if (e != MSA_OK) return e;
 
-  const size_t smem = sizeof(BwdSmem) + 1024;
+  const size_t smem = sizeof(BwdSmem);
   static bool attr_set = false;
   if (!attr_set) {
     cudaFuncSetAttribute(sparse_bwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          static_cast<int>(smem));
     attr_set = true;
   }
-  dim3 grid(ws.max_items, Hkv);
+  const int per_head = (sm_count() + Hkv - 1) / Hkv;
+  dim3 grid(static_cast<unsigned>(per_head < ws.max_items ? per_head : ws.max_items), Hkv);
   {
     TraceScope trace_("sparse_bwd_kernel", stream);
     sparse_bwd_kernel<<<grid, kBwdThreads, smem, stream>>>(
-      tq, tk, tv, tdo, sel, cu, lse, ws.delta, ws.items, ws.num_items, Hq, Hkv, G, scale,
-      ws.dq_acc, ws.dk_acc, ws.dv_acc, st);
+        tq, tk, tv, tdo, sel, cu, lse, ws.delta, ws.items, ws.num_items, Hq, Hkv, scale,
+        ws.dq_acc, ws.dk_acc, ws.dv_acc, st);
   }
   e = check_launch("sparse_bwd_kernel");
   if (e != MSA_OK) return e;
@@ -533,17 +652,17 @@ msa_status_t launch_sparse_bwd(const void* q, const void* k, const void* v, cons
   {
     TraceScope trace_("bwd_convert_kernel", stream);
     bwd_convert_kernel<<<static_cast<unsigned>((nq / 8 + 255) / 256), 256, 0, stream>>>(
-      ws.dq_acc, static_cast<__nv_bfloat16*>(dq), nq / 8, scale);
+        ws.dq_acc, static_cast<__nv_bfloat16*>(dq), nq / 8, scale);
   }
   {
     TraceScope trace_("bwd_convert_kernel", stream);
     bwd_convert_kernel<<<static_cast<unsigned>((nkv / 8 + 255) / 256), 256, 0, stream>>>(
-      ws.dk_acc, static_cast<__nv_bfloat16*>(dk), nkv / 8, scale);
+        ws.dk_acc, static_cast<__nv_bfloat16*>(dk), nkv / 8, scale);
   }
   {
     TraceScope trace_("bwd_convert_kernel", stream);
     bwd_convert_kernel<<<static_cast<unsigned>((nkv / 8 + 255) / 256), 256, 0, stream>>>(
-      ws.dv_acc, static_cast<__nv_bfloat16*>(dv), nkv / 8, 1.0f);
+        ws.dv_acc, static_cast<__nv_bfloat16*>(dv), nkv / 8, 1.0f);
   }
   return check_launch("bwd_convert_kernel");
 }
