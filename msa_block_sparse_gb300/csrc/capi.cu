@@ -41,7 +41,9 @@ msa_status_t check_launch(const char* what) {
 
 // ------------------------------------------------------------------ status word
 
-__device__ uint32_t g_device_status;
+// [0] status bits, [1] first expired wait (0x80000000 | site id), [2] its block
+// (x + y << 20), [3] its thread
+__device__ uint32_t g_device_status[4];
 
 uint32_t* status_word() {
   static uint32_t* ptrs[64] = {nullptr};
@@ -282,12 +284,15 @@ msa_status_t msa_check_status(msa_stream_t stream) {
   if (e != cudaSuccess) return fail(MSA_ERR_CUDA, "stream sync: %s", cudaGetErrorString(e));
   uint32_t* sw = status_word();
   if (!sw) return fail(MSA_ERR_CUDA, "status word unavailable");
-  uint32_t v = 0;
-  e = cudaMemcpy(&v, sw, sizeof(v), cudaMemcpyDeviceToHost);
+  uint32_t v[4] = {0, 0, 0, 0};
+  e = cudaMemcpy(v, sw, sizeof(v), cudaMemcpyDeviceToHost);
   if (e == cudaSuccess) e = cudaMemset(sw, 0, sizeof(v));
   if (e != cudaSuccess) return fail(MSA_ERR_CUDA, "status read: %s", cudaGetErrorString(e));
-  if (v & kStatusTimeout) return fail(MSA_ERR_TIMEOUT, "a kernel wait ran out (status %u)", v);
-  if (v & kStatusBounds) return fail(MSA_ERR_BOUNDS, "an index was out of range (status %u)", v);
+  if (v[0] & kStatusTimeout)
+    return fail(MSA_ERR_TIMEOUT,
+                "a kernel wait ran out (status %u; first: wait site %u, block (%u, %u), thread %u)",
+                v[0], v[1] & 0x7fffffffu, v[2] & 0xfffffu, v[2] >> 20, v[3]);
+  if (v[0] & kStatusBounds) return fail(MSA_ERR_BOUNDS, "an index was out of range (status %u)", v[0]);
   return MSA_OK;
 }
 

@@ -76,9 +76,11 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Bounded wait on phase `parity`.  Returns false (and flags the status word)
-// when the limit runs out; callers then skip the remaining work.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t* status) {
+// Bounded wait on phase `parity`.  Returns false when the limit runs out and
+// flags the status word; the first wait to run out also records its site id,
+// block and thread in words 1..3.  Callers then skip the remaining work.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t* status,
+                                          uint32_t site = 0) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
   while (true) {
@@ -86,7 +88,13 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32
     for (int i = 0; i < 32; ++i)
       if (mbar_try_wait(bar, parity)) return true;
     if (globaltimer() - t0 > kWaitLimitNs) {
-      if (status) atomicOr(status, kStatusTimeout);
+      if (status) {
+        atomicOr(status, kStatusTimeout);
+        if (atomicCAS(status + 1, 0u, 0x80000000u | site) == 0u) {
+          status[2] = blockIdx.x + (blockIdx.y << 20);
+          status[3] = threadIdx.x;
+        }
+      }
       return false;
     }
   }

@@ -2,25 +2,34 @@
 // Introduction": each query attends to its 16 selected 128-token blocks, own
 // block included, causally; "#4581", "Kernel tuning": QSA block-sparse kernel).
 //
-// Tile = 128 rows = (128/G consecutive tokens) x (the G query heads of one KV
-// head), so a single K/V block feeds all rows.  The tile's tokens lie in one
-// 128-token block, hence share their own block.  The CTA walks the union of the
-// tokens' selected blocks in ascending order; a row whose token did not select
-// the current block gets P = 0 for it.  Per union block b:
-//   TMA     : K_b and V_b (128 x 128 bf16 each, 128B swizzle), 2-stage ring
-//   MMA     : S = Q K_b^T -> TMEM (two buffers, so S_{i+1} overlaps softmax_i)
-//   softmax : thread = row = TMEM lane; running max in the log2 domain, only
-//             rescaled when it grows by more than 2^8 (P stays < 256 in bf16);
-//             P (bf16) written to shared memory in the MMA's K-major layout
-//   MMA     : O += P V_b (V as an MN-major operand) -> TMEM
-// The epilogue divides by the row sum and writes o (bf16) and lse (natural log).
+// Tile = 128 rows = 8 consecutive tokens x the 16 query heads of one KV head, so
+// a single K/V block feeds every row.  The tile's tokens lie in one 128-token
+// block and share their own block.  The tile walks the union of its tokens'
+// selected blocks in ascending order; a row whose token did not select the
+// current block gets P = 0 for it.
+//
+// Persistent CTAs (one per SM) stride over the tiles:
+//   producer (warp 0): builds the next tile's block union (bitmaps in shared
+//            memory, double-buffered) and loads its Q tile, then streams K_b and
+//            V_b through separate 2-stage TMA rings (K runs one block ahead)
+//   MMA (warp 1): S_i = Q K_b^T into one of two TMEM buffers; then
+//            O_h += P_h V_b[64h, 64h+64) for the two 64-key halves h, with P_h
+//            read from TMEM as the A operand
+//   softmax (warps 2..9): warp = 32 rows x one 64-key half h.  Each half keeps
+//            its own running max (log2 domain, rescaled only when it grows by
+//            more than 2^8, so P < 256 fits bf16), row sum and O_h accumulator;
+//            P_h is packed to bf16 into the S buffer it came from.  The epilogue
+//            merges the halves: o = (O_0 2^(m_0-m) + O_1 2^(m_1-m)) / l.
 #include "kernels.cuh"
 
 namespace msa {
 
 namespace {
 
-constexpr int kFwdThreads = 192;            // warp 0 TMA, warp 1 MMA, warps 2..5 softmax
+constexpr int kFwdThreads = 320;            // warp 0 producer, warp 1 MMA, warps 2..9 softmax
+constexpr int kSoftmaxThreads = 256;
+constexpr int kG = 16;                      // query heads per KV head
+constexpr int kTpt = 8;                     // tokens per tile
 constexpr int kTile = 128 * 128 * 2;        // bytes of a 128 x 128 bf16 tile
 constexpr int kHalf = kTile / 2;            // one 64-column half
 constexpr int kMaskWords = kMaxSeqlen / kBlock / 32;
@@ -28,24 +37,56 @@ constexpr uint32_t kIdescS = idesc_bf16(128, 128, false, false);
 constexpr uint32_t kIdescPV = idesc_bf16(128, 128, false, true);
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleThreshold = 8.0f;   // log2 of the largest P before a rescale
+constexpr uint32_t kColO = 256;             // O_0 at 256, O_1 at 384; S buffers at 0, 128
 
 struct FwdSmem {
-  uint8_t q[kTile];
+  uint8_t q[2][kTile];
   uint8_t k[2][kTile];
   uint8_t v[2][kTile];
-  uint8_t p[kTile];
-  uint32_t tok_mask[128][kMaskWords];       // [token of tile][block bitmap], sized for G = 1
-  int ublk[kMaxSeqlen / kBlock];
-  int n_union;
-  uint64_t q_full;
-  uint64_t kv_full[2];
-  uint64_t kv_empty[2];
-  uint64_t s_full[2];
-  uint64_t s_empty[2];
-  uint64_t p_full;
-  uint64_t pv_done;
+  uint32_t tok_mask[2][kTpt][kMaskWords];
+  int ublk[2][kTpt * kTopK];
+  int n_union[2];
+  float2 ml[2][128];                        // per half: (max, sum) of each row, for the merge
+  uint64_t tile_full[2], tile_empty[2];
+  uint64_t k_full[2], k_empty[2], v_full[2], v_empty[2];
+  // per S buffer: a waiter is then never more than one phase behind
+  uint64_t s_full[2], p_full[2], pv_done[2], ml_full;
   uint32_t tmem_base;
 };
+static_assert(sizeof(FwdSmem) <= 232448, "forward shared memory above the 227 KB limit");
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ void umma_bf16_tmem_a(uint32_t d_tmem, uint32_t a_tmem,
+                                                 uint64_t b_desc, uint32_t idesc,
+                                                 uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+struct TileInfo {
+  int s, qb, seq0, len, p0, ntok;
+};
+
+// Global tile ti -> plan tile ti / 16 (a 128-token block), sub-tile ti % 16.
+__device__ __forceinline__ bool tile_info(int ti, const int2* tiles, const int32_t* cu,
+                                          TileInfo& t) {
+  const int2 pt = tiles[ti >> 4];
+  t.s = pt.x;
+  t.qb = pt.y;
+  t.seq0 = cu[t.s];
+  t.len = cu[t.s + 1] - t.seq0;
+  t.p0 = t.qb * kBlock + (ti & 15) * kTpt;
+  t.ntok = min(kTpt, t.len - t.p0);
+  return t.p0 < t.len;
+}
 
 }  // namespace
 
@@ -54,263 +95,320 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                       const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v, const int32_t* __restrict__ sel,
                       const int32_t* __restrict__ cu, const int2* __restrict__ tiles,
-                      const int* __restrict__ num_tiles, int Hq, int Hkv, int G, float scale,
+                      const int* __restrict__ num_tiles, int Hq, int Hkv, float scale,
                       __nv_bfloat16* __restrict__ o, float* __restrict__ lse, uint32_t* status) {
-  const int tpt = 128 / G;                       // tokens per tile
-  const int tile_idx = blockIdx.x / G;
-  const int sub = blockIdx.x % G;
-  if (tile_idx >= *num_tiles) return;
-  const int2 tile = tiles[tile_idx];
-  const int s = tile.x, qb = tile.y, g = blockIdx.y;
-  const int seq0 = cu[s];
-  const int len = cu[s + 1] - seq0;
-  const int p0 = qb * kBlock + sub * tpt;        // first query position of the tile
-  if (p0 >= len) return;
-  const int ntok = min(tpt, len - p0);
-  const int nb_seq = (len + kBlock - 1) / kBlock;
-
-  extern __shared__ uint8_t smem_raw[];
-  FwdSmem& sm = *reinterpret_cast<FwdSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                            ~static_cast<uintptr_t>(1023));
+  const int total = *num_tiles * kG;
+  if (static_cast<int>(blockIdx.x) >= total) return;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  if (smem_u32(smem_raw) & 1023u) {   // the tiles need 1024-byte alignment
+    if (threadIdx.x == 0) atomicOr(status, kStatusBounds);
+    return;
+  }
+  FwdSmem& sm = *reinterpret_cast<FwdSmem*>(smem_raw);
+  const int g = blockIdx.y;
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
-  const int words = min((nb_seq + 31) >> 5, kMaskWords);
 
-  // ---- union of the tile's selected blocks
-  for (int i = tid; i < tpt * kMaskWords; i += kFwdThreads) sm.tok_mask[i / kMaskWords][i % kMaskWords] = 0;
   if (tid == 0) {
-    mbar_init(&sm.q_full, 1);
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&sm.kv_full[i], 1);
-      mbar_init(&sm.kv_empty[i], 1);
+      mbar_init(&sm.tile_full[i], 1);
+      mbar_init(&sm.tile_empty[i], 1 + kSoftmaxThreads);
+      mbar_init(&sm.k_full[i], 1);
+      mbar_init(&sm.k_empty[i], 1);
+      mbar_init(&sm.v_full[i], 1);
+      mbar_init(&sm.v_empty[i], 1);
       mbar_init(&sm.s_full[i], 1);
-      mbar_init(&sm.s_empty[i], 128);
+      mbar_init(&sm.p_full[i], kSoftmaxThreads);
+      mbar_init(&sm.pv_done[i], 1);
     }
-    mbar_init(&sm.p_full, 128);
-    mbar_init(&sm.pv_done, 1);
+    mbar_init(&sm.ml_full, kSoftmaxThreads);
     fence_mbar_init();
   }
   if (warp == 1) {
     tmem_alloc(&sm.tmem_base, 512);
     tmem_relinquish();
   }
-  __syncthreads();
-  for (int i = tid; i < ntok * kTopK; i += kFwdThreads) {
-    const int tl = i / kTopK;
-    const int b = __ldg(sel + (static_cast<size_t>(seq0 + p0 + tl) * Hkv + g) * kTopK + (i % kTopK));
-    if (b < 0) continue;
-    if (b > qb) {
-      atomicOr(status, kStatusBounds);
-      continue;
-    }
-    atomicOr(&sm.tok_mask[tl][b >> 5], 1u << (b & 31));
-  }
-  __syncthreads();
-  if (warp == 0) {
-    int base = 0;
-    for (int w0 = 0; w0 < words; w0 += 32) {
-      const int w = w0 + lane;
-      uint32_t u = 0;
-      if (w < words)
-        for (int tl = 0; tl < ntok; ++tl) u |= sm.tok_mask[tl][w];
-      const int c = __popc(u);
-      int incl = c;
-#pragma unroll
-      for (int d = 1; d < 32; d <<= 1) {
-        const int n = __shfl_up_sync(0xffffffffu, incl, d);
-        if (lane >= d) incl += n;
-      }
-      int off = base + incl - c;
-      while (u) {
-        const int bit = __ffs(u) - 1;
-        sm.ublk[off++] = w * 32 + bit;
-        u &= u - 1;
-      }
-      base += __shfl_sync(0xffffffffu, incl, 31);
-    }
-    if (lane == 0) sm.n_union = base;
-  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const int nU = sm.n_union;
   const uint32_t tmem = sm.tmem_base;
-  const uint32_t tmem_o = tmem + 256;
 
   if (warp == 0) {
-    // ---------------------------------------------------------------- TMA producer
-    if (elect_one()) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
       prefetch_tmap(&tm_q);
       prefetch_tmap(&tm_k);
       prefetch_tmap(&tm_v);
-      mbar_arrive_expect_tx(&sm.q_full, kTile);
-      tma_load_3d(sm.q, &tm_q, &sm.q_full, 0, g * G, seq0 + p0);
-      tma_load_3d(sm.q + kHalf, &tm_q, &sm.q_full, 64, g * G, seq0 + p0);
-      for (int i = 0; i < nU; ++i) {
-        const int st = i & 1;
-        if (!mbar_wait(&sm.kv_empty[st], ((i >> 1) & 1) ^ 1, status)) break;
-        const int row = seq0 + sm.ublk[i] * kBlock;
-        mbar_arrive_expect_tx(&sm.kv_full[st], 2 * kTile);
-        tma_load_3d(sm.k[st], &tm_k, &sm.kv_full[st], 0, g, row);
-        tma_load_3d(sm.k[st] + kHalf, &tm_k, &sm.kv_full[st], 64, g, row);
-        tma_load_3d(sm.v[st], &tm_v, &sm.kv_full[st], 0, g, row);
-        tma_load_3d(sm.v[st] + kHalf, &tm_v, &sm.kv_full[st], 64, g, row);
+    }
+    uint32_t tcount = 0, kc = 0, vc = 0;
+    bool alive = true;
+    for (int ti = blockIdx.x; alive && ti < total; ti += gridDim.x) {
+      TileInfo t;
+      if (!tile_info(ti, tiles, cu, t)) continue;
+      const int tb = tcount & 1;
+      if (lane == 0) alive = mbar_wait(&sm.tile_empty[tb], ((tcount >> 1) & 1) ^ 1, status, 1);
+      alive = __shfl_sync(0xffffffffu, alive ? 1 : 0, 0) != 0;
+      if (!alive) break;
+      // ---- union of the tile tokens' selected blocks
+      const int nb_seq = (t.len + kBlock - 1) / kBlock;
+      const int words = min((nb_seq + 31) >> 5, kMaskWords);
+      for (int w = lane; w < kTpt * kMaskWords; w += 32) sm.tok_mask[tb][w / kMaskWords][w % kMaskWords] = 0;
+      __syncwarp();
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int idx = lane * 4 + e;          // (token, slot) of the 8 x 16 ids
+        const int tl = idx >> 4;
+        if (tl < t.ntok) {
+          const int b = __ldg(sel + (static_cast<size_t>(t.seq0 + t.p0 + tl) * Hkv + g) * kTopK +
+                              (idx & 15));
+          if (b >= 0 && b <= t.qb) atomicOr(&sm.tok_mask[tb][tl][b >> 5], 1u << (b & 31));
+          else if (b > t.qb) atomicOr(status, kStatusBounds);
+        }
       }
+      __syncwarp();
+      int base = 0;
+      for (int w0 = 0; w0 < words; w0 += 32) {
+        const int w = w0 + lane;
+        uint32_t u = 0;
+        if (w < words)
+          for (int tl = 0; tl < t.ntok; ++tl) u |= sm.tok_mask[tb][tl][w];
+        const int c = __popc(u);
+        int incl = c;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+          const int x = __shfl_up_sync(0xffffffffu, incl, d);
+          if (lane >= d) incl += x;
+        }
+        int off = base + incl - c;
+        while (u) {
+          const int bit = __ffs(u) - 1;
+          if (off < kTpt * kTopK) sm.ublk[tb][off] = w * 32 + bit;
+          ++off;
+          u &= u - 1;
+        }
+        base += __shfl_sync(0xffffffffu, incl, 31);
+      }
+      const int nU = min(base, kTpt * kTopK);
+      if (lane == 0) sm.n_union[tb] = nU;
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&sm.tile_full[tb], kTile);
+        tma_load_3d(sm.q[tb], &tm_q, &sm.tile_full[tb], 0, g * kG, t.seq0 + t.p0);
+        tma_load_3d(sm.q[tb] + kHalf, &tm_q, &sm.tile_full[tb], 64, g * kG, t.seq0 + t.p0);
+        // ---- K runs one block ahead of V
+        for (int i = 0; alive && i <= nU; ++i) {
+          if (i < nU) {
+            const int st = kc & 1;
+            if (!(alive = mbar_wait(&sm.k_empty[st], ((kc >> 1) & 1) ^ 1, status, 2))) break;
+            const int row = t.seq0 + sm.ublk[tb][i] * kBlock;
+            mbar_arrive_expect_tx(&sm.k_full[st], kTile);
+            tma_load_3d(sm.k[st], &tm_k, &sm.k_full[st], 0, g, row);
+            tma_load_3d(sm.k[st] + kHalf, &tm_k, &sm.k_full[st], 64, g, row);
+            ++kc;
+          }
+          if (i > 0) {
+            const int st = vc & 1;
+            if (!(alive = mbar_wait(&sm.v_empty[st], ((vc >> 1) & 1) ^ 1, status, 3))) break;
+            const int row = t.seq0 + sm.ublk[tb][i - 1] * kBlock;
+            mbar_arrive_expect_tx(&sm.v_full[st], kTile);
+            tma_load_3d(sm.v[st], &tm_v, &sm.v_full[st], 0, g, row);
+            tma_load_3d(sm.v[st] + kHalf, &tm_v, &sm.v_full[st], 64, g, row);
+            ++vc;
+          }
+        }
+      }
+      alive = __shfl_sync(0xffffffffu, alive ? 1 : 0, 0) != 0;
+      ++tcount;
     }
   } else if (warp == 1) {
-    // ---------------------------------------------------------------- MMA issuer
+    // ------------------------------------------------------------ MMA issuer
     if (elect_one()) {
-      bool ok = mbar_wait(&sm.q_full, 0, status);
-      const uint32_t qa = smem_u32(sm.q);
-      const uint32_t pa = smem_u32(sm.p);
-      for (int i = 0; ok && i <= nU; ++i) {
-        if (i < nU) {
-          const int st = i & 1, buf = i & 1;
-          ok = mbar_wait(&sm.kv_full[st], (i >> 1) & 1, status) &&
-               mbar_wait(&sm.s_empty[buf], ((i >> 1) & 1) ^ 1, status);
-          if (!ok) break;
-          tc_fence_after();
-          const uint32_t ka = smem_u32(sm.k[st]);
+      uint32_t tcount = 0, kc = 0, vc = 0, bc = 0;
+      bool ok = true;
+      for (int ti = blockIdx.x; ok && ti < total; ti += gridDim.x) {
+        TileInfo t;
+        if (!tile_info(ti, tiles, cu, t)) continue;
+        const int tb = tcount & 1;
+        if (!(ok = mbar_wait(&sm.tile_full[tb], (tcount >> 1) & 1, status, 4))) break;
+        tc_fence_after();
+        const int nU = sm.n_union[tb];
+        const uint32_t qa = smem_u32(sm.q[tb]);
+        const uint32_t bc0 = bc;
+        for (int i = 0; ok && i <= nU; ++i) {
+          if (i < nU) {
+            const int st = kc & 1;
+            if (!(ok = mbar_wait(&sm.k_full[st], (kc >> 1) & 1, status, 5))) break;
+            // the S buffer of block bc held P of block bc - 2: wait for its PV
+            if (bc >= 2 && !(ok = mbar_wait(&sm.pv_done[bc & 1], ((bc - 2) >> 1) & 1, status, 6)))
+              break;
+            tc_fence_after();
+            const uint32_t ka = smem_u32(sm.k[st]);
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
-            const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
-            umma_bf16(tmem + buf * 128, sdesc_sw128(qa + off, 16, 1024),
-                      sdesc_sw128(ka + off, 16, 1024), kIdescS, kk > 0);
+            for (int kk = 0; kk < 8; ++kk) {
+              const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
+              umma_bf16(tmem + (bc & 1) * 128, sdesc_sw128(qa + off, 16, 1024),
+                        sdesc_sw128(ka + off, 16, 1024), kIdescS, kk > 0);
+            }
+            umma_commit(&sm.s_full[bc & 1]);
+            umma_commit(&sm.k_empty[st]);
+            ++kc;
+            ++bc;
           }
-          umma_commit(&sm.s_full[buf]);
-        }
-        if (i > 0) {
-          const int j = i - 1, stj = j & 1;
-          ok = mbar_wait(&sm.p_full, j & 1, status);
-          if (!ok) break;
-          tc_fence_after();
-          const uint32_t va = smem_u32(sm.v[stj]);
+          if (i > 0) {
+            const uint32_t j = bc0 + i - 1;
+            const int st = vc & 1;
+            if (!(ok = mbar_wait(&sm.p_full[j & 1], (j >> 1) & 1, status, 7))) break;
+            if (!(ok = mbar_wait(&sm.v_full[st], (vc >> 1) & 1, status, 8))) break;
+            tc_fence_after();
+            const uint32_t va = smem_u32(sm.v[st]);
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
-            const uint32_t aoff = (kk >> 2) * kHalf + (kk & 3) * 32;
-            umma_bf16(tmem_o, sdesc_sw128(pa + aoff, 16, 1024),
-                      sdesc_sw128(va + kk * 2048, kHalf, 1024), kIdescPV, (j > 0 || kk > 0));
+            for (int kk = 0; kk < 8; ++kk) {
+              const int hh = kk >> 2;
+              const uint32_t a_t = tmem + (j & 1) * 128 + hh * 64 + (kk & 3) * 8;
+              umma_bf16_tmem_a(tmem + kColO + hh * 128, a_t,
+                               sdesc_sw128(va + kk * 2048, kHalf, 1024), kIdescPV,
+                               (i > 1 || (kk & 3) > 0));
+            }
+            umma_commit(&sm.pv_done[j & 1]);
+            umma_commit(&sm.v_empty[st]);
+            ++vc;
           }
-          umma_commit(&sm.pv_done);
-          umma_commit(&sm.kv_empty[stj]);
         }
+        umma_commit(&sm.tile_empty[tb]);   // Q of this tile is free once its S MMAs are done
+        ++tcount;
       }
     }
   } else {
-    // ---------------------------------------------------------------- softmax
+    // ------------------------------------------------------------ softmax
+    const int cw = warp - 2;
     const int subp = warp & 3;
-    const int r = subp * 32 + lane;              // tile row = TMEM lane
-    const int tl = r / G, hd = r % G;
-    const bool row_valid = tl < ntok;
-    const int pos = p0 + tl;
-    const float sl2 = scale * kLog2e;
+    const int h = cw >> 2;                   // key half [64h, 64h + 64) of every block
+    const int r = subp * 32 + lane;          // tile row = TMEM lane
+    const int tl = r >> 4, hd = r & 15;      // token of the tile, head of the group
     const uint32_t trow = static_cast<uint32_t>(subp * 32) << 16;
-    float m = -INFINITY, l = 0.f;
+    const float sl2 = scale * kLog2e;
+    uint32_t tcount = 0, bc = 0;
     bool ok = true;
-    for (int i = 0; i < nU; ++i) {
-      const int buf = i & 1;
-      const int b = sm.ublk[i];
-      if (!mbar_wait(&sm.s_full[buf], (i >> 1) & 1, status)) { ok = false; break; }
-      __syncwarp();
-      tc_fence_after();
-      float sv[128];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t v[32];
-        tmem_ld32(tmem + trow + buf * 128 + c * 32, v);
-        tmem_ld_wait();
-#pragma unroll
-        for (int j = 0; j < 32; ++j) sv[c * 32 + j] = __uint_as_float(v[j]);
-      }
-      tc_fence_before();
-      mbar_arrive(&sm.s_empty[buf]);
-
-      const bool selected = row_valid && ((sm.tok_mask[tl][b >> 5] >> (b & 31)) & 1u);
-      const int kmax = (b == qb) ? (pos & (kBlock - 1)) : (kBlock - 1);
-      bool rescale = false;
-      float m_use = m, rowsum = 0.f;
-      if (selected) {
-        float mx = -INFINITY;
-#pragma unroll
-        for (int j = 0; j < 128; ++j)
-          if (j <= kmax) mx = fmaxf(mx, sv[j]);
-        const float m_new = fmaxf(m, mx * sl2);
-        rescale = m_new > m + kRescaleThreshold;
-        m_use = rescale ? m_new : m;
-#pragma unroll
-        for (int j = 0; j < 128; ++j) {
-          const float pj = (j <= kmax) ? exp2f(fmaf(sv[j], sl2, -m_use)) : 0.f;
-          sv[j] = pj;
-          rowsum += pj;
-        }
-      } else {
-#pragma unroll
-        for (int j = 0; j < 128; ++j) sv[j] = 0.f;
-      }
-      // O and the P buffer are free once PV of the previous block is done.
-      if (i > 0) {
-        if (!mbar_wait(&sm.pv_done, (i - 1) & 1, status)) { ok = false; break; }
+    for (int ti = blockIdx.x; ok && ti < total; ti += gridDim.x) {
+      TileInfo t;
+      if (!tile_info(ti, tiles, cu, t)) continue;
+      const int tb = tcount & 1;
+      if (!(ok = mbar_wait(&sm.tile_full[tb], (tcount >> 1) & 1, status, 9))) break;
+      const int nU = sm.n_union[tb];
+      const bool row_valid = tl < t.ntok;
+      const int pos = t.p0 + tl;
+      float m = -INFINITY, l = 0.f;
+      for (int i = 0; i < nU; ++i) {
+        const int b = sm.ublk[tb][i];
+        const uint32_t sbuf = tmem + (bc & 1) * 128 + trow + 64 * h;
+        if (!(ok = mbar_wait(&sm.s_full[bc & 1], (bc >> 1) & 1, status, 10))) break;
         __syncwarp();
         tc_fence_after();
-        const bool mine = rescale && m != -INFINITY;
-        if (__any_sync(0xffffffffu, mine)) {
-          const float alpha = mine ? exp2f(m - m_use) : 1.f;
+        uint32_t sv[64];
+        tmem_ld32(sbuf, sv);
+        tmem_ld32(sbuf + 32, sv + 32);
+        tmem_ld_wait();
+        const bool selected =
+            row_valid && ((sm.tok_mask[tb][tl][b >> 5] >> (b & 31)) & 1u);
+        const int kmax = (b == t.qb) ? (pos & (kBlock - 1)) - 64 * h : 63;
+        bool resc = false;
+        float mu = m, rs = 0.f;
+        float p[64];
+        if (selected && kmax >= 0) {
+          float mx = -INFINITY;
+#pragma unroll
+          for (int j = 0; j < 64; ++j)
+            if (j <= kmax) mx = fmaxf(mx, __uint_as_float(sv[j]));
+          const float mnew = fmaxf(m, mx * sl2);
+          resc = mnew > m + kRescaleThreshold;
+          mu = resc ? mnew : m;
+#pragma unroll
+          for (int j = 0; j < 64; ++j) {
+            p[j] = (j <= kmax) ? ex2(fmaf(__uint_as_float(sv[j]), sl2, -mu)) : 0.f;
+            rs += p[j];
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < 64; ++j) p[j] = 0.f;
+        }
+        const bool need = resc && m != -INFINITY;
+        if (__any_sync(0xffffffffu, need)) {
+          // O_h is stable only once the PV of the previous block is done
+          if (!(ok = mbar_wait(&sm.pv_done[(bc - 1) & 1], ((bc - 1) >> 1) & 1, status, 11))) break;
+          __syncwarp();
+          tc_fence_after();
+          const float alpha = need ? ex2(m - mu) : 1.f;
+          const uint32_t orow = tmem + kColO + h * 128 + trow;
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
             uint32_t v[32];
-            tmem_ld32(tmem_o + trow + c * 32, v);
+            tmem_ld32(orow + c * 32, v);
             tmem_ld_wait();
 #pragma unroll
             for (int j = 0; j < 32; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) * alpha);
-            tmem_st16(tmem_o + trow + c * 32, v);
-            tmem_st16(tmem_o + trow + c * 32 + 16, v + 16);
+            tmem_st16(orow + c * 32, v);
+            tmem_st16(orow + c * 32 + 16, v + 16);
           }
-          tmem_st_wait();
         }
-      }
-      if (selected) {
-        l = (m == -INFINITY) ? rowsum : (rescale ? l * exp2f(m - m_use) : l) + rowsum;
-        m = m_use;
-      }
-      // P row -> shared memory (bf16, 128B-swizzled K-major, two 64-key halves)
+        if (selected && kmax >= 0) {
+          l = (m == -INFINITY) ? rs : (resc ? l * ex2(m - mu) : l) + rs;
+          m = mu;
+        }
+        uint32_t pk[32];
 #pragma unroll
-      for (int c = 0; c < 16; ++c) {
-        uint4 pk;
-        pk.x = pack_bf16x2(sv[8 * c + 0], sv[8 * c + 1]);
-        pk.y = pack_bf16x2(sv[8 * c + 2], sv[8 * c + 3]);
-        pk.z = pack_bf16x2(sv[8 * c + 4], sv[8 * c + 5]);
-        pk.w = pack_bf16x2(sv[8 * c + 6], sv[8 * c + 7]);
-        *reinterpret_cast<uint4*>(sm.p + (c >> 3) * kHalf + sw128_offset(r, c & 7)) = pk;
+        for (int j = 0; j < 32; ++j) pk[j] = pack_bf16x2(p[2 * j], p[2 * j + 1]);
+        tmem_st16(sbuf, pk);
+        tmem_st16(sbuf + 16, pk + 16);
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(&sm.p_full[bc & 1]);
+        ++bc;
       }
-      fence_proxy_async_smem();
-      tc_fence_before();
-      mbar_arrive(&sm.p_full);
-    }
-    if (ok && mbar_wait(&sm.pv_done, (nU - 1) & 1, status)) {
+      if (!ok) break;
+      mbar_arrive(&sm.tile_empty[tb]);
+      // ---- epilogue: merge the two halves of every row
+      // the PV of the tile's last block completes after all earlier ones
+      if (!(ok = mbar_wait(&sm.pv_done[(bc - 1) & 1], ((bc - 1) >> 1) & 1, status, 13))) break;
+      sm.ml[h][r] = make_float2(m, l);
+      mbar_arrive(&sm.ml_full);
+      if (!(ok = mbar_wait(&sm.ml_full, tcount & 1, status, 14))) break;
+      const float2 other = sm.ml[h ^ 1][r];
       __syncwarp();
       tc_fence_after();
-      const float inv = (l > 0.f) ? 1.f / l : 0.f;
-      const size_t orow = static_cast<size_t>(seq0 + pos) * Hq + g * G + hd;
-      uint4* dst = reinterpret_cast<uint4*>(o + orow * kD);
+      const float M = fmaxf(m, other.x);
+      const float f_me = (m == -INFINITY) ? 0.f : ex2(m - M);
+      const float f_ot = (other.x == -INFINITY) ? 0.f : ex2(other.x - M);
+      const float L = l * f_me + other.y * f_ot;
+      const float f0 = (h == 0) ? f_me : f_ot, f1 = (h == 0) ? f_ot : f_me;
+      const float inv = (L > 0.f) ? 1.f / L : 0.f;
+      const size_t orow_g = static_cast<size_t>(t.seq0 + pos) * Hq + g * kG + hd;
+      uint4* dst = reinterpret_cast<uint4*>(o + orow_g * kD + 64 * h);
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t v[32];
-        tmem_ld32(tmem_o + trow + c * 32, v);
+      for (int c = 0; c < 2; ++c) {
+        uint32_t a[32], bq[32];
+        tmem_ld32(tmem + kColO + trow + 64 * h + 32 * c, a);
+        tmem_ld32(tmem + kColO + 128 + trow + 64 * h + 32 * c, bq);
         tmem_ld_wait();
         if (row_valid) {
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
+          for (int q = 0; q < 4; ++q) {
+            float x[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+              x[e] = (__uint_as_float(a[8 * q + e]) * f0 + __uint_as_float(bq[8 * q + e]) * f1) * inv;
             uint4 pk;
-            pk.x = pack_bf16x2(__uint_as_float(v[8 * j + 0]) * inv, __uint_as_float(v[8 * j + 1]) * inv);
-            pk.y = pack_bf16x2(__uint_as_float(v[8 * j + 2]) * inv, __uint_as_float(v[8 * j + 3]) * inv);
-            pk.z = pack_bf16x2(__uint_as_float(v[8 * j + 4]) * inv, __uint_as_float(v[8 * j + 5]) * inv);
-            pk.w = pack_bf16x2(__uint_as_float(v[8 * j + 6]) * inv, __uint_as_float(v[8 * j + 7]) * inv);
-            dst[c * 4 + j] = pk;
+            pk.x = pack_bf16x2(x[0], x[1]);
+            pk.y = pack_bf16x2(x[2], x[3]);
+            pk.z = pack_bf16x2(x[4], x[5]);
+            pk.w = pack_bf16x2(x[6], x[7]);
+            dst[4 * c + q] = pk;
           }
         }
       }
-      if (row_valid) lse[orow] = (m + __log2f(l)) * 0.6931471805599453f;
+      if (h == 0 && row_valid) lse[orow_g] = (M + __log2f(L)) * 0.6931471805599453f;
+      tc_fence_before();
+      ++tcount;
     }
   }
   tc_fence_before();
@@ -319,36 +417,52 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   if (warp == 1) tmem_dealloc(tmem, 512);
 }
 
+static int fwd_sm_count() {
+  static int cached[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) return 148;
+  if (!cached[dev]) {
+    int n = 0;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    cached[dev] = n > 0 ? n : 148;
+  }
+  return cached[dev];
+}
+
 msa_status_t launch_sparse_fwd(const void* q, const void* k, const void* v, const int32_t* sel,
                                const int32_t* cu, int S, int T, int Hq, int Hkv, int max_seqlen,
                                float scale, const Plan& plan, void* o, float* lse,
                                cudaStream_t stream) {
   (void)S;
   (void)max_seqlen;
-  const int G = Hq / Hkv;
+  if (Hq / Hkv != kG)
+    return fail(MSA_ERR_UNSUPPORTED, "forward supports Hq/Hkv = 16 (got %d)", Hq / Hkv);
   CUtensorMap tq, tk, tv;
   const uint64_t dq[3] = {static_cast<uint64_t>(kD), static_cast<uint64_t>(Hq),
                           static_cast<uint64_t>(T)};
   const uint64_t dkv[3] = {static_cast<uint64_t>(kD), static_cast<uint64_t>(Hkv),
                            static_cast<uint64_t>(T)};
-  const uint32_t bq[3] = {64, static_cast<uint32_t>(G), static_cast<uint32_t>(128 / G)};
+  const uint32_t bq[3] = {64, static_cast<uint32_t>(kG), static_cast<uint32_t>(kTpt)};
   const uint32_t bkv[3] = {64, 1, 128};
   if (!make_tmap_bf16(&tq, q, 3, dq, bq) || !make_tmap_bf16(&tk, k, 3, dkv, bkv) ||
       !make_tmap_bf16(&tv, v, 3, dkv, bkv))
     return fail(MSA_ERR_CUDA, "cuTensorMapEncodeTiled failed for q/k/v");
-  const size_t smem = sizeof(FwdSmem) + 1024;
+  const size_t smem = sizeof(FwdSmem);
   static bool attr_set = false;
   if (!attr_set) {
     cudaFuncSetAttribute(sparse_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          static_cast<int>(smem));
     attr_set = true;
   }
-  dim3 grid(plan.max_tiles * G, Hkv);
+  const int per_head = (fwd_sm_count() + Hkv - 1) / Hkv;
+  const int max_ctas = plan.max_tiles * kG;
+  dim3 grid(static_cast<unsigned>(per_head < max_ctas ? per_head : max_ctas), Hkv);
   {
     TraceScope trace_("sparse_fwd_kernel", stream);
     sparse_fwd_kernel<<<grid, kFwdThreads, smem, stream>>>(
-      tq, tk, tv, sel, cu, plan.tiles, plan.num_tiles, Hq, Hkv, G, scale,
-      static_cast<__nv_bfloat16*>(o), lse, status_word());
+        tq, tk, tv, sel, cu, plan.tiles, plan.num_tiles, Hq, Hkv, scale,
+        static_cast<__nv_bfloat16*>(o), lse, status_word());
   }
   return check_launch("sparse_fwd_kernel");
 }
