@@ -57,6 +57,20 @@ uint32_t* status_word() {
   return ptrs[dev];
 }
 
+// ------------------------------------------------------------------ device
+
+int device_sm_count() {
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  if (!cached[dev]) {
+    int n = 0;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    cached[dev] = n > 0 ? n : 148;
+  }
+  return cached[dev];
+}
+
 // ------------------------------------------------------------------ tracing
 
 namespace {
@@ -106,23 +120,33 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-bool make_tmap_bf16(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
-                    const uint32_t* box) {
+static bool make_tmap(CUtensorMap* map, const void* base, CUtensorMapDataType dtype,
+                      uint64_t elem_bytes, int rank, const uint64_t* dims, const uint32_t* box) {
   auto fn = encode_fn();
   if (!fn) return false;
   cuuint64_t gdim[3], gstride[2];
   cuuint32_t bdim[3], estr[3] = {1, 1, 1};
-  uint64_t stride = 2;
+  uint64_t stride = elem_bytes;
   for (int i = 0; i < rank; ++i) {
     gdim[i] = dims[i];
     bdim[i] = box[i];
     if (i > 0) gstride[i - 1] = stride;
     stride *= dims[i];
   }
-  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), gdim,
-                  gstride, bdim, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+  CUresult r = fn(map, dtype, rank, const_cast<void*>(base), gdim, gstride, bdim, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
+}
+
+bool make_tmap_bf16(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
+                    const uint32_t* box) {
+  return make_tmap(map, base, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, rank, dims, box);
+}
+
+bool make_tmap_f32(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
+                   const uint32_t* box) {
+  return make_tmap(map, base, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, rank, dims, box);
 }
 
 // ------------------------------------------------------------------ tile plan
@@ -397,11 +421,10 @@ static msa_status_t check_heads(int Hq, int Hkv) {
 
 size_t msa_sparse_attn_fwd_workspace_size(int T, int S, int Hq, int Hkv, int max_seqlen) {
   (void)Hq;
-  (void)Hkv;
   (void)max_seqlen;
-  if (T < 1 || S < 1) return 0;
+  if (T < 1 || S < 1 || Hkv < 1) return 0;
   WsCursor ws(nullptr);
-  carve_plan(ws, T, S);
+  carve_fwd_workspace(ws, T, S, Hkv);
   return ws.used + 256;
 }
 
@@ -422,10 +445,10 @@ msa_status_t msa_sparse_attn_fwd(const void* q, const void* k, const void* v, co
   if (workspace_bytes < msa_sparse_attn_fwd_workspace_size(T, S, Hq, Hkv, max_seqlen))
     return fail(MSA_ERR_INVALID_ARG, "workspace too small");
   WsCursor ws(workspace);
-  Plan plan = carve_plan(ws, T, S);
+  FwdWorkspace fw = carve_fwd_workspace(ws, T, S, Hkv);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  MSA_TRY(launch_plan(plan, cu_seqlens, S, max_seqlen, st));
-  return launch_sparse_fwd(q, k, v, sel, cu_seqlens, S, T, Hq, Hkv, max_seqlen, scale, plan, o,
+  MSA_TRY(launch_plan(fw.plan, cu_seqlens, S, max_seqlen, st));
+  return launch_sparse_fwd(q, k, v, sel, cu_seqlens, S, T, Hq, Hkv, max_seqlen, scale, fw, o,
                            lse, st);
 }
 

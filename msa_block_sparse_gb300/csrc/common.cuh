@@ -45,6 +45,9 @@ class TraceScope {
 // bf16 tensor with up to 3 dims (dims[0] innermost, contiguous), 128B swizzle.
 bool make_tmap_bf16(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
                     const uint32_t* box);
+// fp32 tensor, same conventions (128B swizzle: the box's inner extent is 32 floats).
+bool make_tmap_f32(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
+                   const uint32_t* box);
 
 // ------------------------------------------------------------------ workspace
 

@@ -25,9 +25,17 @@ msa_status_t launch_index_select(const void* q_idx, const void* k_idx, const int
                                  cudaStream_t stream);
 
 // ---------------------------------------------------------------- sparse forward
+// Per (8-token query tile, KV head): word 0 = number of union blocks, words
+// 4.. = entries (block << 8) | (bit i: token i of the tile selected the block).
+constexpr int kFwdUnionStride = 132;
+struct FwdWorkspace {
+  Plan plan;
+  int* ulist;          // [max_tiles * 16, Hkv, kFwdUnionStride]
+};
+FwdWorkspace carve_fwd_workspace(WsCursor& ws, int T, int S, int Hkv);
 msa_status_t launch_sparse_fwd(const void* q, const void* k, const void* v, const int32_t* sel,
                                const int32_t* cu, int S, int T, int Hq, int Hkv, int max_seqlen,
-                               float scale, const Plan& plan, void* o, float* lse,
+                               float scale, const FwdWorkspace& fw, void* o, float* lse,
                                cudaStream_t stream);
 
 // ---------------------------------------------------------------- sparse backward
@@ -40,12 +48,15 @@ struct BwdWorkspace {
   int4* items;         // [max_items] (s, b, token_begin, token_end) in sequence positions
   int* num_items;      // [1]
   int max_items;
+  int* lists;          // [max_items, Hkv, kBwdSegment] positions that selected the item's block
+  int* list_len;       // [max_items, Hkv]
   float* delta;        // [T, Hq]  rowsum(dout * o)
   float* dq_acc;       // [T, Hq, 128] fp32
   float* dk_acc;       // [T, Hkv, 128] fp32
   float* dv_acc;       // [T, Hkv, 128] fp32
 };
 BwdWorkspace carve_bwd_workspace(WsCursor& ws, int T, int S, int Hq, int Hkv, int max_seqlen);
+int device_sm_count();
 msa_status_t launch_sparse_bwd(const void* q, const void* k, const void* v, const void* o,
                                const void* dout, const float* lse, const int32_t* sel,
                                const int32_t* cu, int S, int T, int Hq, int Hkv, int max_seqlen,

@@ -8,18 +8,21 @@
 // windows only and the fp32 dQ accumulator lines stay in L2.  Persistent CTAs
 // (one per SM) stride over the items.  Per item the CTA holds K_b and V_b in
 // shared memory and streams the query tokens of the window that selected b, in
-// ascending order, in chunks of 128/G tokens x G heads = 128 columns:
-//   scanner (warp 0): reads each candidate's 16 selected ids, compacts the
-//            matches with a ballot, loads the chunk's Q and dO rows by TMA
-//            (one box per token) and its lse / Delta into a 2-stage ring
+// ascending order, in chunks of 128/G tokens x G heads = 128 columns.  A
+// pre-pass (bwd_lists_kernel) lists, per item, the window's tokens that
+// selected the block (one thread per candidate, ballot compaction).
+//   producer (warp 0): loads the chunk's Q and dO rows by TMA (one box per
+//            token) and its lse / Delta by bulk copies into a 2-stage ring
 //   MMA (warp 1): S^T = K_b Q^T -> TMEM, dP^T = V_b dO^T -> TMEM,
 //            dV += P^T dO (P^T read from TMEM), dK += dS^T Q,
 //            dQ = dS K_b (dS^T in shared memory read as an MN-major operand)
 //   compute (warps 2..9, thread = key row x 64 columns):
 //            P^T = exp2(S^T scale log2e - lse log2e), causally masked, packed
 //            to bf16 into TMEM; dS^T = P^T (dP^T - Delta) to shared memory;
-//            then dQ rows (lane = column) added to the fp32 accumulator with
-//            16-byte atomics; at the end of an item dK, dV likewise.
+//            then dQ rows (lane = column) are staged, 128B-swizzled, in the
+//            chunk's own Q/dO buffers, which the producer adds into the fp32
+//            accumulator with TMA reduce-add before refilling the stage; at the
+//            end of an item dK and dV go to their accumulators with atomics.
 // A last kernel scales and converts the accumulators to bf16.
 #include "kernels.cuh"
 
@@ -27,7 +30,7 @@ namespace msa {
 
 namespace {
 
-constexpr int kBwdThreads = 320;            // warp 0 scan + TMA, warp 1 MMA, warps 2..9 compute
+constexpr int kBwdThreads = 320;            // warp 0 TMA, warp 1 MMA, warps 2..9 compute
 constexpr int kComputeThreads = 256;
 constexpr int kTile = 128 * 128 * 2;
 constexpr int kHalf = kTile / 2;
@@ -44,7 +47,7 @@ struct BwdSmem {
   uint8_t q[2][kTile];
   uint8_t dout[2][kTile];
   uint8_t dst[kTile];
-  float lse2[2][128];
+  float lse[2][128];      // natural-log lse of the chunk's 128 columns (bulk-copied)
   float delta[2][128];
   int tok[2][16];
   int ntok[2];
@@ -136,6 +139,50 @@ __global__ void __launch_bounds__(1024) bwd_items_kernel(const int32_t* __restri
   if (threadIdx.x == 0) *num_items = min(carry, max_items);
 }
 
+// ---------------------------------------------------------------- token lists
+
+// One CTA of kBwdSegment threads per (item, KV head), grid-striding over items:
+// thread t checks candidate position first + t; the matches are compacted in
+// ascending order into the item's list.
+__global__ void __launch_bounds__(kBwdSegment) bwd_lists_kernel(
+    const int32_t* __restrict__ cu, const int32_t* __restrict__ sel,
+    const int4* __restrict__ items, const int* __restrict__ num_items, int Hkv,
+    int* __restrict__ lists, int* __restrict__ list_len) {
+  static_assert(kBwdSegment == 256, "one thread per candidate position");
+  __shared__ int warp_cnt[kBwdSegment / 32];
+  const int n = *num_items;
+  const int g = blockIdx.y;
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  for (int it = blockIdx.x; it < n; it += gridDim.x) {
+    const int4 item = items[it];
+    const int s = item.x, b = item.y;
+    const int p = item.z + static_cast<int>(threadIdx.x);
+    bool hit = false;
+    if (p < item.w) {
+      const int4* row = reinterpret_cast<const int4*>(
+          sel + (static_cast<size_t>(cu[s] + p) * Hkv + g) * kTopK);
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const int4 v = __ldg(row + c);
+        hit |= (v.x == b) | (v.y == b) | (v.z == b) | (v.w == b);
+      }
+    }
+    const uint32_t m = __ballot_sync(0xffffffffu, hit);
+    if (lane == 0) warp_cnt[w] = __popc(m);
+    __syncthreads();
+    int off = 0, total = 0;
+#pragma unroll
+    for (int i = 0; i < kBwdSegment / 32; ++i) {
+      off += (i < w) ? warp_cnt[i] : 0;
+      total += warp_cnt[i];
+    }
+    const size_t li = static_cast<size_t>(it) * Hkv + g;
+    if (hit) lists[li * kBwdSegment + off + __popc(m & ((1u << lane) - 1u))] = p;
+    if (threadIdx.x == 0) list_len[li] = total;
+    __syncthreads();
+  }
+}
+
 // ---------------------------------------------------------------- Delta
 
 // delta[t, i] = sum_d dout[t, i, d] * o[t, i, d]; one warp per row.
@@ -183,8 +230,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     sparse_bwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                       const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v,
-                      const __grid_constant__ CUtensorMap tm_do, const int32_t* __restrict__ sel,
-                      const int32_t* __restrict__ cu, const float* __restrict__ lse,
+                      const __grid_constant__ CUtensorMap tm_do,
+                      const __grid_constant__ CUtensorMap tm_dq, const int* __restrict__ lists,
+                      const int* __restrict__ list_len, const int32_t* __restrict__ cu,
+                      const float* __restrict__ lse,
                       const float* __restrict__ delta, const int4* __restrict__ items,
                       const int* __restrict__ num_items, int Hq, int Hkv, float scale,
                       float* __restrict__ dq_acc, float* __restrict__ dk_acc,
@@ -229,7 +278,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const uint32_t tmem = sm.tmem_base;
 
   if (warp == 0) {
-    // ------------------------------------------------------------ scanner / TMA
+    // ------------------------------------------------------------ producer
     if (lane == 0) {
       prefetch_tmap(&tm_q);
       prefetch_tmap(&tm_do);
@@ -239,12 +288,43 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     uint32_t cg = 0;
     bool alive = true;
     int itl = 0;
+    // dQ rows of the chunk that last used a stage are staged in that stage's Q/dO
+    // buffers (8 tokens x 4 boxes of 16 heads x 32 fp32, 128B-swizzled); before the
+    // stage is refilled they are added into the fp32 accumulator by TMA reduce.
+    int pend_n[2] = {0, 0}, pend_seq0[2] = {0, 0};
+    auto flush_dq = [&](int st) {
+      if (pend_n[st] == 0) return;
+      if (lane < pend_n[st]) {
+        const int y = (pend_seq0[st] + sm.tok[st][lane]) * Hq + g * G;
+        const uint8_t* box = (lane < 4 ? sm.q[st] : sm.dout[st]) + (lane & 3) * 4 * 2048;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) tma_reduce_add_2d(&tm_dq, box + j * 2048, 32 * j, y);
+        bulk_commit_group();
+        bulk_wait_read_all();
+      }
+      __syncwarp();
+      pend_n[st] = 0;
+    };
     for (int it = blockIdx.x; alive && it < n_items; it += gridDim.x, ++itl) {
       const int4 item = items[it];
-      const int s = item.x, b = item.y, pbeg = item.z, pend = item.w;
+      const int s = item.x, b = item.y;
       const int seq0 = cu[s];
+      const size_t li = static_cast<size_t>(it) * Hkv + g;
+      const int nlist = list_len[li];
+      // lane L holds list entries 8L .. 8L+7 (chunk L)
+      int ent[tpt];
+      {
+        const int4* src = reinterpret_cast<const int4*>(lists + li * kBwdSegment) + 2 * lane;
+        int4 e0 = make_int4(0, 0, 0, 0), e1 = e0;
+        if (8 * lane < nlist) {
+          e0 = __ldg(src);
+          e1 = __ldg(src + 1);
+        }
+        ent[0] = e0.x; ent[1] = e0.y; ent[2] = e0.z; ent[3] = e0.w;
+        ent[4] = e1.x; ent[5] = e1.y; ent[6] = e1.z; ent[7] = e1.w;
+      }
       if (lane == 0) {
-        alive = mbar_wait(&sm.kv_empty, (itl & 1) ^ 1, status);
+        alive = mbar_wait(&sm.kv_empty, (itl & 1) ^ 1, status, 21);
         if (alive) {
           mbar_arrive_expect_tx(&sm.kv_full, 2 * kTile);
           const int row = seq0 + b * kBlock;
@@ -255,77 +335,59 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
       }
       alive = __shfl_sync(0xffffffffu, alive ? 1 : 0, 0) != 0;
-      int cnt = 0, my_pos = -1;
-      auto emit = [&](int n) {
+      const int nchunks = (nlist + tpt - 1) / tpt;
+      for (int c = 0; alive && c <= nchunks; ++c) {
+        const int n = (c < nchunks) ? min(tpt, nlist - tpt * c) : 0;   // 0: end of the item
         const int st = cg & 1;
-        if (lane == 0) alive = mbar_wait(&sm.ld_empty[st], ((cg >> 1) & 1) ^ 1, status);
+        if (lane == 0) alive = mbar_wait(&sm.ld_empty[st], ((cg >> 1) & 1) ^ 1, status, 22);
         alive = __shfl_sync(0xffffffffu, alive ? 1 : 0, 0) != 0;
-        if (!alive) return;
-        const int first = __shfl_sync(0xffffffffu, my_pos, 0);
-        const int pos = (lane < n) ? my_pos : first;
-        if (lane < tpt && n > 0) {
-          sm.tok[st][lane] = (lane < n) ? pos : -1;
-          const size_t base = static_cast<size_t>(seq0 + pos) * Hq + g * G;
-          const float4* l4 = reinterpret_cast<const float4*>(lse + base);
-          const float4* d4 = reinterpret_cast<const float4*>(delta + base);
+        if (!alive) break;
+        flush_dq(st);
+        // positions of the chunk's tokens, broadcast from lane c (slots >= n repeat slot 0)
+        int pos = 0;
 #pragma unroll
-          for (int q4 = 0; q4 < G / 4; ++q4) {
-            float4 lv = __ldg(l4 + q4);
-            lv.x *= kLog2e; lv.y *= kLog2e; lv.z *= kLog2e; lv.w *= kLog2e;
-            reinterpret_cast<float4*>(&sm.lse2[st][lane * G])[q4] = lv;
-            reinterpret_cast<float4*>(&sm.delta[st][lane * G])[q4] = __ldg(d4 + q4);
-          }
+        for (int j = 0; j < tpt; ++j) {
+          const int pj = __shfl_sync(0xffffffffu, ent[j], c & 31);
+          if (lane == j) pos = pj;
         }
-        if (lane == 0) sm.ntok[st] = n;
+        const int pos0 = __shfl_sync(0xffffffffu, pos, 0);
+        if (lane < tpt) sm.tok[st][lane] = (lane < n) ? pos : -1;
+        if (lane == 0) {
+          sm.ntok[st] = n;
+          if (n > 0) mbar_arrive_expect_tx(&sm.ld_full[st], 2 * kTile + tpt * 2 * G * 4);
+        }
         __syncwarp();
         if (n > 0) {
-          int slot_pos[tpt];
-#pragma unroll
-          for (int i = 0; i < tpt; ++i) slot_pos[i] = __shfl_sync(0xffffffffu, pos, i);
-          if (lane == 0) {
-            mbar_arrive_expect_tx(&sm.ld_full[st], 2 * kTile);
-#pragma unroll
-            for (int i = 0; i < tpt; ++i) {
-              const int t = seq0 + slot_pos[i];
-              const uint32_t off = i * G * 128;
-              tma_load_3d(sm.q[st] + off, &tm_q, &sm.ld_full[st], 0, g * G, t);
-              tma_load_3d(sm.q[st] + kHalf + off, &tm_q, &sm.ld_full[st], 64, g * G, t);
-              tma_load_3d(sm.dout[st] + off, &tm_do, &sm.ld_full[st], 0, g * G, t);
-              tma_load_3d(sm.dout[st] + kHalf + off, &tm_do, &sm.ld_full[st], 64, g * G, t);
-            }
+          if (lane < tpt) {
+            const int t = seq0 + ((lane < n) ? pos : pos0);
+            const uint32_t off = lane * G * 128;
+            tma_load_3d(sm.q[st] + off, &tm_q, &sm.ld_full[st], 0, g * G, t);
+            tma_load_3d(sm.q[st] + kHalf + off, &tm_q, &sm.ld_full[st], 64, g * G, t);
+            tma_load_3d(sm.dout[st] + off, &tm_do, &sm.ld_full[st], 0, g * G, t);
+            tma_load_3d(sm.dout[st] + kHalf + off, &tm_do, &sm.ld_full[st], 64, g * G, t);
+            const size_t row = static_cast<size_t>(t) * Hq + g * G;
+            bulk_load(&sm.lse[st][lane * G], lse + row, G * 4, &sm.ld_full[st]);
+            bulk_load(&sm.delta[st][lane * G], delta + row, G * 4, &sm.ld_full[st]);
           }
         } else if (lane == 0) {
           mbar_arrive(&sm.ld_full[st]);   // end of the item: no data
         }
+        pend_n[st] = n;
+        pend_seq0[st] = seq0;
         ++cg;
-      };
-      for (int base = pbeg; alive && base < pend; base += 32) {
-        const int p = base + lane;
-        bool hit = false;
-        if (p < pend) {
-          const int4* row = reinterpret_cast<const int4*>(
-              sel + (static_cast<size_t>(seq0 + p) * Hkv + g) * kTopK);
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            const int4 v = __ldg(row + c);
-            hit |= (v.x == b) | (v.y == b) | (v.z == b) | (v.w == b);
-          }
-        }
-        uint32_t mask = __ballot_sync(0xffffffffu, hit);
-        while (mask) {
-          const int bit = __ffs(mask) - 1;
-          mask &= mask - 1;
-          if (lane == cnt) my_pos = base + bit;
-          if (++cnt == tpt) {
-            emit(tpt);
-            cnt = 0;
-            if (!alive) break;
-          }
-        }
       }
-      if (alive && cnt > 0) emit(cnt);
-      if (alive) emit(0);
     }
+    // the last two stage uses may still hold staged dQ rows
+    for (int k = 0; alive && k < 2; ++k) {
+      const int st = cg & 1;
+      if (pend_n[st] > 0) {
+        if (lane == 0) alive = mbar_wait(&sm.ld_empty[st], ((cg >> 1) & 1) ^ 1, status, 23);
+        alive = __shfl_sync(0xffffffffu, alive ? 1 : 0, 0) != 0;
+        if (alive) flush_dq(st);
+      }
+      ++cg;
+    }
+    bulk_wait_all();
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (elect_one()) {
@@ -334,11 +396,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       bool ok = true;
       int itl = 0;
       for (int it = blockIdx.x; ok && it < n_items; it += gridDim.x, ++itl) {
-        ok = mbar_wait(&sm.kv_full, itl & 1, status);
+        if (!(ok = mbar_wait(&sm.kv_full, itl & 1, status, 31))) break;
         bool first = true;
         while (ok) {
           const int st = cg & 1;
-          ok = mbar_wait(&sm.ld_full[st], (cg >> 1) & 1, status);
+          ok = mbar_wait(&sm.ld_full[st], (cg >> 1) & 1, status, 32);
           ++cg;
           if (!ok) break;
           if (sm.ntok[st] == 0) {
@@ -348,7 +410,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           tc_fence_after();
           const uint32_t qa = smem_u32(sm.q[st]), da = smem_u32(sm.dout[st]);
           // S^T = K Q^T (needs P^T of the previous chunk consumed by its dV)
-          if (cm > 0 && !(ok = mbar_wait(&sm.dv_done, (cm - 1) & 1, status))) break;
+          if (cm > 0 && !(ok = mbar_wait(&sm.dv_done, (cm - 1) & 1, status, 33))) break;
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk) {
@@ -358,7 +420,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           }
           umma_commit(&sm.s_full);
           // dP^T = V dO^T (needs dQ of the previous chunk drained)
-          if (cm > 0 && !(ok = mbar_wait(&sm.dq_free, (cm - 1) & 1, status))) break;
+          if (cm > 0 && !(ok = mbar_wait(&sm.dq_free, (cm - 1) & 1, status, 34))) break;
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk) {
@@ -367,9 +429,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                       sdesc_sw128(da + off, 16, 1024), kIdescKK, kk > 0);
           }
           umma_commit(&sm.dp_full);
-          // dV += P^T dO, P^T packed in TMEM: columns [64h, 64h+64) of the chunk
-          // at TMEM kColS + 64h .. + 32
-          if (!(ok = mbar_wait(&sm.p_full, cm & 1, status))) break;
+          // dV += P^T dO, P^T packed in TMEM: chunk columns [64h, 64h+64) at
+          // TMEM kColS + 64h .. + 32
+          if (!(ok = mbar_wait(&sm.p_full, cm & 1, status, 35))) break;
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk) {
@@ -379,7 +441,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           }
           umma_commit(&sm.dv_done);
           // dK += dS^T Q and dQ = dS K
-          if (!(ok = mbar_wait(&sm.ds_full, cm & 1, status))) break;
+          if (!(ok = mbar_wait(&sm.ds_full, cm & 1, status, 38))) break;
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk) {
@@ -420,7 +482,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       int nch = 0;
       while (true) {
         const int st = cg & 1;
-        if (!(ok = mbar_wait(&sm.ld_full[st], (cg >> 1) & 1, status))) break;
+        if (!(ok = mbar_wait(&sm.ld_full[st], (cg >> 1) & 1, status, 41))) break;
         ++cg;
         const int n = sm.ntok[st];
         if (n == 0) {
@@ -431,11 +493,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
         for (int i = 0; i < 4; ++i) tokp[i] = sm.tok[st][4 * h + i];
         const int tokd = sm.tok[st][r >> 4];     // token of this thread's dQ column
-        const float* lse2 = sm.lse2[st] + 64 * h;
+        const float* lsen = sm.lse[st] + 64 * h;
         const float* dlt = sm.delta[st] + 64 * h;
 
         // ---- P^T = exp2(S^T * scale log2e - lse log2e), causally masked
-        if (!(ok = mbar_wait(&sm.s_full, cm & 1, status))) break;
+        if (!(ok = mbar_wait(&sm.s_full, cm & 1, status, 42))) break;
         __syncwarp();
         tc_fence_after();
         float p[64];
@@ -446,8 +508,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           tmem_ld_wait();
 #pragma unroll
           for (int j4 = 0; j4 < 16; ++j4) {
-            const float4 l4 = reinterpret_cast<const float4*>(lse2)[j4];
-            const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+            const float4 l4 = reinterpret_cast<const float4*>(lsen)[j4];
+            const float lv[4] = {l4.x * kLog2e, l4.y * kLog2e, l4.z * kLog2e, l4.w * kLog2e};
             const bool valid = kp <= tokp[j4 >> 2];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
@@ -466,7 +528,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         mbar_arrive(&sm.p_full);
 
         // ---- dS^T = P^T (dP^T - Delta) -> shared memory (K-major rows = keys)
-        if (!(ok = mbar_wait(&sm.dp_full, cm & 1, status))) break;
+        if (!(ok = mbar_wait(&sm.dp_full, cm & 1, status, 43))) break;
         __syncwarp();
         tc_fence_after();
         {
@@ -494,10 +556,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         fence_proxy_async_smem();
         tc_fence_before();
         mbar_arrive(&sm.ds_full);
-        mbar_arrive(&sm.ld_empty[st]);     // done with this stage's metadata
 
-        // ---- dQ rows (lane = chunk column) -> fp32 accumulator
-        if (!(ok = mbar_wait(&sm.dq_full, cm & 1, status))) break;
+        // ---- dQ rows (lane = chunk column) -> staging in this stage's Q/dO
+        // buffers (their operands are consumed once dQ is done); the producer
+        // adds them into the accumulator with TMA reduce before refilling
+        if (!(ok = mbar_wait(&sm.dq_full, cm & 1, status, 45))) break;
         __syncwarp();
         tc_fence_after();
         {
@@ -505,19 +568,24 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           tmem_ld32(tmem + kColDP + trow + 64 * h, qv);
           tmem_ld32(tmem + kColDP + trow + 64 * h + 32, qv + 32);
           tmem_ld_wait();
+          tc_fence_before();
+          mbar_arrive(&sm.dq_free);           // the TMEM region is free once read
           if (tokd >= 0) {
-            float4* dst = reinterpret_cast<float4*>(
-                dq_acc + (static_cast<size_t>(seq0 + tokd) * Hq + g * G + (r & 15)) * kD + 64 * h);
+            const int ti = r >> 4, hd = r & 15;
+            uint8_t* box = (ti < 4 ? sm.q[st] : sm.dout[st]) + (ti & 3) * 4 * 2048 + hd * 128;
 #pragma unroll
-            for (int j = 0; j < 16; ++j)
-              atomicAdd(dst + j, make_float4(__uint_as_float(qv[4 * j]),
-                                             __uint_as_float(qv[4 * j + 1]),
-                                             __uint_as_float(qv[4 * j + 2]),
-                                             __uint_as_float(qv[4 * j + 3])));
+            for (int jj = 0; jj < 2; ++jj) {
+              uint8_t* bx = box + (2 * h + jj) * 2048;
+#pragma unroll
+              for (int c = 0; c < 8; ++c)
+                *reinterpret_cast<uint4*>(bx + ((c ^ (hd & 7)) << 4)) =
+                    make_uint4(qv[32 * jj + 4 * c], qv[32 * jj + 4 * c + 1],
+                               qv[32 * jj + 4 * c + 2], qv[32 * jj + 4 * c + 3]);
+            }
           }
         }
-        tc_fence_before();
-        mbar_arrive(&sm.dq_free);
+        fence_proxy_async_smem();
+        mbar_arrive(&sm.ld_empty[st]);        // staged; done with the stage
         ++cm;
         ++nch;
       }
@@ -563,25 +631,14 @@ static int bwd_max_items(int T, int S, int max_seqlen) {
   return static_cast<int>(n < (1LL << 30) ? n : (1LL << 30));
 }
 
-static int sm_count() {
-  static int cached[64] = {0};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev < 0 || dev >= 64) return 148;
-  if (!cached[dev]) {
-    int n = 0;
-    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    cached[dev] = n > 0 ? n : 148;
-  }
-  return cached[dev];
-}
-
 BwdWorkspace carve_bwd_workspace(WsCursor& ws, int T, int S, int Hq, int Hkv, int max_seqlen) {
   BwdWorkspace w;
   w.plan = carve_plan(ws, T, S);
   w.max_items = bwd_max_items(T, S, max_seqlen);
   w.items = ws.take<int4>(w.max_items);
   w.num_items = ws.take<int>(1);
+  w.lists = ws.take<int>(static_cast<size_t>(w.max_items) * Hkv * kBwdSegment);
+  w.list_len = ws.take<int>(static_cast<size_t>(w.max_items) * Hkv);
   w.delta = ws.take<float>(static_cast<size_t>(T) * Hq);
   w.dq_acc = ws.take<float>(static_cast<size_t>(T) * Hq * kD);
   w.dk_acc = ws.take<float>(static_cast<size_t>(T) * Hkv * kD);
@@ -604,8 +661,12 @@ msa_status_t launch_sparse_bwd(const void* q, const void* k, const void* v, cons
                             static_cast<uint64_t>(T)};
   const uint32_t bq[3] = {64, static_cast<uint32_t>(G), 1};
   const uint32_t bkv[3] = {64, 1, 128};
+  CUtensorMap tdq;
+  const uint64_t dacc[2] = {static_cast<uint64_t>(kD), static_cast<uint64_t>(T) * Hq};
+  const uint32_t bacc[2] = {32, 16};
   if (!make_tmap_bf16(&tq, q, 3, dq3, bq) || !make_tmap_bf16(&tdo, dout, 3, dq3, bq) ||
-      !make_tmap_bf16(&tk, k, 3, dkv3, bkv) || !make_tmap_bf16(&tv, v, 3, dkv3, bkv))
+      !make_tmap_bf16(&tk, k, 3, dkv3, bkv) || !make_tmap_bf16(&tv, v, 3, dkv3, bkv) ||
+      !make_tmap_f32(&tdq, ws.dq_acc, 2, dacc, bacc))
     return fail(MSA_ERR_CUDA, "cuTensorMapEncodeTiled failed for the backward");
   uint32_t* st = status_word();
 
@@ -628,7 +689,14 @@ msa_status_t launch_sparse_bwd(const void* q, const void* k, const void* v, cons
     bwd_items_kernel<<<1, 1024, 0, stream>>>(cu, S, bwd_windows(max_seqlen), ws.items,
                                              ws.num_items, ws.max_items, st);
   }
-  msa_status_t e = check_launch("bwd_delta/items");
+  {
+    const int sms = device_sm_count();
+    dim3 lgrid(static_cast<unsigned>(ws.max_items < 4 * sms ? ws.max_items : 4 * sms), Hkv);
+    TraceScope trace_("bwd_lists_kernel", stream);
+    bwd_lists_kernel<<<lgrid, kBwdSegment, 0, stream>>>(cu, sel, ws.items, ws.num_items, Hkv,
+                                                         ws.lists, ws.list_len);
+  }
+  msa_status_t e = check_launch("bwd_delta/items/lists");
   if (e != MSA_OK) return e;
 
   const size_t smem = sizeof(BwdSmem);
@@ -638,12 +706,13 @@ msa_status_t launch_sparse_bwd(const void* q, const void* k, const void* v, cons
                          static_cast<int>(smem));
     attr_set = true;
   }
-  const int per_head = (sm_count() + Hkv - 1) / Hkv;
+  const int per_head = (device_sm_count() + Hkv - 1) / Hkv;
   dim3 grid(static_cast<unsigned>(per_head < ws.max_items ? per_head : ws.max_items), Hkv);
   {
     TraceScope trace_("sparse_bwd_kernel", stream);
     sparse_bwd_kernel<<<grid, kBwdThreads, smem, stream>>>(
-        tq, tk, tv, tdo, sel, cu, lse, ws.delta, ws.items, ws.num_items, Hq, Hkv, scale,
+        tq, tk, tv, tdo, tdq, ws.lists, ws.list_len, cu, lse, ws.delta, ws.items, ws.num_items, Hq,
+        Hkv, scale,
         ws.dq_acc, ws.dk_acc, ws.dv_acc, st);
   }
   e = check_launch("sparse_bwd_kernel");

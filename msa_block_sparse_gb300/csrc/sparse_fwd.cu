@@ -9,9 +9,10 @@
 // current block gets P = 0 for it.
 //
 // Persistent CTAs (one per SM) stride over the tiles:
-//   producer (warp 0): builds the next tile's block union (bitmaps in shared
-//            memory, double-buffered) and loads its Q tile, then streams K_b and
-//            V_b through separate 2-stage TMA rings (K runs one block ahead)
+//   producer (warp 0): copies the next tile's block union (built beforehand by
+//            fwd_union_kernel, one warp per tile) into a double-buffered slot and
+//            loads its Q tile, then streams K_b and V_b through separate 2-stage
+//            TMA rings (K runs one block ahead)
 //   MMA (warp 1): S_i = Q K_b^T into one of two TMEM buffers; then
 //            O_h += P_h V_b[64h, 64h+64) for the two 64-key halves h, with P_h
 //            read from TMEM as the A operand
@@ -43,8 +44,7 @@ struct FwdSmem {
   uint8_t q[2][kTile];
   uint8_t k[2][kTile];
   uint8_t v[2][kTile];
-  uint32_t tok_mask[2][kTpt][kMaskWords];
-  int ublk[2][kTpt * kTopK];
+  int ublk[2][kTpt * kTopK];                 // union entries (block << 8) | token mask
   int n_union[2];
   float2 ml[2][128];                        // per half: (max, sum) of each row, for the merge
   uint64_t tile_full[2], tile_empty[2];
@@ -90,10 +90,72 @@ __device__ __forceinline__ bool tile_info(int ti, const int2* tiles, const int32
 
 }  // namespace
 
+// One warp per (tile, KV head), grid-striding: the union of the 8 tokens'
+// selected blocks in ascending order, each entry (block << 8) | token mask.
+__global__ void __launch_bounds__(256) fwd_union_kernel(const int32_t* __restrict__ sel,
+                                                        const int32_t* __restrict__ cu,
+                                                        const int2* __restrict__ tiles,
+                                                        const int* __restrict__ num_tiles,
+                                                        int Hkv, int* __restrict__ ulist,
+                                                        uint32_t* status) {
+  __shared__ uint32_t words_s[8][kMaskWords];
+  const int total = *num_tiles * kG;
+  const int g = blockIdx.y;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int ti = blockIdx.x * 8 + warp; ti < total; ti += gridDim.x * 8) {
+    int* out = ulist + (static_cast<size_t>(ti) * Hkv + g) * kFwdUnionStride;
+    TileInfo t;
+    if (!tile_info(ti, tiles, cu, t)) {
+      if (lane == 0) out[0] = 0;
+      continue;
+    }
+    int ids[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int idx = lane * 4 + e;             // lanes 4i .. 4i+3 hold token i's 16 ids
+      const int tl = idx >> 4;
+      int b = -1;
+      if (tl < t.ntok) {
+        b = __ldg(sel + (static_cast<size_t>(t.seq0 + t.p0 + tl) * Hkv + g) * kTopK + (idx & 15));
+        if (b > t.qb) {
+          atomicOr(status, kStatusBounds);
+          b = -1;
+        }
+      }
+      ids[e] = b;
+    }
+    const int nb_seq = (t.len + kBlock - 1) / kBlock;
+    const int words = min((nb_seq + 31) >> 5, kMaskWords);
+    if (lane < words) words_s[warp][lane] = 0;
+    __syncwarp();
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      if (ids[e] >= 0) atomicOr(&words_s[warp][ids[e] >> 5], 1u << (ids[e] & 31));
+    __syncwarp();
+    int n = 0;
+    for (int w = 0; w < words; ++w) {
+      uint32_t u = words_s[warp][w];
+      while (u) {
+        const int b = w * 32 + __ffs(u) - 1;
+        u &= u - 1;
+        const bool mine = (ids[0] == b) | (ids[1] == b) | (ids[2] == b) | (ids[3] == b);
+        const uint32_t bal = __ballot_sync(0xffffffffu, mine);
+        uint32_t tm = 0;
+#pragma unroll
+        for (int i = 0; i < kTpt; ++i) tm |= ((bal >> (4 * i)) & 0xFu) ? (1u << i) : 0u;
+        if (lane == 0 && n < kTpt * kTopK) out[4 + n] = (b << 8) | static_cast<int>(tm);
+        ++n;
+      }
+    }
+    if (lane == 0) out[0] = min(n, kTpt * kTopK);
+    __syncwarp();
+  }
+}
+
 __global__ void __launch_bounds__(kFwdThreads, 1)
     sparse_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                       const __grid_constant__ CUtensorMap tm_k,
-                      const __grid_constant__ CUtensorMap tm_v, const int32_t* __restrict__ sel,
+                      const __grid_constant__ CUtensorMap tm_v, const int* __restrict__ ulist,
                       const int32_t* __restrict__ cu, const int2* __restrict__ tiles,
                       const int* __restrict__ num_tiles, int Hq, int Hkv, float scale,
                       __nv_bfloat16* __restrict__ o, float* __restrict__ lse, uint32_t* status) {
@@ -150,46 +212,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       if (lane == 0) alive = mbar_wait(&sm.tile_empty[tb], ((tcount >> 1) & 1) ^ 1, status, 1);
       alive = __shfl_sync(0xffffffffu, alive ? 1 : 0, 0) != 0;
       if (!alive) break;
-      // ---- union of the tile tokens' selected blocks
-      const int nb_seq = (t.len + kBlock - 1) / kBlock;
-      const int words = min((nb_seq + 31) >> 5, kMaskWords);
-      for (int w = lane; w < kTpt * kMaskWords; w += 32) sm.tok_mask[tb][w / kMaskWords][w % kMaskWords] = 0;
-      __syncwarp();
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int idx = lane * 4 + e;          // (token, slot) of the 8 x 16 ids
-        const int tl = idx >> 4;
-        if (tl < t.ntok) {
-          const int b = __ldg(sel + (static_cast<size_t>(t.seq0 + t.p0 + tl) * Hkv + g) * kTopK +
-                              (idx & 15));
-          if (b >= 0 && b <= t.qb) atomicOr(&sm.tok_mask[tb][tl][b >> 5], 1u << (b & 31));
-          else if (b > t.qb) atomicOr(status, kStatusBounds);
-        }
-      }
-      __syncwarp();
-      int base = 0;
-      for (int w0 = 0; w0 < words; w0 += 32) {
-        const int w = w0 + lane;
-        uint32_t u = 0;
-        if (w < words)
-          for (int tl = 0; tl < t.ntok; ++tl) u |= sm.tok_mask[tb][tl][w];
-        const int c = __popc(u);
-        int incl = c;
-#pragma unroll
-        for (int d = 1; d < 32; d <<= 1) {
-          const int x = __shfl_up_sync(0xffffffffu, incl, d);
-          if (lane >= d) incl += x;
-        }
-        int off = base + incl - c;
-        while (u) {
-          const int bit = __ffs(u) - 1;
-          if (off < kTpt * kTopK) sm.ublk[tb][off] = w * 32 + bit;
-          ++off;
-          u &= u - 1;
-        }
-        base += __shfl_sync(0xffffffffu, incl, 31);
-      }
-      const int nU = min(base, kTpt * kTopK);
+      // ---- the tile's union entries (built by fwd_union_kernel)
+      const int* ul = ulist + (static_cast<size_t>(ti) * Hkv + g) * kFwdUnionStride;
+      const int nU = min(__ldg(ul), kTpt * kTopK);
+      for (int i = lane; i < nU; i += 32) sm.ublk[tb][i] = __ldg(ul + 4 + i);
       if (lane == 0) sm.n_union[tb] = nU;
       __syncwarp();
       if (lane == 0) {
@@ -201,7 +227,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           if (i < nU) {
             const int st = kc & 1;
             if (!(alive = mbar_wait(&sm.k_empty[st], ((kc >> 1) & 1) ^ 1, status, 2))) break;
-            const int row = t.seq0 + sm.ublk[tb][i] * kBlock;
+            const int row = t.seq0 + (sm.ublk[tb][i] >> 8) * kBlock;
             mbar_arrive_expect_tx(&sm.k_full[st], kTile);
             tma_load_3d(sm.k[st], &tm_k, &sm.k_full[st], 0, g, row);
             tma_load_3d(sm.k[st] + kHalf, &tm_k, &sm.k_full[st], 64, g, row);
@@ -210,7 +236,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           if (i > 0) {
             const int st = vc & 1;
             if (!(alive = mbar_wait(&sm.v_empty[st], ((vc >> 1) & 1) ^ 1, status, 3))) break;
-            const int row = t.seq0 + sm.ublk[tb][i - 1] * kBlock;
+            const int row = t.seq0 + (sm.ublk[tb][i - 1] >> 8) * kBlock;
             mbar_arrive_expect_tx(&sm.v_full[st], kTile);
             tma_load_3d(sm.v[st], &tm_v, &sm.v_full[st], 0, g, row);
             tma_load_3d(sm.v[st] + kHalf, &tm_v, &sm.v_full[st], 64, g, row);
@@ -300,7 +326,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       const int pos = t.p0 + tl;
       float m = -INFINITY, l = 0.f;
       for (int i = 0; i < nU; ++i) {
-        const int b = sm.ublk[tb][i];
+        const int ent = sm.ublk[tb][i];
+        const int b = ent >> 8;
         const uint32_t sbuf = tmem + (bc & 1) * 128 + trow + 64 * h;
         if (!(ok = mbar_wait(&sm.s_full[bc & 1], (bc >> 1) & 1, status, 10))) break;
         __syncwarp();
@@ -309,8 +336,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         tmem_ld32(sbuf, sv);
         tmem_ld32(sbuf + 32, sv + 32);
         tmem_ld_wait();
-        const bool selected =
-            row_valid && ((sm.tok_mask[tb][tl][b >> 5] >> (b & 31)) & 1u);
+        const bool selected = row_valid && ((ent >> tl) & 1);
         const int kmax = (b == t.qb) ? (pos & (kBlock - 1)) - 64 * h : 63;
         bool resc = false;
         float mu = m, rs = 0.f;
@@ -417,23 +443,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   if (warp == 1) tmem_dealloc(tmem, 512);
 }
 
-static int fwd_sm_count() {
-  static int cached[64] = {0};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev < 0 || dev >= 64) return 148;
-  if (!cached[dev]) {
-    int n = 0;
-    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    cached[dev] = n > 0 ? n : 148;
-  }
-  return cached[dev];
-}
-
 msa_status_t launch_sparse_fwd(const void* q, const void* k, const void* v, const int32_t* sel,
                                const int32_t* cu, int S, int T, int Hq, int Hkv, int max_seqlen,
-                               float scale, const Plan& plan, void* o, float* lse,
+                               float scale, const FwdWorkspace& fw, void* o, float* lse,
                                cudaStream_t stream) {
+  const Plan& plan = fw.plan;
   (void)S;
   (void)max_seqlen;
   if (Hq / Hkv != kG)
@@ -455,16 +469,32 @@ msa_status_t launch_sparse_fwd(const void* q, const void* k, const void* v, cons
                          static_cast<int>(smem));
     attr_set = true;
   }
-  const int per_head = (fwd_sm_count() + Hkv - 1) / Hkv;
+  const int per_head = (device_sm_count() + Hkv - 1) / Hkv;
   const int max_ctas = plan.max_tiles * kG;
   dim3 grid(static_cast<unsigned>(per_head < max_ctas ? per_head : max_ctas), Hkv);
   {
+    const int max_tiles16 = plan.max_tiles * kG;
+    const int ublocks = (max_tiles16 + 7) / 8;
+    const int cap = 4 * device_sm_count();
+    dim3 ugrid(static_cast<unsigned>(ublocks < cap ? ublocks : cap), Hkv);
+    TraceScope trace_("fwd_union_kernel", stream);
+    fwd_union_kernel<<<ugrid, 256, 0, stream>>>(sel, cu, plan.tiles, plan.num_tiles, Hkv,
+                                               fw.ulist, status_word());
+  }
+  {
     TraceScope trace_("sparse_fwd_kernel", stream);
     sparse_fwd_kernel<<<grid, kFwdThreads, smem, stream>>>(
-        tq, tk, tv, sel, cu, plan.tiles, plan.num_tiles, Hq, Hkv, scale,
+        tq, tk, tv, fw.ulist, cu, plan.tiles, plan.num_tiles, Hq, Hkv, scale,
         static_cast<__nv_bfloat16*>(o), lse, status_word());
   }
   return check_launch("sparse_fwd_kernel");
+}
+
+FwdWorkspace carve_fwd_workspace(WsCursor& ws, int T, int S, int Hkv) {
+  FwdWorkspace w;
+  w.plan = carve_plan(ws, T, S);
+  w.ulist = ws.take<int>(static_cast<size_t>(w.plan.max_tiles) * kG * Hkv * kFwdUnionStride);
+  return w;
 }
 
 }  // namespace msa
