@@ -149,6 +149,23 @@ bool make_tmap_f32(CUtensorMap* map, const void* base, int rank, const uint64_t*
   return make_tmap(map, base, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, rank, dims, box);
 }
 
+bool make_tmap_bf16_strided(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
+                            const uint64_t* strides, const uint32_t* box) {
+  auto fn = encode_fn();
+  if (!fn || rank < 2 || rank > 5) return false;
+  cuuint64_t gdim[5], gstride[4];
+  cuuint32_t bdim[5], estr[5] = {1, 1, 1, 1, 1};
+  for (int i = 0; i < rank; ++i) {
+    gdim[i] = dims[i];
+    bdim[i] = box[i];
+    if (i > 0) gstride[i - 1] = strides[i - 1];
+  }
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), gdim,
+                  gstride, bdim, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 // ------------------------------------------------------------------ tile plan
 
 // One CTA.  nb(s) = ceil(len_s / 128) tiles per sequence; tiles are listed with

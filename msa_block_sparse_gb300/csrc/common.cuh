@@ -48,6 +48,10 @@ bool make_tmap_bf16(CUtensorMap* map, const void* base, int rank, const uint64_t
 // fp32 tensor, same conventions (128B swizzle: the box's inner extent is 32 floats).
 bool make_tmap_f32(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
                    const uint32_t* box);
+// bf16 tensor of rank 2..5 with explicit byte strides of dims 1.. (multiples of
+// 16, in any order), 128B swizzle; dims[0] is contiguous.
+bool make_tmap_bf16_strided(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
+                            const uint64_t* strides, const uint32_t* box);
 
 // ------------------------------------------------------------------ workspace
 

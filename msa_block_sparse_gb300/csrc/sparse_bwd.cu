@@ -6,23 +6,26 @@
 // 256-position window of candidate query positions).  Items are listed window
 // by window, so the items running at any moment add into dQ rows of a few
 // windows only and the fp32 dQ accumulator lines stay in L2.  Persistent CTAs
-// (one per SM) stride over the items.  Per item the CTA holds K_b and V_b in
-// shared memory and streams the query tokens of the window that selected b, in
-// ascending order, in chunks of 128/G tokens x G heads = 128 columns.  A
-// pre-pass (bwd_lists_kernel) lists, per item, the window's tokens that
-// selected the block (one thread per candidate, ballot compaction).
-//   producer (warp 0): loads the chunk's Q and dO rows by TMA (one box per
-//            token) and its lse / Delta by bulk copies into a 2-stage ring
-//   MMA (warp 1): S^T = K_b Q^T -> TMEM, dP^T = V_b dO^T -> TMEM,
+// (one per SM and KV head share) stride over the items.  Per item the CTA holds
+// K_b and V_b in shared memory and streams the window's query tokens that
+// selected b, in ascending order, in half-chunks of 4 tokens x G = 16 heads =
+// 64 columns.  A pre-pass (bwd_lists_kernel) lists, per item, those tokens
+// (one thread per candidate, ballot compaction); another packs (lse log2 e,
+// Delta) per query row.
+//   producer (warp 0): per token one 4 KB tensor load of Q, one of dO (a 5-D
+//            tensor map that lays the 16 heads out as the operands need them)
+//            and one 128-byte bulk copy of (lse, Delta), into a 4-stage ring
+//   MMA (warp 1): S^T = K_b Q^T, dP^T = V_b dO^T -> TMEM slot u & 1;
 //            dV += P^T dO (P^T read from TMEM), dK += dS^T Q,
-//            dQ = dS K_b (dS^T in shared memory read as an MN-major operand)
-//   compute (warps 2..9, thread = key row x 64 columns):
-//            P^T = exp2(S^T scale log2e - lse log2e), causally masked, packed
-//            to bf16 into TMEM; dS^T = P^T (dP^T - Delta) to shared memory;
-//            then dQ rows (lane = column) are staged, 128B-swizzled, in the
-//            chunk's own Q/dO buffers, which the producer adds into the fp32
-//            accumulator with TMA reduce-add before refilling the stage; at the
-//            end of an item dK and dV go to their accumulators with atomics.
+//            dQ^T = K_b^T dS^T (both operands MN-major) into the dP^T columns
+//   compute (warps 2..9: warpgroup z takes the half-chunks u with u & 1 == z;
+//            thread = key row): P^T = exp2(S^T scale log2e - lse log2e),
+//            causally masked, packed to bf16 into TMEM; dS^T = P^T (dP^T -
+//            Delta) to shared memory; then the dQ^T rows are staged as plain
+//            fp32 rows in the half-chunk's own stage; at the end of an item
+//            warpgroup 0 adds dK, warpgroup 1 dV into the fp32 accumulators
+//   dQ writer (warp 10): one 8 KB bulk reduce-add per token into the fp32 dQ
+//            accumulator, then the stage goes back to the producer.
 // A last kernel scales and converts the accumulators to bf16.
 #include "kernels.cuh"
 
@@ -30,30 +33,41 @@ namespace msa {
 
 namespace {
 
-constexpr int kBwdThreads = 320;            // warp 0 TMA, warp 1 MMA, warps 2..9 compute
-constexpr int kComputeThreads = 256;
+constexpr int kGroupThreads = 128;          // a compute warpgroup
+// warp 0 TMA, warp 1 MMA, warps 2..9 compute (two warpgroups), warp 10 dQ writer
+constexpr int kBwdThreads = 64 + 2 * kGroupThreads + 32;
 constexpr int kTile = 128 * 128 * 2;
 constexpr int kHalf = kTile / 2;
+constexpr int kHc = 64;                     // columns of a half-chunk: 4 tokens x 16 heads
+constexpr int kHcTok = 4;
+constexpr int kStages = 4;
+constexpr int kTokBytes = 16 * kD * 2;      // Q (or dO) rows of one token: 4 KB
+constexpr int kStageBytes = 2 * kHcTok * kTokBytes;   // Q then dO of a half-chunk: 32 KB
+constexpr int kDqTokBytes = 16 * kD * 4;    // staged fp32 dQ rows of one token: 8 KB
+static_assert(kHcTok * kDqTokBytes <= kStageBytes, "dQ staging must fit the stage");
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr uint32_t kIdescKK = idesc_bf16(128, 128, false, false);   // both K-major
-constexpr uint32_t kIdescKM = idesc_bf16(128, 128, false, true);    // B MN-major
-constexpr uint32_t kIdescMM = idesc_bf16(128, 128, true, true);     // both MN-major
-// TMEM columns
-constexpr uint32_t kColDV = 0, kColDK = 128, kColS = 256, kColDP = 384;
+constexpr uint32_t kIdescS = idesc_bf16(128, kHc, false, false);    // S^T, dP^T (N = 64)
+constexpr uint32_t kIdescKM = idesc_bf16(128, 128, false, true);    // dV, dK: B MN-major
+constexpr uint32_t kIdescQ = idesc_bf16(128, kHc, true, true);      // dQ^T: both MN-major
+// TMEM columns: dV, dK accumulators, then two slots of (S^T | P^T, dP^T | dQ^T)
+constexpr uint32_t kColDV = 0, kColDK = 128, kColSlot = 256;
 
+// A token's Q (or dO) image: 32 rows of 128 B, row = 16 (head / 8) + 8 (D half)
+// + head % 8, 128B-swizzled.  Column n = 16 token + head of a half-chunk then
+// lies in 8-row group n / 8 at 2048 (n / 8) bytes, its D halves 1024 bytes
+// apart: a K-major operand with group stride 2048, or an MN-major one with
+// D-chunk stride 1024 and K-group stride 2048.
 struct BwdSmem {
   uint8_t k[kTile];
   uint8_t v[kTile];
-  uint8_t q[2][kTile];
-  uint8_t dout[2][kTile];
-  uint8_t dst[kTile];
-  float lse[2][128];      // natural-log lse of the chunk's 128 columns (bulk-copied)
-  float delta[2][128];
-  int tok[2][16];
-  int ntok[2];
+  uint8_t dst[2][kHc * 128 * 2];        // dS^T of each slot: 128 keys x 64 columns
+  uint8_t stage[kStages][kStageBytes];  // Q then dO token images; later dQ staging
+  float2 ld2[kStages][kHc];             // (lse log2 e, Delta) of the half-chunk's columns
+  int tok[kStages][kHcTok];
   uint64_t kv_full, kv_empty;
-  uint64_t ld_full[2], ld_empty[2];
-  uint64_t s_full, dp_full, p_full, ds_full, dv_done, dq_full, dq_free;
+  uint64_t ld_full[kStages], ld_empty[kStages], staged[kStages];
+  uint64_t s_full[2], dp_full[2], p_full[2], ds_full[2], dv_done[2], dq_full[2], dq_free[2];
+  uint64_t acc_full, acc_free;
   uint32_t tmem_base;
 };
 static_assert(sizeof(BwdSmem) <= 232448, "backward shared memory above the 227 KB limit");
@@ -185,9 +199,10 @@ __global__ void __launch_bounds__(kBwdSegment) bwd_lists_kernel(
 
 // ---------------------------------------------------------------- Delta
 
-// delta[t, i] = sum_d dout[t, i, d] * o[t, i, d]; one warp per row.
+// ld2[t, i] = (lse[t, i] log2 e, sum_d dout[t, i, d] o[t, i, d]); one warp per row.
 __global__ void bwd_delta_kernel(const __nv_bfloat16* __restrict__ o,
-                                 const __nv_bfloat16* __restrict__ dout, float* __restrict__ delta,
+                                 const __nv_bfloat16* __restrict__ dout,
+                                 const float* __restrict__ lse, float2* __restrict__ ld2,
                                  size_t rows) {
   const size_t row = (static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
@@ -205,7 +220,7 @@ __global__ void bwd_delta_kernel(const __nv_bfloat16* __restrict__ o,
   }
 #pragma unroll
   for (int m = 16; m >= 1; m >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, m);
-  if (lane == 0) delta[row] = acc;
+  if (lane == 0) ld2[row] = make_float2(lse[row] * kLog2e, acc);
 }
 
 // ---------------------------------------------------------------- convert
@@ -230,15 +245,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     sparse_bwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                       const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v,
-                      const __grid_constant__ CUtensorMap tm_do,
-                      const __grid_constant__ CUtensorMap tm_dq, const int* __restrict__ lists,
+                      const __grid_constant__ CUtensorMap tm_do, const int* __restrict__ lists,
                       const int* __restrict__ list_len, const int32_t* __restrict__ cu,
-                      const float* __restrict__ lse,
-                      const float* __restrict__ delta, const int4* __restrict__ items,
+                      const float2* __restrict__ ld2, const int4* __restrict__ items,
                       const int* __restrict__ num_items, int Hq, int Hkv, float scale,
                       float* __restrict__ dq_acc, float* __restrict__ dk_acc,
                       float* __restrict__ dv_acc, uint32_t* status) {
-  constexpr int G = 16, tpt = 8;    // heads per KV group, tokens per chunk
+  constexpr int G = 16;
   const int n_items = *num_items;
   if (static_cast<int>(blockIdx.x) >= n_items) return;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -255,17 +268,22 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   if (tid == 0) {
     mbar_init(&sm.kv_full, 1);
     mbar_init(&sm.kv_empty, 1);
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kStages; ++i) {
       mbar_init(&sm.ld_full[i], 1);
-      mbar_init(&sm.ld_empty[i], 1 + kComputeThreads);
+      mbar_init(&sm.ld_empty[i], 1);
+      mbar_init(&sm.staged[i], kGroupThreads);
     }
-    mbar_init(&sm.s_full, 1);
-    mbar_init(&sm.dp_full, 1);
-    mbar_init(&sm.p_full, kComputeThreads);
-    mbar_init(&sm.ds_full, kComputeThreads);
-    mbar_init(&sm.dv_done, 1);
-    mbar_init(&sm.dq_full, 1);
-    mbar_init(&sm.dq_free, kComputeThreads);
+    for (int z = 0; z < 2; ++z) {
+      mbar_init(&sm.s_full[z], 1);
+      mbar_init(&sm.dp_full[z], 1);
+      mbar_init(&sm.p_full[z], kGroupThreads);
+      mbar_init(&sm.ds_full[z], kGroupThreads);
+      mbar_init(&sm.dv_done[z], 1);
+      mbar_init(&sm.dq_full[z], 1);
+      mbar_init(&sm.dq_free[z], kGroupThreads);
+    }
+    mbar_init(&sm.acc_full, 1);
+    mbar_init(&sm.acc_free, 2 * kGroupThreads);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -277,6 +295,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   tc_fence_after();
   const uint32_t tmem = sm.tmem_base;
 
+  // Half-chunk u of this CTA (counted over all its items) uses stage u % 4 and
+  // TMEM slot / compute warpgroup u & 1.
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
@@ -285,34 +305,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       prefetch_tmap(&tm_k);
       prefetch_tmap(&tm_v);
     }
-    uint32_t cg = 0;
     bool alive = true;
+    uint32_t u = 0;
     int itl = 0;
-    // dQ rows of the chunk that last used a stage are staged in that stage's Q/dO
-    // buffers (8 tokens x 4 boxes of 16 heads x 32 fp32, 128B-swizzled); before the
-    // stage is refilled they are added into the fp32 accumulator by TMA reduce.
-    int pend_n[2] = {0, 0}, pend_seq0[2] = {0, 0};
-    auto flush_dq = [&](int st) {
-      if (pend_n[st] == 0) return;
-      if (lane < pend_n[st]) {
-        const int y = (pend_seq0[st] + sm.tok[st][lane]) * Hq + g * G;
-        const uint8_t* box = (lane < 4 ? sm.q[st] : sm.dout[st]) + (lane & 3) * 4 * 2048;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) tma_reduce_add_2d(&tm_dq, box + j * 2048, 32 * j, y);
-        bulk_commit_group();
-        bulk_wait_read_all();
-      }
-      __syncwarp();
-      pend_n[st] = 0;
-    };
     for (int it = blockIdx.x; alive && it < n_items; it += gridDim.x, ++itl) {
       const int4 item = items[it];
       const int s = item.x, b = item.y;
       const int seq0 = cu[s];
       const size_t li = static_cast<size_t>(it) * Hkv + g;
       const int nlist = list_len[li];
-      // lane L holds list entries 8L .. 8L+7 (chunk L)
-      int ent[tpt];
+      // lane L holds list entries 8L .. 8L+7 (half-chunks 2L and 2L+1)
+      int ent[8];
       {
         const int4* src = reinterpret_cast<const int4*>(lists + li * kBwdSegment) + 2 * lane;
         int4 e0 = make_int4(0, 0, 0, 0), e1 = e0;
@@ -335,143 +338,133 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
       }
       alive = __shfl_sync(0xffffffffu, alive ? 1 : 0, 0) != 0;
-      const int nchunks = (nlist + tpt - 1) / tpt;
-      for (int c = 0; alive && c <= nchunks; ++c) {
-        const int n = (c < nchunks) ? min(tpt, nlist - tpt * c) : 0;   // 0: end of the item
-        const int st = cg & 1;
-        if (lane == 0) alive = mbar_wait(&sm.ld_empty[st], ((cg >> 1) & 1) ^ 1, status, 22);
+      const int nh = (nlist + kHcTok - 1) / kHcTok;
+      for (int j = 0; alive && j < nh; ++j, ++u) {
+        const int n = min(kHcTok, nlist - kHcTok * j);
+        const int st = u % kStages;
+        if (lane == 0)
+          alive = mbar_wait(&sm.ld_empty[st], ((u / kStages) & 1) ^ 1, status, 22);
         alive = __shfl_sync(0xffffffffu, alive ? 1 : 0, 0) != 0;
         if (!alive) break;
-        flush_dq(st);
-        // positions of the chunk's tokens, broadcast from lane c (slots >= n repeat slot 0)
+        // positions of the half-chunk's tokens (slots >= n repeat slot 0)
         int pos = 0;
 #pragma unroll
-        for (int j = 0; j < tpt; ++j) {
-          const int pj = __shfl_sync(0xffffffffu, ent[j], c & 31);
-          if (lane == j) pos = pj;
+        for (int e = 0; e < 8; ++e) {
+          const int pe = __shfl_sync(0xffffffffu, ent[e], (j >> 1) & 31);
+          if (lane == e - 4 * (j & 1)) pos = pe;
         }
         const int pos0 = __shfl_sync(0xffffffffu, pos, 0);
-        if (lane < tpt) sm.tok[st][lane] = (lane < n) ? pos : -1;
-        if (lane == 0) {
-          sm.ntok[st] = n;
-          if (n > 0) mbar_arrive_expect_tx(&sm.ld_full[st], 2 * kTile + tpt * 2 * G * 4);
-        }
+        if (lane < kHcTok) sm.tok[st][lane] = (lane < n) ? pos : -1;
         __syncwarp();
-        if (n > 0) {
-          if (lane < tpt) {
-            const int t = seq0 + ((lane < n) ? pos : pos0);
-            const uint32_t off = lane * G * 128;
-            tma_load_3d(sm.q[st] + off, &tm_q, &sm.ld_full[st], 0, g * G, t);
-            tma_load_3d(sm.q[st] + kHalf + off, &tm_q, &sm.ld_full[st], 64, g * G, t);
-            tma_load_3d(sm.dout[st] + off, &tm_do, &sm.ld_full[st], 0, g * G, t);
-            tma_load_3d(sm.dout[st] + kHalf + off, &tm_do, &sm.ld_full[st], 64, g * G, t);
-            const size_t row = static_cast<size_t>(t) * Hq + g * G;
-            bulk_load(&sm.lse[st][lane * G], lse + row, G * 4, &sm.ld_full[st]);
-            bulk_load(&sm.delta[st][lane * G], delta + row, G * 4, &sm.ld_full[st]);
-          }
-        } else if (lane == 0) {
-          mbar_arrive(&sm.ld_full[st]);   // end of the item: no data
+        if (lane == 0) mbar_arrive_expect_tx(&sm.ld_full[st], kStageBytes + kHcTok * G * 8);
+        __syncwarp();
+        if (lane < kHcTok) {
+          // one 4 KB box per token and tensor: rows (head octet, D half, head % 8)
+          const int t = seq0 + ((lane < n) ? pos : pos0);
+          uint8_t* qb = sm.stage[st] + lane * kTokBytes;
+          tma_load_5d(qb, &tm_q, &sm.ld_full[st], 0, 0, 0, 2 * g, t);
+          tma_load_5d(qb + kStageBytes / 2, &tm_do, &sm.ld_full[st], 0, 0, 0, 2 * g, t);
+          bulk_load(&sm.ld2[st][lane * G], ld2 + static_cast<size_t>(t) * Hq + g * G, G * 8,
+                    &sm.ld_full[st]);
         }
-        pend_n[st] = n;
-        pend_seq0[st] = seq0;
-        ++cg;
       }
     }
-    // the last two stage uses may still hold staged dQ rows
-    for (int k = 0; alive && k < 2; ++k) {
-      const int st = cg & 1;
-      if (pend_n[st] > 0) {
-        if (lane == 0) alive = mbar_wait(&sm.ld_empty[st], ((cg >> 1) & 1) ^ 1, status, 23);
-        alive = __shfl_sync(0xffffffffu, alive ? 1 : 0, 0) != 0;
-        if (alive) flush_dq(st);
-      }
-      ++cg;
-    }
-    bulk_wait_all();
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (elect_one()) {
-      const uint32_t ka = smem_u32(sm.k), va = smem_u32(sm.v), sa = smem_u32(sm.dst);
-      uint32_t cg = 0, cm = 0;
+      const uint32_t ka = smem_u32(sm.k), va = smem_u32(sm.v);
+      uint32_t u0 = 0;
       bool ok = true;
-      int itl = 0;
+      int itl = 0, ii = 0;      // items, items with work
       for (int it = blockIdx.x; ok && it < n_items; it += gridDim.x, ++itl) {
+        const int nlist = list_len[static_cast<size_t>(it) * Hkv + g];
+        const int nh = (nlist + kHcTok - 1) / kHcTok;
         if (!(ok = mbar_wait(&sm.kv_full, itl & 1, status, 31))) break;
-        bool first = true;
-        while (ok) {
-          const int st = cg & 1;
-          ok = mbar_wait(&sm.ld_full[st], (cg >> 1) & 1, status, 32);
-          ++cg;
-          if (!ok) break;
-          if (sm.ntok[st] == 0) {
-            mbar_arrive(&sm.ld_empty[st]);
-            break;
-          }
-          tc_fence_after();
-          const uint32_t qa = smem_u32(sm.q[st]), da = smem_u32(sm.dout[st]);
-          // S^T = K Q^T (needs P^T of the previous chunk consumed by its dV)
-          if (cm > 0 && !(ok = mbar_wait(&sm.dv_done, (cm - 1) & 1, status, 33))) break;
-          tc_fence_after();
+        tc_fence_after();
+        for (int j = 0; ok && j <= nh; ++j) {
+          if (j < nh) {
+            // S^T and dP^T of half-chunk u into slot z
+            const uint32_t u = u0 + j;
+            const int z = u & 1, st = u % kStages;
+            const uint32_t slot = tmem + kColSlot + 128 * z;
+            if (!(ok = mbar_wait(&sm.ld_full[st], (u / kStages) & 1, status, 32))) break;
+            if (u >= 2 && !(ok = mbar_wait(&sm.dv_done[z], ((u - 2) >> 1) & 1, status, 33))) break;
+            tc_fence_after();
+            const uint32_t qa = smem_u32(sm.stage[st]), da = qa + kStageBytes / 2;
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
-            const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
-            umma_bf16(tmem + kColS, sdesc_sw128(ka + off, 16, 1024),
-                      sdesc_sw128(qa + off, 16, 1024), kIdescKK, kk > 0);
-          }
-          umma_commit(&sm.s_full);
-          // dP^T = V dO^T (needs dQ of the previous chunk drained)
-          if (cm > 0 && !(ok = mbar_wait(&sm.dq_free, (cm - 1) & 1, status, 34))) break;
-          tc_fence_after();
+            for (int kk = 0; kk < 8; ++kk) {
+              const uint32_t ao = (kk >> 2) * kHalf + (kk & 3) * 32;
+              const uint32_t bo = (kk >> 2) * 1024 + (kk & 3) * 32;
+              umma_bf16(slot, sdesc_sw128(ka + ao, 16, 1024), sdesc_sw128(qa + bo, 16, 2048),
+                        kIdescS, kk > 0);
+            }
+            umma_commit(&sm.s_full[z]);
+            if (u >= 2 && !(ok = mbar_wait(&sm.dq_free[z], ((u - 2) >> 1) & 1, status, 34))) break;
+            tc_fence_after();
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
-            const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
-            umma_bf16(tmem + kColDP, sdesc_sw128(va + off, 16, 1024),
-                      sdesc_sw128(da + off, 16, 1024), kIdescKK, kk > 0);
+            for (int kk = 0; kk < 8; ++kk) {
+              const uint32_t ao = (kk >> 2) * kHalf + (kk & 3) * 32;
+              const uint32_t bo = (kk >> 2) * 1024 + (kk & 3) * 32;
+              umma_bf16(slot + kHc, sdesc_sw128(va + ao, 16, 1024), sdesc_sw128(da + bo, 16, 2048),
+                        kIdescS, kk > 0);
+            }
+            umma_commit(&sm.dp_full[z]);
           }
-          umma_commit(&sm.dp_full);
-          // dV += P^T dO, P^T packed in TMEM: chunk columns [64h, 64h+64) at
-          // TMEM kColS + 64h .. + 32
-          if (!(ok = mbar_wait(&sm.p_full, cm & 1, status, 35))) break;
-          tc_fence_after();
+          if (j >= 1) {
+            // dV, dK and dQ^T of half-chunk v = u - 1
+            const uint32_t v = u0 + j - 1;
+            const int z = v & 1, st = v % kStages;
+            const uint32_t slot = tmem + kColSlot + 128 * z;
+            const uint32_t qa = smem_u32(sm.stage[st]), da = qa + kStageBytes / 2;
+            const uint32_t sa = smem_u32(sm.dst[z]);
+            const bool first = (j == 1);
+            if (first && ii > 0 && !(ok = mbar_wait(&sm.acc_free, (ii - 1) & 1, status, 35))) break;
+            if (!(ok = mbar_wait(&sm.p_full[z], (v >> 1) & 1, status, 36))) break;
+            tc_fence_after();
+            // dV += P^T dO (P^T packed in the slot's first 32 columns; dO read
+            // MN-major: one token = 16 K-rows per step)
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
-            const uint32_t a_t = tmem + kColS + (kk >> 2) * 64 + (kk & 3) * 8;
-            umma_bf16_tmem_a(tmem + kColDV, a_t, sdesc_sw128(da + kk * 2048, kHalf, 1024),
-                             kIdescKM, (!first || kk > 0));
-          }
-          umma_commit(&sm.dv_done);
-          // dK += dS^T Q and dQ = dS K
-          if (!(ok = mbar_wait(&sm.ds_full, cm & 1, status, 38))) break;
-          tc_fence_after();
+            for (int kk = 0; kk < 4; ++kk)
+              umma_bf16_tmem_a(tmem + kColDV, slot + kk * 8,
+                               sdesc_sw128(da + kk * kTokBytes, 1024, 2048), kIdescKM,
+                               !(first && kk == 0));
+            umma_commit(&sm.dv_done[z]);
+            if (!(ok = mbar_wait(&sm.ds_full[z], (v >> 1) & 1, status, 37))) break;
+            tc_fence_after();
+            // dK += dS^T Q
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
-            const uint32_t aoff = (kk >> 2) * kHalf + (kk & 3) * 32;
-            umma_bf16(tmem + kColDK, sdesc_sw128(sa + aoff, 16, 1024),
-                      sdesc_sw128(qa + kk * 2048, kHalf, 1024), kIdescKM, (!first || kk > 0));
-          }
+            for (int kk = 0; kk < 4; ++kk)
+              umma_bf16(tmem + kColDK, sdesc_sw128(sa + kk * 32, 16, 1024),
+                        sdesc_sw128(qa + kk * kTokBytes, 1024, 2048), kIdescKM,
+                        !(first && kk == 0));
+            // dQ^T = K^T dS^T  (M = head dim, N = the 64 columns) into the dP^T columns
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
-            const uint32_t off = kk * 2048;
-            umma_bf16(tmem + kColDP, sdesc_sw128(sa + off, kHalf, 1024),
-                      sdesc_sw128(ka + off, kHalf, 1024), kIdescMM, kk > 0);
+            for (int kk = 0; kk < 8; ++kk)
+              umma_bf16(slot + kHc, sdesc_sw128(ka + kk * 2048, kHalf, 1024),
+                        sdesc_sw128(sa + kk * 2048, kHalf, 1024), kIdescQ, kk > 0);
+            umma_commit(&sm.dq_full[z]);
           }
-          umma_commit(&sm.dq_full);
-          umma_commit(&sm.ld_empty[st]);
-          first = false;
-          ++cm;
         }
-        umma_commit(&sm.kv_empty);   // K_b / V_b free once this item's MMAs are done
+        if (!ok) break;
+        if (nh > 0) {
+          umma_commit(&sm.acc_full);   // dK, dV of this item are final
+          ++ii;
+        }
+        umma_commit(&sm.kv_empty);     // K_b / V_b free once this item's MMAs are done
+        u0 += nh;
       }
     }
-  } else {
+  } else if (warp < 2 + 2 * kGroupThreads / 32) {
     // ------------------------------------------------------------ compute
     const int cw = warp - 2;                // 0..7
+    const int z = cw >> 2;                  // warpgroup = TMEM slot: half-chunks u with u & 1 == z
     const int subp = warp & 3;              // TMEM sub-partition (lanes 32 subp ..)
-    const int h = cw >> 2;                  // column half: chunk columns [64h, 64h + 64)
-    const int r = subp * 32 + lane;         // key row; also the dQ column (token, head)
+    const int r = subp * 32 + lane;         // key row; also the head-dim row of dQ^T
     const uint32_t trow = static_cast<uint32_t>(subp * 32) << 16;
+    const uint32_t slot = tmem + kColSlot + 128 * z + trow;
     const float sl2 = scale * kLog2e;
-    uint32_t cg = 0, cm = 0;
+    uint32_t u0 = 0;
+    int ii = 0;
     bool ok = true;
     for (int it = blockIdx.x; ok && it < n_items; it += gridDim.x) {
       const int4 item = items[it];
@@ -479,140 +472,160 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const int seq0 = cu[s];
       const int len = cu[s + 1] - seq0;
       const int kp = b * kBlock + r;        // key position of this row
-      int nch = 0;
-      while (true) {
-        const int st = cg & 1;
-        if (!(ok = mbar_wait(&sm.ld_full[st], (cg >> 1) & 1, status, 41))) break;
-        ++cg;
-        const int n = sm.ntok[st];
-        if (n == 0) {
-          mbar_arrive(&sm.ld_empty[st]);
-          break;
-        }
-        int tokp[4];
+      const int nlist = list_len[static_cast<size_t>(it) * Hkv + g];
+      const int nh = (nlist + kHcTok - 1) / kHcTok;
+      for (int j = 0; j < nh; ++j) {
+        const uint32_t u = u0 + j;
+        if ((u & 1) != static_cast<uint32_t>(z)) continue;
+        const int st = u % kStages;
+        const uint32_t ph = (u >> 1) & 1;
+        if (!(ok = mbar_wait(&sm.ld_full[st], (u / kStages) & 1, status, 41))) break;
+        int tokp[kHcTok];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) tokp[i] = sm.tok[st][4 * h + i];
-        const int tokd = sm.tok[st][r >> 4];     // token of this thread's dQ column
-        const float* lsen = sm.lse[st] + 64 * h;
-        const float* dlt = sm.delta[st] + 64 * h;
+        for (int i = 0; i < kHcTok; ++i) tokp[i] = sm.tok[st][i];
+        const float4* ldv = reinterpret_cast<const float4*>(sm.ld2[st]);   // 2 columns each
 
         // ---- P^T = exp2(S^T * scale log2e - lse log2e), causally masked
-        if (!(ok = mbar_wait(&sm.s_full, cm & 1, status, 42))) break;
+        if (!(ok = mbar_wait(&sm.s_full[z], ph, status, 42))) break;
         __syncwarp();
         tc_fence_after();
-        float p[64];
+        float p[kHc];
         {
-          uint32_t sv[64];
-          tmem_ld32(tmem + kColS + trow + 64 * h, sv);
-          tmem_ld32(tmem + kColS + trow + 64 * h + 32, sv + 32);
+          uint32_t sv[kHc];
+          tmem_ld32(slot, sv);
+          tmem_ld32(slot + 32, sv + 32);
           tmem_ld_wait();
 #pragma unroll
-          for (int j4 = 0; j4 < 16; ++j4) {
-            const float4 l4 = reinterpret_cast<const float4*>(lsen)[j4];
-            const float lv[4] = {l4.x * kLog2e, l4.y * kLog2e, l4.z * kLog2e, l4.w * kLog2e};
-            const bool valid = kp <= tokp[j4 >> 2];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int j = 4 * j4 + e;
-              p[j] = valid ? ex2(fmaf(__uint_as_float(sv[j]), sl2, -lv[e])) : 0.f;
-            }
+          for (int c2 = 0; c2 < kHc / 2; ++c2) {
+            const float4 l = ldv[c2];
+            const bool valid = kp <= tokp[c2 >> 3];
+            p[2 * c2] = valid ? ex2(fmaf(__uint_as_float(sv[2 * c2]), sl2, -l.x)) : 0.f;
+            p[2 * c2 + 1] = valid ? ex2(fmaf(__uint_as_float(sv[2 * c2 + 1]), sl2, -l.z)) : 0.f;
           }
-          uint32_t pk[32];
+          uint32_t pk[kHc / 2];
 #pragma unroll
-          for (int j = 0; j < 32; ++j) pk[j] = pack_bf16x2(p[2 * j], p[2 * j + 1]);
-          tmem_st16(tmem + kColS + trow + 64 * h, pk);
-          tmem_st16(tmem + kColS + trow + 64 * h + 16, pk + 16);
+          for (int c = 0; c < kHc / 2; ++c) pk[c] = pack_bf16x2(p[2 * c], p[2 * c + 1]);
+          tmem_st16(slot, pk);
+          tmem_st16(slot + 16, pk + 16);
           tmem_st_wait();
         }
         tc_fence_before();
-        mbar_arrive(&sm.p_full);
+        mbar_arrive(&sm.p_full[z]);
 
-        // ---- dS^T = P^T (dP^T - Delta) -> shared memory (K-major rows = keys)
-        if (!(ok = mbar_wait(&sm.dp_full, cm & 1, status, 43))) break;
+        // ---- dS^T = P^T (dP^T - Delta) -> shared memory (K-major, rows = keys)
+        if (!(ok = mbar_wait(&sm.dp_full[z], ph, status, 43))) break;
         __syncwarp();
         tc_fence_after();
         {
-          uint32_t dv[64];
-          tmem_ld32(tmem + kColDP + trow + 64 * h, dv);
-          tmem_ld32(tmem + kColDP + trow + 64 * h + 32, dv + 32);
+          uint32_t dv[kHc];
+          tmem_ld32(slot + kHc, dv);
+          tmem_ld32(slot + kHc + 32, dv + 32);
           tmem_ld_wait();
 #pragma unroll
           for (int c = 0; c < 8; ++c) {
-            const float4 d0 = reinterpret_cast<const float4*>(dlt)[2 * c];
-            const float4 d1 = reinterpret_cast<const float4*>(dlt)[2 * c + 1];
-            const float dd[8] = {d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, d1.z, d1.w};
             float x[8];
 #pragma unroll
-            for (int e = 0; e < 8; ++e)
-              x[e] = p[8 * c + e] * (__uint_as_float(dv[8 * c + e]) - dd[e]);
+            for (int e2 = 0; e2 < 4; ++e2) {
+              const float4 l = ldv[4 * c + e2];
+              x[2 * e2] = p[8 * c + 2 * e2] * (__uint_as_float(dv[8 * c + 2 * e2]) - l.y);
+              x[2 * e2 + 1] =
+                  p[8 * c + 2 * e2 + 1] * (__uint_as_float(dv[8 * c + 2 * e2 + 1]) - l.w);
+            }
             uint4 pk;
             pk.x = pack_bf16x2(x[0], x[1]);
             pk.y = pack_bf16x2(x[2], x[3]);
             pk.z = pack_bf16x2(x[4], x[5]);
             pk.w = pack_bf16x2(x[6], x[7]);
-            *reinterpret_cast<uint4*>(sm.dst + h * kHalf + sw128_offset(r, c)) = pk;
+            *reinterpret_cast<uint4*>(sm.dst[z] + sw128_offset(r, c)) = pk;
           }
         }
         fence_proxy_async_smem();
         tc_fence_before();
-        mbar_arrive(&sm.ds_full);
+        mbar_arrive(&sm.ds_full[z]);
 
-        // ---- dQ rows (lane = chunk column) -> staging in this stage's Q/dO
-        // buffers (their operands are consumed once dQ is done); the producer
-        // adds them into the accumulator with TMA reduce before refilling
-        if (!(ok = mbar_wait(&sm.dq_full, cm & 1, status, 45))) break;
+        // ---- dQ^T (lane = head-dim row r, 64 columns) -> staging in this stage
+        // (its Q / dO operands are consumed once dQ^T is done): plain rows of
+        // 128 fp32 per (token, head), which the writer warp adds into the
+        // accumulator with one bulk reduce per token
+        if (!(ok = mbar_wait(&sm.dq_full[z], ph, status, 45))) break;
         __syncwarp();
         tc_fence_after();
         {
-          uint32_t qv[64];
-          tmem_ld32(tmem + kColDP + trow + 64 * h, qv);
-          tmem_ld32(tmem + kColDP + trow + 64 * h + 32, qv + 32);
+          uint32_t qv[kHc];
+          tmem_ld32(slot + kHc, qv);
+          tmem_ld32(slot + kHc + 32, qv + 32);
           tmem_ld_wait();
           tc_fence_before();
-          mbar_arrive(&sm.dq_free);           // the TMEM region is free once read
-          if (tokd >= 0) {
-            const int ti = r >> 4, hd = r & 15;
-            uint8_t* box = (ti < 4 ? sm.q[st] : sm.dout[st]) + (ti & 3) * 4 * 2048 + hd * 128;
+          mbar_arrive(&sm.dq_free[z]);          // the TMEM columns are free once read
+          uint8_t* stg = sm.stage[st] + r * 4;
 #pragma unroll
-            for (int jj = 0; jj < 2; ++jj) {
-              uint8_t* bx = box + (2 * h + jj) * 2048;
-#pragma unroll
-              for (int c = 0; c < 8; ++c)
-                *reinterpret_cast<uint4*>(bx + ((c ^ (hd & 7)) << 4)) =
-                    make_uint4(qv[32 * jj + 4 * c], qv[32 * jj + 4 * c + 1],
-                               qv[32 * jj + 4 * c + 2], qv[32 * jj + 4 * c + 3]);
-            }
+          for (int c = 0; c < kHc; ++c) {
+            const int ti = c >> 4, hd = c & 15;
+            if (tokp[ti] >= 0)
+              *reinterpret_cast<uint32_t*>(stg + ti * kDqTokBytes + hd * kD * 4) = qv[c];
           }
         }
         fence_proxy_async_smem();
-        mbar_arrive(&sm.ld_empty[st]);        // staged; done with the stage
-        ++cm;
-        ++nch;
+        mbar_arrive(&sm.staged[st]);
       }
-      // ---- dK, dV of this item (all its MMAs completed before the last dq_full)
-      if (ok && nch > 0) {
-        __syncwarp();
+      if (!ok) break;
+      u0 += nh;
+      if (nh == 0) continue;
+      // ---- dK (warpgroup 0) or dV (warpgroup 1) of this item -> fp32 accumulator
+      if (!(ok = mbar_wait(&sm.acc_full, ii & 1, status, 46))) break;
+      __syncwarp();
+      tc_fence_after();
+      {
         const bool key_valid = kp < len;
-        const size_t krow = (static_cast<size_t>(seq0 + kp) * Hkv + g) * kD + 64 * h;
+        float* dst_acc = (z == 0) ? dk_acc : dv_acc;
+        const uint32_t col = (z == 0) ? kColDK : kColDV;
+        float4* dst = reinterpret_cast<float4*>(
+            dst_acc + (static_cast<size_t>(seq0 + kp) * Hkv + g) * kD);
 #pragma unroll
-        for (int which = 0; which < 2; ++which) {
-          uint32_t a[64];
-          const uint32_t col = (which == 0 ? kColDK : kColDV) + 64 * h;
-          tmem_ld32(tmem + col + trow, a);
-          tmem_ld32(tmem + col + trow + 32, a + 32);
+        for (int c0 = 0; c0 < 128; c0 += 32) {
+          uint32_t a[32];
+          tmem_ld32(tmem + col + trow + c0, a);
           tmem_ld_wait();
           if (key_valid) {
-            float4* dst = reinterpret_cast<float4*>((which == 0 ? dk_acc : dv_acc) + krow);
 #pragma unroll
-            for (int j = 0; j < 16; ++j)
-              atomicAdd(dst + j, make_float4(__uint_as_float(a[4 * j]), __uint_as_float(a[4 * j + 1]),
-                                             __uint_as_float(a[4 * j + 2]),
-                                             __uint_as_float(a[4 * j + 3])));
+            for (int q = 0; q < 8; ++q)
+              atomicAdd(dst + c0 / 4 + q,
+                        make_float4(__uint_as_float(a[4 * q]), __uint_as_float(a[4 * q + 1]),
+                                    __uint_as_float(a[4 * q + 2]), __uint_as_float(a[4 * q + 3])));
           }
         }
-        tc_fence_before();
+      }
+      tc_fence_before();
+      mbar_arrive(&sm.acc_free);
+      ++ii;
+    }
+  } else if (lane == 0) {
+    // ------------------------------------------------------------ dQ writer
+    // Adds each staged half-chunk into the fp32 dQ accumulator (one 8 KB bulk
+    // reduce per token: G rows of 128), waits until the stage has been read
+    // and hands it back to the producer.
+    uint32_t u = 0;
+    bool ok = true;
+    for (int it = blockIdx.x; ok && it < n_items; it += gridDim.x) {
+      const int seq0 = cu[items[it].x];
+      const int nlist = list_len[static_cast<size_t>(it) * Hkv + g];
+      const int nh = (nlist + kHcTok - 1) / kHcTok;
+      for (int j = 0; j < nh; ++j, ++u) {
+        const int st = u % kStages;
+        if (!(ok = mbar_wait(&sm.staged[st], (u / kStages) & 1, status, 51))) break;
+#pragma unroll
+        for (int i = 0; i < kHcTok; ++i) {
+          const int p = sm.tok[st][i];
+          if (p >= 0)
+            bulk_reduce_add_f32(dq_acc + (static_cast<size_t>(seq0 + p) * Hq + g * G) * kD,
+                                sm.stage[st] + i * kDqTokBytes, kDqTokBytes);
+        }
+        bulk_commit_group();
+        bulk_wait_read_all();
+        mbar_arrive(&sm.ld_empty[st]);
       }
     }
+    bulk_wait_all();
   }
   tc_fence_before();
   __syncthreads();
@@ -639,7 +652,7 @@ BwdWorkspace carve_bwd_workspace(WsCursor& ws, int T, int S, int Hq, int Hkv, in
   w.num_items = ws.take<int>(1);
   w.lists = ws.take<int>(static_cast<size_t>(w.max_items) * Hkv * kBwdSegment);
   w.list_len = ws.take<int>(static_cast<size_t>(w.max_items) * Hkv);
-  w.delta = ws.take<float>(static_cast<size_t>(T) * Hq);
+  w.ld2 = ws.take<float2>(static_cast<size_t>(T) * Hq);
   w.dq_acc = ws.take<float>(static_cast<size_t>(T) * Hq * kD);
   w.dk_acc = ws.take<float>(static_cast<size_t>(T) * Hkv * kD);
   w.dv_acc = ws.take<float>(static_cast<size_t>(T) * Hkv * kD);
@@ -655,18 +668,18 @@ msa_status_t launch_sparse_bwd(const void* q, const void* k, const void* v, cons
   if (G != 16)
     return fail(MSA_ERR_UNSUPPORTED, "backward supports Hq/Hkv = 16 (got %d)", G);
   CUtensorMap tq, tk, tv, tdo;
-  const uint64_t dq3[3] = {static_cast<uint64_t>(kD), static_cast<uint64_t>(Hq),
-                           static_cast<uint64_t>(T)};
+  // Q / dO as (d % 64, head % 8, d / 64, head / 8, token): a (64, 8, 2, 2, 1)
+  // box is one token's 16 heads of KV group g in the order the kernel reads.
+  const uint64_t dq5[5] = {64, 8, 2, static_cast<uint64_t>(Hq / 8), static_cast<uint64_t>(T)};
+  const uint64_t sq5[4] = {static_cast<uint64_t>(kD) * 2, 128, 8 * static_cast<uint64_t>(kD) * 2,
+                           static_cast<uint64_t>(Hq) * kD * 2};
+  const uint32_t bq5[5] = {64, 8, 2, 2, 1};
   const uint64_t dkv3[3] = {static_cast<uint64_t>(kD), static_cast<uint64_t>(Hkv),
                             static_cast<uint64_t>(T)};
-  const uint32_t bq[3] = {64, static_cast<uint32_t>(G), 1};
   const uint32_t bkv[3] = {64, 1, 128};
-  CUtensorMap tdq;
-  const uint64_t dacc[2] = {static_cast<uint64_t>(kD), static_cast<uint64_t>(T) * Hq};
-  const uint32_t bacc[2] = {32, 16};
-  if (!make_tmap_bf16(&tq, q, 3, dq3, bq) || !make_tmap_bf16(&tdo, dout, 3, dq3, bq) ||
-      !make_tmap_bf16(&tk, k, 3, dkv3, bkv) || !make_tmap_bf16(&tv, v, 3, dkv3, bkv) ||
-      !make_tmap_f32(&tdq, ws.dq_acc, 2, dacc, bacc))
+  if (!make_tmap_bf16_strided(&tq, q, 5, dq5, sq5, bq5) ||
+      !make_tmap_bf16_strided(&tdo, dout, 5, dq5, sq5, bq5) ||
+      !make_tmap_bf16(&tk, k, 3, dkv3, bkv) || !make_tmap_bf16(&tv, v, 3, dkv3, bkv))
     return fail(MSA_ERR_CUDA, "cuTensorMapEncodeTiled failed for the backward");
   uint32_t* st = status_word();
 
@@ -681,7 +694,7 @@ msa_status_t launch_sparse_bwd(const void* q, const void* k, const void* v, cons
   {
     TraceScope trace_("bwd_delta_kernel", stream);
     bwd_delta_kernel<<<static_cast<unsigned>((rows * 32 + 255) / 256), 256, 0, stream>>>(
-        static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dout), ws.delta,
+        static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dout), lse, ws.ld2,
         rows);
   }
   {
@@ -711,8 +724,7 @@ msa_status_t launch_sparse_bwd(const void* q, const void* k, const void* v, cons
   {
     TraceScope trace_("sparse_bwd_kernel", stream);
     sparse_bwd_kernel<<<grid, kBwdThreads, smem, stream>>>(
-        tq, tk, tv, tdo, tdq, ws.lists, ws.list_len, cu, lse, ws.delta, ws.items, ws.num_items, Hq,
-        Hkv, scale,
+        tq, tk, tv, tdo, ws.lists, ws.list_len, cu, ws.ld2, ws.items, ws.num_items, Hq, Hkv, scale,
         ws.dq_acc, ws.dk_acc, ws.dv_acc, st);
   }
   e = check_launch("sparse_bwd_kernel");
