@@ -12,20 +12,22 @@
 // 64 columns.  A pre-pass (bwd_lists_kernel) lists, per item, those tokens
 // (one thread per candidate, ballot compaction); another packs (lse log2 e,
 // Delta) per query row.
-//   producer (warp 0): per token one 4 KB tensor load of Q, one of dO (a 5-D
-//            tensor map that lays the 16 heads out as the operands need them)
-//            and one 128-byte bulk copy of (lse, Delta), into a 4-stage ring
+//   producers (warp 0: K_b / V_b and the even half-chunks; warp 10: the odd
+//            ones; one warp alone cannot issue the copies fast enough): per
+//            token one 4 KB tensor load of Q, one of dO (a 5-D tensor map that
+//            lays the 16 heads out as the operands need them) and one 128-byte
+//            bulk copy of (lse, Delta), into a 4-stage ring
 //   MMA (warp 1): S^T = K_b Q^T, dP^T = V_b dO^T -> TMEM slot u & 1;
-//            dV += P^T dO (P^T read from TMEM), dK += dS^T Q,
-//            dQ^T = K_b^T dS^T (both operands MN-major) into the dP^T columns
+//            dV += P^T dO (P^T read from TMEM), dK += dS^T Q (after which the
+//            stage is free), dQ^T = K_b^T dS^T (both operands MN-major) into
+//            the dP^T columns
 //   compute (warps 2..9: warpgroup z takes the half-chunks u with u & 1 == z;
 //            thread = key row): P^T = exp2(S^T scale log2e - lse log2e),
 //            causally masked, packed to bf16 into TMEM; dS^T = P^T (dP^T -
-//            Delta) to shared memory; then the dQ^T rows are staged as plain
-//            fp32 rows in the half-chunk's own stage; at the end of an item
-//            warpgroup 0 adds dK, warpgroup 1 dV into the fp32 accumulators
-//   dQ writer (warp 10): one 8 KB bulk reduce-add per token into the fp32 dQ
-//            accumulator, then the stage goes back to the producer.
+//            Delta) to shared memory; then the dQ^T rows are added into the
+//            fp32 dQ accumulator with reductions straight from registers (a
+//            warp covers 32 consecutive floats of a row); at the end of an item
+//            warpgroup 0 adds dK, warpgroup 1 dV into their accumulators.
 // A last kernel scales and converts the accumulators to bf16.
 #include "kernels.cuh"
 
@@ -34,8 +36,11 @@ namespace msa {
 namespace {
 
 constexpr int kGroupThreads = 128;          // a compute warpgroup
-// warp 0 TMA, warp 1 MMA, warps 2..9 compute (two warpgroups), warp 10 dQ writer
+// warp 0 TMA (even half-chunks, K/V), warp 1 MMA, warps 2..9 compute (two
+// warpgroups), warp 10 TMA (odd half-chunks): one TMA-issuing warp cannot keep
+// up with one 4 KB copy per token and tensor
 constexpr int kBwdThreads = 64 + 2 * kGroupThreads + 32;
+constexpr int kLoaderWarp1 = 2 + 2 * kGroupThreads / 32;
 constexpr int kTile = 128 * 128 * 2;
 constexpr int kHalf = kTile / 2;
 constexpr int kHc = 64;                     // columns of a half-chunk: 4 tokens x 16 heads
@@ -43,8 +48,6 @@ constexpr int kHcTok = 4;
 constexpr int kStages = 4;
 constexpr int kTokBytes = 16 * kD * 2;      // Q (or dO) rows of one token: 4 KB
 constexpr int kStageBytes = 2 * kHcTok * kTokBytes;   // Q then dO of a half-chunk: 32 KB
-constexpr int kDqTokBytes = 16 * kD * 4;    // staged fp32 dQ rows of one token: 8 KB
-static_assert(kHcTok * kDqTokBytes <= kStageBytes, "dQ staging must fit the stage");
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr uint32_t kIdescS = idesc_bf16(128, kHc, false, false);    // S^T, dP^T (N = 64)
 constexpr uint32_t kIdescKM = idesc_bf16(128, 128, false, true);    // dV, dK: B MN-major
@@ -61,11 +64,11 @@ struct BwdSmem {
   uint8_t k[kTile];
   uint8_t v[kTile];
   uint8_t dst[2][kHc * 128 * 2];        // dS^T of each slot: 128 keys x 64 columns
-  uint8_t stage[kStages][kStageBytes];  // Q then dO token images; later dQ staging
+  uint8_t stage[kStages][kStageBytes];  // Q then dO token images
   float2 ld2[kStages][kHc];             // (lse log2 e, Delta) of the half-chunk's columns
   int tok[kStages][kHcTok];
   uint64_t kv_full, kv_empty;
-  uint64_t ld_full[kStages], ld_empty[kStages], staged[kStages];
+  uint64_t ld_full[kStages], ld_empty[kStages];
   uint64_t s_full[2], dp_full[2], p_full[2], ds_full[2], dv_done[2], dq_full[2], dq_free[2];
   uint64_t acc_full, acc_free;
   uint32_t tmem_base;
@@ -76,6 +79,10 @@ __device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
+}
+
+__device__ __forceinline__ void red_add_f32(float* p, float v) {
+  asm volatile("red.global.add.f32 [%0], %1;" ::"l"(p), "f"(v) : "memory");
 }
 
 __device__ __forceinline__ void umma_bf16_tmem_a(uint32_t d_tmem, uint32_t a_tmem,
@@ -271,7 +278,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     for (int i = 0; i < kStages; ++i) {
       mbar_init(&sm.ld_full[i], 1);
       mbar_init(&sm.ld_empty[i], 1);
-      mbar_init(&sm.staged[i], kGroupThreads);
     }
     for (int z = 0; z < 2; ++z) {
       mbar_init(&sm.s_full[z], 1);
@@ -297,8 +303,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
   // Half-chunk u of this CTA (counted over all its items) uses stage u % 4 and
   // TMEM slot / compute warpgroup u & 1.
-  if (warp == 0) {
-    // ------------------------------------------------------------ producer
+  if (warp == 0 || warp == kLoaderWarp1) {
+    // ------------------------------------------------------------ producers
+    // warp 0 loads K_b / V_b and the even half-chunks, kLoaderWarp1 the odd ones
+    const uint32_t par = (warp == 0) ? 0u : 1u;
     if (lane == 0) {
       prefetch_tmap(&tm_q);
       prefetch_tmap(&tm_do);
@@ -326,7 +334,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         ent[0] = e0.x; ent[1] = e0.y; ent[2] = e0.z; ent[3] = e0.w;
         ent[4] = e1.x; ent[5] = e1.y; ent[6] = e1.z; ent[7] = e1.w;
       }
-      if (lane == 0) {
+      if (lane == 0 && par == 0) {
         alive = mbar_wait(&sm.kv_empty, (itl & 1) ^ 1, status, 21);
         if (alive) {
           mbar_arrive_expect_tx(&sm.kv_full, 2 * kTile);
@@ -340,6 +348,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       alive = __shfl_sync(0xffffffffu, alive ? 1 : 0, 0) != 0;
       const int nh = (nlist + kHcTok - 1) / kHcTok;
       for (int j = 0; alive && j < nh; ++j, ++u) {
+        if ((u & 1u) != par) continue;
         const int n = min(kHcTok, nlist - kHcTok * j);
         const int st = u % kStages;
         if (lane == 0)
@@ -437,6 +446,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
               umma_bf16(tmem + kColDK, sdesc_sw128(sa + kk * 32, 16, 1024),
                         sdesc_sw128(qa + kk * kTokBytes, 1024, 2048), kIdescKM,
                         !(first && kk == 0));
+            umma_commit(&sm.ld_empty[st]);   // Q / dO of the stage consumed
             // dQ^T = K^T dS^T  (M = head dim, N = the 64 columns) into the dP^T columns
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk)
@@ -454,7 +464,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         u0 += nh;
       }
     }
-  } else if (warp < 2 + 2 * kGroupThreads / 32) {
+  } else {
     // ------------------------------------------------------------ compute
     const int cw = warp - 2;                // 0..7
     const int z = cw >> 2;                  // warpgroup = TMEM slot: half-chunks u with u & 1 == z
@@ -543,10 +553,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         tc_fence_before();
         mbar_arrive(&sm.ds_full[z]);
 
-        // ---- dQ^T (lane = head-dim row r, 64 columns) -> staging in this stage
-        // (its Q / dO operands are consumed once dQ^T is done): plain rows of
-        // 128 fp32 per (token, head), which the writer warp adds into the
-        // accumulator with one bulk reduce per token
+        // ---- dQ^T (lane = head-dim row r, 64 columns) added into the fp32
+        // accumulator: per column a warp adds 32 consecutive floats of one row
         if (!(ok = mbar_wait(&sm.dq_full[z], ph, status, 45))) break;
         __syncwarp();
         tc_fence_after();
@@ -557,16 +565,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           tmem_ld_wait();
           tc_fence_before();
           mbar_arrive(&sm.dq_free[z]);          // the TMEM columns are free once read
-          uint8_t* stg = sm.stage[st] + r * 4;
 #pragma unroll
-          for (int c = 0; c < kHc; ++c) {
-            const int ti = c >> 4, hd = c & 15;
-            if (tokp[ti] >= 0)
-              *reinterpret_cast<uint32_t*>(stg + ti * kDqTokBytes + hd * kD * 4) = qv[c];
+          for (int ti = 0; ti < kHcTok; ++ti) {
+            if (tokp[ti] < 0) continue;
+            float* row = dq_acc + (static_cast<size_t>(seq0 + tokp[ti]) * Hq + g * G) * kD + r;
+#pragma unroll
+            for (int hd = 0; hd < G; ++hd) red_add_f32(row + hd * kD, __uint_as_float(qv[16 * ti + hd]));
           }
         }
-        fence_proxy_async_smem();
-        mbar_arrive(&sm.staged[st]);
       }
       if (!ok) break;
       u0 += nh;
@@ -599,33 +605,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       mbar_arrive(&sm.acc_free);
       ++ii;
     }
-  } else if (lane == 0) {
-    // ------------------------------------------------------------ dQ writer
-    // Adds each staged half-chunk into the fp32 dQ accumulator (one 8 KB bulk
-    // reduce per token: G rows of 128), waits until the stage has been read
-    // and hands it back to the producer.
-    uint32_t u = 0;
-    bool ok = true;
-    for (int it = blockIdx.x; ok && it < n_items; it += gridDim.x) {
-      const int seq0 = cu[items[it].x];
-      const int nlist = list_len[static_cast<size_t>(it) * Hkv + g];
-      const int nh = (nlist + kHcTok - 1) / kHcTok;
-      for (int j = 0; j < nh; ++j, ++u) {
-        const int st = u % kStages;
-        if (!(ok = mbar_wait(&sm.staged[st], (u / kStages) & 1, status, 51))) break;
-#pragma unroll
-        for (int i = 0; i < kHcTok; ++i) {
-          const int p = sm.tok[st][i];
-          if (p >= 0)
-            bulk_reduce_add_f32(dq_acc + (static_cast<size_t>(seq0 + p) * Hq + g * G) * kD,
-                                sm.stage[st] + i * kDqTokBytes, kDqTokBytes);
-        }
-        bulk_commit_group();
-        bulk_wait_read_all();
-        mbar_arrive(&sm.ld_empty[st]);
-      }
-    }
-    bulk_wait_all();
   }
   tc_fence_before();
   __syncthreads();
