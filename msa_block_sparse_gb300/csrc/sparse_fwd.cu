@@ -61,6 +61,32 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
+// Three-input maximum (sm_100 and later).
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// Two-lane fp32 fused multiply-add and add (sm_100 and later).
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+  float2 d;
+  asm("{\n .reg .b64 ra, rb, rc, rd;\n mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %5};\n"
+      " mov.b64 rc, {%6, %7};\n fma.rn.f32x2 rd, ra, rb, rc;\n mov.b64 {%0, %1}, rd;\n}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+  return d;
+}
+
+__device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
+  float2 d;
+  asm("{\n .reg .b64 ra, rb, rd;\n mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %5};\n"
+      " add.rn.f32x2 rd, ra, rb;\n mov.b64 {%0, %1}, rd;\n}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
+}
+
 __device__ __forceinline__ void umma_bf16_tmem_a(uint32_t d_tmem, uint32_t a_tmem,
                                                  uint64_t b_desc, uint32_t idesc,
                                                  uint32_t accumulate) {
@@ -340,23 +366,44 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         const int kmax = (b == t.qb) ? (pos & (kBlock - 1)) - 64 * h : 63;
         bool resc = false;
         float mu = m, rs = 0.f;
-        float p[64];
+        uint32_t pk[32];
         if (selected && kmax >= 0) {
-          float mx = -INFINITY;
+          float x[64];
 #pragma unroll
-          for (int j = 0; j < 64; ++j)
-            if (j <= kmax) mx = fmaxf(mx, __uint_as_float(sv[j]));
+          for (int j = 0; j < 64; ++j) x[j] = __uint_as_float(sv[j]);
+          if (kmax < 63) {                    // own block: keys after the query are masked
+#pragma unroll
+            for (int j = 0; j < 64; ++j) x[j] = (j <= kmax) ? x[j] : -INFINITY;
+          }
+          // row max: eight independent chains of three-input maxima
+          float mx8[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const float* xi = x + 8 * i;
+            mx8[i] = fmaxf(max3f(max3f(max3f(xi[0], xi[1], xi[2]), xi[3], xi[4]), xi[5], xi[6]),
+                           xi[7]);
+          }
+          const float mx = max3f(max3f(mx8[0], mx8[1], mx8[2]), max3f(mx8[3], mx8[4], mx8[5]),
+                                 fmaxf(mx8[6], mx8[7]));
           const float mnew = fmaxf(m, mx * sl2);
           resc = mnew > m + kRescaleThreshold;
           mu = resc ? mnew : m;
+          // p = exp2(s scale log2e - mu), two lanes of fp32 per instruction
+          const float2 sl2v = make_float2(sl2, sl2), nmu = make_float2(-mu, -mu);
+          float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                           make_float2(0.f, 0.f)};
 #pragma unroll
-          for (int j = 0; j < 64; ++j) {
-            p[j] = (j <= kmax) ? ex2(fmaf(__uint_as_float(sv[j]), sl2, -mu)) : 0.f;
-            rs += p[j];
+          for (int j2 = 0; j2 < 32; ++j2) {
+            const float2 y = ffma2(make_float2(x[2 * j2], x[2 * j2 + 1]), sl2v, nmu);
+            const float2 pe = make_float2(ex2(y.x), ex2(y.y));
+            acc[j2 & 3] = fadd2(acc[j2 & 3], pe);
+            pk[j2] = pack_bf16x2(pe.x, pe.y);
           }
+          const float2 a01 = fadd2(fadd2(acc[0], acc[1]), fadd2(acc[2], acc[3]));
+          rs = a01.x + a01.y;
         } else {
 #pragma unroll
-          for (int j = 0; j < 64; ++j) p[j] = 0.f;
+          for (int j = 0; j < 32; ++j) pk[j] = 0u;
         }
         const bool need = resc && m != -INFINITY;
         if (__any_sync(0xffffffffu, need)) {
@@ -381,9 +428,6 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           l = (m == -INFINITY) ? rs : (resc ? l * ex2(m - mu) : l) + rs;
           m = mu;
         }
-        uint32_t pk[32];
-#pragma unroll
-        for (int j = 0; j < 32; ++j) pk[j] = pack_bf16x2(p[2 * j], p[2 * j + 1]);
         tmem_st16(sbuf, pk);
         tmem_st16(sbuf + 16, pk + 16);
         tmem_st_wait();
