@@ -50,7 +50,7 @@ struct BwdWorkspace {
   int max_items;
   int* lists;          // [max_items, Hkv, kBwdSegment] positions that selected the item's block
   int* list_len;       // [max_items, Hkv]
-  float2* ld2;         // [T, Hq]  (lse log2(e), rowsum(dout * o))
+  float* lsd;          // [T, Hkv, 2, 16]  -lse log2(e) of the group's 16 rows, then -rowsum(dout * o)
   float* dq_acc;       // [T, Hq, 128] fp32
   float* dk_acc;       // [T, Hkv, 128] fp32
   float* dv_acc;       // [T, Hkv, 128] fp32

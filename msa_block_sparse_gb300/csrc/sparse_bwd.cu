@@ -65,7 +65,7 @@ struct BwdSmem {
   uint8_t v[kTile];
   uint8_t dst[2][kHc * 128 * 2];        // dS^T of each slot: 128 keys x 64 columns
   uint8_t stage[kStages][kStageBytes];  // Q then dO token images
-  float2 ld2[kStages][kHc];             // (lse log2 e, Delta) of the half-chunk's columns
+  float lsd[kStages][2 * kHc];          // per token: -lse log2 e of its 16 heads, then -Delta
   int tok[kStages][kHcTok];
   uint64_t kv_full, kv_empty;
   uint64_t ld_full[kStages], ld_empty[kStages];
@@ -206,10 +206,11 @@ __global__ void __launch_bounds__(kBwdSegment) bwd_lists_kernel(
 
 // ---------------------------------------------------------------- Delta
 
-// ld2[t, i] = (lse[t, i] log2 e, sum_d dout[t, i, d] o[t, i, d]); one warp per row.
+// For query row (t, 16 g + j): lsd[32 (t Hkv + g) + j] = -lse log2 e and
+// lsd[32 (t Hkv + g) + 16 + j] = -sum_d dout o (= -Delta); one warp per row.
 __global__ void bwd_delta_kernel(const __nv_bfloat16* __restrict__ o,
                                  const __nv_bfloat16* __restrict__ dout,
-                                 const float* __restrict__ lse, float2* __restrict__ ld2,
+                                 const float* __restrict__ lse, float* __restrict__ lsd,
                                  size_t rows) {
   const size_t row = (static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
@@ -227,7 +228,11 @@ __global__ void bwd_delta_kernel(const __nv_bfloat16* __restrict__ o,
   }
 #pragma unroll
   for (int m = 16; m >= 1; m >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, m);
-  if (lane == 0) ld2[row] = make_float2(lse[row] * kLog2e, acc);
+  if (lane == 0) {
+    const size_t j = row & 15, base = (row - j) * 2 + j;
+    lsd[base] = -lse[row] * kLog2e;
+    lsd[base + 16] = -acc;
+  }
 }
 
 // ---------------------------------------------------------------- convert
@@ -254,7 +259,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                       const __grid_constant__ CUtensorMap tm_v,
                       const __grid_constant__ CUtensorMap tm_do, const int* __restrict__ lists,
                       const int* __restrict__ list_len, const int32_t* __restrict__ cu,
-                      const float2* __restrict__ ld2, const int4* __restrict__ items,
+                      const float* __restrict__ lsd, const int4* __restrict__ items,
                       const int* __restrict__ num_items, int Hq, int Hkv, float scale,
                       float* __restrict__ dq_acc, float* __restrict__ dk_acc,
                       float* __restrict__ dv_acc, uint32_t* status) {
@@ -373,7 +378,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           uint8_t* qb = sm.stage[st] + lane * kTokBytes;
           tma_load_5d(qb, &tm_q, &sm.ld_full[st], 0, 0, 0, 2 * g, t);
           tma_load_5d(qb + kStageBytes / 2, &tm_do, &sm.ld_full[st], 0, 0, 0, 2 * g, t);
-          bulk_load(&sm.ld2[st][lane * G], ld2 + static_cast<size_t>(t) * Hq + g * G, G * 8,
+          bulk_load(&sm.lsd[st][lane * 2 * G], lsd + (static_cast<size_t>(t) * Hq + g * G) * 2, G * 8,
                     &sm.ld_full[st]);
         }
       }
@@ -493,7 +498,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         int tokp[kHcTok];
 #pragma unroll
         for (int i = 0; i < kHcTok; ++i) tokp[i] = sm.tok[st][i];
-        const float4* ldv = reinterpret_cast<const float4*>(sm.ld2[st]);   // 2 columns each
+        const float* ls = sm.lsd[st];
 
         // ---- P^T = exp2(S^T * scale log2e - lse log2e), causally masked
         if (!(ok = mbar_wait(&sm.s_full[z], ph, status, 42))) break;
@@ -505,12 +510,31 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           tmem_ld32(slot, sv);
           tmem_ld32(slot + 32, sv + 32);
           tmem_ld_wait();
+          const float2 sl2v = make_float2(sl2, sl2);
 #pragma unroll
-          for (int c2 = 0; c2 < kHc / 2; ++c2) {
-            const float4 l = ldv[c2];
-            const bool valid = kp <= tokp[c2 >> 3];
-            p[2 * c2] = valid ? ex2(fmaf(__uint_as_float(sv[2 * c2]), sl2, -l.x)) : 0.f;
-            p[2 * c2 + 1] = valid ? ex2(fmaf(__uint_as_float(sv[2 * c2 + 1]), sl2, -l.z)) : 0.f;
+          for (int c4 = 0; c4 < kHc / 4; ++c4) {   // columns 4 c4 .. 4 c4 + 3 of token c4 / 4
+            const float4 nl = *reinterpret_cast<const float4*>(ls + 32 * (c4 >> 2) + 4 * (c4 & 3));
+            const float2 y0 = ffma2(make_float2(__uint_as_float(sv[4 * c4]), __uint_as_float(sv[4 * c4 + 1])),
+                                    sl2v, make_float2(nl.x, nl.y));
+            const float2 y1 = ffma2(make_float2(__uint_as_float(sv[4 * c4 + 2]), __uint_as_float(sv[4 * c4 + 3])),
+                                    sl2v, make_float2(nl.z, nl.w));
+            p[4 * c4] = ex2(y0.x);
+            p[4 * c4 + 1] = ex2(y0.y);
+            p[4 * c4 + 2] = ex2(y1.x);
+            p[4 * c4 + 3] = ex2(y1.y);
+          }
+          // causal mask (keys after the query: only in the token's own block)
+          // and padding slots (token -1)
+          bool mask[kHcTok];
+          bool any = false;
+#pragma unroll
+          for (int i = 0; i < kHcTok; ++i) {
+            mask[i] = kp > tokp[i];
+            any |= mask[i];
+          }
+          if (__any_sync(0xffffffffu, any)) {
+#pragma unroll
+            for (int c = 0; c < kHc; ++c) p[c] = mask[c >> 4] ? 0.f : p[c];
           }
           uint32_t pk[kHc / 2];
 #pragma unroll
@@ -535,11 +559,19 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           for (int c = 0; c < 8; ++c) {
             float x[8];
 #pragma unroll
-            for (int e2 = 0; e2 < 4; ++e2) {
-              const float4 l = ldv[4 * c + e2];
-              x[2 * e2] = p[8 * c + 2 * e2] * (__uint_as_float(dv[8 * c + 2 * e2]) - l.y);
-              x[2 * e2 + 1] =
-                  p[8 * c + 2 * e2 + 1] * (__uint_as_float(dv[8 * c + 2 * e2 + 1]) - l.w);
+            for (int e4 = 0; e4 < 2; ++e4) {
+              const int c0 = 8 * c + 4 * e4;   // token c0 / 16, heads c0 % 16 ..
+              const float4 nd = *reinterpret_cast<const float4*>(ls + 32 * (c0 >> 4) + 16 + (c0 & 15));
+              const float2 t0 = fadd2(make_float2(__uint_as_float(dv[c0]), __uint_as_float(dv[c0 + 1])),
+                                      make_float2(nd.x, nd.y));
+              const float2 t1 = fadd2(make_float2(__uint_as_float(dv[c0 + 2]), __uint_as_float(dv[c0 + 3])),
+                                      make_float2(nd.z, nd.w));
+              const float2 x0 = fmul2(make_float2(p[c0], p[c0 + 1]), t0);
+              const float2 x1 = fmul2(make_float2(p[c0 + 2], p[c0 + 3]), t1);
+              x[4 * e4] = x0.x;
+              x[4 * e4 + 1] = x0.y;
+              x[4 * e4 + 2] = x1.x;
+              x[4 * e4 + 3] = x1.y;
             }
             uint4 pk;
             pk.x = pack_bf16x2(x[0], x[1]);
@@ -631,7 +663,7 @@ BwdWorkspace carve_bwd_workspace(WsCursor& ws, int T, int S, int Hq, int Hkv, in
   w.num_items = ws.take<int>(1);
   w.lists = ws.take<int>(static_cast<size_t>(w.max_items) * Hkv * kBwdSegment);
   w.list_len = ws.take<int>(static_cast<size_t>(w.max_items) * Hkv);
-  w.ld2 = ws.take<float2>(static_cast<size_t>(T) * Hq);
+  w.lsd = ws.take<float>(static_cast<size_t>(T) * Hq * 2);
   w.dq_acc = ws.take<float>(static_cast<size_t>(T) * Hq * kD);
   w.dk_acc = ws.take<float>(static_cast<size_t>(T) * Hkv * kD);
   w.dv_acc = ws.take<float>(static_cast<size_t>(T) * Hkv * kD);
@@ -673,7 +705,7 @@ msa_status_t launch_sparse_bwd(const void* q, const void* k, const void* v, cons
   {
     TraceScope trace_("bwd_delta_kernel", stream);
     bwd_delta_kernel<<<static_cast<unsigned>((rows * 32 + 255) / 256), 256, 0, stream>>>(
-        static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dout), lse, ws.ld2,
+        static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dout), lse, ws.lsd,
         rows);
   }
   {
@@ -703,7 +735,7 @@ msa_status_t launch_sparse_bwd(const void* q, const void* k, const void* v, cons
   {
     TraceScope trace_("sparse_bwd_kernel", stream);
     sparse_bwd_kernel<<<grid, kBwdThreads, smem, stream>>>(
-        tq, tk, tv, tdo, ws.lists, ws.list_len, cu, ws.ld2, ws.items, ws.num_items, Hq, Hkv, scale,
+        tq, tk, tv, tdo, ws.lists, ws.list_len, cu, ws.lsd, ws.items, ws.num_items, Hq, Hkv, scale,
         ws.dq_acc, ws.dk_acc, ws.dv_acc, st);
   }
   e = check_launch("sparse_bwd_kernel");
