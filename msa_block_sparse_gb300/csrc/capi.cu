@@ -502,7 +502,6 @@ msa_status_t msa_sparse_attn_bwd(const void* q, const void* k, const void* v, co
   WsCursor ws(workspace);
   BwdWorkspace bw = carve_bwd_workspace(ws, T, S, Hq, Hkv, max_seqlen);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  MSA_TRY(launch_plan(bw.plan, cu_seqlens, S, max_seqlen, st));
   return launch_sparse_bwd(q, k, v, o, dout, lse, sel, cu_seqlens, S, T, Hq, Hkv, max_seqlen,
                            scale, bw, dq, dk, dv, st);
 }

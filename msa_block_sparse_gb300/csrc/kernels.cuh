@@ -44,7 +44,6 @@ msa_status_t launch_sparse_fwd(const void* q, const void* k, const void* v, cons
 constexpr int kBwdSegment = 256;    // window of candidate query positions per work item
 
 struct BwdWorkspace {
-  Plan plan;
   int4* items;         // [max_items] (s, b, token_begin, token_end) in sequence positions
   int* num_items;      // [1]
   int max_items;

@@ -102,8 +102,10 @@ __device__ __forceinline__ void umma_bf16_tmem_a(uint32_t d_tmem, uint32_t a_tme
 // One CTA.  Pairs (window w, sequence s) in w-major order; pair (w, s) holds the
 // key blocks b that some query of window w can select: 128 b < min(len, (w+1) W).
 // Each becomes an item (s, b, first position, end position) of that window.
+// A sequence longer than max_seqlen (or of negative length) is flagged in the
+// status word and clipped.
 __global__ void __launch_bounds__(1024) bwd_items_kernel(const int32_t* __restrict__ cu, int S,
-                                                         int num_windows,
+                                                         int max_seqlen, int num_windows,
                                                          int4* __restrict__ items,
                                                          int* __restrict__ num_items,
                                                          int max_items, uint32_t* status) {
@@ -119,6 +121,10 @@ __global__ void __launch_bounds__(1024) bwd_items_kernel(const int32_t* __restri
       w = static_cast<int>(pi / S);
       s = static_cast<int>(pi % S);
       len = cu[s + 1] - cu[s];
+      if (len < 0 || len > max_seqlen) {
+        if (w == 0) atomicOr(status, kStatusBounds);
+        len = len < 0 ? 0 : max_seqlen;
+      }
       const int w0 = w * kBwdSegment;
       if (len > w0) {
         const int hi = min(len, w0 + kBwdSegment);
@@ -207,42 +213,77 @@ __global__ void __launch_bounds__(kBwdSegment) bwd_lists_kernel(
 // ---------------------------------------------------------------- Delta
 
 // For query row (t, 16 g + j): lsd[32 (t Hkv + g) + j] = -lse log2 e and
-// lsd[32 (t Hkv + g) + 16 + j] = -sum_d dout o (= -Delta); one warp per row.
-__global__ void bwd_delta_kernel(const __nv_bfloat16* __restrict__ o,
-                                 const __nv_bfloat16* __restrict__ dout,
-                                 const float* __restrict__ lse, float* __restrict__ lsd,
-                                 size_t rows) {
-  const size_t row = (static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-  const int lane = threadIdx.x & 31;
-  if (row >= rows) return;
-  const uint2 a = reinterpret_cast<const uint2*>(o + row * kD)[lane];
-  const uint2 b = reinterpret_cast<const uint2*>(dout + row * kD)[lane];
-  const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a);
-  const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&b);
-  float acc = 0.f;
+// lsd[32 (t Hkv + g) + 16 + j] = -sum_d dout o (= -Delta).  16 lanes per row
+// (16-byte loads), kDeltaRows rows per thread with all loads issued first.
+constexpr int kDeltaRows = 4;
+__global__ void __launch_bounds__(256) bwd_delta_kernel(const __nv_bfloat16* __restrict__ o,
+                                                        const __nv_bfloat16* __restrict__ dout,
+                                                        const float* __restrict__ lse,
+                                                        float* __restrict__ lsd, size_t rows) {
+  const int sub = threadIdx.x & 15;
+  const size_t row0 =
+      (static_cast<size_t>(blockIdx.x) * (blockDim.x >> 4) + (threadIdx.x >> 4)) * kDeltaRows;
+  uint4 a[kDeltaRows], b[kDeltaRows];
+  float ls[kDeltaRows];
 #pragma unroll
-  for (int j = 0; j < 2; ++j) {
-    const float2 x = __bfloat1622float2(a2[j]);
-    const float2 y = __bfloat1622float2(b2[j]);
-    acc = fmaf(x.x, y.x, fmaf(x.y, y.y, acc));
+  for (int i = 0; i < kDeltaRows; ++i) {
+    const size_t row = row0 + i;
+    ls[i] = 0.f;
+    if (row < rows) {
+      a[i] = __ldcs(reinterpret_cast<const uint4*>(o + row * kD) + sub);
+      b[i] = __ldcs(reinterpret_cast<const uint4*>(dout + row * kD) + sub);
+      if (sub == 0) ls[i] = __ldg(lse + row);
+    }
   }
 #pragma unroll
-  for (int m = 16; m >= 1; m >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, m);
-  if (lane == 0) {
-    const size_t j = row & 15, base = (row - j) * 2 + j;
-    lsd[base] = -lse[row] * kLog2e;
-    lsd[base + 16] = -acc;
+  for (int i = 0; i < kDeltaRows; ++i) {
+    const size_t row = row0 + i;
+    const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a[i]);
+    const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&b[i]);
+    float acc = 0.f;
+    if (row < rows) {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float2 x = __bfloat1622float2(a2[j]);
+        const float2 y = __bfloat1622float2(b2[j]);
+        acc = fmaf(x.x, y.x, fmaf(x.y, y.y, acc));
+      }
+    }
+#pragma unroll
+    for (int m = 8; m >= 1; m >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, m);
+    if (sub == 0 && row < rows) {
+      const size_t j = row & 15, base = (row - j) * 2 + j;
+      lsd[base] = -ls[i] * kLog2e;
+      lsd[base + 16] = -acc;
+    }
   }
 }
 
 // ---------------------------------------------------------------- convert
 
-__global__ void bwd_convert_kernel(const float* __restrict__ src, __nv_bfloat16* __restrict__ dst,
-                                   size_t n8, float mul) {
-  const size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (i >= n8) return;
-  const float4 a = reinterpret_cast<const float4*>(src)[2 * i];
-  const float4 b = reinterpret_cast<const float4*>(src)[2 * i + 1];
+// dq = scale dq_acc, dk = scale dk_acc, dv = dv_acc to bf16 in one launch:
+// thread i converts 8 elements; the first nq8 groups are dQ, then dK, then dV.
+__global__ void bwd_convert_kernel(const float* __restrict__ dq_acc,
+                                   const float* __restrict__ dk_acc,
+                                   const float* __restrict__ dv_acc,
+                                   __nv_bfloat16* __restrict__ dq, __nv_bfloat16* __restrict__ dk,
+                                   __nv_bfloat16* __restrict__ dv, size_t nq8, size_t nkv8,
+                                   float scale) {
+  size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const float* src;
+  __nv_bfloat16* dst;
+  float mul;
+  if (i < nq8) {
+    src = dq_acc; dst = dq; mul = scale;
+  } else if ((i -= nq8) < nkv8) {
+    src = dk_acc; dst = dk; mul = scale;
+  } else if ((i -= nkv8) < nkv8) {
+    src = dv_acc; dst = dv; mul = 1.f;
+  } else {
+    return;
+  }
+  const float4 a = __ldcs(reinterpret_cast<const float4*>(src) + 2 * i);
+  const float4 b = __ldcs(reinterpret_cast<const float4*>(src) + 2 * i + 1);
   uint4 out;
   out.x = pack_bf16x2(a.x * mul, a.y * mul);
   out.y = pack_bf16x2(a.z * mul, a.w * mul);
@@ -657,13 +698,13 @@ static int bwd_max_items(int T, int S, int max_seqlen) {
 
 BwdWorkspace carve_bwd_workspace(WsCursor& ws, int T, int S, int Hq, int Hkv, int max_seqlen) {
   BwdWorkspace w;
-  w.plan = carve_plan(ws, T, S);
   w.max_items = bwd_max_items(T, S, max_seqlen);
   w.items = ws.take<int4>(w.max_items);
   w.num_items = ws.take<int>(1);
   w.lists = ws.take<int>(static_cast<size_t>(w.max_items) * Hkv * kBwdSegment);
   w.list_len = ws.take<int>(static_cast<size_t>(w.max_items) * Hkv);
   w.lsd = ws.take<float>(static_cast<size_t>(T) * Hq * 2);
+  // the three accumulators stay adjacent and in this order: one clear covers them
   w.dq_acc = ws.take<float>(static_cast<size_t>(T) * Hq * kD);
   w.dk_acc = ws.take<float>(static_cast<size_t>(T) * Hkv * kD);
   w.dv_acc = ws.take<float>(static_cast<size_t>(T) * Hkv * kD);
@@ -696,21 +737,23 @@ msa_status_t launch_sparse_bwd(const void* q, const void* k, const void* v, cons
 
   const size_t nq = static_cast<size_t>(T) * Hq * kD;
   const size_t nkv = static_cast<size_t>(T) * Hkv * kD;
-  if (cudaMemsetAsync(ws.dq_acc, 0, nq * sizeof(float), stream) != cudaSuccess ||
-      cudaMemsetAsync(ws.dk_acc, 0, nkv * sizeof(float), stream) != cudaSuccess ||
-      cudaMemsetAsync(ws.dv_acc, 0, nkv * sizeof(float), stream) != cudaSuccess)
+  // the three accumulators are carved back to back: one clear covers them
+  const size_t acc_bytes = reinterpret_cast<uint8_t*>(ws.dv_acc + nkv) -
+                           reinterpret_cast<uint8_t*>(ws.dq_acc);
+  if (cudaMemsetAsync(ws.dq_acc, 0, acc_bytes, stream) != cudaSuccess)
     return fail(MSA_ERR_CUDA, "workspace clear failed");
 
   const size_t rows = static_cast<size_t>(T) * Hq;
   {
     TraceScope trace_("bwd_delta_kernel", stream);
-    bwd_delta_kernel<<<static_cast<unsigned>((rows * 32 + 255) / 256), 256, 0, stream>>>(
+    const size_t per_block = 256 / 16 * kDeltaRows;
+    bwd_delta_kernel<<<static_cast<unsigned>((rows + per_block - 1) / per_block), 256, 0, stream>>>(
         static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dout), lse, ws.lsd,
         rows);
   }
   {
     TraceScope trace_("bwd_items_kernel", stream);
-    bwd_items_kernel<<<1, 1024, 0, stream>>>(cu, S, bwd_windows(max_seqlen), ws.items,
+    bwd_items_kernel<<<1, 1024, 0, stream>>>(cu, S, max_seqlen, bwd_windows(max_seqlen), ws.items,
                                              ws.num_items, ws.max_items, st);
   }
   {
@@ -742,19 +785,11 @@ msa_status_t launch_sparse_bwd(const void* q, const void* k, const void* v, cons
   if (e != MSA_OK) return e;
 
   {
+    const size_t n8 = nq / 8 + 2 * (nkv / 8);
     TraceScope trace_("bwd_convert_kernel", stream);
-    bwd_convert_kernel<<<static_cast<unsigned>((nq / 8 + 255) / 256), 256, 0, stream>>>(
-        ws.dq_acc, static_cast<__nv_bfloat16*>(dq), nq / 8, scale);
-  }
-  {
-    TraceScope trace_("bwd_convert_kernel", stream);
-    bwd_convert_kernel<<<static_cast<unsigned>((nkv / 8 + 255) / 256), 256, 0, stream>>>(
-        ws.dk_acc, static_cast<__nv_bfloat16*>(dk), nkv / 8, scale);
-  }
-  {
-    TraceScope trace_("bwd_convert_kernel", stream);
-    bwd_convert_kernel<<<static_cast<unsigned>((nkv / 8 + 255) / 256), 256, 0, stream>>>(
-        ws.dv_acc, static_cast<__nv_bfloat16*>(dv), nkv / 8, 1.0f);
+    bwd_convert_kernel<<<static_cast<unsigned>((n8 + 255) / 256), 256, 0, stream>>>(
+        ws.dq_acc, ws.dk_acc, ws.dv_acc, static_cast<__nv_bfloat16*>(dq),
+        static_cast<__nv_bfloat16*>(dk), static_cast<__nv_bfloat16*>(dv), nq / 8, nkv / 8, scale);
   }
   return check_launch("bwd_convert_kernel");
 }
