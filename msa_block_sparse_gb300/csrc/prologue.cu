@@ -5,10 +5,12 @@
 // Notes".)  bf16 [T, H, 128] -> bf16 [T, H, 128] (in place allowed); HBM-bound.
 //
 // Layout of the work: a CTA takes 16 consecutive tokens of every tensor of the
-// call (q, k, index q, index k: one set of angles serves them all).  It first
-// issues the loads of its first 128 rows (8 per thread), computes the 16 x 32
-// (cos, sin) pairs of its tokens meanwhile, then sweeps the rows, 16 threads
-// per row and 8 channels (16 bytes) per thread.
+// call (q, k, index q, index k: one set of angles serves them all) and sweeps
+// their rows with 8 threads per row.  Thread c < 4 of a row holds channels
+// [8c, 8c + 8) and [8c + 32, 8c + 40): the rotated pairs (i, i + 32) sit in one
+// thread, so the rotation needs no shuffles; threads 4..7 hold the
+// pass-through channels 64..127.  Each thread keeps the loads of four rows in
+// flight; the first rows' loads are issued before the angles are computed.
 //
 // Angles avoid a large fp32 argument: the host turns each frequency f_i into
 // the 64-bit fixed-point fraction F_i = f_i / (2 pi) * 2^64 of a turn, so
@@ -30,52 +32,77 @@ struct PrologueArgs {
 };
 
 constexpr int kProTokens = 16;
-constexpr int kProUnroll = 8;      // rows per thread per sweep step (loads in flight)
+constexpr int kProThreads = 256;
+constexpr int kProSlots = kProThreads / 8;   // rows processed side by side
+constexpr int kProUnroll = 2;                // rows per thread in flight
 
-__global__ void __launch_bounds__(256, 4) prologue_kernel(const PrologueArgs args,
-                                                       const RopeTurns turns,
-                                                       const int32_t* __restrict__ cu, int S,
-                                                       int T, float eps, uint32_t* status) {
+__global__ void __launch_bounds__(kProThreads) prologue_kernel(const PrologueArgs args,
+                                                               const RopeTurns turns,
+                                                               const int32_t* __restrict__ cu,
+                                                               int S, int T, float eps,
+                                                               uint32_t* status) {
   __shared__ float2 cs[kProTokens][kRopeDim / 2];
   __shared__ float wsh[4][kD];
   const int t0 = blockIdx.x * kProTokens;
   const int tid = threadIdx.x;
   const int hsum = args.hstart[4];
+  const int c = tid & 7;                  // channel group of the row
+  const int slot = tid >> 3;
+  // channel offsets (elements) of this thread's two 8-channel pieces
+  const int off0 = (c < 4) ? 8 * c : 64 + 16 * (c - 4);
+  const int off1 = (c < 4) ? 8 * c + 32 : 64 + 16 * (c - 4) + 8;
   // 1 + w of every job (read after the barrier below)
   for (int k = tid; k < 4 * kD; k += blockDim.x) {
     const int j = k / kD;
     wsh[j][k % kD] = (args.hstart[j] < args.hstart[j + 1])
                          ? 1.f + __bfloat162float(args.jobs[j].w[k % kD]) : 0.f;
   }
-  const int chunk = tid & 15;           // 8 channels: [8 chunk, 8 chunk + 8)
   const int ntok = min(kProTokens, T - t0);
   const int rows = ntok * hsum;
-  uint4 xv[kProUnroll];
-  // sweep row r of the CTA -> job j, row of that tensor, token of the CTA
-  auto row_of = [&](int r, int& j, size_t& row, int& tl) {
-    tl = r / hsum;
-    const int k = r - tl * hsum;
-    j = (k >= args.hstart[1]) + (k >= args.hstart[2]) + (k >= args.hstart[3]);
-    row = static_cast<size_t>(t0 + tl) * args.jobs[j].H + (k - args.hstart[j]);
+
+  // This thread's rows are slot, slot + 32, slot + 64, ...; (tl, k) = (token of
+  // the CTA, row within the token) advances by 32 rows per step without a
+  // division once hsum is known.
+  int tl = slot / hsum, k = slot - (slot / hsum) * hsum;
+  auto advance = [&]() {
+    k += kProSlots;
+    while (k >= hsum) {
+      k -= hsum;
+      ++tl;
+    }
   };
+  uint4 xa[kProUnroll], xb[kProUnroll];
+  int rj[kProUnroll], rtl[kProUnroll];
+  size_t rrow[kProUnroll];
   auto load_rows = [&](int base) {
 #pragma unroll
     for (int u = 0; u < kProUnroll; ++u) {
-      const int r = base + (tid >> 4) + 16 * u;
-      xv[u] = make_uint4(0, 0, 0, 0);
+      const int r = base + slot + kProSlots * u;
+      rj[u] = -1;
+      rtl[u] = 0;
+      rrow[u] = 0;
+      xa[u] = make_uint4(0, 0, 0, 0);
+      xb[u] = xa[u];
       if (r < rows) {
-        int j, tl; size_t row;
-        row_of(r, j, row, tl);
-        xv[u] = __ldcs(reinterpret_cast<const uint4*>(args.jobs[j].x + row * kD) + chunk);
+        const int j = (k >= args.hstart[1]) + (k >= args.hstart[2]) + (k >= args.hstart[3]);
+        const size_t row = static_cast<size_t>(t0 + tl) * args.jobs[j].H + (k - args.hstart[j]);
+        const __nv_bfloat16* src = args.jobs[j].x + row * kD;
+        xa[u] = __ldcs(reinterpret_cast<const uint4*>(src + off0));
+        xb[u] = __ldcs(reinterpret_cast<const uint4*>(src + off1));
+        rj[u] = j;
+        rtl[u] = tl;
+        rrow[u] = row;
       }
+      advance();
     }
   };
   load_rows(0);   // in flight while the angles are computed
+
   // (cos, sin) for the CTA's tokens: thread = (token, frequency)
-  for (int k = tid; k < kProTokens * (kRopeDim / 2); k += blockDim.x) {
-    const int tl = k / (kRopeDim / 2), i = k % (kRopeDim / 2);
-    const int t = t0 + tl;
-    float c = 1.f, s = 0.f;
+  for (int q = tid; q < kProTokens * (kRopeDim / 2); q += blockDim.x) {
+    const int qt = q / (kRopeDim / 2), i = q % (kRopeDim / 2);
+    const int t = t0 + qt;
+    float cv = 1.f, sv = 0.f;
     if (t < T) {
       int lo = 0, hi = S;   // largest s with cu[s] <= t
       while (hi - lo > 1) {
@@ -85,53 +112,77 @@ __global__ void __launch_bounds__(256, 4) prologue_kernel(const PrologueArgs arg
       const unsigned long long pos = static_cast<unsigned long long>(t - __ldg(cu + lo));
       const long long ang = static_cast<long long>(pos * turns.f[i]);
       const float x = static_cast<float>(ang) * 1.0842021724855044e-19f;   // * 2^-63
-      sincospif(x, &s, &c);
+      sincospif(x, &sv, &cv);
     }
-    cs[tl][i] = make_float2(c, s);
+    cs[qt][i] = make_float2(cv, sv);
   }
   __syncthreads();
+
   // the loop bound is uniform over the CTA: every lane reaches the shuffles
-  for (int base = 0; base < rows; base += 16 * kProUnroll) {
+  for (int base = 0; base < rows; base += kProSlots * kProUnroll) {
     if (base > 0) load_rows(base);
 #pragma unroll
     for (int u = 0; u < kProUnroll; ++u) {
-      const int r = base + (tid >> 4) + 16 * u;
-      int j = 0, tl = 0; size_t row = 0;
-      if (r < rows) row_of(r, j, row, tl);
-      float x[8];
+      float x[16];
       {
-        const __nv_bfloat162* xp = reinterpret_cast<const __nv_bfloat162*>(&xv[u]);
+        const __nv_bfloat162* pa = reinterpret_cast<const __nv_bfloat162*>(&xa[u]);
+        const __nv_bfloat162* pb = reinterpret_cast<const __nv_bfloat162*>(&xb[u]);
 #pragma unroll
-        for (int e = 0; e < 4; ++e) { float2 f = __bfloat1622float2(xp[e]); x[2 * e] = f.x; x[2 * e + 1] = f.y; }
-      }
-      float ss = 0.f;
-#pragma unroll
-      for (int e = 0; e < 8; ++e) ss = fmaf(x[e], x[e], ss);
-#pragma unroll
-      for (int m = 8; m >= 1; m >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, m);
-      const float rinv = rsqrtf(ss * (1.f / kD) + eps);
-      const float4 w0 = *reinterpret_cast<const float4*>(&wsh[j][8 * chunk]);
-      const float4 w1 = *reinterpret_cast<const float4*>(&wsh[j][8 * chunk + 4]);
-      const float w[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
-#pragma unroll
-      for (int e = 0; e < 8; ++e) x[e] = x[e] * rinv * w[e];
-      // rotate-half on channels [0, 64): chunk c < 4 holds x1, chunk c + 4 holds x2
-      float y[8];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) y[e] = __shfl_xor_sync(0xffffffffu, x[e], 4);
-      if (chunk < 8) {
-        const int fbase = (chunk & 3) * 8;
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const float2 c = cs[tl][fbase + e];
-          x[e] = (chunk < 4) ? (x[e] * c.x - y[e] * c.y) : (x[e] * c.x + y[e] * c.y);
+        for (int e = 0; e < 4; ++e) {
+          const float2 fa = __bfloat1622float2(pa[e]);
+          const float2 fb = __bfloat1622float2(pb[e]);
+          x[2 * e] = fa.x;
+          x[2 * e + 1] = fa.y;
+          x[8 + 2 * e] = fb.x;
+          x[8 + 2 * e + 1] = fb.y;
         }
       }
-      if (r < rows) {
-        uint4 out;
-        out.x = pack_bf16x2(x[0], x[1]); out.y = pack_bf16x2(x[2], x[3]);
-        out.z = pack_bf16x2(x[4], x[5]); out.w = pack_bf16x2(x[6], x[7]);
-        reinterpret_cast<uint4*>(args.jobs[j].y + row * kD)[chunk] = out;
+      float s4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int e = 0; e < 16; ++e) s4[e & 3] = fmaf(x[e], x[e], s4[e & 3]);
+      float ss = (s4[0] + s4[1]) + (s4[2] + s4[3]);
+#pragma unroll
+      for (int m = 4; m >= 1; m >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, m);
+      const int j = rj[u] < 0 ? 0 : rj[u];
+      const float rinv = rsqrtf(ss * (1.f / kD) + eps);
+      {
+        const float4* wa = reinterpret_cast<const float4*>(&wsh[j][off0]);
+        const float4* wb = reinterpret_cast<const float4*>(&wsh[j][off1]);
+        const float4 w0 = wa[0], w1 = wa[1], w2 = wb[0], w3 = wb[1];
+        const float w[16] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w,
+                             w2.x, w2.y, w2.z, w2.w, w3.x, w3.y, w3.z, w3.w};
+#pragma unroll
+        for (int e = 0; e < 16; ++e) x[e] *= rinv * w[e];
+      }
+      if (c < 4) {
+        // rotate channel 8c + e (x1) with 8c + 32 + e (x2), frequency 8c + e
+        const float4* cp = reinterpret_cast<const float4*>(&cs[rtl[u]][8 * c]);
+#pragma unroll
+        for (int e2 = 0; e2 < 4; ++e2) {
+          const float4 q = cp[e2];   // (cos, sin) of frequencies 2 e2, 2 e2 + 1
+          const float cc[2] = {q.x, q.z}, sn[2] = {q.y, q.w};
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int e = 2 * e2 + h;
+            const float x1 = x[e], x2 = x[8 + e];
+            x[e] = x1 * cc[h] - x2 * sn[h];
+            x[8 + e] = x2 * cc[h] + x1 * sn[h];
+          }
+        }
+      }
+      if (rj[u] >= 0) {
+        uint4 oa, ob;
+        oa.x = pack_bf16x2(x[0], x[1]);
+        oa.y = pack_bf16x2(x[2], x[3]);
+        oa.z = pack_bf16x2(x[4], x[5]);
+        oa.w = pack_bf16x2(x[6], x[7]);
+        ob.x = pack_bf16x2(x[8], x[9]);
+        ob.y = pack_bf16x2(x[10], x[11]);
+        ob.z = pack_bf16x2(x[12], x[13]);
+        ob.w = pack_bf16x2(x[14], x[15]);
+        __nv_bfloat16* dst = args.jobs[rj[u]].y + rrow[u] * kD;
+        *reinterpret_cast<uint4*>(dst + off0) = oa;
+        *reinterpret_cast<uint4*>(dst + off1) = ob;
       }
     }
   }
@@ -157,7 +208,8 @@ msa_status_t launch_prologue(const PrologueJob* jobs, int njobs, const int32_t* 
   dim3 grid((T + kProTokens - 1) / kProTokens);
   {
     TraceScope trace_("prologue_kernel", stream);
-    prologue_kernel<<<grid, 256, 0, stream>>>(args, turns, cu, S, T, eps, status_word());
+    prologue_kernel<<<grid, kProThreads, 0, stream>>>(args, turns, cu, S, T, eps,
+                                                      status_word());
   }
   return check_launch("prologue_kernel");
 }
