@@ -9,10 +9,11 @@
 // current block gets P = 0 for it.
 //
 // Persistent CTAs (one per SM) stride over the tiles:
-//   producer (warp 0): copies the next tile's block union (built beforehand by
-//            fwd_union_kernel, one warp per tile) into a double-buffered slot and
-//            loads its Q tile, then streams K_b and V_b through separate 2-stage
-//            TMA rings (K runs one block ahead)
+//   producers: warp 0 copies the next tile's block union (built beforehand by
+//            fwd_union_kernel, one warp per tile) into a double-buffered slot,
+//            loads its Q tile and streams K_b through a 2-stage TMA ring;
+//            warp 10 streams V_b through its own 2-stage ring, so neither
+//            ring's release holds up the other
 //   MMA (warp 1): S_i = Q K_b^T into one of two TMEM buffers; then
 //            O_h += P_h V_b[64h, 64h+64) for the two 64-key halves h, with P_h
 //            read from TMEM as the A operand
@@ -27,7 +28,9 @@ namespace msa {
 
 namespace {
 
-constexpr int kFwdThreads = 320;            // warp 0 producer, warp 1 MMA, warps 2..9 softmax
+// warp 0 Q/K producer, warp 1 MMA, warps 2..9 softmax, warp 10 V producer
+constexpr int kFwdThreads = 352;
+constexpr int kVLoaderWarp = 10;
 constexpr int kSoftmaxThreads = 256;
 constexpr int kG = 16;                      // query heads per KV head
 constexpr int kTpt = 8;                     // tokens per tile
@@ -175,7 +178,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   if (tid == 0) {
     for (int i = 0; i < 2; ++i) {
       mbar_init(&sm.tile_full[i], 1);
-      mbar_init(&sm.tile_empty[i], 1 + kSoftmaxThreads);
+      mbar_init(&sm.tile_empty[i], 1 + kSoftmaxThreads + 1);
       mbar_init(&sm.k_full[i], 1);
       mbar_init(&sm.k_empty[i], 1);
       mbar_init(&sm.v_full[i], 1);
@@ -201,9 +204,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     if (lane == 0) {
       prefetch_tmap(&tm_q);
       prefetch_tmap(&tm_k);
-      prefetch_tmap(&tm_v);
     }
-    uint32_t tcount = 0, kc = 0, vc = 0;
+    uint32_t tcount = 0, kc = 0;
     bool alive = true;
     for (int ti = blockIdx.x; alive && ti < total; ti += gridDim.x) {
       TileInfo t;
@@ -222,30 +224,46 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         mbar_arrive_expect_tx(&sm.tile_full[tb], kTile);
         tma_load_3d(sm.q[tb], &tm_q, &sm.tile_full[tb], 0, g * kG, t.seq0 + t.p0);
         tma_load_3d(sm.q[tb] + kHalf, &tm_q, &sm.tile_full[tb], 64, g * kG, t.seq0 + t.p0);
-        // ---- K runs one block ahead of V
-        for (int i = 0; alive && i <= nU; ++i) {
-          if (i < nU) {
-            const int st = kc & 1;
-            if (!(alive = mbar_wait(&sm.k_empty[st], ((kc >> 1) & 1) ^ 1, status, 2))) break;
-            const int row = t.seq0 + (sm.ublk[tb][i] >> 8) * kBlock;
-            mbar_arrive_expect_tx(&sm.k_full[st], kTile);
-            tma_load_3d(sm.k[st], &tm_k, &sm.k_full[st], 0, g, row);
-            tma_load_3d(sm.k[st] + kHalf, &tm_k, &sm.k_full[st], 64, g, row);
-            ++kc;
-          }
-          if (i > 0) {
-            const int st = vc & 1;
-            if (!(alive = mbar_wait(&sm.v_empty[st], ((vc >> 1) & 1) ^ 1, status, 3))) break;
-            const int row = t.seq0 + (sm.ublk[tb][i - 1] >> 8) * kBlock;
-            mbar_arrive_expect_tx(&sm.v_full[st], kTile);
-            tma_load_3d(sm.v[st], &tm_v, &sm.v_full[st], 0, g, row);
-            tma_load_3d(sm.v[st] + kHalf, &tm_v, &sm.v_full[st], 64, g, row);
-            ++vc;
-          }
+        // ---- K tiles through their 2-stage ring (V has its own warp, so a V
+        // slot that frees late does not hold up the next K)
+        for (int i = 0; alive && i < nU; ++i) {
+          const int st = kc & 1;
+          if (!(alive = mbar_wait(&sm.k_empty[st], ((kc >> 1) & 1) ^ 1, status, 2))) break;
+          const int row = t.seq0 + (sm.ublk[tb][i] >> 8) * kBlock;
+          mbar_arrive_expect_tx(&sm.k_full[st], kTile);
+          tma_load_3d(sm.k[st], &tm_k, &sm.k_full[st], 0, g, row);
+          tma_load_3d(sm.k[st] + kHalf, &tm_k, &sm.k_full[st], 64, g, row);
+          ++kc;
         }
       }
       alive = __shfl_sync(0xffffffffu, alive ? 1 : 0, 0) != 0;
       ++tcount;
+    }
+  } else if (warp == kVLoaderWarp) {
+    // ------------------------------------------------------------ V producer
+    if (lane == 0) {
+      prefetch_tmap(&tm_v);
+      uint32_t tcount = 0, vc = 0;
+      bool alive = true;
+      for (int ti = blockIdx.x; alive && ti < total; ti += gridDim.x) {
+        TileInfo t;
+        if (!tile_info(ti, tiles, cu, t)) continue;
+        const int tb = tcount & 1;
+        // the tile's union list is in place once its Q has landed
+        if (!(alive = mbar_wait(&sm.tile_full[tb], (tcount >> 1) & 1, status, 15))) break;
+        const int nU = sm.n_union[tb];
+        for (int i = 0; alive && i < nU; ++i) {
+          const int st = vc & 1;
+          if (!(alive = mbar_wait(&sm.v_empty[st], ((vc >> 1) & 1) ^ 1, status, 3))) break;
+          const int row = t.seq0 + (sm.ublk[tb][i] >> 8) * kBlock;
+          mbar_arrive_expect_tx(&sm.v_full[st], kTile);
+          tma_load_3d(sm.v[st], &tm_v, &sm.v_full[st], 0, g, row);
+          tma_load_3d(sm.v[st] + kHalf, &tm_v, &sm.v_full[st], 64, g, row);
+          ++vc;
+        }
+        mbar_arrive(&sm.tile_empty[tb]);   // done reading the tile's union list
+        ++tcount;
+      }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
