@@ -207,7 +207,7 @@ MSA_API msa_status_t msa_decode_step(const void* q, const void* q_idx, const voi
  * workspace: the scratch (per-block scores and per-split partial outputs)
  * lives in one fixed array in the library's device memory, sized for
  *   B * Hkv <= 256   and   max_pages <= 1024   (128K cached tokens),
- * about 9.2 MB, which every GPU that loads the library keeps until the
+ * about 9.6 MB, which every GPU that loads the library keeps until the
  * process exits.  Larger calls return MSA_ERR_UNSUPPORTED and enqueue nothing.
  * The call allocates nothing: no cudaMalloc, no cudaFree, no allocating
  * library routine.  Its first call on a device looks up that device's copy

@@ -5,12 +5,13 @@
 //
 //   decode_score_kernel  : streams the index-key cache (the bulk of the bytes,
 //                          HBM-bound), one max-logit score per (seq, head, page)
-//   decode_attend_kernel : per (seq, KV head, split): top-15 + own block from the
-//                          scores (bitonic sort in shared memory), then
-//                          attention of the 16 query heads over 4 of the
-//                          selected pages with mma.sync m16n8k16 (M = 16 heads
-//                          is below tcgen05's smallest M), per-warp online
-//                          softmax, cp.async double buffering
+//   decode_select_kernel : per (seq, KV head): the own block + the best 15
+//                          earlier blocks by score (rank of each score)
+//   decode_attend_kernel : per (seq, KV head, split): attention of the 16 query
+//                          heads over 4 of the selected blocks with mma.sync
+//                          m16n8k16 (M = 16 heads is below tcgen05's smallest M);
+//                          K and V of a block arrive by TMA (128B-swizzled) into
+//                          single buffers that refill while the other is in use
 //   decode_merge_kernel  : combines the 4 splits' (max, sum, o)
 #include "kernels.cuh"
 
@@ -22,18 +23,6 @@ constexpr int kPagesPerCta = 8;
 constexpr int kRowPad = 136;                 // padded bf16 row (272 B) in shared memory
 constexpr float kLog2e = 1.4426950408889634f;
 
-__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src)
-               : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() {
-  asm volatile("cp.async.commit_group;" ::: "memory");
-}
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
-
 __device__ __forceinline__ void mma_bf16_16816(float* c, const uint32_t* a, uint32_t b0,
                                                uint32_t b1) {
   asm volatile(
@@ -41,12 +30,6 @@ __device__ __forceinline__ void mma_bf16_16816(float* c, const uint32_t* a, uint
       "{%8,%9}, {%0,%1,%2,%3};"
       : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-
-__device__ __forceinline__ void ldmatrix_x4_trans(uint32_t* r, const void* p) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "r"(smem_u32(p)));
 }
 
 __device__ __forceinline__ int clamp_len(int L, int max_pages, uint32_t* status) {
@@ -123,65 +106,50 @@ __global__ void __launch_bounds__(256) decode_score_kernel(
   }
 }
 
-// ---------------------------------------------------------------- select + attend
+// ---------------------------------------------------------------- select
 
-struct AttendSmem {
-  __nv_bfloat16 q[16][kRowPad];
-  __nv_bfloat16 kv[2][2][kBlock][kRowPad];     // [buffer][K or V][key][dim]
-  float key[1024];
-  int id[1024];
-  int chosen[16];
-};
-
-__global__ void __launch_bounds__(128) decode_attend_kernel(
-    const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k_cache,
-    const __nv_bfloat16* __restrict__ v_cache, const int32_t* __restrict__ block_table,
-    const int32_t* __restrict__ cache_lens, int Hq, int Hkv, int num_pages, int max_pages,
-    float scale, const float* __restrict__ scores, int32_t* __restrict__ sel_out,
-    float* __restrict__ part_o, float* __restrict__ part_ml, uint32_t* status) {
-  extern __shared__ uint8_t smem_raw[];
-  AttendSmem& sm = *reinterpret_cast<AttendSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) &
-                                                  ~static_cast<uintptr_t>(127));
-  const int b = blockIdx.x, h = blockIdx.y, split = blockIdx.z;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+// grid (B * Hkv), 128 threads: the own block plus the best min(15, own)
+// earlier blocks by score (descending, ties: lower id).  Block i is kept when
+// fewer than 15 blocks rank before it (higher score, or equal score and lower
+// id); each thread counts for its blocks over the whole row, four scores per
+// shared-memory load and four independent counters.  The kept ids are written
+// ascending with the own block, -1 padded, to sel and, if given, sel_out.
+__global__ void __launch_bounds__(128) decode_select_kernel(
+    const float* __restrict__ scores, const int32_t* __restrict__ cache_lens, int Hkv,
+    int max_pages, int32_t* __restrict__ sel, int32_t* __restrict__ sel_out, uint32_t* status) {
+  __shared__ __align__(16) float key[1024];
+  __shared__ int kept[16];
+  __shared__ int nkept;
+  const int bh = blockIdx.x;
+  const int b = bh / Hkv;
+  const int tid = threadIdx.x;
   const int L = clamp_len(cache_lens[b], max_pages, status);
-  const int nb = (L + kBlock - 1) / kBlock;
-  const int own = nb - 1;
-
-  // ---- top-15 earlier blocks by score (descending, ties: lower id), then own
-  int n2 = 1;
-  while (n2 < own) n2 <<= 1;
-  const float* sc = scores + (static_cast<size_t>(b) * Hkv + h) * max_pages;
-  for (int i = tid; i < n2; i += 128) {
-    sm.key[i] = (i < own) ? sc[i] : -INFINITY;
-    sm.id[i] = (i < own) ? i : 0x7fffffff;
+  const int own = (L + kBlock - 1) / kBlock - 1;
+  const int own4 = (own + 3) & ~3;
+  const float* sc = scores + static_cast<size_t>(bh) * max_pages;
+  for (int i = tid; i < own4; i += blockDim.x) key[i] = (i < own) ? sc[i] : -INFINITY;
+  if (tid == 0) nkept = 0;
+  __syncthreads();
+  for (int i = tid; i < own; i += blockDim.x) {
+    const float ki = key[i];
+    int c0 = 0, c1 = 0, c2 = 0, c3 = 0;
+    // padding entries (-inf at j >= own) never rank before a real block: their
+    // score is not above ki and their index is not below i
+#pragma unroll 4
+    for (int j = 0; j < own4; j += 4) {
+      const float4 k4 = *reinterpret_cast<const float4*>(&key[j]);
+      c0 += (k4.x > ki || (k4.x == ki && j < i)) ? 1 : 0;
+      c1 += (k4.y > ki || (k4.y == ki && j + 1 < i)) ? 1 : 0;
+      c2 += (k4.z > ki || (k4.z == ki && j + 2 < i)) ? 1 : 0;
+      c3 += (k4.w > ki || (k4.w == ki && j + 3 < i)) ? 1 : 0;
+    }
+    if (c0 + c1 + c2 + c3 < 15) kept[atomicAdd(&nkept, 1)] = i;   // at most 15 blocks
   }
   __syncthreads();
-  for (int kk = 2; kk <= n2; kk <<= 1) {
-    for (int j = kk >> 1; j > 0; j >>= 1) {
-      for (int i = tid; i < n2; i += 128) {
-        const int l = i ^ j;
-        if (l > i) {
-          const float ki = sm.key[i], kl = sm.key[l];
-          const int ii = sm.id[i], il = sm.id[l];
-          // "i before l" in the target order: higher score, then lower id
-          const bool l_first = (kl > ki) || (kl == ki && il < ii);
-          const bool desc = (i & kk) == 0;
-          if (desc ? l_first : !l_first) {
-            sm.key[i] = kl;
-            sm.key[l] = ki;
-            sm.id[i] = il;
-            sm.id[l] = ii;
-          }
-        }
-      }
-      __syncthreads();
-    }
-  }
   if (tid == 0) {
+    const int n = nkept;
     int v[16];
-    const int nkeep = min(15, own);
-    for (int i = 0; i < 16; ++i) v[i] = (i < nkeep) ? sm.id[i] : (i == nkeep ? own : -1);
+    for (int i = 0; i < 16; ++i) v[i] = (i < n) ? kept[i] : (i == n ? own : -1);
     // ascending order, -1 last (insertion sort on 16 values)
     for (int i = 1; i < 16; ++i) {
       int x = v[i], j = i - 1;
@@ -191,72 +159,117 @@ __global__ void __launch_bounds__(128) decode_attend_kernel(
       }
       v[j + 1] = x;
     }
-    for (int i = 0; i < 16; ++i) sm.chosen[i] = v[i];
-    if (split == 0 && sel_out)
-      for (int i = 0; i < 16; ++i) sel_out[(static_cast<size_t>(b) * Hkv + h) * kTopK + i] = v[i];
-  }
-  __syncthreads();
-
-  // ---- this split's blocks
-  int my_blk[4], nmy = 0;
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int blk = sm.chosen[split * 4 + i];
-    my_blk[i] = blk;
-    if (blk >= 0) nmy = i + 1;
-  }
-  int my_page[4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    int pg = (i < nmy) ? block_table[static_cast<size_t>(b) * max_pages + my_blk[i]] : 0;
-    if (pg < 0 || pg >= num_pages) {
-      atomicOr(status, kStatusBounds);
-      pg = 0;
+    for (int i = 0; i < 16; ++i) {
+      sel[static_cast<size_t>(bh) * kTopK + i] = v[i];
+      if (sel_out) sel_out[static_cast<size_t>(bh) * kTopK + i] = v[i];
     }
-    my_page[i] = pg;
   }
+}
+
+// ---------------------------------------------------------------- attend
+
+// One selected block's K or V slab (128 keys x 128 dims) as two 128B-swizzled
+// 64-dim halves of 16 KB, as TMA writes them: key r, 16-byte chunk c of a half
+// sits at r * 128 + ((c ^ (r % 8)) << 4).
+struct AttendSmem {
+  uint8_t k[2 * 16384];
+  uint8_t v[2 * 16384];
+  __nv_bfloat16 q[16][kRowPad];
+  int page[4];
+  int blk[4];
+  uint64_t k_full, v_full;
+};
+
+__device__ __forceinline__ uint32_t swz(int row, int chunk) {
+  return static_cast<uint32_t>(row * 128 + ((chunk ^ (row & 7)) << 4));
+}
+
+__device__ __forceinline__ void ldmatrix_x4_trans_u32(uint32_t* r, uint32_t saddr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(saddr));
+}
+
+// grid (B, Hkv, kDecodeSplits), 128 threads (4 warps x 32 keys of each block):
+// attention of the KV group's 16 query heads over 4 of the selected blocks.
+// K and V of a block arrive by TMA into single buffers with their own
+// barriers: K(i + 1) is fetched once every warp has used K(i) for S, V(i + 1)
+// once P V(i) is done, so each load overlaps the other half of the block.
+__global__ void __launch_bounds__(128) decode_attend_kernel(
+    const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+    const __nv_bfloat16* __restrict__ q, const int32_t* __restrict__ block_table,
+    const int32_t* __restrict__ cache_lens, const int32_t* __restrict__ sel, int Hq, int Hkv,
+    int num_pages, int max_pages, float scale, float* __restrict__ part_o,
+    float* __restrict__ part_ml, uint32_t* status) {
+  extern __shared__ uint8_t smem_raw[];
+  AttendSmem& sm = *reinterpret_cast<AttendSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                  ~static_cast<uintptr_t>(1023));
+  const int b = blockIdx.x, h = blockIdx.y, split = blockIdx.z;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int L = clamp_len(cache_lens[b], max_pages, status);
+  const int own = (L + kBlock - 1) / kBlock - 1;
   const size_t obase = ((static_cast<size_t>(b) * Hkv + h) * kDecodeSplits + split) * 16;
+
+  // ---- this split's blocks (sel is ascending, -1 last)
+  int nmy = 0;
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    if (sel[(static_cast<size_t>(b) * Hkv + h) * kTopK + split * 4 + i] >= 0) nmy = i + 1;
   if (nmy == 0) {
-    for (int i = tid; i < 16; i += 128) {
+    for (int i = tid; i < 16; i += blockDim.x) {
       part_ml[(obase + i) * 2] = -INFINITY;
       part_ml[(obase + i) * 2 + 1] = 0.f;
     }
     return;
   }
-
-  // Q (16 heads x 128) -> shared
-  for (int i = tid; i < 16 * 16; i += 128) {
-    const int r = i >> 4, c = i & 15;
-    cp_async16(&sm.q[r][c * 8], q + (static_cast<size_t>(b) * Hq + h * 16 + r) * kD + c * 8);
-  }
-  auto load_block = [&](int i, int buf) {
-    const size_t base = (static_cast<size_t>(my_page[i]) * Hkv + h) * kBlock * kD;
-    for (int x = tid; x < 2 * kBlock * 16; x += 128) {
-      const int which = x >> 11, rr = (x >> 4) & 127, c = x & 15;
-      const __nv_bfloat16* src = (which ? v_cache : k_cache) + base + rr * kD + c * 8;
-      cp_async16(&sm.kv[buf][which][rr][c * 8], src);
+  if (tid < 4) {
+    const int blk = (tid < nmy) ? sel[(static_cast<size_t>(b) * Hkv + h) * kTopK + split * 4 + tid] : 0;
+    int pg = (tid < nmy) ? block_table[static_cast<size_t>(b) * max_pages + blk] : 0;
+    if (pg < 0 || pg >= num_pages) {
+      atomicOr(status, kStatusBounds);
+      pg = 0;
     }
+    sm.page[tid] = pg;
+    sm.blk[tid] = blk;
+  }
+  if (tid == 0) {
+    mbar_init(&sm.k_full, 1);
+    mbar_init(&sm.v_full, 1);
+    fence_mbar_init();
+    prefetch_tmap(&tm_k);
+    prefetch_tmap(&tm_v);
+  }
+  __syncthreads();
+  auto load = [&](const CUtensorMap* map, uint8_t* dst, uint64_t* bar, int i) {
+    const int row = (sm.page[i] * Hkv + h) * kBlock;
+    mbar_arrive_expect_tx(bar, 2 * 16384);
+    tma_load_2d(dst, map, bar, 0, row);
+    tma_load_2d(dst + 16384, map, bar, 64, row);
   };
-  load_block(0, 0);
-  cp_async_commit();
+  if (tid == 0) {
+    load(&tm_k, sm.k, &sm.k_full, 0);
+    load(&tm_v, sm.v, &sm.v_full, 0);
+  }
+  // Q (16 heads x 128) -> padded shared rows
+  for (int i = tid; i < 16 * 16; i += blockDim.x) {
+    const int r = i >> 4, c = i & 15;
+    *reinterpret_cast<uint4*>(&sm.q[r][c * 8]) =
+        __ldg(reinterpret_cast<const uint4*>(q + (static_cast<size_t>(b) * Hq + h * 16 + r) * kD) + c);
+  }
+  __syncthreads();
 
   const int g = lane >> 2, cq = lane & 3;
   const float sl2 = scale * kLog2e;
+  const uint32_t ka = smem_u32(sm.k), va = smem_u32(sm.v);
   float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
   float acc[16][4];
 #pragma unroll
   for (int nt = 0; nt < 16; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
+  bool ok = true;
 
   for (int i = 0; i < nmy; ++i) {
-    const int buf = i & 1;
-    if (i + 1 < nmy) {
-      load_block(i + 1, buf ^ 1);
-      cp_async_commit();
-      cp_async_wait<1>();
-    } else {
-      cp_async_wait<0>();
-    }
-    __syncthreads();
+    ok = mbar_wait(&sm.k_full, i & 1, status, 70);
+    if (!__syncthreads_and(ok)) break;
     // S = Q K^T for this warp's 32 keys
     float s[4][4];
 #pragma unroll
@@ -268,25 +281,32 @@ __global__ void __launch_bounds__(128) decode_attend_kernel(
       a[1] = *reinterpret_cast<const uint32_t*>(&sm.q[g + 8][kk * 16 + 2 * cq]);
       a[2] = *reinterpret_cast<const uint32_t*>(&sm.q[g][kk * 16 + 2 * cq + 8]);
       a[3] = *reinterpret_cast<const uint32_t*>(&sm.q[g + 8][kk * 16 + 2 * cq + 8]);
+      const uint8_t* kh = sm.k + (kk >> 2) * 16384;
 #pragma unroll
       for (int nt = 0; nt < 4; ++nt) {
         const int key = warp * 32 + nt * 8 + g;
-        const uint32_t b0 = *reinterpret_cast<const uint32_t*>(&sm.kv[buf][0][key][kk * 16 + 2 * cq]);
-        const uint32_t b1 = *reinterpret_cast<const uint32_t*>(&sm.kv[buf][0][key][kk * 16 + 2 * cq + 8]);
+        const int c0 = (kk & 3) * 2;
+        const uint32_t b0 = *reinterpret_cast<const uint32_t*>(kh + swz(key, c0) + 4 * cq);
+        const uint32_t b1 = *reinterpret_cast<const uint32_t*>(kh + swz(key, c0 + 1) + 4 * cq);
         mma_bf16_16816(s[nt], a, b0, b1);
       }
     }
+    __syncthreads();                            // every warp is done with K(i)
+    if (tid == 0 && i + 1 < nmy) {
+      fence_proxy_async_smem();
+      load(&tm_k, sm.k, &sm.k_full, i + 1);
+    }
     // mask keys past the new token (own block only) and update this warp's softmax
-    const int nvalid = (my_blk[i] == own) ? (L - own * kBlock) : kBlock;
+    const int nvalid = (sm.blk[i] == own) ? (L - own * kBlock) : kBlock;
     float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
     for (int nt = 0; nt < 4; ++nt) {
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
         const int key = warp * 32 + nt * 8 + 2 * cq + e;
-        const bool ok = key < nvalid;
-        s[nt][e] = ok ? s[nt][e] * sl2 : -INFINITY;
-        s[nt][2 + e] = ok ? s[nt][2 + e] * sl2 : -INFINITY;
+        const bool valid = key < nvalid;
+        s[nt][e] = valid ? s[nt][e] * sl2 : -INFINITY;
+        s[nt][2 + e] = valid ? s[nt][2 + e] * sl2 : -INFINITY;
         mx0 = fmaxf(mx0, s[nt][e]);
         mx1 = fmaxf(mx1, s[nt][2 + e]);
       }
@@ -324,29 +344,37 @@ __global__ void __launch_bounds__(128) decode_attend_kernel(
       pa[kk][hi * 2 + 0] = pack_bf16x2(p00, p01);
       pa[kk][hi * 2 + 1] = pack_bf16x2(p10, p11);
     }
-    // O += P V over this warp's 32 keys
+    ok = mbar_wait(&sm.v_full, i & 1, status, 71);
+    if (!__syncthreads_and(ok)) break;
+    // O += P V over this warp's 32 keys (V rows read transposed by ldmatrix)
 #pragma unroll
     for (int kk = 0; kk < 2; ++kk) {
       const uint32_t a[4] = {pa[kk][0], pa[kk][1], pa[kk][2], pa[kk][3]};
       const int krow = warp * 32 + kk * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
 #pragma unroll
       for (int nt = 0; nt < 16; nt += 2) {
+        const int d = nt * 8 + (lane >> 4) * 8;
         uint32_t bb[4];
-        ldmatrix_x4_trans(bb, &sm.kv[buf][1][krow][nt * 8 + (lane >> 4) * 8]);
+        ldmatrix_x4_trans_u32(bb, va + (d >> 6) * 16384 + swz(krow, (d & 63) >> 3));
         mma_bf16_16816(acc[nt], a, bb[0], bb[1]);
         mma_bf16_16816(acc[nt + 1], a, bb[2], bb[3]);
       }
     }
-    __syncthreads();
+    __syncthreads();                            // every warp is done with V(i)
+    if (tid == 0 && i + 1 < nmy) {
+      fence_proxy_async_smem();
+      load(&tm_v, sm.v, &sm.v_full, i + 1);
+    }
   }
+  if (!ok) return;
   l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
   l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
   l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
   l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
 
-  // ---- merge the 4 warps (shared memory reused)
-  float* wo = reinterpret_cast<float*>(&sm.kv[0][0][0][0]);     // [4][16][128]
-  float* wml = wo + 4 * 16 * 128;                                // [4][16][2]
+  // ---- merge the 4 warps (the K/V buffers are free: every load has landed)
+  float* wo = reinterpret_cast<float*>(sm.k);     // [4][16][128]
+  float* wml = wo + 4 * 16 * 128;                 // [4][16][2]
 #pragma unroll
   for (int nt = 0; nt < 16; ++nt) {
     wo[(warp * 16 + g) * 128 + nt * 8 + 2 * cq] = acc[nt][0];
@@ -442,6 +470,7 @@ DecodeWorkspace carve_decode_workspace(WsCursor& ws, int B, int Hq, int Hkv, int
   DecodeWorkspace w;
   w.max_pages = max_pages;
   w.scores = ws.take<float>(static_cast<size_t>(B) * Hkv * max_pages);
+  w.sel = ws.take<int32_t>(static_cast<size_t>(B) * Hkv * kTopK);
   w.part_o = ws.take<float>(static_cast<size_t>(B) * Hkv * kDecodeSplits * 16 * kD);
   w.part_ml = ws.take<float>(static_cast<size_t>(B) * Hkv * kDecodeSplits * 16 * 2);
   return w;
@@ -462,7 +491,21 @@ msa_status_t launch_decode(const void* q, const void* q_idx, const void* k_cache
   }
   msa_status_t e = check_launch("decode_score_kernel");
   if (e != MSA_OK) return e;
-  const size_t smem = sizeof(AttendSmem) + 128;
+  {
+    TraceScope trace_("decode_select_kernel", stream);
+    decode_select_kernel<<<B * Hkv, 128, 0, stream>>>(ws.scores, cache_lens, Hkv, max_pages,
+                                                      ws.sel, sel_out, st);
+  }
+  e = check_launch("decode_select_kernel");
+  if (e != MSA_OK) return e;
+  // K and V caches as 2-D (dims, key rows) tensors; one box = 64 dims x one block
+  CUtensorMap tk, tv;
+  const uint64_t dims[2] = {static_cast<uint64_t>(kD),
+                            static_cast<uint64_t>(num_pages) * Hkv * kBlock};
+  const uint32_t box[2] = {64, static_cast<uint32_t>(kBlock)};
+  if (!make_tmap_bf16(&tk, k_cache, 2, dims, box) || !make_tmap_bf16(&tv, v_cache, 2, dims, box))
+    return fail(MSA_ERR_CUDA, "cuTensorMapEncodeTiled failed for the paged K/V caches");
+  const size_t smem = sizeof(AttendSmem) + 1024;
   static bool attr_set = false;
   if (!attr_set) {
     cudaFuncSetAttribute(decode_attend_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -473,9 +516,8 @@ msa_status_t launch_decode(const void* q, const void* q_idx, const void* k_cache
   {
     TraceScope trace_("decode_attend_kernel", stream);
     decode_attend_kernel<<<g2, 128, smem, stream>>>(
-      static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k_cache),
-      static_cast<const __nv_bfloat16*>(v_cache), block_table, cache_lens, Hq, Hkv, num_pages,
-      max_pages, scale, ws.scores, sel_out, ws.part_o, ws.part_ml, st);
+      tk, tv, static_cast<const __nv_bfloat16*>(q), block_table, cache_lens, ws.sel, Hq, Hkv,
+      num_pages, max_pages, scale, ws.part_o, ws.part_ml, st);
   }
   e = check_launch("decode_attend_kernel");
   if (e != MSA_OK) return e;
@@ -504,15 +546,16 @@ namespace {
 constexpr int kStaticMaxRows = 256;     // B * Hkv
 constexpr int kStaticMaxPages = 1024;   // pages (128-token blocks) per sequence
 constexpr size_t kStaticScores = static_cast<size_t>(kStaticMaxRows) * kStaticMaxPages;
+constexpr size_t kStaticSel = static_cast<size_t>(kStaticMaxRows) * kTopK;   // int32, float-sized
 constexpr size_t kStaticPartO = static_cast<size_t>(kStaticMaxRows) * kDecodeSplits * 16 * kD;
 constexpr size_t kStaticPartMl = static_cast<size_t>(kStaticMaxRows) * kDecodeSplits * 16 * 2;
 
 // One copy per GPU that loads the library, kept until the process exits
-// (about 9.2 MB).  In host code this name is only a host-side stand-in for
+// (about 9.6 MB).  In host code this name is only a host-side stand-in for
 // the symbol: kernels must be given the device address that
 // cudaGetSymbolAddress returns for the current device.
-static __device__ __align__(256) float g_decode_scratch[kStaticScores + kStaticPartO +
-                                                        kStaticPartMl];
+static __device__ __align__(256) float g_decode_scratch[kStaticScores + kStaticSel +
+                                                        kStaticPartO + kStaticPartMl];
 
 std::mutex g_static_mu;
 float* g_static_ptr[64] = {nullptr};
@@ -578,8 +621,9 @@ extern "C" msa_status_t msa_decode_step_static(const void* q, const void* q_idx,
   DecodeWorkspace ws;
   ws.max_pages = max_pages;
   ws.scores = base;                                   // [B, Hkv, max_pages]
-  ws.part_o = base + kStaticScores;                   // [B, Hkv, splits, 16, 128]
-  ws.part_ml = base + kStaticScores + kStaticPartO;   // [B, Hkv, splits, 16, 2]
+  ws.sel = reinterpret_cast<int32_t*>(base + kStaticScores);                    // [B, Hkv, 16]
+  ws.part_o = base + kStaticScores + kStaticSel;                                // [B, Hkv, splits, 16, 128]
+  ws.part_ml = base + kStaticScores + kStaticSel + kStaticPartO;                // [B, Hkv, splits, 16, 2]
   return launch_decode(q, q_idx, k_cache, v_cache, kidx_cache, block_table, cache_lens, B, Hq,
                        Hkv, num_pages, max_pages, scale, o, sel_out, ws,
                        static_cast<cudaStream_t>(stream));

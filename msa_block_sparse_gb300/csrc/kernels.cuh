@@ -65,6 +65,7 @@ msa_status_t launch_sparse_bwd(const void* q, const void* k, const void* v, cons
 // ---------------------------------------------------------------- decode
 struct DecodeWorkspace {
   float* scores;       // [B, Hkv, max_pages] per-block max logits
+  int32_t* sel;        // [B, Hkv, 16] selected blocks (ascending, -1 padded)
   float* part_o;       // [B, Hkv, kDecodeSplits, 16, 128] partial outputs
   float* part_ml;      // [B, Hkv, kDecodeSplits, 16, 2] partial (max, sum)
   int max_pages;
