@@ -293,6 +293,37 @@ def test_decode_small_edges(m):
     _decode_check(m, shape, seed=5)
 
 
+def test_decode_exact_ties(m):
+    """Twenty earlier blocks of sequence 0 share one dominant index-key page, so
+    their scores are exactly equal and straddle the 15-block cut: the rule
+    (equal scores: lower block id first) must keep the 15 lowest of them."""
+    shape = W.DecodeShape("decode-ties", (5120, 3000, 129, 4096), 32, 2, 2)
+    x = W.make_decode(shape, seed=11, device="cpu")
+    table = x["block_table"].numpy()
+    tied = [2, 3, 5, 7, 8, 11, 13, 14, 17, 19, 21, 22, 24, 26, 27, 29, 31, 33, 35, 37]
+    kidx = x["kidx_cache"].clone()
+    for h in range(shape.hi):
+        row = (x["q_idx"][0, h].float() * 4.0).to(torch.bfloat16)
+        for blk in tied:
+            kidx[int(table[0, blk]), h] = row
+    x["kidx_cache"] = kidx
+    g = {k: v.to(DEV) for k, v in x.items()}
+    o, sel = m.msa_decode_step(g["q"], g["q_idx"], g["k_cache"], g["v_cache"], g["kidx_cache"],
+                               g["block_table"], g["cache_lens"])
+    m.msa_check_status()
+    lens = x["cache_lens"].numpy()
+    ro, rsel, rgap = O.decode_step(f64(x["q"]), f64(x["q_idx"]), f64(x["k_cache"]),
+                                   f64(x["v_cache"]), f64(x["kidx_cache"]), table, lens, SCALE)
+    gsel = sel.cpu().numpy()
+    own0 = (lens[0] + 127) // 128 - 1
+    want = sorted(tied[:15]) + [own0]
+    for h in range(shape.hi):
+        assert list(rsel[0, h]) == want, (h, rsel[0, h])      # the oracle applies the rule
+        assert list(gsel[0, h]) == want, (h, gsel[0, h])      # and so must the kernels
+    np.testing.assert_array_equal(gsel, rsel)
+    assert_close(f64(o), ro, 2e-2, 1e-2, "decode-ties o")
+
+
 def test_decode_full_size(m):
     _decode_check(m, W.config(3), seed=0, rows=[0, 1, 17, 33, 63])
 
