@@ -28,17 +28,21 @@ namespace msa {
 
 namespace {
 
-// warp 0 Q/K producer, warp 1 MMA, warps 2..9 softmax, warp 10 V producer
-constexpr int kFwdThreads = 352;
+// warp 0 Q/K producer, warps 1 and 11 MMA (key half 0 / 1), warps 2..9
+// softmax, warp 10 V producer
+constexpr int kFwdThreads = 384;
 constexpr int kVLoaderWarp = 10;
+constexpr int kMmaWarp1 = 11;
+
 constexpr int kSoftmaxThreads = 256;
+constexpr int kHalfThreads = kSoftmaxThreads / 2;   // softmax threads of one key half
 constexpr int kG = 16;                      // query heads per KV head
 constexpr int kTpt = 8;                     // tokens per tile
 constexpr int kTile = 128 * 128 * 2;        // bytes of a 128 x 128 bf16 tile
 constexpr int kHalf = kTile / 2;            // one 64-column half
 constexpr int kMaskWords = kMaxSeqlen / kBlock / 32;
-constexpr uint32_t kIdescS = idesc_bf16(128, 128, false, false);
-constexpr uint32_t kIdescPV = idesc_bf16(128, 128, false, true);
+constexpr uint32_t kIdescS = idesc_bf16(128, 64, false, false);    // S_h: 64 keys of a half
+constexpr uint32_t kIdescPV = idesc_bf16(128, 128, false, true);   // O_h += P_h V_h
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleThreshold = 8.0f;   // log2 of the largest P before a rescale
 constexpr uint32_t kColO = 256;             // O_0 at 256, O_1 at 384; S buffers at 0, 128
@@ -52,8 +56,8 @@ struct FwdSmem {
   float2 ml[2][128];                        // per half: (max, sum) of each row, for the merge
   uint64_t tile_full[2], tile_empty[2];
   uint64_t k_full[2], k_empty[2], v_full[2], v_empty[2];
-  // per S buffer: a waiter is then never more than one phase behind
-  uint64_t s_full[2], p_full[2], pv_done[2], ml_full;
+  // per key half and S buffer: a waiter is then never more than one phase behind
+  uint64_t s_full[2][2], p_full[2][2], pv_done[2][2], ml_full;
   uint32_t tmem_base;
 };
 static_assert(sizeof(FwdSmem) <= 232448, "forward shared memory above the 227 KB limit");
@@ -178,14 +182,16 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   if (tid == 0) {
     for (int i = 0; i < 2; ++i) {
       mbar_init(&sm.tile_full[i], 1);
-      mbar_init(&sm.tile_empty[i], 1 + kSoftmaxThreads + 1);
+      mbar_init(&sm.tile_empty[i], 2 + kSoftmaxThreads + 1);
       mbar_init(&sm.k_full[i], 1);
-      mbar_init(&sm.k_empty[i], 1);
+      mbar_init(&sm.k_empty[i], 2);
       mbar_init(&sm.v_full[i], 1);
-      mbar_init(&sm.v_empty[i], 1);
-      mbar_init(&sm.s_full[i], 1);
-      mbar_init(&sm.p_full[i], kSoftmaxThreads);
-      mbar_init(&sm.pv_done[i], 1);
+      mbar_init(&sm.v_empty[i], 2);
+      for (int hh = 0; hh < 2; ++hh) {
+        mbar_init(&sm.s_full[hh][i], 1);
+        mbar_init(&sm.p_full[hh][i], kHalfThreads);
+        mbar_init(&sm.pv_done[hh][i], 1);
+      }
     }
     mbar_init(&sm.ml_full, kSoftmaxThreads);
     fence_mbar_init();
@@ -265,8 +271,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         ++tcount;
       }
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
+  } else if (warp == 1 || warp == kMmaWarp1) {
+    // ------------------------------------------------------------ MMA issuers
+    // one per key half hh: S_hh = Q K[64hh, 64hh+64)^T and O_hh += P_hh V[64hh, ..)
+    const int hh = (warp == 1) ? 0 : 1;
     if (elect_one()) {
       uint32_t tcount = 0, kc = 0, vc = 0, bc = 0;
       bool ok = true;
@@ -283,18 +291,20 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           if (i < nU) {
             const int st = kc & 1;
             if (!(ok = mbar_wait(&sm.k_full[st], (kc >> 1) & 1, status, 5))) break;
-            // the S buffer of block bc held P of block bc - 2: wait for its PV
-            if (bc >= 2 && !(ok = mbar_wait(&sm.pv_done[bc & 1], ((bc - 2) >> 1) & 1, status, 6)))
+            // this half of S buffer bc held P of block bc - 2: wait for its PV
+            if (bc >= 2 &&
+                !(ok = mbar_wait(&sm.pv_done[hh][bc & 1], ((bc - 2) >> 1) & 1, status, 6)))
               break;
             tc_fence_after();
-            const uint32_t ka = smem_u32(sm.k[st]);
+            // keys [64hh, 64hh + 64) of the K tile: rows 64hh.. of both D halves
+            const uint32_t ka = smem_u32(sm.k[st]) + hh * 64 * 128;
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) {
               const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
-              umma_bf16(tmem + (bc & 1) * 128, sdesc_sw128(qa + off, 16, 1024),
+              umma_bf16(tmem + (bc & 1) * 128 + 64 * hh, sdesc_sw128(qa + off, 16, 1024),
                         sdesc_sw128(ka + off, 16, 1024), kIdescS, kk > 0);
             }
-            umma_commit(&sm.s_full[bc & 1]);
+            umma_commit(&sm.s_full[hh][bc & 1]);
             umma_commit(&sm.k_empty[st]);
             ++kc;
             ++bc;
@@ -302,19 +312,19 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           if (i > 0) {
             const uint32_t j = bc0 + i - 1;
             const int st = vc & 1;
-            if (!(ok = mbar_wait(&sm.p_full[j & 1], (j >> 1) & 1, status, 7))) break;
+            if (!(ok = mbar_wait(&sm.p_full[hh][j & 1], (j >> 1) & 1, status, 7))) break;
             if (!(ok = mbar_wait(&sm.v_full[st], (vc >> 1) & 1, status, 8))) break;
             tc_fence_after();
-            const uint32_t va = smem_u32(sm.v[st]);
+            // V rows (keys) [64hh, 64hh + 64): four K-steps of 16 keys
+            const uint32_t va = smem_u32(sm.v[st]) + hh * 64 * 128;
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-              const int hh = kk >> 2;
-              const uint32_t a_t = tmem + (j & 1) * 128 + hh * 64 + (kk & 3) * 8;
+            for (int kk = 0; kk < 4; ++kk) {
+              const uint32_t a_t = tmem + (j & 1) * 128 + hh * 64 + kk * 8;
               umma_bf16_tmem_a(tmem + kColO + hh * 128, a_t,
                                sdesc_sw128(va + kk * 2048, kHalf, 1024), kIdescPV,
-                               (i > 1 || (kk & 3) > 0));
+                               (i > 1 || kk > 0));
             }
-            umma_commit(&sm.pv_done[j & 1]);
+            umma_commit(&sm.pv_done[hh][j & 1]);
             umma_commit(&sm.v_empty[st]);
             ++vc;
           }
@@ -347,7 +357,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         const int ent = sm.ublk[tb][i];
         const int b = ent >> 8;
         const uint32_t sbuf = tmem + (bc & 1) * 128 + trow + 64 * h;
-        if (!(ok = mbar_wait(&sm.s_full[bc & 1], (bc >> 1) & 1, status, 10))) break;
+        if (!(ok = mbar_wait(&sm.s_full[h][bc & 1], (bc >> 1) & 1, status, 10))) break;
         __syncwarp();
         tc_fence_after();
         uint32_t sv[64];
@@ -400,7 +410,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         const bool need = resc && m != -INFINITY;
         if (__any_sync(0xffffffffu, need)) {
           // O_h is stable only once the PV of the previous block is done
-          if (!(ok = mbar_wait(&sm.pv_done[(bc - 1) & 1], ((bc - 1) >> 1) & 1, status, 11))) break;
+          if (!(ok = mbar_wait(&sm.pv_done[h][(bc - 1) & 1], ((bc - 1) >> 1) & 1, status, 11)))
+            break;
           __syncwarp();
           tc_fence_after();
           const float alpha = need ? ex2(m - mu) : 1.f;
@@ -424,14 +435,14 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         tmem_st16(sbuf + 16, pk + 16);
         tmem_st_wait();
         tc_fence_before();
-        mbar_arrive(&sm.p_full[bc & 1]);
+        mbar_arrive(&sm.p_full[h][bc & 1]);
         ++bc;
       }
       if (!ok) break;
       mbar_arrive(&sm.tile_empty[tb]);
       // ---- epilogue: merge the two halves of every row
       // the PV of the tile's last block completes after all earlier ones
-      if (!(ok = mbar_wait(&sm.pv_done[(bc - 1) & 1], ((bc - 1) >> 1) & 1, status, 13))) break;
+      if (!(ok = mbar_wait(&sm.pv_done[h][(bc - 1) & 1], ((bc - 1) >> 1) & 1, status, 13))) break;
       sm.ml[h][r] = make_float2(m, l);
       mbar_arrive(&sm.ml_full);
       if (!(ok = mbar_wait(&sm.ml_full, tcount & 1, status, 14))) break;
