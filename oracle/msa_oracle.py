@@ -119,6 +119,30 @@ def qk_norm_rope(x, w, cu_seqlens, eps: float = 1e-6, rope_dim: int = 64,
     return bf16_round(y) if round_bf16 else y
 
 
+def qk_norm_rope_bwd(x, w, dy, cu_seqlens, eps: float = 1e-6, rope_dim: int = 64,
+                     base: float = 1.0e7):
+    """Gradients of the prologue of one tensor [T, H, 128] (gemma norm, then
+    partial RoPE [M31, MB]) for an upstream gradient dy = dL/dy.
+
+    RoPE is a rotation, so dL/dz = R^T dy: the same pairs rotated by the
+    negative angle.  With r = 1 / sqrt(mean(x^2) + eps), xh = x r and
+    z = xh (1 + w):
+        dL/dw = sum over tokens and heads of dz * xh                 [128]
+        dL/dx = r (g - xh * mean(g * xh)),   g = dz (1 + w)          [T, H, 128]
+    (the norm's own derivative: d xh_i / d x_k = r (delta_ik - xh_i xh_k / D)).
+    Returns (dx, dw) in fp64."""
+    x = np.asarray(x, dtype=np.float64)
+    w = np.asarray(w, dtype=np.float64)
+    dy = np.asarray(dy, dtype=np.float64)
+    dz = partial_rope(dy, -positions(cu_seqlens).astype(np.float64), rope_dim, base)
+    r = 1.0 / np.sqrt(np.mean(x * x, axis=-1, keepdims=True) + eps)
+    xh = x * r
+    dw = np.sum(dz * xh, axis=tuple(range(x.ndim - 1)))
+    g = dz * (1.0 + w)
+    dx = r * (g - xh * np.mean(g * xh, axis=-1, keepdims=True))
+    return dx, dw
+
+
 # --------------------------------------------------------------------------- indexer
 
 def block_scores_seq(qi: np.ndarray, ki: np.ndarray, rows: Optional[np.ndarray] = None,

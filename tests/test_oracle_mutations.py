@@ -82,7 +82,33 @@ def _scores_no_causal(qi, ki, rows=None, block=O.BLOCK):
     return out
 
 
-_ORIG = {"select_from_scores": O.select_from_scores}
+def _bwd_rotate_forward(x, w, dy, cu_seqlens, eps=1e-6, rope_dim=64, base=1.0e7):
+    # rotates the gradient by +angle instead of -angle
+    dz = O.partial_rope(np.asarray(dy, np.float64), O.positions(cu_seqlens).astype(np.float64),
+                        rope_dim, base)
+    x = np.asarray(x, np.float64)
+    r = 1.0 / np.sqrt(np.mean(x * x, axis=-1, keepdims=True) + eps)
+    xh = x * r
+    g = dz * (1.0 + np.asarray(w, np.float64))
+    return r * (g - xh * np.mean(g * xh, axis=-1, keepdims=True)), np.sum(dz * xh, axis=(0, 1))
+
+
+def _bwd_drop_norm_term(x, w, dy, cu_seqlens, eps=1e-6, rope_dim=64, base=1.0e7):
+    # forgets that the rms depends on x
+    dz = O.partial_rope(np.asarray(dy, np.float64), -O.positions(cu_seqlens).astype(np.float64),
+                        rope_dim, base)
+    x = np.asarray(x, np.float64)
+    r = 1.0 / np.sqrt(np.mean(x * x, axis=-1, keepdims=True) + eps)
+    return r * dz * (1.0 + np.asarray(w, np.float64)), np.sum(dz * x * r, axis=(0, 1))
+
+
+def _bwd_dw_scaled(x, w, dy, cu_seqlens, eps=1e-6, rope_dim=64, base=1.0e7):
+    # weight gradient taken through the (1 + w) factor a second time
+    dx, dw = _ORIG["qk_norm_rope_bwd"](x, w, dy, cu_seqlens, eps, rope_dim, base)
+    return dx, dw * (1.0 + np.asarray(w, np.float64))
+
+
+_ORIG = {"select_from_scores": O.select_from_scores, "qk_norm_rope_bwd": O.qk_norm_rope_bwd}
 
 MUTATIONS = [
     ("partial_rope", _rope_adjacent_pairs, [P.test_rope_matches_complex_rotation]),
@@ -97,6 +123,9 @@ MUTATIONS = [
     ("_row_grads", _grads_without_delta, [P.test_backward_finite_differences]),
     ("_row_grads", _grads_transposed_dp, [P.test_backward_finite_differences]),
     ("block_scores_seq", _scores_no_causal, [P.test_block_scores_brute_force]),
+    ("qk_norm_rope_bwd", _bwd_rotate_forward, [P.test_prologue_backward_finite_differences]),
+    ("qk_norm_rope_bwd", _bwd_drop_norm_term, [P.test_prologue_backward_scale_invariance]),
+    ("qk_norm_rope_bwd", _bwd_dw_scaled, [P.test_prologue_backward_matches_autograd]),
 ]
 
 

@@ -129,6 +129,76 @@ def test_prologue_is_norm_then_rope_then_bf16():
     assert np.all(O.bf16_round(y) == y)
 
 
+def _prologue_case(seed, T=9, H=2, D=128, cu=(0, 4, 9)):
+    r = rng(seed)
+    x = r.standard_normal((T, H, D)) * 1.5
+    w = r.standard_normal(D) * 0.3
+    dy = r.standard_normal((T, H, D))
+    return x, w, dy, np.array(cu)
+
+
+def test_prologue_backward_finite_differences():
+    """Central differences of L = sum(dy * y(x, w)) against the closed form, for
+    rotated and pass-through channels, at several positions."""
+    x, w, dy, cu = _prologue_case(21)
+    loss = lambda x_, w_: float(np.sum(dy * O.qk_norm_rope(x_, w_, cu, round_bf16=False)))
+    dx, dw = O.qk_norm_rope_bwd(x, w, dy, cu)
+    h = 1e-6
+    for idx in [(0, 0, 3), (2, 1, 40), (3, 0, 70), (5, 1, 10), (8, 0, 127), (7, 1, 33)]:
+        xp = x.copy(); xp[idx] += h
+        xm = x.copy(); xm[idx] -= h
+        fd = (loss(xp, w) - loss(xm, w)) / (2 * h)
+        assert fd == pytest.approx(dx[idx], rel=1e-6, abs=1e-8), idx
+    for c in [0, 31, 32, 63, 64, 100]:
+        wp = w.copy(); wp[c] += h
+        wm = w.copy(); wm[c] -= h
+        fd = (loss(x, wp) - loss(x, wm)) / (2 * h)
+        assert fd == pytest.approx(dw[c], rel=1e-6, abs=1e-8), c
+
+
+def test_prologue_backward_matches_autograd():
+    """fp64 torch autograd through an independent statement of the forward."""
+    x, w, dy, cu = _prologue_case(22, T=13, H=3, cu=(0, 5, 6, 13))
+    pos = torch.tensor(O.positions(cu), dtype=torch.float64)
+    xt = torch.tensor(x, requires_grad=True)
+    wt = torch.tensor(w, requires_grad=True)
+    z = xt * torch.rsqrt((xt * xt).mean(-1, keepdim=True) + 1e-6) * (1 + wt)
+    inv = 1e7 ** (-torch.arange(0, 64, 2, dtype=torch.float64) / 64)
+    ang = pos[:, None, None] * inv[None, None, :]
+    z1, z2, rest = z[..., :32], z[..., 32:64], z[..., 64:]
+    y = torch.cat([z1 * torch.cos(ang) - z2 * torch.sin(ang),
+                   z2 * torch.cos(ang) + z1 * torch.sin(ang), rest], dim=-1)
+    (y * torch.tensor(dy)).sum().backward()
+    dx, dw = O.qk_norm_rope_bwd(x, w, dy, cu)
+    np.testing.assert_allclose(dx, xt.grad.numpy(), rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(dw, wt.grad.numpy(), rtol=1e-10, atol=1e-12)
+
+
+def test_prologue_backward_reduces_to_plain_rmsnorm():
+    """w = 0 and every token at position 0 (one-token sequences): the textbook
+    RMSNorm gradient dx = (dy - y mean(dy y)) / rms, and dw = sum dy * y."""
+    T = 5
+    x, _, dy, _ = _prologue_case(23, T=T)
+    cu = np.arange(T + 1)
+    w = np.zeros(x.shape[-1])
+    rms = np.sqrt(np.mean(x * x, axis=-1, keepdims=True) + 1e-6)
+    y = x / rms
+    want = (dy - y * np.mean(dy * y, axis=-1, keepdims=True)) / rms
+    dx, dw = O.qk_norm_rope_bwd(x, w, dy, cu)
+    np.testing.assert_allclose(dx, want, rtol=1e-12, atol=1e-14)
+    np.testing.assert_allclose(dw, np.sum(dy * y, axis=(0, 1)), rtol=1e-12, atol=1e-12)
+
+
+def test_prologue_backward_scale_invariance():
+    """With eps -> 0 the norm output does not depend on the scale of x, so the
+    gradient is orthogonal to x and scales as 1/c."""
+    x, w, dy, cu = _prologue_case(24)
+    dx, _ = O.qk_norm_rope_bwd(x, w, dy, cu, eps=0.0)
+    assert np.max(np.abs(np.sum(dx * x, axis=-1))) < 1e-10
+    dx3, _ = O.qk_norm_rope_bwd(3.0 * x, w, dy, cu, eps=0.0)
+    np.testing.assert_allclose(dx3, dx / 3.0, rtol=1e-10, atol=1e-14)
+
+
 # ------------------------------------------------------------------ indexer
 
 def _brute_scores(qi, ki, block):
