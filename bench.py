@@ -47,6 +47,7 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-prologue-bwd", action="store_true")
     return ap.parse_args()
 
 
@@ -149,6 +150,7 @@ def run_reference(args):
 def kernel_source_hash(name: str) -> str:
     files = {"sparse_bwd_kernel": "sparse_bwd.cu", "sparse_fwd_kernel": "sparse_fwd.cu",
              "index_select_kernel": "index_select.cu", "prologue_kernel": "prologue.cu",
+             "prologue_bwd_kernel": "prologue.cu",
              "decode_score_kernel": "decode.cu"}
     f = files.get(name)
     if f is None:
@@ -387,6 +389,52 @@ def run_ours(args):
                       "d2h_bytes_per_step": d2h, "steps": n_e2e,
                       "schedule": "upload, compute and download on three streams, "
                                   "double-buffered; each step includes its own copies"}
+
+    # ---- prologue backward (q and k of the same pack): dx, dw from x and dy
+    if not args.no_prologue_bwd:
+        gen = torch.Generator(device=dev).manual_seed(args.seed + 77)
+        dyk = [torch.randn((T, hkv, 128), generator=gen, device=dev).to(torch.bfloat16)
+               for _ in range(args.pool)]
+        dxq = torch.empty((T, hq, 128), dtype=torch.bfloat16, device=dev)
+        dxk = torch.empty((T, hkv, 128), dtype=torch.bfloat16, device=dev)
+        dwq = torch.empty(128, dtype=torch.float32, device=dev)
+        dwk = torch.empty(128, dtype=torch.float32, device=dev)
+        pws = torch.empty(m.workspace_bytes("qk_norm_rope_bwd", T, hq), dtype=torch.uint8,
+                          device=dev)
+
+        def pstep(i):
+            x = pool[i % args.pool]
+            m.msa_qk_norm_rope_bwd(x["q"], x["do"], x["w_q"], x["cu_seqlens"], dx=dxq, dw=dwq,
+                                   workspace=pws)
+            m.msa_qk_norm_rope_bwd(x["k"], dyk[i % args.pool], x["w_k"], x["cu_seqlens"],
+                                   dx=dxk, dw=dwk, workspace=pws)
+
+        for i in range(3):
+            pstep(i)
+        torch.cuda.synchronize(dev)
+        npb = max(10, args.steps)
+        m.msa_trace_begin()
+        p0, p1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        p0.record(stream)
+        for i in range(npb):
+            pstep(i)
+        p1.record(stream)
+        torch.cuda.synchronize(dev)
+        ptrace = m.msa_trace_end()
+        m.msa_check_status(dev)
+        pms = p0.elapsed_time(p1) / npb
+        pbytes = 3 * 2 * T * (hq + hkv) * 128          # x, dy read; dx written (bf16)
+        pgbs = pbytes / (pms * 1e-3) / 1e9
+        out["prologue_bwd"] = {
+            "workload": f"{shape.name}: q ({hq} heads) and k ({hkv})", "ms_per_step": pms,
+            "gbs": pgbs, "bytes_per_step": pbytes,
+            "roofline": {"bound": "hbm", "achieved": pgbs, "peak": peaks.get("hbm_gbs", 6800.0),
+                         "unit": "GB/s", "frac": pgbs / peaks.get("hbm_gbs", 6800.0),
+                         "traffic": traffic_for("prologue_bwd_kernel"),
+                         "peak_source": f"{peak_src} HBM copy"},
+            "kernels": {n: {"launches": v["launches"] // npb, "ms_per_launch": v["ms"] / v["launches"]}
+                        for n, v in ptrace.items()},
+        }
 
     # ---- decode step on the paged-cache workload
     if not args.no_decode:

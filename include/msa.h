@@ -118,6 +118,26 @@ MSA_API msa_status_t msa_qk_norm_rope4(const void* q, void* q_out, int Hq, const
                                        float rope_base, float eps, msa_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * Prologue backward (the gradients of msa_qk_norm_rope for one tensor; the
+ * indexer's prologue needs none: "MiniMax-M3.1-Flash", 5.4 "Notable quirks").
+ * x: the prologue's input, bf16 [T, H, 128]; dy = dL/dy for its output (same
+ * shape, e.g. dq or dk from msa_sparse_attn_bwd).  With z = gemma_norm(x, w)
+ * and y = RoPE(z):  dz = R^T dy (the rotation turned back), r =
+ * 1/sqrt(mean(x^2) + eps), xh = x r, g = dz (1 + w):
+ *   dx = r (g - xh mean(g xh))          bf16 [T, H, 128]  (dx may be dy)
+ *   dw = sum over tokens and heads of dz * xh     fp32 [128] (overwritten)
+ * dw is summed in a fixed order (run to run identical).  Workspace from
+ * msa_qk_norm_rope_bwd_workspace_size; other arguments as for msa_qk_norm_rope.
+ */
+MSA_API size_t msa_qk_norm_rope_bwd_workspace_size(int T, int H);
+
+MSA_API msa_status_t msa_qk_norm_rope_bwd(const void* x, const void* dy, void* dx, float* dw,
+                                          int T, int H, const void* w,
+                                          const int32_t* cu_seqlens, int S, int rope_dim,
+                                          float rope_base, float eps, void* workspace,
+                                          size_t workspace_bytes, msa_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * Index select ("MiniMax-M3.1-Flash", 1 "Model Introduction"; "#4581",
  * "Kernel tuning").  q_idx, k_idx: post-prologue bf16 [T, Hi, 128].
  * For token t at position p and index head h the own block is p / 128; every

@@ -12,6 +12,7 @@ from .api import (  # noqa: F401
     msa_index_select,
     msa_qk_norm_rope,
     msa_qk_norm_rope4,
+    msa_qk_norm_rope_bwd,
     msa_sparse_attn_bwd,
     msa_sparse_attn_fwd,
     msa_trace_begin,

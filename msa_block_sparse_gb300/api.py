@@ -33,6 +33,9 @@ _SIGNATURES = {
     "msa_qk_norm_rope4": (_c_int, [_vp, _vp, _c_int, _vp, _vp, _c_int, _vp, _vp, _vp, _vp,
                                    _c_int, _vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int,
                                    _c_float, _c_float, _vp]),
+    "msa_qk_norm_rope_bwd_workspace_size": (_c_size, [_c_int, _c_int]),
+    "msa_qk_norm_rope_bwd": (_c_int, [_vp, _vp, _vp, _vp, _c_int, _c_int, _vp, _vp, _c_int,
+                                      _c_int, _c_float, _c_float, _vp, _c_size, _vp]),
     "msa_index_select_workspace_size": (_c_size, [_c_int, _c_int, _c_int, _c_int]),
     "msa_index_select": (_c_int, [_vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_int, _vp,
                                   _vp, _c_size, _vp]),
@@ -147,6 +150,30 @@ def msa_qk_norm_rope(x, w, cu_seqlens, out: Optional[torch.Tensor] = None, rope_
     _check(lib().msa_qk_norm_rope(_ptr(x), _ptr(out), T, H, _ptr(w), _ptr(cu_seqlens), S,
                                   rope_dim, rope_base, eps, _stream(x)))
     return out
+
+
+def msa_qk_norm_rope_bwd(x, dy, w, cu_seqlens, dx: Optional[torch.Tensor] = None,
+                         dw: Optional[torch.Tensor] = None, rope_dim: int = 64,
+                         rope_base: float = 1.0e7, eps: float = 1.0e-6,
+                         workspace: Optional[torch.Tensor] = None):
+    """Gradients of msa_qk_norm_rope: (dx bf16 [T, H, 128], dw fp32 [128]) from
+    the prologue input x and dy = dL/dy (pass dx=dy to overwrite dy)."""
+    T, H = x.shape[0], x.shape[1]
+    _req(x, "x", torch.bfloat16, (T, H, D))
+    _req(dy, "dy", torch.bfloat16, (T, H, D))
+    _req(w, "w", torch.bfloat16, (D,))
+    _req(cu_seqlens, "cu_seqlens", torch.int32)
+    dx = torch.empty_like(x) if dx is None else dx
+    _req(dx, "dx", torch.bfloat16, (T, H, D))
+    dw = torch.empty(D, dtype=torch.float32, device=x.device) if dw is None else dw
+    _req(dw, "dw", torch.float32, (D,))
+    S = cu_seqlens.numel() - 1
+    size = lib().msa_qk_norm_rope_bwd_workspace_size(T, H)
+    ws = _workspace(size, x.device, workspace)
+    _check(lib().msa_qk_norm_rope_bwd(_ptr(x), _ptr(dy), _ptr(dx), _ptr(dw), T, H, _ptr(w),
+                                      _ptr(cu_seqlens), S, rope_dim, rope_base, eps, _ptr(ws),
+                                      ws.numel(), _stream(x)))
+    return dx, dw
 
 
 def msa_qk_norm_rope4(q, k, q_idx, k_idx, w_q, w_k, w_qi, w_ki, cu_seqlens, outs=None,
@@ -280,6 +307,6 @@ def msa_decode_step(q, q_idx, k_cache, v_cache, kidx_cache, block_table, cache_l
 
 
 def workspace_bytes(call: str, *args) -> int:
-    """Workspace size of `call` ('index_select', 'sparse_attn_fwd', 'sparse_attn_bwd',
-    'decode_step') for the given sizes, as the C ABI reports it."""
+    """Workspace size of `call` ('qk_norm_rope_bwd', 'index_select', 'sparse_attn_fwd',
+    'sparse_attn_bwd', 'decode_step') for the given sizes, as the C ABI reports it."""
     return int(getattr(lib(), f"msa_{call}_workspace_size")(*args))

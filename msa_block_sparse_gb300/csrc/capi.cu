@@ -395,6 +395,33 @@ msa_status_t msa_qk_norm_rope4(const void* q, void* q_out, int Hq, const void* k
                          static_cast<cudaStream_t>(stream));
 }
 
+size_t msa_qk_norm_rope_bwd_workspace_size(int T, int H) {
+  if (T < 1 || H < 1) return 0;
+  return prologue_bwd_workspace_floats(T) * sizeof(float);
+}
+
+msa_status_t msa_qk_norm_rope_bwd(const void* x, const void* dy, void* dx, float* dw, int T,
+                                  int H, const void* w, const int32_t* cu_seqlens, int S,
+                                  int rope_dim, float rope_base, float eps, void* workspace,
+                                  size_t workspace_bytes, msa_stream_t stream) {
+  MSA_REQUIRE_PTR(x);
+  MSA_REQUIRE_PTR(dy);
+  MSA_REQUIRE_PTR(dx);
+  MSA_REQUIRE_PTR(dw);
+  MSA_REQUIRE_PTR(w);
+  MSA_REQUIRE_PTR(workspace);
+  MSA_TRY(check_pack(cu_seqlens, S, T, T));
+  MSA_TRY(check_rope(rope_dim, rope_base, eps));
+  if (H < 1) return fail(MSA_ERR_INVALID_ARG, "H must be >= 1");
+  if (workspace_bytes < msa_qk_norm_rope_bwd_workspace_size(T, H))
+    return fail(MSA_ERR_INVALID_ARG, "workspace too small");
+  using bf = __nv_bfloat16;
+  return launch_prologue_bwd(static_cast<const bf*>(x), static_cast<const bf*>(dy),
+                             static_cast<bf*>(dx), dw, static_cast<const bf*>(w), H, cu_seqlens,
+                             S, T, rope_base, eps, static_cast<float*>(workspace),
+                             static_cast<cudaStream_t>(stream));
+}
+
 // ---------------------------------------------------------------- index select
 
 size_t msa_index_select_workspace_size(int T, int S, int Hi, int max_seqlen) {

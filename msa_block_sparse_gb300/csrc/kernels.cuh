@@ -18,6 +18,11 @@ struct PrologueJob {
 };
 msa_status_t launch_prologue(const PrologueJob* jobs, int njobs, const int32_t* cu, int S,
                              int T, float rope_base, float eps, cudaStream_t stream);
+size_t prologue_bwd_workspace_floats(int T);
+msa_status_t launch_prologue_bwd(const __nv_bfloat16* x, const __nv_bfloat16* dy,
+                                 __nv_bfloat16* dx, float* dw, const __nv_bfloat16* w, int H,
+                                 const int32_t* cu, int S, int T, float rope_base, float eps,
+                                 float* dw_part, cudaStream_t stream);
 
 // ---------------------------------------------------------------- index select
 msa_status_t launch_index_select(const void* q_idx, const void* k_idx, const int32_t* cu, int S,

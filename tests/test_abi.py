@@ -47,6 +47,8 @@ def test_workspace_sizes_are_host_only(lib):
     assert big >= 32768 * 64 * 128 * 4 and small < big
     assert lib.msa_decode_step_workspace_size(64, 64, 4, 256) >= 64 * 4 * 256 * 4
     assert lib.msa_sparse_attn_fwd_workspace_size(0, 1, 16, 1, 1) == 0
+    assert lib.msa_qk_norm_rope_bwd_workspace_size(16384, 16) >= 16384 // 16 * 128 * 4
+    assert lib.msa_qk_norm_rope_bwd_workspace_size(0, 16) == 0
 
 
 FAKE = ctypes.c_void_p(1 << 20)   # 16-byte aligned, never dereferenced: validation fails first

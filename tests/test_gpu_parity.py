@@ -141,6 +141,36 @@ def test_prologue_matches_oracle(m, name):
         assert np.mean(off > 0) < 0.01, f"{n}: {np.mean(off > 0):.4f} of elements off by a step"
 
 
+@pytest.mark.parametrize("name", ["tiny", "ragged"])
+def test_prologue_backward_matches_oracle(m, name):
+    """dx (bf16) and dw (fp32) of the q and k prologues against the fp64 closed
+    form: every element of dx within one bf16 step (plus a small fp32 term),
+    dw to 1e-4 relative; dx written over dy gives the same bits; dw is the same
+    on a second run."""
+    shape = SMALL[name]
+    cpu, gpu = inputs(name, shape)
+    cu = gpu["cu_seqlens"]
+    cun = cpu["cu_seqlens"].numpy()
+    gen = torch.Generator().manual_seed(7)
+    for n, wn in (("q", "w_q"), ("k", "w_k")):
+        dy_cpu = torch.randn(cpu[n].shape, generator=gen).to(torch.bfloat16)
+        dy = dy_cpu.to(DEV)
+        dx, dw = m.msa_qk_norm_rope_bwd(gpu[n], dy, gpu[wn], cu)
+        dy2 = dy.clone()
+        dx2, dw2 = m.msa_qk_norm_rope_bwd(gpu[n], dy2, gpu[wn], cu, dx=dy2)
+        m.msa_check_status()
+        assert torch.equal(dx2, dx) and torch.equal(dw2, dw), n
+        want_dx, want_dw = O.qk_norm_rope_bwd(f64(cpu[n]), f64(cpu[wn]), f64(dy_cpu), cun)
+        g = f64(dx)
+        off = np.abs(g - want_dx)
+        row_scale = np.max(np.abs(want_dx), axis=-1, keepdims=True)
+        tol = bf16_step(want_dx) * 1.0001 + 1e-5 * row_scale
+        worst = float(np.max(off - tol))
+        assert worst <= 0, f"{n} dx: {int(np.sum(off > tol))} elements beyond tolerance, " \
+                           f"worst excess {worst:.3e}"
+        assert rel_l2(f64(dw), want_dw) <= 1e-4, f"{n} dw rel-L2 {rel_l2(f64(dw), want_dw):.3e}"
+
+
 # ------------------------------------------------------------------ index select
 
 @pytest.mark.parametrize("name", ["tiny", "ragged"])
