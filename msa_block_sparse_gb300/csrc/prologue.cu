@@ -221,11 +221,12 @@ msa_status_t launch_prologue(const PrologueJob* jobs, int njobs, const int32_t* 
 // tokens and heads).  RoPE is a rotation, so dz = R^T dy (the pairs turned back
 // by the angle); with r = rsqrt(mean(x^2) + eps), xh = x r, g = dz (1 + w):
 //   dx = r (g - xh mean(g xh)),   dw = sum dz xh.
-// Same layout as the forward: a CTA takes 16 tokens, 8 threads per row, thread
-// c < 4 holding the rotated pairs (8c + e, 8c + 32 + e).  Each thread sums dw
-// for its 16 channels over its rows; the CTA adds its 32 row slots into one
-// partial row of dw_part, and prologue_bwd_sum_kernel adds the partials in a
-// fixed order (the result does not depend on scheduling).
+// Same layout as the forward: groups of 16 tokens, 8 threads per row, thread
+// c < 4 holding the rotated pairs (8c + e, 8c + 32 + e).  CTAs (two per SM)
+// stride over the groups; each thread sums dw for its 16 channels over all its
+// rows, the CTA adds its 32 row slots into one partial row of dw_part, and
+// prologue_bwd_sum_kernel adds the partials in a fixed order (the result does
+// not depend on scheduling).
 
 constexpr int kProBwdUnroll = 2;
 
@@ -237,35 +238,13 @@ __global__ void __launch_bounds__(kProThreads) prologue_bwd_kernel(
   __shared__ float2 cs[kProTokens][kRopeDim / 2];
   __shared__ float wsh[kD];
   __shared__ float red[kProSlots][kD];
-  const int t0 = blockIdx.x * kProTokens;
   const int tid = threadIdx.x;
   const int c = tid & 7;
   const int slot = tid >> 3;
   const int off0 = (c < 4) ? 8 * c : 64 + 16 * (c - 4);
   const int off1 = (c < 4) ? 8 * c + 32 : 64 + 16 * (c - 4) + 8;
   for (int k = tid; k < kD; k += blockDim.x) wsh[k] = 1.f + __bfloat162float(w[k]);
-  for (int q = tid; q < kProTokens * (kRopeDim / 2); q += blockDim.x) {
-    const int qt = q / (kRopeDim / 2), i = q % (kRopeDim / 2);
-    const int t = t0 + qt;
-    float cv = 1.f, sv = 0.f;
-    if (t < T) {
-      int lo = 0, hi = S;   // largest s with cu[s] <= t
-      while (hi - lo > 1) {
-        int mid = (lo + hi) >> 1;
-        if (__ldg(cu + mid) <= t) lo = mid; else hi = mid;
-      }
-      const unsigned long long pos = static_cast<unsigned long long>(t - __ldg(cu + lo));
-      const long long ang = static_cast<long long>(pos * turns.f[i]);
-      const float a = static_cast<float>(ang) * 1.0842021724855044e-19f;   // * 2^-63
-      sincospif(a, &sv, &cv);
-    }
-    cs[qt][i] = make_float2(cv, sv);
-  }
   __syncthreads();
-
-  const int ntok = min(kProTokens, T - t0);
-  const int rows = ntok * H;
-  const size_t row_base = static_cast<size_t>(t0) * H;   // the CTA's rows are contiguous
   float wl[16];
 #pragma unroll
   for (int e = 0; e < 8; ++e) {
@@ -275,102 +254,129 @@ __global__ void __launch_bounds__(kProThreads) prologue_bwd_kernel(
   float aw[16];
 #pragma unroll
   for (int e = 0; e < 16; ++e) aw[e] = 0.f;
-
-  // the loop bound is uniform over the CTA: every lane reaches the shuffles
-  for (int base = 0; base < rows; base += kProSlots * kProBwdUnroll) {
-    uint4 xa[kProBwdUnroll], xb[kProBwdUnroll], ga[kProBwdUnroll], gb[kProBwdUnroll];
-#pragma unroll
-    for (int u = 0; u < kProBwdUnroll; ++u) {
-      const int r = base + slot + kProSlots * u;
-      xa[u] = xb[u] = ga[u] = gb[u] = make_uint4(0, 0, 0, 0);
-      if (r < rows) {
-        const __nv_bfloat16* xr = x + (row_base + r) * kD;
-        const __nv_bfloat16* gr = dy + (row_base + r) * kD;
-        xa[u] = __ldcs(reinterpret_cast<const uint4*>(xr + off0));
-        xb[u] = __ldcs(reinterpret_cast<const uint4*>(xr + off1));
-        ga[u] = __ldcs(reinterpret_cast<const uint4*>(gr + off0));
-        gb[u] = __ldcs(reinterpret_cast<const uint4*>(gr + off1));
+  const int ngroups = (T + kProTokens - 1) / kProTokens;
+  // grid-stride over groups of 16 tokens; dw accumulates across all of them
+  for (int grp = blockIdx.x; grp < ngroups; grp += gridDim.x) {
+    const int t0 = grp * kProTokens;
+    __syncthreads();                       // the previous group's angles are consumed
+    for (int q = tid; q < kProTokens * (kRopeDim / 2); q += blockDim.x) {
+      const int qt = q / (kRopeDim / 2), i = q % (kRopeDim / 2);
+      const int t = t0 + qt;
+      float cv = 1.f, sv = 0.f;
+      if (t < T) {
+        int lo = 0, hi = S;   // largest s with cu[s] <= t
+        while (hi - lo > 1) {
+          int mid = (lo + hi) >> 1;
+          if (__ldg(cu + mid) <= t) lo = mid; else hi = mid;
+        }
+        const unsigned long long pos = static_cast<unsigned long long>(t - __ldg(cu + lo));
+        const long long ang = static_cast<long long>(pos * turns.f[i]);
+        const float a = static_cast<float>(ang) * 1.0842021724855044e-19f;   // * 2^-63
+        sincospif(a, &sv, &cv);
       }
+      cs[qt][i] = make_float2(cv, sv);
     }
+    __syncthreads();
+
+    const int ntok = min(kProTokens, T - t0);
+    const int rows = ntok * H;
+    const size_t row_base = static_cast<size_t>(t0) * H;   // the CTA's rows are contiguous
+    // the loop bound is uniform over the CTA: every lane reaches the shuffles
+    for (int base = 0; base < rows; base += kProSlots * kProBwdUnroll) {
+      uint4 xa[kProBwdUnroll], xb[kProBwdUnroll], ga[kProBwdUnroll], gb[kProBwdUnroll];
 #pragma unroll
-    for (int u = 0; u < kProBwdUnroll; ++u) {
-      const int r = base + slot + kProSlots * u;
-      const bool valid = r < rows;
-      const int tl = valid ? r / H : 0;
-      float xv[16], dz[16];
-      {
-        const __nv_bfloat162* pa = reinterpret_cast<const __nv_bfloat162*>(&xa[u]);
-        const __nv_bfloat162* pb = reinterpret_cast<const __nv_bfloat162*>(&xb[u]);
-        const __nv_bfloat162* qa = reinterpret_cast<const __nv_bfloat162*>(&ga[u]);
-        const __nv_bfloat162* qb = reinterpret_cast<const __nv_bfloat162*>(&gb[u]);
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float2 fa = __bfloat1622float2(pa[e]), fb = __bfloat1622float2(pb[e]);
-          const float2 da = __bfloat1622float2(qa[e]), db = __bfloat1622float2(qb[e]);
-          xv[2 * e] = fa.x;
-          xv[2 * e + 1] = fa.y;
-          xv[8 + 2 * e] = fb.x;
-          xv[8 + 2 * e + 1] = fb.y;
-          dz[2 * e] = da.x;
-          dz[2 * e + 1] = da.y;
-          dz[8 + 2 * e] = db.x;
-          dz[8 + 2 * e + 1] = db.y;
+      for (int u = 0; u < kProBwdUnroll; ++u) {
+        const int r = base + slot + kProSlots * u;
+        xa[u] = xb[u] = ga[u] = gb[u] = make_uint4(0, 0, 0, 0);
+        if (r < rows) {
+          const __nv_bfloat16* xr = x + (row_base + r) * kD;
+          const __nv_bfloat16* gr = dy + (row_base + r) * kD;
+          xa[u] = __ldcs(reinterpret_cast<const uint4*>(xr + off0));
+          xb[u] = __ldcs(reinterpret_cast<const uint4*>(xr + off1));
+          ga[u] = __ldcs(reinterpret_cast<const uint4*>(gr + off0));
+          gb[u] = __ldcs(reinterpret_cast<const uint4*>(gr + off1));
         }
       }
-      if (c < 4) {
-        // dz = R^T dy for the pairs (8c + e, 8c + 32 + e), frequency 8c + e
-        const float4* cp = reinterpret_cast<const float4*>(&cs[tl][8 * c]);
 #pragma unroll
-        for (int e2 = 0; e2 < 4; ++e2) {
-          const float4 q4 = cp[e2];
-          const float cc[2] = {q4.x, q4.z}, sn[2] = {q4.y, q4.w};
+      for (int u = 0; u < kProBwdUnroll; ++u) {
+        const int r = base + slot + kProSlots * u;
+        const bool valid = r < rows;
+        const int tl = valid ? r / H : 0;
+        float xv[16], dz[16];
+        {
+          const __nv_bfloat162* pa = reinterpret_cast<const __nv_bfloat162*>(&xa[u]);
+          const __nv_bfloat162* pb = reinterpret_cast<const __nv_bfloat162*>(&xb[u]);
+          const __nv_bfloat162* qa = reinterpret_cast<const __nv_bfloat162*>(&ga[u]);
+          const __nv_bfloat162* qb = reinterpret_cast<const __nv_bfloat162*>(&gb[u]);
 #pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const int e = 2 * e2 + h;
-            const float d1 = dz[e], d2 = dz[8 + e];
-            dz[e] = d1 * cc[h] + d2 * sn[h];
-            dz[8 + e] = d2 * cc[h] - d1 * sn[h];
+          for (int e = 0; e < 4; ++e) {
+            const float2 fa = __bfloat1622float2(pa[e]), fb = __bfloat1622float2(pb[e]);
+            const float2 da = __bfloat1622float2(qa[e]), db = __bfloat1622float2(qb[e]);
+            xv[2 * e] = fa.x;
+            xv[2 * e + 1] = fa.y;
+            xv[8 + 2 * e] = fb.x;
+            xv[8 + 2 * e + 1] = fb.y;
+            dz[2 * e] = da.x;
+            dz[2 * e + 1] = da.y;
+            dz[8 + 2 * e] = db.x;
+            dz[8 + 2 * e + 1] = db.y;
           }
         }
-      }
-      float s4[4] = {0.f, 0.f, 0.f, 0.f};
+        if (c < 4) {
+          // dz = R^T dy for the pairs (8c + e, 8c + 32 + e), frequency 8c + e
+          const float4* cp = reinterpret_cast<const float4*>(&cs[tl][8 * c]);
 #pragma unroll
-      for (int e = 0; e < 16; ++e) s4[e & 3] = fmaf(xv[e], xv[e], s4[e & 3]);
-      float ss = (s4[0] + s4[1]) + (s4[2] + s4[3]);
+          for (int e2 = 0; e2 < 4; ++e2) {
+            const float4 q4 = cp[e2];
+            const float cc[2] = {q4.x, q4.z}, sn[2] = {q4.y, q4.w};
 #pragma unroll
-      for (int m = 4; m >= 1; m >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, m);
-      const float rinv = rsqrtf(ss * (1.f / kD) + eps);
-      float xh[16], gg[16];
-      float d4[4] = {0.f, 0.f, 0.f, 0.f};
+            for (int h = 0; h < 2; ++h) {
+              const int e = 2 * e2 + h;
+              const float d1 = dz[e], d2 = dz[8 + e];
+              dz[e] = d1 * cc[h] + d2 * sn[h];
+              dz[8 + e] = d2 * cc[h] - d1 * sn[h];
+            }
+          }
+        }
+        float s4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int e = 0; e < 16; ++e) {
-        xh[e] = xv[e] * rinv;
-        gg[e] = dz[e] * wl[e];
-        d4[e & 3] = fmaf(gg[e], xh[e], d4[e & 3]);
-      }
-      float dot = (d4[0] + d4[1]) + (d4[2] + d4[3]);
+        for (int e = 0; e < 16; ++e) s4[e & 3] = fmaf(xv[e], xv[e], s4[e & 3]);
+        float ss = (s4[0] + s4[1]) + (s4[2] + s4[3]);
 #pragma unroll
-      for (int m = 4; m >= 1; m >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, m);
-      const float mean = dot * (1.f / kD);
-      if (valid) {
-        float o[16];
+        for (int m = 4; m >= 1; m >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, m);
+        const float rinv = rsqrtf(ss * (1.f / kD) + eps);
+        float xh[16], gg[16];
+        float d4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
-          o[e] = rinv * (gg[e] - xh[e] * mean);
-          aw[e] = fmaf(dz[e], xh[e], aw[e]);
+          xh[e] = xv[e] * rinv;
+          gg[e] = dz[e] * wl[e];
+          d4[e & 3] = fmaf(gg[e], xh[e], d4[e & 3]);
         }
-        uint4 oa, ob;
-        oa.x = pack_bf16x2(o[0], o[1]);
-        oa.y = pack_bf16x2(o[2], o[3]);
-        oa.z = pack_bf16x2(o[4], o[5]);
-        oa.w = pack_bf16x2(o[6], o[7]);
-        ob.x = pack_bf16x2(o[8], o[9]);
-        ob.y = pack_bf16x2(o[10], o[11]);
-        ob.z = pack_bf16x2(o[12], o[13]);
-        ob.w = pack_bf16x2(o[14], o[15]);
-        __nv_bfloat16* dr = dx + (row_base + r) * kD;
-        *reinterpret_cast<uint4*>(dr + off0) = oa;
-        *reinterpret_cast<uint4*>(dr + off1) = ob;
+        float dot = (d4[0] + d4[1]) + (d4[2] + d4[3]);
+#pragma unroll
+        for (int m = 4; m >= 1; m >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, m);
+        const float mean = dot * (1.f / kD);
+        if (valid) {
+          float o[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            o[e] = rinv * (gg[e] - xh[e] * mean);
+            aw[e] = fmaf(dz[e], xh[e], aw[e]);
+          }
+          uint4 oa, ob;
+          oa.x = pack_bf16x2(o[0], o[1]);
+          oa.y = pack_bf16x2(o[2], o[3]);
+          oa.z = pack_bf16x2(o[4], o[5]);
+          oa.w = pack_bf16x2(o[6], o[7]);
+          ob.x = pack_bf16x2(o[8], o[9]);
+          ob.y = pack_bf16x2(o[10], o[11]);
+          ob.z = pack_bf16x2(o[12], o[13]);
+          ob.w = pack_bf16x2(o[14], o[15]);
+          __nv_bfloat16* dr = dx + (row_base + r) * kD;
+          *reinterpret_cast<uint4*>(dr + off0) = oa;
+          *reinterpret_cast<uint4*>(dr + off1) = ob;
+        }
       }
     }
   }
@@ -407,8 +413,18 @@ __global__ void __launch_bounds__(1024) prologue_bwd_sum_kernel(const float* __r
   }
 }
 
+constexpr int kProBwdMaxCtas = 2 * 1024;   // partial rows at most (2 per SM)
+
+static int prologue_bwd_ctas(int T) {
+  const int groups = (T + kProTokens - 1) / kProTokens;
+  int ctas = 2 * device_sm_count();
+  if (ctas > kProBwdMaxCtas) ctas = kProBwdMaxCtas;
+  return groups < ctas ? groups : ctas;
+}
+
 size_t prologue_bwd_workspace_floats(int T) {
-  return static_cast<size_t>((T + kProTokens - 1) / kProTokens) * kD;
+  const int groups = (T + kProTokens - 1) / kProTokens;
+  return static_cast<size_t>(groups < kProBwdMaxCtas ? groups : kProBwdMaxCtas) * kD;
 }
 
 msa_status_t launch_prologue_bwd(const __nv_bfloat16* x, const __nv_bfloat16* dy,
@@ -421,7 +437,7 @@ msa_status_t launch_prologue_bwd(const __nv_bfloat16* x, const __nv_bfloat16* dy
     double f = std::pow(static_cast<double>(rope_base), -2.0 * i / kRopeDim);
     turns.f[i] = static_cast<unsigned long long>(f / two_pi * 18446744073709551616.0);
   }
-  const int nparts = (T + kProTokens - 1) / kProTokens;
+  const int nparts = prologue_bwd_ctas(T);
   {
     TraceScope trace_("prologue_bwd_kernel", stream);
     prologue_bwd_kernel<<<nparts, kProThreads, 0, stream>>>(x, dy, dx, w, H, turns, cu, S, T,
