@@ -143,6 +143,37 @@ def qk_norm_rope_bwd(x, w, dy, cu_seqlens, eps: float = 1e-6, rope_dim: int = 64
     return dx, dw
 
 
+def decode_append(q, k, v, q_idx, k_idx, w_q, w_k, w_qi, w_ki, k_cache, v_cache,
+                  kidx_cache, block_table, cache_lens, eps: float = 1e-6,
+                  rope_dim: int = 64, base: float = 1.0e7):
+    """Prologue of one new token per sequence, appended to a paged cache.
+
+    Sequence b's new token sits at position p = cache_lens[b] - 1 (the length
+    counts it).  Its q and index-q ([B, H, 128], pre-norm) get the prologue at
+    p; its k and index-k get the same and, with v unchanged, are stored in slot
+    p % 128 of page block_table[b, p // 128] ([page, head, slot, 128] caches).
+    Returns (q_out, q_idx_out, k_cache, v_cache, kidx_cache) as new arrays, the
+    prologue outputs rounded to bf16 like every stored value [M31, MB]."""
+    lens = np.asarray(cache_lens, dtype=np.int64)
+    pos = lens - 1
+
+    def pro(x, w):
+        return bf16_round(partial_rope(gemma_rmsnorm(x, w, eps), pos, rope_dim, base))
+
+    q_out, qi_out = pro(q, w_q), pro(q_idx, w_qi)
+    kn, kin = pro(k, w_k), pro(k_idx, w_ki)
+    kc = np.array(k_cache, dtype=np.float64, copy=True)
+    vc = np.array(v_cache, dtype=np.float64, copy=True)
+    ic = np.array(kidx_cache, dtype=np.float64, copy=True)
+    for b in range(len(lens)):
+        page = int(block_table[b, pos[b] // BLOCK])
+        slot = int(pos[b] % BLOCK)
+        kc[page, :, slot] = kn[b]
+        vc[page, :, slot] = np.asarray(v[b], dtype=np.float64)
+        ic[page, :, slot] = kin[b]
+    return q_out, qi_out, kc, vc, ic
+
+
 # --------------------------------------------------------------------------- indexer
 
 def block_scores_seq(qi: np.ndarray, ki: np.ndarray, rows: Optional[np.ndarray] = None,

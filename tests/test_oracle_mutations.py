@@ -108,7 +108,16 @@ def _bwd_dw_scaled(x, w, dy, cu_seqlens, eps=1e-6, rope_dim=64, base=1.0e7):
     return dx, dw * (1.0 + np.asarray(w, np.float64))
 
 
-_ORIG = {"select_from_scores": O.select_from_scores, "qk_norm_rope_bwd": O.qk_norm_rope_bwd}
+def _append_at_length(q, k, v, q_idx, k_idx, w_q, w_k, w_qi, w_ki, k_cache, v_cache,
+                      kidx_cache, block_table, cache_lens, eps=1e-6, rope_dim=64, base=1.0e7):
+    # the new token placed at position L instead of L - 1
+    return _ORIG["decode_append"](q, k, v, q_idx, k_idx, w_q, w_k, w_qi, w_ki, k_cache, v_cache,
+                                  kidx_cache, block_table, np.asarray(cache_lens) + 1, eps,
+                                  rope_dim, base)
+
+
+_ORIG = {"select_from_scores": O.select_from_scores, "qk_norm_rope_bwd": O.qk_norm_rope_bwd,
+         "decode_append": O.decode_append}
 
 MUTATIONS = [
     ("partial_rope", _rope_adjacent_pairs, [P.test_rope_matches_complex_rotation]),
@@ -126,6 +135,7 @@ MUTATIONS = [
     ("qk_norm_rope_bwd", _bwd_rotate_forward, [P.test_prologue_backward_finite_differences]),
     ("qk_norm_rope_bwd", _bwd_drop_norm_term, [P.test_prologue_backward_scale_invariance]),
     ("qk_norm_rope_bwd", _bwd_dw_scaled, [P.test_prologue_backward_matches_autograd]),
+    ("decode_append", _append_at_length, [P.test_decode_append_matches_prefill_prologue]),
 ]
 
 

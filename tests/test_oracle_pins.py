@@ -201,6 +201,45 @@ def test_prologue_backward_scale_invariance():
 
 # ------------------------------------------------------------------ indexer
 
+def test_decode_append_matches_prefill_prologue():
+    """The appended token's stored k / index-k and its q / index-q equal the
+    prefill prologue of the same token at the same position of its sequence;
+    v is stored verbatim; nothing else in the caches changes."""
+    r = rng(31)
+    lens = np.array([1, 130, 257, 128])
+    B, H, D = len(lens), 2, 128
+    pages = [(L + 127) // 128 for L in lens]
+    P = sum(pages) + 3
+    perm = r.permutation(P)
+    table = np.full((B, max(pages)), -1)
+    at = 0
+    for b in range(B):
+        table[b, :pages[b]] = perm[at:at + pages[b]]
+        at += pages[b]
+    kc, vc, ic = (O.bf16_round(r.standard_normal((P, H, 128, D))) for _ in range(3))
+    q, k, v, qi, ki = (r.standard_normal((B, H, D)) for _ in range(5))
+    v = O.bf16_round(v)
+    w_q, w_k, w_qi, w_ki = (r.standard_normal(D) * 0.2 for _ in range(4))
+    q_out, qi_out, kc2, vc2, ic2 = O.decode_append(q, k, v, qi, ki, w_q, w_k, w_qi, w_ki,
+                                                   kc, vc, ic, table, lens)
+    touched = np.zeros((P, 128), dtype=bool)
+    for b in range(B):
+        # the same token placed at position L-1 of a packed sequence of length L
+        L = int(lens[b])
+        cu = np.array([0, L])
+        pack = lambda x: np.concatenate([r.standard_normal((L - 1, H, D)), x[b][None]], axis=0)
+        for got, x, w in ((q_out[b], q, w_q), (qi_out[b], qi, w_qi)):
+            np.testing.assert_array_equal(got, O.qk_norm_rope(pack(x), w, cu)[-1])
+        page, slot = int(table[b, (L - 1) // 128]), (L - 1) % 128
+        np.testing.assert_array_equal(kc2[page, :, slot], O.qk_norm_rope(pack(k), w_k, cu)[-1])
+        np.testing.assert_array_equal(ic2[page, :, slot], O.qk_norm_rope(pack(ki), w_ki, cu)[-1])
+        np.testing.assert_array_equal(vc2[page, :, slot], v[b])
+        touched[page, slot] = True
+    keep = np.broadcast_to(~touched[:, None, :, None], kc.shape)
+    for old, new in ((kc, kc2), (vc, vc2), (ic, ic2)):
+        np.testing.assert_array_equal(old[keep], new[keep])
+
+
 def _brute_scores(qi, ki, block):
     L = qi.shape[0]
     nb = (L + block - 1) // block
