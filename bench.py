@@ -465,6 +465,46 @@ def run_ours(args):
         dtrace = m.msa_trace_end()
         m.msa_check_status(dev)
         dms = d0.elapsed_time(d1) / nd
+        # the decode append (prologue of the new tokens, written into their pages)
+        # on the same caches, timed on its own
+        agen = torch.Generator(device=dev).manual_seed(args.seed + 5)
+        araw = {n: torch.randn((B, h, 128), generator=agen, device=dev).to(torch.bfloat16)
+                for n, h in (("q", dshape.hq), ("q_idx", dshape.hkv), ("k", dshape.hkv),
+                             ("v", dshape.hkv), ("k_idx", dshape.hkv))}
+        aw = {n: (torch.randn(128, generator=agen, device=dev) * 0.2).to(torch.bfloat16)
+              for n in ("w_q", "w_qi", "w_k", "w_ki")}
+        aq, aqi = torch.empty_like(dx["q"]), torch.empty_like(dx["q_idx"])
+
+        def astep():
+            m.msa_decode_append(araw["q"], araw["q_idx"], araw["k"], araw["v"], araw["k_idx"],
+                                aw["w_q"], aw["w_qi"], aw["w_k"], aw["w_ki"], dx["k_cache"],
+                                dx["v_cache"], dx["kidx_cache"], dx["block_table"],
+                                dx["cache_lens"], q_out=aq, q_idx_out=aqi)
+
+        for _ in range(3):
+            astep()
+        torch.cuda.synchronize(dev)
+        # one call is a few microseconds of GPU work, less than the binding's
+        # host-side checks: time ten calls captured in a CUDA graph instead
+        graph = torch.cuda.CUDAGraph()
+        cap = torch.cuda.Stream(dev)
+        cap.wait_stream(stream)
+        with torch.cuda.stream(cap):
+            with torch.cuda.graph(graph, stream=cap):
+                for _ in range(10):
+                    astep()
+        stream.wait_stream(cap)
+        graph.replay()
+        torch.cuda.synchronize(dev)
+        reps = max(3, nd // 10)
+        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a0.record(stream)
+        for _ in range(reps):
+            graph.replay()
+        a1.record(stream)
+        torch.cuda.synchronize(dev)
+        m.msa_check_status(dev)
+        ams = a0.elapsed_time(a1) / (10 * reps)
         dbytes = workmodel.decode_bytes(dshape.cache_lens, dshape.hq, dshape.hkv)
         gbs = dbytes / (dms * 1e-3) / 1e9
         out["decode"] = {
@@ -478,6 +518,10 @@ def run_ours(args):
                         for n, v in dtrace.items()},
             "l2": "the index-key cache (%.2f GB) is larger than L2" %
                   (dx["kidx_cache"].numel() * 2 / 1e9),
+            "append": {"ms_per_step": ams, "kernel": "decode_append_kernel",
+                       "what": "prologue of B new tokens (q, index-q; k, index-k, v into "
+                               "their pages), timed on its own from a CUDA graph of ten "
+                               "calls"},
         }
         del dx
 

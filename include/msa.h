@@ -214,6 +214,31 @@ MSA_API msa_status_t msa_decode_step(const void* q, const void* q_idx, const voi
                              size_t workspace_bytes, msa_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * Decode append (the prologue of one new token per sequence, written into its
+ * page; "MiniMax-M3.1-Flash", 1 "Model Introduction"; "MiniMax-M3",
+ * "Architecture Notes").  Sequence b's new token is at position
+ * p = cache_lens[b] - 1 (the length counts it).  q [B,Hq,128], q_idx, k, v,
+ * k_idx [B,Hkv,128] are its pre-norm projections (bf16).  Then:
+ *   q_out, q_idx_out = prologue(q, w_q), prologue(q_idx, w_qi) at p
+ *                      (may be q / q_idx themselves, for an in-place update)
+ *   k_cache[page, h, p % 128]    = prologue(k, w_k)[h]
+ *   kidx_cache[page, h, p % 128] = prologue(k_idx, w_ki)[h]
+ *   v_cache[page, h, p % 128]    = v[h]
+ * with page = block_table[b, p / 128] and prologue = gemma norm + partial RoPE
+ * as in msa_qk_norm_rope.  Caches as in msa_decode_step, which can follow on
+ * the same stream.  A length outside [1, 128 max_pages] or a page outside
+ * [0, num_pages) sets MSA_STATUS_BOUNDS and leaves that sequence untouched.
+ */
+MSA_API msa_status_t msa_decode_append(const void* q, const void* q_idx, const void* k,
+                                       const void* v, const void* k_idx, const void* w_q,
+                                       const void* w_qi, const void* w_k, const void* w_ki,
+                                       void* k_cache, void* v_cache, void* kidx_cache,
+                                       const int32_t* block_table, const int32_t* cache_lens,
+                                       int B, int Hq, int Hkv, int num_pages, int max_pages,
+                                       int rope_dim, float rope_base, float eps, void* q_out,
+                                       void* q_idx_out, msa_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * msa_decode_step_static: the decode step above for callers that cannot
  * allocate device memory.  The pages have no counterpart of this call; it
  * exists for integration.  Some callers of a decode step own no allocator:

@@ -36,6 +36,7 @@ _SIGNATURES = {
     "msa_qk_norm_rope_bwd_workspace_size": (_c_size, [_c_int, _c_int]),
     "msa_qk_norm_rope_bwd": (_c_int, [_vp, _vp, _vp, _vp, _c_int, _c_int, _vp, _vp, _c_int,
                                       _c_int, _c_float, _c_float, _vp, _c_size, _vp]),
+    "msa_decode_append": (_c_int, [_vp] * 14 + [_c_int] * 6 + [_c_float, _c_float, _vp, _vp, _vp]),
     "msa_index_select_workspace_size": (_c_size, [_c_int, _c_int, _c_int, _c_int]),
     "msa_index_select": (_c_int, [_vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_int, _vp,
                                   _vp, _c_size, _vp]),
@@ -278,6 +279,34 @@ def msa_sparse_attn_bwd(q, k, v, o, dout, lse, sel, cu_seqlens, max_seqlen: int,
 
 
 # ------------------------------------------------------------------ decode
+
+def msa_decode_append(q, q_idx, k, v, k_idx, w_q, w_qi, w_k, w_ki, k_cache, v_cache,
+                      kidx_cache, block_table, cache_lens, q_out=None, q_idx_out=None,
+                      rope_dim: int = 64, rope_base: float = 1.0e7, eps: float = 1.0e-6):
+    """Prologue of one new token per sequence (position cache_lens - 1), its k,
+    index-k and v written into the paged caches in place; returns (q_out,
+    q_idx_out) for msa_decode_step (pass q / q_idx to update them in place)."""
+    B, Hq = q.shape[0], q.shape[1]
+    P, Hkv = k_cache.shape[0], k_cache.shape[1]
+    maxp = block_table.shape[1]
+    _req(q, "q", torch.bfloat16, (B, Hq, D))
+    for n, t in (("q_idx", q_idx), ("k", k), ("v", v), ("k_idx", k_idx)):
+        _req(t, n, torch.bfloat16, (B, Hkv, D))
+    for n, w in (("w_q", w_q), ("w_qi", w_qi), ("w_k", w_k), ("w_ki", w_ki)):
+        _req(w, n, torch.bfloat16, (D,))
+    for n, c in (("k_cache", k_cache), ("v_cache", v_cache), ("kidx_cache", kidx_cache)):
+        _req(c, n, torch.bfloat16, (P, Hkv, 128, D))
+    _req(block_table, "block_table", torch.int32, (B, maxp))
+    _req(cache_lens, "cache_lens", torch.int32, (B,))
+    q_out = torch.empty_like(q) if q_out is None else q_out
+    q_idx_out = torch.empty_like(q_idx) if q_idx_out is None else q_idx_out
+    _check(lib().msa_decode_append(_ptr(q), _ptr(q_idx), _ptr(k), _ptr(v), _ptr(k_idx),
+                                   _ptr(w_q), _ptr(w_qi), _ptr(w_k), _ptr(w_ki), _ptr(k_cache),
+                                   _ptr(v_cache), _ptr(kidx_cache), _ptr(block_table),
+                                   _ptr(cache_lens), B, Hq, Hkv, P, maxp, rope_dim, rope_base, eps,
+                                   _ptr(q_out), _ptr(q_idx_out), _stream(q)))
+    return q_out, q_idx_out
+
 
 def msa_decode_step(q, q_idx, k_cache, v_cache, kidx_cache, block_table, cache_lens,
                     scale: Optional[float] = None, out: Optional[torch.Tensor] = None,

@@ -576,4 +576,56 @@ msa_status_t msa_decode_step(const void* q, const void* q_idx, const void* k_cac
                        static_cast<cudaStream_t>(stream));
 }
 
+msa_status_t msa_decode_append(const void* q, const void* q_idx, const void* k, const void* v,
+                               const void* k_idx, const void* w_q, const void* w_qi,
+                               const void* w_k, const void* w_ki, void* k_cache, void* v_cache,
+                               void* kidx_cache, const int32_t* block_table,
+                               const int32_t* cache_lens, int B, int Hq, int Hkv, int num_pages,
+                               int max_pages, int rope_dim, float rope_base, float eps,
+                               void* q_out, void* q_idx_out, msa_stream_t stream) {
+  MSA_REQUIRE_PTR(q);
+  MSA_REQUIRE_PTR(q_idx);
+  MSA_REQUIRE_PTR(k);
+  MSA_REQUIRE_PTR(v);
+  MSA_REQUIRE_PTR(k_idx);
+  MSA_REQUIRE_PTR(w_q);
+  MSA_REQUIRE_PTR(w_qi);
+  MSA_REQUIRE_PTR(w_k);
+  MSA_REQUIRE_PTR(w_ki);
+  MSA_REQUIRE_PTR(k_cache);
+  MSA_REQUIRE_PTR(v_cache);
+  MSA_REQUIRE_PTR(kidx_cache);
+  MSA_REQUIRE_PTR(block_table);
+  MSA_REQUIRE_PTR(cache_lens);
+  MSA_REQUIRE_PTR(q_out);
+  MSA_REQUIRE_PTR(q_idx_out);
+  if (B < 1 || num_pages < 1 || max_pages < 1)
+    return fail(MSA_ERR_INVALID_ARG, "B, num_pages and max_pages must be >= 1");
+  if (max_pages > kMaxSeqlen / kBlock)
+    return fail(MSA_ERR_UNSUPPORTED, "max_pages %d above the supported %d", max_pages,
+                kMaxSeqlen / kBlock);
+  MSA_TRY(check_heads(Hq, Hkv));
+  MSA_TRY(check_rope(rope_dim, rope_base, eps));
+  using bf = __nv_bfloat16;
+  DecodeAppendJob j;
+  j.q = static_cast<const bf*>(q);
+  j.q_idx = static_cast<const bf*>(q_idx);
+  j.k = static_cast<const bf*>(k);
+  j.v = static_cast<const bf*>(v);
+  j.k_idx = static_cast<const bf*>(k_idx);
+  j.w_q = static_cast<const bf*>(w_q);
+  j.w_qi = static_cast<const bf*>(w_qi);
+  j.w_k = static_cast<const bf*>(w_k);
+  j.w_ki = static_cast<const bf*>(w_ki);
+  j.q_out = static_cast<bf*>(q_out);
+  j.q_idx_out = static_cast<bf*>(q_idx_out);
+  j.k_cache = static_cast<bf*>(k_cache);
+  j.v_cache = static_cast<bf*>(v_cache);
+  j.kidx_cache = static_cast<bf*>(kidx_cache);
+  j.Hq = Hq;
+  j.Hkv = Hkv;
+  return launch_decode_append(j, block_table, cache_lens, B, num_pages, max_pages, rope_base,
+                              eps, static_cast<cudaStream_t>(stream));
+}
+
 }  // extern "C"

@@ -18,6 +18,17 @@ struct PrologueJob {
 };
 msa_status_t launch_prologue(const PrologueJob* jobs, int njobs, const int32_t* cu, int S,
                              int T, float rope_base, float eps, cudaStream_t stream);
+struct DecodeAppendJob {
+  const __nv_bfloat16 *q, *q_idx, *k, *v, *k_idx;        // new token, pre-norm [B, H, 128]
+  const __nv_bfloat16 *w_q, *w_qi, *w_k, *w_ki;          // [128]
+  __nv_bfloat16 *q_out, *q_idx_out;                       // [B, Hq / Hkv, 128]
+  __nv_bfloat16 *k_cache, *v_cache, *kidx_cache;          // [page, Hkv, 128, 128]
+  int Hq, Hkv;
+};
+msa_status_t launch_decode_append(const DecodeAppendJob& j, const int32_t* block_table,
+                                  const int32_t* cache_lens, int B, int num_pages,
+                                  int max_pages, float rope_base, float eps,
+                                  cudaStream_t stream);
 size_t prologue_bwd_workspace_floats(int T);
 msa_status_t launch_prologue_bwd(const __nv_bfloat16* x, const __nv_bfloat16* dy,
                                  __nv_bfloat16* dx, float* dw, const __nv_bfloat16* w, int H,

@@ -452,4 +452,181 @@ msa_status_t launch_prologue_bwd(const __nv_bfloat16* x, const __nv_bfloat16* dy
   return check_launch("prologue_bwd_sum_kernel");
 }
 
+// ---------------------------------------------------------------- decode append
+//
+// One new token per sequence b at position p = cache_lens[b] - 1: the prologue
+// of its q and index-q (to q_out, q_idx_out) and of its k and index-k, which
+// go with its v (unchanged) into slot p % 128 of page block_table[b, p / 128].
+// Grid (B, row chunks): a CTA takes 32 of sequence b's rows, 8 threads per row
+// as in the prologue kernels.  Row order: q (Hq), index-q (H), k (H),
+// index-k (H), v (H), H = Hkv.
+
+struct AppendArgs {
+  const __nv_bfloat16* src[5];    // q, q_idx, k, k_idx, v  [B, heads, 128]
+  const __nv_bfloat16* w[4];      // w_q, w_qi, w_k, w_ki
+  __nv_bfloat16* q_out;
+  __nv_bfloat16* qi_out;
+  __nv_bfloat16* cache[3];        // k, k_idx, v caches [page, H, 128 slots, 128]
+  int Hq, H;
+};
+
+__global__ void __launch_bounds__(kProThreads) decode_append_kernel(
+    const AppendArgs a, const RopeTurns turns, const int32_t* __restrict__ block_table,
+    const int32_t* __restrict__ cache_lens, int num_pages, int max_pages, float eps,
+    uint32_t* status) {
+  __shared__ float2 cs[kRopeDim / 2];
+  __shared__ float wsh[4][kD];
+  const int b = blockIdx.x, tid = threadIdx.x;
+  const int L = cache_lens[b];
+  if (L < 1 || L > max_pages * kBlock) {
+    if (tid == 0 && blockIdx.y == 0) atomicOr(status, kStatusBounds);
+    return;
+  }
+  const int p = L - 1;
+  const int page = block_table[static_cast<size_t>(b) * max_pages + p / kBlock];
+  if (page < 0 || page >= num_pages) {
+    if (tid == 0 && blockIdx.y == 0) atomicOr(status, kStatusBounds);
+    return;
+  }
+  const int slot_in_page = p % kBlock;
+  for (int k = tid; k < 4 * kD; k += blockDim.x) {
+    const int j = k / kD;
+    const __nv_bfloat16* wp = (j == 0) ? a.w[0] : (j == 1) ? a.w[1] : (j == 2) ? a.w[2] : a.w[3];
+    wsh[j][k % kD] = 1.f + __bfloat162float(wp[k % kD]);
+  }
+  if (tid < kRopeDim / 2) {
+    const long long ang = static_cast<long long>(static_cast<unsigned long long>(p) * turns.f[tid]);
+    float cv, sv;
+    sincospif(static_cast<float>(ang) * 1.0842021724855044e-19f, &sv, &cv);   // * 2^-63
+    cs[tid] = make_float2(cv, sv);
+  }
+  __syncthreads();
+  const int c = tid & 7, rs = tid >> 3;
+  const int off0 = (c < 4) ? 8 * c : 64 + 16 * (c - 4);
+  const int off1 = (c < 4) ? 8 * c + 32 : 64 + 16 * (c - 4) + 8;
+  const int H = a.H, Hq = a.Hq;
+  const int rows = Hq + 4 * H;
+  // the loop bound is uniform over the CTA: every lane reaches the shuffles
+  for (int base = blockIdx.y * kProSlots; base < rows; base += gridDim.y * kProSlots) {
+    const int r = base + rs;
+    const bool valid = r < rows;
+    // job: 0 q, 1 index-q, 2 k, 3 index-k, 4 v
+    int job = 0, h = r;
+    if (r >= Hq) {
+      job = 1 + (r - Hq) / H;
+      h = (r - Hq) % H;
+    }
+    if (!valid) job = 0, h = 0;
+    const int heads = (job == 0) ? Hq : H;
+    const __nv_bfloat16* sbase = (job == 0) ? a.src[0] : (job == 1) ? a.src[1]
+                               : (job == 2) ? a.src[2] : (job == 3) ? a.src[3] : a.src[4];
+    const __nv_bfloat16* src = sbase + (static_cast<size_t>(b) * heads + h) * kD;
+    uint4 xa = make_uint4(0, 0, 0, 0), xb = xa;
+    if (valid) {
+      xa = *reinterpret_cast<const uint4*>(src + off0);
+      xb = *reinterpret_cast<const uint4*>(src + off1);
+    }
+    __nv_bfloat16* dst;
+    if (job <= 1) {
+      dst = (job == 0 ? a.q_out : a.qi_out) + (static_cast<size_t>(b) * heads + h) * kD;
+    } else {
+      __nv_bfloat16* cbase = (job == 2) ? a.cache[0] : (job == 3) ? a.cache[1] : a.cache[2];
+      dst = cbase + ((static_cast<size_t>(page) * H + h) * kBlock + slot_in_page) * kD;
+    }
+    if (job == 4) {                        // v: stored as given
+      if (valid) {
+        *reinterpret_cast<uint4*>(dst + off0) = xa;
+        *reinterpret_cast<uint4*>(dst + off1) = xb;
+      }
+      continue;
+    }
+    float x[16];
+    {
+      const __nv_bfloat162* pa = reinterpret_cast<const __nv_bfloat162*>(&xa);
+      const __nv_bfloat162* pb = reinterpret_cast<const __nv_bfloat162*>(&xb);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 fa = __bfloat1622float2(pa[e]);
+        const float2 fb = __bfloat1622float2(pb[e]);
+        x[2 * e] = fa.x;
+        x[2 * e + 1] = fa.y;
+        x[8 + 2 * e] = fb.x;
+        x[8 + 2 * e + 1] = fb.y;
+      }
+    }
+    float s4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int e = 0; e < 16; ++e) s4[e & 3] = fmaf(x[e], x[e], s4[e & 3]);
+    float ss = (s4[0] + s4[1]) + (s4[2] + s4[3]);
+#pragma unroll
+    for (int m = 4; m >= 1; m >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, m);
+    const float rinv = rsqrtf(ss * (1.f / kD) + eps);
+    const int wj = (job == 0) ? 0 : (job == 1) ? 1 : (job == 2) ? 2 : 3;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      x[e] *= rinv * wsh[wj][off0 + e];
+      x[8 + e] *= rinv * wsh[wj][off1 + e];
+    }
+    if (c < 4) {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const float2 q = cs[8 * c + e];
+        const float x1 = x[e], x2 = x[8 + e];
+        x[e] = x1 * q.x - x2 * q.y;
+        x[8 + e] = x2 * q.x + x1 * q.y;
+      }
+    }
+    if (valid) {
+      uint4 oa, ob;
+      oa.x = pack_bf16x2(x[0], x[1]);
+      oa.y = pack_bf16x2(x[2], x[3]);
+      oa.z = pack_bf16x2(x[4], x[5]);
+      oa.w = pack_bf16x2(x[6], x[7]);
+      ob.x = pack_bf16x2(x[8], x[9]);
+      ob.y = pack_bf16x2(x[10], x[11]);
+      ob.z = pack_bf16x2(x[12], x[13]);
+      ob.w = pack_bf16x2(x[14], x[15]);
+      *reinterpret_cast<uint4*>(dst + off0) = oa;
+      *reinterpret_cast<uint4*>(dst + off1) = ob;
+    }
+  }
+}
+
+msa_status_t launch_decode_append(const DecodeAppendJob& j, const int32_t* block_table,
+                                  const int32_t* cache_lens, int B, int num_pages,
+                                  int max_pages, float rope_base, float eps,
+                                  cudaStream_t stream) {
+  AppendArgs a;
+  a.src[0] = j.q;
+  a.src[1] = j.q_idx;
+  a.src[2] = j.k;
+  a.src[3] = j.k_idx;
+  a.src[4] = j.v;
+  a.w[0] = j.w_q;
+  a.w[1] = j.w_qi;
+  a.w[2] = j.w_k;
+  a.w[3] = j.w_ki;
+  a.q_out = j.q_out;
+  a.qi_out = j.q_idx_out;
+  a.cache[0] = j.k_cache;
+  a.cache[1] = j.kidx_cache;
+  a.cache[2] = j.v_cache;
+  a.Hq = j.Hq;
+  a.H = j.Hkv;
+  RopeTurns turns;
+  const double two_pi = 6.283185307179586476925286766559;
+  for (int i = 0; i < kRopeDim / 2; ++i) {
+    double f = std::pow(static_cast<double>(rope_base), -2.0 * i / kRopeDim);
+    turns.f[i] = static_cast<unsigned long long>(f / two_pi * 18446744073709551616.0);
+  }
+  {
+    TraceScope trace_("decode_append_kernel", stream);
+    dim3 grid(B, (j.Hq + 4 * j.Hkv + kProSlots - 1) / kProSlots);
+    decode_append_kernel<<<grid, kProThreads, 0, stream>>>(a, turns, block_table, cache_lens,
+                                                           num_pages, max_pages, eps,
+                                                           status_word());
+  }
+  return check_launch("decode_append_kernel");
+}
+
 }  // namespace msa

@@ -358,6 +358,61 @@ def test_decode_full_size(m):
     _decode_check(m, W.config(3), seed=0, rows=[0, 1, 17, 33, 63])
 
 
+def test_decode_append_then_step(m):
+    """New tokens appended (prologue + page write) at ragged positions, including
+    the first slot of a fresh page and a one-token cache, then a decode step on
+    the result: append outputs within one bf16 step of the oracle, every other
+    cache byte unchanged, the decode step as in test_decode_small_edges."""
+    shape = W.DecodeShape("decode-append", (1, 128, 129, 300, 2049, 4096), 32, 2, 2)
+    x = W.make_decode(shape, seed=9, device="cpu")
+    gen = torch.Generator().manual_seed(3)
+    B, hq, hkv = shape.B, shape.hq, shape.hkv
+    raw = {n: torch.randn((B, h, 128), generator=gen).to(torch.bfloat16)
+           for n, h in (("q", hq), ("q_idx", hkv), ("k", hkv), ("v", hkv), ("k_idx", hkv))}
+    ws = {n: (torch.randn(128, generator=gen) * 0.2).to(torch.bfloat16)
+          for n in ("w_q", "w_qi", "w_k", "w_ki")}
+    g = {k: v.to(DEV) for k, v in x.items()}
+    gr = {k: v.to(DEV) for k, v in raw.items()}
+    gw = {k: v.to(DEV) for k, v in ws.items()}
+    q_out, qi_out = m.msa_decode_append(gr["q"], gr["q_idx"], gr["k"], gr["v"], gr["k_idx"],
+                                        gw["w_q"], gw["w_qi"], gw["w_k"], gw["w_ki"],
+                                        g["k_cache"], g["v_cache"], g["kidx_cache"],
+                                        g["block_table"], g["cache_lens"])
+    m.msa_check_status()
+    table = x["block_table"].numpy()
+    lens = x["cache_lens"].numpy()
+    oq, oqi, okc, ovc, oic = O.decode_append(
+        f64(raw["q"]), f64(raw["k"]), f64(raw["v"]), f64(raw["q_idx"]), f64(raw["k_idx"]),
+        f64(ws["w_q"]), f64(ws["w_k"]), f64(ws["w_qi"]), f64(ws["w_ki"]),
+        f64(x["k_cache"]), f64(x["v_cache"]), f64(x["kidx_cache"]), table, lens)
+
+    def within_step(got, want, what):
+        off = np.abs(got - want)
+        tol = bf16_step(want) * 1.0001 + 1e-5 * np.max(np.abs(want), axis=-1, keepdims=True)
+        assert np.all(off <= tol), f"{what}: {int(np.sum(off > tol))} elements beyond one bf16 step"
+
+    within_step(f64(q_out), oq, "q_out")
+    within_step(f64(qi_out), oqi, "q_idx_out")
+    touched = np.zeros(x["k_cache"].shape, dtype=bool)
+    for b in range(B):
+        p = int(lens[b]) - 1
+        touched[int(table[b, p // 128]), :, p % 128] = True
+    for n, want in (("k_cache", okc), ("kidx_cache", oic), ("v_cache", ovc)):
+        got = f64(g[n])
+        within_step(got[touched].reshape(-1, 128), want[touched].reshape(-1, 128), n)
+        assert np.array_equal(got[~touched], f64(x[n])[~touched]), f"{n}: untouched bytes changed"
+    # the decode step on the appended caches
+    o, sel = m.msa_decode_step(q_out, qi_out, g["k_cache"], g["v_cache"], g["kidx_cache"],
+                               g["block_table"], g["cache_lens"])
+    m.msa_check_status()
+    ro, rsel, rgap = O.decode_step(f64(q_out), f64(qi_out), f64(g["k_cache"]), f64(g["v_cache"]),
+                                   f64(g["kidx_cache"]), table, lens, SCALE)
+    gsel = sel.cpu().numpy()
+    compare_selection(gsel, rsel, rgap, shape.name)
+    same = np.all(np.all(gsel == rsel, axis=-1), axis=-1)
+    assert_close(f64(o)[same], ro[same], 2e-2, 1e-2, "decode after append")
+
+
 # ------------------------------------------------------------------ pipeline
 
 def test_prefill_pipeline_tiny(m):
