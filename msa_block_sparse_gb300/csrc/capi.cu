@@ -176,6 +176,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ 
                                                     int max_nb, int2* __restrict__ tiles,
                                                     int* __restrict__ num_tiles, int max_tiles,
                                                     uint32_t* status) {
+  pdl_enter();
   extern __shared__ int sh[];
   int* cnt = sh;                // [max_nb + 1]
   int* start = sh + max_nb + 1; // [max_nb + 1]
@@ -233,8 +234,8 @@ msa_status_t launch_plan(const Plan& plan, const int32_t* cu_seqlens, int S, int
   size_t smem = 2 * (max_nb + 1) * sizeof(int);
   {
     TraceScope trace_("plan_kernel", stream);
-    plan_kernel<<<1, 1024, smem, stream>>>(cu_seqlens, S, max_nb, plan.tiles, plan.num_tiles,
-                                         plan.max_tiles, status_word());
+    launch_pdl(plan_kernel, 1, 1024, smem, stream, cu_seqlens, S, max_nb, plan.tiles, plan.num_tiles,
+        plan.max_tiles, status_word());
   }
   return check_launch("plan_kernel");
 }

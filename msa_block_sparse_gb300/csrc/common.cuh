@@ -7,6 +7,7 @@
 #include <cstdint>
 #include <cstddef>
 #include <string>
+#include <utility>
 
 #include "../../include/msa.h"
 
@@ -82,6 +83,25 @@ inline int plan_max_tiles(int T, int S) { return T / kBlock + S; }
 Plan carve_plan(WsCursor& ws, int T, int S);
 msa_status_t launch_plan(const Plan& plan, const int32_t* cu_seqlens, int S, int max_seqlen,
                          cudaStream_t stream);
+
+// Launches `kernel` with programmatic stream serialization, so that its launch
+// overlaps the tail of the previous kernel on `stream`; the kernel itself
+// orders its memory accesses after that kernel with pdl_wait().
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t stream, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 

@@ -50,6 +50,7 @@ __global__ void __launch_bounds__(256) decode_score_kernel(
     const __nv_bfloat16* __restrict__ q_idx, const __nv_bfloat16* __restrict__ kidx_cache,
     const int32_t* __restrict__ block_table, const int32_t* __restrict__ cache_lens, int Hkv,
     int num_pages, int max_pages, float* __restrict__ scores, uint32_t* status) {
+  pdl_enter();
   const int b = blockIdx.y;
   const int L = clamp_len(cache_lens[b], max_pages, status);
   const int npages = (L + kBlock - 1) / kBlock;
@@ -117,6 +118,7 @@ __global__ void __launch_bounds__(256) decode_score_kernel(
 __global__ void __launch_bounds__(128) decode_select_kernel(
     const float* __restrict__ scores, const int32_t* __restrict__ cache_lens, int Hkv,
     int max_pages, int32_t* __restrict__ sel, int32_t* __restrict__ sel_out, uint32_t* status) {
+  pdl_enter();
   __shared__ __align__(16) float key[1024];
   __shared__ int kept[16];
   __shared__ int nkept;
@@ -201,6 +203,7 @@ __global__ void __launch_bounds__(128) decode_attend_kernel(
     const int32_t* __restrict__ cache_lens, const int32_t* __restrict__ sel, int Hq, int Hkv,
     int num_pages, int max_pages, float scale, float* __restrict__ part_o,
     float* __restrict__ part_ml, uint32_t* status) {
+  pdl_enter();
   extern __shared__ uint8_t smem_raw[];
   AttendSmem& sm = *reinterpret_cast<AttendSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                   ~static_cast<uintptr_t>(1023));
@@ -425,6 +428,7 @@ __global__ void __launch_bounds__(128) decode_merge_kernel(const float* __restri
                                                            const float* __restrict__ part_ml,
                                                            int Hq, int Hkv,
                                                            __nv_bfloat16* __restrict__ o) {
+  pdl_enter();
   const int bh = blockIdx.x;
   const int b = bh / Hkv, h = bh % Hkv;
   const int hd = threadIdx.x >> 3, d0 = (threadIdx.x & 7) * 16;
@@ -485,16 +489,16 @@ msa_status_t launch_decode(const void* q, const void* q_idx, const void* k_cache
   dim3 g1((max_pages + kPagesPerCta - 1) / kPagesPerCta, B);
   {
     TraceScope trace_("decode_score_kernel", stream);
-    decode_score_kernel<<<g1, 256, 0, stream>>>(
-      static_cast<const __nv_bfloat16*>(q_idx), static_cast<const __nv_bfloat16*>(kidx_cache),
-      block_table, cache_lens, Hkv, num_pages, max_pages, ws.scores, st);
+    launch_pdl(decode_score_kernel, g1, 256, 0, stream,
+        static_cast<const __nv_bfloat16*>(q_idx), static_cast<const __nv_bfloat16*>(kidx_cache),
+        block_table, cache_lens, Hkv, num_pages, max_pages, ws.scores, st);
   }
   msa_status_t e = check_launch("decode_score_kernel");
   if (e != MSA_OK) return e;
   {
     TraceScope trace_("decode_select_kernel", stream);
-    decode_select_kernel<<<B * Hkv, 128, 0, stream>>>(ws.scores, cache_lens, Hkv, max_pages,
-                                                      ws.sel, sel_out, st);
+    launch_pdl(decode_select_kernel, B * Hkv, 128, 0, stream, ws.scores, cache_lens, Hkv, max_pages,
+        ws.sel, sel_out, st);
   }
   e = check_launch("decode_select_kernel");
   if (e != MSA_OK) return e;
@@ -515,16 +519,16 @@ msa_status_t launch_decode(const void* q, const void* q_idx, const void* k_cache
   dim3 g2(B, Hkv, kDecodeSplits);
   {
     TraceScope trace_("decode_attend_kernel", stream);
-    decode_attend_kernel<<<g2, 128, smem, stream>>>(
-      tk, tv, static_cast<const __nv_bfloat16*>(q), block_table, cache_lens, ws.sel, Hq, Hkv,
-      num_pages, max_pages, scale, ws.part_o, ws.part_ml, st);
+    launch_pdl(decode_attend_kernel, g2, 128, smem, stream,
+        tk, tv, static_cast<const __nv_bfloat16*>(q), block_table, cache_lens, ws.sel, Hq, Hkv,
+        num_pages, max_pages, scale, ws.part_o, ws.part_ml, st);
   }
   e = check_launch("decode_attend_kernel");
   if (e != MSA_OK) return e;
   {
     TraceScope trace_("decode_merge_kernel", stream);
-    decode_merge_kernel<<<B * Hkv, 128, 0, stream>>>(ws.part_o, ws.part_ml, Hq, Hkv,
-                                                   static_cast<__nv_bfloat16*>(o));
+    launch_pdl(decode_merge_kernel, B * Hkv, 128, 0, stream, ws.part_o, ws.part_ml, Hq, Hkv,
+        static_cast<__nv_bfloat16*>(o));
   }
   return check_launch("decode_merge_kernel");
 }

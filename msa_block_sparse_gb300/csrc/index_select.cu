@@ -76,6 +76,7 @@ __global__ void __launch_bounds__(kSelThreads, 1)
                         const __grid_constant__ CUtensorMap tm_k, const int32_t* __restrict__ cu,
                         const int2* __restrict__ tiles, const int* __restrict__ num_tiles, int Hi,
                         int32_t* __restrict__ sel, uint32_t* status) {
+  pdl_enter();
   if (static_cast<int>(blockIdx.x) >= *num_tiles) return;
   extern __shared__ uint8_t smem_raw[];
   SelSmem& sm = *reinterpret_cast<SelSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -228,9 +229,9 @@ msa_status_t launch_index_select(const void* q_idx, const void* k_idx, const int
   dim3 grid(plan.max_tiles, Hi);
   {
     TraceScope trace_("index_select_kernel", stream);
-    index_select_kernel<<<grid, kSelThreads, smem, stream>>>(tq, tk, cu, plan.tiles,
-                                                           plan.num_tiles, Hi, sel,
-                                                           status_word());
+    launch_pdl(index_select_kernel, grid, kSelThreads, smem, stream, tq, tk, cu, plan.tiles,
+        plan.num_tiles, Hi, sel,
+        status_word());
   }
   return check_launch("index_select_kernel");
 }

@@ -41,6 +41,7 @@ __global__ void __launch_bounds__(kProThreads) prologue_kernel(const PrologueArg
                                                                const int32_t* __restrict__ cu,
                                                                int S, int T, float eps,
                                                                uint32_t* status) {
+  pdl_enter();
   __shared__ float2 cs[kProTokens][kRopeDim / 2];
   __shared__ float wsh[4][kD];
   const int t0 = blockIdx.x * kProTokens;
@@ -208,8 +209,8 @@ msa_status_t launch_prologue(const PrologueJob* jobs, int njobs, const int32_t* 
   dim3 grid((T + kProTokens - 1) / kProTokens);
   {
     TraceScope trace_("prologue_kernel", stream);
-    prologue_kernel<<<grid, kProThreads, 0, stream>>>(args, turns, cu, S, T, eps,
-                                                      status_word());
+    launch_pdl(prologue_kernel, grid, kProThreads, 0, stream, args, turns, cu, S, T, eps,
+        status_word());
   }
   return check_launch("prologue_kernel");
 }
@@ -235,6 +236,7 @@ __global__ void __launch_bounds__(kProThreads) prologue_bwd_kernel(
     __nv_bfloat16* __restrict__ dx, const __nv_bfloat16* __restrict__ w, int H,
     const RopeTurns turns, const int32_t* __restrict__ cu, int S, int T, float eps,
     float* __restrict__ dw_part) {
+  pdl_enter();
   __shared__ float2 cs[kProTokens][kRopeDim / 2];
   __shared__ float wsh[kD];
   __shared__ float red[kProSlots][kD];
@@ -399,6 +401,7 @@ __global__ void __launch_bounds__(kProThreads) prologue_bwd_kernel(
 __global__ void __launch_bounds__(1024) prologue_bwd_sum_kernel(const float* __restrict__ part,
                                                                 int nparts,
                                                                 float* __restrict__ dw) {
+  pdl_enter();
   __shared__ float red[8][kD];
   const int ch = threadIdx.x & (kD - 1), k = threadIdx.x >> 7;
   float acc = 0.f;
@@ -440,14 +443,14 @@ msa_status_t launch_prologue_bwd(const __nv_bfloat16* x, const __nv_bfloat16* dy
   const int nparts = prologue_bwd_ctas(T);
   {
     TraceScope trace_("prologue_bwd_kernel", stream);
-    prologue_bwd_kernel<<<nparts, kProThreads, 0, stream>>>(x, dy, dx, w, H, turns, cu, S, T,
-                                                            eps, dw_part);
+    launch_pdl(prologue_bwd_kernel, nparts, kProThreads, 0, stream, x, dy, dx, w, H, turns, cu, S, T,
+        eps, dw_part);
   }
   msa_status_t e = check_launch("prologue_bwd_kernel");
   if (e != MSA_OK) return e;
   {
     TraceScope trace_("prologue_bwd_sum_kernel", stream);
-    prologue_bwd_sum_kernel<<<1, 1024, 0, stream>>>(dw_part, nparts, dw);
+    launch_pdl(prologue_bwd_sum_kernel, 1, 1024, 0, stream, dw_part, nparts, dw);
   }
   return check_launch("prologue_bwd_sum_kernel");
 }
@@ -474,6 +477,7 @@ __global__ void __launch_bounds__(kProThreads) decode_append_kernel(
     const AppendArgs a, const RopeTurns turns, const int32_t* __restrict__ block_table,
     const int32_t* __restrict__ cache_lens, int num_pages, int max_pages, float eps,
     uint32_t* status) {
+  pdl_enter();
   __shared__ float2 cs[kRopeDim / 2];
   __shared__ float wsh[4][kD];
   const int b = blockIdx.x, tid = threadIdx.x;
@@ -622,9 +626,9 @@ msa_status_t launch_decode_append(const DecodeAppendJob& j, const int32_t* block
   {
     TraceScope trace_("decode_append_kernel", stream);
     dim3 grid(B, (j.Hq + 4 * j.Hkv + kProSlots - 1) / kProSlots);
-    decode_append_kernel<<<grid, kProThreads, 0, stream>>>(a, turns, block_table, cache_lens,
-                                                           num_pages, max_pages, eps,
-                                                           status_word());
+    launch_pdl(decode_append_kernel, grid, kProThreads, 0, stream, a, turns, block_table, cache_lens,
+        num_pages, max_pages, eps,
+        status_word());
   }
   return check_launch("decode_append_kernel");
 }

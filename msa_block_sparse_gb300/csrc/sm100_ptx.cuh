@@ -28,6 +28,23 @@ __device__ __forceinline__ uint64_t globaltimer() {
   return t;
 }
 
+// Programmatic dependent launch.  A grid launched with programmatic stream
+// serialization may start while the previous kernel of its stream drains;
+// pdl_wait() returns once that kernel has completed and its writes are
+// visible (immediately for a grid launched without the attribute).  Every
+// kernel of this library calls it, in every CTA, before its first global
+// access, so completion stays ordered along the stream.  pdl_launch() lets
+// the next grid of the stream begin its launch.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+// Both, at the top of a kernel.
+__device__ __forceinline__ void pdl_enter() {
+  pdl_wait();
+  pdl_launch();
+}
+
 __device__ __forceinline__ uint32_t lane_id() {
   uint32_t l;
   asm volatile("mov.u32 %0, %%laneid;" : "=r"(l));

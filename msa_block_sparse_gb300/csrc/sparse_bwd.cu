@@ -109,6 +109,7 @@ __global__ void __launch_bounds__(1024) bwd_items_kernel(const int32_t* __restri
                                                          int4* __restrict__ items,
                                                          int* __restrict__ num_items,
                                                          int max_items, uint32_t* status) {
+  pdl_enter();
   __shared__ int warp_sums[32];
   __shared__ int carry;
   if (threadIdx.x == 0) carry = 0;
@@ -175,6 +176,7 @@ __global__ void __launch_bounds__(kBwdSegment) bwd_lists_kernel(
     const int32_t* __restrict__ cu, const int32_t* __restrict__ sel,
     const int4* __restrict__ items, const int* __restrict__ num_items, int Hkv,
     int* __restrict__ lists, int* __restrict__ list_len) {
+  pdl_enter();
   static_assert(kBwdSegment == 256, "one thread per candidate position");
   __shared__ int warp_cnt[kBwdSegment / 32];
   const int n = *num_items;
@@ -220,6 +222,7 @@ __global__ void __launch_bounds__(256) bwd_delta_kernel(const __nv_bfloat16* __r
                                                         const __nv_bfloat16* __restrict__ dout,
                                                         const float* __restrict__ lse,
                                                         float* __restrict__ lsd, size_t rows) {
+  pdl_enter();
   const int sub = threadIdx.x & 15;
   const size_t row0 =
       (static_cast<size_t>(blockIdx.x) * (blockDim.x >> 4) + (threadIdx.x >> 4)) * kDeltaRows;
@@ -269,6 +272,7 @@ __global__ void bwd_convert_kernel(const float* __restrict__ dq_acc,
                                    __nv_bfloat16* __restrict__ dq, __nv_bfloat16* __restrict__ dk,
                                    __nv_bfloat16* __restrict__ dv, size_t nq8, size_t nkv8,
                                    float scale) {
+  pdl_enter();
   size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   const float* src;
   __nv_bfloat16* dst;
@@ -304,6 +308,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                       const int* __restrict__ num_items, int Hq, int Hkv, float scale,
                       float* __restrict__ dq_acc, float* __restrict__ dk_acc,
                       float* __restrict__ dv_acc, uint32_t* status) {
+  pdl_enter();
   constexpr int G = 16;
   const int n_items = *num_items;
   if (static_cast<int>(blockIdx.x) >= n_items) return;
@@ -747,21 +752,23 @@ msa_status_t launch_sparse_bwd(const void* q, const void* k, const void* v, cons
   {
     TraceScope trace_("bwd_delta_kernel", stream);
     const size_t per_block = 256 / 16 * kDeltaRows;
-    bwd_delta_kernel<<<static_cast<unsigned>((rows + per_block - 1) / per_block), 256, 0, stream>>>(
+    launch_pdl(bwd_delta_kernel, static_cast<unsigned>((rows + per_block - 1) / per_block), 256,
+        0, stream,
         static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dout), lse, ws.lsd,
         rows);
   }
   {
     TraceScope trace_("bwd_items_kernel", stream);
-    bwd_items_kernel<<<1, 1024, 0, stream>>>(cu, S, max_seqlen, bwd_windows(max_seqlen), ws.items,
-                                             ws.num_items, ws.max_items, st);
+    launch_pdl(bwd_items_kernel, 1, 1024, 0, stream, cu, S, max_seqlen, bwd_windows(max_seqlen),
+        ws.items,
+        ws.num_items, ws.max_items, st);
   }
   {
     const int sms = device_sm_count();
     dim3 lgrid(static_cast<unsigned>(ws.max_items < 4 * sms ? ws.max_items : 4 * sms), Hkv);
     TraceScope trace_("bwd_lists_kernel", stream);
-    bwd_lists_kernel<<<lgrid, kBwdSegment, 0, stream>>>(cu, sel, ws.items, ws.num_items, Hkv,
-                                                         ws.lists, ws.list_len);
+    launch_pdl(bwd_lists_kernel, lgrid, kBwdSegment, 0, stream, cu, sel, ws.items, ws.num_items, Hkv,
+        ws.lists, ws.list_len);
   }
   msa_status_t e = check_launch("bwd_delta/items/lists");
   if (e != MSA_OK) return e;
@@ -777,7 +784,7 @@ msa_status_t launch_sparse_bwd(const void* q, const void* k, const void* v, cons
   dim3 grid(static_cast<unsigned>(per_head < ws.max_items ? per_head : ws.max_items), Hkv);
   {
     TraceScope trace_("sparse_bwd_kernel", stream);
-    sparse_bwd_kernel<<<grid, kBwdThreads, smem, stream>>>(
+    launch_pdl(sparse_bwd_kernel, grid, kBwdThreads, smem, stream,
         tq, tk, tv, tdo, ws.lists, ws.list_len, cu, ws.lsd, ws.items, ws.num_items, Hq, Hkv, scale,
         ws.dq_acc, ws.dk_acc, ws.dv_acc, st);
   }
@@ -787,7 +794,7 @@ msa_status_t launch_sparse_bwd(const void* q, const void* k, const void* v, cons
   {
     const size_t n8 = nq / 8 + 2 * (nkv / 8);
     TraceScope trace_("bwd_convert_kernel", stream);
-    bwd_convert_kernel<<<static_cast<unsigned>((n8 + 255) / 256), 256, 0, stream>>>(
+    launch_pdl(bwd_convert_kernel, static_cast<unsigned>((n8 + 255) / 256), 256, 0, stream,
         ws.dq_acc, ws.dk_acc, ws.dv_acc, static_cast<__nv_bfloat16*>(dq),
         static_cast<__nv_bfloat16*>(dk), static_cast<__nv_bfloat16*>(dv), nq / 8, nkv / 8, scale);
   }

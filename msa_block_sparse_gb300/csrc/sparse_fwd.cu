@@ -105,6 +105,7 @@ __global__ void __launch_bounds__(256) fwd_union_kernel(const int32_t* __restric
                                                         const int* __restrict__ num_tiles,
                                                         int Hkv, int* __restrict__ ulist,
                                                         uint32_t* status) {
+  pdl_enter();
   __shared__ uint32_t words_s[8][kMaskWords];
   const int total = *num_tiles * kG;
   const int g = blockIdx.y;
@@ -166,6 +167,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                       const int32_t* __restrict__ cu, const int2* __restrict__ tiles,
                       const int* __restrict__ num_tiles, int Hq, int Hkv, float scale,
                       __nv_bfloat16* __restrict__ o, float* __restrict__ lse, uint32_t* status) {
+  pdl_enter();
   const int total = *num_tiles * kG;
   if (static_cast<int>(blockIdx.x) >= total) return;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -525,12 +527,12 @@ msa_status_t launch_sparse_fwd(const void* q, const void* k, const void* v, cons
     const int cap = 4 * device_sm_count();
     dim3 ugrid(static_cast<unsigned>(ublocks < cap ? ublocks : cap), Hkv);
     TraceScope trace_("fwd_union_kernel", stream);
-    fwd_union_kernel<<<ugrid, 256, 0, stream>>>(sel, cu, plan.tiles, plan.num_tiles, Hkv,
-                                               fw.ulist, status_word());
+    launch_pdl(fwd_union_kernel, ugrid, 256, 0, stream, sel, cu, plan.tiles, plan.num_tiles, Hkv,
+        fw.ulist, status_word());
   }
   {
     TraceScope trace_("sparse_fwd_kernel", stream);
-    sparse_fwd_kernel<<<grid, kFwdThreads, smem, stream>>>(
+    launch_pdl(sparse_fwd_kernel, grid, kFwdThreads, smem, stream,
         tq, tk, tv, fw.ulist, cu, plan.tiles, plan.num_tiles, Hq, Hkv, scale,
         static_cast<__nv_bfloat16*>(o), lse, status_word());
   }
