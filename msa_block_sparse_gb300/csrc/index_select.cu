@@ -175,17 +175,25 @@ __global__ void __launch_bounds__(kSelThreads, 1)
       if (!mbar_wait(&sm.s_full[buf], (b >> 1) & 1, status)) break;
       __syncwarp();
       tc_fence_after();
-      float mx = -INFINITY;
+      // all 128 columns in flight at once, one wait, then the buffer is free
+      // for the MMA two blocks ahead while the row max is taken
+      uint32_t v[128];
 #pragma unroll
-      for (int c = 0; c < 128; c += 32) {
-        uint32_t v[32];
-        tmem_ld32(trow + buf * 128 + c, v);
-        tmem_ld_wait();
-#pragma unroll
-        for (int j = 0; j < 32; ++j) mx = fmaxf(mx, __uint_as_float(v[j]));
-      }
+      for (int c = 0; c < 128; c += 32) tmem_ld32(trow + buf * 128 + c, v + c);
+      tmem_ld_wait();
       tc_fence_before();
       mbar_arrive(&sm.s_empty[buf]);
+      float m4[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const uint32_t* w = v + 32 * q;
+        float t = max3f(__uint_as_float(w[0]), __uint_as_float(w[1]), __uint_as_float(w[2]));
+#pragma unroll
+        for (int j = 3; j < 31; j += 2)
+          t = max3f(t, __uint_as_float(w[j]), __uint_as_float(w[j + 1]));
+        m4[q] = fmaxf(t, __uint_as_float(w[31]));
+      }
+      const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
       float cv = mx;
       int ci = b;
 #pragma unroll
