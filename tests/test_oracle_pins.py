@@ -422,6 +422,56 @@ def test_sparse_forward_and_backward_match_masked_library_attention():
     np.testing.assert_allclose(dvb2, dv[cu[3]:cu[3] + 4, 1], rtol=1e-12, atol=1e-13)
 
 
+def test_narrow_block_regime_matches_masked_library_attention():
+    """The narrow-block variant ("#4581", Kernel tuning: 12 q / 1 kv head, head dim
+    256, 4-token blocks) runs the same oracle with block=4: forward, lse and all
+    three gradients equal masked library attention (fp64 autograd) on a ragged
+    pack with seeded random block subsets, own block kept."""
+    import workloads as W
+    seqlens = (9, 23, 1)
+    cu = np.concatenate([[0], np.cumsum(seqlens)])
+    T, Hq, Hkv, D = sum(seqlens), 12, 1, 256
+    r = rng(21)
+    q, k, v, do = (r.standard_normal((T, h, D)) for h in (Hq, Hkv, Hkv, Hq))
+    g = torch.Generator().manual_seed(3)
+    sel = W.qsa_selection(seqlens, Hkv, 3, g, "cpu").numpy()
+    assert np.all(sel[:, 0, 0] >= 0) and np.any(sel[:, 0, -1] >= 0)
+    assert np.any(O.positions(cu) // 4 >= 3)        # some rows keep a strict subset
+    scale = 1 / math.sqrt(D)
+    o, lse = O.sparse_attn_fwd(q, k, v, sel, cu, scale, block=4)
+    ro, rlse, rdq, rdk, rdv = _gqa_reference(q, k, v, do, sel, cu, scale, 4)
+    np.testing.assert_allclose(o, ro, rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(lse, rlse, rtol=1e-10, atol=1e-12)
+    dq, dk, dv = O.sparse_attn_bwd(q, k, v, do, sel, cu, scale, block=4)
+    np.testing.assert_allclose(dq, rdq, rtol=1e-9, atol=1e-11)
+    np.testing.assert_allclose(dk, rdk, rtol=1e-9, atol=1e-11)
+    np.testing.assert_allclose(dv, rdv, rtol=1e-9, atol=1e-11)
+
+
+def test_narrow_block_full_selection_is_causal_attention():
+    """With every causal 4-token block selected the narrow-block forward is plain
+    causal GQA attention (two KV heads of 12 query heads each, head dim 256)."""
+    import workloads as W
+    seqlens = (37, 5)
+    cu = np.concatenate([[0], np.cumsum(seqlens)])
+    T, Hq, Hkv, D = sum(seqlens), 24, 2, 256
+    r = rng(22)
+    q, k, v = (r.standard_normal((T, h, D)) for h in (Hq, Hkv, Hkv))
+    g = torch.Generator().manual_seed(4)
+    sel = W.qsa_selection(seqlens, Hkv, 16, g, "cpu").numpy()    # 16 >= 10 blocks
+    scale = 1 / math.sqrt(D)
+    o, _ = O.sparse_attn_fwd(q, k, v, sel, cu, scale, block=4)
+    G = Hq // Hkv
+    for s in range(len(seqlens)):
+        a, b = cu[s], cu[s + 1]
+        qq = torch.from_numpy(q[a:b].transpose(1, 0, 2).copy())
+        kk = torch.from_numpy(np.repeat(k[a:b], G, axis=1).transpose(1, 0, 2).copy())
+        vv = torch.from_numpy(np.repeat(v[a:b], G, axis=1).transpose(1, 0, 2).copy())
+        want = F.scaled_dot_product_attention(qq, kk, vv, is_causal=True, scale=scale)
+        np.testing.assert_allclose(o[a:b], want.numpy().transpose(1, 0, 2), rtol=1e-10,
+                                   atol=1e-12)
+
+
 def test_backward_finite_differences():
     block, topk = 4, 2
     r = rng(13)

@@ -208,3 +208,105 @@ def make_decode(shape: DecodeShape, seed: int = 0, device="cpu") -> dict:
     out["block_table"] = table
     out["cache_lens"] = torch.tensor(lens, dtype=torch.int32, device=device)
     return out
+
+
+# ---------------------------------------------------------------- narrow-block variant
+# The pages' second block-sparse workload ("[1/4] Add MiniMax-M3 support - #4581",
+# Kernel tuning): qwen3.8-next's QSA layers with 12 query heads per KV head, head
+# dim 256 and 4-token key blocks, timed fwd+bwd on 16k-token packs.  The pages
+# give no selection rule for it; the synthetic selection keeps each query's own
+# block plus distinct earlier blocks drawn uniformly at random, up to 512 blocks
+# (2048 keys, the key budget of the MiniMax layers' 16 x 128).
+
+QSA_D = 256
+QSA_BLOCK = 4
+QSA_GROUP = 12
+QSA_TOPK = 512
+
+
+@dataclasses.dataclass(frozen=True)
+class QsaShape:
+    name: str
+    seqlens: tuple
+    hq: int
+    hkv: int
+    topk: int
+
+    @property
+    def T(self) -> int:
+        return int(sum(self.seqlens))
+
+    @property
+    def S(self) -> int:
+        return len(self.seqlens)
+
+    @property
+    def max_seqlen(self) -> int:
+        return int(max(self.seqlens))
+
+    def cu_seqlens(self) -> torch.Tensor:
+        cu = [0]
+        for L in self.seqlens:
+            cu.append(cu[-1] + int(L))
+        return torch.tensor(cu, dtype=torch.int32)
+
+
+def qsa_config(idx: int, seed: int = 0) -> QsaShape:
+    """0: a ragged 4-sequence pack (an empty-ish 1-token sequence, lengths not
+    multiples of the block), top-64, so rows past 256 tokens are sparse;
+    1: the 16,384-token pack of the pages' timing (4 sequences, the same length
+    draw as the MiniMax pack), top-512; 2: two KV heads (24 q / 2 kv), top-128."""
+    if idx == 0:
+        return QsaShape("qsa-ragged-12q1kv", (300, 37, 1, 702), 12, 1, 64)
+    if idx == 1:
+        return QsaShape("qsa-pack16k-4seq-12q1kv", seqlens_composition(seed), 12, 1, QSA_TOPK)
+    if idx == 2:
+        return QsaShape("qsa-2kv-24q2kv", (1500, 777), 24, 2, 128)
+    raise ValueError(idx)
+
+
+def qsa_selection(seqlens, hkv: int, topk: int, g: torch.Generator, device) -> torch.Tensor:
+    """sel [T, hkv, topk] int32: for a token at position p, its own block p // 4
+    plus min(topk, p // 4 + 1) - 1 distinct earlier blocks drawn uniformly,
+    ascending, padded with -1.  Block ids are relative to the sequence start."""
+    device = torch.device(device)
+    T = int(sum(seqlens))
+    sel = torch.full((T, hkv, topk), -1, dtype=torch.int32, device=device)
+    t0 = 0
+    for L in seqlens:
+        L = int(L)
+        nb = (L + QSA_BLOCK - 1) // QSA_BLOCK
+        kk = min(topk, nb)
+        cols = torch.arange(nb, device=device)
+        for a in range(0, L, 1024):
+            b = min(L, a + 1024)
+            own = (torch.arange(a, b, device=device) // QSA_BLOCK)[:, None]
+            for h in range(hkv):
+                r = torch.rand((b - a, nb), generator=g, device=device)
+                r = torch.where(cols[None] > own, torch.full_like(r, -1.0), r)
+                r = torch.where(cols[None] == own, torch.full_like(r, 2.0), r)
+                vals, idx = r.topk(kk, dim=1)
+                idx = torch.where(vals < 0, torch.full_like(idx, nb), idx)
+                idx, _ = idx.sort(dim=1)
+                idx = torch.where(idx >= nb, torch.full_like(idx, -1), idx)
+                sel[t0 + a:t0 + b, h, :kk] = idx.to(torch.int32)
+        t0 += L
+    return sel
+
+
+def make_qsa(shape: QsaShape, seed: int = 0, device="cpu", with_grad_out: bool = True) -> dict:
+    """q [T, hq, 256], k and v [T, hkv, 256] bf16 N(0, 1) (the attention inputs; the
+    pages name no prologue for this variant), the selection, cu_seqlens and dO."""
+    device = torch.device(device)
+    g = _gen(seed, device)
+    T, hq, hkv = shape.T, shape.hq, shape.hkv
+    out = {
+        "q": _normal_bf16((T, hq, QSA_D), g, device),
+        "k": _normal_bf16((T, hkv, QSA_D), g, device),
+        "v": _normal_bf16((T, hkv, QSA_D), g, device),
+    }
+    out["sel"] = qsa_selection(shape.seqlens, hkv, shape.topk, g, device)
+    out["cu_seqlens"] = shape.cu_seqlens().to(device)
+    if with_grad_out:
+        out["do"] = _normal_bf16((T, hq, QSA_D), g, device)
+    return out
