@@ -190,6 +190,39 @@ MSA_API msa_status_t msa_sparse_attn_bwd(const void* q, const void* k, const voi
                                  size_t workspace_bytes, msa_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * Narrow-block sparse attention ("[1/4] Add MiniMax-M3 support - #4581",
+ * Kernel tuning: the QSA layers of qwen3.8-next, 12 query heads per KV head,
+ * head dim 256, 4-token key blocks, timed fwd+bwd on 16k-token packs).
+ * Same definition as msa_sparse_attn_fwd / _bwd with blocks of 4 tokens:
+ *   q bf16 [T, Hq, 256]; k, v bf16 [T, Hkv, 256]; Hq must equal 12 Hkv;
+ *   sel int32 [T, Hkv, topk], 1 <= topk <= 1024: block ids relative to the
+ *   sequence start (block b = positions 4b .. 4b+3), distinct, each at most
+ *   the token's own block p / 4 (larger ids set MSA_STATUS_BOUNDS and are
+ *   dropped), -1 for unused slots.  A token attends to the keys j <= p of its
+ *   listed blocks; the own block should be listed (a row with no key gets
+ *   o = 0, lse = -inf).  max_seqlen <= 32768.
+ *   o bf16 [T, Hq, 256], lse fp32 [T, Hq] (natural log);
+ *   dq bf16 [T, Hq, 256], dk, dv bf16 [T, Hkv, 256].
+ * Ownership, alignment, streams and errors as for the 128-token calls.
+ */
+MSA_API size_t msa_qsa_attn_fwd_workspace_size(int T, int S, int Hq, int Hkv, int max_seqlen);
+
+MSA_API msa_status_t msa_qsa_attn_fwd(const void* q, const void* k, const void* v,
+                              const int32_t* sel, const int32_t* cu_seqlens, int S, int T,
+                              int Hq, int Hkv, int topk, int max_seqlen, float scale,
+                              void* o, float* lse, void* workspace, size_t workspace_bytes,
+                              msa_stream_t stream);
+
+MSA_API size_t msa_qsa_attn_bwd_workspace_size(int T, int S, int Hq, int Hkv, int max_seqlen);
+
+MSA_API msa_status_t msa_qsa_attn_bwd(const void* q, const void* k, const void* v,
+                              const void* o, const void* dout, const float* lse,
+                              const int32_t* sel, const int32_t* cu_seqlens, int S, int T,
+                              int Hq, int Hkv, int topk, int max_seqlen, float scale,
+                              void* dq, void* dk, void* dv, void* workspace,
+                              size_t workspace_bytes, msa_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * Decode step against a paged cache (scoring and selection rule of
  * "MiniMax-M3.1-Flash", 1 "Model Introduction", applied to one new token).
  * A page holds one 128-token block: k_cache, v_cache bf16 [num_pages, Hkv,

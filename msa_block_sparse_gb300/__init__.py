@@ -15,6 +15,8 @@ from .api import (  # noqa: F401
     msa_qk_norm_rope4,
     msa_qk_norm_rope_bwd,
     msa_sparse_attn_bwd,
+    msa_qsa_attn_fwd,
+    msa_qsa_attn_bwd,
     msa_sparse_attn_fwd,
     msa_trace_begin,
     msa_trace_end,

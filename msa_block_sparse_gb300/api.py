@@ -47,6 +47,13 @@ _SIGNATURES = {
     "msa_sparse_attn_bwd": (_c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _c_int, _c_int,
                                      _c_int, _c_int, _c_int, _c_float, _vp, _vp, _vp, _vp,
                                      _c_size, _vp]),
+    "msa_qsa_attn_fwd_workspace_size": (_c_size, [_c_int, _c_int, _c_int, _c_int, _c_int]),
+    "msa_qsa_attn_fwd": (_c_int, [_vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int,
+                                  _c_int, _c_int, _c_float, _vp, _vp, _vp, _c_size, _vp]),
+    "msa_qsa_attn_bwd_workspace_size": (_c_size, [_c_int, _c_int, _c_int, _c_int, _c_int]),
+    "msa_qsa_attn_bwd": (_c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _c_int, _c_int,
+                                  _c_int, _c_int, _c_int, _c_int, _c_float, _vp, _vp, _vp, _vp,
+                                  _c_size, _vp]),
     "msa_decode_step_workspace_size": (_c_size, [_c_int, _c_int, _c_int, _c_int]),
     "msa_decode_step": (_c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int,
                                  _c_int, _c_int, _c_float, _vp, _vp, _vp, _c_size, _vp]),
@@ -335,7 +342,67 @@ def msa_decode_step(q, q_idx, k_cache, v_cache, kidx_cache, block_table, cache_l
     return out, sel_out
 
 
+# ------------------------------------------------------------------ narrow blocks
+
+QSA_D = 256
+
+
+def msa_qsa_attn_fwd(q, k, v, sel, cu_seqlens, max_seqlen: int, scale: Optional[float] = None,
+                     out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+                     workspace: Optional[torch.Tensor] = None):
+    """Narrow-block (4-token) sparse attention forward, head dim 256, Hq = 12 Hkv:
+    (o bf16 [T, Hq, 256], lse fp32 [T, Hq]).  sel int32 [T, Hkv, topk]."""
+    T, Hq, Hkv = q.shape[0], q.shape[1], k.shape[1]
+    topk = sel.shape[-1]
+    _req(q, "q", torch.bfloat16, (T, Hq, QSA_D))
+    _req(k, "k", torch.bfloat16, (T, Hkv, QSA_D))
+    _req(v, "v", torch.bfloat16, (T, Hkv, QSA_D))
+    _req(sel, "sel", torch.int32, (T, Hkv, topk))
+    _req(cu_seqlens, "cu_seqlens", torch.int32)
+    S = cu_seqlens.numel() - 1
+    scale = 1.0 / math.sqrt(QSA_D) if scale is None else scale
+    out = torch.empty_like(q) if out is None else out
+    lse = torch.empty((T, Hq), dtype=torch.float32, device=q.device) if lse is None else lse
+    _req(out, "out", torch.bfloat16, (T, Hq, QSA_D))
+    _req(lse, "lse", torch.float32, (T, Hq))
+    size = lib().msa_qsa_attn_fwd_workspace_size(T, S, Hq, Hkv, max_seqlen)
+    ws = _workspace(size, q.device, workspace)
+    _check(lib().msa_qsa_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(sel), _ptr(cu_seqlens), S, T,
+                                  Hq, Hkv, topk, max_seqlen, scale, _ptr(out), _ptr(lse),
+                                  _ptr(ws), ws.numel(), _stream(q)))
+    return out, lse
+
+
+def msa_qsa_attn_bwd(q, k, v, o, dout, lse, sel, cu_seqlens, max_seqlen: int,
+                     scale: Optional[float] = None, dq=None, dk=None, dv=None,
+                     workspace: Optional[torch.Tensor] = None):
+    """Narrow-block sparse attention backward: (dq, dk, dv) in bf16."""
+    T, Hq, Hkv = q.shape[0], q.shape[1], k.shape[1]
+    topk = sel.shape[-1]
+    _req(q, "q", torch.bfloat16, (T, Hq, QSA_D))
+    _req(k, "k", torch.bfloat16, (T, Hkv, QSA_D))
+    _req(v, "v", torch.bfloat16, (T, Hkv, QSA_D))
+    _req(o, "o", torch.bfloat16, (T, Hq, QSA_D))
+    _req(dout, "dout", torch.bfloat16, (T, Hq, QSA_D))
+    _req(lse, "lse", torch.float32, (T, Hq))
+    _req(sel, "sel", torch.int32, (T, Hkv, topk))
+    _req(cu_seqlens, "cu_seqlens", torch.int32)
+    S = cu_seqlens.numel() - 1
+    scale = 1.0 / math.sqrt(QSA_D) if scale is None else scale
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    size = lib().msa_qsa_attn_bwd_workspace_size(T, S, Hq, Hkv, max_seqlen)
+    ws = _workspace(size, q.device, workspace)
+    _check(lib().msa_qsa_attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse),
+                                  _ptr(sel), _ptr(cu_seqlens), S, T, Hq, Hkv, topk, max_seqlen,
+                                  scale, _ptr(dq), _ptr(dk), _ptr(dv), _ptr(ws), ws.numel(),
+                                  _stream(q)))
+    return dq, dk, dv
+
+
 def workspace_bytes(call: str, *args) -> int:
     """Workspace size of `call` ('qk_norm_rope_bwd', 'index_select', 'sparse_attn_fwd',
-    'sparse_attn_bwd', 'decode_step') for the given sizes, as the C ABI reports it."""
+    'sparse_attn_bwd', 'qsa_attn_fwd', 'qsa_attn_bwd', 'decode_step') for the given sizes,
+    as the C ABI reports it."""
     return int(getattr(lib(), f"msa_{call}_workspace_size")(*args))

@@ -168,12 +168,13 @@ bool make_tmap_bf16_strided(CUtensorMap* map, const void* base, int rank, const 
 
 // ------------------------------------------------------------------ tile plan
 
-// One CTA.  nb(s) = ceil(len_s / 128) tiles per sequence; tiles are listed with
+// One CTA.  nb(s) = ceil(len_s / tile) tiles per sequence; tiles are listed with
 // qb descending, s ascending.  cnt[q] = #{s : nb(s) > q}; start[q] = sum of
 // cnt[q'] for q' > q; thread q then appends (s, q) for every qualifying s in
 // order, so the list is deterministic.
 __global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ cu, int S,
-                                                    int max_nb, int2* __restrict__ tiles,
+                                                    int tile, int max_nb,
+                                                    int2* __restrict__ tiles,
                                                     int* __restrict__ num_tiles, int max_tiles,
                                                     uint32_t* status) {
   pdl_enter();
@@ -185,7 +186,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ 
   __syncthreads();
   for (int s = tid; s < S; s += blockDim.x) {
     int len = cu[s + 1] - cu[s];
-    int nb = (len + kBlock - 1) / kBlock;
+    int nb = (len + tile - 1) / tile;
     if (len < 0 || nb > max_nb) {
       atomicOr(status, kStatusBounds);
       nb = len < 0 ? 0 : max_nb;
@@ -213,16 +214,17 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ 
     int pos = start[q];
     for (int s = 0; s < S; ++s) {
       int len = cu[s + 1] - cu[s];
-      int nb = (len + kBlock - 1) / kBlock;
+      int nb = (len + tile - 1) / tile;
       if (nb > max_nb) nb = max_nb;
       if (nb > q && pos < max_tiles) tiles[pos++] = make_int2(s, q);
     }
   }
 }
 
-Plan carve_plan(WsCursor& ws, int T, int S) {
+Plan carve_plan(WsCursor& ws, int T, int S, int tile) {
   Plan p;
-  p.max_tiles = plan_max_tiles(T, S);
+  p.tile = tile;
+  p.max_tiles = plan_max_tiles(T, S, tile);
   p.tiles = ws.take<int2>(p.max_tiles);
   p.num_tiles = ws.take<int>(1);
   return p;
@@ -230,12 +232,12 @@ Plan carve_plan(WsCursor& ws, int T, int S) {
 
 msa_status_t launch_plan(const Plan& plan, const int32_t* cu_seqlens, int S, int max_seqlen,
                          cudaStream_t stream) {
-  int max_nb = (max_seqlen + kBlock - 1) / kBlock;
+  int max_nb = (max_seqlen + plan.tile - 1) / plan.tile;
   size_t smem = 2 * (max_nb + 1) * sizeof(int);
   {
     TraceScope trace_("plan_kernel", stream);
-    launch_pdl(plan_kernel, 1, 1024, smem, stream, cu_seqlens, S, max_nb, plan.tiles, plan.num_tiles,
-        plan.max_tiles, status_word());
+    launch_pdl(plan_kernel, 1, 1024, smem, stream, cu_seqlens, S, plan.tile, max_nb, plan.tiles,
+        plan.num_tiles, plan.max_tiles, status_word());
   }
   return check_launch("plan_kernel");
 }
@@ -532,6 +534,84 @@ msa_status_t msa_sparse_attn_bwd(const void* q, const void* k, const void* v, co
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   return launch_sparse_bwd(q, k, v, o, dout, lse, sel, cu_seqlens, S, T, Hq, Hkv, max_seqlen,
                            scale, bw, dq, dk, dv, st);
+}
+
+// ---------------------------------------------------------------- narrow blocks
+
+static msa_status_t check_qsa(const int32_t* cu, int S, int T, int Hq, int Hkv, int topk,
+                              int max_seqlen, float scale) {
+  MSA_TRY(check_pack(cu, S, T, max_seqlen));
+  if (Hkv < 1 || Hq != 12 * Hkv)
+    return fail(MSA_ERR_UNSUPPORTED, "narrow-block attention needs Hq = 12 Hkv (got %d, %d)",
+                Hq, Hkv);
+  if (topk < 1 || topk > kQsaMaxTopk)
+    return fail(MSA_ERR_INVALID_ARG, "topk %d outside [1, %d]", topk, kQsaMaxTopk);
+  if (max_seqlen > kQsaMaxSeqlen)
+    return fail(MSA_ERR_UNSUPPORTED, "max_seqlen %d above the supported %d for 4-token blocks",
+                max_seqlen, kQsaMaxSeqlen);
+  if (!(scale > 0.0f)) return fail(MSA_ERR_INVALID_ARG, "scale must be > 0");
+  return MSA_OK;
+}
+
+size_t msa_qsa_attn_fwd_workspace_size(int T, int S, int Hq, int Hkv, int max_seqlen) {
+  (void)Hq;
+  if (T < 1 || S < 1 || Hkv < 1 || max_seqlen < 1 || max_seqlen > kQsaMaxSeqlen) return 0;
+  WsCursor ws(nullptr);
+  carve_qsa_fwd_workspace(ws, T, S, Hkv, max_seqlen);
+  return ws.used + 256;
+}
+
+msa_status_t msa_qsa_attn_fwd(const void* q, const void* k, const void* v, const int32_t* sel,
+                              const int32_t* cu_seqlens, int S, int T, int Hq, int Hkv, int topk,
+                              int max_seqlen, float scale, void* o, float* lse, void* workspace,
+                              size_t workspace_bytes, msa_stream_t stream) {
+  MSA_REQUIRE_PTR(q);
+  MSA_REQUIRE_PTR(k);
+  MSA_REQUIRE_PTR(v);
+  MSA_REQUIRE_PTR(sel);
+  MSA_REQUIRE_PTR(o);
+  MSA_REQUIRE_PTR(lse);
+  MSA_REQUIRE_PTR(workspace);
+  MSA_TRY(check_qsa(cu_seqlens, S, T, Hq, Hkv, topk, max_seqlen, scale));
+  if (workspace_bytes < msa_qsa_attn_fwd_workspace_size(T, S, Hq, Hkv, max_seqlen))
+    return fail(MSA_ERR_INVALID_ARG, "workspace too small");
+  WsCursor ws(workspace);
+  QsaFwdWorkspace fw = carve_qsa_fwd_workspace(ws, T, S, Hkv, max_seqlen);
+  return launch_qsa_fwd(q, k, v, sel, cu_seqlens, S, T, Hq, Hkv, topk, max_seqlen, scale, fw, o,
+                        lse, static_cast<cudaStream_t>(stream));
+}
+
+size_t msa_qsa_attn_bwd_workspace_size(int T, int S, int Hq, int Hkv, int max_seqlen) {
+  if (T < 1 || S < 1 || Hq < 1 || Hkv < 1 || max_seqlen < 1 || max_seqlen > kQsaMaxSeqlen)
+    return 0;
+  WsCursor ws(nullptr);
+  carve_qsa_bwd_workspace(ws, T, S, Hq, Hkv, max_seqlen);
+  return ws.used + 256;
+}
+
+msa_status_t msa_qsa_attn_bwd(const void* q, const void* k, const void* v, const void* o,
+                              const void* dout, const float* lse, const int32_t* sel,
+                              const int32_t* cu_seqlens, int S, int T, int Hq, int Hkv, int topk,
+                              int max_seqlen, float scale, void* dq, void* dk, void* dv,
+                              void* workspace, size_t workspace_bytes, msa_stream_t stream) {
+  MSA_REQUIRE_PTR(q);
+  MSA_REQUIRE_PTR(k);
+  MSA_REQUIRE_PTR(v);
+  MSA_REQUIRE_PTR(o);
+  MSA_REQUIRE_PTR(dout);
+  MSA_REQUIRE_PTR(lse);
+  MSA_REQUIRE_PTR(sel);
+  MSA_REQUIRE_PTR(dq);
+  MSA_REQUIRE_PTR(dk);
+  MSA_REQUIRE_PTR(dv);
+  MSA_REQUIRE_PTR(workspace);
+  MSA_TRY(check_qsa(cu_seqlens, S, T, Hq, Hkv, topk, max_seqlen, scale));
+  if (workspace_bytes < msa_qsa_attn_bwd_workspace_size(T, S, Hq, Hkv, max_seqlen))
+    return fail(MSA_ERR_INVALID_ARG, "workspace too small");
+  WsCursor ws(workspace);
+  QsaBwdWorkspace bw = carve_qsa_bwd_workspace(ws, T, S, Hq, Hkv, max_seqlen);
+  return launch_qsa_bwd(q, k, v, o, dout, lse, sel, cu_seqlens, S, T, Hq, Hkv, topk, max_seqlen,
+                        scale, bw, dq, dk, dv, static_cast<cudaStream_t>(stream));
 }
 
 // ---------------------------------------------------------------- decode

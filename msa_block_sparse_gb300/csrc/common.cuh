@@ -70,17 +70,18 @@ struct WsCursor {
 };
 
 // ------------------------------------------------------------------ tile plan
-// The 128-token tiles (sequence s, block qb) of a pack, ordered by qb
-// descending (heaviest causal work first), then s ascending.  Built on the
-// device from cu_seqlens by `launch_plan`.
+// The tiles (sequence s, tile q) of a pack, `tile` consecutive tokens each
+// (128 by default: one key block), ordered by q descending (heaviest causal work
+// first), then s ascending.  Built on the device from cu_seqlens by `launch_plan`.
 struct Plan {
-  int2* tiles;      // [max_tiles] (s, qb)
+  int2* tiles;      // [max_tiles] (s, q)
   int* num_tiles;   // [1]
-  int max_tiles;    // host-side upper bound: T/128 + S
+  int max_tiles;    // host-side upper bound: T / tile + S
+  int tile;         // tokens per tile
 };
 
-inline int plan_max_tiles(int T, int S) { return T / kBlock + S; }
-Plan carve_plan(WsCursor& ws, int T, int S);
+inline int plan_max_tiles(int T, int S, int tile = kBlock) { return T / tile + S; }
+Plan carve_plan(WsCursor& ws, int T, int S, int tile = kBlock);
 msa_status_t launch_plan(const Plan& plan, const int32_t* cu_seqlens, int S, int max_seqlen,
                          cudaStream_t stream);
 

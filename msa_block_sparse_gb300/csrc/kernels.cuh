@@ -94,4 +94,40 @@ msa_status_t launch_decode(const void* q, const void* q_idx, const void* k_cache
                            int Hkv, int num_pages, int max_pages, float scale, void* o,
                            int32_t* sel_out, const DecodeWorkspace& ws, cudaStream_t stream);
 
+// ---------------------------------------------------------------- narrow blocks
+// 4-token key blocks, head dim 256, 12 query heads per KV head.
+constexpr int kQsaMaxSeqlen = 32768;
+constexpr int kQsaMaxWords = kQsaMaxSeqlen / 128;   // bitmap words per (token, KV head)
+constexpr int kQsaMaxTopk = 1024;
+int qsa_mask_words(int max_seqlen);
+struct QsaFwdWorkspace {
+  Plan plan;           // 10-token query tiles
+  uint32_t* masks;     // [T, Hkv, W] selected-block bitmaps
+  int W;
+  int* ulist;          // [max_tiles, Hkv, ustride]: count, then key tiles
+  int ustride;
+};
+struct QsaBwdWorkspace {
+  QsaFwdWorkspace map;
+  float2* lsd;         // [T, Hq] (-lse log2 e, -Delta)
+  int4* items;         // [max_items] (s, key tile, window, 0)
+  int* num_items;
+  int max_items;
+  int* klist;          // [max_items, Hkv, 129]: count, then query tiles
+  float* dk_acc;       // [T, Hkv, 256] fp32 (scaled)
+  float* dv_acc;       // [T, Hkv, 256] fp32, right after dk_acc
+};
+QsaFwdWorkspace carve_qsa_fwd_workspace(WsCursor& ws, int T, int S, int Hkv, int max_seqlen);
+QsaBwdWorkspace carve_qsa_bwd_workspace(WsCursor& ws, int T, int S, int Hq, int Hkv,
+                                        int max_seqlen);
+msa_status_t launch_qsa_fwd(const void* q, const void* k, const void* v, const int32_t* sel,
+                            const int32_t* cu, int S, int T, int Hq, int Hkv, int topk,
+                            int max_seqlen, float scale, const QsaFwdWorkspace& fw, void* o,
+                            float* lse, cudaStream_t stream);
+msa_status_t launch_qsa_bwd(const void* q, const void* k, const void* v, const void* o,
+                            const void* dout, const float* lse, const int32_t* sel,
+                            const int32_t* cu, int S, int T, int Hq, int Hkv, int topk,
+                            int max_seqlen, float scale, const QsaBwdWorkspace& w, void* dq,
+                            void* dk, void* dv, cudaStream_t stream);
+
 }  // namespace msa
