@@ -48,6 +48,7 @@ def parse():
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-prologue-bwd", action="store_true")
+    ap.add_argument("--no-qsa", action="store_true")
     return ap.parse_args()
 
 
@@ -542,6 +543,71 @@ def run_ours(args):
                                "calls"},
         }
         del dx
+
+    # ---- narrow-block variant: 16k pack, 12 q / 1 kv heads, head dim 256, 4-token
+    # blocks, fwd + bwd (the pages' second timed workload)
+    if not args.no_qsa:
+        qshape = W.qsa_config(1, args.seed)
+        qx = W.make_qsa(qshape, seed=args.seed + 1000 * rank, device=dev)
+        qcu, qL = qx["cu_seqlens"], qshape.max_seqlen
+        qo = torch.empty_like(qx["q"])
+        qlse = torch.empty((qshape.T, qshape.hq), dtype=torch.float32, device=dev)
+        qdq, qdk, qdv = torch.empty_like(qx["q"]), torch.empty_like(qx["k"]), torch.empty_like(qx["v"])
+        qws_f = torch.empty(m.workspace_bytes("qsa_attn_fwd", qshape.T, qshape.S, qshape.hq,
+                                              qshape.hkv, qL), dtype=torch.uint8, device=dev)
+        qws_b = torch.empty(m.workspace_bytes("qsa_attn_bwd", qshape.T, qshape.S, qshape.hq,
+                                              qshape.hkv, qL), dtype=torch.uint8, device=dev)
+
+        def qstep():
+            m.msa_qsa_attn_fwd(qx["q"], qx["k"], qx["v"], qx["sel"], qcu, qL, out=qo, lse=qlse,
+                               workspace=qws_f)
+            m.msa_qsa_attn_bwd(qx["q"], qx["k"], qx["v"], qo, qx["do"], qlse, qx["sel"], qcu, qL,
+                               dq=qdq, dk=qdk, dv=qdv, workspace=qws_b)
+
+        for _ in range(3):
+            qstep()
+        torch.cuda.synchronize(dev)
+        nq = max(5, min(args.steps, 20))
+        q0, q1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        q0.record(stream)
+        for _ in range(nq):
+            qstep()
+        q1.record(stream)
+        torch.cuda.synchronize(dev)
+        m.msa_trace_begin()          # per-kernel times from a second, event-bracketed pass
+        for _ in range(nq):
+            qstep()
+        torch.cuda.synchronize(dev)
+        qtrace = m.msa_trace_end()
+        m.msa_check_status(dev)
+        qms = q0.elapsed_time(q1) / nq
+        qwk = workmodel.qsa_work(qshape.seqlens, qx["sel"].cpu().numpy(), qshape.hq)
+        qflops = qwk["fwd_flops"] + qwk["bwd_flops"]
+        sus = peaks.get("bf16_tflops_sustained", 1700.0)
+        qk = {n: {"launches": v["launches"] // nq, "ms_per_launch": v["ms"] / v["launches"]}
+              for n, v in qtrace.items()}
+        qkr = {}
+        for n, f in (("qsa_fwd_kernel", qwk["fwd_flops"]),
+                     ("qsa_bwd_dq_kernel", qwk["bwd_flops"] * 3 / 5),
+                     ("qsa_bwd_dkv_kernel", qwk["bwd_flops"] * 2 / 5)):
+            if n in qk:
+                t = qk[n]["ms_per_launch"]
+                qkr[n] = {"ms": t, "useful_tflops": f / (t * 1e-3) / 1e12,
+                          "frac": f / (t * 1e-3) / 1e12 / sus}
+        out["qsa"] = {
+            "workload": qshape.name, "seqlens": list(qshape.seqlens), "hq": qshape.hq,
+            "hkv": qshape.hkv, "d": W.QSA_D, "block": W.QSA_BLOCK, "topk": qshape.topk,
+            "ms_per_step": qms, "step": "msa_qsa_attn_fwd + msa_qsa_attn_bwd",
+            "useful_tflops": qflops / (qms * 1e-3) / 1e12,
+            "frac_of_sustained": qflops / (qms * 1e-3) / 1e12 / sus,
+            "work": qwk, "kernels": qk, "kernel_roofline": qkr,
+            "useful_split": "dq pass: S, dP, dQ = 3 of the 5 backward products; dkv pass: "
+                            "dV, dK = 2 of 5 (each pass also recomputes S and dP)",
+            "l2": "q, dO, o (100 MB each) and the fp32 accumulators exceed L2",
+            "pages_context": {"fwd_bwd_ms": 16.4, "note": "the pages' GB300 Triton time for "
+                              "this workload shape (pack composition and selection unstated)"},
+        }
+        del qx
 
     # ---- CPU oracle on a bounded sample (rank 0, N = 1 only)
     if not args.no_cpu_baseline and rank == 0 and world == 1:

@@ -114,6 +114,8 @@ struct QsaBwdWorkspace {
   int* num_items;
   int max_items;
   int* klist;          // [max_items, Hkv, 129]: count, then query tiles
+  int* order;          // [Hkv, max_items] non-empty items, most query tiles first
+  int* num_busy;       // [Hkv] non-empty items
   float* dk_acc;       // [T, Hkv, 256] fp32 (scaled)
   float* dv_acc;       // [T, Hkv, 256] fp32, right after dk_acc
 };

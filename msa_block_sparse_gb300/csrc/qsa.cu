@@ -618,6 +618,39 @@ __global__ void __launch_bounds__(256) qsa_kvlist_kernel(const uint32_t* __restr
   }
 }
 
+// One CTA per KV head: the non-empty items ordered by their number of query
+// tiles, largest first (counting sort), so that CTAs striding over the order
+// get nearly equal work.
+__global__ void __launch_bounds__(1024) qsa_order_kernel(const int* __restrict__ klist,
+                                                         const int* __restrict__ num_items,
+                                                         int Hkv, int max_items,
+                                                         int* __restrict__ order,
+                                                         int* __restrict__ num_busy) {
+  pdl_enter();
+  __shared__ int hist[kQWin + 1];
+  __shared__ int start[kQWin + 1];
+  const int g = blockIdx.x;
+  const int n = *num_items;
+  for (int c = threadIdx.x; c <= kQWin; c += blockDim.x) hist[c] = 0;
+  __syncthreads();
+  for (int i = threadIdx.x; i < n; i += blockDim.x)
+    atomicAdd(&hist[min(klist[(static_cast<size_t>(i) * Hkv + g) * (1 + kQWin)], kQWin)], 1);
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int acc = 0;
+    for (int c = kQWin; c >= 1; --c) {
+      start[c] = acc;
+      acc += hist[c];
+    }
+    num_busy[g] = acc;
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < n; i += blockDim.x) {
+    const int c = min(klist[(static_cast<size_t>(i) * Hkv + g) * (1 + kQWin)], kQWin);
+    if (c > 0) order[static_cast<size_t>(g) * max_items + atomicAdd(&start[c], 1)] = i;
+  }
+}
+
 __global__ void __launch_bounds__(kQBwdThreads, 1)
     qsa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q,
                       const __grid_constant__ CUtensorMap tm_do,
@@ -733,19 +766,10 @@ __global__ void __launch_bounds__(kQBwdThreads, 1)
         for (int i = 0; ok && i <= nk; ++i) {
           if (i < nk) {
             const int st = kc & 1;
-            if (!(ok = mbar_wait(&sm.k_full[st], (kc >> 1) & 1, status, 25))) break;
-            // S buffer n & 1 last held dS of step n - 2: its dQ MMA must be done
+            // S / dP buffers n & 1 last held step n - 2: its dQ MMA must be done
             if (n >= 2 && !(ok = mbar_wait(&sm.dq_done[n & 1], ((n - 2) >> 1) & 1, status, 27)))
               break;
-            tc_fence_after();
-            const uint32_t ka = smem_u32(sm.k[st]);
-#pragma unroll
-            for (int kk = 0; kk < 16; ++kk) {
-              const uint32_t cq = (kk >> 2) * kQChunk + (kk & 3) * 32;
-              const uint32_t ck = (kk >> 2) * kKChunk + (kk & 3) * 32;
-              umma_bf16(tmem + kColS + (n & 1) * 64, sdesc_sw128(qa + cq, 16, 1024),
-                        sdesc_sw128(ka + ck, 16, 1024), kQIdS, kk > 0);
-            }
+            // dP first: the single V stage is released as early as possible
             if (!(ok = mbar_wait(&sm.v_full, vc & 1, status, 26))) break;
             tc_fence_after();
 #pragma unroll
@@ -755,8 +779,18 @@ __global__ void __launch_bounds__(kQBwdThreads, 1)
               umma_bf16(tmem + kColDp + (n & 1) * 64, sdesc_sw128(da + cq, 16, 1024),
                         sdesc_sw128(va + ck, 16, 1024), kQIdS, kk > 0);
             }
-            umma_commit(&sm.s_full[n & 1]);
             umma_commit(&sm.v_empty);
+            if (!(ok = mbar_wait(&sm.k_full[st], (kc >> 1) & 1, status, 25))) break;
+            tc_fence_after();
+            const uint32_t ka = smem_u32(sm.k[st]);
+#pragma unroll
+            for (int kk = 0; kk < 16; ++kk) {
+              const uint32_t cq = (kk >> 2) * kQChunk + (kk & 3) * 32;
+              const uint32_t ck = (kk >> 2) * kKChunk + (kk & 3) * 32;
+              umma_bf16(tmem + kColS + (n & 1) * 64, sdesc_sw128(qa + cq, 16, 1024),
+                        sdesc_sw128(ka + ck, 16, 1024), kQIdS, kk > 0);
+            }
+            umma_commit(&sm.s_full[n & 1]);
             if (i == nk - 1) umma_commit(&sm.qd_empty);
             ++kc;
             ++vc;
@@ -883,12 +917,14 @@ __global__ void __launch_bounds__(kQBwdThreads, 1)
                        const __grid_constant__ CUtensorMap tm_v,
                        const uint32_t* __restrict__ masks, int W, const int* __restrict__ klist,
                        const float2* __restrict__ lsd, const int32_t* __restrict__ cu,
-                       const int4* __restrict__ items, const int* __restrict__ num_items, int Hq,
-                       int Hkv, float scale, float* __restrict__ dk_acc,
-                       float* __restrict__ dv_acc, uint32_t* status) {
+                       const int4* __restrict__ items, const int* __restrict__ order,
+                       const int* __restrict__ num_busy, int max_items, int Hq, int Hkv,
+                       float scale, float* __restrict__ dk_acc, float* __restrict__ dv_acc,
+                       uint32_t* status) {
   pdl_enter();
-  const int nitems = *num_items;
+  const int nitems = num_busy[blockIdx.y];
   if (static_cast<int>(blockIdx.x) >= nitems) return;
+  const int* ord = order + static_cast<size_t>(blockIdx.y) * max_items;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   QsaDkvSmem& sm = *reinterpret_cast<QsaDkvSmem*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -933,7 +969,8 @@ __global__ void __launch_bounds__(kQBwdThreads, 1)
       prefetch_tmap(&tm_v);
       uint32_t ic = 0, qc = 0;
       bool ok = true;
-      for (int it = blockIdx.x; ok && it < nitems; it += gridDim.x) {
+      for (int jt = blockIdx.x; ok && jt < nitems; jt += gridDim.x) {
+        const int it = __ldg(ord + jt);
         const int* kl = klist + (static_cast<size_t>(it) * Hkv + g) * (1 + kQWin);
         const int nq = __ldg(kl);
         if (nq == 0) continue;
@@ -963,7 +1000,8 @@ __global__ void __launch_bounds__(kQBwdThreads, 1)
       prefetch_tmap(&tm_do);
       uint32_t dc = 0;
       bool ok = true;
-      for (int it = blockIdx.x; ok && it < nitems; it += gridDim.x) {
+      for (int jt = blockIdx.x; ok && jt < nitems; jt += gridDim.x) {
+        const int it = __ldg(ord + jt);
         const int* kl = klist + (static_cast<size_t>(it) * Hkv + g) * (1 + kQWin);
         const int nq = __ldg(kl);
         if (nq == 0) continue;
@@ -986,7 +1024,8 @@ __global__ void __launch_bounds__(kQBwdThreads, 1)
       bool ok = true;
       const uint32_t qa = smem_u32(sm.q), da = smem_u32(sm.dout), ka = smem_u32(sm.k),
                      va = smem_u32(sm.v), pa = smem_u32(sm.p), sa = smem_u32(sm.ds);
-      for (int it = blockIdx.x; ok && it < nitems; it += gridDim.x) {
+      for (int jt = blockIdx.x; ok && jt < nitems; jt += gridDim.x) {
+        const int it = __ldg(ord + jt);
         const int nq = __ldg(klist + (static_cast<size_t>(it) * Hkv + g) * (1 + kQWin));
         if (nq == 0) continue;
         if (!(ok = mbar_wait(&sm.kv_full, ic & 1, status, 44))) break;
@@ -1016,14 +1055,8 @@ __global__ void __launch_bounds__(kQBwdThreads, 1)
           if (i == 0 && ic > 0 && !(ok = mbar_wait(&sm.acc_free, (ic - 1) & 1, status, 48)))
             break;
           tc_fence_after();
-#pragma unroll
-          for (int hf = 0; hf < 2; ++hf)
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk)
-              umma_bf16(tmem + kColDv + hf * 64,
-                        sdesc_sw128(da + hf * 2 * kQChunk + kk * 2048, kQChunk, 1024),
-                        sdesc_sw128(pa + kk * 2048, kQChunk, 1024), kQIdKV, (i > 0 || kk > 0));
-          umma_commit(&sm.do_empty);
+          // dK first: Q is released first, so the next tile's Q (which its S
+          // needs before its dP needs dO) loads while dV runs
 #pragma unroll
           for (int hf = 0; hf < 2; ++hf)
 #pragma unroll
@@ -1032,6 +1065,14 @@ __global__ void __launch_bounds__(kQBwdThreads, 1)
                         sdesc_sw128(qa + hf * 2 * kQChunk + kk * 2048, kQChunk, 1024),
                         sdesc_sw128(sa + kk * 2048, kQChunk, 1024), kQIdKV, (i > 0 || kk > 0));
           umma_commit(&sm.q_empty);
+#pragma unroll
+          for (int hf = 0; hf < 2; ++hf)
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk)
+              umma_bf16(tmem + kColDv + hf * 64,
+                        sdesc_sw128(da + hf * 2 * kQChunk + kk * 2048, kQChunk, 1024),
+                        sdesc_sw128(pa + kk * 2048, kQChunk, 1024), kQIdKV, (i > 0 || kk > 0));
+          umma_commit(&sm.do_empty);
           umma_commit(&sm.pds_empty);
         }
         umma_commit(&sm.acc_full);
@@ -1047,7 +1088,8 @@ __global__ void __launch_bounds__(kQBwdThreads, 1)
     const float sl2 = scale * kQLog2e;
     uint32_t ic = 0, n = 0;
     bool ok = true;
-    for (int it = blockIdx.x; ok && it < nitems; it += gridDim.x) {
+    for (int jt = blockIdx.x; ok && jt < nitems; jt += gridDim.x) {
+      const int it = __ldg(ord + jt);
       const int* kl = klist + (static_cast<size_t>(it) * Hkv + g) * (1 + kQWin);
       const int nq = __ldg(kl);
       if (nq == 0) continue;
@@ -1201,6 +1243,8 @@ QsaBwdWorkspace carve_qsa_bwd_workspace(WsCursor& ws, int T, int S, int Hq, int 
   w.items = ws.take<int4>(w.max_items);
   w.num_items = ws.take<int>(1);
   w.klist = ws.take<int>(static_cast<size_t>(w.max_items) * Hkv * (1 + kQWin));
+  w.order = ws.take<int>(static_cast<size_t>(w.max_items) * Hkv);
+  w.num_busy = ws.take<int>(Hkv);
   // the two accumulators stay adjacent: one clear covers them
   w.dk_acc = ws.take<float>(static_cast<size_t>(T) * Hkv * kQD);
   w.dv_acc = ws.take<float>(static_cast<size_t>(T) * Hkv * kQD);
@@ -1313,7 +1357,12 @@ msa_status_t launch_qsa_bwd(const void* q, const void* k, const void* v, const v
     launch_pdl(qsa_kvlist_kernel, capped_blocks(static_cast<size_t>(w.max_items) * Hkv, 8, 4 * sms),
         256, 0, stream, fw.masks, fw.W, cu, w.items, w.num_items, Hkv, w.klist);
   }
-  QSA_TRY(check_launch("qsa_delta/items/kvlist"));
+  {
+    TraceScope trace_("qsa_order_kernel", stream);
+    launch_pdl(qsa_order_kernel, Hkv, 1024, 0, stream, w.klist, w.num_items, Hkv, w.max_items,
+        w.order, w.num_busy);
+  }
+  QSA_TRY(check_launch("qsa_delta/items/kvlist/order"));
 
   const size_t smem_dq = sizeof(QsaDqSmem) + 1024;
   static bool dq_attr = false;
@@ -1336,8 +1385,8 @@ msa_status_t launch_qsa_bwd(const void* q, const void* k, const void* v, const v
     dim3 grid(static_cast<unsigned>(per_head < w.max_items ? per_head : w.max_items), Hkv);
     TraceScope trace_("qsa_bwd_dkv_kernel", stream);
     launch_pdl(qsa_bwd_dkv_kernel, grid, kQBwdThreads, smem_kv, stream, tq, tdo, tk, tv,
-        fw.masks, fw.W, w.klist, w.lsd, cu, w.items, w.num_items, Hq, Hkv, scale, w.dk_acc,
-        w.dv_acc, status_word());
+        fw.masks, fw.W, w.klist, w.lsd, cu, w.items, w.order, w.num_busy, w.max_items, Hq, Hkv,
+        scale, w.dk_acc, w.dv_acc, status_word());
   }
   QSA_TRY(check_launch("qsa_bwd_dkv_kernel"));
   {

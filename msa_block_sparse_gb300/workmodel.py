@@ -10,6 +10,8 @@ avoids is not counted, nor are padded or masked tensor-core lanes):
              K and V + q, index-q and o
 A query at position p attends to 128 * (min(16, p // 128 + 1) - 1) + p % 128 + 1
 keys: the full earlier selected blocks and its own block up to itself.
+Narrow-block calls (4-token blocks, head dim 256) count the keys of the actual
+selection: every listed block contributes its keys at positions <= p.
 """
 from __future__ import annotations
 
@@ -56,3 +58,16 @@ def decode_bytes(cache_lens, hq: int, hkv: int) -> float:
         total += 2 * hkv * keys * D * 2       # selected K and V
         total += (hq + hkv + hq) * D * 2      # q, index-q, o
     return total
+
+
+def qsa_work(seqlens, sel: np.ndarray, hq: int, block: int = 4, d: int = 256) -> dict:
+    """Useful work of the narrow-block forward / backward for a selection
+    sel [T, Hkv, topk] (block ids relative to the sequence start, -1 unused)."""
+    pos = _positions(seqlens)
+    T, hkv, _ = sel.shape
+    b = sel.astype(np.int64)
+    keys = np.clip(pos[:, None, None] - block * b + 1, 0, block)
+    keys = np.where(b >= 0, keys, 0).sum(axis=2)            # [T, Hkv]
+    fwd = float(keys.sum()) * (hq // hkv) * 4 * d
+    return {"tokens": int(T), "attended_keys": float(keys.sum()), "fwd_flops": fwd,
+            "bwd_flops": 2.5 * fwd}
