@@ -152,7 +152,9 @@ def kernel_source_hash(name: str) -> str:
     files = {"sparse_bwd_kernel": "sparse_bwd.cu", "sparse_fwd_kernel": "sparse_fwd.cu",
              "index_select_kernel": "index_select.cu", "prologue_kernel": "prologue.cu",
              "prologue_bwd_kernel": "prologue.cu",
-             "decode_score_kernel": "decode.cu"}
+             "decode_score_kernel": "decode.cu",
+             "qsa_fwd_kernel": "qsa.cu", "qsa_bwd_dq_kernel": "qsa.cu",
+             "qsa_bwd_dkv_kernel": "qsa.cu"}
     f = files.get(name)
     if f is None:
         return ""
@@ -593,7 +595,7 @@ def run_ours(args):
             if n in qk:
                 t = qk[n]["ms_per_launch"]
                 qkr[n] = {"ms": t, "useful_tflops": f / (t * 1e-3) / 1e12,
-                          "frac": f / (t * 1e-3) / 1e12 / sus}
+                          "frac": f / (t * 1e-3) / 1e12 / sus, "traffic": traffic_for(n)}
         out["qsa"] = {
             "workload": qshape.name, "seqlens": list(qshape.seqlens), "hq": qshape.hq,
             "hkv": qshape.hkv, "d": W.QSA_D, "block": W.QSA_BLOCK, "topk": qshape.topk,
