@@ -195,39 +195,46 @@ def block_scores_seq(qi: np.ndarray, ki: np.ndarray, rows: Optional[np.ndarray] 
     return out
 
 
-def select_from_scores(scores: np.ndarray, own: np.ndarray, topk: int = TOPK):
+def select_from_scores(scores: np.ndarray, own: np.ndarray, topk: int = TOPK, n_init: int = 0):
     """Top-k blocks with the own block forced [M31]: own block plus the best
     min(topk-1, own) earlier blocks by score (equal scores: lower id first);
     output sorted ascending, padded with -1.
 
+    With n_init > 0 the "init" rule named in [PR] (Kernel tuning) is applied as
+    read here: the first n_init blocks of the sequence (those before the own
+    block) are kept as well, and the best of the remaining earlier blocks fill
+    the other topk - 1 - min(n_init, own) slots.
+
     Also returns, per row, the relative gap between the last kept and the first
-    dropped earlier block (inf when every causal block is kept), which the
-    near-tie rule compares with 1e-3."""
+    dropped scored block (inf when no scored block is dropped or none is kept),
+    which the near-tie rule compares with 1e-3."""
     n = scores.shape[0]
     sel = np.full((n, topk), -1, dtype=np.int64)
     gap = np.full(n, np.inf)
     for r in range(n):
         o = int(own[r])
-        cand = np.arange(o)
-        order = cand[np.lexsort((cand, -scores[r, :o]))] if o > 0 else cand
-        keep = order[:topk - 1]
-        ids = np.sort(np.concatenate([keep, [o]]))
+        ni = min(n_init, o)
+        slots = topk - 1 - ni
+        cand = np.arange(ni, o)
+        order = cand[np.lexsort((cand, -scores[r, ni:o]))] if o > ni else cand
+        keep = order[:max(slots, 0)]
+        ids = np.sort(np.concatenate([np.arange(ni), keep, [o]]))
         sel[r, :len(ids)] = ids
-        if o > topk - 1:
-            a = scores[r, order[topk - 2]]
-            b = scores[r, order[topk - 1]]
+        if slots > 0 and len(cand) > slots:
+            a = scores[r, order[slots - 1]]
+            b = scores[r, order[slots]]
             den = max(abs(a), abs(b))
             gap[r] = abs(a - b) / den if den > 0 else 0.0
     return sel, gap
 
 
 def index_select(q_idx, k_idx, cu_seqlens, topk: int = TOPK,
-                 tokens: Optional[Iterable[int]] = None, block: int = BLOCK):
+                 tokens: Optional[Iterable[int]] = None, block: int = BLOCK, n_init: int = 0):
     """Block selection of every (token, index head) [M31, PR].
 
     q_idx, k_idx: [T, Hi, D] post-prologue values.  Returns sel [n, Hi, topk]
     (ids relative to the sequence start) and gap [n, Hi] for the requested
-    tokens (all when None), in the order given."""
+    tokens (all when None), in the order given.  n_init: see select_from_scores."""
     q_idx = np.asarray(q_idx, dtype=np.float64)
     k_idx = np.asarray(k_idx, dtype=np.float64)
     cu = np.asarray(cu_seqlens, dtype=np.int64)
@@ -242,7 +249,7 @@ def index_select(q_idx, k_idx, cu_seqlens, topk: int = TOPK,
         rows = toks[idx] - b0
         for h in range(Hi):
             sc = block_scores_seq(q_idx[b0:b1, h], k_idx[b0:b1, h], rows, block)
-            ss, gg = select_from_scores(sc, rows // block, topk)
+            ss, gg = select_from_scores(sc, rows // block, topk, n_init)
             sel[idx, h] = ss
             gap[idx, h] = gg
     return sel, gap
@@ -385,7 +392,7 @@ def sparse_attn_bwd(q, k, v, do, sel, cu_seqlens, scale: float,
 
 def decode_step(q, q_idx, k_cache, v_cache, kidx_cache, block_table, cache_lens,
                 scale: float, topk: int = TOPK, batch: Optional[Iterable[int]] = None,
-                block: int = BLOCK):
+                block: int = BLOCK, n_init: int = 0):
     """One decode step against a paged cache (page = one 128-token block,
     layout [page, head, token, dim]).
 
@@ -394,7 +401,8 @@ def decode_step(q, q_idx, k_cache, v_cache, kidx_cache, block_table, cache_lens,
     max logit q_idx[b,h] . kidx over its cached keys, the own block is forced and
     the best others fill it up to `topk` [M31]; the 16 query heads of KV head h
     then attend over the selected keys.  Returns o [n, Hq, D], sel [n, Hi, topk]
-    and gap [n, Hi] for the requested batch rows (all when None)."""
+    and gap [n, Hi] for the requested batch rows (all when None).  n_init: see
+    select_from_scores."""
     q = np.asarray(q, dtype=np.float64)
     q_idx = np.asarray(q_idx, dtype=np.float64)
     bt = np.asarray(block_table, dtype=np.int64)
@@ -421,7 +429,7 @@ def decode_step(q, q_idx, k_cache, v_cache, kidx_cache, block_table, cache_lens,
         for h in range(Hi):
             logits = ki[h] @ q_idx[b, h]
             sc = np.array([logits[c * block:min((c + 1) * block, L)].max() for c in range(npg)])
-            ss, gg = select_from_scores(sc[None, :], np.array([own]), topk)
+            ss, gg = select_from_scores(sc[None, :], np.array([own]), topk, n_init)
             sel[n, h] = ss[0]
             gap[n, h] = gg[0]
         for g in range(Hkv):

@@ -28,14 +28,28 @@ def _norm_eps_outside(x, w, eps=1e-6):
     return x / (np.sqrt(np.mean(x * x, axis=-1, keepdims=True)) + 1e-2) * (1 + w)
 
 
-def _select_higher_id_on_tie(scores, own, topk=O.TOPK):
+def _select_higher_id_on_tie(scores, own, topk=O.TOPK, n_init=0):
     s = scores.copy()
     n = s.shape[1]
     s = s + 1e-12 * np.arange(n)[None, :]      # breaks ties towards the higher id
-    return _ORIG["select_from_scores"](s, own, topk)
+    return _ORIG["select_from_scores"](s, own, topk, n_init)
 
 
-def _select_own_not_forced(scores, own, topk=O.TOPK):
+def _select_init_rescored(scores, own, topk=O.TOPK, n_init=0):
+    # keeps the init blocks but still lets them compete for the scored slots
+    n = scores.shape[0]
+    sel = np.full((n, topk), -1, dtype=np.int64)
+    for r in range(n):
+        o = int(own[r])
+        ni = min(n_init, o)
+        cand = np.arange(o)
+        order = cand[np.lexsort((cand, -scores[r, :o]))] if o > 0 else cand
+        ids = np.unique(np.concatenate([np.arange(ni), order[:topk - 1 - ni], [o]]))
+        sel[r, :len(ids)] = ids
+    return sel, np.full(n, np.inf)
+
+
+def _select_own_not_forced(scores, own, topk=O.TOPK, n_init=0):
     n = scores.shape[0]
     sel = np.full((n, topk), -1, dtype=np.int64)
     for r in range(n):
@@ -125,6 +139,7 @@ MUTATIONS = [
     ("gemma_rmsnorm", _norm_eps_outside, [P.test_gemma_rmsnorm_zero_weight_gives_unit_rms]),
     ("select_from_scores", _select_higher_id_on_tie, [P.test_selection_tie_prefers_lower_block]),
     ("select_from_scores", _select_own_not_forced, [P.test_selection_invariants]),
+    ("select_from_scores", _select_init_rescored, [P.test_init_rule_by_enumeration]),
     ("_keys_of", _keys_one_past_causal,
      [P.test_sparse_forward_and_backward_match_masked_library_attention]),
     ("_keys_of", _keys_ignore_selection,

@@ -278,6 +278,49 @@ def test_selection_is_best_subset_by_enumeration():
             assert list(sel[t]) == want
 
 
+def test_init_rule_by_enumeration():
+    """With the init rule ("#4581", Kernel tuning names it; read here as: the first
+    n_init blocks of the sequence are always kept) the scored slots hold the best
+    subset of the blocks between the init blocks and the own block."""
+    r = rng(31)
+    block, topk = 4, 4
+    for n_init in (1, 2, 3):
+        for trial in range(12):
+            L = int(r.integers(1, 48))
+            qi = r.standard_normal((L, 6))
+            ki = r.standard_normal((L, 6))
+            sc = _brute_scores(qi, ki, block)
+            own = np.arange(L) // block
+            sel, _ = O.select_from_scores(sc, own, topk, n_init=n_init)
+            for t in range(L):
+                o = int(own[t])
+                ni = min(n_init, o)
+                m = min(topk - 1 - ni, o - ni)
+                best = max(itertools.combinations(range(ni, o), m),
+                           key=lambda c: sum(sc[t, list(c)]))
+                want = sorted(list(range(ni)) + list(best) + [o])
+                want += [-1] * (topk - len(want))
+                assert list(sel[t]) == want, (n_init, t)
+
+
+def test_init_rule_is_infinite_score_for_the_first_blocks():
+    """Keeping the first n_init blocks equals the plain rule on scores where those
+    blocks score +inf (they then win every comparison), on a real index pack."""
+    qi, ki, cu = _small_pack(33, [700, 1, 2600], hi=2)
+    for n_init in (1, 2):
+        sel, _ = O.index_select(qi, ki, cu, n_init=n_init)
+        pos = O.positions(cu)
+        for s in range(len(cu) - 1):
+            a, b = cu[s], cu[s + 1]
+            for h in range(2):
+                sc = O.block_scores_seq(qi[a:b, h], ki[a:b, h])
+                sc[:, :n_init] = np.inf
+                want, _ = O.select_from_scores(sc, pos[a:b] // 128)
+                np.testing.assert_array_equal(sel[a:b, h], want)
+    sel0, _ = O.index_select(qi, ki, cu, n_init=0)
+    np.testing.assert_array_equal(sel0, O.index_select(qi, ki, cu)[0])
+
+
 def test_selection_tie_prefers_lower_block():
     sc = np.array([[5.0, 7.0, 5.0, 5.0, 1.0, 0.0]])
     sel, gap = O.select_from_scores(sc, np.array([5]), topk=3)
