@@ -153,6 +153,19 @@ MSA_API msa_status_t msa_index_select(const void* q_idx, const void* k_idx,
                               int max_seqlen, int topk, int32_t* sel, void* workspace,
                               size_t workspace_bytes, msa_stream_t stream);
 
+/* The same selection with the "init" rule that "#4581" (Kernel tuning) names
+ * beside the local and causal rules but does not define.  Read here as: the
+ * first n_init blocks of every sequence (those before the token's own block)
+ * are always kept; the best of the other earlier blocks fill the remaining
+ * 15 - min(n_init, own) slots.  0 <= n_init <= 15; n_init = 0 is
+ * msa_index_select.  Workspace: msa_index_select_workspace_size.
+ */
+MSA_API msa_status_t msa_index_select_ex(const void* q_idx, const void* k_idx,
+                                 const int32_t* cu_seqlens, int S, int T, int Hi,
+                                 int max_seqlen, int topk, int n_init, int32_t* sel,
+                                 void* workspace, size_t workspace_bytes,
+                                 msa_stream_t stream);
+
 /* ------------------------------------------------------------------------
  * Block-sparse attention forward ("MiniMax-M3.1-Flash", 1; "#4581").
  * q bf16 [T, Hq, 128]; k, v bf16 [T, Hkv, 128]; sel int32 [T, Hkv, 16].
@@ -245,6 +258,18 @@ MSA_API msa_status_t msa_decode_step(const void* q, const void* q_idx, const voi
                              int Hq, int Hkv, int num_pages, int max_pages, float scale,
                              void* o, int32_t* sel_out, void* workspace,
                              size_t workspace_bytes, msa_stream_t stream);
+
+/* msa_decode_step with the init rule of msa_index_select_ex: blocks
+ * 0 .. min(n_init, own) - 1 of every sequence are always selected
+ * (0 <= n_init <= 15; n_init = 0 is msa_decode_step).  Same workspace.
+ */
+MSA_API msa_status_t msa_decode_step_ex(const void* q, const void* q_idx, const void* k_cache,
+                                const void* v_cache, const void* kidx_cache,
+                                const int32_t* block_table, const int32_t* cache_lens,
+                                int B, int Hq, int Hkv, int num_pages, int max_pages,
+                                float scale, int n_init, void* o, int32_t* sel_out,
+                                void* workspace, size_t workspace_bytes,
+                                msa_stream_t stream);
 
 /* ------------------------------------------------------------------------
  * Decode append (the prologue of one new token per sequence, written into its

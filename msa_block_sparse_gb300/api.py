@@ -40,6 +40,8 @@ _SIGNATURES = {
     "msa_index_select_workspace_size": (_c_size, [_c_int, _c_int, _c_int, _c_int]),
     "msa_index_select": (_c_int, [_vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_int, _vp,
                                   _vp, _c_size, _vp]),
+    "msa_index_select_ex": (_c_int, [_vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_int,
+                                     _c_int, _vp, _vp, _c_size, _vp]),
     "msa_sparse_attn_fwd_workspace_size": (_c_size, [_c_int, _c_int, _c_int, _c_int, _c_int]),
     "msa_sparse_attn_fwd": (_c_int, [_vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int,
                                      _c_int, _c_float, _vp, _vp, _vp, _c_size, _vp]),
@@ -57,6 +59,9 @@ _SIGNATURES = {
     "msa_decode_step_workspace_size": (_c_size, [_c_int, _c_int, _c_int, _c_int]),
     "msa_decode_step": (_c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int,
                                  _c_int, _c_int, _c_float, _vp, _vp, _vp, _c_size, _vp]),
+    "msa_decode_step_ex": (_c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int,
+                                    _c_int, _c_int, _c_float, _c_int, _vp, _vp, _vp, _c_size,
+                                    _vp]),
     "msa_decode_step_static": (_c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _c_int, _c_int,
                                         _c_int, _c_int, _c_int, _c_float, _vp, _vp, _vp]),
 }
@@ -214,8 +219,9 @@ def msa_qk_norm_rope4(q, k, q_idx, k_idx, w_q, w_k, w_qi, w_ki, cu_seqlens, outs
 
 def msa_index_select(q_idx, k_idx, cu_seqlens, max_seqlen: int, topk: int = TOPK,
                      out: Optional[torch.Tensor] = None,
-                     workspace: Optional[torch.Tensor] = None) -> torch.Tensor:
-    """Selected blocks int32 [T, Hi, 16] (ascending, -1 padded)."""
+                     workspace: Optional[torch.Tensor] = None, n_init: int = 0) -> torch.Tensor:
+    """Selected blocks int32 [T, Hi, 16] (ascending, -1 padded).  n_init > 0 applies
+    the init rule (msa_index_select_ex: the first n_init blocks are always kept)."""
     T, Hi = q_idx.shape[0], q_idx.shape[1]
     _req(q_idx, "q_idx", torch.bfloat16, (T, Hi, D))
     _req(k_idx, "k_idx", torch.bfloat16, (T, Hi, D))
@@ -226,9 +232,14 @@ def msa_index_select(q_idx, k_idx, cu_seqlens, max_seqlen: int, topk: int = TOPK
     _req(out, "out", torch.int32, (T, Hi, topk))
     size = lib().msa_index_select_workspace_size(T, S, Hi, max_seqlen)
     ws = _workspace(size, q_idx.device, workspace)
-    _check(lib().msa_index_select(_ptr(q_idx), _ptr(k_idx), _ptr(cu_seqlens), S, T, Hi,
-                                  max_seqlen, topk, _ptr(out), _ptr(ws), ws.numel(),
-                                  _stream(q_idx)))
+    if n_init:
+        _check(lib().msa_index_select_ex(_ptr(q_idx), _ptr(k_idx), _ptr(cu_seqlens), S, T, Hi,
+                                         max_seqlen, topk, n_init, _ptr(out), _ptr(ws),
+                                         ws.numel(), _stream(q_idx)))
+    else:
+        _check(lib().msa_index_select(_ptr(q_idx), _ptr(k_idx), _ptr(cu_seqlens), S, T, Hi,
+                                      max_seqlen, topk, _ptr(out), _ptr(ws), ws.numel(),
+                                      _stream(q_idx)))
     return out
 
 
@@ -318,8 +329,9 @@ def msa_decode_append(q, q_idx, k, v, k_idx, w_q, w_qi, w_k, w_ki, k_cache, v_ca
 def msa_decode_step(q, q_idx, k_cache, v_cache, kidx_cache, block_table, cache_lens,
                     scale: Optional[float] = None, out: Optional[torch.Tensor] = None,
                     sel_out: Optional[torch.Tensor] = None,
-                    workspace: Optional[torch.Tensor] = None):
-    """One decode step: (o bf16 [B, Hq, 128], sel int32 [B, Hkv, 16])."""
+                    workspace: Optional[torch.Tensor] = None, n_init: int = 0):
+    """One decode step: (o bf16 [B, Hq, 128], sel int32 [B, Hkv, 16]).  n_init > 0
+    applies the init rule (msa_decode_step_ex)."""
     B, Hq = q.shape[0], q.shape[1]
     P, Hkv = k_cache.shape[0], k_cache.shape[1]
     maxp = block_table.shape[1]
@@ -335,10 +347,16 @@ def msa_decode_step(q, q_idx, k_cache, v_cache, kidx_cache, block_table, cache_l
         sel_out = torch.empty((B, Hkv, TOPK), dtype=torch.int32, device=q.device)
     size = lib().msa_decode_step_workspace_size(B, Hq, Hkv, maxp)
     ws = _workspace(size, q.device, workspace)
-    _check(lib().msa_decode_step(_ptr(q), _ptr(q_idx), _ptr(k_cache), _ptr(v_cache),
-                                 _ptr(kidx_cache), _ptr(block_table), _ptr(cache_lens), B, Hq,
-                                 Hkv, P, maxp, scale, _ptr(out), _ptr(sel_out), _ptr(ws),
-                                 ws.numel(), _stream(q)))
+    if n_init:
+        _check(lib().msa_decode_step_ex(_ptr(q), _ptr(q_idx), _ptr(k_cache), _ptr(v_cache),
+                                        _ptr(kidx_cache), _ptr(block_table), _ptr(cache_lens), B,
+                                        Hq, Hkv, P, maxp, scale, n_init, _ptr(out),
+                                        _ptr(sel_out), _ptr(ws), ws.numel(), _stream(q)))
+    else:
+        _check(lib().msa_decode_step(_ptr(q), _ptr(q_idx), _ptr(k_cache), _ptr(v_cache),
+                                     _ptr(kidx_cache), _ptr(block_table), _ptr(cache_lens), B,
+                                     Hq, Hkv, P, maxp, scale, _ptr(out), _ptr(sel_out),
+                                     _ptr(ws), ws.numel(), _stream(q)))
     return out, sel_out
 
 

@@ -439,6 +439,14 @@ size_t msa_index_select_workspace_size(int T, int S, int Hi, int max_seqlen) {
 msa_status_t msa_index_select(const void* q_idx, const void* k_idx, const int32_t* cu_seqlens,
                               int S, int T, int Hi, int max_seqlen, int topk, int32_t* sel,
                               void* workspace, size_t workspace_bytes, msa_stream_t stream) {
+  return msa_index_select_ex(q_idx, k_idx, cu_seqlens, S, T, Hi, max_seqlen, topk, 0, sel,
+                             workspace, workspace_bytes, stream);
+}
+
+msa_status_t msa_index_select_ex(const void* q_idx, const void* k_idx, const int32_t* cu_seqlens,
+                                 int S, int T, int Hi, int max_seqlen, int topk, int n_init,
+                                 int32_t* sel, void* workspace, size_t workspace_bytes,
+                                 msa_stream_t stream) {
   MSA_REQUIRE_PTR(q_idx);
   MSA_REQUIRE_PTR(k_idx);
   MSA_REQUIRE_PTR(sel);
@@ -446,13 +454,15 @@ msa_status_t msa_index_select(const void* q_idx, const void* k_idx, const int32_
   MSA_TRY(check_pack(cu_seqlens, S, T, max_seqlen));
   if (topk != kTopK) return fail(MSA_ERR_UNSUPPORTED, "topk must be %d (got %d)", kTopK, topk);
   if (Hi < 1) return fail(MSA_ERR_INVALID_ARG, "Hi must be >= 1");
+  if (n_init < 0 || n_init > kTopK - 1)
+    return fail(MSA_ERR_INVALID_ARG, "n_init %d outside [0, %d]", n_init, kTopK - 1);
   if (workspace_bytes < msa_index_select_workspace_size(T, S, Hi, max_seqlen))
     return fail(MSA_ERR_INVALID_ARG, "workspace too small");
   WsCursor ws(workspace);
   Plan plan = carve_plan(ws, T, S);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   MSA_TRY(launch_plan(plan, cu_seqlens, S, max_seqlen, st));
-  return launch_index_select(q_idx, k_idx, cu_seqlens, S, T, Hi, plan, sel, st);
+  return launch_index_select(q_idx, k_idx, cu_seqlens, S, T, Hi, n_init, plan, sel, st);
 }
 
 // ---------------------------------------------------------------- sparse forward
@@ -629,6 +639,17 @@ msa_status_t msa_decode_step(const void* q, const void* q_idx, const void* k_cac
                              int Hkv, int num_pages, int max_pages, float scale, void* o,
                              int32_t* sel_out, void* workspace, size_t workspace_bytes,
                              msa_stream_t stream) {
+  return msa_decode_step_ex(q, q_idx, k_cache, v_cache, kidx_cache, block_table, cache_lens, B,
+                            Hq, Hkv, num_pages, max_pages, scale, 0, o, sel_out, workspace,
+                            workspace_bytes, stream);
+}
+
+msa_status_t msa_decode_step_ex(const void* q, const void* q_idx, const void* k_cache,
+                                const void* v_cache, const void* kidx_cache,
+                                const int32_t* block_table, const int32_t* cache_lens, int B,
+                                int Hq, int Hkv, int num_pages, int max_pages, float scale,
+                                int n_init, void* o, int32_t* sel_out, void* workspace,
+                                size_t workspace_bytes, msa_stream_t stream) {
   MSA_REQUIRE_PTR(q);
   MSA_REQUIRE_PTR(q_idx);
   MSA_REQUIRE_PTR(k_cache);
@@ -648,12 +669,14 @@ msa_status_t msa_decode_step(const void* q, const void* q_idx, const void* k_cac
   MSA_TRY(check_heads(Hq, Hkv));
   if (Hq / Hkv != 16) return fail(MSA_ERR_UNSUPPORTED, "decode needs Hq/Hkv = 16");
   if (!(scale > 0.0f)) return fail(MSA_ERR_INVALID_ARG, "scale must be > 0");
+  if (n_init < 0 || n_init > kTopK - 1)
+    return fail(MSA_ERR_INVALID_ARG, "n_init %d outside [0, %d]", n_init, kTopK - 1);
   if (workspace_bytes < msa_decode_step_workspace_size(B, Hq, Hkv, max_pages))
     return fail(MSA_ERR_INVALID_ARG, "workspace too small");
   WsCursor ws(workspace);
   DecodeWorkspace dw = carve_decode_workspace(ws, B, Hq, Hkv, max_pages);
   return launch_decode(q, q_idx, k_cache, v_cache, kidx_cache, block_table, cache_lens, B, Hq, Hkv,
-                       num_pages, max_pages, scale, o, sel_out, dw,
+                       num_pages, max_pages, scale, n_init, o, sel_out, dw,
                        static_cast<cudaStream_t>(stream));
 }
 

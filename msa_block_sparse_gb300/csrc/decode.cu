@@ -110,14 +110,17 @@ __global__ void __launch_bounds__(256) decode_score_kernel(
 // ---------------------------------------------------------------- select
 
 // grid (B * Hkv), 128 threads: the own block plus the best min(15, own)
-// earlier blocks by score (descending, ties: lower id).  Block i is kept when
+// earlier blocks by score (descending, ties: lower id); blocks b < n_init (the
+// init rule, "#4581" Kernel tuning, read as: the first blocks are always kept)
+// score +inf and so rank first.  Block i is kept when
 // fewer than 15 blocks rank before it (higher score, or equal score and lower
 // id); each thread counts for its blocks over the whole row, four scores per
 // shared-memory load and four independent counters.  The kept ids are written
 // ascending with the own block, -1 padded, to sel and, if given, sel_out.
 __global__ void __launch_bounds__(128) decode_select_kernel(
     const float* __restrict__ scores, const int32_t* __restrict__ cache_lens, int Hkv,
-    int max_pages, int32_t* __restrict__ sel, int32_t* __restrict__ sel_out, uint32_t* status) {
+    int max_pages, int n_init, int32_t* __restrict__ sel, int32_t* __restrict__ sel_out,
+    uint32_t* status) {
   pdl_enter();
   __shared__ __align__(16) float key[1024];
   __shared__ int kept[16];
@@ -129,7 +132,8 @@ __global__ void __launch_bounds__(128) decode_select_kernel(
   const int own = (L + kBlock - 1) / kBlock - 1;
   const int own4 = (own + 3) & ~3;
   const float* sc = scores + static_cast<size_t>(bh) * max_pages;
-  for (int i = tid; i < own4; i += blockDim.x) key[i] = (i < own) ? sc[i] : -INFINITY;
+  for (int i = tid; i < own4; i += blockDim.x)
+    key[i] = (i < own) ? ((i < n_init) ? INFINITY : sc[i]) : -INFINITY;
   if (tid == 0) nkept = 0;
   __syncthreads();
   for (int i = tid; i < own; i += blockDim.x) {
@@ -483,8 +487,9 @@ DecodeWorkspace carve_decode_workspace(WsCursor& ws, int B, int Hq, int Hkv, int
 msa_status_t launch_decode(const void* q, const void* q_idx, const void* k_cache,
                            const void* v_cache, const void* kidx_cache,
                            const int32_t* block_table, const int32_t* cache_lens, int B, int Hq,
-                           int Hkv, int num_pages, int max_pages, float scale, void* o,
-                           int32_t* sel_out, const DecodeWorkspace& ws, cudaStream_t stream) {
+                           int Hkv, int num_pages, int max_pages, float scale, int n_init,
+                           void* o, int32_t* sel_out, const DecodeWorkspace& ws,
+                           cudaStream_t stream) {
   uint32_t* st = status_word();
   dim3 g1((max_pages + kPagesPerCta - 1) / kPagesPerCta, B);
   {
@@ -498,7 +503,7 @@ msa_status_t launch_decode(const void* q, const void* q_idx, const void* k_cache
   {
     TraceScope trace_("decode_select_kernel", stream);
     launch_pdl(decode_select_kernel, B * Hkv, 128, 0, stream, ws.scores, cache_lens, Hkv, max_pages,
-        ws.sel, sel_out, st);
+        n_init, ws.sel, sel_out, st);
   }
   e = check_launch("decode_select_kernel");
   if (e != MSA_OK) return e;
@@ -629,6 +634,6 @@ extern "C" msa_status_t msa_decode_step_static(const void* q, const void* q_idx,
   ws.part_o = base + kStaticScores + kStaticSel;                                // [B, Hkv, splits, 16, 128]
   ws.part_ml = base + kStaticScores + kStaticSel + kStaticPartO;                // [B, Hkv, splits, 16, 2]
   return launch_decode(q, q_idx, k_cache, v_cache, kidx_cache, block_table, cache_lens, B, Hq,
-                       Hkv, num_pages, max_pages, scale, o, sel_out, ws,
+                       Hkv, num_pages, max_pages, scale, 0, o, sel_out, ws,
                        static_cast<cudaStream_t>(stream));
 }

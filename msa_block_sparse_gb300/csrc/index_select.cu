@@ -11,6 +11,9 @@
 //   epilogue (4 warps, thread = query row = TMEM lane): row max of S_b,
 //            then a register-resident insertion into a descending top-15
 //            list (strictly greater wins, so equal scores keep the lower id).
+// With the init rule ("#4581", Kernel tuning; read as: the first n_init
+// blocks are always kept) blocks b < n_init enter the list with score +inf,
+// so they take the first places and the best others fill the rest.
 // The scores never leave the SM.
 #include "kernels.cuh"
 
@@ -75,7 +78,7 @@ __global__ void __launch_bounds__(kSelThreads, 1)
     index_select_kernel(const __grid_constant__ CUtensorMap tm_q,
                         const __grid_constant__ CUtensorMap tm_k, const int32_t* __restrict__ cu,
                         const int2* __restrict__ tiles, const int* __restrict__ num_tiles, int Hi,
-                        int32_t* __restrict__ sel, uint32_t* status) {
+                        int n_init, int32_t* __restrict__ sel, uint32_t* status) {
   pdl_enter();
   if (static_cast<int>(blockIdx.x) >= *num_tiles) return;
   extern __shared__ uint8_t smem_raw[];
@@ -193,7 +196,7 @@ __global__ void __launch_bounds__(kSelThreads, 1)
           t = max3f(t, __uint_as_float(w[j]), __uint_as_float(w[j + 1]));
         m4[q] = fmaxf(t, __uint_as_float(w[31]));
       }
-      const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+      const float mx = (b < n_init) ? INFINITY : fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
       float cv = mx;
       int ci = b;
 #pragma unroll
@@ -218,7 +221,7 @@ __global__ void __launch_bounds__(kSelThreads, 1)
 }
 
 msa_status_t launch_index_select(const void* q_idx, const void* k_idx, const int32_t* cu, int S,
-                                 int T, int Hi, const Plan& plan, int32_t* sel,
+                                 int T, int Hi, int n_init, const Plan& plan, int32_t* sel,
                                  cudaStream_t stream) {
   (void)S;
   CUtensorMap tq, tk;
@@ -238,8 +241,7 @@ msa_status_t launch_index_select(const void* q_idx, const void* k_idx, const int
   {
     TraceScope trace_("index_select_kernel", stream);
     launch_pdl(index_select_kernel, grid, kSelThreads, smem, stream, tq, tk, cu, plan.tiles,
-        plan.num_tiles, Hi, sel,
-        status_word());
+        plan.num_tiles, Hi, n_init, sel, status_word());
   }
   return check_launch("index_select_kernel");
 }

@@ -37,7 +37,7 @@ msa_status_t launch_prologue_bwd(const __nv_bfloat16* x, const __nv_bfloat16* dy
 
 // ---------------------------------------------------------------- index select
 msa_status_t launch_index_select(const void* q_idx, const void* k_idx, const int32_t* cu, int S,
-                                 int T, int Hi, const Plan& plan, int32_t* sel,
+                                 int T, int Hi, int n_init, const Plan& plan, int32_t* sel,
                                  cudaStream_t stream);
 
 // ---------------------------------------------------------------- sparse forward
@@ -91,8 +91,9 @@ DecodeWorkspace carve_decode_workspace(WsCursor& ws, int B, int Hq, int Hkv, int
 msa_status_t launch_decode(const void* q, const void* q_idx, const void* k_cache,
                            const void* v_cache, const void* kidx_cache,
                            const int32_t* block_table, const int32_t* cache_lens, int B, int Hq,
-                           int Hkv, int num_pages, int max_pages, float scale, void* o,
-                           int32_t* sel_out, const DecodeWorkspace& ws, cudaStream_t stream);
+                           int Hkv, int num_pages, int max_pages, float scale, int n_init,
+                           void* o, int32_t* sel_out, const DecodeWorkspace& ws,
+                           cudaStream_t stream);
 
 // ---------------------------------------------------------------- narrow blocks
 // 4-token key blocks, head dim 256, 12 query heads per KV head.

@@ -197,6 +197,27 @@ def test_index_select_full_size(m, idx):
     print(f"cfg{idx}: {ndiff} differing rows, {nnear} near-tie rows of {len(toks) * shape.hi}")
 
 
+@pytest.mark.parametrize("n_init", [1, 3])
+def test_index_select_init_rule(m, n_init):
+    """The init rule (msa_index_select_ex): the first n_init blocks are always
+    kept, on the ragged pack and sampled rows of the 16k pack."""
+    for name, shape in (("ragged", RAGGED), ("cfg1", W.config(1))):
+        cpu, gpu = inputs(name, shape)
+        sel = m.msa_index_select(gpu["q_idx"], gpu["k_idx"], gpu["cu_seqlens"],
+                                 max(shape.max_seqlen, 1), n_init=n_init)
+        m.msa_check_status()
+        toks = None if shape.T <= 8192 else sample_tokens(shape, n_random=512, seed=7)
+        osel, gap = O.index_select(f64(cpu["q_idx"]), f64(cpu["k_idx"]),
+                                   cpu["cu_seqlens"].numpy(), tokens=toks, n_init=n_init)
+        g = sel.cpu().numpy() if toks is None else sel.cpu().numpy()[toks]
+        compare_selection(g, osel, gap, f"{name} n_init={n_init}")
+        pos = O.positions(cpu["cu_seqlens"].numpy())
+        own = (pos if toks is None else pos[toks]) // 128
+        for i in range(n_init):
+            keep = own > i
+            assert np.all(np.any(g[keep] == i, axis=-1)), f"{name}: block {i} not kept"
+
+
 # ------------------------------------------------------------------ forward
 
 @pytest.mark.parametrize("name", ["tiny", "ragged"])
@@ -289,12 +310,12 @@ def test_sparse_bwd_full_size(m, idx):
 
 # ------------------------------------------------------------------ decode
 
-def _decode_check(m, shape, seed, rows=None):
+def _decode_check(m, shape, seed, rows=None, n_init=0):
     big = shape.B > 16
     x = W.make_decode(shape, seed=seed, device=DEV if big else "cpu")
     g = {k: v.to(DEV) for k, v in x.items()}
     o, sel = m.msa_decode_step(g["q"], g["q_idx"], g["k_cache"], g["v_cache"], g["kidx_cache"],
-                               g["block_table"], g["cache_lens"])
+                               g["block_table"], g["cache_lens"], n_init=n_init)
     m.msa_check_status()
     rows = list(range(shape.B)) if rows is None else rows
     # copy to the host only the pages the sampled rows use, with a remapped table
@@ -310,7 +331,7 @@ def _decode_check(m, shape, seed, rows=None):
     kc, vc, ic = (x[n].index_select(0, idx).float().cpu().numpy()
                   for n in ("k_cache", "v_cache", "kidx_cache"))
     ro, rsel, rgap = O.decode_step(f64(x["q"][rows]), f64(x["q_idx"][rows]), kc, vc, ic,
-                                   sub_table, lens[rows], SCALE)
+                                   sub_table, lens[rows], SCALE, n_init=n_init)
     gsel = sel.cpu().numpy()[rows]
     compare_selection(gsel, rsel, rgap, shape.name)
     same = np.all(np.all(gsel == rsel, axis=-1), axis=-1)
@@ -321,6 +342,11 @@ def _decode_check(m, shape, seed, rows=None):
 def test_decode_small_edges(m):
     shape = W.DecodeShape("decode-edges", (1, 127, 128, 129, 2048, 2049, 5000, 300), 32, 2, 2)
     _decode_check(m, shape, seed=5)
+
+
+def test_decode_init_rule(m):
+    shape = W.DecodeShape("decode-init", (1, 127, 128, 129, 2048, 2049, 5000, 300), 32, 2, 2)
+    _decode_check(m, shape, seed=6, n_init=2)
 
 
 def test_decode_exact_ties(m):
