@@ -253,8 +253,10 @@ def run_ours(args):
     torch.cuda.synchronize(dev)
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     ev0.record(stream)
+    h0 = time.perf_counter()
     for i in range(args.steps):
         step(pool[i % args.pool])
+    host_ms = (time.perf_counter() - h0) * 1e3 / args.steps
     ev1.record(stream)
     torch.cuda.synchronize(dev)
     # per-kernel times: the same steps again, every launch bracketed by CUDA
@@ -341,6 +343,7 @@ def run_ours(args):
         "kernels": kernels,
         "kernels_pass": {"what": "a second pass of the same steps with every launch "
                                  "bracketed by CUDA events", "ms_per_step": ms_step_traced},
+        "host_enqueue_ms_per_step": host_ms,
         "kernel_roofline": per_kernel_roofline,
         "gpu_launches": gpu_launches,
         "clocks": clocks,

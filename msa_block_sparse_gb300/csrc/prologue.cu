@@ -9,8 +9,9 @@
 // their rows with 8 threads per row.  Thread c < 4 of a row holds channels
 // [8c, 8c + 8) and [8c + 32, 8c + 40): the rotated pairs (i, i + 32) sit in one
 // thread, so the rotation needs no shuffles; threads 4..7 hold the
-// pass-through channels 64..127.  Each thread keeps the loads of four rows in
-// flight; the first rows' loads are issued before the angles are computed.
+// pass-through channels 64..127.  Each thread keeps two rows in registers: the
+// next row's loads are issued before the current row is processed, and the
+// first rows' loads before the angles are computed.
 //
 // Angles avoid a large fp32 argument: the host turns each frequency f_i into
 // the 64-bit fixed-point fraction F_i = f_i / (2 pi) * 2^64 of a turn, so
@@ -32,11 +33,16 @@ struct PrologueArgs {
 };
 
 constexpr int kProTokens = 16;
-constexpr int kProThreads = 256;
+constexpr int kProThreads = 256;             // backward and decode-append kernels
 constexpr int kProSlots = kProThreads / 8;   // rows processed side by side
-constexpr int kProUnroll = 2;                // rows per thread in flight
+// forward kernel: 128 threads (16 rows side by side), one row per thread in
+// each of two register buffers, so the next rows' loads are in flight while
+// the current rows are normalised, rotated and stored
+constexpr int kPfThreads = 128;
+constexpr int kPfSlots = kPfThreads / 8;
+constexpr int kPfUnroll = 1;
 
-__global__ void __launch_bounds__(kProThreads) prologue_kernel(const PrologueArgs args,
+__global__ void __launch_bounds__(kPfThreads) prologue_kernel(const PrologueArgs args,
                                                                const RopeTurns turns,
                                                                const int32_t* __restrict__ cu,
                                                                int S, int T, float eps,
@@ -66,39 +72,41 @@ __global__ void __launch_bounds__(kProThreads) prologue_kernel(const PrologueArg
   // division once hsum is known.
   int tl = slot / hsum, k = slot - (slot / hsum) * hsum;
   auto advance = [&]() {
-    k += kProSlots;
+    k += kPfSlots;
     while (k >= hsum) {
       k -= hsum;
       ++tl;
     }
   };
-  uint4 xa[kProUnroll], xb[kProUnroll];
-  int rj[kProUnroll], rtl[kProUnroll];
-  size_t rrow[kProUnroll];
-  auto load_rows = [&](int base) {
+  struct Rows {
+    uint4 xa[kPfUnroll], xb[kPfUnroll];
+    int rj[kPfUnroll], rtl[kPfUnroll];
+    size_t rrow[kPfUnroll];
+  };
+  Rows ra, rb;
+  auto load_rows = [&](int base, Rows& R) {
 #pragma unroll
-    for (int u = 0; u < kProUnroll; ++u) {
-      const int r = base + slot + kProSlots * u;
-      rj[u] = -1;
-      rtl[u] = 0;
-      rrow[u] = 0;
-      xa[u] = make_uint4(0, 0, 0, 0);
-      xb[u] = xa[u];
+    for (int u = 0; u < kPfUnroll; ++u) {
+      const int r = base + slot + kPfSlots * u;
+      R.rj[u] = -1;
+      R.rtl[u] = 0;
+      R.rrow[u] = 0;
+      R.xa[u] = make_uint4(0, 0, 0, 0);
+      R.xb[u] = R.xa[u];
       if (r < rows) {
         const int j = (k >= args.hstart[1]) + (k >= args.hstart[2]) + (k >= args.hstart[3]);
         const size_t row = static_cast<size_t>(t0 + tl) * args.jobs[j].H + (k - args.hstart[j]);
         const __nv_bfloat16* src = args.jobs[j].x + row * kD;
-        xa[u] = __ldcs(reinterpret_cast<const uint4*>(src + off0));
-        xb[u] = __ldcs(reinterpret_cast<const uint4*>(src + off1));
-        rj[u] = j;
-        rtl[u] = tl;
-        rrow[u] = row;
+        R.xa[u] = __ldcs(reinterpret_cast<const uint4*>(src + off0));
+        R.xb[u] = __ldcs(reinterpret_cast<const uint4*>(src + off1));
+        R.rj[u] = j;
+        R.rtl[u] = tl;
+        R.rrow[u] = row;
       }
       advance();
     }
   };
-  load_rows(0);   // in flight while the angles are computed
-
+  load_rows(0, ra);   // in flight while the angles are computed
   // (cos, sin) for the CTA's tokens: thread = (token, frequency)
   for (int q = tid; q < kProTokens * (kRopeDim / 2); q += blockDim.x) {
     const int qt = q / (kRopeDim / 2), i = q % (kRopeDim / 2);
@@ -119,15 +127,13 @@ __global__ void __launch_bounds__(kProThreads) prologue_kernel(const PrologueArg
   }
   __syncthreads();
 
-  // the loop bound is uniform over the CTA: every lane reaches the shuffles
-  for (int base = 0; base < rows; base += kProSlots * kProUnroll) {
-    if (base > 0) load_rows(base);
+  auto process = [&](Rows& R) {
 #pragma unroll
-    for (int u = 0; u < kProUnroll; ++u) {
+    for (int u = 0; u < kPfUnroll; ++u) {
       float x[16];
       {
-        const __nv_bfloat162* pa = reinterpret_cast<const __nv_bfloat162*>(&xa[u]);
-        const __nv_bfloat162* pb = reinterpret_cast<const __nv_bfloat162*>(&xb[u]);
+        const __nv_bfloat162* pa = reinterpret_cast<const __nv_bfloat162*>(&R.xa[u]);
+        const __nv_bfloat162* pb = reinterpret_cast<const __nv_bfloat162*>(&R.xb[u]);
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const float2 fa = __bfloat1622float2(pa[e]);
@@ -144,7 +150,7 @@ __global__ void __launch_bounds__(kProThreads) prologue_kernel(const PrologueArg
       float ss = (s4[0] + s4[1]) + (s4[2] + s4[3]);
 #pragma unroll
       for (int m = 4; m >= 1; m >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, m);
-      const int j = rj[u] < 0 ? 0 : rj[u];
+      const int j = R.rj[u] < 0 ? 0 : R.rj[u];
       const float rinv = rsqrtf(ss * (1.f / kD) + eps);
       {
         const float4* wa = reinterpret_cast<const float4*>(&wsh[j][off0]);
@@ -157,7 +163,7 @@ __global__ void __launch_bounds__(kProThreads) prologue_kernel(const PrologueArg
       }
       if (c < 4) {
         // rotate channel 8c + e (x1) with 8c + 32 + e (x2), frequency 8c + e
-        const float4* cp = reinterpret_cast<const float4*>(&cs[rtl[u]][8 * c]);
+        const float4* cp = reinterpret_cast<const float4*>(&cs[R.rtl[u]][8 * c]);
 #pragma unroll
         for (int e2 = 0; e2 < 4; ++e2) {
           const float4 q = cp[e2];   // (cos, sin) of frequencies 2 e2, 2 e2 + 1
@@ -171,7 +177,7 @@ __global__ void __launch_bounds__(kProThreads) prologue_kernel(const PrologueArg
           }
         }
       }
-      if (rj[u] >= 0) {
+      if (R.rj[u] >= 0) {
         uint4 oa, ob;
         oa.x = pack_bf16x2(x[0], x[1]);
         oa.y = pack_bf16x2(x[2], x[3]);
@@ -181,11 +187,21 @@ __global__ void __launch_bounds__(kProThreads) prologue_kernel(const PrologueArg
         ob.y = pack_bf16x2(x[10], x[11]);
         ob.z = pack_bf16x2(x[12], x[13]);
         ob.w = pack_bf16x2(x[14], x[15]);
-        __nv_bfloat16* dst = args.jobs[rj[u]].y + rrow[u] * kD;
+        __nv_bfloat16* dst = args.jobs[R.rj[u]].y + R.rrow[u] * kD;
         *reinterpret_cast<uint4*>(dst + off0) = oa;
         *reinterpret_cast<uint4*>(dst + off1) = ob;
       }
     }
+  };
+  // the loop bound is uniform over the CTA: every lane reaches the shuffles;
+  // the next rows' loads are in flight while the current ones are processed
+  constexpr int kStep = kPfSlots * kPfUnroll;
+  for (int base = 0; base < rows; base += 2 * kStep) {
+    if (base + kStep < rows) load_rows(base + kStep, rb);
+    process(ra);
+    if (base + kStep >= rows) break;
+    if (base + 2 * kStep < rows) load_rows(base + 2 * kStep, ra);
+    process(rb);
   }
 }
 
@@ -209,7 +225,7 @@ msa_status_t launch_prologue(const PrologueJob* jobs, int njobs, const int32_t* 
   dim3 grid((T + kProTokens - 1) / kProTokens);
   {
     TraceScope trace_("prologue_kernel", stream);
-    launch_pdl(prologue_kernel, grid, kProThreads, 0, stream, args, turns, cu, S, T, eps,
+    launch_pdl(prologue_kernel, grid, kPfThreads, 0, stream, args, turns, cu, S, T, eps,
         status_word());
   }
   return check_launch("prologue_kernel");
