@@ -49,6 +49,8 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-prologue-bwd", action="store_true")
     ap.add_argument("--no-qsa", action="store_true")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the 64-head 16k prefill and the 32k training pack")
     return ap.parse_args()
 
 
@@ -175,6 +177,76 @@ def traffic_for(name: str):
     if not d or d.get("source_hash") != kernel_source_hash(name):
         return None
     return d.get("bytes_per_launch")
+
+
+def time_pack(m, W, workmodel, shape, dev, stream, seed, nsteps, with_bwd, sustained):
+    """Prologue + select + forward (+ backward) on one pack (inputs larger than
+    L2); untimed warm-up, CUDA events over `nsteps`, then an event-bracketed pass
+    for the per-kernel split."""
+    import torch
+    x = W.make_prefill(shape, seed=seed, device=dev, with_grad_out=with_bwd)
+    T, S, hq, hkv, hi, L = shape.T, shape.S, shape.hq, shape.hkv, shape.hi, shape.max_seqlen
+    bf = torch.bfloat16
+    b = {n: torch.empty((T, h, 128), dtype=bf, device=dev)
+         for n, h in (("q", hq), ("k", hkv), ("qi", hi), ("ki", hi), ("o", hq))}
+    sel = torch.empty((T, hi, 16), dtype=torch.int32, device=dev)
+    lse = torch.empty((T, hq), dtype=torch.float32, device=dev)
+    ws = {c: torch.empty(m.workspace_bytes(c, *a), dtype=torch.uint8, device=dev)
+          for c, a in (("index_select", (T, S, hi, L)), ("sparse_attn_fwd", (T, S, hq, hkv, L)),
+                       ("sparse_attn_bwd", (T, S, hq, hkv, L)))
+          if with_bwd or c != "sparse_attn_bwd"}
+    if with_bwd:
+        g = {n: torch.empty_like(b[r]) for n, r in (("dq", "q"), ("dk", "k"), ("dv", "k"))}
+
+    def step():
+        m.msa_qk_norm_rope4(x["q"], x["k"], x["q_idx"], x["k_idx"], x["w_q"], x["w_k"],
+                            x["w_qi"], x["w_ki"], x["cu_seqlens"],
+                            outs=(b["q"], b["k"], b["qi"], b["ki"]))
+        m.msa_index_select(b["qi"], b["ki"], x["cu_seqlens"], L, out=sel,
+                           workspace=ws["index_select"])
+        m.msa_sparse_attn_fwd(b["q"], b["k"], x["v"], sel, x["cu_seqlens"], L, out=b["o"],
+                              lse=lse, workspace=ws["sparse_attn_fwd"])
+        if with_bwd:
+            m.msa_sparse_attn_bwd(b["q"], b["k"], x["v"], b["o"], x["do"], lse, sel,
+                                  x["cu_seqlens"], L, dq=g["dq"], dk=g["dk"], dv=g["dv"],
+                                  workspace=ws["sparse_attn_bwd"])
+
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(nsteps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    m.msa_trace_begin()
+    for _ in range(nsteps):
+        step()
+    torch.cuda.synchronize(dev)
+    tr = m.msa_trace_end()
+    m.msa_check_status(dev)
+    ms = e0.elapsed_time(e1) / nsteps
+    wk = workmodel.prefill_work(shape.seqlens, hq, hkv, hi)
+    per = {n: v["ms"] / v["launches"] for n, v in tr.items()}
+    flops = wk["fwd_flops"] + wk["select_flops"] + (wk["bwd_flops"] if with_bwd else 0.0)
+    out = {"workload": shape.name, "seqlens": list(shape.seqlens), "hq": hq, "hkv": hkv,
+           "hi": hi, "ms_per_step": ms,
+           "step": "qk_norm_rope4 + index_select + sparse_attn_fwd" +
+                   (" + sparse_attn_bwd" if with_bwd else ""),
+           "useful_tflops": flops / (ms * 1e-3) / 1e12,
+           "frac_of_sustained": flops / (ms * 1e-3) / 1e12 / sustained,
+           "kernels_ms": per, "work": wk}
+    pf = per.get("index_select_kernel", 0.0) + per.get("sparse_fwd_kernel", 0.0)
+    if pf > 0:
+        f = wk["fwd_flops"] + wk["select_flops"]
+        out["prefill_select_fwd"] = {"ms": pf, "useful_tflops": f / (pf * 1e-3) / 1e12,
+                                     "frac_of_sustained": f / (pf * 1e-3) / 1e12 / sustained}
+    if with_bwd and "sparse_bwd_kernel" in per:
+        t = per["sparse_bwd_kernel"]
+        out["backward"] = {"ms": t, "useful_tflops": wk["bwd_flops"] / (t * 1e-3) / 1e12,
+                           "frac_of_sustained": wk["bwd_flops"] / (t * 1e-3) / 1e12 / sustained}
+    return out
 
 
 def run_ours(args):
@@ -548,6 +620,17 @@ def run_ours(args):
                                "calls"},
         }
         del dx
+
+    # ---- the other prefill workloads: full layer shape on a 16k pack (prefill)
+    # and the 32k training pack (prefill + backward)
+    if not args.no_configs:
+        sus = peaks.get("bf16_tflops_sustained", 1700.0)
+        out["configs"] = {
+            "pack16k-8seq-64q4kv": time_pack(m, W, workmodel, W.config(2, args.seed), dev, stream,
+                                             args.seed + 1000 * rank, 10, False, sus),
+            "pack32k-4seq-64q4kv": time_pack(m, W, workmodel, W.config(4, args.seed), dev, stream,
+                                             args.seed + 1000 * rank, 5, True, sus),
+        }
 
     # ---- narrow-block variant: 16k pack, 12 q / 1 kv heads, head dim 256, 4-token
     # blocks, fwd + bwd (the pages' second timed workload)
