@@ -503,7 +503,10 @@ struct QsaDkvSmem {
   uint8_t v[kKTileBytes];
   uint8_t p[128 * 128];                     // P, rows x 64 keys, 128B-swizzled
   uint8_t ds[128 * 128];                    // dS, same layout
-  uint64_t kv_full, kv_empty, q_full, q_empty, do_full, do_empty;
+  // Q and dO move as two halves of 128 head-dim columns each: half h is what
+  // the h-th dK^T / dV^T MMA reads, so the next tile's half h loads as soon as
+  // that MMA is done
+  uint64_t kv_full, kv_empty, q_full[2], q_empty[2], do_full[2], do_empty[2];
   uint64_t s_full, pds_full, pds_empty, acc_full, acc_free;
   uint32_t tmem_base;
 };
@@ -935,10 +938,12 @@ __global__ void __launch_bounds__(kQBwdThreads, 1)
   if (tid == 0) {
     mbar_init(&sm.kv_full, 1);
     mbar_init(&sm.kv_empty, 1);
-    mbar_init(&sm.q_full, 1);
-    mbar_init(&sm.q_empty, 1);
-    mbar_init(&sm.do_full, 1);
-    mbar_init(&sm.do_empty, 1);
+    for (int hf = 0; hf < 2; ++hf) {
+      mbar_init(&sm.q_full[hf], 1);
+      mbar_init(&sm.q_empty[hf], 1);
+      mbar_init(&sm.do_full[hf], 1);
+      mbar_init(&sm.do_empty[hf], 1);
+    }
     mbar_init(&sm.s_full, 1);
     mbar_init(&sm.pds_full, 128);
     mbar_init(&sm.pds_empty, 1);
@@ -982,13 +987,15 @@ __global__ void __launch_bounds__(kQBwdThreads, 1)
           tma_load_3d(sm.k + c * kKChunk, &tm_k, &sm.kv_full, 64 * c, g, seq0 + item.y * kQKeys);
           tma_load_3d(sm.v + c * kKChunk, &tm_v, &sm.kv_full, 64 * c, g, seq0 + item.y * kQKeys);
         }
-        for (int i = 0; i < nq; ++i) {
-          if (!(ok = mbar_wait(&sm.q_empty, (qc & 1) ^ 1, status, 42))) break;
+        for (int i = 0; ok && i < nq; ++i) {
           const int qt = __ldg(kl + 1 + i);
-          mbar_arrive_expect_tx(&sm.q_full, 4 * kQRows * 128);
-          for (int c = 0; c < 4; ++c)
-            tma_load_3d(sm.q + c * kQChunk, &tm_q, &sm.q_full, 64 * c, g * kQG,
-                        seq0 + qt * kQTok);
+          for (int hf = 0; hf < 2; ++hf) {
+            if (!(ok = mbar_wait(&sm.q_empty[hf], (qc & 1) ^ 1, status, 42))) break;
+            mbar_arrive_expect_tx(&sm.q_full[hf], 2 * kQRows * 128);
+            for (int c = 2 * hf; c < 2 * hf + 2; ++c)
+              tma_load_3d(sm.q + c * kQChunk, &tm_q, &sm.q_full[hf], 64 * c, g * kQG,
+                          seq0 + qt * kQTok);
+          }
           ++qc;
         }
         ++ic;
@@ -1006,13 +1013,15 @@ __global__ void __launch_bounds__(kQBwdThreads, 1)
         const int nq = __ldg(kl);
         if (nq == 0) continue;
         const int seq0 = __ldg(cu + items[it].x);
-        for (int i = 0; i < nq; ++i) {
-          if (!(ok = mbar_wait(&sm.do_empty, (dc & 1) ^ 1, status, 43))) break;
+        for (int i = 0; ok && i < nq; ++i) {
           const int qt = __ldg(kl + 1 + i);
-          mbar_arrive_expect_tx(&sm.do_full, 4 * kQRows * 128);
-          for (int c = 0; c < 4; ++c)
-            tma_load_3d(sm.dout + c * kQChunk, &tm_do, &sm.do_full, 64 * c, g * kQG,
-                        seq0 + qt * kQTok);
+          for (int hf = 0; hf < 2; ++hf) {
+            if (!(ok = mbar_wait(&sm.do_empty[hf], (dc & 1) ^ 1, status, 43))) break;
+            mbar_arrive_expect_tx(&sm.do_full[hf], 2 * kQRows * 128);
+            for (int c = 2 * hf; c < 2 * hf + 2; ++c)
+              tma_load_3d(sm.dout + c * kQChunk, &tm_do, &sm.do_full[hf], 64 * c, g * kQG,
+                          seq0 + qt * kQTok);
+          }
           ++dc;
         }
       }
@@ -1030,23 +1039,32 @@ __global__ void __launch_bounds__(kQBwdThreads, 1)
         if (nq == 0) continue;
         if (!(ok = mbar_wait(&sm.kv_full, ic & 1, status, 44))) break;
         for (int i = 0; ok && i < nq; ++i, ++n) {
-          if (!(ok = mbar_wait(&sm.q_full, n & 1, status, 45))) break;
-          if (!(ok = mbar_wait(&sm.do_full, n & 1, status, 46))) break;
-          tc_fence_after();
+          // S over the two Q halves as they land, then dP over the dO halves
+          for (int hf = 0; ok && hf < 2; ++hf) {
+            if (!(ok = mbar_wait(&sm.q_full[hf], n & 1, status, 45))) break;
+            tc_fence_after();
 #pragma unroll
-          for (int kk = 0; kk < 16; ++kk) {
-            const uint32_t cq = (kk >> 2) * kQChunk + (kk & 3) * 32;
-            const uint32_t ck = (kk >> 2) * kKChunk + (kk & 3) * 32;
-            umma_bf16(tmem + kColS, sdesc_sw128(qa + cq, 16, 1024),
-                      sdesc_sw128(ka + ck, 16, 1024), kQIdS, kk > 0);
+            for (int k8 = 0; k8 < 8; ++k8) {
+              const int kk = 8 * hf + k8;
+              const uint32_t cq = (kk >> 2) * kQChunk + (kk & 3) * 32;
+              const uint32_t ck = (kk >> 2) * kKChunk + (kk & 3) * 32;
+              umma_bf16(tmem + kColS, sdesc_sw128(qa + cq, 16, 1024),
+                        sdesc_sw128(ka + ck, 16, 1024), kQIdS, kk > 0);
+            }
           }
+          for (int hf = 0; ok && hf < 2; ++hf) {
+            if (!(ok = mbar_wait(&sm.do_full[hf], n & 1, status, 46))) break;
+            tc_fence_after();
 #pragma unroll
-          for (int kk = 0; kk < 16; ++kk) {
-            const uint32_t cq = (kk >> 2) * kQChunk + (kk & 3) * 32;
-            const uint32_t ck = (kk >> 2) * kKChunk + (kk & 3) * 32;
-            umma_bf16(tmem + kColDp, sdesc_sw128(da + cq, 16, 1024),
-                      sdesc_sw128(va + ck, 16, 1024), kQIdS, kk > 0);
+            for (int k8 = 0; k8 < 8; ++k8) {
+              const int kk = 8 * hf + k8;
+              const uint32_t cq = (kk >> 2) * kQChunk + (kk & 3) * 32;
+              const uint32_t ck = (kk >> 2) * kKChunk + (kk & 3) * 32;
+              umma_bf16(tmem + kColDp, sdesc_sw128(da + cq, 16, 1024),
+                        sdesc_sw128(va + ck, 16, 1024), kQIdS, kk > 0);
+            }
           }
+          if (!ok) break;
           umma_commit(&sm.s_full);
           if (i == nq - 1) umma_commit(&sm.kv_empty);    // K, V are free once S, dP are done
           if (!(ok = mbar_wait(&sm.pds_full, n & 1, status, 47))) break;
@@ -1055,24 +1073,27 @@ __global__ void __launch_bounds__(kQBwdThreads, 1)
           if (i == 0 && ic > 0 && !(ok = mbar_wait(&sm.acc_free, (ic - 1) & 1, status, 48)))
             break;
           tc_fence_after();
-          // dK first: Q is released first, so the next tile's Q (which its S
-          // needs before its dP needs dO) loads while dV runs
+          // dK first, one head-dim half at a time: each Q half is released as
+          // soon as its MMAs are done, so the next tile's Q (which its S needs
+          // before its dP needs dO) loads while the rest runs
 #pragma unroll
-          for (int hf = 0; hf < 2; ++hf)
+          for (int hf = 0; hf < 2; ++hf) {
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk)
               umma_bf16(tmem + kColDk + hf * 64,
                         sdesc_sw128(qa + hf * 2 * kQChunk + kk * 2048, kQChunk, 1024),
                         sdesc_sw128(sa + kk * 2048, kQChunk, 1024), kQIdKV, (i > 0 || kk > 0));
-          umma_commit(&sm.q_empty);
+            umma_commit(&sm.q_empty[hf]);
+          }
 #pragma unroll
-          for (int hf = 0; hf < 2; ++hf)
+          for (int hf = 0; hf < 2; ++hf) {
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk)
               umma_bf16(tmem + kColDv + hf * 64,
                         sdesc_sw128(da + hf * 2 * kQChunk + kk * 2048, kQChunk, 1024),
                         sdesc_sw128(pa + kk * 2048, kQChunk, 1024), kQIdKV, (i > 0 || kk > 0));
-          umma_commit(&sm.do_empty);
+            umma_commit(&sm.do_empty[hf]);
+          }
           umma_commit(&sm.pds_empty);
         }
         umma_commit(&sm.acc_full);
