@@ -59,6 +59,27 @@ def dist_env():
             int(os.environ.get("LOCAL_RANK", "0")))
 
 
+def rank_seed(seed: int, rank: int, j: int = 0) -> int:
+    """Seed of input copy j on `rank`: every rank draws its own packs (weak scaling)."""
+    return seed + 1000 * rank + j
+
+
+def slowest_rank_ms(ms_local: float, world: int, device=None) -> float:
+    """Max over ranks of a per-rank time: the job ends with its slowest rank."""
+    if world <= 1:
+        return ms_local
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([ms_local], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_ms_per_pack(ms_step_max: float, world: int) -> float:
+    """Whole-job value of the metric: `world` packs complete every ms_step_max."""
+    return ms_step_max / world
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -119,9 +140,11 @@ class ClockSampler:
 # ------------------------------------------------------------------ reference arm
 
 def run_reference(args):
+    """The oracle arm: rank 0 alone times the oracle and returns its JSON line;
+    the other ranks return None without work."""
     rank, world, _ = dist_env()
     if rank != 0:
-        return
+        return None
     from oracle import cpu_sample
     import workloads as W
     n_tok = 128
@@ -145,7 +168,7 @@ def run_reference(args):
                                    f"tokens per step (all heads), scaled by T/{n_tok}"},
         "e2e": {"value": ms, "unit": "ms", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
-    print(json.dumps(line), flush=True)
+    return line
 
 
 # ------------------------------------------------------------------ our arm
@@ -274,7 +297,7 @@ def run_ours(args):
     # ---- input pool (each rank draws its own pack: weak scaling)
     pool = []
     for j in range(args.pool):
-        pool.append(W.make_prefill(shape, seed=args.seed + 1000 * rank + j, device=dev,
+        pool.append(W.make_prefill(shape, seed=rank_seed(args.seed, rank, j), device=dev,
                                    with_grad_out=True))
     cu = pool[0]["cu_seqlens"]
     bf = torch.bfloat16
@@ -347,11 +370,7 @@ def run_ours(args):
     m.msa_check_status(dev)
     ms_step = ev0.elapsed_time(ev1) / args.steps
     ms_step_traced = ev2.elapsed_time(ev3) / args.steps
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([ms_step], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_step = float(t.item())
+    ms_step = slowest_rank_ms(ms_step, world, dev)
 
     wk = workmodel.prefill_work(shape.seqlens, hq, hkv, hi)
     total_flops = wk["fwd_flops"] + wk["bwd_flops"] + wk["select_flops"]
@@ -391,7 +410,7 @@ def run_ours(args):
 
     out = {
         "metric": METRIC,
-        "value": ms_step / world,
+        "value": job_ms_per_pack(ms_step, world),
         "unit": "ms",
         "n_gpus": world,
         "steps": args.steps,
@@ -474,8 +493,9 @@ def run_ours(args):
         e1.record(s_down)
         torch.cuda.synchronize(dev)
         barrier()
-        e2e_ms = e0.elapsed_time(e1) / n_e2e
-        out["e2e"] = {"value": e2e_ms / world, "unit": "ms", "h2d_bytes_per_step": h2d,
+        e2e_ms = slowest_rank_ms(e0.elapsed_time(e1) / n_e2e, world, dev)
+        out["e2e"] = {"value": job_ms_per_pack(e2e_ms, world), "unit": "ms",
+                      "h2d_bytes_per_step": h2d,
                       "d2h_bytes_per_step": d2h, "steps": n_e2e,
                       "schedule": "upload, compute and download on three streams, "
                                   "double-buffered; each step includes its own copies"}
@@ -532,7 +552,7 @@ def run_ours(args):
     # ---- decode step on the paged-cache workload
     if not args.no_decode:
         dshape = W.config(3, args.seed)
-        dx = W.make_decode(dshape, seed=args.seed + 1000 * rank, device=dev)
+        dx = W.make_decode(dshape, seed=rank_seed(args.seed, rank), device=dev)
         B, maxp = dshape.B, dx["block_table"].shape[1]
         dws = torch.empty(m.workspace_bytes("decode_step", B, dshape.hq, dshape.hkv, maxp),
                           dtype=torch.uint8, device=dev)
@@ -627,16 +647,16 @@ def run_ours(args):
         sus = peaks.get("bf16_tflops_sustained", 1700.0)
         out["configs"] = {
             "pack16k-8seq-64q4kv": time_pack(m, W, workmodel, W.config(2, args.seed), dev, stream,
-                                             args.seed + 1000 * rank, 10, False, sus),
+                                             rank_seed(args.seed, rank), 10, False, sus),
             "pack32k-4seq-64q4kv": time_pack(m, W, workmodel, W.config(4, args.seed), dev, stream,
-                                             args.seed + 1000 * rank, 5, True, sus),
+                                             rank_seed(args.seed, rank), 5, True, sus),
         }
 
     # ---- narrow-block variant: 16k pack, 12 q / 1 kv heads, head dim 256, 4-token
     # blocks, fwd + bwd (the pages' second timed workload)
     if not args.no_qsa:
         qshape = W.qsa_config(1, args.seed)
-        qx = W.make_qsa(qshape, seed=args.seed + 1000 * rank, device=dev)
+        qx = W.make_qsa(qshape, seed=rank_seed(args.seed, rank), device=dev)
         qcu, qL = qx["cu_seqlens"], qshape.max_seqlen
         qo = torch.empty_like(qx["q"])
         qlse = torch.empty((qshape.T, qshape.hq), dtype=torch.float32, device=dev)
@@ -731,7 +751,9 @@ def main():
         for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS",
                     "NUMEXPR_NUM_THREADS", "BLIS_NUM_THREADS"):
             os.environ[var] = "1"
-        run_reference(args)
+        line = run_reference(args)
+        if line is not None:
+            print(json.dumps(line), flush=True)
     else:
         run_ours(args)
 
