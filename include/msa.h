@@ -94,6 +94,13 @@ MSA_API const char* msa_last_error(void);
  * debugging; it blocks the host. */
 MSA_API msa_status_t msa_check_status(msa_stream_t stream);
 
+/* Diagnostic of the failure-detection path: launches one kernel on `stream`
+ * whose bounded wait on an mbarrier that nothing completes runs out (after the
+ * library's wait limit, about 2 s) and sets the timeout bit of the status word,
+ * then returns.  No fault is raised and the context stays usable; the next
+ * msa_check_status returns MSA_ERR_TIMEOUT (wait site 65535). */
+MSA_API msa_status_t msa_selftest_wait(msa_stream_t stream);
+
 /* ------------------------------------------------------------------------
  * Prologue ("MiniMax-M3.1-Flash", 1 "Model Introduction"; "MiniMax-M3",
  * "Architecture Notes").  x bf16 [T, H, 128] -> y bf16 [T, H, 128] (y may be

@@ -8,6 +8,7 @@ from .api import (  # noqa: F401
     MSAError,
     lib,
     msa_check_status,
+    msa_selftest_wait,
     msa_decode_append,
     msa_decode_step,
     msa_index_select,

@@ -26,6 +26,7 @@ _SIGNATURES = {
     "msa_abi_version": (_c_int, []),
     "msa_last_error": (ctypes.c_char_p, []),
     "msa_check_status": (_c_int, [_vp]),
+    "msa_selftest_wait": (_c_int, [_vp]),
     "msa_trace_begin": (_c_int, []),
     "msa_trace_end": (_c_int, [ctypes.c_char_p, _c_size]),
     "msa_qk_norm_rope": (_c_int, [_vp, _vp, _c_int, _c_int, _vp, _vp, _c_int, _c_int, _c_float,
@@ -134,6 +135,13 @@ def msa_check_status(device=None) -> None:
 
 
 # ------------------------------------------------------------------ prologue
+
+def msa_selftest_wait(device=None) -> None:
+    """Launch the diagnostic kernel whose bounded wait runs out (~2 s); the next
+    msa_check_status raises MSAError (timeout)."""
+    s = torch.cuda.current_stream(device).cuda_stream
+    _check(lib().msa_selftest_wait(ctypes.c_void_p(s)))
+
 
 def msa_trace_begin() -> None:
     """Start recording CUDA-event timings around every library kernel launch."""

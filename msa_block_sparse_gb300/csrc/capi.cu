@@ -340,6 +340,28 @@ msa_status_t msa_check_status(msa_stream_t stream) {
   return MSA_OK;
 }
 
+// One thread waits on an mbarrier that nothing arrives on: the bounded wait
+// runs out, records site 65535 in the status word and returns.
+__global__ void selftest_wait_kernel(uint32_t* status) {
+  pdl_enter();
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) (void)mbar_wait(&bar, 0, status, 0xFFFFu);
+}
+
+msa_status_t msa_selftest_wait(msa_stream_t stream) {
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  {
+    TraceScope trace_("selftest_wait_kernel", st);
+    launch_pdl(selftest_wait_kernel, 1, 32, 0, st, status_word());
+  }
+  return check_launch("selftest_wait_kernel");
+}
+
 // ---------------------------------------------------------------- prologue
 
 static msa_status_t check_rope(int rope_dim, float rope_base, float eps) {
