@@ -181,8 +181,8 @@ struct AttendSmem {
   uint8_t k[2 * 16384];
   uint8_t v[2 * 16384];
   __nv_bfloat16 q[16][kRowPad];
-  int page[4];
-  int blk[4];
+  int page[kSplitBlocks];
+  int blk[kSplitBlocks];
   uint64_t k_full, v_full;
 };
 
@@ -220,8 +220,9 @@ __global__ void __launch_bounds__(128) decode_attend_kernel(
   // ---- this split's blocks (sel is ascending, -1 last)
   int nmy = 0;
 #pragma unroll
-  for (int i = 0; i < 4; ++i)
-    if (sel[(static_cast<size_t>(b) * Hkv + h) * kTopK + split * 4 + i] >= 0) nmy = i + 1;
+  for (int i = 0; i < kSplitBlocks; ++i)
+    if (sel[(static_cast<size_t>(b) * Hkv + h) * kTopK + split * kSplitBlocks + i] >= 0)
+      nmy = i + 1;
   if (nmy == 0) {
     for (int i = tid; i < 16; i += blockDim.x) {
       part_ml[(obase + i) * 2] = -INFINITY;
@@ -229,8 +230,9 @@ __global__ void __launch_bounds__(128) decode_attend_kernel(
     }
     return;
   }
-  if (tid < 4) {
-    const int blk = (tid < nmy) ? sel[(static_cast<size_t>(b) * Hkv + h) * kTopK + split * 4 + tid] : 0;
+  if (tid < kSplitBlocks) {
+    const int blk =
+        (tid < nmy) ? sel[(static_cast<size_t>(b) * Hkv + h) * kTopK + split * kSplitBlocks + tid] : 0;
     int pg = (tid < nmy) ? block_table[static_cast<size_t>(b) * max_pages + blk] : 0;
     if (pg < 0 || pg >= num_pages) {
       atomicOr(status, kStatusBounds);

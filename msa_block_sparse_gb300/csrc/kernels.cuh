@@ -86,7 +86,8 @@ struct DecodeWorkspace {
   float* part_ml;      // [B, Hkv, kDecodeSplits, 16, 2] partial (max, sum)
   int max_pages;
 };
-constexpr int kDecodeSplits = 4;     // selected blocks are attended in 4 groups of 4
+constexpr int kDecodeSplits = 4;     // the 16 selected blocks are attended in 4 groups
+constexpr int kSplitBlocks = kTopK / kDecodeSplits;   // blocks per group
 DecodeWorkspace carve_decode_workspace(WsCursor& ws, int B, int Hq, int Hkv, int max_pages);
 msa_status_t launch_decode(const void* q, const void* q_idx, const void* k_cache,
                            const void* v_cache, const void* kidx_cache,
