@@ -861,17 +861,21 @@ __global__ void __launch_bounds__(kQBwdThreads, 1)
         tmem_ld32(pbuf + 32, dv + 32);
         tmem_ld_wait();
         uint32_t pk[32];
+        // keys in pairs: one selection bit per pair, fp32 math two lanes at a time
+        const float2 sl2v = make_float2(sl2, sl2), lxv = make_float2(ld.x, ld.x),
+                     lyv = make_float2(ld.y, ld.y);
 #pragma unroll
         for (int j2 = 0; j2 < 32; ++j2) {
-          float d2[2];
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int j = 2 * j2 + e;
-            const bool keep = ((bits >> (j >> 2)) & 1u) && j <= kmax;
-            const float p = qex2(fmaf(__uint_as_float(sv[j]), sl2, ld.x));
-            d2[e] = keep ? p * (__uint_as_float(dv[j]) + ld.y) : 0.f;
-          }
-          pk[j2] = pack_bf16x2(d2[0], d2[1]);
+          const int j = 2 * j2;
+          const bool blk = (bits >> (j >> 2)) & 1u;
+          const float2 y = ffma2(make_float2(__uint_as_float(sv[j]), __uint_as_float(sv[j + 1])),
+                                 sl2v, lxv);
+          const float2 pe = make_float2(qex2(y.x), qex2(y.y));
+          float2 dd = fmul2(
+              pe, fadd2(make_float2(__uint_as_float(dv[j]), __uint_as_float(dv[j + 1])), lyv));
+          dd.x = (blk && j <= kmax) ? dd.x : 0.f;
+          dd.y = (blk && j + 1 <= kmax) ? dd.y : 0.f;
+          pk[j2] = pack_bf16x2(dd.x, dd.y);
         }
         tmem_st16(sbuf, pk);
         tmem_st16(sbuf + 16, pk + 16);
@@ -1139,22 +1143,25 @@ __global__ void __launch_bounds__(kQBwdThreads, 1)
         if (n > 0 && !(ok = mbar_wait(&sm.pds_empty, (n - 1) & 1, status, 50))) break;
         uint8_t* prow = sm.p;
         uint8_t* srow = sm.ds;
+        // keys in pairs: both lie in one 4-key block, so one selection bit
+        // serves the pair; fp32 math two lanes at a time
+        const float2 sl2v = make_float2(sl2, sl2), lxv = make_float2(ld.x, ld.x),
+                     lyv = make_float2(ld.y, ld.y);
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
           uint32_t pw[4], sw[4];
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            float pp[2], dd[2];
-#pragma unroll
-            for (int h2 = 0; h2 < 2; ++h2) {
-              const int j = 8 * c + 2 * e + h2;
-              const bool keep = ((bits >> (j >> 2)) & 1u) && j <= kmax;
-              const float p = keep ? qex2(fmaf(__uint_as_float(sv[j]), sl2, ld.x)) : 0.f;
-              pp[h2] = p;
-              dd[h2] = keep ? p * (__uint_as_float(dv[j]) + ld.y) : 0.f;
-            }
-            pw[e] = pack_bf16x2(pp[0], pp[1]);
-            sw[e] = pack_bf16x2(dd[0], dd[1]);
+            const int j = 8 * c + 2 * e;
+            const bool blk = (bits >> (j >> 2)) & 1u;
+            const float2 y = ffma2(make_float2(__uint_as_float(sv[j]), __uint_as_float(sv[j + 1])),
+                                   sl2v, lxv);
+            const float2 pe = make_float2(qex2(y.x), qex2(y.y));
+            const float2 dd = fmul2(
+                pe, fadd2(make_float2(__uint_as_float(dv[j]), __uint_as_float(dv[j + 1])), lyv));
+            const bool k0 = blk && j <= kmax, k1 = blk && j + 1 <= kmax;
+            pw[e] = pack_bf16x2(k0 ? pe.x : 0.f, k1 ? pe.y : 0.f);
+            sw[e] = pack_bf16x2(k0 ? dd.x : 0.f, k1 ? dd.y : 0.f);
           }
           const uint32_t off = sw128_offset(static_cast<uint32_t>(r), static_cast<uint32_t>(c));
           *reinterpret_cast<uint4*>(prow + off) = make_uint4(pw[0], pw[1], pw[2], pw[3]);
