@@ -47,6 +47,7 @@ constexpr int kFwdUnionStride = 132;
 struct FwdWorkspace {
   Plan plan;
   int* ulist;          // [max_tiles * 16, Hkv, kFwdUnionStride]
+  int* tile_ctr;       // [Hkv] next tile to claim, zeroed by fwd_union_kernel
 };
 FwdWorkspace carve_fwd_workspace(WsCursor& ws, int T, int S, int Hkv);
 msa_status_t launch_sparse_fwd(const void* q, const void* k, const void* v, const int32_t* sel,

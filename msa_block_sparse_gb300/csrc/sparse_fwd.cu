@@ -53,6 +53,7 @@ struct FwdSmem {
   uint8_t v[2][kTile];
   int ublk[2][kTpt * kTopK];                 // union entries (block << 8) | token mask
   int n_union[2];
+  int tile_id[2];                           // tile of the slot; -1: no tiles left
   float2 ml[2][128];                        // per half: (max, sum) of each row, for the merge
   uint64_t tile_full[2], tile_empty[2];
   uint64_t k_full[2], k_empty[2], v_full[2], v_empty[2];
@@ -104,11 +105,13 @@ __global__ void __launch_bounds__(256) fwd_union_kernel(const int32_t* __restric
                                                         const int2* __restrict__ tiles,
                                                         const int* __restrict__ num_tiles,
                                                         int Hkv, int* __restrict__ ulist,
+                                                        int* __restrict__ tile_ctr,
                                                         uint32_t* status) {
   pdl_enter();
   __shared__ uint32_t words_s[8][kMaskWords];
   const int total = *num_tiles * kG;
   const int g = blockIdx.y;
+  if (blockIdx.x == 0 && threadIdx.x == 0) tile_ctr[g] = 0;   // the forward claims from 0
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   for (int ti = blockIdx.x * 8 + warp; ti < total; ti += gridDim.x * 8) {
     int* out = ulist + (static_cast<size_t>(ti) * Hkv + g) * kFwdUnionStride;
@@ -164,7 +167,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     sparse_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                       const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v, const int* __restrict__ ulist,
-                      const int32_t* __restrict__ cu, const int2* __restrict__ tiles,
+                      int* __restrict__ tile_ctr, const int32_t* __restrict__ cu, const int2* __restrict__ tiles,
                       const int* __restrict__ num_tiles, int Hq, int Hkv, float scale,
                       __nv_bfloat16* __restrict__ o, float* __restrict__ lse, uint32_t* status) {
   pdl_enter();
@@ -213,22 +216,46 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       prefetch_tmap(&tm_q);
       prefetch_tmap(&tm_k);
     }
+    // Tiles are claimed from a per-KV-head counter (heaviest first, as the plan
+    // orders them) so that CTAs finishing early take more; the claimed id goes
+    // to the other roles through the tile slot, -1 once none are left.
     uint32_t tcount = 0, kc = 0;
     bool alive = true;
-    for (int ti = blockIdx.x; alive && ti < total; ti += gridDim.x) {
-      TileInfo t;
-      if (!tile_info(ti, tiles, cu, t)) continue;
+    int pending = 0;
+    if (lane == 0) pending = atomicAdd(tile_ctr + g, 1);
+    while (alive) {
+      int ti = -1;
+      if (lane == 0) {
+        ti = pending;
+        TileInfo tt;
+        while (ti < total && !tile_info(ti, tiles, cu, tt)) ti = atomicAdd(tile_ctr + g, 1);
+        if (ti >= total) ti = -1;
+      }
+      ti = __shfl_sync(0xffffffffu, ti, 0);
       const int tb = tcount & 1;
       if (lane == 0) alive = mbar_wait(&sm.tile_empty[tb], ((tcount >> 1) & 1) ^ 1, status, 1);
       alive = __shfl_sync(0xffffffffu, alive ? 1 : 0, 0) != 0;
       if (!alive) break;
+      if (ti < 0) {
+        if (lane == 0) {
+          sm.tile_id[tb] = -1;
+          mbar_arrive(&sm.tile_full[tb]);
+        }
+        break;
+      }
+      TileInfo t;
+      tile_info(ti, tiles, cu, t);
       // ---- the tile's union entries (built by fwd_union_kernel)
       const int* ul = ulist + (static_cast<size_t>(ti) * Hkv + g) * kFwdUnionStride;
       const int nU = min(__ldg(ul), kTpt * kTopK);
       for (int i = lane; i < nU; i += 32) sm.ublk[tb][i] = __ldg(ul + 4 + i);
-      if (lane == 0) sm.n_union[tb] = nU;
+      if (lane == 0) {
+        sm.n_union[tb] = nU;
+        sm.tile_id[tb] = ti;
+      }
       __syncwarp();
       if (lane == 0) {
+        pending = atomicAdd(tile_ctr + g, 1);   // next claim, in flight while K streams
         mbar_arrive_expect_tx(&sm.tile_full[tb], kTile);
         tma_load_3d(sm.q[tb], &tm_q, &sm.tile_full[tb], 0, g * kG, t.seq0 + t.p0);
         tma_load_3d(sm.q[tb] + kHalf, &tm_q, &sm.tile_full[tb], 64, g * kG, t.seq0 + t.p0);
@@ -253,12 +280,14 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       prefetch_tmap(&tm_v);
       uint32_t tcount = 0, vc = 0;
       bool alive = true;
-      for (int ti = blockIdx.x; alive && ti < total; ti += gridDim.x) {
-        TileInfo t;
-        if (!tile_info(ti, tiles, cu, t)) continue;
+      for (;;) {
         const int tb = tcount & 1;
         // the tile's union list is in place once its Q has landed
         if (!(alive = mbar_wait(&sm.tile_full[tb], (tcount >> 1) & 1, status, 15))) break;
+        const int ti = sm.tile_id[tb];
+        if (ti < 0) break;
+        TileInfo t;
+        tile_info(ti, tiles, cu, t);
         const int nU = sm.n_union[tb];
         for (int i = 0; alive && i < nU; ++i) {
           const int st = vc & 1;
@@ -269,6 +298,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           tma_load_3d(sm.v[st] + kHalf, &tm_v, &sm.v_full[st], 64, g, row);
           ++vc;
         }
+        if (!alive) break;
         mbar_arrive(&sm.tile_empty[tb]);   // done reading the tile's union list
         ++tcount;
       }
@@ -280,11 +310,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     if (elect_one()) {
       uint32_t tcount = 0, kc = 0, vc = 0, bc = 0;
       bool ok = true;
-      for (int ti = blockIdx.x; ok && ti < total; ti += gridDim.x) {
-        TileInfo t;
-        if (!tile_info(ti, tiles, cu, t)) continue;
+      for (;;) {
         const int tb = tcount & 1;
         if (!(ok = mbar_wait(&sm.tile_full[tb], (tcount >> 1) & 1, status, 4))) break;
+        if (sm.tile_id[tb] < 0) break;
         tc_fence_after();
         const int nU = sm.n_union[tb];
         const uint32_t qa = smem_u32(sm.q[tb]);
@@ -331,6 +360,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             ++vc;
           }
         }
+        if (!ok) break;
         umma_commit(&sm.tile_empty[tb]);   // Q of this tile is free once its S MMAs are done
         ++tcount;
       }
@@ -346,11 +376,14 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     const float sl2 = scale * kLog2e;
     uint32_t tcount = 0, bc = 0;
     bool ok = true;
-    for (int ti = blockIdx.x; ok && ti < total; ti += gridDim.x) {
-      TileInfo t;
-      if (!tile_info(ti, tiles, cu, t)) continue;
+    for (;;) {
       const int tb = tcount & 1;
-      if (!(ok = mbar_wait(&sm.tile_full[tb], (tcount >> 1) & 1, status, 9))) break;
+      if (!(ok = __all_sync(0xffffffffu, mbar_wait(&sm.tile_full[tb], (tcount >> 1) & 1, status, 9))))
+        break;
+      const int ti = sm.tile_id[tb];
+      if (ti < 0) break;
+      TileInfo t;
+      tile_info(ti, tiles, cu, t);
       const int nU = sm.n_union[tb];
       const bool row_valid = tl < t.ntok;
       const int pos = t.p0 + tl;
@@ -528,12 +561,12 @@ msa_status_t launch_sparse_fwd(const void* q, const void* k, const void* v, cons
     dim3 ugrid(static_cast<unsigned>(ublocks < cap ? ublocks : cap), Hkv);
     TraceScope trace_("fwd_union_kernel", stream);
     launch_pdl(fwd_union_kernel, ugrid, 256, 0, stream, sel, cu, plan.tiles, plan.num_tiles, Hkv,
-        fw.ulist, status_word());
+        fw.ulist, fw.tile_ctr, status_word());
   }
   {
     TraceScope trace_("sparse_fwd_kernel", stream);
     launch_pdl(sparse_fwd_kernel, grid, kFwdThreads, smem, stream,
-        tq, tk, tv, fw.ulist, cu, plan.tiles, plan.num_tiles, Hq, Hkv, scale,
+        tq, tk, tv, fw.ulist, fw.tile_ctr, cu, plan.tiles, plan.num_tiles, Hq, Hkv, scale,
         static_cast<__nv_bfloat16*>(o), lse, status_word());
   }
   return check_launch("sparse_fwd_kernel");
@@ -543,6 +576,7 @@ FwdWorkspace carve_fwd_workspace(WsCursor& ws, int T, int S, int Hkv) {
   FwdWorkspace w;
   w.plan = carve_plan(ws, T, S);
   w.ulist = ws.take<int>(static_cast<size_t>(w.plan.max_tiles) * kG * Hkv * kFwdUnionStride);
+  w.tile_ctr = ws.take<int>(Hkv);
   return w;
 }
 
