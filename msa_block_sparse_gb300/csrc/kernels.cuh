@@ -70,6 +70,7 @@ struct BwdWorkspace {
   float* dq_acc;       // [T, Hq, 128] fp32
   float* dk_acc;       // [T, Hkv, 128] fp32
   float* dv_acc;       // [T, Hkv, 128] fp32
+  int* item_ctr;       // [Hkv] next item to claim (cleared with the accumulators)
 };
 BwdWorkspace carve_bwd_workspace(WsCursor& ws, int T, int S, int Hq, int Hkv, int max_seqlen);
 int device_sm_count();

@@ -6,7 +6,8 @@
 // 256-position window of candidate query positions).  Items are listed window
 // by window, so the items running at any moment add into dQ rows of a few
 // windows only and the fp32 dQ accumulator lines stay in L2.  Persistent CTAs
-// (one per SM and KV head share) stride over the items.  Per item the CTA holds
+// (one per SM and KV head share) claim the items in that order from a counter,
+// so that a CTA that drew short items takes more.  Per item the CTA holds
 // K_b and V_b in shared memory and streams the window's query tokens that
 // selected b, in ascending order, in half-chunks of 4 tokens x G = 16 heads =
 // 64 columns.  A pre-pass (bwd_lists_kernel) lists, per item, those tokens
@@ -46,6 +47,11 @@ constexpr int kHalf = kTile / 2;
 constexpr int kHc = 64;                     // columns of a half-chunk: 4 tokens x 16 heads
 constexpr int kHcTok = 4;
 constexpr int kStages = 4;
+// Claimed item ids pass from the claiming producer to the other roles through a
+// ring of slots; each slot is read by the second loader, the MMA issuer and the
+// 8 compute warps before it is reused.
+constexpr int kItemSlots = 4;
+constexpr int kItemReaders = 1 + 1 + 8;
 constexpr int kTokBytes = 16 * kD * 2;      // Q (or dO) rows of one token: 4 KB
 constexpr int kStageBytes = 2 * kHcTok * kTokBytes;   // Q then dO of a half-chunk: 32 KB
 constexpr float kLog2e = 1.4426950408889634f;
@@ -71,6 +77,8 @@ struct BwdSmem {
   uint64_t ld_full[kStages], ld_empty[kStages];
   uint64_t s_full[2], dp_full[2], p_full[2], ds_full[2], dv_done[2], dq_full[2], dq_free[2];
   uint64_t acc_full, acc_free;
+  uint64_t item_full[kItemSlots], item_empty[kItemSlots];
+  int item_id[kItemSlots];              // claimed item of the slot; -1: none left
   uint32_t tmem_base;
 };
 static_assert(sizeof(BwdSmem) <= 232448, "backward shared memory above the 227 KB limit");
@@ -307,7 +315,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                       const float* __restrict__ lsd, const int4* __restrict__ items,
                       const int* __restrict__ num_items, int Hq, int Hkv, float scale,
                       float* __restrict__ dq_acc, float* __restrict__ dk_acc,
-                      float* __restrict__ dv_acc, uint32_t* status) {
+                      float* __restrict__ dv_acc, int* __restrict__ item_ctr,
+                      uint32_t* status) {
   pdl_enter();
   constexpr int G = 16;
   const int n_items = *num_items;
@@ -341,6 +350,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
     mbar_init(&sm.acc_full, 1);
     mbar_init(&sm.acc_free, 2 * kGroupThreads);
+    for (int i = 0; i < kItemSlots; ++i) {
+      mbar_init(&sm.item_full[i], 1);
+      mbar_init(&sm.item_empty[i], kItemReaders);
+    }
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -366,8 +379,35 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
     bool alive = true;
     uint32_t u = 0;
-    int itl = 0;
-    for (int it = blockIdx.x; alive && it < n_items; it += gridDim.x, ++itl) {
+    int pending = 0;
+    if (par == 0 && lane == 0) pending = atomicAdd(item_ctr + g, 1);
+    for (int itl = 0; alive; ++itl) {
+      // Items are claimed in list order, first come first served: warp 0 takes
+      // the next one from the KV head's counter and publishes its id (-1 once
+      // none are left) in slot itl % kItemSlots, where the other roles read it.
+      const int si = itl % kItemSlots;
+      const uint32_t sph = (itl / kItemSlots) & 1;
+      int it = -1;
+      if (lane == 0) {
+        if (par == 0) {
+          it = pending < n_items ? pending : -1;
+          alive = mbar_wait(&sm.item_empty[si], sph ^ 1, status, 23);
+          if (alive) {
+            sm.item_id[si] = it;
+            mbar_arrive(&sm.item_full[si]);
+            if (it >= 0) pending = atomicAdd(item_ctr + g, 1);   // next claim, in flight
+          }
+        } else {
+          alive = mbar_wait(&sm.item_full[si], sph, status, 24);
+          if (alive) {
+            it = sm.item_id[si];
+            mbar_arrive(&sm.item_empty[si]);
+          }
+        }
+      }
+      alive = __shfl_sync(0xffffffffu, alive ? 1 : 0, 0) != 0;
+      it = __shfl_sync(0xffffffffu, it, 0);
+      if (!alive || it < 0) break;
       const int4 item = items[it];
       const int s = item.x, b = item.y;
       const int seq0 = cu[s];
@@ -435,8 +475,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const uint32_t ka = smem_u32(sm.k), va = smem_u32(sm.v);
       uint32_t u0 = 0;
       bool ok = true;
-      int itl = 0, ii = 0;      // items, items with work
-      for (int it = blockIdx.x; ok && it < n_items; it += gridDim.x, ++itl) {
+      int ii = 0;      // items with work
+      for (int itl = 0;; ++itl) {
+        const int si = itl % kItemSlots;
+        if (!(ok = mbar_wait(&sm.item_full[si], (itl / kItemSlots) & 1, status, 38))) break;
+        const int it = sm.item_id[si];
+        mbar_arrive(&sm.item_empty[si]);
+        if (it < 0) break;
         const int nlist = list_len[static_cast<size_t>(it) * Hkv + g];
         const int nh = (nlist + kHcTok - 1) / kHcTok;
         if (!(ok = mbar_wait(&sm.kv_full, itl & 1, status, 31))) break;
@@ -527,7 +572,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     uint32_t u0 = 0;
     int ii = 0;
     bool ok = true;
-    for (int it = blockIdx.x; ok && it < n_items; it += gridDim.x) {
+    for (int itl = 0;; ++itl) {
+      const int si = itl % kItemSlots;
+      if (!(ok = __all_sync(0xffffffffu,
+                            mbar_wait(&sm.item_full[si], (itl / kItemSlots) & 1, status, 40))))
+        break;
+      const int it = sm.item_id[si];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.item_empty[si]);
+      if (it < 0) break;
       const int4 item = items[it];
       const int s = item.x, b = item.y;
       const int seq0 = cu[s];
@@ -709,10 +762,12 @@ BwdWorkspace carve_bwd_workspace(WsCursor& ws, int T, int S, int Hq, int Hkv, in
   w.lists = ws.take<int>(static_cast<size_t>(w.max_items) * Hkv * kBwdSegment);
   w.list_len = ws.take<int>(static_cast<size_t>(w.max_items) * Hkv);
   w.lsd = ws.take<float>(static_cast<size_t>(T) * Hq * 2);
-  // the three accumulators stay adjacent and in this order: one clear covers them
+  // the three accumulators and the item counters stay adjacent and in this
+  // order: one clear covers them
   w.dq_acc = ws.take<float>(static_cast<size_t>(T) * Hq * kD);
   w.dk_acc = ws.take<float>(static_cast<size_t>(T) * Hkv * kD);
   w.dv_acc = ws.take<float>(static_cast<size_t>(T) * Hkv * kD);
+  w.item_ctr = ws.take<int>(Hkv);
   return w;
 }
 
@@ -742,8 +797,9 @@ msa_status_t launch_sparse_bwd(const void* q, const void* k, const void* v, cons
 
   const size_t nq = static_cast<size_t>(T) * Hq * kD;
   const size_t nkv = static_cast<size_t>(T) * Hkv * kD;
-  // the three accumulators are carved back to back: one clear covers them
-  const size_t acc_bytes = reinterpret_cast<uint8_t*>(ws.dv_acc + nkv) -
+  // the three accumulators and the item counters are carved back to back: one
+  // clear covers them
+  const size_t acc_bytes = reinterpret_cast<uint8_t*>(ws.item_ctr + Hkv) -
                            reinterpret_cast<uint8_t*>(ws.dq_acc);
   if (cudaMemsetAsync(ws.dq_acc, 0, acc_bytes, stream) != cudaSuccess)
     return fail(MSA_ERR_CUDA, "workspace clear failed");
@@ -786,7 +842,7 @@ msa_status_t launch_sparse_bwd(const void* q, const void* k, const void* v, cons
     TraceScope trace_("sparse_bwd_kernel", stream);
     launch_pdl(sparse_bwd_kernel, grid, kBwdThreads, smem, stream,
         tq, tk, tv, tdo, ws.lists, ws.list_len, cu, ws.lsd, ws.items, ws.num_items, Hq, Hkv, scale,
-        ws.dq_acc, ws.dk_acc, ws.dv_acc, st);
+        ws.dq_acc, ws.dk_acc, ws.dv_acc, ws.item_ctr, st);
   }
   e = check_launch("sparse_bwd_kernel");
   if (e != MSA_OK) return e;
