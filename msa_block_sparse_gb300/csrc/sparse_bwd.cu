@@ -6,8 +6,9 @@
 // 256-position window of candidate query positions).  Items are listed window
 // by window, so the items running at any moment add into dQ rows of a few
 // windows only and the fp32 dQ accumulator lines stay in L2.  Persistent CTAs
-// (one per SM and KV head share) claim the items in that order from a counter,
-// so that a CTA that drew short items takes more.  Per item the CTA holds
+// (one per SM and KV head share) claim the items from a counter, so that a CTA
+// that drew short items takes more; the last fifth of the list is claimed
+// largest first (bwd_order_kernel) so that the CTAs finish together.  Per item the CTA holds
 // K_b and V_b in shared memory and streams the window's query tokens that
 // selected b, in ascending order, in half-chunks of 4 tokens x G = 16 heads =
 // 64 columns.  A pre-pass (bwd_lists_kernel) lists, per item, those tokens
@@ -220,6 +221,48 @@ __global__ void __launch_bounds__(kBwdSegment) bwd_lists_kernel(
   }
 }
 
+// ---------------------------------------------------------------- claim order
+
+// One CTA per KV head.  The first 4/5 of the items keep their window-major order
+// (concurrent items add into the dQ rows of a few windows); the rest follow by
+// half-chunk count, largest first, so that the last items claimed are short and
+// the CTAs finish together.  Order within equal counts is unspecified.
+constexpr int kMaxHalfChunks = kBwdSegment / 4;
+__global__ void __launch_bounds__(1024) bwd_order_kernel(const int* __restrict__ list_len,
+                                                         const int* __restrict__ num_items,
+                                                         int Hkv, int max_items,
+                                                         int* __restrict__ order) {
+  pdl_enter();
+  __shared__ int hist[kMaxHalfChunks + 1], start[kMaxHalfChunks + 1];
+  const int n = *num_items;
+  const int g = blockIdx.x;
+  const int k = n - n / 5;
+  int* ord = order + static_cast<size_t>(g) * max_items;
+  for (int i = threadIdx.x; i <= kMaxHalfChunks; i += blockDim.x) hist[i] = 0;
+  __syncthreads();
+  for (int i = threadIdx.x; i < n; i += blockDim.x) {
+    if (i < k) {
+      ord[i] = i;
+    } else {
+      const int nh = min((list_len[static_cast<size_t>(i) * Hkv + g] + 3) / 4, kMaxHalfChunks);
+      atomicAdd(&hist[nh], 1);
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int acc = k;
+    for (int c = kMaxHalfChunks; c >= 0; --c) {
+      start[c] = acc;
+      acc += hist[c];
+    }
+  }
+  __syncthreads();
+  for (int i = k + static_cast<int>(threadIdx.x); i < n; i += blockDim.x) {
+    const int nh = min((list_len[static_cast<size_t>(i) * Hkv + g] + 3) / 4, kMaxHalfChunks);
+    ord[atomicAdd(&start[nh], 1)] = i;
+  }
+}
+
 // ---------------------------------------------------------------- Delta
 
 // For query row (t, 16 g + j): lsd[32 (t Hkv + g) + j] = -lse log2 e and
@@ -311,7 +354,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                       const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v,
                       const __grid_constant__ CUtensorMap tm_do, const int* __restrict__ lists,
-                      const int* __restrict__ list_len, const int32_t* __restrict__ cu,
+                      const int* __restrict__ list_len, const int* __restrict__ order,
+                      int max_items, const int32_t* __restrict__ cu,
                       const float* __restrict__ lsd, const int4* __restrict__ items,
                       const int* __restrict__ num_items, int Hq, int Hkv, float scale,
                       float* __restrict__ dq_acc, float* __restrict__ dk_acc,
@@ -382,15 +426,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     int pending = 0;
     if (par == 0 && lane == 0) pending = atomicAdd(item_ctr + g, 1);
     for (int itl = 0; alive; ++itl) {
-      // Items are claimed in list order, first come first served: warp 0 takes
-      // the next one from the KV head's counter and publishes its id (-1 once
-      // none are left) in slot itl % kItemSlots, where the other roles read it.
+      // Items are claimed in the order bwd_order_kernel set, first come first
+      // served: warp 0 takes the next one from the KV head's counter and
+      // publishes its id (-1 once none are left) in slot itl % kItemSlots, where
+      // the other roles read it.
       const int si = itl % kItemSlots;
       const uint32_t sph = (itl / kItemSlots) & 1;
       int it = -1;
       if (lane == 0) {
         if (par == 0) {
-          it = pending < n_items ? pending : -1;
+          it = pending < n_items ? __ldg(order + static_cast<size_t>(g) * max_items + pending) : -1;
           alive = mbar_wait(&sm.item_empty[si], sph ^ 1, status, 23);
           if (alive) {
             sm.item_id[si] = it;
@@ -761,6 +806,7 @@ BwdWorkspace carve_bwd_workspace(WsCursor& ws, int T, int S, int Hq, int Hkv, in
   w.num_items = ws.take<int>(1);
   w.lists = ws.take<int>(static_cast<size_t>(w.max_items) * Hkv * kBwdSegment);
   w.list_len = ws.take<int>(static_cast<size_t>(w.max_items) * Hkv);
+  w.order = ws.take<int>(static_cast<size_t>(w.max_items) * Hkv);
   w.lsd = ws.take<float>(static_cast<size_t>(T) * Hq * 2);
   // the three accumulators and the item counters stay adjacent and in this
   // order: one clear covers them
@@ -826,7 +872,12 @@ msa_status_t launch_sparse_bwd(const void* q, const void* k, const void* v, cons
     launch_pdl(bwd_lists_kernel, lgrid, kBwdSegment, 0, stream, cu, sel, ws.items, ws.num_items, Hkv,
         ws.lists, ws.list_len);
   }
-  msa_status_t e = check_launch("bwd_delta/items/lists");
+  {
+    TraceScope trace_("bwd_order_kernel", stream);
+    launch_pdl(bwd_order_kernel, static_cast<unsigned>(Hkv), 1024, 0, stream, ws.list_len,
+        ws.num_items, Hkv, ws.max_items, ws.order);
+  }
+  msa_status_t e = check_launch("bwd_delta/items/lists/order");
   if (e != MSA_OK) return e;
 
   const size_t smem = sizeof(BwdSmem);
@@ -841,7 +892,7 @@ msa_status_t launch_sparse_bwd(const void* q, const void* k, const void* v, cons
   {
     TraceScope trace_("sparse_bwd_kernel", stream);
     launch_pdl(sparse_bwd_kernel, grid, kBwdThreads, smem, stream,
-        tq, tk, tv, tdo, ws.lists, ws.list_len, cu, ws.lsd, ws.items, ws.num_items, Hq, Hkv, scale,
+        tq, tk, tv, tdo, ws.lists, ws.list_len, ws.order, ws.max_items, cu, ws.lsd, ws.items, ws.num_items, Hq, Hkv, scale,
         ws.dq_acc, ws.dk_acc, ws.dv_acc, ws.item_ctr, st);
   }
   e = check_launch("sparse_bwd_kernel");
