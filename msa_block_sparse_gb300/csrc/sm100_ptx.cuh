@@ -181,6 +181,17 @@ __device__ __forceinline__ void tma_reduce_add_2d(const CUtensorMap* map, const 
       : "memory");
 }
 
+// Tiled copy of a shared-memory box to global memory (the tensor map's layout
+// and swizzle), tracked by the issuing thread's bulk async-group.
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, const void* src, int c0,
+                                             int c1, int c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::
+          "l"(map),
+      "r"(smem_u32(src)), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+
 __device__ __forceinline__ void bulk_commit_group() {
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }

@@ -8,20 +8,23 @@
 // selected blocks in ascending order; a row whose token did not select the
 // current block gets P = 0 for it.
 //
-// Persistent CTAs (one per SM) stride over the tiles:
-//   producers: warp 0 copies the next tile's block union (built beforehand by
-//            fwd_union_kernel, one warp per tile) into a double-buffered slot,
-//            loads its Q tile and streams K_b through a 2-stage TMA ring;
-//            warp 10 streams V_b through its own 2-stage ring, so neither
-//            ring's release holds up the other
-//   MMA (warp 1): S_i = Q K_b^T into one of two TMEM buffers; then
-//            O_h += P_h V_b[64h, 64h+64) for the two 64-key halves h, with P_h
-//            read from TMEM as the A operand
+// Persistent CTAs (one per SM) claim tiles from a counter:
+//   producers: warp 0 claims the next tile, copies its block union (built
+//            beforehand by fwd_union_kernel, one warp per tile) into a
+//            double-buffered slot, loads its Q tile and streams K_b through a
+//            2-stage TMA ring; warp 10 streams V_b through its own 2-stage
+//            ring, so neither ring's release holds up the other
+//   MMA (warps 1 and 11, one per 64-key half h): S_h = Q K_b[64h, 64h+64)^T
+//            into one of two TMEM buffers of the half; then
+//            O_h += P_h V_b[64h, 64h+64) with P_h read from TMEM as the A operand
 //   softmax (warps 2..9): warp = 32 rows x one 64-key half h.  Each half keeps
 //            its own running max (log2 domain, rescaled only when it grows by
 //            more than 2^8, so P < 256 fits bf16), row sum and O_h accumulator;
-//            P_h is packed to bf16 into the S buffer it came from.  The epilogue
-//            merges the halves: o = (O_0 2^(m_0-m) + O_1 2^(m_1-m)) / l.
+//            P_h is packed to bf16 into the S buffer it came from.  The
+//            epilogue merges the halves, o = (O_0 2^(m_0-m) + O_1 2^(m_1-m)) / l,
+//            stages a full tile in its (finished) Q buffer and writes it with
+//            one tensor store per half; the next tile's first PV waits until
+//            both halves have read O_0 and O_1.
 #include "kernels.cuh"
 
 namespace msa {
@@ -36,6 +39,7 @@ constexpr int kMmaWarp1 = 11;
 
 constexpr int kSoftmaxThreads = 256;
 constexpr int kHalfThreads = kSoftmaxThreads / 2;   // softmax threads of one key half
+constexpr int kFirstHalfWarp = 2;           // warps 2..5: key half 0, 6..9: key half 1
 constexpr int kG = 16;                      // query heads per KV head
 constexpr int kTpt = 8;                     // tokens per tile
 constexpr int kTile = 128 * 128 * 2;        // bytes of a 128 x 128 bf16 tile
@@ -47,6 +51,10 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleThreshold = 8.0f;   // log2 of the largest P before a rescale
 constexpr uint32_t kColO = 256;             // O_0 at 256, O_1 at 384; S buffers at 0, 128
 
+struct TileInfo {
+  int s, qb, seq0, len, p0, ntok;
+};
+
 struct FwdSmem {
   uint8_t q[2][kTile];
   uint8_t k[2][kTile];
@@ -54,11 +62,14 @@ struct FwdSmem {
   int ublk[2][kTpt * kTopK];                 // union entries (block << 8) | token mask
   int n_union[2];
   int tile_id[2];                           // tile of the slot; -1: no tiles left
+  TileInfo tinfo[2];                        // its decoded plan entry (read once, by warp 0)
   float2 ml[2][128];                        // per half: (max, sum) of each row, for the merge
   uint64_t tile_full[2], tile_empty[2];
   uint64_t k_full[2], k_empty[2], v_full[2], v_empty[2];
   // per key half and S buffer: a waiter is then never more than one phase behind
   uint64_t s_full[2][2], p_full[2][2], pv_done[2][2], ml_full;
+  uint64_t o_done[2];                       // a half's threads have read O and staged their rows
+  uint64_t o_free;                          // both halves have read O_0 and O_1 of the tile
   uint32_t tmem_base;
 };
 static_assert(sizeof(FwdSmem) <= 232448, "forward shared memory above the 227 KB limit");
@@ -79,9 +90,7 @@ __device__ __forceinline__ void umma_bf16_tmem_a(uint32_t d_tmem, uint32_t a_tme
       : "memory");
 }
 
-struct TileInfo {
-  int s, qb, seq0, len, p0, ntok;
-};
+
 
 // Global tile ti -> plan tile ti / 16 (a 128-token block), sub-tile ti % 16.
 __device__ __forceinline__ bool tile_info(int ti, const int2* tiles, const int32_t* cu,
@@ -166,7 +175,8 @@ __global__ void __launch_bounds__(256) fwd_union_kernel(const int32_t* __restric
 __global__ void __launch_bounds__(kFwdThreads, 1)
     sparse_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                       const __grid_constant__ CUtensorMap tm_k,
-                      const __grid_constant__ CUtensorMap tm_v, const int* __restrict__ ulist,
+                      const __grid_constant__ CUtensorMap tm_v,
+                      const __grid_constant__ CUtensorMap tm_o, const int* __restrict__ ulist,
                       int* __restrict__ tile_ctr, const int32_t* __restrict__ cu, const int2* __restrict__ tiles,
                       const int* __restrict__ num_tiles, int Hq, int Hkv, float scale,
                       __nv_bfloat16* __restrict__ o, float* __restrict__ lse, uint32_t* status) {
@@ -187,7 +197,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   if (tid == 0) {
     for (int i = 0; i < 2; ++i) {
       mbar_init(&sm.tile_full[i], 1);
-      mbar_init(&sm.tile_empty[i], 2 + kSoftmaxThreads + 1);
+      mbar_init(&sm.tile_empty[i], 2 + 2 + 1);
       mbar_init(&sm.k_full[i], 1);
       mbar_init(&sm.k_empty[i], 2);
       mbar_init(&sm.v_full[i], 1);
@@ -199,6 +209,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       }
     }
     mbar_init(&sm.ml_full, kSoftmaxThreads);
+    mbar_init(&sm.o_free, 2);
+    mbar_init(&sm.o_done[0], kHalfThreads);
+    mbar_init(&sm.o_done[1], kHalfThreads);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -252,6 +265,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       if (lane == 0) {
         sm.n_union[tb] = nU;
         sm.tile_id[tb] = ti;
+        sm.tinfo[tb] = t;
       }
       __syncwarp();
       if (lane == 0) {
@@ -284,10 +298,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         const int tb = tcount & 1;
         // the tile's union list is in place once its Q has landed
         if (!(alive = mbar_wait(&sm.tile_full[tb], (tcount >> 1) & 1, status, 15))) break;
-        const int ti = sm.tile_id[tb];
-        if (ti < 0) break;
-        TileInfo t;
-        tile_info(ti, tiles, cu, t);
+        if (sm.tile_id[tb] < 0) break;
+        const TileInfo t = sm.tinfo[tb];
         const int nU = sm.n_union[tb];
         for (int i = 0; alive && i < nU; ++i) {
           const int st = vc & 1;
@@ -345,6 +357,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             const int st = vc & 1;
             if (!(ok = mbar_wait(&sm.p_full[hh][j & 1], (j >> 1) & 1, status, 7))) break;
             if (!(ok = mbar_wait(&sm.v_full[st], (vc >> 1) & 1, status, 8))) break;
+            // the tile's first PV overwrites O_hh: the previous tile's epilogue
+            // (both halves) must have read it
+            if (i == 1 && tcount > 0 &&
+                !(ok = mbar_wait(&sm.o_free, (tcount - 1) & 1, status, 16)))
+              break;
             tc_fence_after();
             // V rows (keys) [64hh, 64hh + 64): four K-steps of 16 keys
             const uint32_t va = smem_u32(sm.v[st]) + hh * 64 * 128;
@@ -380,10 +397,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       const int tb = tcount & 1;
       if (!(ok = __all_sync(0xffffffffu, mbar_wait(&sm.tile_full[tb], (tcount >> 1) & 1, status, 9))))
         break;
-      const int ti = sm.tile_id[tb];
-      if (ti < 0) break;
-      TileInfo t;
-      tile_info(ti, tiles, cu, t);
+      if (sm.tile_id[tb] < 0) break;
+      const TileInfo t = sm.tinfo[tb];
       const int nU = sm.n_union[tb];
       const bool row_valid = tl < t.ntok;
       const int pos = t.p0 + tl;
@@ -474,7 +489,6 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         ++bc;
       }
       if (!ok) break;
-      mbar_arrive(&sm.tile_empty[tb]);
       // ---- epilogue: merge the two halves of every row
       // the PV of the tile's last block completes after all earlier ones
       if (!(ok = mbar_wait(&sm.pv_done[h][(bc - 1) & 1], ((bc - 1) >> 1) & 1, status, 13))) break;
@@ -491,6 +505,12 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       const float f0 = (h == 0) ? f_me : f_ot, f1 = (h == 0) ? f_ot : f_me;
       const float inv = (L > 0.f) ? 1.f / L : 0.f;
       const size_t orow_g = static_cast<size_t>(t.seq0 + pos) * Hq + g * kG + hd;
+      // A full tile is staged in its Q buffer (free: every MMA of the tile is
+      // done) in the 128B-swizzled layout of the tensor map and written by one
+      // tensor store per half; a partial tile (the end of a sequence) is
+      // written row by row so that no row of the next sequence is touched.
+      const bool full = t.ntok == kTpt;
+      uint8_t* stage = sm.q[tb] + h * kHalf;
       uint4* dst = reinterpret_cast<uint4*>(o + orow_g * kD + 64 * h);
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
@@ -498,22 +518,41 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         tmem_ld32(tmem + kColO + trow + 64 * h + 32 * c, a);
         tmem_ld32(tmem + kColO + 128 + trow + 64 * h + 32 * c, bq);
         tmem_ld_wait();
-        if (row_valid) {
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            float x[8];
+        for (int q = 0; q < 4; ++q) {
+          float x[8];
 #pragma unroll
-            for (int e = 0; e < 8; ++e)
-              x[e] = (__uint_as_float(a[8 * q + e]) * f0 + __uint_as_float(bq[8 * q + e]) * f1) * inv;
-            uint4 pk;
-            pk.x = pack_bf16x2(x[0], x[1]);
-            pk.y = pack_bf16x2(x[2], x[3]);
-            pk.z = pack_bf16x2(x[4], x[5]);
-            pk.w = pack_bf16x2(x[6], x[7]);
+          for (int e = 0; e < 8; ++e)
+            x[e] = (__uint_as_float(a[8 * q + e]) * f0 + __uint_as_float(bq[8 * q + e]) * f1) * inv;
+          uint4 pk;
+          pk.x = pack_bf16x2(x[0], x[1]);
+          pk.y = pack_bf16x2(x[2], x[3]);
+          pk.z = pack_bf16x2(x[4], x[5]);
+          pk.w = pack_bf16x2(x[6], x[7]);
+          if (full)
+            *reinterpret_cast<uint4*>(stage + sw128_offset(r, 4 * c + q)) = pk;
+          else if (row_valid)
             dst[4 * c + q] = pk;
-          }
         }
       }
+      tc_fence_before();
+      if (full) fence_proxy_async_smem();      // staged rows -> the tensor store's reads
+      mbar_arrive(&sm.o_done[h]);
+      if (subp == kFirstHalfWarp % 4 && lane == 0) {
+        // one thread per half: once all its rows are read and staged, release
+        // O, store the staged half and hand the Q buffer back to the producer
+        ok = mbar_wait(&sm.o_done[h], tcount & 1, status, 17);
+        if (ok) {
+          mbar_arrive(&sm.o_free);
+          if (full) {
+            tma_store_3d(&tm_o, stage, 64 * h, g * kG, t.seq0 + t.p0);
+            bulk_commit_group();
+            bulk_wait_read_all();             // the Q buffer may be reloaded after this
+          }
+          mbar_arrive(&sm.tile_empty[tb]);
+        }
+      }
+      if (!(ok = __all_sync(0xffffffffu, ok))) break;
       if (h == 0 && row_valid) lse[orow_g] = (M + __log2f(L)) * 0.6931471805599453f;
       tc_fence_before();
       ++tcount;
@@ -534,16 +573,17 @@ msa_status_t launch_sparse_fwd(const void* q, const void* k, const void* v, cons
   (void)max_seqlen;
   if (Hq / Hkv != kG)
     return fail(MSA_ERR_UNSUPPORTED, "forward supports Hq/Hkv = 16 (got %d)", Hq / Hkv);
-  CUtensorMap tq, tk, tv;
+  CUtensorMap tq, tk, tv, to;
   const uint64_t dq[3] = {static_cast<uint64_t>(kD), static_cast<uint64_t>(Hq),
                           static_cast<uint64_t>(T)};
   const uint64_t dkv[3] = {static_cast<uint64_t>(kD), static_cast<uint64_t>(Hkv),
                            static_cast<uint64_t>(T)};
   const uint32_t bq[3] = {64, static_cast<uint32_t>(kG), static_cast<uint32_t>(kTpt)};
   const uint32_t bkv[3] = {64, 1, 128};
+  // o has q's layout: the same box stores one half of a tile's output
   if (!make_tmap_bf16(&tq, q, 3, dq, bq) || !make_tmap_bf16(&tk, k, 3, dkv, bkv) ||
-      !make_tmap_bf16(&tv, v, 3, dkv, bkv))
-    return fail(MSA_ERR_CUDA, "cuTensorMapEncodeTiled failed for q/k/v");
+      !make_tmap_bf16(&tv, v, 3, dkv, bkv) || !make_tmap_bf16(&to, o, 3, dq, bq))
+    return fail(MSA_ERR_CUDA, "cuTensorMapEncodeTiled failed for q/k/v/o");
   const size_t smem = sizeof(FwdSmem);
   static bool attr_set = false;
   if (!attr_set) {
@@ -566,7 +606,7 @@ msa_status_t launch_sparse_fwd(const void* q, const void* k, const void* v, cons
   {
     TraceScope trace_("sparse_fwd_kernel", stream);
     launch_pdl(sparse_fwd_kernel, grid, kFwdThreads, smem, stream,
-        tq, tk, tv, fw.ulist, fw.tile_ctr, cu, plan.tiles, plan.num_tiles, Hq, Hkv, scale,
+        tq, tk, tv, to, fw.ulist, fw.tile_ctr, cu, plan.tiles, plan.num_tiles, Hq, Hkv, scale,
         static_cast<__nv_bfloat16*>(o), lse, status_word());
   }
   return check_launch("sparse_fwd_kernel");
