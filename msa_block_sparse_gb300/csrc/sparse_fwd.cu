@@ -2,11 +2,12 @@
 // Introduction": each query attends to its 16 selected 128-token blocks, own
 // block included, causally; "#4581", "Kernel tuning": QSA block-sparse kernel).
 //
-// Tile = 128 rows = 8 consecutive tokens x the 16 query heads of one KV head, so
-// a single K/V block feeds every row.  The tile's tokens lie in one 128-token
-// block and share their own block.  The tile walks the union of its tokens'
-// selected blocks in ascending order; a row whose token did not select the
-// current block gets P = 0 for it.
+// Tile = 128 rows = 8 tokens x the 16 query heads of one KV head, so a single
+// K/V block feeds every row.  The tile's tokens lie in one 128-token query
+// block (they share their own block) and are grouped there by selection
+// similarity (fwd_union_kernel), so that the union of their selected blocks,
+// which the tile walks in ascending order, stays small; a row whose token did
+// not select the current block gets P = 0 for it.
 //
 // Persistent CTAs (one per SM) claim tiles from a counter:
 //   producers: warp 0 claims the next tile, copies its block union (built
@@ -22,9 +23,9 @@
 //            more than 2^8, so P < 256 fits bf16), row sum and O_h accumulator;
 //            P_h is packed to bf16 into the S buffer it came from.  The
 //            epilogue merges the halves, o = (O_0 2^(m_0-m) + O_1 2^(m_1-m)) / l,
-//            stages a full tile in its (finished) Q buffer and writes it with
-//            one tensor store per half; the next tile's first PV waits until
-//            both halves have read O_0 and O_1.
+//            stages the tile in its (finished) Q buffer and writes it with one
+//            tensor store per token and half; the next tile's first PV waits
+//            until both halves have read O_0 and O_1.
 #include "kernels.cuh"
 
 namespace msa {
@@ -44,7 +45,7 @@ constexpr int kG = 16;                      // query heads per KV head
 constexpr int kTpt = 8;                     // tokens per tile
 constexpr int kTile = 128 * 128 * 2;        // bytes of a 128 x 128 bf16 tile
 constexpr int kHalf = kTile / 2;            // one 64-column half
-constexpr int kMaskWords = kMaxSeqlen / kBlock / 32;
+constexpr int kTokRows = kG * 128;          // one token's 16 rows of a 64-column half
 constexpr uint32_t kIdescS = idesc_bf16(128, 64, false, false);    // S_h: 64 keys of a half
 constexpr uint32_t kIdescPV = idesc_bf16(128, 128, false, true);   // O_h += P_h V_h
 constexpr float kLog2e = 1.4426950408889634f;
@@ -52,7 +53,8 @@ constexpr float kRescaleThreshold = 8.0f;   // log2 of the largest P before a re
 constexpr uint32_t kColO = 256;             // O_0 at 256, O_1 at 384; S buffers at 0, 128
 
 struct TileInfo {
-  int s, qb, seq0, len, p0, ntok;
+  int s, qb, seq0, len, p0, ntok;   // p0: first position of the 128-token query block
+  uint32_t offs[2];                 // byte i: offset in the block of the tile's i-th token
 };
 
 struct FwdSmem {
@@ -92,7 +94,9 @@ __device__ __forceinline__ void umma_bf16_tmem_a(uint32_t d_tmem, uint32_t a_tme
 
 
 
-// Global tile ti -> plan tile ti / 16 (a 128-token block), sub-tile ti % 16.
+// Global tile ti -> plan tile ti / 16 (a 128-token query block), sub-tile
+// (token group) ti % 16 of up to 8 of its tokens; the members are chosen by
+// fwd_union_kernel and listed in the tile's union header.
 __device__ __forceinline__ bool tile_info(int ti, const int2* tiles, const int32_t* cu,
                                           TileInfo& t) {
   const int2 pt = tiles[ti >> 4];
@@ -100,75 +104,212 @@ __device__ __forceinline__ bool tile_info(int ti, const int2* tiles, const int32
   t.qb = pt.y;
   t.seq0 = cu[t.s];
   t.len = cu[t.s + 1] - t.seq0;
-  t.p0 = t.qb * kBlock + (ti & 15) * kTpt;
-  t.ntok = min(kTpt, t.len - t.p0);
-  return t.p0 < t.len;
+  t.p0 = t.qb * kBlock;
+  const int first = (ti & 15) * kTpt;
+  t.ntok = min(kTpt, t.len - t.p0 - first);
+  t.offs[0] = t.offs[1] = 0;
+  return t.p0 + first < t.len;
+}
+
+__device__ __forceinline__ int member_offset(const TileInfo& t, int i) {
+  const uint32_t w = (i < 4) ? t.offs[0] : t.offs[1];
+  return static_cast<int>((w >> (8 * (i & 3))) & 0xFFu);
 }
 
 }  // namespace
 
-// One warp per (tile, KV head), grid-striding: the union of the 8 tokens'
-// selected blocks in ascending order, each entry (block << 8) | token mask.
-__global__ void __launch_bounds__(256) fwd_union_kernel(const int32_t* __restrict__ sel,
-                                                        const int32_t* __restrict__ cu,
-                                                        const int2* __restrict__ tiles,
-                                                        const int* __restrict__ num_tiles,
-                                                        int Hkv, int* __restrict__ ulist,
-                                                        int* __restrict__ tile_ctr,
-                                                        uint32_t* status) {
+namespace {
+
+// Token masks held in registers by the grouping: blocks below 32 x kGroupWords
+// (query blocks of sequences up to 16,384 tokens); longer ones group
+// consecutive tokens.
+constexpr int kGroupWords = 4;
+
+// Appends the union list of one token group: the blocks below the own block
+// that any member selected (ascending, from the members' masks mm), each
+// (block << 8) | member mask, then the own block (selected by every member).
+__device__ __forceinline__ void write_union(int* out, const uint32_t (&mm)[kTpt][kGroupWords],
+                                            int nm, int words, int qb, int lane) {
+  int n = 0;
+#pragma unroll
+  for (int w = 0; w < kGroupWords; ++w) {
+    if (w >= words) break;
+    uint32_t tm = 0;
+#pragma unroll
+    for (int i = 0; i < kTpt; ++i) tm |= ((mm[i][w] >> lane) & 1u) << i;
+    const uint32_t bal = __ballot_sync(0xffffffffu, tm != 0u);
+    if (tm) out[4 + n + __popc(bal & ((1u << lane) - 1u))] = ((32 * w + lane) << 8) | tm;
+    n += __popc(bal);
+  }
+  if (lane == 0) {
+    out[4 + n] = (qb << 8) | ((1 << nm) - 1);
+    out[0] = n + 1;
+  }
+}
+
+}  // namespace
+
+// One CTA of two warps per (128-token query block, KV head), grid-striding;
+// warp w groups the block's tokens [64 w, 64 w + 64) into the tiles (sub-tiles
+// 8 w .. 8 w + 7) of up to 8 tokens (the tile's MMA rows are 8 tokens x 16
+// heads) so that each tile's union of selected blocks - what its MMAs walk -
+// stays small: a group starts from the lowest ungrouped token and repeatedly
+// takes the token that adds the fewest blocks to the group's union (ties: the
+// lower token).  Per tile the header holds the member offsets and count, then
+// the union in ascending order, each entry (block << 8) | member mask.
+constexpr int kUnionThreads = 64;
+constexpr int kHalfTokens = kBlock / 2;
+__global__ void __launch_bounds__(kUnionThreads) fwd_union_kernel(const int32_t* __restrict__ sel,
+                                                                  const int32_t* __restrict__ cu,
+                                                                  const int2* __restrict__ tiles,
+                                                                  const int* __restrict__ num_tiles,
+                                                                  int Hkv, int* __restrict__ ulist,
+                                                                  int* __restrict__ tile_ctr,
+                                                                  uint32_t* status) {
   pdl_enter();
-  __shared__ uint32_t words_s[8][kMaskWords];
-  const int total = *num_tiles * kG;
+  __shared__ uint4 tok_mask[2][kHalfTokens];   // per warp: its tokens' masks (kGroupWords = 4)
+  static_assert(kGroupWords == 4, "one uint4 per token mask");
+  const int nblk = *num_tiles;
   const int g = blockIdx.y;
   if (blockIdx.x == 0 && threadIdx.x == 0) tile_ctr[g] = 0;   // the forward claims from 0
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int ti = blockIdx.x * 8 + warp; ti < total; ti += gridDim.x * 8) {
-    int* out = ulist + (static_cast<size_t>(ti) * Hkv + g) * kFwdUnionStride;
-    TileInfo t;
-    if (!tile_info(ti, tiles, cu, t)) {
-      if (lane == 0) out[0] = 0;
-      continue;
-    }
-    int ids[4];
+  for (int pb = blockIdx.x; pb < nblk; pb += gridDim.x) {
+    const int2 pt = tiles[pb];
+    const int qb = pt.y;
+    const int seq0 = cu[pt.x];
+    const int n = min(kBlock, cu[pt.x + 1] - seq0 - qb * kBlock);   // tokens of the block
+    const int t0 = kHalfTokens * warp;                              // this warp's first token
+    const int nw = max(0, min(kHalfTokens, n - t0));                 // and its token count
+    const int ngrp = (nw + kTpt - 1) / kTpt;
+    auto tile_out = [&](int grp) {
+      return ulist + (static_cast<size_t>(pb * kG + 8 * warp + grp) * Hkv + g) * kFwdUnionStride;
+    };
+    if (lane >= ngrp && lane < 8) tile_out(lane)[0] = 0;
+    const bool fits = qb < 32 * kGroupWords;
+    const int words = fits ? (qb + 31) / 32 : 0;
+    // ---- the tokens' masks of selected earlier blocks (own block left out);
+    // all loads first, then the bits
+    int4 ids[2][4];
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const int idx = lane * 4 + e;             // lanes 4i .. 4i+3 hold token i's 16 ids
-      const int tl = idx >> 4;
-      int b = -1;
-      if (tl < t.ntok) {
-        b = __ldg(sel + (static_cast<size_t>(t.seq0 + t.p0 + tl) * Hkv + g) * kTopK + (idx & 15));
-        if (b > t.qb) {
-          atomicOr(status, kStatusBounds);
-          b = -1;
+    for (int k = 0; k < 2; ++k) {
+      const int tok = t0 + lane + 32 * k;
+      const int4* row = reinterpret_cast<const int4*>(
+          sel + (static_cast<size_t>(seq0 + qb * kBlock + tok) * Hkv + g) * kTopK);
+#pragma unroll
+      for (int c = 0; c < 4; ++c) ids[k][c] = tok < n ? __ldg(row + c) : make_int4(-1, -1, -1, -1);
+    }
+    uint32_t m[2][kGroupWords];
+    uint32_t left = 0;                     // bit k: token t0 + lane + 32 k not grouped yet
+    bool bad = false;
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+#pragma unroll
+      for (int w = 0; w < kGroupWords; ++w) m[k][w] = 0;
+      if (t0 + lane + 32 * k < n) left |= 1u << k;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const int v4[4] = {ids[k][c].x, ids[k][c].y, ids[k][c].z, ids[k][c].w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int b = v4[e];
+          bad |= b > qb;
+          const bool keep = fits && b >= 0 && b < qb;
+          const uint32_t bit = keep ? (1u << (b & 31)) : 0u;
+#pragma unroll
+          for (int w = 0; w < kGroupWords; ++w) m[k][w] |= ((b >> 5) == w) ? bit : 0u;
         }
       }
-      ids[e] = b;
+      tok_mask[warp][lane + 32 * k] = make_uint4(m[k][0], m[k][1], m[k][2], m[k][3]);
     }
-    const int nb_seq = (t.len + kBlock - 1) / kBlock;
-    const int words = min((nb_seq + 31) >> 5, kMaskWords);
-    if (lane < words) words_s[warp][lane] = 0;
+    if (bad) atomicOr(status, kStatusBounds);
     __syncwarp();
+    if (!fits) {
+      // ---- long sequence: consecutive tokens per tile, union built from sel
+      for (int grp = 0; grp < ngrp; ++grp) {
+        int* out = tile_out(grp);
+        const int first = t0 + kTpt * grp;
+        const int nm = min(kTpt, nw - kTpt * grp);
+        const int nwords = (qb + 31) / 32;
+        int cnt = 0;
+        for (int w = 0; w < nwords; ++w) {
+          // lane l: block 32 w + l; member i selected it?
+          uint32_t tm = 0;
+          for (int i = 0; i < nm; ++i) {
+            const int4* row = reinterpret_cast<const int4*>(
+                sel + (static_cast<size_t>(seq0 + qb * kBlock + first + i) * Hkv + g) * kTopK);
+            bool hit = false;
 #pragma unroll
-    for (int e = 0; e < 4; ++e)
-      if (ids[e] >= 0) atomicOr(&words_s[warp][ids[e] >> 5], 1u << (ids[e] & 31));
-    __syncwarp();
-    int n = 0;
-    for (int w = 0; w < words; ++w) {
-      uint32_t u = words_s[warp][w];
-      while (u) {
-        const int b = w * 32 + __ffs(u) - 1;
-        u &= u - 1;
-        const bool mine = (ids[0] == b) | (ids[1] == b) | (ids[2] == b) | (ids[3] == b);
-        const uint32_t bal = __ballot_sync(0xffffffffu, mine);
-        uint32_t tm = 0;
-#pragma unroll
-        for (int i = 0; i < kTpt; ++i) tm |= ((bal >> (4 * i)) & 0xFu) ? (1u << i) : 0u;
-        if (lane == 0 && n < kTpt * kTopK) out[4 + n] = (b << 8) | static_cast<int>(tm);
-        ++n;
+            for (int c = 0; c < 4; ++c) {
+              const int4 v = __ldg(row + c);
+              hit |= (v.x == 32 * w + lane) | (v.y == 32 * w + lane) | (v.z == 32 * w + lane) |
+                     (v.w == 32 * w + lane);
+            }
+            tm |= hit && (32 * w + lane < qb) ? (1u << i) : 0u;
+          }
+          const uint32_t bal = __ballot_sync(0xffffffffu, tm != 0u);
+          if (tm) out[4 + cnt + __popc(bal & ((1u << lane) - 1u))] = ((32 * w + lane) << 8) | tm;
+          cnt += __popc(bal);
+        }
+        if (lane == 0) {
+          out[1] = 0x03020100 + 0x01010101 * first;
+          out[2] = 0x07060504 + 0x01010101 * first;
+          out[3] = nm;
+          out[4 + cnt] = (qb << 8) | ((1 << nm) - 1);
+          out[0] = cnt + 1;
+        }
       }
+      continue;
     }
-    if (lane == 0) out[0] = min(n, kTpt * kTopK);
-    __syncwarp();
+    // ---- greedy grouping
+    for (int grp = 0; grp < ngrp; ++grp) {
+      const int nm = min(kTpt, nw - kTpt * grp);
+      uint32_t u[kGroupWords];
+      uint32_t mm[kTpt][kGroupWords];
+      uint32_t offs0 = 0, offs1 = 0;
+#pragma unroll
+      for (int j = 0; j < kTpt; ++j) {
+        int tok = 0;                       // index among the warp's tokens
+        if (j < nm) {
+          uint32_t key = 0xFFFFFFFFu;
+          if (j == 0) {
+            // seed: the lowest ungrouped token
+            if (left) key = static_cast<uint32_t>(lane + 32 * (__ffs(left) - 1));
+          } else {
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+              if (left & (1u << k)) {
+                int cost = 0;
+#pragma unroll
+                for (int w = 0; w < kGroupWords; ++w) cost += __popc(m[k][w] & ~u[w]);
+                key = min(key, (static_cast<uint32_t>(cost) << 8) | static_cast<uint32_t>(lane + 32 * k));
+              }
+            }
+          }
+          tok = static_cast<int>(__reduce_min_sync(0xffffffffu, key) & 0xFFu);
+          if ((tok & 31) == lane) left &= ~(1u << (tok >> 5));
+          const uint4 tw = tok_mask[warp][tok];   // broadcast read
+          mm[j][0] = tw.x;
+          mm[j][1] = tw.y;
+          mm[j][2] = tw.z;
+          mm[j][3] = tw.w;
+#pragma unroll
+          for (int w = 0; w < kGroupWords; ++w) u[w] = (j == 0) ? mm[j][w] : (u[w] | mm[j][w]);
+        } else {
+#pragma unroll
+          for (int w = 0; w < kGroupWords; ++w) mm[j][w] = 0;
+        }
+        const uint32_t off = static_cast<uint32_t>(t0 + tok);   // offset in the query block
+        if (j < 4) offs0 |= off << (8 * j);
+        else offs1 |= off << (8 * (j - 4));
+      }
+      int* out = tile_out(grp);
+      if (lane == 0) {
+        out[1] = static_cast<int>(offs0);
+        out[2] = static_cast<int>(offs1);
+        out[3] = nm;
+      }
+      write_union(out, mm, nm, words, qb, lane);
+    }
   }
 }
 
@@ -261,18 +402,25 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       // ---- the tile's union entries (built by fwd_union_kernel)
       const int* ul = ulist + (static_cast<size_t>(ti) * Hkv + g) * kFwdUnionStride;
       const int nU = min(__ldg(ul), kTpt * kTopK);
+      t.offs[0] = static_cast<uint32_t>(__ldg(ul + 1));
+      t.offs[1] = static_cast<uint32_t>(__ldg(ul + 2));
       for (int i = lane; i < nU; i += 32) sm.ublk[tb][i] = __ldg(ul + 4 + i);
       if (lane == 0) {
         sm.n_union[tb] = nU;
         sm.tile_id[tb] = ti;
         sm.tinfo[tb] = t;
+        pending = atomicAdd(tile_ctr + g, 1);   // next claim, in flight while K streams
+        mbar_arrive_expect_tx(&sm.tile_full[tb], t.ntok * 2 * kTokRows);
+      }
+      __syncwarp();
+      // Q rows of the tile's tokens (16 heads each), one copy per token and D half
+      if (lane < 2 * t.ntok) {
+        const int i = lane >> 1, hf = lane & 1;
+        tma_load_3d(sm.q[tb] + hf * kHalf + i * kTokRows, &tm_q, &sm.tile_full[tb], 64 * hf,
+                    g * kG, t.seq0 + t.p0 + member_offset(t, i));
       }
       __syncwarp();
       if (lane == 0) {
-        pending = atomicAdd(tile_ctr + g, 1);   // next claim, in flight while K streams
-        mbar_arrive_expect_tx(&sm.tile_full[tb], kTile);
-        tma_load_3d(sm.q[tb], &tm_q, &sm.tile_full[tb], 0, g * kG, t.seq0 + t.p0);
-        tma_load_3d(sm.q[tb] + kHalf, &tm_q, &sm.tile_full[tb], 64, g * kG, t.seq0 + t.p0);
         // ---- K tiles through their 2-stage ring (V has its own warp, so a V
         // slot that frees late does not hold up the next K)
         for (int i = 0; alive && i < nU; ++i) {
@@ -401,7 +549,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       const TileInfo t = sm.tinfo[tb];
       const int nU = sm.n_union[tb];
       const bool row_valid = tl < t.ntok;
-      const int pos = t.p0 + tl;
+      const int pos = t.p0 + (row_valid ? member_offset(t, tl) : 0);
       float m = -INFINITY, l = 0.f;
       for (int i = 0; i < nU; ++i) {
         const int ent = sm.ublk[tb][i];
@@ -505,13 +653,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       const float f0 = (h == 0) ? f_me : f_ot, f1 = (h == 0) ? f_ot : f_me;
       const float inv = (L > 0.f) ? 1.f / L : 0.f;
       const size_t orow_g = static_cast<size_t>(t.seq0 + pos) * Hq + g * kG + hd;
-      // A full tile is staged in its Q buffer (free: every MMA of the tile is
-      // done) in the 128B-swizzled layout of the tensor map and written by one
-      // tensor store per half; a partial tile (the end of a sequence) is
-      // written row by row so that no row of the next sequence is touched.
-      const bool full = t.ntok == kTpt;
+      // The tile's normalised O is staged in its Q buffer (free: every MMA of
+      // the tile is done) in the 128B-swizzled layout of the tensor map and
+      // written by one tensor store per token and half.
       uint8_t* stage = sm.q[tb] + h * kHalf;
-      uint4* dst = reinterpret_cast<uint4*>(o + orow_g * kD + 64 * h);
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
         uint32_t a[32], bq[32];
@@ -529,28 +674,30 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           pk.y = pack_bf16x2(x[2], x[3]);
           pk.z = pack_bf16x2(x[4], x[5]);
           pk.w = pack_bf16x2(x[6], x[7]);
-          if (full)
-            *reinterpret_cast<uint4*>(stage + sw128_offset(r, 4 * c + q)) = pk;
-          else if (row_valid)
-            dst[4 * c + q] = pk;
+          *reinterpret_cast<uint4*>(stage + sw128_offset(r, 4 * c + q)) = pk;
         }
       }
       tc_fence_before();
-      if (full) fence_proxy_async_smem();      // staged rows -> the tensor store's reads
+      fence_proxy_async_smem();                // staged rows -> the tensor stores' reads
       mbar_arrive(&sm.o_done[h]);
-      if (subp == kFirstHalfWarp % 4 && lane == 0) {
-        // one thread per half: once all its rows are read and staged, release
-        // O, store the staged half and hand the Q buffer back to the producer
-        ok = mbar_wait(&sm.o_done[h], tcount & 1, status, 17);
-        if (ok) {
-          mbar_arrive(&sm.o_free);
-          if (full) {
-            tma_store_3d(&tm_o, stage, 64 * h, g * kG, t.seq0 + t.p0);
+      if (subp == kFirstHalfWarp % 4) {
+        // one warp per half: once all the half's rows are read and staged,
+        // release O, store each token's rows and hand the Q buffer back
+        bool okw = true;
+        if (lane == 0) okw = mbar_wait(&sm.o_done[h], tcount & 1, status, 17);
+        okw = __shfl_sync(0xffffffffu, okw ? 1 : 0, 0) != 0;
+        if (okw) {
+          if (lane == 0) mbar_arrive(&sm.o_free);
+          if (lane < t.ntok) {
+            tma_store_3d(&tm_o, stage + lane * kTokRows, 64 * h, g * kG,
+                         t.seq0 + t.p0 + member_offset(t, lane));
             bulk_commit_group();
             bulk_wait_read_all();             // the Q buffer may be reloaded after this
           }
-          mbar_arrive(&sm.tile_empty[tb]);
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sm.tile_empty[tb]);
         }
+        ok = okw;
       }
       if (!(ok = __all_sync(0xffffffffu, ok))) break;
       if (h == 0 && row_valid) lse[orow_g] = (M + __log2f(L)) * 0.6931471805599453f;
@@ -578,9 +725,9 @@ msa_status_t launch_sparse_fwd(const void* q, const void* k, const void* v, cons
                           static_cast<uint64_t>(T)};
   const uint64_t dkv[3] = {static_cast<uint64_t>(kD), static_cast<uint64_t>(Hkv),
                            static_cast<uint64_t>(T)};
-  const uint32_t bq[3] = {64, static_cast<uint32_t>(kG), static_cast<uint32_t>(kTpt)};
+  const uint32_t bq[3] = {64, static_cast<uint32_t>(kG), 1};   // one token's 16 heads
   const uint32_t bkv[3] = {64, 1, 128};
-  // o has q's layout: the same box stores one half of a tile's output
+  // o has q's layout: the same box stores one token's half rows
   if (!make_tmap_bf16(&tq, q, 3, dq, bq) || !make_tmap_bf16(&tk, k, 3, dkv, bkv) ||
       !make_tmap_bf16(&tv, v, 3, dkv, bkv) || !make_tmap_bf16(&to, o, 3, dq, bq))
     return fail(MSA_ERR_CUDA, "cuTensorMapEncodeTiled failed for q/k/v/o");
@@ -595,12 +742,12 @@ msa_status_t launch_sparse_fwd(const void* q, const void* k, const void* v, cons
   const int max_ctas = plan.max_tiles * kG;
   dim3 grid(static_cast<unsigned>(per_head < max_ctas ? per_head : max_ctas), Hkv);
   {
-    const int max_tiles16 = plan.max_tiles * kG;
-    const int ublocks = (max_tiles16 + 7) / 8;
-    const int cap = 4 * device_sm_count();
+    // one CTA of two warps per (128-token query block, KV head)
+    const int ublocks = plan.max_tiles;
+    const int cap = 8 * device_sm_count();
     dim3 ugrid(static_cast<unsigned>(ublocks < cap ? ublocks : cap), Hkv);
     TraceScope trace_("fwd_union_kernel", stream);
-    launch_pdl(fwd_union_kernel, ugrid, 256, 0, stream, sel, cu, plan.tiles, plan.num_tiles, Hkv,
+    launch_pdl(fwd_union_kernel, ugrid, kUnionThreads, 0, stream, sel, cu, plan.tiles, plan.num_tiles, Hkv,
         fw.ulist, fw.tile_ctr, status_word());
   }
   {
