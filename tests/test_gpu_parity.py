@@ -254,6 +254,29 @@ def test_sparse_fwd_full_size(m, idx):
     assert_close(lse[toks].cpu().numpy().astype(np.float64), olse, 1e-3, 1e-4, f"cfg{idx} lse")
 
 
+LONG = W.PrefillShape("long-17000-16q1kv", (17000, 700), 16, 1, 1)
+
+
+def test_sparse_fwd_long_sequence(m):
+    """A sequence longer than 16,384 tokens: the query blocks past that point
+    form their 8-token tiles from consecutive tokens (their selection masks do
+    not fit the grouping's registers), the earlier ones by selection
+    similarity; rows on both sides compare with the oracle."""
+    shape = LONG
+    cpu, gpu = inputs("long", shape)
+    osel, _ = oracle_selection("long", shape, cpu)
+    sel = torch.from_numpy(osel.astype(np.int32)).to(DEV)
+    o, lse = m.msa_sparse_attn_fwd(gpu["q"], gpu["k"], gpu["v"], sel, gpu["cu_seqlens"],
+                                   shape.max_seqlen)
+    m.msa_check_status()
+    toks = sorted(set(sample_tokens(shape, n_random=64, seed=21))
+                  | {16383, 16384, 16385, 16391, 16392, 16511, 16512, 16999})
+    oo, olse = O.sparse_attn_fwd(f64(cpu["q"]), f64(cpu["k"]), f64(cpu["v"]), osel,
+                                 cpu["cu_seqlens"].numpy(), SCALE, tokens=toks)
+    assert_close(f64(o[toks]), oo, 2e-2, 1e-2, "long o")
+    assert_close(lse[toks].cpu().numpy().astype(np.float64), olse, 1e-3, 1e-4, "long lse")
+
+
 # ------------------------------------------------------------------ backward
 
 BWD_SMALL = {
