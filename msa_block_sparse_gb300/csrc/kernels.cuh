@@ -111,6 +111,7 @@ struct QsaFwdWorkspace {
   int W;
   int* ulist;          // [max_tiles, Hkv, ustride]: count, then key tiles
   int ustride;
+  int* tile_ctr;       // [Hkv] next query tile to claim (zeroed by qsa_union_kernel)
 };
 struct QsaBwdWorkspace {
   QsaFwdWorkspace map;
@@ -121,6 +122,7 @@ struct QsaBwdWorkspace {
   int* klist;          // [max_items, Hkv, 129]: count, then query tiles
   int* order;          // [Hkv, max_items] non-empty items, most query tiles first
   int* num_busy;       // [Hkv] non-empty items
+  int* item_ctr;       // [Hkv] next item to claim (zeroed by qsa_order_kernel)
   float* dk_acc;       // [T, Hkv, 256] fp32 (scaled)
   float* dv_acc;       // [T, Hkv, 256] fp32, right after dk_acc
 };

@@ -11,8 +11,9 @@
 //   ulist  per (query tile, g): count, then the 64-key tiles (16 blocks each)
 //          holding a block selected by any of the tile's tokens ("tile map")
 //
-// Forward, persistent CTAs over the query tiles.  Tile = 128 rows = 10 tokens x
-// the 12 query heads of one KV head (rows 120..127 are padding):
+// Forward, persistent CTAs claiming the query tiles (heaviest first) from a
+// counter.  Tile = 128 rows = 10 tokens x the 12 query heads of one KV head
+// (rows 120..127 are padding):
 //   warp 0 : TMA Q (4 x 64-column chunks) and K tiles (2-stage ring)
 //   warp 2 : TMA V tiles (own 2-stage ring)
 //   warp 1 : MMA  S_n = Q K_n^T (M 128, N 64, K 256) into one of two TMEM
@@ -43,12 +44,48 @@ constexpr float kQLog2e = 1.4426950408889634f;
 constexpr float kQRescale = 8.0f;
 constexpr int kQFwdThreads = 256;           // warps 0 Q/K, 1 MMA, 2 V, 3 idle, 4..7 softmax
 
+// Work units (query tiles, or key-tile items) are claimed from a counter by
+// one thread (the first producer) and passed to the other roles through a
+// ring of slots: the second producer, the MMA thread and lane 0 of each of
+// the four softmax / compute warps read every slot once.  -1 ends the loops.
+constexpr int kRing = 4;
+constexpr int kRingReaders = 6;
+constexpr int kRingTimeout = -2;
+struct ClaimRing {
+  uint64_t full[kRing], empty[kRing];
+  int id[kRing];
+};
+__device__ __forceinline__ void ring_init(ClaimRing& r) {
+  for (int i = 0; i < kRing; ++i) {
+    mbar_init(&r.full[i], 1);
+    mbar_init(&r.empty[i], kRingReaders);
+  }
+}
+// Publishes the id of the claimer's k-th unit; false if the wait ran out.
+__device__ __forceinline__ bool ring_put(ClaimRing& r, uint32_t k, int id, uint32_t* status,
+                                         uint32_t site) {
+  const int sl = k % kRing;
+  if (!mbar_wait(&r.empty[sl], ((k / kRing) & 1) ^ 1, status, site)) return false;
+  r.id[sl] = id;
+  mbar_arrive(&r.full[sl]);
+  return true;
+}
+// The id of a reader's k-th unit (-1: none left; kRingTimeout: the wait ran out).
+__device__ __forceinline__ int ring_get(ClaimRing& r, uint32_t k, uint32_t* status, uint32_t site) {
+  const int sl = k % kRing;
+  if (!mbar_wait(&r.full[sl], (k / kRing) & 1, status, site)) return kRingTimeout;
+  const int id = r.id[sl];
+  mbar_arrive(&r.empty[sl]);
+  return id;
+}
+
 struct QsaFwdSmem {
   uint8_t q[kQTileBytes];
   uint8_t k[2][kKTileBytes];
   uint8_t v[2][kKTileBytes];
   uint64_t q_full, q_empty, k_full[2], k_empty[2], v_full[2], v_empty[2];
   uint64_t s_full[2], p_full[2], pv_done[2], o_free;
+  ClaimRing ring;
   uint32_t tmem_base;
 };
 static_assert(sizeof(QsaFwdSmem) + 1024 <= 232448, "QSA forward shared memory");
@@ -138,9 +175,12 @@ __global__ void __launch_bounds__(256) qsa_union_kernel(const uint32_t* __restri
                                                         const int* __restrict__ num_tiles,
                                                         int Hkv, int ustride,
                                                         int* __restrict__ ulist,
+                                                        int* __restrict__ tile_ctr,
                                                         uint32_t* status) {
   pdl_enter();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (blockIdx.x == 0)   // the persistent kernels claim query tiles from 0
+    for (int i = threadIdx.x; i < Hkv; i += blockDim.x) tile_ctr[i] = 0;
   const int total = *num_tiles * Hkv;
   for (int gw = blockIdx.x * 8 + warp; gw < total; gw += gridDim.x * 8) {
     const int ti = gw / Hkv, g = gw % Hkv;
@@ -173,7 +213,8 @@ __global__ void __launch_bounds__(kQFwdThreads, 1)
                    int W, const int* __restrict__ ulist, int ustride,
                    const int32_t* __restrict__ cu, const int2* __restrict__ tiles,
                    const int* __restrict__ num_tiles, int Hq, int Hkv, float scale,
-                   __nv_bfloat16* __restrict__ o, float* __restrict__ lse, uint32_t* status) {
+                   __nv_bfloat16* __restrict__ o, float* __restrict__ lse, int* __restrict__ ctr,
+                      uint32_t* status) {
   pdl_enter();
   const int ntiles = *num_tiles;
   if (static_cast<int>(blockIdx.x) >= ntiles) return;
@@ -196,6 +237,7 @@ __global__ void __launch_bounds__(kQFwdThreads, 1)
       mbar_init(&sm.p_full[i], 128);
       mbar_init(&sm.pv_done[i], 1);
     }
+    ring_init(sm.ring);
     fence_mbar_init();
   }
   if (warp >= 4) {
@@ -222,7 +264,12 @@ __global__ void __launch_bounds__(kQFwdThreads, 1)
       prefetch_tmap(&tm_k);
       uint32_t tc = 0, kc = 0;
       bool ok = true;
-      for (int ti = blockIdx.x; ok && ti < ntiles; ti += gridDim.x) {
+      int pending = atomicAdd(ctr + g, 1);
+      for (uint32_t wu = 0; ok; ++wu) {
+        const int ti = pending < ntiles ? pending : -1;
+        if (!(ok = ring_put(sm.ring, wu, ti, status, 60))) break;
+        if (ti < 0) break;
+        pending = atomicAdd(ctr + g, 1);
         const QTile t = qsa_tile(tiles, cu, ti);
         const int* ul = ulist + (static_cast<size_t>(ti) * Hkv + g) * ustride;
         const int nk = __ldg(ul);
@@ -249,7 +296,10 @@ __global__ void __launch_bounds__(kQFwdThreads, 1)
       prefetch_tmap(&tm_v);
       uint32_t vc = 0;
       bool ok = true;
-      for (int ti = blockIdx.x; ok && ti < ntiles; ti += gridDim.x) {
+      for (uint32_t wu = 0; ok; ++wu) {
+        const int ti = ring_get(sm.ring, wu, status, 61);
+        if (ti == kRingTimeout) ok = false;
+        if (ti < 0) break;
         const QTile t = qsa_tile(tiles, cu, ti);
         const int* ul = ulist + (static_cast<size_t>(ti) * Hkv + g) * ustride;
         const int nk = __ldg(ul);
@@ -270,7 +320,10 @@ __global__ void __launch_bounds__(kQFwdThreads, 1)
       uint32_t tc = 0, kc = 0, vc = 0, n = 0;
       bool ok = true;
       const uint32_t qa = smem_u32(sm.q);
-      for (int ti = blockIdx.x; ok && ti < ntiles; ti += gridDim.x) {
+      for (uint32_t wu = 0; ok; ++wu) {
+        const int ti = ring_get(sm.ring, wu, status, 61);
+        if (ti == kRingTimeout) ok = false;
+        if (ti < 0) break;
         const int nk = __ldg(ulist + (static_cast<size_t>(ti) * Hkv + g) * ustride);
         if (nk == 0) continue;
         if (!(ok = mbar_wait(&sm.q_full, tc & 1, status, 4))) break;
@@ -330,7 +383,12 @@ __global__ void __launch_bounds__(kQFwdThreads, 1)
     const float sl2 = scale * kQLog2e;
     uint32_t tc = 0, n = 0;
     bool ok = true;
-    for (int ti = blockIdx.x; ok && ti < ntiles; ti += gridDim.x) {
+    for (uint32_t wu = 0; ok; ++wu) {
+      int ti = 0;
+      if (lane == 0) ti = ring_get(sm.ring, wu, status, 62);
+      ti = __shfl_sync(0xffffffffu, ti, 0);
+      if (ti == kRingTimeout) ok = false;
+      if (ti < 0) break;
       const QTile t = qsa_tile(tiles, cu, ti);
       const int* ul = ulist + (static_cast<size_t>(ti) * Hkv + g) * ustride;
       const int nk = __ldg(ul);
@@ -492,6 +550,7 @@ struct QsaDqSmem {
   uint8_t v[kKTileBytes];
   uint64_t qd_full, qd_empty, k_full[2], k_empty[2], v_full, v_empty;
   uint64_t s_full[2], ds_full[2], dq_done[2], dq_free;
+  ClaimRing ring;
   uint32_t tmem_base;
 };
 static_assert(sizeof(QsaDqSmem) + 1024 <= 232448, "QSA dQ shared memory");
@@ -508,6 +567,7 @@ struct QsaDkvSmem {
   // that MMA is done
   uint64_t kv_full, kv_empty, q_full[2], q_empty[2], do_full[2], do_empty[2];
   uint64_t s_full, pds_full, pds_empty, acc_full, acc_free;
+  ClaimRing ring;
   uint32_t tmem_base;
 };
 static_assert(sizeof(QsaDkvSmem) + 1024 <= 232448, "QSA dK/dV shared memory");
@@ -628,8 +688,10 @@ __global__ void __launch_bounds__(1024) qsa_order_kernel(const int* __restrict__
                                                          const int* __restrict__ num_items,
                                                          int Hkv, int max_items,
                                                          int* __restrict__ order,
-                                                         int* __restrict__ num_busy) {
+                                                         int* __restrict__ num_busy,
+                                                         int* __restrict__ item_ctr) {
   pdl_enter();
+  if (threadIdx.x == 0) item_ctr[blockIdx.x] = 0;   // the dK/dV kernel claims items from 0
   __shared__ int hist[kQWin + 1];
   __shared__ int start[kQWin + 1];
   const int g = blockIdx.x;
@@ -662,7 +724,8 @@ __global__ void __launch_bounds__(kQBwdThreads, 1)
                       const uint32_t* __restrict__ masks, int W, const int* __restrict__ ulist,
                       int ustride, const float2* __restrict__ lsd, const int32_t* __restrict__ cu,
                       const int2* __restrict__ tiles, const int* __restrict__ num_tiles, int Hq,
-                      int Hkv, float scale, __nv_bfloat16* __restrict__ dq, uint32_t* status) {
+                      int Hkv, float scale, __nv_bfloat16* __restrict__ dq, int* __restrict__ ctr,
+                      uint32_t* status) {
   pdl_enter();
   const int ntiles = *num_tiles;
   if (static_cast<int>(blockIdx.x) >= ntiles) return;
@@ -686,6 +749,7 @@ __global__ void __launch_bounds__(kQBwdThreads, 1)
       mbar_init(&sm.ds_full[i], 128);
       mbar_init(&sm.dq_done[i], 1);
     }
+    ring_init(sm.ring);
     fence_mbar_init();
   }
   if (warp >= 4) {
@@ -710,7 +774,12 @@ __global__ void __launch_bounds__(kQBwdThreads, 1)
       prefetch_tmap(&tm_k);
       uint32_t tc = 0, kc = 0;
       bool ok = true;
-      for (int ti = blockIdx.x; ok && ti < ntiles; ti += gridDim.x) {
+      int pending = atomicAdd(ctr + g, 1);
+      for (uint32_t wu = 0; ok; ++wu) {
+        const int ti = pending < ntiles ? pending : -1;
+        if (!(ok = ring_put(sm.ring, wu, ti, status, 60))) break;
+        if (ti < 0) break;
+        pending = atomicAdd(ctr + g, 1);
         const QTile t = qsa_tile(tiles, cu, ti);
         const int* ul = ulist + (static_cast<size_t>(ti) * Hkv + g) * ustride;
         const int nk = __ldg(ul);
@@ -740,7 +809,10 @@ __global__ void __launch_bounds__(kQBwdThreads, 1)
       prefetch_tmap(&tm_v);
       uint32_t vc = 0;
       bool ok = true;
-      for (int ti = blockIdx.x; ok && ti < ntiles; ti += gridDim.x) {
+      for (uint32_t wu = 0; ok; ++wu) {
+        const int ti = ring_get(sm.ring, wu, status, 61);
+        if (ti == kRingTimeout) ok = false;
+        if (ti < 0) break;
         const QTile t = qsa_tile(tiles, cu, ti);
         const int* ul = ulist + (static_cast<size_t>(ti) * Hkv + g) * ustride;
         const int nk = __ldg(ul);
@@ -760,7 +832,10 @@ __global__ void __launch_bounds__(kQBwdThreads, 1)
       uint32_t tc = 0, kc = 0, kq = 0, vc = 0, n = 0;
       bool ok = true;
       const uint32_t qa = smem_u32(sm.q), da = smem_u32(sm.dout), va = smem_u32(sm.v);
-      for (int ti = blockIdx.x; ok && ti < ntiles; ti += gridDim.x) {
+      for (uint32_t wu = 0; ok; ++wu) {
+        const int ti = ring_get(sm.ring, wu, status, 61);
+        if (ti == kRingTimeout) ok = false;
+        if (ti < 0) break;
         const int nk = __ldg(ulist + (static_cast<size_t>(ti) * Hkv + g) * ustride);
         if (nk == 0) continue;
         if (!(ok = mbar_wait(&sm.qd_full, tc & 1, status, 24))) break;
@@ -829,7 +904,12 @@ __global__ void __launch_bounds__(kQBwdThreads, 1)
     const float sl2 = scale * kQLog2e;
     uint32_t tc = 0, n = 0;
     bool ok = true;
-    for (int ti = blockIdx.x; ok && ti < ntiles; ti += gridDim.x) {
+    for (uint32_t wu = 0; ok; ++wu) {
+      int ti = 0;
+      if (lane == 0) ti = ring_get(sm.ring, wu, status, 62);
+      ti = __shfl_sync(0xffffffffu, ti, 0);
+      if (ti == kRingTimeout) ok = false;
+      if (ti < 0) break;
       const QTile t = qsa_tile(tiles, cu, ti);
       const int* ul = ulist + (static_cast<size_t>(ti) * Hkv + g) * ustride;
       const int nk = __ldg(ul);
@@ -927,7 +1007,8 @@ __global__ void __launch_bounds__(kQBwdThreads, 1)
                        const int4* __restrict__ items, const int* __restrict__ order,
                        const int* __restrict__ num_busy, int max_items, int Hq, int Hkv,
                        float scale, float* __restrict__ dk_acc, float* __restrict__ dv_acc,
-                       uint32_t* status) {
+                       int* __restrict__ ctr,
+                      uint32_t* status) {
   pdl_enter();
   const int nitems = num_busy[blockIdx.y];
   if (static_cast<int>(blockIdx.x) >= nitems) return;
@@ -953,6 +1034,7 @@ __global__ void __launch_bounds__(kQBwdThreads, 1)
     mbar_init(&sm.pds_empty, 1);
     mbar_init(&sm.acc_full, 1);
     mbar_init(&sm.acc_free, 128);
+    ring_init(sm.ring);
     fence_mbar_init();
   }
   if (warp >= 4) {
@@ -978,7 +1060,12 @@ __global__ void __launch_bounds__(kQBwdThreads, 1)
       prefetch_tmap(&tm_v);
       uint32_t ic = 0, qc = 0;
       bool ok = true;
-      for (int jt = blockIdx.x; ok && jt < nitems; jt += gridDim.x) {
+      int pending = atomicAdd(ctr + g, 1);
+      for (uint32_t wu = 0; ok; ++wu) {
+        const int jt = pending < nitems ? pending : -1;
+        if (!(ok = ring_put(sm.ring, wu, jt, status, 60))) break;
+        if (jt < 0) break;
+        pending = atomicAdd(ctr + g, 1);
         const int it = __ldg(ord + jt);
         const int* kl = klist + (static_cast<size_t>(it) * Hkv + g) * (1 + kQWin);
         const int nq = __ldg(kl);
@@ -1011,7 +1098,10 @@ __global__ void __launch_bounds__(kQBwdThreads, 1)
       prefetch_tmap(&tm_do);
       uint32_t dc = 0;
       bool ok = true;
-      for (int jt = blockIdx.x; ok && jt < nitems; jt += gridDim.x) {
+      for (uint32_t wu = 0; ok; ++wu) {
+        const int jt = ring_get(sm.ring, wu, status, 61);
+        if (jt == kRingTimeout) ok = false;
+        if (jt < 0) break;
         const int it = __ldg(ord + jt);
         const int* kl = klist + (static_cast<size_t>(it) * Hkv + g) * (1 + kQWin);
         const int nq = __ldg(kl);
@@ -1037,7 +1127,10 @@ __global__ void __launch_bounds__(kQBwdThreads, 1)
       bool ok = true;
       const uint32_t qa = smem_u32(sm.q), da = smem_u32(sm.dout), ka = smem_u32(sm.k),
                      va = smem_u32(sm.v), pa = smem_u32(sm.p), sa = smem_u32(sm.ds);
-      for (int jt = blockIdx.x; ok && jt < nitems; jt += gridDim.x) {
+      for (uint32_t wu = 0; ok; ++wu) {
+        const int jt = ring_get(sm.ring, wu, status, 61);
+        if (jt == kRingTimeout) ok = false;
+        if (jt < 0) break;
         const int it = __ldg(ord + jt);
         const int nq = __ldg(klist + (static_cast<size_t>(it) * Hkv + g) * (1 + kQWin));
         if (nq == 0) continue;
@@ -1113,7 +1206,12 @@ __global__ void __launch_bounds__(kQBwdThreads, 1)
     const float sl2 = scale * kQLog2e;
     uint32_t ic = 0, n = 0;
     bool ok = true;
-    for (int jt = blockIdx.x; ok && jt < nitems; jt += gridDim.x) {
+    for (uint32_t wu = 0; ok; ++wu) {
+      int jt = 0;
+      if (lane == 0) jt = ring_get(sm.ring, wu, status, 62);
+      jt = __shfl_sync(0xffffffffu, jt, 0);
+      if (jt == kRingTimeout) ok = false;
+      if (jt < 0) break;
       const int it = __ldg(ord + jt);
       const int* kl = klist + (static_cast<size_t>(it) * Hkv + g) * (1 + kQWin);
       const int nq = __ldg(kl);
@@ -1259,6 +1357,7 @@ QsaFwdWorkspace carve_qsa_fwd_workspace(WsCursor& ws, int T, int S, int Hkv, int
   w.masks = ws.take<uint32_t>(static_cast<size_t>(T) * Hkv * w.W);
   w.ustride = qsa_ustride(max_seqlen);
   w.ulist = ws.take<int>(static_cast<size_t>(w.plan.max_tiles) * Hkv * w.ustride);
+  w.tile_ctr = ws.take<int>(Hkv);
   return w;
 }
 
@@ -1273,6 +1372,7 @@ QsaBwdWorkspace carve_qsa_bwd_workspace(WsCursor& ws, int T, int S, int Hq, int 
   w.klist = ws.take<int>(static_cast<size_t>(w.max_items) * Hkv * (1 + kQWin));
   w.order = ws.take<int>(static_cast<size_t>(w.max_items) * Hkv);
   w.num_busy = ws.take<int>(Hkv);
+  w.item_ctr = ws.take<int>(Hkv);
   // the two accumulators stay adjacent: one clear covers them
   w.dk_acc = ws.take<float>(static_cast<size_t>(T) * Hkv * kQD);
   w.dv_acc = ws.take<float>(static_cast<size_t>(T) * Hkv * kQD);
@@ -1296,7 +1396,7 @@ static msa_status_t launch_qsa_tilemap(const int32_t* sel, const int32_t* cu, in
     launch_pdl(qsa_union_kernel,
         capped_blocks(static_cast<size_t>(fw.plan.max_tiles) * Hkv, 8, 4 * sms), 256, 0, stream,
         fw.masks, fw.W, cu, fw.plan.tiles, fw.plan.num_tiles, Hkv, fw.ustride, fw.ulist,
-        status_word());
+        fw.tile_ctr, status_word());
   }
   return check_launch("qsa_union_kernel");
 }
@@ -1344,7 +1444,7 @@ msa_status_t launch_qsa_fwd(const void* q, const void* k, const void* v, const i
     TraceScope trace_("qsa_fwd_kernel", stream);
     launch_pdl(qsa_fwd_kernel, grid, kQFwdThreads, smem, stream, tq, tk, tv, fw.masks, fw.W,
         fw.ulist, fw.ustride, cu, fw.plan.tiles, fw.plan.num_tiles, Hq, Hkv, scale,
-        static_cast<__nv_bfloat16*>(o), lse, status_word());
+        static_cast<__nv_bfloat16*>(o), lse, fw.tile_ctr, status_word());
   }
   return check_launch("qsa_fwd_kernel");
 }
@@ -1388,7 +1488,7 @@ msa_status_t launch_qsa_bwd(const void* q, const void* k, const void* v, const v
   {
     TraceScope trace_("qsa_order_kernel", stream);
     launch_pdl(qsa_order_kernel, Hkv, 1024, 0, stream, w.klist, w.num_items, Hkv, w.max_items,
-        w.order, w.num_busy);
+        w.order, w.num_busy, w.item_ctr);
   }
   QSA_TRY(check_launch("qsa_delta/items/kvlist/order"));
 
@@ -1402,7 +1502,7 @@ msa_status_t launch_qsa_bwd(const void* q, const void* k, const void* v, const v
     TraceScope trace_("qsa_bwd_dq_kernel", stream);
     launch_pdl(qsa_bwd_dq_kernel, grid, kQBwdThreads, smem_dq, stream, tq, tdo, tk, tv,
         fw.masks, fw.W, fw.ulist, fw.ustride, w.lsd, cu, fw.plan.tiles, fw.plan.num_tiles, Hq,
-        Hkv, scale, static_cast<__nv_bfloat16*>(dq), status_word());
+        Hkv, scale, static_cast<__nv_bfloat16*>(dq), w.map.tile_ctr, status_word());
   }
   QSA_TRY(check_launch("qsa_bwd_dq_kernel"));
 
@@ -1414,7 +1514,7 @@ msa_status_t launch_qsa_bwd(const void* q, const void* k, const void* v, const v
     TraceScope trace_("qsa_bwd_dkv_kernel", stream);
     launch_pdl(qsa_bwd_dkv_kernel, grid, kQBwdThreads, smem_kv, stream, tq, tdo, tk, tv,
         fw.masks, fw.W, w.klist, w.lsd, cu, w.items, w.order, w.num_busy, w.max_items, Hq, Hkv,
-        scale, w.dk_acc, w.dv_acc, status_word());
+        scale, w.dk_acc, w.dv_acc, w.item_ctr, status_word());
   }
   QSA_TRY(check_launch("qsa_bwd_dkv_kernel"));
   {
