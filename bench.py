@@ -486,7 +486,9 @@ def run_ours(args):
 
         e2e_steps(3)
         torch.cuda.synchronize(dev)
-        n_e2e = max(5, args.steps // 4)
+        # as many steps as the device-resident timing, so that the unoverlapped
+        # first upload and last download weigh as little as in a long job
+        n_e2e = max(5, args.steps)
         barrier()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e2e_steps(n_e2e, first=e0)

@@ -149,17 +149,18 @@ __device__ __forceinline__ void write_union(int* out, const uint32_t (&mm)[kTpt]
 
 }  // namespace
 
-// One CTA of two warps per (128-token query block, KV head), grid-striding;
-// warp w groups the block's tokens [64 w, 64 w + 64) into the tiles (sub-tiles
-// 8 w .. 8 w + 7) of up to 8 tokens (the tile's MMA rows are 8 tokens x 16
-// heads) so that each tile's union of selected blocks - what its MMAs walk -
-// stays small: a group starts from the lowest ungrouped token and repeatedly
-// takes the token that adds the fewest blocks to the group's union (ties: the
-// lower token).  Per tile the header holds the member offsets and count, then
-// the union in ascending order, each entry (block << 8) | member mask.
-constexpr int kUnionThreads = 64;
-constexpr int kHalfTokens = kBlock / 2;
-__global__ void __launch_bounds__(kUnionThreads) fwd_union_kernel(const int32_t* __restrict__ sel,
+// One CTA per (128-token query block, KV head), grid-striding, of kWarps
+// warps: warp w groups the block's tokens [w 128 / kWarps, (w + 1) 128 / kWarps)
+// into tiles (sub-tiles 16 w / kWarps ..) of up to 8 tokens (the tile's MMA rows
+// are 8 tokens x 16 heads) so that each tile's union of selected blocks - what
+// its MMAs walk - stays small: a group starts from the lowest ungrouped token
+// and repeatedly takes the token that adds the fewest blocks to the group's
+// union (ties: the lower token).  Two warps (64 tokens each) halve the serial
+// chain of greedy steps; one warp over all 128 tokens groups better, which pays
+// on long sequences.  Per tile the header holds the member offsets and count,
+// then the union in ascending order, each entry (block << 8) | member mask.
+template <int kWarps>
+__global__ void __launch_bounds__(32 * kWarps) fwd_union_kernel(const int32_t* __restrict__ sel,
                                                                   const int32_t* __restrict__ cu,
                                                                   const int2* __restrict__ tiles,
                                                                   const int* __restrict__ num_tiles,
@@ -167,7 +168,9 @@ __global__ void __launch_bounds__(kUnionThreads) fwd_union_kernel(const int32_t*
                                                                   int* __restrict__ tile_ctr,
                                                                   uint32_t* status) {
   pdl_enter();
-  __shared__ uint4 tok_mask[2][kHalfTokens];   // per warp: its tokens' masks (kGroupWords = 4)
+  constexpr int kWTok = kBlock / kWarps;         // tokens of one warp
+  constexpr int kPerLane = kWTok / 32;
+  __shared__ uint4 tok_mask[kWarps][kWTok];      // per warp: its tokens' masks (kGroupWords = 4)
   static_assert(kGroupWords == 4, "one uint4 per token mask");
   const int nblk = *num_tiles;
   const int g = blockIdx.y;
@@ -178,31 +181,32 @@ __global__ void __launch_bounds__(kUnionThreads) fwd_union_kernel(const int32_t*
     const int qb = pt.y;
     const int seq0 = cu[pt.x];
     const int n = min(kBlock, cu[pt.x + 1] - seq0 - qb * kBlock);   // tokens of the block
-    const int t0 = kHalfTokens * warp;                              // this warp's first token
-    const int nw = max(0, min(kHalfTokens, n - t0));                 // and its token count
+    const int t0 = kWTok * warp;                                    // this warp's first token
+    const int nw = max(0, min(kWTok, n - t0));                       // and its token count
     const int ngrp = (nw + kTpt - 1) / kTpt;
     auto tile_out = [&](int grp) {
-      return ulist + (static_cast<size_t>(pb * kG + 8 * warp + grp) * Hkv + g) * kFwdUnionStride;
+      return ulist + (static_cast<size_t>(pb * kG + (kG / kWarps) * warp + grp) * Hkv + g) *
+                         kFwdUnionStride;
     };
-    if (lane >= ngrp && lane < 8) tile_out(lane)[0] = 0;
+    if (lane >= ngrp && lane < kG / kWarps) tile_out(lane)[0] = 0;
     const bool fits = qb < 32 * kGroupWords;
     const int words = fits ? (qb + 31) / 32 : 0;
     // ---- the tokens' masks of selected earlier blocks (own block left out);
     // all loads first, then the bits
-    int4 ids[2][4];
+    int4 ids[kPerLane][4];
 #pragma unroll
-    for (int k = 0; k < 2; ++k) {
+    for (int k = 0; k < kPerLane; ++k) {
       const int tok = t0 + lane + 32 * k;
       const int4* row = reinterpret_cast<const int4*>(
           sel + (static_cast<size_t>(seq0 + qb * kBlock + tok) * Hkv + g) * kTopK);
 #pragma unroll
       for (int c = 0; c < 4; ++c) ids[k][c] = tok < n ? __ldg(row + c) : make_int4(-1, -1, -1, -1);
     }
-    uint32_t m[2][kGroupWords];
+    uint32_t m[kPerLane][kGroupWords];
     uint32_t left = 0;                     // bit k: token t0 + lane + 32 k not grouped yet
     bool bad = false;
 #pragma unroll
-    for (int k = 0; k < 2; ++k) {
+    for (int k = 0; k < kPerLane; ++k) {
 #pragma unroll
       for (int w = 0; w < kGroupWords; ++w) m[k][w] = 0;
       if (t0 + lane + 32 * k < n) left |= 1u << k;
@@ -276,7 +280,7 @@ __global__ void __launch_bounds__(kUnionThreads) fwd_union_kernel(const int32_t*
             if (left) key = static_cast<uint32_t>(lane + 32 * (__ffs(left) - 1));
           } else {
 #pragma unroll
-            for (int k = 0; k < 2; ++k) {
+            for (int k = 0; k < kPerLane; ++k) {
               if (left & (1u << k)) {
                 int cost = 0;
 #pragma unroll
@@ -717,7 +721,6 @@ msa_status_t launch_sparse_fwd(const void* q, const void* k, const void* v, cons
                                cudaStream_t stream) {
   const Plan& plan = fw.plan;
   (void)S;
-  (void)max_seqlen;
   if (Hq / Hkv != kG)
     return fail(MSA_ERR_UNSUPPORTED, "forward supports Hq/Hkv = 16 (got %d)", Hq / Hkv);
   CUtensorMap tq, tk, tv, to;
@@ -742,12 +745,15 @@ msa_status_t launch_sparse_fwd(const void* q, const void* k, const void* v, cons
   const int max_ctas = plan.max_tiles * kG;
   dim3 grid(static_cast<unsigned>(per_head < max_ctas ? per_head : max_ctas), Hkv);
   {
-    // one CTA of two warps per (128-token query block, KV head)
+    // one CTA per (128-token query block, KV head): the one-warp grouping over
+    // whole blocks when sequences are long enough for its better tiles to
+    // outweigh its longer serial chain (measured on 12k-token sequences)
     const int ublocks = plan.max_tiles;
     const int cap = 8 * device_sm_count();
     dim3 ugrid(static_cast<unsigned>(ublocks < cap ? ublocks : cap), Hkv);
+    const bool whole = max_seqlen >= 8192;
     TraceScope trace_("fwd_union_kernel", stream);
-    launch_pdl(fwd_union_kernel, ugrid, kUnionThreads, 0, stream, sel, cu, plan.tiles, plan.num_tiles, Hkv,
+    launch_pdl(whole ? fwd_union_kernel<1> : fwd_union_kernel<2>, ugrid, whole ? 32 : 64, 0, stream, sel, cu, plan.tiles, plan.num_tiles, Hkv,
         fw.ulist, fw.tile_ctr, status_word());
   }
   {
