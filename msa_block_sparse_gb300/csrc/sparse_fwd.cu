@@ -116,10 +116,6 @@ __device__ __forceinline__ int member_offset(const TileInfo& t, int i) {
   return static_cast<int>((w >> (8 * (i & 3))) & 0xFFu);
 }
 
-}  // namespace
-
-namespace {
-
 // Token masks held in registers by the grouping: blocks below 32 x kGroupWords
 // (query blocks of sequences up to 16,384 tokens); longer ones group
 // consecutive tokens.
@@ -414,9 +410,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         sm.tile_id[tb] = ti;
         sm.tinfo[tb] = t;
         pending = atomicAdd(tile_ctr + g, 1);   // next claim, in flight while K streams
-        mbar_arrive_expect_tx(&sm.tile_full[tb], t.ntok * 2 * kTokRows);
       }
-      __syncwarp();
+      __syncwarp();                             // the slot is written (released by the arrive)
+      if (lane == 0) mbar_arrive_expect_tx(&sm.tile_full[tb], t.ntok * 2 * kTokRows);
+      __syncwarp();                             // the copies below complete after it
       // Q rows of the tile's tokens (16 heads each), one copy per token and D half
       if (lane < 2 * t.ntok) {
         const int i = lane >> 1, hf = lane & 1;
