@@ -71,6 +71,22 @@ int device_sm_count() {
   return cached[dev];
 }
 
+msa_status_t ensure_smem_ptr(const void* kernel, size_t bytes, const char* name) {
+  static std::mutex mu;
+  static std::map<std::pair<const void*, int>, size_t> done;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return fail(MSA_ERR_CUDA, "cudaGetDevice failed");
+  std::lock_guard<std::mutex> lk(mu);
+  size_t& have = done[std::make_pair(kernel, dev)];
+  if (have < bytes) {
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(bytes)) != cudaSuccess)
+      return fail(MSA_ERR_CUDA, "%s: %zu bytes of dynamic shared memory refused", name, bytes);
+    have = bytes;
+  }
+  return MSA_OK;
+}
+
 // ------------------------------------------------------------------ tracing
 
 namespace {

@@ -517,11 +517,9 @@ msa_status_t launch_decode(const void* q, const void* q_idx, const void* k_cache
   if (!make_tmap_bf16(&tk, k_cache, 2, dims, box) || !make_tmap_bf16(&tv, v_cache, 2, dims, box))
     return fail(MSA_ERR_CUDA, "cuTensorMapEncodeTiled failed for the paged K/V caches");
   const size_t smem = sizeof(AttendSmem) + 1024;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaFuncSetAttribute(decode_attend_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         static_cast<int>(smem));
-    attr_set = true;
+  {
+    const msa_status_t e = ensure_smem(decode_attend_kernel, smem, "decode_attend_kernel");
+    if (e != MSA_OK) return e;
   }
   dim3 g2(B, Hkv, kDecodeSplits);
   {

@@ -231,11 +231,9 @@ msa_status_t launch_index_select(const void* q_idx, const void* k_idx, const int
   if (!make_tmap_bf16(&tq, q_idx, 3, dims, box) || !make_tmap_bf16(&tk, k_idx, 3, dims, box))
     return fail(MSA_ERR_CUDA, "cuTensorMapEncodeTiled failed for q_idx/k_idx");
   const size_t smem = sizeof(SelSmem) + 1024;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaFuncSetAttribute(index_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         static_cast<int>(smem));
-    attr_set = true;
+  {
+    const msa_status_t e = ensure_smem(index_select_kernel, smem, "index_select_kernel");
+    if (e != MSA_OK) return e;
   }
   dim3 grid(plan.max_tiles, Hi);
   {

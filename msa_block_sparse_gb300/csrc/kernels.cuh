@@ -75,6 +75,13 @@ struct BwdWorkspace {
 };
 BwdWorkspace carve_bwd_workspace(WsCursor& ws, int T, int S, int Hq, int Hkv, int max_seqlen);
 int device_sm_count();
+// Raises `kernel`'s dynamic shared-memory limit to `bytes` on the current
+// device, once per (kernel, device): the attribute is kept per device.
+msa_status_t ensure_smem_ptr(const void* kernel, size_t bytes, const char* name);
+template <typename K>
+inline msa_status_t ensure_smem(K kernel, size_t bytes, const char* name) {
+  return ensure_smem_ptr(reinterpret_cast<const void*>(kernel), bytes, name);
+}
 msa_status_t launch_sparse_bwd(const void* q, const void* k, const void* v, const void* o,
                                const void* dout, const float* lse, const int32_t* sel,
                                const int32_t* cu, int S, int T, int Hq, int Hkv, int max_seqlen,

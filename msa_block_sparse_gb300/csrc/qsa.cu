@@ -1414,15 +1414,6 @@ static bool qsa_maps(const void* q, const void* k, const void* v, const void* do
          make_tmap_bf16(tv, v, 3, dkv, bkv) && (!dout || make_tmap_bf16(tdo, dout, 3, dq, bq));
 }
 
-template <typename K>
-static void set_smem(K kernel, size_t bytes, bool& done) {
-  if (!done) {
-    cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         static_cast<int>(bytes));
-    done = true;
-  }
-}
-
 msa_status_t launch_qsa_fwd(const void* q, const void* k, const void* v, const int32_t* sel,
                             const int32_t* cu, int S, int T, int Hq, int Hkv, int topk,
                             int max_seqlen, float scale, const QsaFwdWorkspace& fw, void* o,
@@ -1435,8 +1426,7 @@ msa_status_t launch_qsa_fwd(const void* q, const void* k, const void* v, const i
     return fail(MSA_ERR_CUDA, "cuTensorMapEncodeTiled failed for the narrow-block q/k/v");
   QSA_TRY(launch_qsa_tilemap(sel, cu, S, T, Hkv, topk, max_seqlen, fw, stream));
   const size_t smem = sizeof(QsaFwdSmem) + 1024;
-  static bool attr_set = false;
-  set_smem(qsa_fwd_kernel, smem, attr_set);
+  QSA_TRY(ensure_smem(qsa_fwd_kernel, smem, "qsa_fwd_kernel"));
   const int per_head = (device_sm_count() + Hkv - 1) / Hkv;
   dim3 grid(static_cast<unsigned>(per_head < fw.plan.max_tiles ? per_head : fw.plan.max_tiles),
             Hkv);
@@ -1493,8 +1483,7 @@ msa_status_t launch_qsa_bwd(const void* q, const void* k, const void* v, const v
   QSA_TRY(check_launch("qsa_delta/items/kvlist/order"));
 
   const size_t smem_dq = sizeof(QsaDqSmem) + 1024;
-  static bool dq_attr = false;
-  set_smem(qsa_bwd_dq_kernel, smem_dq, dq_attr);
+  QSA_TRY(ensure_smem(qsa_bwd_dq_kernel, smem_dq, "qsa_bwd_dq_kernel"));
   const int per_head = (sms + Hkv - 1) / Hkv;
   {
     dim3 grid(static_cast<unsigned>(per_head < fw.plan.max_tiles ? per_head : fw.plan.max_tiles),
@@ -1507,8 +1496,7 @@ msa_status_t launch_qsa_bwd(const void* q, const void* k, const void* v, const v
   QSA_TRY(check_launch("qsa_bwd_dq_kernel"));
 
   const size_t smem_kv = sizeof(QsaDkvSmem) + 1024;
-  static bool kv_attr = false;
-  set_smem(qsa_bwd_dkv_kernel, smem_kv, kv_attr);
+  QSA_TRY(ensure_smem(qsa_bwd_dkv_kernel, smem_kv, "qsa_bwd_dkv_kernel"));
   {
     dim3 grid(static_cast<unsigned>(per_head < w.max_items ? per_head : w.max_items), Hkv);
     TraceScope trace_("qsa_bwd_dkv_kernel", stream);

@@ -881,11 +881,9 @@ msa_status_t launch_sparse_bwd(const void* q, const void* k, const void* v, cons
   if (e != MSA_OK) return e;
 
   const size_t smem = sizeof(BwdSmem);
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaFuncSetAttribute(sparse_bwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         static_cast<int>(smem));
-    attr_set = true;
+  {
+    const msa_status_t e = ensure_smem(sparse_bwd_kernel, smem, "sparse_bwd_kernel");
+    if (e != MSA_OK) return e;
   }
   const int per_head = (device_sm_count() + Hkv - 1) / Hkv;
   dim3 grid(static_cast<unsigned>(per_head < ws.max_items ? per_head : ws.max_items), Hkv);

@@ -732,11 +732,9 @@ msa_status_t launch_sparse_fwd(const void* q, const void* k, const void* v, cons
       !make_tmap_bf16(&tv, v, 3, dkv, bkv) || !make_tmap_bf16(&to, o, 3, dq, bq))
     return fail(MSA_ERR_CUDA, "cuTensorMapEncodeTiled failed for q/k/v/o");
   const size_t smem = sizeof(FwdSmem);
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaFuncSetAttribute(sparse_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         static_cast<int>(smem));
-    attr_set = true;
+  {
+    const msa_status_t e = ensure_smem(sparse_fwd_kernel, smem, "sparse_fwd_kernel");
+    if (e != MSA_OK) return e;
   }
   const int per_head = (device_sm_count() + Hkv - 1) / Hkv;
   const int max_ctas = plan.max_tiles * kG;
