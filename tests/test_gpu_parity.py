@@ -19,6 +19,7 @@ import torch
 
 import workloads as W
 from oracle import msa_oracle as O
+from tests import selection_check as SC
 
 pytestmark = pytest.mark.gpu
 
@@ -54,14 +55,19 @@ def bf16_step(v):
     return np.ldexp(1.0, np.floor(np.log2(a)).astype(np.int64) - 7)
 
 
-def compare_selection(gsel, osel, gap, what):
-    """Rows that differ must be near-ties; returns (differing rows, near-tie rows)."""
-    diff = np.any(gsel != osel, axis=-1)
-    near = gap < O.NEAR_TIE_REL
-    bad = diff & ~near
-    assert not bad.any(), f"{what}: {int(bad.sum())} rows differ outside near-ties " \
-                          f"(first {np.argwhere(bad)[:3].tolist()})"
-    return int(diff.sum()), int(near.sum())
+def compare_selection(gsel, osel, gap, what, own, scores_of, n_init=0):
+    """Every GPU row a valid selection; rows that differ from the oracle's are
+    near-ties and differ only inside the tie band (tests/selection_check.py).
+    Returns (differing rows, near-tie rows)."""
+    rep = SC.check_selection(gsel, osel, gap, own, scores_of, what, n_init)
+    print(f"{what}: {rep['differing']} differing rows, {rep['near_tie']} near-tie rows "
+          f"of {rep['rows']}")
+    return rep["differing"], rep["near_tie"]
+
+
+def own_blocks(cpu, tokens=None):
+    pos = O.positions(cpu["cu_seqlens"].numpy())
+    return (pos if tokens is None else pos[np.asarray(tokens)]) // 128
 
 
 RAGGED = W.PrefillShape("ragged-64q4kv", (300, 0, 1, 2000, 129, 2433), 64, 4, 4, runs_bwd=True)
@@ -180,8 +186,10 @@ def test_index_select_small(m, name):
     sel = m.msa_index_select(gpu["q_idx"], gpu["k_idx"], gpu["cu_seqlens"], max(shape.max_seqlen, 1))
     m.msa_check_status()
     osel, gap = oracle_selection(name, shape, cpu)
-    ndiff, nnear = compare_selection(sel.cpu().numpy(), osel, gap, name)
-    print(f"{name}: {ndiff} differing rows, {nnear} near-tie rows of {osel.shape[0] * osel.shape[1]}")
+    cun = cpu["cu_seqlens"].numpy()
+    compare_selection(sel.cpu().numpy(), osel, gap, name, own_blocks(cpu),
+                      SC.prefill_scores_of(f64(cpu["q_idx"]), f64(cpu["k_idx"]), cun,
+                                           np.arange(shape.T)))
 
 
 @pytest.mark.parametrize("idx", [1, 2, 4])
@@ -193,8 +201,9 @@ def test_index_select_full_size(m, idx):
     toks = sample_tokens(shape, n_random=1024, seed=idx)
     osel, gap = O.index_select(f64(cpu["q_idx"]), f64(cpu["k_idx"]), cpu["cu_seqlens"].numpy(),
                                tokens=toks)
-    ndiff, nnear = compare_selection(sel.cpu().numpy()[toks], osel, gap, f"cfg{idx}")
-    print(f"cfg{idx}: {ndiff} differing rows, {nnear} near-tie rows of {len(toks) * shape.hi}")
+    compare_selection(sel.cpu().numpy()[toks], osel, gap, f"cfg{idx}", own_blocks(cpu, toks),
+                      SC.prefill_scores_of(f64(cpu["q_idx"]), f64(cpu["k_idx"]),
+                                           cpu["cu_seqlens"].numpy(), toks))
 
 
 @pytest.mark.parametrize("n_init", [1, 3])
@@ -210,7 +219,10 @@ def test_index_select_init_rule(m, n_init):
         osel, gap = O.index_select(f64(cpu["q_idx"]), f64(cpu["k_idx"]),
                                    cpu["cu_seqlens"].numpy(), tokens=toks, n_init=n_init)
         g = sel.cpu().numpy() if toks is None else sel.cpu().numpy()[toks]
-        compare_selection(g, osel, gap, f"{name} n_init={n_init}")
+        rows = np.arange(shape.T) if toks is None else toks
+        compare_selection(g, osel, gap, f"{name} n_init={n_init}", own_blocks(cpu, rows),
+                          SC.prefill_scores_of(f64(cpu["q_idx"]), f64(cpu["k_idx"]),
+                                               cpu["cu_seqlens"].numpy(), rows), n_init=n_init)
         pos = O.positions(cpu["cu_seqlens"].numpy())
         own = (pos if toks is None else pos[toks]) // 128
         for i in range(n_init):
@@ -356,7 +368,9 @@ def _decode_check(m, shape, seed, rows=None, n_init=0):
     ro, rsel, rgap = O.decode_step(f64(x["q"][rows]), f64(x["q_idx"][rows]), kc, vc, ic,
                                    sub_table, lens[rows], SCALE, n_init=n_init)
     gsel = sel.cpu().numpy()[rows]
-    compare_selection(gsel, rsel, rgap, shape.name)
+    compare_selection(gsel, rsel, rgap, shape.name, (lens[rows] - 1) // 128,
+                      SC.decode_scores_of(f64(x["q_idx"][rows]), ic, sub_table, lens[rows]),
+                      n_init=n_init)
     same = np.all(np.all(gsel == rsel, axis=-1), axis=-1)
     assert same.mean() > 0.5
     assert_close(f64(o)[rows][same], ro[same], 2e-2, 1e-2, f"{shape.name} o")
@@ -457,7 +471,8 @@ def test_decode_append_then_step(m):
     ro, rsel, rgap = O.decode_step(f64(q_out), f64(qi_out), f64(g["k_cache"]), f64(g["v_cache"]),
                                    f64(g["kidx_cache"]), table, lens, SCALE)
     gsel = sel.cpu().numpy()
-    compare_selection(gsel, rsel, rgap, shape.name)
+    compare_selection(gsel, rsel, rgap, shape.name, (lens - 1) // 128,
+                      SC.decode_scores_of(f64(qi_out), f64(g["kidx_cache"]), table, lens))
     same = np.all(np.all(gsel == rsel, axis=-1), axis=-1)
     assert_close(f64(o)[same], ro[same], 2e-2, 1e-2, "decode after append")
 
@@ -481,7 +496,8 @@ def test_prefill_pipeline_tiny(m):
     pki = O.qk_norm_rope(f64(cpu["k_idx"]), f64(cpu["w_ki"]), cun)
     osel, gap = O.index_select(pqi, pki, cun)
     gsel = sel.cpu().numpy()
-    ndiff, nnear = compare_selection(gsel, osel, gap, "pipeline")
+    ndiff, nnear = compare_selection(gsel, osel, gap, "pipeline", own_blocks(cpu),
+                                     SC.prefill_scores_of(pqi, pki, cun, np.arange(shape.T)))
     rows = np.nonzero(np.all(gsel == osel, axis=(1, 2)))[0]
     oo, olse = O.sparse_attn_fwd(pq, pk, f64(cpu["v"]), osel, cun, SCALE, tokens=rows)
     assert_close(f64(o)[rows], oo, 2e-2, 1e-2, "pipeline o")

@@ -49,6 +49,35 @@ def _select_init_rescored(scores, own, topk=O.TOPK, n_init=0):
     return sel, np.full(n, np.inf)
 
 
+def _gap_variant(scores, own, topk, n_init, shift, denom):
+    """select_from_scores with its near-tie gap taken between scored candidates
+    `slots - 1 + shift` and `slots + shift`, relative to `denom` of the two."""
+    sel, _ = _ORIG["select_from_scores"](scores, own, topk, n_init)
+    gap = np.full(scores.shape[0], np.inf)
+    for r in range(scores.shape[0]):
+        o = int(own[r])
+        ni = min(n_init, o)
+        slots = topk - 1 - ni
+        cand = np.arange(ni, o)
+        order = cand[np.lexsort((cand, -scores[r, ni:o]))] if o > ni else cand
+        i = slots - 1 + shift
+        if slots > 0 and 0 <= i and i + 1 < len(order):
+            a, b = scores[r, order[i]], scores[r, order[i + 1]]
+            den = denom(abs(a), abs(b))
+            gap[r] = abs(a - b) / den if den > 0 else 0.0
+    return sel, gap
+
+
+def _gap_one_past_the_cut(scores, own, topk=O.TOPK, n_init=0):
+    # off by one toward the dropped side: first dropped vs second dropped
+    return _gap_variant(scores, own, topk, n_init, 1, max)
+
+
+def _gap_min_denominator(scores, own, topk=O.TOPK, n_init=0):
+    # divides by the smaller magnitude of the two
+    return _gap_variant(scores, own, topk, n_init, 0, min)
+
+
 def _select_own_not_forced(scores, own, topk=O.TOPK, n_init=0):
     n = scores.shape[0]
     sel = np.full((n, topk), -1, dtype=np.int64)
@@ -140,6 +169,8 @@ MUTATIONS = [
     ("select_from_scores", _select_higher_id_on_tie, [P.test_selection_tie_prefers_lower_block]),
     ("select_from_scores", _select_own_not_forced, [P.test_selection_invariants]),
     ("select_from_scores", _select_init_rescored, [P.test_init_rule_by_enumeration]),
+    ("select_from_scores", _gap_one_past_the_cut, [P.test_near_tie_gap_exact_values]),
+    ("select_from_scores", _gap_min_denominator, [P.test_near_tie_gap_exact_values]),
     ("_keys_of", _keys_one_past_causal,
      [P.test_sparse_forward_and_backward_match_masked_library_attention]),
     ("_keys_of", _keys_ignore_selection,

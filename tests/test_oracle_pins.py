@@ -328,6 +328,66 @@ def test_selection_tie_prefers_lower_block():
     assert gap[0] == 0.0
 
 
+def test_near_tie_gap_exact_values():
+    """The near-tie gap compares the last kept scored block with the first
+    dropped one, relative to the larger magnitude of the two (the parity rule:
+    rows whose cut straddles scores within 1e-3 relative are near-ties;
+    "[1/4] Add MiniMax-M3 support - #4581", Kernel tuning, and
+    "MiniMax-M3.1-Flash", 5.4 Notable quirks: selections differ only at
+    near-ties).  Hand-chosen distinct scores, values worked out by hand:
+
+      top-4 (own + 3 scored), earlier scores 9, 7, 5, 4.99, 1 (own block 5):
+        kept 9, 7, 5; first dropped 4.99; gap = 0.01 / 5
+      same with negative scores -1, -2, -3, -3.001, -10:
+        kept -1, -2, -3; first dropped -3.001; gap = 0.001 / 3.001
+      the scored order need not follow block ids: 4.99 at block 0, 9 at block 4
+      top-16 on 20 earlier blocks with scores 20 - b (b = 0..19), block 14 at
+      5.5 and block 15 at 5.4945: kept blocks 0..13 and 14; first dropped 15;
+      gap = 0.0055 / 5.5 = 1e-3 exactly at the boundary (not a near-tie)."""
+    own = np.array([5])
+    sel, gap = O.select_from_scores(np.array([[9.0, 7.0, 5.0, 4.99, 1.0, 0.0]]), own, topk=4)
+    assert list(sel[0]) == [0, 1, 2, 5]
+    assert gap[0] == pytest.approx(0.01 / 5.0, rel=1e-9)
+
+    sel, gap = O.select_from_scores(np.array([[-1.0, -2.0, -3.0, -3.001, -10.0, 0.0]]), own,
+                                    topk=4)
+    assert list(sel[0]) == [0, 1, 2, 5]
+    assert gap[0] == pytest.approx(0.001 / 3.001, rel=1e-9)
+
+    sel, gap = O.select_from_scores(np.array([[4.99, 7.0, 1.0, 5.0, 9.0, 0.0]]), own, topk=4)
+    assert list(sel[0]) == [1, 3, 4, 5]
+    assert gap[0] == pytest.approx(0.01 / 5.0, rel=1e-9)
+
+    sc = np.concatenate([20.0 - np.arange(20), [0.0]])
+    sc[14], sc[15] = 5.5, 5.4945
+    sel, gap = O.select_from_scores(sc[None, :], np.array([20]), topk=16)
+    assert list(sel[0]) == list(range(15)) + [20]
+    assert gap[0] == pytest.approx(0.0055 / 5.5, rel=1e-9)
+    assert not (gap[0] < O.NEAR_TIE_REL * (1 - 1e-9))
+
+
+def test_near_tie_gap_through_index_select():
+    """The gap that index_select reports for a row is the one its block scores
+    give: one sequence of 6 blocks of 4 keys (block 4, top-4), index keys built
+    so that every block's maximum logit is a chosen value (one key per block
+    along the query direction, the others orthogonal and smaller)."""
+    D, blk = 8, 4
+    q = np.zeros(D)
+    q[0] = 1.0
+    want = [9.0, 5.0, 7.0, 4.999, 1.0]                 # earlier blocks 0..4
+    keys = np.zeros((24, D))
+    for b, s in enumerate(want + [0.5]):
+        keys[b * blk, 0] = s                           # logit s
+        keys[b * blk + 1:(b + 1) * blk, 1] = 3.0       # logit 0, never the max here
+    qi = np.zeros((24, 1, D))
+    qi[:, 0] = q
+    ki = keys[:, None, :]
+    sel, gap = O.index_select(qi, ki, np.array([0, 24]), topk=4, block=blk)
+    assert list(sel[23, 0]) == [0, 1, 2, 5]
+    assert gap[23, 0] == pytest.approx((5.0 - 4.999) / 5.0, rel=1e-9)
+    assert gap[23, 0] < O.NEAR_TIE_REL
+
+
 def _small_pack(seed, seqlens, hi=2, d=32):
     r = rng(seed)
     T = sum(seqlens)
