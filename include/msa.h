@@ -322,7 +322,10 @@ MSA_API msa_status_t msa_decode_append(const void* q, const void* q_idx, const v
  * The call allocates nothing: no cudaMalloc, no cudaFree, no allocating
  * library routine.  Its first call on a device looks up that device's copy
  * of the array (a host-side query, done with the device current); make that
- * first call before any stream capture.  All calls share the one array, so
+ * first call before any stream capture.  The address is kept per CUDA
+ * context (keyed by the context's process-unique id), so after
+ * cudaDeviceReset the first call in the new context looks it up again, and
+ * that call too should come before any capture.  All calls share the one array, so
  * two calls whose kernels may overlap on the GPU (different streams, no
  * ordering between them) race and corrupt each other's results; calls on one
  * stream are safe.  Every scratch element a call reads is written earlier in

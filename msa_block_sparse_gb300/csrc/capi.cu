@@ -45,16 +45,74 @@ msa_status_t check_launch(const char* what) {
 // (x + y << 20), [3] its thread
 __device__ uint32_t g_device_status[4];
 
-uint32_t* status_word() {
-  static uint32_t* ptrs[64] = {nullptr};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
-  if (!ptrs[dev]) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_device_status) != cudaSuccess) return nullptr;
-    ptrs[dev] = static_cast<uint32_t*>(p);
+namespace {
+
+template <class F>
+F driver_fn(const char* name, unsigned int version) {
+  void* p = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion(name, &p, version, cudaEnableDefault, &q) != cudaSuccess ||
+      q != cudaDriverEntryPointSuccess)
+    return nullptr;
+  return reinterpret_cast<F>(p);
+}
+
+}  // namespace
+
+// Process-unique id of the calling thread's current context (0 if none).
+msa_status_t current_context_id(unsigned long long* id) {
+  static PFN_cuCtxGetCurrent_v4000 get_current = nullptr;
+  static PFN_cuCtxGetId_v12000 get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    get_current = driver_fn<PFN_cuCtxGetCurrent_v4000>("cuCtxGetCurrent", 4000);
+    get_id = driver_fn<PFN_cuCtxGetId_v12000>("cuCtxGetId", 12000);
+  });
+  if (!get_current || !get_id) return fail(MSA_ERR_CUDA, "cuCtxGetCurrent / cuCtxGetId unavailable");
+  CUcontext ctx = nullptr;
+  if (get_current(&ctx) != CUDA_SUCCESS) return fail(MSA_ERR_CUDA, "cuCtxGetCurrent failed");
+  *id = 0;
+  if (ctx && get_id(ctx, id) != CUDA_SUCCESS) return fail(MSA_ERR_CUDA, "cuCtxGetId failed");
+  return MSA_OK;
+}
+
+namespace {
+
+std::mutex g_symbol_mu;
+std::map<std::pair<const void*, unsigned long long>, void*> g_symbol_cache;
+
+}  // namespace
+
+msa_status_t symbol_address(const void* symbol, const char* what, void** out) {
+  unsigned long long ctx = 0;
+  msa_status_t st = current_context_id(&ctx);
+  if (st != MSA_OK) return st;
+  std::lock_guard<std::mutex> lk(g_symbol_mu);
+  if (ctx != 0) {
+    auto it = g_symbol_cache.find(std::make_pair(symbol, ctx));
+    if (it != g_symbol_cache.end()) {
+      *out = it->second;
+      return MSA_OK;
+    }
   }
-  return ptrs[dev];
+  void* p = nullptr;
+  cudaError_t e = cudaGetSymbolAddress(&p, symbol);   // makes the primary context current if none is
+  if (e != cudaSuccess || p == nullptr)
+    return fail(MSA_ERR_CUDA, "cudaGetSymbolAddress(%s): %s", what, cudaGetErrorString(e));
+  if (ctx == 0) {
+    st = current_context_id(&ctx);
+    if (st != MSA_OK) return st;
+  }
+  if (ctx != 0) g_symbol_cache[std::make_pair(symbol, ctx)] = p;
+  *out = p;
+  return MSA_OK;
+}
+
+msa_status_t status_word(uint32_t** out) {
+  void* p = nullptr;
+  msa_status_t st = symbol_address(&g_device_status, "status word", &p);
+  *out = static_cast<uint32_t*>(p);
+  return st;
 }
 
 // ------------------------------------------------------------------ device
@@ -250,10 +308,12 @@ msa_status_t launch_plan(const Plan& plan, const int32_t* cu_seqlens, int S, int
                          cudaStream_t stream) {
   int max_nb = (max_seqlen + plan.tile - 1) / plan.tile;
   size_t smem = 2 * (max_nb + 1) * sizeof(int);
+  uint32_t* sw = nullptr;
+  if (msa_status_t e = status_word(&sw); e != MSA_OK) return e;
   {
     TraceScope trace_("plan_kernel", stream);
     launch_pdl(plan_kernel, 1, 1024, smem, stream, cu_seqlens, S, plan.tile, max_nb, plan.tiles,
-        plan.num_tiles, plan.max_tiles, status_word());
+        plan.num_tiles, plan.max_tiles, sw);
   }
   return check_launch("plan_kernel");
 }
@@ -342,8 +402,8 @@ const char* msa_last_error(void) { return g_last_error; }
 msa_status_t msa_check_status(msa_stream_t stream) {
   cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail(MSA_ERR_CUDA, "stream sync: %s", cudaGetErrorString(e));
-  uint32_t* sw = status_word();
-  if (!sw) return fail(MSA_ERR_CUDA, "status word unavailable");
+  uint32_t* sw = nullptr;
+  if (msa_status_t st = status_word(&sw); st != MSA_OK) return st;
   uint32_t v[4] = {0, 0, 0, 0};
   e = cudaMemcpy(v, sw, sizeof(v), cudaMemcpyDeviceToHost);
   if (e == cudaSuccess) e = cudaMemset(sw, 0, sizeof(v));
@@ -371,9 +431,11 @@ __global__ void selftest_wait_kernel(uint32_t* status) {
 
 msa_status_t msa_selftest_wait(msa_stream_t stream) {
   cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint32_t* sw = nullptr;
+  if (msa_status_t e = status_word(&sw); e != MSA_OK) return e;
   {
     TraceScope trace_("selftest_wait_kernel", st);
-    launch_pdl(selftest_wait_kernel, 1, 32, 0, st, status_word());
+    launch_pdl(selftest_wait_kernel, 1, 32, 0, st, sw);
   }
   return check_launch("selftest_wait_kernel");
 }

@@ -24,8 +24,20 @@ void set_error(const char* fmt, ...);
 msa_status_t fail(msa_status_t code, const char* fmt, ...);
 msa_status_t check_launch(const char* what);
 
-// Address of the device status word on the current device.
-uint32_t* status_word();
+// Process-unique id (cuCtxGetId) of the calling thread's current CUDA
+// context, 0 when none is current.
+msa_status_t current_context_id(unsigned long long* id);
+
+// Device address of a file-scope __device__ variable (given by its host-side
+// stand-in `symbol`) in the calling thread's current CUDA context, looked up
+// with cudaGetSymbolAddress once per (variable, context) and cached.  The key
+// is the context's process-unique id (cuCtxGetId), so a context created after
+// cudaDeviceReset gets its own lookup instead of a stale address.
+msa_status_t symbol_address(const void* symbol, const char* what, void** out);
+
+// Address of the device status word in the current context; MSA_ERR_CUDA
+// (nothing enqueued) when it cannot be had.
+msa_status_t status_word(uint32_t** out);
 
 // Brackets one kernel launch with CUDA events on `stream` while tracing is on
 // (msa_trace_begin / msa_trace_end); does nothing otherwise.

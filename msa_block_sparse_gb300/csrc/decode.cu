@@ -492,7 +492,8 @@ msa_status_t launch_decode(const void* q, const void* q_idx, const void* k_cache
                            int Hkv, int num_pages, int max_pages, float scale, int n_init,
                            void* o, int32_t* sel_out, const DecodeWorkspace& ws,
                            cudaStream_t stream) {
-  uint32_t* st = status_word();
+  uint32_t* st = nullptr;
+  if (msa_status_t e_ = status_word(&st); e_ != MSA_OK) return e_;
   dim3 g1((max_pages + kPagesPerCta - 1) / kPagesPerCta, B);
   {
     TraceScope trace_("decode_score_kernel", stream);
@@ -547,6 +548,7 @@ msa_status_t launch_decode(const void* q, const void* q_idx, const void* k_cache
 // caller workspace; the kernels and their launch sequence are those of
 // msa_decode_step.
 
+#include <map>
 #include <mutex>
 
 namespace msa {
@@ -567,25 +569,35 @@ static __device__ __align__(256) float g_decode_scratch[kStaticScores + kStaticS
                                                         kStaticPartO + kStaticPartMl];
 
 std::mutex g_static_mu;
-float* g_static_ptr[64] = {nullptr};
+std::map<unsigned long long, float*> g_static_ptr;   // context id -> device address
 
-// Device address of g_decode_scratch on the current device, looked up once
-// per device (with that device current) and cached.
+// Device address of g_decode_scratch in the calling thread's current context.
+// Looked up with cudaGetSymbolAddress on the first call in each context (so
+// once per device, with that device current) and cached under the context's
+// process-unique id: a context made after cudaDeviceReset, whose module may
+// sit at another address, gets a fresh lookup instead of the stale one.
 msa_status_t static_scratch(float** out) {
-  int dev = -1;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return fail(MSA_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
-  if (dev < 0 || dev >= 64) return fail(MSA_ERR_UNSUPPORTED, "device index %d above 63", dev);
+  unsigned long long ctx = 0;
+  msa_status_t st = current_context_id(&ctx);
+  if (st != MSA_OK) return st;
   std::lock_guard<std::mutex> lk(g_static_mu);
-  if (!g_static_ptr[dev]) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_decode_scratch);
-    if (e != cudaSuccess || p == nullptr)
-      return fail(MSA_ERR_CUDA, "cudaGetSymbolAddress(decode scratch): %s",
-                  cudaGetErrorString(e));
-    g_static_ptr[dev] = static_cast<float*>(p);
+  if (ctx != 0) {
+    auto it = g_static_ptr.find(ctx);
+    if (it != g_static_ptr.end()) {
+      *out = it->second;
+      return MSA_OK;
+    }
   }
-  *out = g_static_ptr[dev];
+  void* p = nullptr;
+  cudaError_t e = cudaGetSymbolAddress(&p, g_decode_scratch);
+  if (e != cudaSuccess || p == nullptr)
+    return fail(MSA_ERR_CUDA, "cudaGetSymbolAddress(decode scratch): %s", cudaGetErrorString(e));
+  if (ctx == 0) {                 // the lookup made the device's primary context current
+    st = current_context_id(&ctx);
+    if (st != MSA_OK) return st;
+  }
+  if (ctx != 0) g_static_ptr[ctx] = static_cast<float*>(p);
+  *out = static_cast<float*>(p);
   return MSA_OK;
 }
 

@@ -235,11 +235,13 @@ msa_status_t launch_index_select(const void* q_idx, const void* k_idx, const int
     const msa_status_t e = ensure_smem(index_select_kernel, smem, "index_select_kernel");
     if (e != MSA_OK) return e;
   }
+  uint32_t* sw = nullptr;
+  if (msa_status_t e_ = status_word(&sw); e_ != MSA_OK) return e_;
   dim3 grid(plan.max_tiles, Hi);
   {
     TraceScope trace_("index_select_kernel", stream);
     launch_pdl(index_select_kernel, grid, kSelThreads, smem, stream, tq, tk, cu, plan.tiles,
-        plan.num_tiles, Hi, n_init, sel, status_word());
+        plan.num_tiles, Hi, n_init, sel, sw);
   }
   return check_launch("index_select_kernel");
 }

@@ -222,11 +222,13 @@ msa_status_t launch_prologue(const PrologueJob* jobs, int njobs, const int32_t* 
     double f = std::pow(static_cast<double>(rope_base), -2.0 * i / kRopeDim);
     turns.f[i] = static_cast<unsigned long long>(f / two_pi * 18446744073709551616.0);
   }
+  uint32_t* sw = nullptr;
+  if (msa_status_t e_ = status_word(&sw); e_ != MSA_OK) return e_;
   dim3 grid((T + kProTokens - 1) / kProTokens);
   {
     TraceScope trace_("prologue_kernel", stream);
     launch_pdl(prologue_kernel, grid, kPfThreads, 0, stream, args, turns, cu, S, T, eps,
-        status_word());
+        sw);
   }
   return check_launch("prologue_kernel");
 }
@@ -639,12 +641,14 @@ msa_status_t launch_decode_append(const DecodeAppendJob& j, const int32_t* block
     double f = std::pow(static_cast<double>(rope_base), -2.0 * i / kRopeDim);
     turns.f[i] = static_cast<unsigned long long>(f / two_pi * 18446744073709551616.0);
   }
+  uint32_t* sw = nullptr;
+  if (msa_status_t e_ = status_word(&sw); e_ != MSA_OK) return e_;
   {
     TraceScope trace_("decode_append_kernel", stream);
     dim3 grid(B, (j.Hq + 4 * j.Hkv + kProSlots - 1) / kProSlots);
     launch_pdl(decode_append_kernel, grid, kProThreads, 0, stream, a, turns, block_table, cache_lens,
         num_pages, max_pages, eps,
-        status_word());
+        sw);
   }
   return check_launch("decode_append_kernel");
 }

@@ -1384,10 +1384,12 @@ static msa_status_t launch_qsa_tilemap(const int32_t* sel, const int32_t* cu, in
                                        int Hkv, int topk, int max_seqlen,
                                        const QsaFwdWorkspace& fw, cudaStream_t stream) {
   const int sms = device_sm_count();
+  uint32_t* sw = nullptr;
+  if (msa_status_t e_ = status_word(&sw); e_ != MSA_OK) return e_;
   {
     TraceScope trace_("qsa_mask_kernel", stream);
     launch_pdl(qsa_mask_kernel, capped_blocks(static_cast<size_t>(T) * Hkv, 8, 8 * sms), 256, 0,
-        stream, sel, cu, S, T, Hkv, topk, fw.W, fw.masks, status_word());
+        stream, sel, cu, S, T, Hkv, topk, fw.W, fw.masks, sw);
   }
   QSA_TRY(check_launch("qsa_mask_kernel"));
   QSA_TRY(launch_plan(fw.plan, cu, S, max_seqlen, stream));
@@ -1396,7 +1398,7 @@ static msa_status_t launch_qsa_tilemap(const int32_t* sel, const int32_t* cu, in
     launch_pdl(qsa_union_kernel,
         capped_blocks(static_cast<size_t>(fw.plan.max_tiles) * Hkv, 8, 4 * sms), 256, 0, stream,
         fw.masks, fw.W, cu, fw.plan.tiles, fw.plan.num_tiles, Hkv, fw.ustride, fw.ulist,
-        fw.tile_ctr, status_word());
+        fw.tile_ctr, sw);
   }
   return check_launch("qsa_union_kernel");
 }
@@ -1424,6 +1426,8 @@ msa_status_t launch_qsa_fwd(const void* q, const void* k, const void* v, const i
   CUtensorMap tq, tk, tv;
   if (!qsa_maps(q, k, v, nullptr, T, Hq, Hkv, &tq, &tk, &tv, nullptr))
     return fail(MSA_ERR_CUDA, "cuTensorMapEncodeTiled failed for the narrow-block q/k/v");
+  uint32_t* sw = nullptr;
+  if (msa_status_t e_ = status_word(&sw); e_ != MSA_OK) return e_;
   QSA_TRY(launch_qsa_tilemap(sel, cu, S, T, Hkv, topk, max_seqlen, fw, stream));
   const size_t smem = sizeof(QsaFwdSmem) + 1024;
   QSA_TRY(ensure_smem(qsa_fwd_kernel, smem, "qsa_fwd_kernel"));
@@ -1434,7 +1438,7 @@ msa_status_t launch_qsa_fwd(const void* q, const void* k, const void* v, const i
     TraceScope trace_("qsa_fwd_kernel", stream);
     launch_pdl(qsa_fwd_kernel, grid, kQFwdThreads, smem, stream, tq, tk, tv, fw.masks, fw.W,
         fw.ulist, fw.ustride, cu, fw.plan.tiles, fw.plan.num_tiles, Hq, Hkv, scale,
-        static_cast<__nv_bfloat16*>(o), lse, fw.tile_ctr, status_word());
+        static_cast<__nv_bfloat16*>(o), lse, fw.tile_ctr, sw);
   }
   return check_launch("qsa_fwd_kernel");
 }
@@ -1450,6 +1454,8 @@ msa_status_t launch_qsa_bwd(const void* q, const void* k, const void* v, const v
   CUtensorMap tq, tk, tv, tdo;
   if (!qsa_maps(q, k, v, dout, T, Hq, Hkv, &tq, &tk, &tv, &tdo))
     return fail(MSA_ERR_CUDA, "cuTensorMapEncodeTiled failed for the narrow-block backward");
+  uint32_t* sw = nullptr;
+  if (msa_status_t e_ = status_word(&sw); e_ != MSA_OK) return e_;
   const int sms = device_sm_count();
   const QsaFwdWorkspace& fw = w.map;
   QSA_TRY(launch_qsa_tilemap(sel, cu, S, T, Hkv, topk, max_seqlen, fw, stream));
@@ -1468,7 +1474,7 @@ msa_status_t launch_qsa_bwd(const void* q, const void* k, const void* v, const v
   {
     TraceScope trace_("qsa_items_kernel", stream);
     launch_pdl(qsa_items_kernel, 1, 1024, 0, stream, cu, S, w.items, w.num_items, w.max_items,
-        status_word());
+        sw);
   }
   {
     TraceScope trace_("qsa_kvlist_kernel", stream);
@@ -1491,7 +1497,7 @@ msa_status_t launch_qsa_bwd(const void* q, const void* k, const void* v, const v
     TraceScope trace_("qsa_bwd_dq_kernel", stream);
     launch_pdl(qsa_bwd_dq_kernel, grid, kQBwdThreads, smem_dq, stream, tq, tdo, tk, tv,
         fw.masks, fw.W, fw.ulist, fw.ustride, w.lsd, cu, fw.plan.tiles, fw.plan.num_tiles, Hq,
-        Hkv, scale, static_cast<__nv_bfloat16*>(dq), w.map.tile_ctr, status_word());
+        Hkv, scale, static_cast<__nv_bfloat16*>(dq), w.map.tile_ctr, sw);
   }
   QSA_TRY(check_launch("qsa_bwd_dq_kernel"));
 
@@ -1502,7 +1508,7 @@ msa_status_t launch_qsa_bwd(const void* q, const void* k, const void* v, const v
     TraceScope trace_("qsa_bwd_dkv_kernel", stream);
     launch_pdl(qsa_bwd_dkv_kernel, grid, kQBwdThreads, smem_kv, stream, tq, tdo, tk, tv,
         fw.masks, fw.W, w.klist, w.lsd, cu, w.items, w.order, w.num_busy, w.max_items, Hq, Hkv,
-        scale, w.dk_acc, w.dv_acc, w.item_ctr, status_word());
+        scale, w.dk_acc, w.dv_acc, w.item_ctr, sw);
   }
   QSA_TRY(check_launch("qsa_bwd_dkv_kernel"));
   {

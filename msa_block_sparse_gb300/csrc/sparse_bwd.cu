@@ -839,7 +839,8 @@ msa_status_t launch_sparse_bwd(const void* q, const void* k, const void* v, cons
       !make_tmap_bf16_strided(&tdo, dout, 5, dq5, sq5, bq5) ||
       !make_tmap_bf16(&tk, k, 3, dkv3, bkv) || !make_tmap_bf16(&tv, v, 3, dkv3, bkv))
     return fail(MSA_ERR_CUDA, "cuTensorMapEncodeTiled failed for the backward");
-  uint32_t* st = status_word();
+  uint32_t* st = nullptr;
+  if (msa_status_t e_ = status_word(&st); e_ != MSA_OK) return e_;
 
   const size_t nq = static_cast<size_t>(T) * Hq * kD;
   const size_t nkv = static_cast<size_t>(T) * Hkv * kD;

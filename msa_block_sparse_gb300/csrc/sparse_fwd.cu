@@ -739,6 +739,8 @@ msa_status_t launch_sparse_fwd(const void* q, const void* k, const void* v, cons
   const int per_head = (device_sm_count() + Hkv - 1) / Hkv;
   const int max_ctas = plan.max_tiles * kG;
   dim3 grid(static_cast<unsigned>(per_head < max_ctas ? per_head : max_ctas), Hkv);
+  uint32_t* sw = nullptr;
+  if (msa_status_t e_ = status_word(&sw); e_ != MSA_OK) return e_;
   {
     // one CTA per (128-token query block, KV head): the one-warp grouping over
     // whole blocks when sequences are long enough for its better tiles to
@@ -749,13 +751,13 @@ msa_status_t launch_sparse_fwd(const void* q, const void* k, const void* v, cons
     const bool whole = max_seqlen >= 8192;
     TraceScope trace_("fwd_union_kernel", stream);
     launch_pdl(whole ? fwd_union_kernel<1> : fwd_union_kernel<2>, ugrid, whole ? 32 : 64, 0, stream, sel, cu, plan.tiles, plan.num_tiles, Hkv,
-        fw.ulist, fw.tile_ctr, status_word());
+        fw.ulist, fw.tile_ctr, sw);
   }
   {
     TraceScope trace_("sparse_fwd_kernel", stream);
     launch_pdl(sparse_fwd_kernel, grid, kFwdThreads, smem, stream,
         tq, tk, tv, to, fw.ulist, fw.tile_ctr, cu, plan.tiles, plan.num_tiles, Hq, Hkv, scale,
-        static_cast<__nv_bfloat16*>(o), lse, status_word());
+        static_cast<__nv_bfloat16*>(o), lse, sw);
   }
   return check_launch("sparse_fwd_kernel");
 }

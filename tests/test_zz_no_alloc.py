@@ -15,6 +15,8 @@ import pytest
 import torch
 
 import workloads as W
+from oracle import msa_oracle as O
+from tests import selection_check as SC
 
 pytestmark = pytest.mark.gpu
 
@@ -67,6 +69,25 @@ def test_static_decode_matches_workspace_decode_twice(m, shape):
         m.msa_check_status()
         assert torch.equal(sel, ref_sel)
         _check_close(o, ref_o)
+    if shape.B <= 8:
+        # and against the oracle directly: selections by the near-tie rule,
+        # o on the rows whose selection agrees
+        f64 = lambda t: t.float().cpu().double().numpy()    # noqa: E731
+        lens = x["cache_lens"].cpu().numpy()
+        table = x["block_table"].cpu().numpy()
+        ro, rsel, rgap = O.decode_step(f64(x["q"]), f64(x["q_idx"]), f64(x["k_cache"]),
+                                       f64(x["v_cache"]), f64(x["kidx_cache"]), table, lens,
+                                       1.0 / math.sqrt(128))
+        gsel = sel.cpu().numpy()
+        SC.check_selection(gsel, rsel, rgap, (lens - 1) // 128,
+                           SC.decode_scores_of(f64(x["q_idx"]), f64(x["kidx_cache"]), table, lens),
+                           "static decode")
+        same = np.all(np.all(gsel == rsel, axis=-1), axis=-1)
+        assert same.any()
+        g = f64(o)[same]
+        err = float(np.max(np.abs(g - ro[same])))
+        rel = float(np.linalg.norm(g - ro[same]) / np.linalg.norm(ro[same]))
+        assert err <= 2e-2 and rel <= 1e-2, (err, rel)
 
 
 def test_static_decode_rejects_sizes_beyond_its_scratch(m):
