@@ -133,18 +133,44 @@ def test_prologue_matches_oracle(m, name):
     assert torch.equal(q1, q) and torch.equal(k2, k)
     cun = cpu["cu_seqlens"].numpy()
     for got, n, wn in ((q, "q", "w_q"), (k, "k", "w_k"), (qi, "q_idx", "w_qi"), (ki, "k_idx", "w_ki")):
-        want = O.qk_norm_rope(f64(cpu[n]), f64(cpu[wn]), cun)
-        g = f64(got)
-        off = np.abs(g - want)
-        # fp32 evaluation leaves an absolute error of a few 2^-24 of the row's
-        # magnitude before the bf16 rounding (cancellation in the rotation makes
-        # it large relative to small outputs); then rounding may land one step off.
-        row_scale = np.max(np.abs(want), axis=-1, keepdims=True)
-        tol = bf16_step(want) * 1.0001 + 1e-5 * row_scale
-        worst = float(np.max(off - tol))
-        assert worst <= 0, f"{n}: {int(np.sum(off > tol))} elements beyond tolerance, " \
-                           f"worst excess {worst:.3e}, max off {float(off.max()):.3e}"
-        assert np.mean(off > 0) < 0.01, f"{n}: {np.mean(off > 0):.4f} of elements off by a step"
+        assert_prologue_close(f64(got), O.qk_norm_rope(f64(cpu[n]), f64(cpu[wn]), cun), n)
+
+
+def assert_prologue_close(g, want, n):
+    """Each bf16 output within one bf16 step of the oracle's bf16 value: fp32
+    evaluation leaves an absolute error of a few 2^-24 of the row's magnitude
+    before the rounding (cancellation in the rotation makes it large relative
+    to small outputs), and the rounding may then land one step off; fewer
+    than 1% of the elements may be off."""
+    off = np.abs(g - want)
+    row_scale = np.max(np.abs(want), axis=-1, keepdims=True)
+    tol = bf16_step(want) * 1.0001 + 1e-5 * row_scale
+    worst = float(np.max(off - tol))
+    assert worst <= 0, f"{n}: {int(np.sum(off > tol))} elements beyond tolerance, " \
+                       f"worst excess {worst:.3e}, max off {float(off.max()):.3e}"
+    assert np.mean(off > 0) < 0.01, f"{n}: {np.mean(off > 0):.4f} of elements off by a step"
+
+
+def oracle_prologue_rows(cpu, name, wname, tokens):
+    """The oracle's prologue (gemma norm, partial RoPE at each token's position,
+    bf16 storage) of the given packed rows only: the prologue acts row by row."""
+    pos = O.positions(cpu["cu_seqlens"].numpy())[tokens]
+    x = f64(cpu[name][tokens])
+    return O.bf16_round(O.partial_rope(O.gemma_rmsnorm(x, f64(cpu[wname])), pos))
+
+
+def test_prologue_full_size_sampled(m):
+    """The four prologue outputs of the full layer shape (64 q / 4 kv / 4 index
+    heads, 16k pack of 8 sequences) on sampled rows of every sequence."""
+    shape = W.config(2)
+    cpu, gpu = inputs("cfg2", shape)
+    q, k, qi, ki = m.msa_qk_norm_rope4(gpu["q"], gpu["k"], gpu["q_idx"], gpu["k_idx"],
+                                       gpu["w_q"], gpu["w_k"], gpu["w_qi"], gpu["w_ki"],
+                                       gpu["cu_seqlens"])
+    m.msa_check_status()
+    toks = sample_tokens(shape, n_random=512, seed=31)
+    for got, n, wn in ((q, "q", "w_q"), (k, "k", "w_k"), (qi, "q_idx", "w_qi"), (ki, "k_idx", "w_ki")):
+        assert_prologue_close(f64(got[toks]), oracle_prologue_rows(cpu, n, wn, toks), f"cfg2 {n}")
 
 
 @pytest.mark.parametrize("name", ["tiny", "ragged"])
@@ -315,8 +341,52 @@ def test_sparse_bwd_small(m, name):
         assert r <= 1e-2, f"{name} {n}: rel-L2 {r:.3e}"
 
 
+def bwd_sample_blocks(shape, seed):
+    """(sequence, KV head, block) triples whose dk/dv a full-size backward test
+    compares: for every sequence and KV head block 0 or 1 (selected by almost
+    every query of the sequence, so its work spans all 256-position windows),
+    one random block past them and the sequence's last block (partly causal,
+    claimed late from the largest-first tail)."""
+    r = np.random.default_rng(seed)
+    out = []
+    for s in range(shape.S):
+        nb = (shape.seqlens[s] + 127) // 128
+        for g in range(shape.hkv):
+            picks = {int(r.integers(0, min(2, nb))), nb - 1}
+            if nb > 3:
+                picks.add(int(r.integers(2, nb - 1)))
+            out += [(s, g, b) for b in sorted(picks)]
+    return out
+
+
+def check_bwd_sampled(cpu, dq, dk, dv, sel, shape, toks, blocks, what, q=None, k=None):
+    """dq on the sampled tokens and dk/dv of the sampled blocks against the
+    oracle's sampled backward (blocks computed in a spawned process pool)."""
+    from tests import oracle_pool
+    cun = cpu["cu_seqlens"].numpy()
+    qq = f64(cpu["q"]) if q is None else q
+    kk = f64(cpu["k"]) if k is None else k
+    vv, dd = f64(cpu["v"]), f64(cpu["do"])
+    ref = O.sparse_attn_bwd(qq, kk, vv, dd, sel, cun, SCALE, dq_tokens=toks)
+    r = rel_l2(f64(dq[toks]), ref["dq"])
+    assert r <= 1e-2, f"{what} dq rel-L2 {r:.3e}"
+    dkv = oracle_pool.dkv_blocks(qq, kk, vv, dd, sel, cun, SCALE, blocks)
+    worst = 0.0
+    for (s, g, b), (rk, rv) in zip(blocks, dkv):
+        k0 = int(cun[s]) + 128 * b
+        n = rk.shape[0]
+        rk_ = rel_l2(f64(dk[k0:k0 + n, g]), rk)
+        rv_ = rel_l2(f64(dv[k0:k0 + n, g]), rv)
+        worst = max(worst, rk_, rv_)
+        assert rk_ <= 1e-2 and rv_ <= 1e-2, f"{what} block {(s, g, b)}: dk {rk_:.3e} dv {rv_:.3e}"
+    print(f"{what}: dq on {len(toks)} tokens rel-L2 {r:.2e}; dk/dv on {len(blocks)} blocks, "
+          f"worst rel-L2 {worst:.2e}")
+
+
 @pytest.mark.parametrize("idx", [1, 4])
 def test_sparse_bwd_full_size(m, idx):
+    """Full-size backward with the oracle's selection: dq on >= 256 sampled
+    tokens, dk / dv on 2-3 blocks of every (sequence, KV head)."""
     shape = W.config(idx)
     cpu, gpu = inputs(f"cfg{idx}", shape)
     osel, _ = oracle_selection(f"cfg{idx}", shape, cpu)
@@ -326,21 +396,46 @@ def test_sparse_bwd_full_size(m, idx):
     dq, dk, dv = m.msa_sparse_attn_bwd(gpu["q"], gpu["k"], gpu["v"], o, gpu["do"], lse, sel, cu,
                                        shape.max_seqlen)
     m.msa_check_status()
-    toks = sample_tokens(shape, n_random=48, seed=20 + idx)
+    toks = sample_tokens(shape, n_random=256, seed=20 + idx)
+    blocks = bwd_sample_blocks(shape, seed=40 + idx)
+    assert len(toks) >= 256 and len(blocks) >= (12 if idx == 1 else 32)
+    check_bwd_sampled(cpu, dq, dk, dv, osel, shape, toks, blocks, f"cfg{idx}")
+
+
+def test_pipeline_full_size_sampled(m):
+    """The whole training step of the 16k pack (16 q / 1 kv / 1 index head) on
+    the GPU -- prologue, index select, forward, backward -- against the oracle
+    pipeline on sampled rows: prologue outputs, the selection (near-tie rule),
+    o and lse, dq, and dk / dv of sampled blocks.  The oracle's attention and
+    backward take the GPU's selection (validated on the sampled rows) and its
+    own prologue outputs."""
+    shape = W.config(1)
+    cpu, gpu = inputs("cfg1", shape)
+    cu = gpu["cu_seqlens"]
+    L = shape.max_seqlen
+    q, k, qi, ki = m.msa_qk_norm_rope4(gpu["q"], gpu["k"], gpu["q_idx"], gpu["k_idx"],
+                                       gpu["w_q"], gpu["w_k"], gpu["w_qi"], gpu["w_ki"], cu)
+    sel = m.msa_index_select(qi, ki, cu, L)
+    o, lse = m.msa_sparse_attn_fwd(q, k, gpu["v"], sel, cu, L)
+    dq, dk, dv = m.msa_sparse_attn_bwd(q, k, gpu["v"], o, gpu["do"], lse, sel, cu, L)
+    m.msa_check_status()
     cun = cpu["cu_seqlens"].numpy()
-    last = shape.S - 1
-    nb_last = (shape.seqlens[last] + 127) // 128
-    blocks = [(0, 0, 0), (last, shape.hkv - 1, nb_last - 1), (last, 0, nb_last // 2)]
-    ref = O.sparse_attn_bwd(f64(cpu["q"]), f64(cpu["k"]), f64(cpu["v"]), f64(cpu["do"]), osel, cun,
-                            SCALE, dq_tokens=toks, dkv_blocks=blocks)
-    r = rel_l2(f64(dq[toks]), ref["dq"])
-    assert r <= 1e-2, f"cfg{idx} dq rel-L2 {r:.3e}"
-    for (s, g, b), (rk, rv) in zip(blocks, ref["dkv"]):
-        k0 = int(cun[s]) + 128 * b
-        n = rk.shape[0]
-        rk_ = rel_l2(f64(dk[k0:k0 + n, g]), rk)
-        rv_ = rel_l2(f64(dv[k0:k0 + n, g]), rv)
-        assert rk_ <= 1e-2 and rv_ <= 1e-2, f"cfg{idx} block {(s, g, b)}: dk {rk_:.3e} dv {rv_:.3e}"
+    pq = O.qk_norm_rope(f64(cpu["q"]), f64(cpu["w_q"]), cun)
+    pk = O.qk_norm_rope(f64(cpu["k"]), f64(cpu["w_k"]), cun)
+    pqi = O.qk_norm_rope(f64(cpu["q_idx"]), f64(cpu["w_qi"]), cun)
+    pki = O.qk_norm_rope(f64(cpu["k_idx"]), f64(cpu["w_ki"]), cun)
+    toks = sample_tokens(shape, n_random=512, seed=51)
+    for got, want, n in ((q, pq, "q"), (k, pk, "k"), (qi, pqi, "q_idx"), (ki, pki, "k_idx")):
+        assert_prologue_close(f64(got[toks]), want[toks], f"pipeline {n}")
+    gsel = sel.cpu().numpy().astype(np.int64)
+    osel, gap = O.index_select(pqi, pki, cun, tokens=toks)
+    compare_selection(gsel[toks], osel, gap, "pipeline cfg1", own_blocks(cpu, toks),
+                      SC.prefill_scores_of(pqi, pki, cun, toks))
+    oo, olse = O.sparse_attn_fwd(pq, pk, f64(cpu["v"]), gsel, cun, SCALE, tokens=toks)
+    assert_close(f64(o[toks]), oo, 2e-2, 1e-2, "pipeline o")
+    assert_close(lse[toks].cpu().numpy().astype(np.float64), olse, 1e-3, 1e-4, "pipeline lse")
+    blocks = [(s, 0, b) for (s, _, b) in bwd_sample_blocks(shape, seed=52)]
+    check_bwd_sampled(cpu, dq, dk, dv, gsel, shape, toks, blocks, "pipeline cfg1", q=pq, k=pk)
 
 
 # ------------------------------------------------------------------ decode
