@@ -9,10 +9,13 @@ A step = msa_qk_norm_rope4 -> msa_index_select -> msa_sparse_attn_fwd ->
 msa_sparse_attn_bwd over one pack.  Each step reads its own copy of the
 inputs from a pool larger than L2, so every step starts L2-cold.
 
-Prints one JSON line.  Also measured in the same run: the decode step on the
-paged-cache workload (B = 64, 64 q / 4 kv heads), the end-to-end time through
-the public API with host buffers, the CPU oracle on a bounded sample, and
-per-kernel CUDA-event timings (library tracing) for the roofline.
+Prints one JSON line (kept short: summaries of every leg, numbers rounded;
+`--detail PATH` writes the full record to a file).  Also measured in the same
+run: the decode step on the paged-cache workload (B = 64, 64 q / 4 kv heads),
+the end-to-end time through the public API with host buffers, the other
+prefill workloads, the narrow-block variant, the CPU oracle on a bounded
+sample (one core and every host core) with a parity report of sampled rows,
+and per-kernel CUDA-event timings (library tracing) for the roofline.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 """
@@ -51,6 +54,11 @@ def parse():
     ap.add_argument("--no-qsa", action="store_true")
     ap.add_argument("--no-configs", action="store_true",
                     help="skip the 64-head 16k prefill and the 32k training pack")
+    ap.add_argument("--no-parity", action="store_true",
+                    help="skip the oracle comparison of sampled rows in the CPU leg")
+    ap.add_argument("--ref-budget-s", type=float, default=150.0,
+                    help="reference arm: seconds its warm-up + timed steps may take")
+    ap.add_argument("--detail", default=None, help="also write the full record here")
     return ap.parse_args()
 
 
@@ -137,35 +145,71 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+# ------------------------------------------------------------------ line helpers
+
+NOMINAL_BF16_TFLOPS = 2250.0      # GB300 dense bf16, datasheet (context only)
+NOMINAL_HBM_GBS = 8000.0          # GB300 HBM3e, about 8 TB/s (context only)
+
+
+def config_dict(shape, pool: int, world: int) -> dict:
+    """The workload the line is quoted on; both arms print the same dict."""
+    return {"workload": shape.name, "tokens": shape.T, "seqlens": list(shape.seqlens),
+            "hq": shape.hq, "hkv": shape.hkv, "hi": shape.hi, "d": 128, "block": 128,
+            "topk": 16,
+            "step": "qk_norm_rope4 + index_select + sparse_attn_fwd + sparse_attn_bwd",
+            "l2": f"inputs larger than L2: each GPU step reads its own input copy from a "
+                  f"pool of {pool} packs ({pool * 144} MB)",
+            "parallelism": f"replicas x{world} (one pack per GPU, no collective)"}
+
+
+def rnd(x, sig: int = 4):
+    """x with `sig` significant digits (recursively through dicts and lists)."""
+    if isinstance(x, dict):
+        return {k: rnd(v, sig) for k, v in x.items()}
+    if isinstance(x, (list, tuple)):
+        return [rnd(v, sig) for v in x]
+    if isinstance(x, float):
+        if x == 0 or x != x or x in (float("inf"), float("-inf")):
+            return x
+        from math import floor, log10
+        return round(x, sig - 1 - int(floor(log10(abs(x)))))
+    return x
+
+
 # ------------------------------------------------------------------ reference arm
 
 def run_reference(args):
-    """The oracle arm: rank 0 alone times the oracle and returns its JSON line;
-    the other ranks return None without work."""
+    """The oracle arm: rank 0 alone times the oracle on every host core (a
+    process per core; oracle/cpu_sample.py) and returns its JSON line; the
+    other ranks return None without work."""
     rank, world, _ = dist_env()
     if rank != 0:
         return None
-    from oracle import cpu_sample
     import workloads as W
-    n_tok = 128
-    sampler = cpu_sample.Sampler(1, args.seed)
-    vals = []
-    for i in range(args.warmup + args.steps):
-        r = sampler.sample(n_tok, sample_seed=i)
-        if i >= args.warmup:
-            vals.append(r["ms_per_pack"])
-    ms = sum(vals) / len(vals)
+    budget = getattr(args, "ref_budget_s", 150.0)
+    r = subprocess.run([sys.executable, "-m", "oracle.cpu_sample", "--mode", "reference",
+                        "--config", "1", "--seed", str(args.seed), "--steps", str(args.steps),
+                        "--warmup", str(args.warmup), "--budget-s", str(budget)],
+                       cwd=ROOT, capture_output=True, text=True, timeout=1800)
+    if r.returncode != 0:
+        raise RuntimeError(f"oracle reference run failed:\n{r.stderr[-2000:]}")
+    res = json.loads(r.stdout.strip().splitlines()[-1])
+    ms = res["ms_per_pack"]
     shape = W.config(1, args.seed)
+    sample = (f"every query token of the pack per step (prologue rows, select, fwd, bwd), "
+              f"dealt over {res['cores']} worker processes"
+              if not res["scaled"] else
+              f"{res['tokens_per_step']} of the pack's {res['tokens']} query tokens per step "
+              f"(evenly strided; prologue rows, select, fwd, bwd) over {res['cores']} worker "
+              f"processes, scaled by T/{res['tokens_per_step']}")
     line = {
         "impl": "reference", "metric": METRIC, "value": ms, "unit": "ms", "n_gpus": args.gpus,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": res["ms_per_step"],
         "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
-        "config": {"workload": shape.name, "tokens": shape.T, "seqlens": list(shape.seqlens),
-                   "hq": shape.hq, "hkv": shape.hkv, "hi": shape.hi},
-        "cpu_baseline": {"value": ms, "unit": "ms", "cores": 1, "kind": "oracle",
-                         "sample": f"prologue + select + fwd + bwd of {n_tok} random query "
-                                   f"tokens per step (all heads), scaled by T/{n_tok}"},
+        "config": config_dict(shape, getattr(args, "pool", 8), args.gpus),
+        "cpu_baseline": {"value": ms, "unit": "ms", "cores": res["cores"], "kind": "oracle",
+                         "sample": sample},
         "e2e": {"value": ms, "unit": "ms", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     return line
@@ -202,12 +246,24 @@ def traffic_for(name: str):
     return d.get("bytes_per_launch")
 
 
-def time_pack(m, W, workmodel, shape, dev, stream, seed, nsteps, with_bwd, sustained):
+PREFILL_KERNELS = ("plan_kernel", "index_select_kernel", "fwd_union_kernel", "sparse_fwd_kernel")
+BACKWARD_KERNELS = ("bwd_delta_kernel", "bwd_items_kernel", "bwd_lists_kernel", "bwd_order_kernel",
+                    "sparse_bwd_kernel", "bwd_convert_kernel")
+
+
+def phase_ms(per_step: dict, names) -> float:
+    return sum(per_step.get(n, 0.0) for n in names)
+
+
+def time_pack(m, W, workmodel, shape, dev, stream, seed, nsteps, with_bwd, peak, sample=None):
     """Prologue + select + forward (+ backward) on one pack (inputs larger than
-    L2); untimed warm-up, CUDA events over `nsteps`, then an event-bracketed pass
-    for the per-kernel split."""
+    L2, drawn on the CPU from `seed` so the oracle can redraw them); untimed
+    warm-up, CUDA events over `nsteps`, then an event-bracketed pass for the
+    per-kernel split.  `sample`: packed token ids whose selections are returned
+    for the parity report."""
     import torch
-    x = W.make_prefill(shape, seed=seed, device=dev, with_grad_out=with_bwd)
+    x = {k: v.to(dev) for k, v in
+         W.make_prefill(shape, seed=seed, device="cpu", with_grad_out=with_bwd).items()}
     T, S, hq, hkv, hi, L = shape.T, shape.S, shape.hq, shape.hkv, shape.hi, shape.max_seqlen
     bf = torch.bfloat16
     b = {n: torch.empty((T, h, 128), dtype=bf, device=dev)
@@ -251,24 +307,27 @@ def time_pack(m, W, workmodel, shape, dev, stream, seed, nsteps, with_bwd, susta
     m.msa_check_status(dev)
     ms = e0.elapsed_time(e1) / nsteps
     wk = workmodel.prefill_work(shape.seqlens, hq, hkv, hi)
-    per = {n: v["ms"] / v["launches"] for n, v in tr.items()}
+    per = {n: v["ms"] / nsteps for n, v in tr.items()}          # ms per step
     flops = wk["fwd_flops"] + wk["select_flops"] + (wk["bwd_flops"] if with_bwd else 0.0)
     out = {"workload": shape.name, "seqlens": list(shape.seqlens), "hq": hq, "hkv": hkv,
            "hi": hi, "ms_per_step": ms,
            "step": "qk_norm_rope4 + index_select + sparse_attn_fwd" +
                    (" + sparse_attn_bwd" if with_bwd else ""),
-           "useful_tflops": flops / (ms * 1e-3) / 1e12,
-           "frac_of_sustained": flops / (ms * 1e-3) / 1e12 / sustained,
-           "kernels_ms": per, "work": wk}
-    pf = per.get("index_select_kernel", 0.0) + per.get("sparse_fwd_kernel", 0.0)
-    if pf > 0:
-        f = wk["fwd_flops"] + wk["select_flops"]
-        out["prefill_select_fwd"] = {"ms": pf, "useful_tflops": f / (pf * 1e-3) / 1e12,
-                                     "frac_of_sustained": f / (pf * 1e-3) / 1e12 / sustained}
-    if with_bwd and "sparse_bwd_kernel" in per:
-        t = per["sparse_bwd_kernel"]
-        out["backward"] = {"ms": t, "useful_tflops": wk["bwd_flops"] / (t * 1e-3) / 1e12,
-                           "frac_of_sustained": wk["bwd_flops"] / (t * 1e-3) / 1e12 / sustained}
+           "useful_tflops": flops / (ms * 1e-3) / 1e12, "kernels_ms": per, "work": wk}
+    pf = phase_ms(per, PREFILL_KERNELS)
+    f = wk["fwd_flops"] + wk["select_flops"]
+    out["prefill"] = {"ms": pf, "tflops": f / (pf * 1e-3) / 1e12,
+                      "frac": f / (pf * 1e-3) / 1e12 / peak,
+                      "kernels": list(PREFILL_KERNELS)}
+    if with_bwd:
+        t = per.get("sparse_bwd_kernel", 0.0)
+        tb = phase_ms(per, BACKWARD_KERNELS)
+        out["backward"] = {"ms": tb, "tflops": wk["bwd_flops"] / (tb * 1e-3) / 1e12,
+                           "frac": wk["bwd_flops"] / (tb * 1e-3) / 1e12 / peak,
+                           "kernel_ms": t,
+                           "kernel_frac": wk["bwd_flops"] / (t * 1e-3) / 1e12 / peak}
+    if sample is not None:
+        out["sample_sel"] = sel[torch.as_tensor(sample, device=dev)].cpu().numpy()
     return out
 
 
@@ -290,15 +349,23 @@ def run_ours(args):
     import workloads as W
 
     peaks, peak_src = load_peaks()
+    parity_arrays = {}             # CUDA-path outputs of sampled rows, for the oracle
     shape = W.config(1, args.seed)
     T, S = shape.T, shape.S
     hq, hkv, hi, maxL = shape.hq, shape.hkv, shape.hi, shape.max_seqlen
 
     # ---- input pool (each rank draws its own pack: weak scaling)
+    # pack 0 is drawn on the CPU (the oracle redraws it for the parity report),
+    # the others on the device
     pool = []
     for j in range(args.pool):
-        pool.append(W.make_prefill(shape, seed=rank_seed(args.seed, rank, j), device=dev,
-                                   with_grad_out=True))
+        if j == 0:
+            pool.append({k: v.to(dev) for k, v in
+                         W.make_prefill(shape, seed=rank_seed(args.seed, rank, j), device="cpu",
+                                        with_grad_out=True).items()})
+        else:
+            pool.append(W.make_prefill(shape, seed=rank_seed(args.seed, rank, j), device=dev,
+                                       with_grad_out=True))
     cu = pool[0]["cu_seqlens"]
     bf = torch.bfloat16
     work = {
@@ -385,28 +452,46 @@ def run_ours(args):
 
     flops_of = {"sparse_bwd_kernel": wk["bwd_flops"], "sparse_fwd_kernel": wk["fwd_flops"],
                 "index_select_kernel": wk["select_flops"]}
+    # the timed region lasts tens of milliseconds at full SM clock (sampled
+    # below), so the tensor roofline is the measured burst bf16 peak; the
+    # sustained (power-capped, seconds-long) figure is kept beside it
+    burst = peaks.get("bf16_tflops", 1900.0)
+    sustained = peaks.get("bf16_tflops_sustained", 1700.0)
+    hbm = peaks.get("hbm_gbs", 6800.0)
     dom = max(trace.items(), key=lambda kv: kv[1]["ms"])[0]
     roofline = None
     if dom in flops_of:
         ms_launch = trace[dom]["ms"] / trace[dom]["launches"]
         ach = flops_of[dom] / (ms_launch * 1e-3) / 1e12
-        peak = peaks.get("bf16_tflops_sustained", 1700.0)
-        roofline = {"kernel": dom, "bound": "tensor", "achieved": ach, "peak": peak,
-                    "unit": "TFLOP/s", "frac": ach / peak, "traffic": traffic_for(dom),
-                    "peak_source": f"{peak_src} bf16 dense sustained (kernel timed inside a long step)",
-                    "frac_of_burst": ach / peaks.get("bf16_tflops", 1900.0),
+        roofline = {"kernel": dom, "bound": "tensor", "achieved": ach, "peak": burst,
+                    "unit": "TFLOP/s", "frac": ach / burst, "traffic": traffic_for(dom),
+                    "peak_source": f"{peak_src} bf16 dense burst (timed region of "
+                                   f"~{ms_step * args.steps:.0f} ms at the sampled SM clock)",
+                    "frac_of_sustained": ach / sustained,
+                    "frac_of_nominal": ach / NOMINAL_BF16_TFLOPS,
                     "flops_per_launch": flops_of[dom], "ms_per_launch": ms_launch}
     per_kernel_roofline = {}
     for n, f in flops_of.items():
         if n in trace:
             msl = trace[n]["ms"] / trace[n]["launches"]
             per_kernel_roofline[n] = {"tflops": f / (msl * 1e-3) / 1e12, "ms": msl,
-                                      "frac": f / (msl * 1e-3) / 1e12 / peaks.get("bf16_tflops_sustained", 1700.0)}
+                                      "frac": f / (msl * 1e-3) / 1e12 / burst}
     if "prologue_kernel" in trace:
         msl = trace["prologue_kernel"]["ms"] / trace["prologue_kernel"]["launches"]
         per_kernel_roofline["prologue_kernel"] = {
             "gbs": wk["prologue_bytes"] / (msl * 1e-3) / 1e9, "ms": msl,
-            "frac": wk["prologue_bytes"] / (msl * 1e-3) / 1e9 / peaks.get("hbm_gbs", 6800.0)}
+            "frac": wk["prologue_bytes"] / (msl * 1e-3) / 1e9 / hbm,
+            "frac_of_nominal": wk["prologue_bytes"] / (msl * 1e-3) / 1e9 / NOMINAL_HBM_GBS}
+    per_step = {n: v["ms"] / args.steps for n, v in trace.items()}
+    pf = phase_ms(per_step, PREFILL_KERNELS)
+    pflops = wk["fwd_flops"] + wk["select_flops"]
+    tb = phase_ms(per_step, BACKWARD_KERNELS)
+    phases = {"prefill": {"ms": pf, "tflops": pflops / (pf * 1e-3) / 1e12,
+                          "frac": pflops / (pf * 1e-3) / 1e12 / burst,
+                          "kernels": list(PREFILL_KERNELS)},
+              "backward": {"ms": tb, "tflops": wk["bwd_flops"] / (tb * 1e-3) / 1e12,
+                           "frac": wk["bwd_flops"] / (tb * 1e-3) / 1e12 / burst,
+                           "kernels": list(BACKWARD_KERNELS)}}
 
     out = {
         "metric": METRIC,
@@ -421,12 +506,7 @@ def run_ours(args):
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic",
-        "config": {"workload": shape.name, "tokens": T, "seqlens": list(shape.seqlens),
-                   "hq": hq, "hkv": hkv, "hi": hi, "d": 128, "block": 128, "topk": 16,
-                   "step": "qk_norm_rope4 + index_select + sparse_attn_fwd + sparse_attn_bwd",
-                   "l2": f"inputs larger than L2: each step reads its own input copy from a "
-                         f"pool of {args.pool} packs ({args.pool * 144} MB)",
-                   "parallelism": f"replicas x{world} (one pack per GPU, no collective)"},
+        "config": config_dict(shape, args.pool, world),
         "tflops": total_flops / (ms_step * 1e-3) / 1e12,
         "tokens_per_s": T * world / (ms_step * 1e-3),
         "work": wk,
@@ -436,6 +516,7 @@ def run_ours(args):
                                  "bracketed by CUDA events", "ms_per_step": ms_step_traced},
         "host_enqueue_ms_per_step": host_ms,
         "kernel_roofline": per_kernel_roofline,
+        "phases": phases,
         "gpu_launches": gpu_launches,
         "clocks": clocks,
         "pages_context": PAGES_CONTEXT,
@@ -583,6 +664,30 @@ def run_ours(args):
         dtrace = m.msa_trace_end()
         m.msa_check_status(dev)
         dms = d0.elapsed_time(d1) / nd
+        # parity rows (two shortest caches and the longest): their pages as bf16
+        # bits, the GPU's selection and output, before the append below writes
+        # new tokens into the caches
+        if not args.no_parity and rank == 0 and world == 1:
+            import numpy as np
+            lens_np = dx["cache_lens"].cpu().numpy()
+            rows = sorted(set(np.argsort(lens_np)[:2].tolist() + [int(np.argmax(lens_np))]))
+            table_np = dx["block_table"].cpu().numpy()
+            used = sorted({int(p_) for r_ in rows for p_ in table_np[r_, :(lens_np[r_] + 127) // 128]})
+            remap = {p_: i for i, p_ in enumerate(used)}
+            sub = np.full((len(rows), table_np.shape[1]), -1, dtype=np.int64)
+            for n_, r_ in enumerate(rows):
+                for c_ in range((lens_np[r_] + 127) // 128):
+                    sub[n_, c_] = remap[int(table_np[r_, c_])]
+            idx = torch.tensor(used, dtype=torch.long, device=dev)
+            bits = lambda t: t.index_select(0, idx).view(torch.int16).cpu().numpy()   # noqa: E731
+            ridx = torch.tensor(rows, dtype=torch.long, device=dev)
+            parity_arrays.update(
+                dec_name=np.array(dshape.name), dec_rows=np.array(rows),
+                dec_q=dx["q"][ridx].float().cpu().numpy(),
+                dec_q_idx=dx["q_idx"][ridx].float().cpu().numpy(),
+                dec_k_bits=bits(dx["k_cache"]), dec_v_bits=bits(dx["v_cache"]),
+                dec_kidx_bits=bits(dx["kidx_cache"]), dec_table=sub, dec_lens=lens_np[rows],
+                dec_sel=sd[ridx].cpu().numpy(), dec_o=od[ridx].float().cpu().numpy())
         # the decode append (prologue of the new tokens, written into their pages)
         # on the same caches, timed on its own
         agen = torch.Generator(device=dev).manual_seed(args.seed + 5)
@@ -646,13 +751,17 @@ def run_ours(args):
     # ---- the other prefill workloads: full layer shape on a 16k pack (prefill)
     # and the 32k training pack (prefill + backward)
     if not args.no_configs:
-        sus = peaks.get("bf16_tflops_sustained", 1700.0)
-        out["configs"] = {
-            "pack16k-8seq-64q4kv": time_pack(m, W, workmodel, W.config(2, args.seed), dev, stream,
-                                             rank_seed(args.seed, rank), 10, False, sus),
-            "pack32k-4seq-64q4kv": time_pack(m, W, workmodel, W.config(4, args.seed), dev, stream,
-                                             rank_seed(args.seed, rank), 5, True, sus),
-        }
+        import numpy as np
+        out["configs"] = {}
+        for key, idx, nsteps, with_bwd in (("cfg2", 2, 10, False), ("cfg4", 4, 5, True)):
+            cshape = W.config(idx, args.seed)
+            cseed = rank_seed(args.seed, rank)
+            samp = np.sort(np.random.default_rng(100 + idx).choice(cshape.T, 512, replace=False))
+            r_ = time_pack(m, W, workmodel, cshape, dev, stream, cseed, nsteps, with_bwd, burst,
+                           sample=samp)
+            parity_arrays.update({f"{key}_tokens": samp, f"{key}_sel": r_.pop("sample_sel"),
+                                  f"{key}_seed": np.array(cseed)})
+            out["configs"][cshape.name] = r_
 
     # ---- narrow-block variant: 16k pack, 12 q / 1 kv heads, head dim 256, 4-token
     # blocks, fwd + bwd (the pages' second timed workload)
@@ -693,7 +802,6 @@ def run_ours(args):
         qms = q0.elapsed_time(q1) / nq
         qwk = workmodel.qsa_work(qshape.seqlens, qx["sel"].cpu().numpy(), qshape.hq)
         qflops = qwk["fwd_flops"] + qwk["bwd_flops"]
-        sus = peaks.get("bf16_tflops_sustained", 1700.0)
         qk = {n: {"launches": v["launches"] // nq, "ms_per_launch": v["ms"] / v["launches"]}
               for n, v in qtrace.items()}
         qkr = {}
@@ -703,13 +811,13 @@ def run_ours(args):
             if n in qk:
                 t = qk[n]["ms_per_launch"]
                 qkr[n] = {"ms": t, "useful_tflops": f / (t * 1e-3) / 1e12,
-                          "frac": f / (t * 1e-3) / 1e12 / sus, "traffic": traffic_for(n)}
+                          "frac": f / (t * 1e-3) / 1e12 / burst, "traffic": traffic_for(n)}
         out["qsa"] = {
             "workload": qshape.name, "seqlens": list(qshape.seqlens), "hq": qshape.hq,
             "hkv": qshape.hkv, "d": W.QSA_D, "block": W.QSA_BLOCK, "topk": qshape.topk,
             "ms_per_step": qms, "step": "msa_qsa_attn_fwd + msa_qsa_attn_bwd",
             "useful_tflops": qflops / (qms * 1e-3) / 1e12,
-            "frac_of_sustained": qflops / (qms * 1e-3) / 1e12 / sus,
+            "frac": qflops / (qms * 1e-3) / 1e12 / burst,
             "work": qwk, "kernels": qk, "kernel_roofline": qkr,
             "useful_split": "dq pass: S, dP, dQ = 3 of the 5 backward products; dkv pass: "
                             "dV, dK = 2 of 5 (each pass also recomputes S and dP)",
@@ -719,40 +827,111 @@ def run_ours(args):
         }
         del qx
 
-    # ---- CPU oracle on a bounded sample (rank 0, N = 1 only)
+    # ---- CPU oracle on a bounded sample (rank 0, N = 1 only): one core and
+    # every host core, and the parity report of sampled rows.  The CUDA
+    # path's outputs go to the oracle process in a temporary .npz.
     if not args.no_cpu_baseline and rank == 0 and world == 1:
-        env = dict(os.environ)
-        from oracle.cpu_sample import THREAD_VARS
-        for v in THREAD_VARS:
-            env[v] = "1"
-        r = subprocess.run([sys.executable, "-m", "oracle.cpu_sample", "--config", "1",
-                            "--tokens", str(args.cpu_sample_tokens), "--seed", str(args.seed)],
-                           cwd=ROOT, env=env, capture_output=True, text=True, timeout=900)
+        import shutil
+        import tempfile
+
+        import numpy as np
+        cmd = [sys.executable, "-m", "oracle.cpu_sample", "--mode", "baseline", "--config", "1",
+               "--tokens", str(args.cpu_sample_tokens), "--seed", str(rank_seed(args.seed, 0, 0))]
+        tmpdir = None
+        if not args.no_parity:
+            step(pool[0])                       # pack 0: drawn on the CPU, redrawn by the oracle
+            torch.cuda.synchronize(dev)
+            m.msa_check_status(dev)
+            toks = np.sort(np.random.default_rng(0).choice(T, size=min(args.cpu_sample_tokens, T),
+                                                           replace=False))
+            ti = torch.as_tensor(toks, device=dev)
+            parity_arrays.update(cfg1_tokens=toks, cfg1_sel=work["sel"][ti].cpu().numpy(),
+                                 cfg1_o=work["o"][ti].float().cpu().numpy(),
+                                 cfg1_lse=work["lse"][ti].cpu().numpy(),
+                                 cfg1_dq=work["dq"][ti].float().cpu().numpy())
+            tmpdir = tempfile.mkdtemp(prefix="msa_parity_")
+            path = os.path.join(tmpdir, "gpu_outputs.npz")
+            np.savez(path, **parity_arrays)
+            cmd += ["--parity", path]
+        try:
+            r = subprocess.run(cmd, cwd=ROOT, capture_output=True, text=True, timeout=1200)
+        finally:
+            if tmpdir:
+                shutil.rmtree(tmpdir, ignore_errors=True)
         if r.returncode == 0:
             cs = json.loads(r.stdout.strip().splitlines()[-1])
             out["cpu_baseline"] = {
-                "value": cs["ms_per_pack"], "unit": "ms", "cores": 1, "kind": "oracle",
-                "sample": f"prologue + select + fwd + bwd of {cs['sample_tokens']} random "
-                          f"query tokens (all heads) of the same pack, scaled by "
-                          f"T/{cs['sample_tokens']}",
-                "seconds": {k: cs[k] for k in ("prologue_s", "select_s", "fwd_s", "bwd_s")}}
+                "value": cs["ms_per_pack"], "unit": "ms", "cores": cs["cores"], "kind": "oracle",
+                "sample": f"prologue + select + fwd + bwd of {cs['sample_tokens']} random query "
+                          f"tokens (all heads) of pack 0, dealt over {cs['cores']} worker "
+                          f"processes (one BLAS thread each), scaled by T/{cs['sample_tokens']}",
+                "one_core": {"value": cs["ms_per_pack_1core"], "cores": 1},
+                "seconds_1core": {k: cs[k] for k in ("prologue_s", "select_s", "fwd_s", "bwd_s")}}
+            if "parity" in cs:
+                out["parity"] = cs["parity"]
         else:
-            out["cpu_baseline"] = {"value": None, "error": r.stderr[-500:]}
+            out["cpu_baseline"] = {"value": None, "error": r.stderr[-800:]}
 
     if rank == 0:
-        print(json.dumps(out), flush=True)
+        if args.detail:
+            with open(args.detail, "w") as f:
+                json.dump(out, f, indent=1, default=str)
+        print(json.dumps(compact_line(out)), flush=True)
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
 
 
+def compact_line(out: dict) -> dict:
+    """The printed line: the contract's keys, then short summaries of every
+    leg (full detail: --detail)."""
+    keep = ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+            "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config", "roofline",
+            "e2e", "gpu_launches", "clocks", "cpu_baseline")
+    line = {k: out[k] for k in keep if k in out}
+    if line.get("roofline"):
+        line["roofline"] = {k: v for k, v in line["roofline"].items()
+                            if k not in ("flops_per_launch",)}
+    if line.get("cpu_baseline"):
+        line["cpu_baseline"] = {k: v for k, v in line["cpu_baseline"].items()
+                                if k != "seconds_1core"}
+    line["tflops"] = out.get("tflops")
+    line["tokens_per_s"] = out.get("tokens_per_s")
+    line["phases"] = {k: {"ms": v["ms"], "tflops": v["tflops"], "frac": v["frac"]}
+                      for k, v in out.get("phases", {}).items()}
+    line["kernels"] = {n: [v["launches"], v["ms_per_launch"]]
+                       for n, v in out.get("kernels", {}).items()}
+    line["kernel_frac"] = {n: v["frac"] for n, v in out.get("kernel_roofline", {}).items()}
+    if "decode" in out:
+        d = out["decode"]
+        line["decode"] = {"ms": d["ms_per_step"], "gbs": d["gbs"], "frac": d["roofline"]["frac"],
+                          "frac_of_nominal": d["gbs"] / NOMINAL_HBM_GBS,
+                          "score_ms": d["kernels"].get("decode_score_kernel", {}).get("ms_per_launch"),
+                          "append_ms": d["append"]["ms_per_step"]}
+    if "prologue_bwd" in out:
+        d = out["prologue_bwd"]
+        line["prologue_bwd"] = {"ms": d["ms_per_step"], "frac": d["roofline"]["frac"]}
+    if "configs" in out:
+        line["configs"] = {}
+        for name, c in out["configs"].items():
+            e = {"ms": c["ms_per_step"], "prefill_ms": c["prefill"]["ms"],
+                 "prefill_frac": c["prefill"]["frac"]}
+            if "backward" in c:
+                e.update(bwd_ms=c["backward"]["ms"], bwd_frac=c["backward"]["frac"],
+                         bwd_kernel_frac=c["backward"]["kernel_frac"])
+            line["configs"][name] = e
+    if "qsa" in out:
+        qd = out["qsa"]
+        line["qsa"] = {"ms": qd["ms_per_step"], "tflops": qd["useful_tflops"], "frac": qd["frac"],
+                       "kernel_frac": {n: v["frac"] for n, v in qd["kernel_roofline"].items()}}
+    if "parity" in out:
+        line["parity"] = {n: {k: v for k, v in p.items()} for n, p in out["parity"].items()}
+    return rnd(line)
+
+
 def main():
     args = parse()
     if args.impl == "reference":
-        # the oracle runs on one host core; set before numpy loads
-        for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS",
-                    "NUMEXPR_NUM_THREADS", "BLIS_NUM_THREADS"):
-            os.environ[var] = "1"
         line = run_reference(args)
         if line is not None:
             print(json.dumps(line), flush=True)

@@ -43,7 +43,8 @@ def _rank_main(rank, world, port, outdir, mode):
                    "seed": bench.rank_seed(7, rank),
                    "q_sum": float(x["q"].float().sum())}
         else:
-            args = types.SimpleNamespace(seed=0, steps=1, warmup=0, gpus=world)
+            args = types.SimpleNamespace(seed=0, steps=1, warmup=0, gpus=world, pool=8,
+                                         ref_budget_s=2.0)
             res = {"line": bench.run_reference(args)}
         dist.barrier()
     finally:
@@ -74,5 +75,9 @@ def test_reference_arm_runs_on_rank_zero_only(tmp_path):
     line = r0["line"]
     assert line["impl"] == "reference" and line["n_gpus"] == WORLD
     assert line["unit"] == "ms" and line["value"] > 0
-    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] == 1
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
     assert line["e2e"]["h2d_bytes_per_step"] == 0
+    # the same workload dict as the GPU arm prints
+    import bench
+    import workloads as W
+    assert line["config"] == bench.config_dict(W.config(1, 0), 8, WORLD)
