@@ -157,8 +157,8 @@ def config_dict(shape, pool: int, world: int) -> dict:
             "hq": shape.hq, "hkv": shape.hkv, "hi": shape.hi, "d": 128, "block": 128,
             "topk": 16,
             "step": "qk_norm_rope4 + index_select + sparse_attn_fwd + sparse_attn_bwd",
-            "l2": f"inputs larger than L2: each GPU step reads its own input copy from a "
-                  f"pool of {pool} packs ({pool * 144} MB)",
+            "l2": f"inputs > L2: each GPU step reads its own copy from a {pool}-pack pool "
+                  f"({pool * 144} MB)",
             "parallelism": f"replicas x{world} (one pack per GPU, no collective)"}
 
 
@@ -465,8 +465,8 @@ def run_ours(args):
         ach = flops_of[dom] / (ms_launch * 1e-3) / 1e12
         roofline = {"kernel": dom, "bound": "tensor", "achieved": ach, "peak": burst,
                     "unit": "TFLOP/s", "frac": ach / burst, "traffic": traffic_for(dom),
-                    "peak_source": f"{peak_src} bf16 dense burst (timed region of "
-                                   f"~{ms_step * args.steps:.0f} ms at the sampled SM clock)",
+                    "peak_source": f"{peak_src} bf16 burst: {ms_step * args.steps:.0f} ms "
+                                   f"timed at the sampled clock",
                     "frac_of_sustained": ach / sustained,
                     "frac_of_nominal": ach / NOMINAL_BF16_TFLOPS,
                     "flops_per_launch": flops_of[dom], "ms_per_launch": ms_launch}
@@ -862,9 +862,8 @@ def run_ours(args):
             cs = json.loads(r.stdout.strip().splitlines()[-1])
             out["cpu_baseline"] = {
                 "value": cs["ms_per_pack"], "unit": "ms", "cores": cs["cores"], "kind": "oracle",
-                "sample": f"prologue + select + fwd + bwd of {cs['sample_tokens']} random query "
-                          f"tokens (all heads) of pack 0, dealt over {cs['cores']} worker "
-                          f"processes (one BLAS thread each), scaled by T/{cs['sample_tokens']}",
+                "sample": f"prologue+select+fwd+bwd of {cs['sample_tokens']} random tokens of "
+                          f"pack 0 over {cs['cores']} processes, x T/{cs['sample_tokens']}",
                 "one_core": {"value": cs["ms_per_pack_1core"], "cores": 1},
                 "seconds_1core": {k: cs[k] for k in ("prologue_s", "select_s", "fwd_s", "bwd_s")}}
             if "parity" in cs:
@@ -891,17 +890,19 @@ def compact_line(out: dict) -> dict:
     line = {k: out[k] for k in keep if k in out}
     if line.get("roofline"):
         line["roofline"] = {k: v for k, v in line["roofline"].items()
-                            if k not in ("flops_per_launch",)}
+                            if k not in ("flops_per_launch", "ms_per_launch")}
     if line.get("cpu_baseline"):
         line["cpu_baseline"] = {k: v for k, v in line["cpu_baseline"].items()
                                 if k != "seconds_1core"}
+    if line.get("e2e"):
+        line["e2e"] = {k: v for k, v in line["e2e"].items() if k not in ("schedule", "steps")}
     line["tflops"] = out.get("tflops")
-    line["tokens_per_s"] = out.get("tokens_per_s")
+    short = lambda n: n[:-len("_kernel")] if n.endswith("_kernel") else n   # noqa: E731
     line["phases"] = {k: {"ms": v["ms"], "tflops": v["tflops"], "frac": v["frac"]}
                       for k, v in out.get("phases", {}).items()}
-    line["kernels"] = {n: [v["launches"], v["ms_per_launch"]]
-                       for n, v in out.get("kernels", {}).items()}
-    line["kernel_frac"] = {n: v["frac"] for n, v in out.get("kernel_roofline", {}).items()}
+    line["kernels_ms"] = {short(n): v["launches"] * v["ms_per_launch"]       # per step
+                          for n, v in out.get("kernels", {}).items()}
+    line["kernel_frac"] = {short(n): v["frac"] for n, v in out.get("kernel_roofline", {}).items()}
     if "decode" in out:
         d = out["decode"]
         line["decode"] = {"ms": d["ms_per_step"], "gbs": d["gbs"], "frac": d["roofline"]["frac"],
@@ -923,7 +924,7 @@ def compact_line(out: dict) -> dict:
     if "qsa" in out:
         qd = out["qsa"]
         line["qsa"] = {"ms": qd["ms_per_step"], "tflops": qd["useful_tflops"], "frac": qd["frac"],
-                       "kernel_frac": {n: v["frac"] for n, v in qd["kernel_roofline"].items()}}
+                       "kernel_frac": {short(n): v["frac"] for n, v in qd["kernel_roofline"].items()}}
     if "parity" in out:
         line["parity"] = {n: {k: v for k, v in p.items()} for n, p in out["parity"].items()}
     return rnd(line)
