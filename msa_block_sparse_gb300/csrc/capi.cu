@@ -528,11 +528,10 @@ msa_status_t msa_qk_norm_rope_bwd(const void* x, const void* dy, void* dx, float
 // ---------------------------------------------------------------- index select
 
 size_t msa_index_select_workspace_size(int T, int S, int Hi, int max_seqlen) {
-  (void)Hi;
   (void)max_seqlen;
-  if (T < 1 || S < 1) return 0;
+  if (T < 1 || S < 1 || Hi < 1) return 0;
   WsCursor ws(nullptr);
-  carve_plan(ws, T, S);
+  carve_select_workspace(ws, T, S, Hi);
   return ws.used + 256;
 }
 
@@ -559,10 +558,9 @@ msa_status_t msa_index_select_ex(const void* q_idx, const void* k_idx, const int
   if (workspace_bytes < msa_index_select_workspace_size(T, S, Hi, max_seqlen))
     return fail(MSA_ERR_INVALID_ARG, "workspace too small");
   WsCursor ws(workspace);
-  Plan plan = carve_plan(ws, T, S);
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  MSA_TRY(launch_plan(plan, cu_seqlens, S, max_seqlen, st));
-  return launch_index_select(q_idx, k_idx, cu_seqlens, S, T, Hi, n_init, plan, sel, st);
+  SelWorkspace w = carve_select_workspace(ws, T, S, Hi);
+  return launch_index_select(q_idx, k_idx, cu_seqlens, S, T, Hi, max_seqlen, n_init, w, sel,
+                             static_cast<cudaStream_t>(stream));
 }
 
 // ---------------------------------------------------------------- sparse forward

@@ -36,9 +36,23 @@ msa_status_t launch_prologue_bwd(const __nv_bfloat16* x, const __nv_bfloat16* dy
                                  float* dw_part, cudaStream_t stream);
 
 // ---------------------------------------------------------------- index select
+// Work units (query tile, index head, chunk of earlier key blocks): at most
+// tiles x Hi + kSelUnitsBeyondTiles of them (the plan sizes the chunks so).
+constexpr int kSelUnitsBeyondTiles = 640;
+struct SelWorkspace {
+  int4* units;         // [max_units] (sequence start, query block, first block, end block)
+  int4* aux;           // [max_units] (tile x Hi + head, chunks, first slot, chunk | rows << 16)
+  int* num_units;      // [1]
+  int* claim;          // [1] next unit to claim
+  int* merge_ctr;      // [max_tiles * Hi] chunks of the tile finished
+  int* tile_start;     // [S + 1] first tile of each sequence
+  unsigned long long* part;   // [max_units][15][128] top-15 lists (entry keys) of split tiles' chunks
+  int max_units, max_tiles;
+};
+SelWorkspace carve_select_workspace(WsCursor& ws, int T, int S, int Hi);
 msa_status_t launch_index_select(const void* q_idx, const void* k_idx, const int32_t* cu, int S,
-                                 int T, int Hi, int n_init, const Plan& plan, int32_t* sel,
-                                 cudaStream_t stream);
+                                 int T, int Hi, int max_seqlen, int n_init,
+                                 const SelWorkspace& w, int32_t* sel, cudaStream_t stream);
 
 // ---------------------------------------------------------------- sparse forward
 // Per (8-token query tile, KV head): word 0 = number of union blocks, words
