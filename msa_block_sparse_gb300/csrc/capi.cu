@@ -129,6 +129,18 @@ int device_sm_count() {
   return cached[dev];
 }
 
+size_t device_l2_bytes() {
+  static size_t cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  if (!cached[dev]) {
+    int n = 0;
+    cudaDeviceGetAttribute(&n, cudaDevAttrL2CacheSize, dev);
+    cached[dev] = n > 0 ? static_cast<size_t>(n) : 1;
+  }
+  return cached[dev];
+}
+
 msa_status_t ensure_smem_ptr(const void* kernel, size_t bytes, const char* name) {
   static std::mutex mu;
   static std::map<std::pair<const void*, int>, size_t> done;

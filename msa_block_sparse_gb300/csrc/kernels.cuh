@@ -89,6 +89,7 @@ struct BwdWorkspace {
 };
 BwdWorkspace carve_bwd_workspace(WsCursor& ws, int T, int S, int Hq, int Hkv, int max_seqlen);
 int device_sm_count();
+size_t device_l2_bytes();   // L2 cache size of the current device
 // Raises `kernel`'s dynamic shared-memory limit to `bytes` on the current
 // device, once per (kernel, device): the attribute is kept per device.
 msa_status_t ensure_smem_ptr(const void* kernel, size_t bytes, const char* name);
