@@ -372,20 +372,58 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     }
     // Tiles are claimed from a per-KV-head counter (heaviest first, as the plan
     // orders them) so that CTAs finishing early take more; the claimed id goes
-    // to the other roles through the tile slot, -1 once none are left.
+    // to the other roles through the tile slot, -1 once none are left.  The
+    // next claim's plan entry, union header and union entries (lane i: entries
+    // i, i + 32, ...) are read before the current tile's K blocks are issued,
+    // so those loads are in flight while K streams.
     uint32_t tcount = 0, kc = 0;
     bool alive = true;
     int pending = 0;
     if (lane == 0) pending = atomicAdd(tile_ctr + g, 1);
+    pending = __shfl_sync(0xffffffffu, pending, 0);
+    int2 n_pt = make_int2(0, 0);
+    int n_hdr[3] = {0, 0, 0};
+    int n_ent[kTpt * kTopK / 32];
+    auto prefetch = [&](int ti) {
+      if (ti >= total) return;
+      n_pt = tiles[ti >> 4];
+      const int* ul = ulist + (static_cast<size_t>(ti) * Hkv + g) * kFwdUnionStride;
+      n_hdr[0] = __ldg(ul);
+      n_hdr[1] = __ldg(ul + 1);
+      n_hdr[2] = __ldg(ul + 2);
+#pragma unroll
+      for (int q = 0; q < kTpt * kTopK / 32; ++q) n_ent[q] = __ldg(ul + 4 + lane + 32 * q);
+    };
+    prefetch(pending);
     while (alive) {
-      int ti = -1;
-      if (lane == 0) {
-        ti = pending;
-        TileInfo tt;
-        while (ti < total && !tile_info(ti, tiles, cu, tt)) ti = atomicAdd(tile_ctr + g, 1);
-        if (ti >= total) ti = -1;
+      int ti = pending;
+      TileInfo t;
+      bool have = false;
+      if (ti < total) {
+        // the prefetched entry, if the claimed tile has tokens
+        t.s = n_pt.x;
+        t.qb = n_pt.y;
+        t.seq0 = cu[t.s];
+        t.len = cu[t.s + 1] - t.seq0;
+        t.p0 = t.qb * kBlock;
+        const int first = (ti & 15) * kTpt;
+        t.ntok = min(kTpt, t.len - t.p0 - first);
+        have = t.p0 + first < t.len;
       }
-      ti = __shfl_sync(0xffffffffu, ti, 0);
+      if (!have && ti < total) {
+        // a token group past the end of its query block: claim on
+        if (lane == 0) {
+          TileInfo tt;
+          ti = atomicAdd(tile_ctr + g, 1);
+          while (ti < total && !tile_info(ti, tiles, cu, tt)) ti = atomicAdd(tile_ctr + g, 1);
+        }
+        ti = __shfl_sync(0xffffffffu, ti, 0);
+        if (ti < total) {
+          tile_info(ti, tiles, cu, t);
+          prefetch(ti);
+        }
+      }
+      if (ti >= total) ti = -1;
       const int tb = tcount & 1;
       if (lane == 0) alive = mbar_wait(&sm.tile_empty[tb], ((tcount >> 1) & 1) ^ 1, status, 1);
       alive = __shfl_sync(0xffffffffu, alive ? 1 : 0, 0) != 0;
@@ -397,20 +435,20 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         }
         break;
       }
-      TileInfo t;
-      tile_info(ti, tiles, cu, t);
       // ---- the tile's union entries (built by fwd_union_kernel)
-      const int* ul = ulist + (static_cast<size_t>(ti) * Hkv + g) * kFwdUnionStride;
-      const int nU = min(__ldg(ul), kTpt * kTopK);
-      t.offs[0] = static_cast<uint32_t>(__ldg(ul + 1));
-      t.offs[1] = static_cast<uint32_t>(__ldg(ul + 2));
-      for (int i = lane; i < nU; i += 32) sm.ublk[tb][i] = __ldg(ul + 4 + i);
+      const int nU = min(n_hdr[0], kTpt * kTopK);
+      t.offs[0] = static_cast<uint32_t>(n_hdr[1]);
+      t.offs[1] = static_cast<uint32_t>(n_hdr[2]);
+#pragma unroll
+      for (int q = 0; q < kTpt * kTopK / 32; ++q)
+        if (lane + 32 * q < nU) sm.ublk[tb][lane + 32 * q] = n_ent[q];
       if (lane == 0) {
         sm.n_union[tb] = nU;
         sm.tile_id[tb] = ti;
         sm.tinfo[tb] = t;
-        pending = atomicAdd(tile_ctr + g, 1);   // next claim, in flight while K streams
+        pending = atomicAdd(tile_ctr + g, 1);   // next claim
       }
+      pending = __shfl_sync(0xffffffffu, pending, 0);
       __syncwarp();                             // the slot is written (released by the arrive)
       if (lane == 0) mbar_arrive_expect_tx(&sm.tile_full[tb], t.ntok * 2 * kTokRows);
       __syncwarp();                             // the copies below complete after it
@@ -421,6 +459,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                     g * kG, t.seq0 + t.p0 + member_offset(t, i));
       }
       __syncwarp();
+      prefetch(pending);                        // the next tile's entries, while K streams
       if (lane == 0) {
         // ---- K tiles through their 2-stage ring (V has its own warp, so a V
         // slot that frees late does not hold up the next K)
