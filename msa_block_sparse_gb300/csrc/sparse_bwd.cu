@@ -7,8 +7,8 @@
 // by window, so the items running at any moment add into dQ rows of a few
 // windows only and the fp32 dQ accumulator lines stay in L2.  Persistent CTAs
 // (one per SM and KV head share) claim the items from a counter, so that a CTA
-// that drew short items takes more; the last fifth of the list (all of it when
-// the dQ accumulator is within twice L2) is claimed largest first
+// that drew short items takes more; the last fifth of the list (the last third
+// when the dQ accumulator is within twice L2) is claimed largest first
 // (bwd_order_kernel) so that the CTAs finish together.  Per item the CTA holds
 // K_b and V_b in shared memory and streams the window's query tokens that
 // selected b, in ascending order, in half-chunks of 4 tokens x G = 16 heads =
@@ -226,11 +226,9 @@ __global__ void __launch_bounds__(kBwdSegment) bwd_lists_kernel(
 
 // One CTA per KV head.  The first n - n / tail_div items keep their
 // window-major order (concurrent items add into the dQ rows of a few windows,
-// which keeps a dQ accumulator larger than L2 from thrashing); the rest follow
-// by half-chunk count, largest first, so that the last items claimed are short
-// and the CTAs finish together.  tail_div = 1 sorts every item (packs whose
-// accumulator is within twice L2: balance then matters more than locality).
-// Order within equal counts is unspecified.
+// which keeps the dQ accumulator lines in L2); the rest follow by half-chunk
+// count, largest first, so that the last items claimed are short and the CTAs
+// finish together.  Order within equal counts is unspecified.
 constexpr int kMaxHalfChunks = kBwdSegment / 4;
 __global__ void __launch_bounds__(1024) bwd_order_kernel(const int* __restrict__ list_len,
                                                          const int* __restrict__ num_items,
@@ -879,9 +877,10 @@ msa_status_t launch_sparse_bwd(const void* q, const void* k, const void* v, cons
   }
   {
     TraceScope trace_("bwd_order_kernel", stream);
-    // measured on GB300: a 16k pack (134 MB of fp32 dQ) runs 2.4 % faster with
-    // every item sorted, a 32k pack with 64 heads (1 GB) 13 % slower
-    const int tail_div = nq * sizeof(float) <= 2 * device_l2_bytes() ? 1 : 5;
+    // measured on GB300: a 16k pack (134 MB of fp32 dQ) runs 2 % faster with
+    // its last third sorted (every item sorted: as fast, but 1.7x the DRAM
+    // bytes); a 32k pack with 64 heads (1 GB) 1.7 % slower (13 % fully sorted)
+    const int tail_div = nq * sizeof(float) <= 2 * device_l2_bytes() ? 3 : 5;
     launch_pdl(bwd_order_kernel, static_cast<unsigned>(Hkv), 1024, 0, stream, ws.list_len,
         ws.num_items, Hkv, ws.max_items, ws.order, tail_div);
   }
