@@ -247,8 +247,8 @@ def traffic_for(name: str):
 
 
 PREFILL_KERNELS = ("plan_kernel", "index_select_kernel", "fwd_union_kernel", "sparse_fwd_kernel")
-BACKWARD_KERNELS = ("bwd_delta_kernel", "bwd_items_kernel", "bwd_lists_kernel", "bwd_order_kernel",
-                    "sparse_bwd_kernel", "bwd_convert_kernel")
+BACKWARD_KERNELS = ("bwd_delta_kernel", "bwd_lists_kernel", "sparse_bwd_kernel",
+                    "bwd_convert_kernel")
 
 
 def phase_ms(per_step: dict, names) -> float:

@@ -81,6 +81,7 @@ struct BwdWorkspace {
   int* lists;          // [max_items, Hkv, kBwdSegment] positions that selected the item's block
   int* list_len;       // [max_items, Hkv]
   int* order;          // [Hkv, max_items] claim order of the items
+  int* lists_done;     // [Hkv] CTAs of bwd_lists_kernel finished (cleared by the Delta kernel)
   float* lsd;          // [T, Hkv, 2, 16]  -lse log2(e) of the group's 16 rows, then -rowsum(dout * o)
   float* dq_acc;       // [T, Hq, 128] fp32
   float* dk_acc;       // [T, Hkv, 128] fp32

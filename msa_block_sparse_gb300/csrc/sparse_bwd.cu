@@ -8,12 +8,14 @@
 // windows only and the fp32 dQ accumulator lines stay in L2.  Persistent CTAs
 // (one per SM and KV head share) claim the items from a counter, so that a CTA
 // that drew short items takes more; the last fifth of the list (the last third
-// when the dQ accumulator is within twice L2) is claimed largest first
-// (bwd_order_kernel) so that the CTAs finish together.  Per item the CTA holds
+// when the dQ accumulator is within twice L2) is claimed largest first (the
+// order the last CTA of bwd_lists_kernel writes) so that the CTAs finish
+// together.  Per item the CTA holds
 // K_b and V_b in shared memory and streams the window's query tokens that
 // selected b, in ascending order, in half-chunks of 4 tokens x G = 16 heads =
 // 64 columns.  A pre-pass (bwd_lists_kernel) lists, per item, those tokens
-// (one thread per candidate, ballot compaction); another packs (lse log2 e,
+// (one thread per candidate, ballot compaction); another (bwd_delta_kernel,
+// whose CTA 0 also lists the items) packs (lse log2 e,
 // Delta) per query row.
 //   producers (warp 0: K_b / V_b and the even half-chunks; warp 10: the odd
 //            ones; one warp alone cannot issue the copies fast enough): per
@@ -109,20 +111,23 @@ __device__ __forceinline__ void umma_bf16_tmem_a(uint32_t d_tmem, uint32_t a_tme
 
 // ---------------------------------------------------------------- items
 
-// One CTA.  Pairs (window w, sequence s) in w-major order; pair (w, s) holds the
-// key blocks b that some query of window w can select: 128 b < min(len, (w+1) W).
-// Each becomes an item (s, b, first position, end position) of that window.
-// A sequence longer than max_seqlen (or of negative length) is flagged in the
-// status word and clipped.
-__global__ void __launch_bounds__(1024) bwd_items_kernel(const int32_t* __restrict__ cu, int S,
-                                                         int max_seqlen, int num_windows,
-                                                         int4* __restrict__ items,
-                                                         int* __restrict__ num_items,
-                                                         int max_items, uint32_t* status) {
-  pdl_enter();
+// Run by one whole CTA (CTA 0 of the Delta kernel, whose other work it
+// overlaps).  Pairs (window w, sequence s) in w-major order; pair (w, s) holds
+// the key blocks b that some query of window w can select: 128 b < min(len,
+// (w+1) W).  Each becomes an item (s, b, first position, end position) of that
+// window.  A sequence longer than max_seqlen (or of negative length) is
+// flagged in the status word and clipped.  Also clears the per-KV-head
+// arrival counters of bwd_lists_kernel.
+__device__ __forceinline__ void build_items(const int32_t* __restrict__ cu, int S,
+                                            int max_seqlen, int num_windows,
+                                            int4* __restrict__ items,
+                                            int* __restrict__ num_items, int max_items,
+                                            int* __restrict__ lists_done, int Hkv,
+                                            uint32_t* status) {
   __shared__ int warp_sums[32];
   __shared__ int carry;
   if (threadIdx.x == 0) carry = 0;
+  for (int g = threadIdx.x; g < Hkv; g += blockDim.x) lists_done[g] = 0;
   __syncthreads();
   const long long npairs = static_cast<long long>(num_windows) * S;
   for (long long base = 0; base < npairs; base += blockDim.x) {
@@ -179,16 +184,29 @@ __global__ void __launch_bounds__(1024) bwd_items_kernel(const int32_t* __restri
 
 // ---------------------------------------------------------------- token lists
 
-// One CTA of kBwdSegment threads per (item, KV head), grid-striding over items:
-// thread t checks candidate position first + t; the matches are compacted in
-// ascending order into the item's list.
+// Claim order of one KV head's items, written by the last CTA of that head to
+// finish its lists.  The first n - n / tail_div items keep their window-major
+// order (concurrent items add into the dQ rows of a few windows, which keeps
+// the dQ accumulator lines in L2); the rest follow by half-chunk count,
+// largest first, so that the last items claimed are short and the CTAs finish
+// together.  Order within equal counts is unspecified.
+constexpr int kMaxHalfChunks = kBwdSegment / 4;
+
+// gridDim.x CTAs of kBwdSegment threads per KV head (blockIdx.y), grid-striding
+// over the items: thread t checks candidate position first + t; the matches
+// are compacted in ascending order into the item's list.  The CTA that
+// finishes last for its KV head (arrival counter, cleared by build_items)
+// then writes that head's claim order.
 __global__ void __launch_bounds__(kBwdSegment) bwd_lists_kernel(
     const int32_t* __restrict__ cu, const int32_t* __restrict__ sel,
     const int4* __restrict__ items, const int* __restrict__ num_items, int Hkv,
-    int* __restrict__ lists, int* __restrict__ list_len) {
+    int* __restrict__ lists, int* __restrict__ list_len, int* __restrict__ lists_done,
+    int max_items, int* __restrict__ order, int tail_div) {
   pdl_enter();
   static_assert(kBwdSegment == 256, "one thread per candidate position");
   __shared__ int warp_cnt[kBwdSegment / 32];
+  __shared__ int hist[kMaxHalfChunks + 1], start[kMaxHalfChunks + 1];
+  __shared__ int last;
   const int n = *num_items;
   const int g = blockIdx.y;
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
@@ -220,24 +238,13 @@ __global__ void __launch_bounds__(kBwdSegment) bwd_lists_kernel(
     if (threadIdx.x == 0) list_len[li] = total;
     __syncthreads();
   }
-}
-
-// ---------------------------------------------------------------- claim order
-
-// One CTA per KV head.  The first n - n / tail_div items keep their
-// window-major order (concurrent items add into the dQ rows of a few windows,
-// which keeps the dQ accumulator lines in L2); the rest follow by half-chunk
-// count, largest first, so that the last items claimed are short and the CTAs
-// finish together.  Order within equal counts is unspecified.
-constexpr int kMaxHalfChunks = kBwdSegment / 4;
-__global__ void __launch_bounds__(1024) bwd_order_kernel(const int* __restrict__ list_len,
-                                                         const int* __restrict__ num_items,
-                                                         int Hkv, int max_items,
-                                                         int* __restrict__ order, int tail_div) {
-  pdl_enter();
-  __shared__ int hist[kMaxHalfChunks + 1], start[kMaxHalfChunks + 1];
-  const int n = *num_items;
-  const int g = blockIdx.x;
+  // the last CTA of this KV head: every list_len of the head is written
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) last = atomicAdd(lists_done + g, 1) == static_cast<int>(gridDim.x) - 1;
+  __syncthreads();
+  if (!last) return;
+  __threadfence();
   const int k = n - n / tail_div;
   int* ord = order + static_cast<size_t>(g) * max_items;
   for (int i = threadIdx.x; i <= kMaxHalfChunks; i += blockDim.x) hist[i] = 0;
@@ -246,7 +253,8 @@ __global__ void __launch_bounds__(1024) bwd_order_kernel(const int* __restrict__
     if (i < k) {
       ord[i] = i;
     } else {
-      const int nh = min((list_len[static_cast<size_t>(i) * Hkv + g] + 3) / 4, kMaxHalfChunks);
+      const int nh = min((__ldcg(list_len + static_cast<size_t>(i) * Hkv + g) + 3) / 4,
+                         kMaxHalfChunks);
       atomicAdd(&hist[nh], 1);
     }
   }
@@ -260,7 +268,8 @@ __global__ void __launch_bounds__(1024) bwd_order_kernel(const int* __restrict__
   }
   __syncthreads();
   for (int i = k + static_cast<int>(threadIdx.x); i < n; i += blockDim.x) {
-    const int nh = min((list_len[static_cast<size_t>(i) * Hkv + g] + 3) / 4, kMaxHalfChunks);
+    const int nh = min((__ldcg(list_len + static_cast<size_t>(i) * Hkv + g) + 3) / 4,
+                       kMaxHalfChunks);
     ord[atomicAdd(&start[nh], 1)] = i;
   }
 }
@@ -271,11 +280,16 @@ __global__ void __launch_bounds__(1024) bwd_order_kernel(const int* __restrict__
 // lsd[32 (t Hkv + g) + 16 + j] = -sum_d dout o (= -Delta).  16 lanes per row
 // (16-byte loads), kDeltaRows rows per thread with all loads issued first.
 constexpr int kDeltaRows = 4;
-__global__ void __launch_bounds__(256) bwd_delta_kernel(const __nv_bfloat16* __restrict__ o,
-                                                        const __nv_bfloat16* __restrict__ dout,
-                                                        const float* __restrict__ lse,
-                                                        float* __restrict__ lsd, size_t rows) {
+__global__ void __launch_bounds__(256) bwd_delta_kernel(
+    const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* __restrict__ dout,
+    const float* __restrict__ lse, float* __restrict__ lsd, size_t rows,
+    const int32_t* __restrict__ cu, int S, int max_seqlen, int num_windows,
+    int4* __restrict__ items, int* __restrict__ num_items, int max_items,
+    int* __restrict__ lists_done, int Hkv, uint32_t* status) {
   pdl_enter();
+  if (blockIdx.x == 0)
+    build_items(cu, S, max_seqlen, num_windows, items, num_items, max_items, lists_done, Hkv,
+                status);
   const int sub = threadIdx.x & 15;
   const size_t row0 =
       (static_cast<size_t>(blockIdx.x) * (blockDim.x >> 4) + (threadIdx.x >> 4)) * kDeltaRows;
@@ -428,7 +442,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     int pending = 0;
     if (par == 0 && lane == 0) pending = atomicAdd(item_ctr + g, 1);
     for (int itl = 0; alive; ++itl) {
-      // Items are claimed in the order bwd_order_kernel set, first come first
+      // Items are claimed in the order bwd_lists_kernel set, first come first
       // served: warp 0 takes the next one from the KV head's counter and
       // publishes its id (-1 once none are left) in slot itl % kItemSlots, where
       // the other roles read it.
@@ -809,6 +823,7 @@ BwdWorkspace carve_bwd_workspace(WsCursor& ws, int T, int S, int Hq, int Hkv, in
   w.lists = ws.take<int>(static_cast<size_t>(w.max_items) * Hkv * kBwdSegment);
   w.list_len = ws.take<int>(static_cast<size_t>(w.max_items) * Hkv);
   w.order = ws.take<int>(static_cast<size_t>(w.max_items) * Hkv);
+  w.lists_done = ws.take<int>(Hkv);
   w.lsd = ws.take<float>(static_cast<size_t>(T) * Hq * 2);
   // the three accumulators and the item counters stay adjacent and in this
   // order: one clear covers them
@@ -855,36 +870,28 @@ msa_status_t launch_sparse_bwd(const void* q, const void* k, const void* v, cons
 
   const size_t rows = static_cast<size_t>(T) * Hq;
   {
+    // CTA 0 also lists the work items and clears the lists kernel's counters
     TraceScope trace_("bwd_delta_kernel", stream);
     const size_t per_block = 256 / 16 * kDeltaRows;
     launch_pdl(bwd_delta_kernel, static_cast<unsigned>((rows + per_block - 1) / per_block), 256,
         0, stream,
         static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dout), lse, ws.lsd,
-        rows);
+        rows, cu, S, max_seqlen, bwd_windows(max_seqlen), ws.items, ws.num_items, ws.max_items,
+        ws.lists_done, Hkv, st);
   }
   {
-    TraceScope trace_("bwd_items_kernel", stream);
-    launch_pdl(bwd_items_kernel, 1, 1024, 0, stream, cu, S, max_seqlen, bwd_windows(max_seqlen),
-        ws.items,
-        ws.num_items, ws.max_items, st);
-  }
-  {
-    const int sms = device_sm_count();
-    dim3 lgrid(static_cast<unsigned>(ws.max_items < 4 * sms ? ws.max_items : 4 * sms), Hkv);
-    TraceScope trace_("bwd_lists_kernel", stream);
-    launch_pdl(bwd_lists_kernel, lgrid, kBwdSegment, 0, stream, cu, sel, ws.items, ws.num_items, Hkv,
-        ws.lists, ws.list_len);
-  }
-  {
-    TraceScope trace_("bwd_order_kernel", stream);
+    // the last CTA of each KV head also writes that head's claim order
     // measured on GB300: a 16k pack (134 MB of fp32 dQ) runs 2 % faster with
     // its last third sorted (every item sorted: as fast, but 1.7x the DRAM
     // bytes); a 32k pack with 64 heads (1 GB) 1.7 % slower (13 % fully sorted)
     const int tail_div = nq * sizeof(float) <= 2 * device_l2_bytes() ? 3 : 5;
-    launch_pdl(bwd_order_kernel, static_cast<unsigned>(Hkv), 1024, 0, stream, ws.list_len,
-        ws.num_items, Hkv, ws.max_items, ws.order, tail_div);
+    const int sms = device_sm_count();
+    dim3 lgrid(static_cast<unsigned>(ws.max_items < 4 * sms ? ws.max_items : 4 * sms), Hkv);
+    TraceScope trace_("bwd_lists_kernel", stream);
+    launch_pdl(bwd_lists_kernel, lgrid, kBwdSegment, 0, stream, cu, sel, ws.items, ws.num_items,
+        Hkv, ws.lists, ws.list_len, ws.lists_done, ws.max_items, ws.order, tail_div);
   }
-  msa_status_t e = check_launch("bwd_delta/items/lists/order");
+  msa_status_t e = check_launch("bwd_delta/lists");
   if (e != MSA_OK) return e;
 
   const size_t smem = sizeof(BwdSmem);
