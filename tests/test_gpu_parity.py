@@ -117,6 +117,10 @@ def oracle_selection(name, shape, cpu):
     return _cache[key]
 
 
+def oracle_gap(name, shape, cpu):
+    return oracle_selection(name, shape, cpu)[1]
+
+
 # ------------------------------------------------------------------ prologue
 
 @pytest.mark.parametrize("name", ["tiny", "ragged"])
@@ -313,6 +317,15 @@ def test_sparse_fwd_long_sequence(m):
                                  cpu["cu_seqlens"].numpy(), SCALE, tokens=toks)
     assert_close(f64(o[toks]), oo, 2e-2, 1e-2, "long o")
     assert_close(lse[toks].cpu().numpy().astype(np.float64), olse, 1e-3, 1e-4, "long lse")
+    # the index select on the same pack: the long sequence's query tiles have
+    # up to 132 earlier blocks, cut into several chunks whose top-15 lists the
+    # last chunk merges
+    gsel = m.msa_index_select(gpu["q_idx"], gpu["k_idx"], gpu["cu_seqlens"], shape.max_seqlen)
+    m.msa_check_status()
+    compare_selection(gsel.cpu().numpy()[toks], osel[toks], oracle_gap("long", shape, cpu)[toks],
+                      "long select", own_blocks(cpu, toks),
+                      SC.prefill_scores_of(f64(cpu["q_idx"]), f64(cpu["k_idx"]),
+                                           cpu["cu_seqlens"].numpy(), toks))
 
 
 # ------------------------------------------------------------------ backward
