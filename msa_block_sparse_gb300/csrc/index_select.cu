@@ -9,11 +9,11 @@
 // (it is always kept).  A plan kernel cuts each tile's blocks 0 .. qb-1 into
 // chunks of at most C blocks, C chosen so that a pack yields a few units per
 // SM (a pack with few long tiles is split, one with many tiles is not), and
-// lists the units largest first.  The main kernel is persistent (one CTA per
-// SM); warp 0 claims units from a counter and passes each id to the others:
-//   TMA    : the unit's Q tile (two buffers, so the next unit's loads while the
-//            current one finishes), then its K blocks (128 x 128 bf16, 128B
-//            swizzle) into a 4-stage ring that runs on across units
+// lists the units largest first.  The main kernel is persistent (two CTAs per
+// SM, so that one's waits are covered by the other's work); warp 0 claims
+// units from a counter and passes each id to the others:
+//   TMA    : the unit's Q tile, then its K blocks (128 x 128 bf16, 128B
+//            swizzle) into a 2-stage ring that runs on across units
 //   MMA    : S_b = Q K_b^T (M = N = K = 128) into one of two TMEM buffers
 //   epilogue (4 warps, thread = query row = TMEM lane): row max of S_b,
 //            then a register-resident insertion into a descending top-15
@@ -33,7 +33,9 @@ namespace msa {
 
 namespace {
 
-constexpr int kSelStages = 4;
+constexpr int kSelStages = 2;
+constexpr int kSelQBufs = 1;
+constexpr int kSelCtasPerSm = 2;
 constexpr int kSelThreads = 192;         // warp 0 TMA, warp 1 MMA, warps 2..5 epilogue
 constexpr int kTileBytes = 128 * 128 * 2;  // one 128 x 128 bf16 tile
 constexpr uint32_t kSelIdesc = idesc_bf16(128, 128, false, false);
@@ -43,9 +45,9 @@ constexpr int kMinChunk = 16;            // blocks
 constexpr int kPartKeys = 15 * 128;      // one chunk's lists: entry keys, [15][128]
 
 struct SelSmem {
-  uint8_t q[2][kTileBytes];
+  uint8_t q[kSelQBufs][kTileBytes];
   uint8_t k[kSelStages][kTileBytes];
-  uint64_t q_full[2], q_empty[2];
+  uint64_t q_full[kSelQBufs], q_empty[kSelQBufs];
   uint64_t k_full[kSelStages];
   uint64_t k_empty[kSelStages];
   uint64_t s_full[2];
@@ -296,7 +298,7 @@ __global__ void __launch_bounds__(1024) select_plan_kernel(
 
 // ---------------------------------------------------------------- main kernel
 
-__global__ void __launch_bounds__(kSelThreads, 1)
+__global__ void __launch_bounds__(kSelThreads, kSelCtasPerSm)
     index_select_kernel(const __grid_constant__ CUtensorMap tm_q,
                         const __grid_constant__ CUtensorMap tm_k, const int32_t* __restrict__ cu,
                         const int4* __restrict__ units, const int4* __restrict__ aux,
@@ -314,9 +316,11 @@ __global__ void __launch_bounds__(kSelThreads, 1)
   const int lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kSelQBufs; ++i) {
       mbar_init(&sm.q_full[i], 1);
       mbar_init(&sm.q_empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
       mbar_init(&sm.s_full[i], 1);
       mbar_init(&sm.s_empty[i], 128);
     }
@@ -369,8 +373,8 @@ __global__ void __launch_bounds__(kSelThreads, 1)
         }
         const int seq0 = un.x, qb = un.y, b0 = un.z, b1 = un.w, h = ax.x % Hi;
         if (b1 <= b0) continue;
-        const int qbuf = nq & 1;
-        if (!mbar_wait(&sm.q_empty[qbuf], ((nq >> 1) & 1) ^ 1, status, 2)) break;
+        const int qbuf = nq % kSelQBufs;
+        if (!mbar_wait(&sm.q_empty[qbuf], ((nq / kSelQBufs) & 1) ^ 1, status, 2)) break;
         ++nq;
         mbar_arrive_expect_tx(&sm.q_full[qbuf], kTileBytes);
         tma_load_3d(sm.q[qbuf], &tm_q, &sm.q_full[qbuf], 0, h, seq0 + qb * kBlock);
@@ -401,8 +405,8 @@ __global__ void __launch_bounds__(kSelThreads, 1)
         if (u < 0) break;
         const int nb = un.w - un.z;
         if (nb <= 0) continue;
-        const int qbuf = nq & 1;
-        if (!(ok = mbar_wait(&sm.q_full[qbuf], (nq >> 1) & 1, status, 5))) break;
+        const int qbuf = nq % kSelQBufs;
+        if (!(ok = mbar_wait(&sm.q_full[qbuf], (nq / kSelQBufs) & 1, status, 5))) break;
         ++nq;
         const uint32_t qa = smem_u32(sm.q[qbuf]);
         for (int i = 0; i < nb; ++i, ++kb) {
@@ -582,7 +586,7 @@ msa_status_t launch_index_select(const void* q_idx, const void* k_idx, const int
   msa_status_t e = check_launch("select_plan_kernel");
   if (e != MSA_OK) return e;
   const int sms = device_sm_count();
-  const int grid = w.max_units < sms ? w.max_units : sms;
+  const int grid = w.max_units < kSelCtasPerSm * sms ? w.max_units : kSelCtasPerSm * sms;
   {
     TraceScope trace_("index_select_kernel", stream);
     launch_pdl(index_select_kernel, grid, kSelThreads, smem, stream, tq, tk, cu, w.units, w.aux,
