@@ -246,13 +246,34 @@ def traffic_for(name: str):
     return d.get("bytes_per_launch")
 
 
-PREFILL_KERNELS = ("plan_kernel", "index_select_kernel", "fwd_union_kernel", "sparse_fwd_kernel")
+# Kernels of the two timed phases: prefill = msa_index_select + msa_sparse_attn_fwd,
+# backward = msa_sparse_attn_bwd (whose accumulator clearing is a memset, not a kernel).
+PREFILL_KERNELS = ("select_plan_kernel", "index_select_kernel", "plan_kernel", "fwd_union_kernel",
+                   "sparse_fwd_kernel")
 BACKWARD_KERNELS = ("bwd_delta_kernel", "bwd_lists_kernel", "sparse_bwd_kernel",
                     "bwd_convert_kernel")
 
 
 def phase_ms(per_step: dict, names) -> float:
     return sum(per_step.get(n, 0.0) for n in names)
+
+
+def phase_pass(step_fn, nsteps, stream):
+    """Runs `nsteps` steps with CUDA events only at the phase boundaries (before
+    the select call, between the forward and backward calls, after the
+    backward call): each phase's time then includes its memsets, launch gaps
+    and the overlap of its own kernels.  step_fn(i, marks) records marks[0..2].
+    Returns (prefill ms, backward ms or None) per step."""
+    import torch
+    marks = []
+    for i in range(nsteps):
+        mk = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        step_fn(i, mk)
+        marks.append(mk)
+    torch.cuda.synchronize()
+    pf = sum(mk[0].elapsed_time(mk[1]) for mk in marks) / nsteps
+    bw = sum(mk[1].elapsed_time(mk[2]) for mk in marks) / nsteps
+    return pf, bw
 
 
 def time_pack(m, W, workmodel, shape, dev, stream, seed, nsteps, with_bwd, peak, sample=None):
@@ -277,18 +298,24 @@ def time_pack(m, W, workmodel, shape, dev, stream, seed, nsteps, with_bwd, peak,
     if with_bwd:
         g = {n: torch.empty_like(b[r]) for n, r in (("dq", "q"), ("dk", "k"), ("dv", "k"))}
 
-    def step():
+    def step(marks=None):
         m.msa_qk_norm_rope4(x["q"], x["k"], x["q_idx"], x["k_idx"], x["w_q"], x["w_k"],
                             x["w_qi"], x["w_ki"], x["cu_seqlens"],
                             outs=(b["q"], b["k"], b["qi"], b["ki"]))
+        if marks:
+            marks[0].record(stream)
         m.msa_index_select(b["qi"], b["ki"], x["cu_seqlens"], L, out=sel,
                            workspace=ws["index_select"])
         m.msa_sparse_attn_fwd(b["q"], b["k"], x["v"], sel, x["cu_seqlens"], L, out=b["o"],
                               lse=lse, workspace=ws["sparse_attn_fwd"])
+        if marks:
+            marks[1].record(stream)
         if with_bwd:
             m.msa_sparse_attn_bwd(b["q"], b["k"], x["v"], b["o"], x["do"], lse, sel,
                                   x["cu_seqlens"], L, dq=g["dq"], dk=g["dk"], dv=g["dv"],
                                   workspace=ws["sparse_attn_bwd"])
+        if marks:
+            marks[2].record(stream)
 
     for _ in range(3):
         step()
@@ -299,6 +326,7 @@ def time_pack(m, W, workmodel, shape, dev, stream, seed, nsteps, with_bwd, peak,
         step()
     e1.record(stream)
     torch.cuda.synchronize(dev)
+    pf_ms, bw_ms = phase_pass(lambda i, mk: step(mk), nsteps, stream)
     m.msa_trace_begin()
     for _ in range(nsteps):
         step()
@@ -314,16 +342,18 @@ def time_pack(m, W, workmodel, shape, dev, stream, seed, nsteps, with_bwd, peak,
            "step": "qk_norm_rope4 + index_select + sparse_attn_fwd" +
                    (" + sparse_attn_bwd" if with_bwd else ""),
            "useful_tflops": flops / (ms * 1e-3) / 1e12, "kernels_ms": per, "work": wk}
-    pf = phase_ms(per, PREFILL_KERNELS)
+    pf = pf_ms
     f = wk["fwd_flops"] + wk["select_flops"]
     out["prefill"] = {"ms": pf, "tflops": f / (pf * 1e-3) / 1e12,
                       "frac": f / (pf * 1e-3) / 1e12 / peak,
+                      "kernels_sum_ms": phase_ms(per, PREFILL_KERNELS),
                       "kernels": list(PREFILL_KERNELS)}
     if with_bwd:
         t = per.get("sparse_bwd_kernel", 0.0)
-        tb = phase_ms(per, BACKWARD_KERNELS)
+        tb = bw_ms
         out["backward"] = {"ms": tb, "tflops": wk["bwd_flops"] / (tb * 1e-3) / 1e12,
                            "frac": wk["bwd_flops"] / (tb * 1e-3) / 1e12 / peak,
+                           "kernels_sum_ms": phase_ms(per, BACKWARD_KERNELS),
                            "kernel_ms": t,
                            "kernel_frac": wk["bwd_flops"] / (t * 1e-3) / 1e12 / peak}
     if sample is not None:
@@ -385,18 +415,24 @@ def run_ours(args):
                        ("fwd", ("sparse_attn_fwd", T, S, hq, hkv, maxL)),
                        ("bwd", ("sparse_attn_bwd", T, S, hq, hkv, maxL)))}
 
-    def step(x, res=None):
+    def step(x, res=None, marks=None):
         res = work if res is None else res          # where o, dq, dk, dv go
         m.msa_qk_norm_rope4(x["q"], x["k"], x["q_idx"], x["k_idx"], x["w_q"], x["w_k"],
                             x["w_qi"], x["w_ki"], x["cu_seqlens"],
                             outs=(work["q"], work["k"], work["qi"], work["ki"]))
+        if marks:
+            marks[0].record(torch.cuda.current_stream())
         m.msa_index_select(work["qi"], work["ki"], x["cu_seqlens"], maxL, out=work["sel"],
                            workspace=ws["index_select"])
         m.msa_sparse_attn_fwd(work["q"], work["k"], x["v"], work["sel"], x["cu_seqlens"], maxL,
                               out=res["o"], lse=work["lse"], workspace=ws["fwd"])
+        if marks:
+            marks[1].record(torch.cuda.current_stream())
         m.msa_sparse_attn_bwd(work["q"], work["k"], x["v"], res["o"], x["do"], work["lse"],
                               work["sel"], x["cu_seqlens"], maxL, dq=res["dq"], dk=res["dk"],
                               dv=res["dv"], workspace=ws["bwd"])
+        if marks:
+            marks[2].record(torch.cuda.current_stream())
 
     def barrier():
         if world > 1:
@@ -421,6 +457,8 @@ def run_ours(args):
     host_ms = (time.perf_counter() - h0) * 1e3 / args.steps
     ev1.record(stream)
     torch.cuda.synchronize(dev)
+    pf_ms, bw_ms = phase_pass(lambda i, mk: step(pool[i % args.pool], marks=mk), args.steps,
+                              stream)
     # per-kernel times: the same steps again, every launch bracketed by CUDA
     # events on its stream (the events sit between kernels and keep each launch
     # from overlapping its predecessor's tail, so this pass is not the step time)
@@ -483,15 +521,20 @@ def run_ours(args):
             "frac": wk["prologue_bytes"] / (msl * 1e-3) / 1e9 / hbm,
             "frac_of_nominal": wk["prologue_bytes"] / (msl * 1e-3) / 1e9 / NOMINAL_HBM_GBS}
     per_step = {n: v["ms"] / args.steps for n, v in trace.items()}
-    pf = phase_ms(per_step, PREFILL_KERNELS)
+    # phase times from the phase-boundary events (memsets and launch gaps
+    # included); the traced kernels' sum is kept beside them
+    pf, tb = slowest_rank_ms(pf_ms, world, dev), slowest_rank_ms(bw_ms, world, dev)
     pflops = wk["fwd_flops"] + wk["select_flops"]
-    tb = phase_ms(per_step, BACKWARD_KERNELS)
     phases = {"prefill": {"ms": pf, "tflops": pflops / (pf * 1e-3) / 1e12,
                           "frac": pflops / (pf * 1e-3) / 1e12 / burst,
-                          "kernels": list(PREFILL_KERNELS)},
+                          "kernels_sum_ms": phase_ms(per_step, PREFILL_KERNELS),
+                          "kernels": list(PREFILL_KERNELS),
+                          "calls": ["msa_index_select", "msa_sparse_attn_fwd"]},
               "backward": {"ms": tb, "tflops": wk["bwd_flops"] / (tb * 1e-3) / 1e12,
                            "frac": wk["bwd_flops"] / (tb * 1e-3) / 1e12 / burst,
-                           "kernels": list(BACKWARD_KERNELS)}}
+                           "kernels_sum_ms": phase_ms(per_step, BACKWARD_KERNELS),
+                           "kernels": list(BACKWARD_KERNELS),
+                           "calls": ["msa_sparse_attn_bwd"]}}
 
     out = {
         "metric": METRIC,

@@ -33,7 +33,7 @@ struct PrologueArgs {
 };
 
 constexpr int kProTokens = 16;
-constexpr int kProThreads = 256;             // backward and decode-append kernels
+constexpr int kProThreads = 256;             // decode-append kernel
 constexpr int kProSlots = kProThreads / 8;   // rows processed side by side
 // forward kernel: 128 threads (16 rows side by side), one row per thread in
 // each of two register buffers, so the next rows' loads are in flight while
@@ -240,45 +240,65 @@ msa_status_t launch_prologue(const PrologueJob* jobs, int njobs, const int32_t* 
 // tokens and heads).  RoPE is a rotation, so dz = R^T dy (the pairs turned back
 // by the angle); with r = rsqrt(mean(x^2) + eps), xh = x r, g = dz (1 + w):
 //   dx = r (g - xh mean(g xh)),   dw = sum dz xh.
-// Same layout as the forward: groups of 16 tokens, 8 threads per row, thread
-// c < 4 holding the rotated pairs (8c + e, 8c + 32 + e).  CTAs (two per SM)
-// stride over the groups; each thread sums dw for its 16 channels over all its
-// rows, the CTA adds its 32 row slots into one partial row of dw_part, and
-// prologue_bwd_sum_kernel adds the partials in a fixed order (the result does
-// not depend on scheduling).
+// A CTA takes one group of 16 tokens (CTAs take several groups when there are
+// more than 2048) with 128 threads: 8 rows side by side, 16 threads per row
+// holding 8 channels each (thread c < 8: the rotated pairs (4c + e,
+// 4c + 32 + e); c >= 8: the pass-through channels 64 + 8 (c - 8) ..).  Each
+// thread keeps three rows in registers: two rows' loads are in flight while
+// the third is processed.  Few live values per thread keep 7 CTAs on an SM.
+// Each thread sums dw for its 8 channels over its rows, the CTA adds its 8 row
+// slots into one partial row of dw_part, and prologue_bwd_sum_kernel adds the
+// partials in a fixed order (the result does not depend on scheduling).
+constexpr int kPbThreads = 128;
+constexpr int kPbLanes = 16;                 // threads per row
+constexpr int kPbSlots = kPbThreads / kPbLanes;
 
-constexpr int kProBwdUnroll = 2;
-
-__global__ void __launch_bounds__(kProThreads) prologue_bwd_kernel(
+__global__ void __launch_bounds__(kPbThreads, 7) prologue_bwd_kernel(
     const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restrict__ dy,
     __nv_bfloat16* __restrict__ dx, const __nv_bfloat16* __restrict__ w, int H,
     const RopeTurns turns, const int32_t* __restrict__ cu, int S, int T, float eps,
     float* __restrict__ dw_part) {
   pdl_enter();
   __shared__ float2 cs[kProTokens][kRopeDim / 2];
-  __shared__ float wsh[kD];
-  __shared__ float red[kProSlots][kD];
+  __shared__ __align__(16) float wsh[kD];
+  __shared__ float red[kPbSlots][kD + 4];
   const int tid = threadIdx.x;
-  const int c = tid & 7;
-  const int slot = tid >> 3;
-  const int off0 = (c < 4) ? 8 * c : 64 + 16 * (c - 4);
-  const int off1 = (c < 4) ? 8 * c + 32 : 64 + 16 * (c - 4) + 8;
+  const int c = tid & (kPbLanes - 1);
+  const int slot = tid / kPbLanes;
+  const int off0 = (c < 8) ? 4 * c : 64 + 8 * (c - 8);
+  const int off1 = (c < 8) ? 4 * c + 32 : 64 + 8 * (c - 8) + 4;
   for (int k = tid; k < kD; k += blockDim.x) wsh[k] = 1.f + __bfloat162float(w[k]);
-  __syncthreads();
-  float wl[16];
+  float aw[8];
 #pragma unroll
-  for (int e = 0; e < 8; ++e) {
-    wl[e] = wsh[off0 + e];
-    wl[8 + e] = wsh[off1 + e];
-  }
-  float aw[16];
-#pragma unroll
-  for (int e = 0; e < 16; ++e) aw[e] = 0.f;
+  for (int e = 0; e < 8; ++e) aw[e] = 0.f;
+  struct Rows {
+    uint2 xa, xb, ga, gb;
+    int r;                                 // row of the group, -1: none
+  };
   const int ngroups = (T + kProTokens - 1) / kProTokens;
   // grid-stride over groups of 16 tokens; dw accumulates across all of them
   for (int grp = blockIdx.x; grp < ngroups; grp += gridDim.x) {
     const int t0 = grp * kProTokens;
+    const int ntok = min(kProTokens, T - t0);
+    const int rows = ntok * H;
+    const size_t row_base = static_cast<size_t>(t0) * H;   // the CTA's rows are contiguous
+    auto load_rows = [&](int r, Rows& R) {
+      R.r = -1;
+      R.xa = R.xb = R.ga = R.gb = make_uint2(0, 0);
+      if (r < rows) {
+        const __nv_bfloat16* xr = x + (row_base + r) * kD;
+        const __nv_bfloat16* gr = dy + (row_base + r) * kD;
+        R.xa = __ldcs(reinterpret_cast<const uint2*>(xr + off0));
+        R.xb = __ldcs(reinterpret_cast<const uint2*>(xr + off1));
+        R.ga = __ldcs(reinterpret_cast<const uint2*>(gr + off0));
+        R.gb = __ldcs(reinterpret_cast<const uint2*>(gr + off1));
+        R.r = r;
+      }
+    };
+    Rows ra, rb, rc;
     __syncthreads();                       // the previous group's angles are consumed
+    load_rows(slot, ra);                   // in flight while the angles are computed
+    load_rows(kPbSlots + slot, rb);
     for (int q = tid; q < kProTokens * (kRopeDim / 2); q += blockDim.x) {
       const int qt = q / (kRopeDim / 2), i = q % (kRopeDim / 2);
       const int t = t0 + qt;
@@ -298,149 +318,146 @@ __global__ void __launch_bounds__(kProThreads) prologue_bwd_kernel(
     }
     __syncthreads();
 
-    const int ntok = min(kProTokens, T - t0);
-    const int rows = ntok * H;
-    const size_t row_base = static_cast<size_t>(t0) * H;   // the CTA's rows are contiguous
-    // the loop bound is uniform over the CTA: every lane reaches the shuffles
-    for (int base = 0; base < rows; base += kProSlots * kProBwdUnroll) {
-      uint4 xa[kProBwdUnroll], xb[kProBwdUnroll], ga[kProBwdUnroll], gb[kProBwdUnroll];
+    auto process = [&](const Rows& R) {
+      const bool valid = R.r >= 0;
+      const int tl = valid ? R.r / H : 0;
+      float xv[8], dz[8];
+      {
+        const __nv_bfloat162* pa = reinterpret_cast<const __nv_bfloat162*>(&R.xa);
+        const __nv_bfloat162* pb = reinterpret_cast<const __nv_bfloat162*>(&R.xb);
+        const __nv_bfloat162* qa = reinterpret_cast<const __nv_bfloat162*>(&R.ga);
+        const __nv_bfloat162* qb = reinterpret_cast<const __nv_bfloat162*>(&R.gb);
 #pragma unroll
-      for (int u = 0; u < kProBwdUnroll; ++u) {
-        const int r = base + slot + kProSlots * u;
-        xa[u] = xb[u] = ga[u] = gb[u] = make_uint4(0, 0, 0, 0);
-        if (r < rows) {
-          const __nv_bfloat16* xr = x + (row_base + r) * kD;
-          const __nv_bfloat16* gr = dy + (row_base + r) * kD;
-          xa[u] = __ldcs(reinterpret_cast<const uint4*>(xr + off0));
-          xb[u] = __ldcs(reinterpret_cast<const uint4*>(xr + off1));
-          ga[u] = __ldcs(reinterpret_cast<const uint4*>(gr + off0));
-          gb[u] = __ldcs(reinterpret_cast<const uint4*>(gr + off1));
+        for (int e = 0; e < 2; ++e) {
+          const float2 fa = __bfloat1622float2(pa[e]), fb = __bfloat1622float2(pb[e]);
+          const float2 da = __bfloat1622float2(qa[e]), db = __bfloat1622float2(qb[e]);
+          xv[2 * e] = fa.x;
+          xv[2 * e + 1] = fa.y;
+          xv[4 + 2 * e] = fb.x;
+          xv[4 + 2 * e + 1] = fb.y;
+          dz[2 * e] = da.x;
+          dz[2 * e + 1] = da.y;
+          dz[4 + 2 * e] = db.x;
+          dz[4 + 2 * e + 1] = db.y;
         }
       }
+      if (c < 8) {
+        // dz = R^T dy for the pairs (4c + e, 4c + 32 + e), frequency 4c + e
+        const float4* cp = reinterpret_cast<const float4*>(&cs[tl][4 * c]);
 #pragma unroll
-      for (int u = 0; u < kProBwdUnroll; ++u) {
-        const int r = base + slot + kProSlots * u;
-        const bool valid = r < rows;
-        const int tl = valid ? r / H : 0;
-        float xv[16], dz[16];
-        {
-          const __nv_bfloat162* pa = reinterpret_cast<const __nv_bfloat162*>(&xa[u]);
-          const __nv_bfloat162* pb = reinterpret_cast<const __nv_bfloat162*>(&xb[u]);
-          const __nv_bfloat162* qa = reinterpret_cast<const __nv_bfloat162*>(&ga[u]);
-          const __nv_bfloat162* qb = reinterpret_cast<const __nv_bfloat162*>(&gb[u]);
+        for (int e2 = 0; e2 < 2; ++e2) {
+          const float4 q4 = cp[e2];
+          const float cc[2] = {q4.x, q4.z}, sn[2] = {q4.y, q4.w};
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float2 fa = __bfloat1622float2(pa[e]), fb = __bfloat1622float2(pb[e]);
-            const float2 da = __bfloat1622float2(qa[e]), db = __bfloat1622float2(qb[e]);
-            xv[2 * e] = fa.x;
-            xv[2 * e + 1] = fa.y;
-            xv[8 + 2 * e] = fb.x;
-            xv[8 + 2 * e + 1] = fb.y;
-            dz[2 * e] = da.x;
-            dz[2 * e + 1] = da.y;
-            dz[8 + 2 * e] = db.x;
-            dz[8 + 2 * e + 1] = db.y;
+          for (int h = 0; h < 2; ++h) {
+            const int e = 2 * e2 + h;
+            const float d1 = dz[e], d2 = dz[4 + e];
+            dz[e] = d1 * cc[h] + d2 * sn[h];
+            dz[4 + e] = d2 * cc[h] - d1 * sn[h];
           }
-        }
-        if (c < 4) {
-          // dz = R^T dy for the pairs (8c + e, 8c + 32 + e), frequency 8c + e
-          const float4* cp = reinterpret_cast<const float4*>(&cs[tl][8 * c]);
-#pragma unroll
-          for (int e2 = 0; e2 < 4; ++e2) {
-            const float4 q4 = cp[e2];
-            const float cc[2] = {q4.x, q4.z}, sn[2] = {q4.y, q4.w};
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-              const int e = 2 * e2 + h;
-              const float d1 = dz[e], d2 = dz[8 + e];
-              dz[e] = d1 * cc[h] + d2 * sn[h];
-              dz[8 + e] = d2 * cc[h] - d1 * sn[h];
-            }
-          }
-        }
-        float s4[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int e = 0; e < 16; ++e) s4[e & 3] = fmaf(xv[e], xv[e], s4[e & 3]);
-        float ss = (s4[0] + s4[1]) + (s4[2] + s4[3]);
-#pragma unroll
-        for (int m = 4; m >= 1; m >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, m);
-        const float rinv = rsqrtf(ss * (1.f / kD) + eps);
-        float xh[16], gg[16];
-        float d4[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          xh[e] = xv[e] * rinv;
-          gg[e] = dz[e] * wl[e];
-          d4[e & 3] = fmaf(gg[e], xh[e], d4[e & 3]);
-        }
-        float dot = (d4[0] + d4[1]) + (d4[2] + d4[3]);
-#pragma unroll
-        for (int m = 4; m >= 1; m >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, m);
-        const float mean = dot * (1.f / kD);
-        if (valid) {
-          float o[16];
-#pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            o[e] = rinv * (gg[e] - xh[e] * mean);
-            aw[e] = fmaf(dz[e], xh[e], aw[e]);
-          }
-          uint4 oa, ob;
-          oa.x = pack_bf16x2(o[0], o[1]);
-          oa.y = pack_bf16x2(o[2], o[3]);
-          oa.z = pack_bf16x2(o[4], o[5]);
-          oa.w = pack_bf16x2(o[6], o[7]);
-          ob.x = pack_bf16x2(o[8], o[9]);
-          ob.y = pack_bf16x2(o[10], o[11]);
-          ob.z = pack_bf16x2(o[12], o[13]);
-          ob.w = pack_bf16x2(o[14], o[15]);
-          __nv_bfloat16* dr = dx + (row_base + r) * kD;
-          *reinterpret_cast<uint4*>(dr + off0) = oa;
-          *reinterpret_cast<uint4*>(dr + off1) = ob;
         }
       }
+      float s2[2] = {0.f, 0.f};
+#pragma unroll
+      for (int e = 0; e < 8; ++e) s2[e & 1] = fmaf(xv[e], xv[e], s2[e & 1]);
+      float ss = s2[0] + s2[1];
+#pragma unroll
+      for (int m = kPbLanes / 2; m >= 1; m >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, m);
+      const float rinv = rsqrtf(ss * (1.f / kD) + eps);
+      float gw[8];
+      {
+        const float4 w0 = *reinterpret_cast<const float4*>(&wsh[off0]);
+        const float4 w1 = *reinterpret_cast<const float4*>(&wsh[off1]);
+        gw[0] = w0.x; gw[1] = w0.y; gw[2] = w0.z; gw[3] = w0.w;
+        gw[4] = w1.x; gw[5] = w1.y; gw[6] = w1.z; gw[7] = w1.w;
+      }
+      float d2[2] = {0.f, 0.f};
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        xv[e] *= rinv;                     // xh
+        gw[e] *= dz[e];                    // g = dz (1 + w)
+        d2[e & 1] = fmaf(gw[e], xv[e], d2[e & 1]);
+      }
+      float dot = d2[0] + d2[1];
+#pragma unroll
+      for (int m = kPbLanes / 2; m >= 1; m >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, m);
+      const float mean = dot * (1.f / kD);
+      if (valid) {
+        float o[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          o[e] = rinv * (gw[e] - xv[e] * mean);
+          aw[e] = fmaf(dz[e], xv[e], aw[e]);
+        }
+        uint2 oa, ob;
+        oa.x = pack_bf16x2(o[0], o[1]);
+        oa.y = pack_bf16x2(o[2], o[3]);
+        ob.x = pack_bf16x2(o[4], o[5]);
+        ob.y = pack_bf16x2(o[6], o[7]);
+        __nv_bfloat16* dr = dx + (row_base + R.r) * kD;
+        *reinterpret_cast<uint2*>(dr + off0) = oa;
+        *reinterpret_cast<uint2*>(dr + off1) = ob;
+      }
+    };
+    // the loop bound is uniform over the CTA: every lane reaches the shuffles;
+    // two rows' loads are in flight while the third row is processed
+    for (int base = 0; base < rows; base += 3 * kPbSlots) {
+      load_rows(base + 2 * kPbSlots + slot, rc);
+      process(ra);
+      if (base + kPbSlots >= rows) break;
+      load_rows(base + 3 * kPbSlots + slot, ra);
+      process(rb);
+      if (base + 2 * kPbSlots >= rows) break;
+      load_rows(base + 4 * kPbSlots + slot, rb);
+      process(rc);
     }
   }
-  // ---- dw: the CTA's 32 row slots -> one partial row
+  // ---- dw: the CTA's 8 row slots -> one partial row
 #pragma unroll
-  for (int e = 0; e < 8; ++e) {
+  for (int e = 0; e < 4; ++e) {
     red[slot][off0 + e] = aw[e];
-    red[slot][off1 + e] = aw[8 + e];
+    red[slot][off1 + e] = aw[4 + e];
   }
   __syncthreads();
   for (int ch = tid; ch < kD; ch += blockDim.x) {
     float acc = 0.f;
-    for (int sl = 0; sl < kProSlots; ++sl) acc += red[sl][ch];
+    for (int sl = 0; sl < kPbSlots; ++sl) acc += red[sl][ch];
     dw_part[static_cast<size_t>(blockIdx.x) * kD + ch] = acc;
   }
 }
 
-// dw[ch] = sum over the partial rows, in a fixed order: 1024 threads, 8 per
-// channel, each summing every 8th partial, then a sum of the 8 in order.
+// dw[ch] = sum over the partial rows in a fixed order (the result does not
+// depend on scheduling): CTA b takes channels 8b .. 8b + 7 with 1024 threads,
+// thread (k, ch) adds the partials k, k + 128, ... of its channel, then a
+// pairwise tree over k in shared memory.
+constexpr int kPbSumChannels = 8;
+constexpr int kPbSumWays = 1024 / kPbSumChannels;
 __global__ void __launch_bounds__(1024) prologue_bwd_sum_kernel(const float* __restrict__ part,
                                                                 int nparts,
                                                                 float* __restrict__ dw) {
   pdl_enter();
-  __shared__ float red[8][kD];
-  const int ch = threadIdx.x & (kD - 1), k = threadIdx.x >> 7;
+  __shared__ float red[kPbSumWays][kPbSumChannels];
+  const int cl = threadIdx.x % kPbSumChannels, k = threadIdx.x / kPbSumChannels;
+  const int ch = blockIdx.x * kPbSumChannels + cl;
   float acc = 0.f;
-  for (int p = k; p < nparts; p += 8) acc += part[static_cast<size_t>(p) * kD + ch];
-  red[k][ch] = acc;
+  for (int p = k; p < nparts; p += kPbSumWays) acc += part[static_cast<size_t>(p) * kD + ch];
+  red[k][cl] = acc;
   __syncthreads();
-  if (k == 0) {
-    float t = 0.f;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) t += red[i][ch];
-    dw[ch] = t;
+  for (int s = kPbSumWays / 2; s >= 1; s >>= 1) {
+    if (k < s) red[k][cl] += red[k + s][cl];
+    __syncthreads();
   }
+  if (k == 0) dw[ch] = red[0][cl];
 }
 
-constexpr int kProBwdMaxCtas = 2 * 1024;   // partial rows at most (2 per SM)
+constexpr int kProBwdMaxCtas = 2048;   // partial rows at most
 
+// one CTA per group of 16 tokens up to 2048 groups (32k tokens), then CTAs
+// take several groups each
 static int prologue_bwd_ctas(int T) {
   const int groups = (T + kProTokens - 1) / kProTokens;
-  int ctas = 2 * device_sm_count();
-  if (ctas > kProBwdMaxCtas) ctas = kProBwdMaxCtas;
-  return groups < ctas ? groups : ctas;
+  return groups < kProBwdMaxCtas ? groups : kProBwdMaxCtas;
 }
 
 size_t prologue_bwd_workspace_floats(int T) {
@@ -461,14 +478,14 @@ msa_status_t launch_prologue_bwd(const __nv_bfloat16* x, const __nv_bfloat16* dy
   const int nparts = prologue_bwd_ctas(T);
   {
     TraceScope trace_("prologue_bwd_kernel", stream);
-    launch_pdl(prologue_bwd_kernel, nparts, kProThreads, 0, stream, x, dy, dx, w, H, turns, cu, S, T,
+    launch_pdl(prologue_bwd_kernel, nparts, kPbThreads, 0, stream, x, dy, dx, w, H, turns, cu, S, T,
         eps, dw_part);
   }
   msa_status_t e = check_launch("prologue_bwd_kernel");
   if (e != MSA_OK) return e;
   {
     TraceScope trace_("prologue_bwd_sum_kernel", stream);
-    launch_pdl(prologue_bwd_sum_kernel, 1, 1024, 0, stream, dw_part, nparts, dw);
+    launch_pdl(prologue_bwd_sum_kernel, kD / kPbSumChannels, 1024, 0, stream, dw_part, nparts, dw);
   }
   return check_launch("prologue_bwd_sum_kernel");
 }
