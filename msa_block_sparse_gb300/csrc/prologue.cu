@@ -6,12 +6,12 @@
 //
 // Layout of the work: a CTA takes 16 consecutive tokens of every tensor of the
 // call (q, k, index q, index k: one set of angles serves them all) and sweeps
-// their rows with 8 threads per row.  Thread c < 4 of a row holds channels
-// [8c, 8c + 8) and [8c + 32, 8c + 40): the rotated pairs (i, i + 32) sit in one
-// thread, so the rotation needs no shuffles; threads 4..7 hold the
-// pass-through channels 64..127.  Each thread keeps two rows in registers: the
-// next row's loads are issued before the current row is processed, and the
-// first rows' loads before the angles are computed.
+// their rows with 16 threads per row.  Thread c < 8 of a row holds channels
+// [4c, 4c + 4) and [4c + 32, 4c + 36): the rotated pairs (i, i + 32) sit in one
+// thread, so the rotation needs no shuffles; threads 8..15 hold the
+// pass-through channels 64..127.  Each thread keeps four rows in registers:
+// three rows' loads are in flight while the fourth is processed, and the first
+// rows' loads are issued before the angles are computed.
 //
 // Angles avoid a large fp32 argument: the host turns each frequency f_i into
 // the 64-bit fixed-point fraction F_i = f_i / (2 pi) * 2^64 of a turn, so
@@ -35,29 +35,31 @@ struct PrologueArgs {
 constexpr int kProTokens = 16;
 constexpr int kProThreads = 256;             // decode-append kernel
 constexpr int kProSlots = kProThreads / 8;   // rows processed side by side
-// forward kernel: 128 threads (16 rows side by side), one row per thread in
-// each of two register buffers, so the next rows' loads are in flight while
-// the current rows are normalised, rotated and stored
+// forward kernel: 128 threads, 8 rows side by side with 16 threads per row
+// (8 channels each: thread c < 8 holds the rotated pairs (4c + e, 4c + 32 + e),
+// c >= 8 the pass-through channels 64 + 8 (c - 8) ..); four rows per thread in
+// registers, so three rows' loads are in flight while the fourth is
+// normalised, rotated and stored (62 registers, 8 CTAs per SM)
 constexpr int kPfThreads = 128;
-constexpr int kPfSlots = kPfThreads / 8;
-constexpr int kPfUnroll = 1;
+constexpr int kPfLanes = 16;
+constexpr int kPfSlots = kPfThreads / kPfLanes;
 
-__global__ void __launch_bounds__(kPfThreads) prologue_kernel(const PrologueArgs args,
-                                                               const RopeTurns turns,
-                                                               const int32_t* __restrict__ cu,
-                                                               int S, int T, float eps,
-                                                               uint32_t* status) {
+__global__ void __launch_bounds__(kPfThreads, 8) prologue_kernel(const PrologueArgs args,
+                                                                  const RopeTurns turns,
+                                                                  const int32_t* __restrict__ cu,
+                                                                  int S, int T, float eps,
+                                                                  uint32_t* status) {
   pdl_enter();
   __shared__ float2 cs[kProTokens][kRopeDim / 2];
-  __shared__ float wsh[4][kD];
+  __shared__ __align__(16) float wsh[4][kD];
   const int t0 = blockIdx.x * kProTokens;
   const int tid = threadIdx.x;
   const int hsum = args.hstart[4];
-  const int c = tid & 7;                  // channel group of the row
-  const int slot = tid >> 3;
-  // channel offsets (elements) of this thread's two 8-channel pieces
-  const int off0 = (c < 4) ? 8 * c : 64 + 16 * (c - 4);
-  const int off1 = (c < 4) ? 8 * c + 32 : 64 + 16 * (c - 4) + 8;
+  const int c = tid & (kPfLanes - 1);     // channel group of the row
+  const int slot = tid / kPfLanes;
+  // channel offsets (elements) of this thread's two 4-channel pieces
+  const int off0 = (c < 8) ? 4 * c : 64 + 8 * (c - 8);
+  const int off1 = (c < 8) ? 4 * c + 32 : 64 + 8 * (c - 8) + 4;
   // 1 + w of every job (read after the barrier below)
   for (int k = tid; k < 4 * kD; k += blockDim.x) {
     const int j = k / kD;
@@ -67,8 +69,8 @@ __global__ void __launch_bounds__(kPfThreads) prologue_kernel(const PrologueArgs
   const int ntok = min(kProTokens, T - t0);
   const int rows = ntok * hsum;
 
-  // This thread's rows are slot, slot + 32, slot + 64, ...; (tl, k) = (token of
-  // the CTA, row within the token) advances by 32 rows per step without a
+  // This thread's rows are slot, slot + 8, slot + 16, ...; (tl, k) = (token of
+  // the CTA, row within the token) advances by 8 rows per step without a
   // division once hsum is known.
   int tl = slot / hsum, k = slot - (slot / hsum) * hsum;
   auto advance = [&]() {
@@ -79,34 +81,34 @@ __global__ void __launch_bounds__(kPfThreads) prologue_kernel(const PrologueArgs
     }
   };
   struct Rows {
-    uint4 xa[kPfUnroll], xb[kPfUnroll];
-    int rj[kPfUnroll], rtl[kPfUnroll];
-    size_t rrow[kPfUnroll];
+    uint2 xa, xb;
+    int rj, rtl;
+    size_t rrow;
   };
-  Rows ra, rb;
-  auto load_rows = [&](int base, Rows& R) {
-#pragma unroll
-    for (int u = 0; u < kPfUnroll; ++u) {
-      const int r = base + slot + kPfSlots * u;
-      R.rj[u] = -1;
-      R.rtl[u] = 0;
-      R.rrow[u] = 0;
-      R.xa[u] = make_uint4(0, 0, 0, 0);
-      R.xb[u] = R.xa[u];
-      if (r < rows) {
-        const int j = (k >= args.hstart[1]) + (k >= args.hstart[2]) + (k >= args.hstart[3]);
-        const size_t row = static_cast<size_t>(t0 + tl) * args.jobs[j].H + (k - args.hstart[j]);
-        const __nv_bfloat16* src = args.jobs[j].x + row * kD;
-        R.xa[u] = __ldcs(reinterpret_cast<const uint4*>(src + off0));
-        R.xb[u] = __ldcs(reinterpret_cast<const uint4*>(src + off1));
-        R.rj[u] = j;
-        R.rtl[u] = tl;
-        R.rrow[u] = row;
-      }
+  Rows ra, rb, rc, rd;
+  // loads the thread's next row (rows are taken in order; r = the row index)
+  auto load_rows = [&](int r, Rows& R) {
+    R.rj = -1;
+    R.rtl = 0;
+    R.rrow = 0;
+    R.xa = make_uint2(0, 0);
+    R.xb = R.xa;
+    if (r < rows) {
+      const int j = (k >= args.hstart[1]) + (k >= args.hstart[2]) + (k >= args.hstart[3]);
+      const size_t row = static_cast<size_t>(t0 + tl) * args.jobs[j].H + (k - args.hstart[j]);
+      const __nv_bfloat16* src = args.jobs[j].x + row * kD;
+      R.xa = __ldcs(reinterpret_cast<const uint2*>(src + off0));
+      R.xb = __ldcs(reinterpret_cast<const uint2*>(src + off1));
+      R.rj = j;
+      R.rtl = tl;
+      R.rrow = row;
       advance();
     }
   };
-  load_rows(0, ra);   // in flight while the angles are computed
+  // the first rows' loads are in flight while the angles are computed
+  load_rows(slot, ra);
+  load_rows(kPfSlots + slot, rb);
+  load_rows(2 * kPfSlots + slot, rc);
   // (cos, sin) for the CTA's tokens: thread = (token, frequency)
   for (int q = tid; q < kProTokens * (kRopeDim / 2); q += blockDim.x) {
     const int qt = q / (kRopeDim / 2), i = q % (kRopeDim / 2);
@@ -127,81 +129,77 @@ __global__ void __launch_bounds__(kPfThreads) prologue_kernel(const PrologueArgs
   }
   __syncthreads();
 
-  auto process = [&](Rows& R) {
+  auto process = [&](const Rows& R) {
+    float x[8];
+    {
+      const __nv_bfloat162* pa = reinterpret_cast<const __nv_bfloat162*>(&R.xa);
+      const __nv_bfloat162* pb = reinterpret_cast<const __nv_bfloat162*>(&R.xb);
 #pragma unroll
-    for (int u = 0; u < kPfUnroll; ++u) {
-      float x[16];
-      {
-        const __nv_bfloat162* pa = reinterpret_cast<const __nv_bfloat162*>(&R.xa[u]);
-        const __nv_bfloat162* pb = reinterpret_cast<const __nv_bfloat162*>(&R.xb[u]);
+      for (int e = 0; e < 2; ++e) {
+        const float2 fa = __bfloat1622float2(pa[e]);
+        const float2 fb = __bfloat1622float2(pb[e]);
+        x[2 * e] = fa.x;
+        x[2 * e + 1] = fa.y;
+        x[4 + 2 * e] = fb.x;
+        x[4 + 2 * e + 1] = fb.y;
+      }
+    }
+    float s2[2] = {0.f, 0.f};
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float2 fa = __bfloat1622float2(pa[e]);
-          const float2 fb = __bfloat1622float2(pb[e]);
-          x[2 * e] = fa.x;
-          x[2 * e + 1] = fa.y;
-          x[8 + 2 * e] = fb.x;
-          x[8 + 2 * e + 1] = fb.y;
+    for (int e = 0; e < 8; ++e) s2[e & 1] = fmaf(x[e], x[e], s2[e & 1]);
+    float ss = s2[0] + s2[1];
+#pragma unroll
+    for (int m = kPfLanes / 2; m >= 1; m >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, m);
+    const int j = R.rj < 0 ? 0 : R.rj;
+    const float rinv = rsqrtf(ss * (1.f / kD) + eps);
+    {
+      const float4 w0 = *reinterpret_cast<const float4*>(&wsh[j][off0]);
+      const float4 w1 = *reinterpret_cast<const float4*>(&wsh[j][off1]);
+      const float w[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+#pragma unroll
+      for (int e = 0; e < 8; ++e) x[e] *= rinv * w[e];
+    }
+    if (c < 8) {
+      // rotate channel 4c + e (x1) with 4c + 32 + e (x2), frequency 4c + e
+      const float4* cp = reinterpret_cast<const float4*>(&cs[R.rtl][4 * c]);
+#pragma unroll
+      for (int e2 = 0; e2 < 2; ++e2) {
+        const float4 q = cp[e2];   // (cos, sin) of frequencies 2 e2, 2 e2 + 1
+        const float cc[2] = {q.x, q.z}, sn[2] = {q.y, q.w};
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int e = 2 * e2 + h;
+          const float x1 = x[e], x2 = x[4 + e];
+          x[e] = x1 * cc[h] - x2 * sn[h];
+          x[4 + e] = x2 * cc[h] + x1 * sn[h];
         }
       }
-      float s4[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-      for (int e = 0; e < 16; ++e) s4[e & 3] = fmaf(x[e], x[e], s4[e & 3]);
-      float ss = (s4[0] + s4[1]) + (s4[2] + s4[3]);
-#pragma unroll
-      for (int m = 4; m >= 1; m >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, m);
-      const int j = R.rj[u] < 0 ? 0 : R.rj[u];
-      const float rinv = rsqrtf(ss * (1.f / kD) + eps);
-      {
-        const float4* wa = reinterpret_cast<const float4*>(&wsh[j][off0]);
-        const float4* wb = reinterpret_cast<const float4*>(&wsh[j][off1]);
-        const float4 w0 = wa[0], w1 = wa[1], w2 = wb[0], w3 = wb[1];
-        const float w[16] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w,
-                             w2.x, w2.y, w2.z, w2.w, w3.x, w3.y, w3.z, w3.w};
-#pragma unroll
-        for (int e = 0; e < 16; ++e) x[e] *= rinv * w[e];
-      }
-      if (c < 4) {
-        // rotate channel 8c + e (x1) with 8c + 32 + e (x2), frequency 8c + e
-        const float4* cp = reinterpret_cast<const float4*>(&cs[R.rtl[u]][8 * c]);
-#pragma unroll
-        for (int e2 = 0; e2 < 4; ++e2) {
-          const float4 q = cp[e2];   // (cos, sin) of frequencies 2 e2, 2 e2 + 1
-          const float cc[2] = {q.x, q.z}, sn[2] = {q.y, q.w};
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const int e = 2 * e2 + h;
-            const float x1 = x[e], x2 = x[8 + e];
-            x[e] = x1 * cc[h] - x2 * sn[h];
-            x[8 + e] = x2 * cc[h] + x1 * sn[h];
-          }
-        }
-      }
-      if (R.rj[u] >= 0) {
-        uint4 oa, ob;
-        oa.x = pack_bf16x2(x[0], x[1]);
-        oa.y = pack_bf16x2(x[2], x[3]);
-        oa.z = pack_bf16x2(x[4], x[5]);
-        oa.w = pack_bf16x2(x[6], x[7]);
-        ob.x = pack_bf16x2(x[8], x[9]);
-        ob.y = pack_bf16x2(x[10], x[11]);
-        ob.z = pack_bf16x2(x[12], x[13]);
-        ob.w = pack_bf16x2(x[14], x[15]);
-        __nv_bfloat16* dst = args.jobs[R.rj[u]].y + R.rrow[u] * kD;
-        *reinterpret_cast<uint4*>(dst + off0) = oa;
-        *reinterpret_cast<uint4*>(dst + off1) = ob;
-      }
+    }
+    if (R.rj >= 0) {
+      uint2 oa, ob;
+      oa.x = pack_bf16x2(x[0], x[1]);
+      oa.y = pack_bf16x2(x[2], x[3]);
+      ob.x = pack_bf16x2(x[4], x[5]);
+      ob.y = pack_bf16x2(x[6], x[7]);
+      __nv_bfloat16* dst = args.jobs[R.rj].y + R.rrow * kD;
+      *reinterpret_cast<uint2*>(dst + off0) = oa;
+      *reinterpret_cast<uint2*>(dst + off1) = ob;
     }
   };
   // the loop bound is uniform over the CTA: every lane reaches the shuffles;
-  // the next rows' loads are in flight while the current ones are processed
-  constexpr int kStep = kPfSlots * kPfUnroll;
-  for (int base = 0; base < rows; base += 2 * kStep) {
-    if (base + kStep < rows) load_rows(base + kStep, rb);
+  // three rows' loads are in flight while the fourth row is processed
+  for (int base = 0; base < rows; base += 4 * kPfSlots) {
+    load_rows(base + 3 * kPfSlots + slot, rd);
     process(ra);
-    if (base + kStep >= rows) break;
-    if (base + 2 * kStep < rows) load_rows(base + 2 * kStep, ra);
+    if (base + kPfSlots >= rows) break;
+    load_rows(base + 4 * kPfSlots + slot, ra);
     process(rb);
+    if (base + 2 * kPfSlots >= rows) break;
+    load_rows(base + 5 * kPfSlots + slot, rb);
+    process(rc);
+    if (base + 3 * kPfSlots >= rows) break;
+    load_rows(base + 6 * kPfSlots + slot, rc);
+    process(rd);
   }
 }
 
@@ -295,7 +293,7 @@ __global__ void __launch_bounds__(kPbThreads, 7) prologue_bwd_kernel(
         R.r = r;
       }
     };
-    Rows ra, rb, rc;
+    Rows ra, rb, rc, rd;
     __syncthreads();                       // the previous group's angles are consumed
     load_rows(slot, ra);                   // in flight while the angles are computed
     load_rows(kPbSlots + slot, rb);
