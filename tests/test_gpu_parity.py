@@ -177,6 +177,40 @@ def test_prologue_full_size_sampled(m):
         assert_prologue_close(f64(got[toks]), oracle_prologue_rows(cpu, n, wn, toks), f"cfg2 {n}")
 
 
+@pytest.mark.parametrize("heads", [(3, 5, 1), (7, 2, 3)])
+def test_prologue_odd_head_counts(m, heads):
+    """Head counts that do not fill the kernels' row slots evenly (the four
+    tensors' rows of a token interleave across slots and CTAs), on a ragged
+    pack with an empty and a one-token sequence: the forward of the 4-tensor
+    call and the backward of each tensor against the oracle."""
+    hq, hkv, hi = heads
+    shape = W.PrefillShape("odd-heads", (300, 0, 1, 777, 129), hq, hkv, hi)
+    gen = torch.Generator().manual_seed(101 + hq)
+    T = shape.T
+    x = {n: torch.randn((T, h, 128), generator=gen).to(torch.bfloat16)
+         for n, h in (("q", hq), ("k", hkv), ("q_idx", hi), ("k_idx", hi))}
+    w = {n: (0.1 * torch.randn(128, generator=gen)).to(torch.bfloat16)
+         for n in ("w_q", "w_k", "w_qi", "w_ki")}
+    cu_cpu = shape.cu_seqlens()
+    cun = cu_cpu.numpy()
+    g = {n: v.to(DEV) for n, v in list(x.items()) + list(w.items())}
+    cu = cu_cpu.to(DEV)
+    outs = m.msa_qk_norm_rope4(g["q"], g["k"], g["q_idx"], g["k_idx"], g["w_q"], g["w_k"],
+                               g["w_qi"], g["w_ki"], cu)
+    m.msa_check_status()
+    for got, n, wn in zip(outs, ("q", "k", "q_idx", "k_idx"), ("w_q", "w_k", "w_qi", "w_ki")):
+        assert_prologue_close(f64(got), O.qk_norm_rope(f64(x[n]), f64(w[wn]), cun), f"{heads} {n}")
+    for n, wn in (("q", "w_q"), ("k", "w_k")):
+        dy_cpu = torch.randn(x[n].shape, generator=gen).to(torch.bfloat16)
+        dx, dw = m.msa_qk_norm_rope_bwd(g[n], dy_cpu.to(DEV), g[wn], cu)
+        m.msa_check_status()
+        want_dx, want_dw = O.qk_norm_rope_bwd(f64(x[n]), f64(w[wn]), f64(dy_cpu), cun)
+        off = np.abs(f64(dx) - want_dx)
+        tol = bf16_step(want_dx) * 1.0001 + 1e-5 * np.max(np.abs(want_dx), axis=-1, keepdims=True)
+        assert float(np.max(off - tol)) <= 0, f"{heads} {n} dx"
+        assert rel_l2(f64(dw), want_dw) <= 1e-4, f"{heads} {n} dw"
+
+
 @pytest.mark.parametrize("name", ["tiny", "ragged"])
 def test_prologue_backward_matches_oracle(m, name):
     """dx (bf16) and dw (fp32) of the q and k prologues against the fp64 closed
