@@ -276,6 +276,30 @@ def phase_pass(step_fn, nsteps, stream):
     return pf, bw
 
 
+class SideClear:
+    """Clears the backward's workspace accumulators on a second stream while
+    the forward runs (msa_sparse_attn_bwd_prepare), ordered after the step's
+    index select (and so after the previous step's backward) and before this
+    step's backward (prepared=True)."""
+
+    def __init__(self, dev):
+        import torch
+        self.stream = torch.cuda.Stream(dev)
+        self.after = torch.cuda.Event()
+        self.cleared = torch.cuda.Event()
+
+    def start(self, m, q, k, cu, max_seqlen, workspace):
+        import torch
+        self.after.record(torch.cuda.current_stream())
+        self.stream.wait_event(self.after)
+        m.msa_sparse_attn_bwd_prepare(q, k, cu, max_seqlen, workspace, stream=self.stream)
+        self.cleared.record(self.stream)
+
+    def join(self):
+        import torch
+        torch.cuda.current_stream().wait_event(self.cleared)
+
+
 def time_pack(m, W, workmodel, shape, dev, stream, seed, nsteps, with_bwd, peak, sample=None):
     """Prologue + select + forward (+ backward) on one pack (inputs larger than
     L2, drawn on the CPU from `seed` so the oracle can redraw them); untimed
@@ -297,6 +321,7 @@ def time_pack(m, W, workmodel, shape, dev, stream, seed, nsteps, with_bwd, peak,
           if with_bwd or c != "sparse_attn_bwd"}
     if with_bwd:
         g = {n: torch.empty_like(b[r]) for n, r in (("dq", "q"), ("dk", "k"), ("dv", "k"))}
+        side = SideClear(dev)
 
     def step(marks=None):
         m.msa_qk_norm_rope4(x["q"], x["k"], x["q_idx"], x["k_idx"], x["w_q"], x["w_k"],
@@ -306,14 +331,17 @@ def time_pack(m, W, workmodel, shape, dev, stream, seed, nsteps, with_bwd, peak,
             marks[0].record(stream)
         m.msa_index_select(b["qi"], b["ki"], x["cu_seqlens"], L, out=sel,
                            workspace=ws["index_select"])
+        if with_bwd:
+            side.start(m, b["q"], b["k"], x["cu_seqlens"], L, ws["sparse_attn_bwd"])
         m.msa_sparse_attn_fwd(b["q"], b["k"], x["v"], sel, x["cu_seqlens"], L, out=b["o"],
                               lse=lse, workspace=ws["sparse_attn_fwd"])
         if marks:
             marks[1].record(stream)
         if with_bwd:
+            side.join()
             m.msa_sparse_attn_bwd(b["q"], b["k"], x["v"], b["o"], x["do"], lse, sel,
                                   x["cu_seqlens"], L, dq=g["dq"], dk=g["dk"], dv=g["dv"],
-                                  workspace=ws["sparse_attn_bwd"])
+                                  workspace=ws["sparse_attn_bwd"], prepared=True)
         if marks:
             marks[2].record(stream)
 
@@ -415,6 +443,8 @@ def run_ours(args):
                        ("fwd", ("sparse_attn_fwd", T, S, hq, hkv, maxL)),
                        ("bwd", ("sparse_attn_bwd", T, S, hq, hkv, maxL)))}
 
+    side = SideClear(dev)
+
     def step(x, res=None, marks=None):
         res = work if res is None else res          # where o, dq, dk, dv go
         m.msa_qk_norm_rope4(x["q"], x["k"], x["q_idx"], x["k_idx"], x["w_q"], x["w_k"],
@@ -424,13 +454,15 @@ def run_ours(args):
             marks[0].record(torch.cuda.current_stream())
         m.msa_index_select(work["qi"], work["ki"], x["cu_seqlens"], maxL, out=work["sel"],
                            workspace=ws["index_select"])
+        side.start(m, work["q"], work["k"], x["cu_seqlens"], maxL, ws["bwd"])
         m.msa_sparse_attn_fwd(work["q"], work["k"], x["v"], work["sel"], x["cu_seqlens"], maxL,
                               out=res["o"], lse=work["lse"], workspace=ws["fwd"])
         if marks:
             marks[1].record(torch.cuda.current_stream())
+        side.join()
         m.msa_sparse_attn_bwd(work["q"], work["k"], x["v"], res["o"], x["do"], work["lse"],
                               work["sel"], x["cu_seqlens"], maxL, dq=res["dq"], dk=res["dk"],
-                              dv=res["dv"], workspace=ws["bwd"])
+                              dv=res["dv"], workspace=ws["bwd"], prepared=True)
         if marks:
             marks[2].record(torch.cuda.current_stream())
 

@@ -209,6 +209,29 @@ MSA_API msa_status_t msa_sparse_attn_bwd(const void* q, const void* k, const voi
                                  void* dq, void* dk, void* dv, void* workspace,
                                  size_t workspace_bytes, msa_stream_t stream);
 
+/* The backward in two parts, so that a caller can clear the workspace's fp32
+ * accumulators (about T * (Hq + 2 Hkv) * 512 bytes, one memset) while other
+ * work runs, e.g. on a second stream during the forward:
+ *   msa_sparse_attn_bwd_prepare  clears them on `stream` (same sizes as the
+ *                                backward that follows);
+ *   msa_sparse_attn_bwd_prepared is msa_sparse_attn_bwd without the clear.
+ * The caller orders the prepare before the prepared call (same stream, or an
+ * event) and writes nothing into the workspace in between; the prepared call
+ * leaves the accumulators dirty, so every call needs its own prepare.
+ * msa_sparse_attn_bwd equals prepare + prepared on one stream.
+ */
+MSA_API msa_status_t msa_sparse_attn_bwd_prepare(int T, int S, int Hq, int Hkv, int max_seqlen,
+                                                 void* workspace, size_t workspace_bytes,
+                                                 msa_stream_t stream);
+
+MSA_API msa_status_t msa_sparse_attn_bwd_prepared(const void* q, const void* k, const void* v,
+                                                  const void* o, const void* dout,
+                                                  const float* lse, const int32_t* sel,
+                                                  const int32_t* cu_seqlens, int S, int T,
+                                                  int Hq, int Hkv, int max_seqlen, float scale,
+                                                  void* dq, void* dk, void* dv, void* workspace,
+                                                  size_t workspace_bytes, msa_stream_t stream);
+
 /* ------------------------------------------------------------------------
  * Narrow-block sparse attention ("[1/4] Add MiniMax-M3 support - #4581",
  * Kernel tuning: the QSA layers of qwen3.8-next, 12 query heads per KV head,

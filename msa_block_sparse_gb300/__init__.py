@@ -16,6 +16,7 @@ from .api import (  # noqa: F401
     msa_qk_norm_rope4,
     msa_qk_norm_rope_bwd,
     msa_sparse_attn_bwd,
+    msa_sparse_attn_bwd_prepare,
     msa_qsa_attn_fwd,
     msa_qsa_attn_bwd,
     msa_sparse_attn_fwd,

@@ -50,6 +50,11 @@ _SIGNATURES = {
     "msa_sparse_attn_bwd": (_c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _c_int, _c_int,
                                      _c_int, _c_int, _c_int, _c_float, _vp, _vp, _vp, _vp,
                                      _c_size, _vp]),
+    "msa_sparse_attn_bwd_prepare": (_c_int, [_c_int, _c_int, _c_int, _c_int, _c_int, _vp, _c_size,
+                                             _vp]),
+    "msa_sparse_attn_bwd_prepared": (_c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _c_int,
+                                              _c_int, _c_int, _c_int, _c_int, _c_float, _vp, _vp,
+                                              _vp, _vp, _c_size, _vp]),
     "msa_qsa_attn_fwd_workspace_size": (_c_size, [_c_int, _c_int, _c_int, _c_int, _c_int]),
     "msa_qsa_attn_fwd": (_c_int, [_vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int,
                                   _c_int, _c_int, _c_float, _vp, _vp, _vp, _c_size, _vp]),
@@ -277,10 +282,25 @@ def msa_sparse_attn_fwd(q, k, v, sel, cu_seqlens, max_seqlen: int, scale: Option
     return out, lse
 
 
+def msa_sparse_attn_bwd_prepare(q, k, cu_seqlens, max_seqlen: int, workspace: torch.Tensor,
+                                stream: Optional[torch.cuda.Stream] = None):
+    """Clears the fp32 accumulators of `workspace` for one following
+    msa_sparse_attn_bwd(..., prepared=True) of the same shapes (q [T, Hq, 128],
+    k [T, Hkv, 128]), on `stream` (default: the current stream); the caller
+    orders the two (an event when the streams differ)."""
+    T, Hq, Hkv = q.shape[0], q.shape[1], k.shape[1]
+    S = cu_seqlens.numel() - 1
+    size = lib().msa_sparse_attn_bwd_workspace_size(T, S, Hq, Hkv, max_seqlen)
+    ws = _workspace(size, q.device, workspace)
+    st = ctypes.c_void_p((stream or torch.cuda.current_stream(q.device)).cuda_stream)
+    _check(lib().msa_sparse_attn_bwd_prepare(T, S, Hq, Hkv, max_seqlen, _ptr(ws), ws.numel(), st))
+
+
 def msa_sparse_attn_bwd(q, k, v, o, dout, lse, sel, cu_seqlens, max_seqlen: int,
                         scale: Optional[float] = None, dq=None, dk=None, dv=None,
-                        workspace: Optional[torch.Tensor] = None):
-    """Block-sparse attention backward: (dq, dk, dv) in bf16."""
+                        workspace: Optional[torch.Tensor] = None, prepared: bool = False):
+    """Block-sparse attention backward: (dq, dk, dv) in bf16.  prepared=True:
+    `workspace` was cleared by msa_sparse_attn_bwd_prepare for this call."""
     T, Hq, Hkv = q.shape[0], q.shape[1], k.shape[1]
     _req(q, "q", torch.bfloat16, (T, Hq, D))
     _req(k, "k", torch.bfloat16, (T, Hkv, D))
@@ -296,11 +316,13 @@ def msa_sparse_attn_bwd(q, k, v, o, dout, lse, sel, cu_seqlens, max_seqlen: int,
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
     size = lib().msa_sparse_attn_bwd_workspace_size(T, S, Hq, Hkv, max_seqlen)
+    if prepared and workspace is None:
+        raise ValueError("prepared=True needs the workspace that msa_sparse_attn_bwd_prepare cleared")
     ws = _workspace(size, q.device, workspace)
-    _check(lib().msa_sparse_attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse),
-                                     _ptr(sel), _ptr(cu_seqlens), S, T, Hq, Hkv, max_seqlen,
-                                     scale, _ptr(dq), _ptr(dk), _ptr(dv), _ptr(ws), ws.numel(),
-                                     _stream(q)))
+    call = lib().msa_sparse_attn_bwd_prepared if prepared else lib().msa_sparse_attn_bwd
+    _check(call(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse), _ptr(sel),
+                _ptr(cu_seqlens), S, T, Hq, Hkv, max_seqlen, scale, _ptr(dq), _ptr(dk), _ptr(dv),
+                _ptr(ws), ws.numel(), _stream(q)))
     return dq, dk, dv
 
 

@@ -628,11 +628,12 @@ size_t msa_sparse_attn_bwd_workspace_size(int T, int S, int Hq, int Hkv, int max
   return ws.used + 256;
 }
 
-msa_status_t msa_sparse_attn_bwd(const void* q, const void* k, const void* v, const void* o,
-                                 const void* dout, const float* lse, const int32_t* sel,
-                                 const int32_t* cu_seqlens, int S, int T, int Hq, int Hkv,
-                                 int max_seqlen, float scale, void* dq, void* dk, void* dv,
-                                 void* workspace, size_t workspace_bytes, msa_stream_t stream) {
+static msa_status_t sparse_attn_bwd(const void* q, const void* k, const void* v, const void* o,
+                                    const void* dout, const float* lse, const int32_t* sel,
+                                    const int32_t* cu_seqlens, int S, int T, int Hq, int Hkv,
+                                    int max_seqlen, float scale, void* dq, void* dk, void* dv,
+                                    void* workspace, size_t workspace_bytes, bool clear_acc,
+                                    msa_stream_t stream) {
   MSA_REQUIRE_PTR(q);
   MSA_REQUIRE_PTR(k);
   MSA_REQUIRE_PTR(v);
@@ -653,7 +654,40 @@ msa_status_t msa_sparse_attn_bwd(const void* q, const void* k, const void* v, co
   BwdWorkspace bw = carve_bwd_workspace(ws, T, S, Hq, Hkv, max_seqlen);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   return launch_sparse_bwd(q, k, v, o, dout, lse, sel, cu_seqlens, S, T, Hq, Hkv, max_seqlen,
-                           scale, bw, dq, dk, dv, st);
+                           scale, bw, dq, dk, dv, clear_acc, st);
+}
+
+msa_status_t msa_sparse_attn_bwd(const void* q, const void* k, const void* v, const void* o,
+                                 const void* dout, const float* lse, const int32_t* sel,
+                                 const int32_t* cu_seqlens, int S, int T, int Hq, int Hkv,
+                                 int max_seqlen, float scale, void* dq, void* dk, void* dv,
+                                 void* workspace, size_t workspace_bytes, msa_stream_t stream) {
+  return sparse_attn_bwd(q, k, v, o, dout, lse, sel, cu_seqlens, S, T, Hq, Hkv, max_seqlen,
+                         scale, dq, dk, dv, workspace, workspace_bytes, true, stream);
+}
+
+msa_status_t msa_sparse_attn_bwd_prepare(int T, int S, int Hq, int Hkv, int max_seqlen,
+                                         void* workspace, size_t workspace_bytes,
+                                         msa_stream_t stream) {
+  MSA_REQUIRE_PTR(workspace);
+  if (T < 1 || S < 1 || max_seqlen < 1 || max_seqlen > T)
+    return fail(MSA_ERR_INVALID_ARG, "bad sizes T=%d S=%d max_seqlen=%d", T, S, max_seqlen);
+  MSA_TRY(check_heads(Hq, Hkv));
+  if (workspace_bytes < msa_sparse_attn_bwd_workspace_size(T, S, Hq, Hkv, max_seqlen))
+    return fail(MSA_ERR_INVALID_ARG, "workspace too small");
+  WsCursor ws(workspace);
+  BwdWorkspace bw = carve_bwd_workspace(ws, T, S, Hq, Hkv, max_seqlen);
+  return launch_bwd_clear(bw, Hkv, static_cast<cudaStream_t>(stream));
+}
+
+msa_status_t msa_sparse_attn_bwd_prepared(const void* q, const void* k, const void* v,
+                                          const void* o, const void* dout, const float* lse,
+                                          const int32_t* sel, const int32_t* cu_seqlens, int S,
+                                          int T, int Hq, int Hkv, int max_seqlen, float scale,
+                                          void* dq, void* dk, void* dv, void* workspace,
+                                          size_t workspace_bytes, msa_stream_t stream) {
+  return sparse_attn_bwd(q, k, v, o, dout, lse, sel, cu_seqlens, S, T, Hq, Hkv, max_seqlen,
+                         scale, dq, dk, dv, workspace, workspace_bytes, false, stream);
 }
 
 // ---------------------------------------------------------------- narrow blocks

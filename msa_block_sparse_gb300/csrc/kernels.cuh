@@ -98,11 +98,15 @@ template <typename K>
 inline msa_status_t ensure_smem(K kernel, size_t bytes, const char* name) {
   return ensure_smem_ptr(reinterpret_cast<const void*>(kernel), bytes, name);
 }
+// clear_acc = false: the accumulators were cleared beforehand by
+// launch_bwd_clear on this workspace.
 msa_status_t launch_sparse_bwd(const void* q, const void* k, const void* v, const void* o,
                                const void* dout, const float* lse, const int32_t* sel,
                                const int32_t* cu, int S, int T, int Hq, int Hkv, int max_seqlen,
                                float scale, const BwdWorkspace& ws, void* dq, void* dk, void* dv,
-                               cudaStream_t stream);
+                               bool clear_acc, cudaStream_t stream);
+// Zeroes the workspace's fp32 accumulators and item counters (one memset).
+msa_status_t launch_bwd_clear(const BwdWorkspace& ws, int Hkv, cudaStream_t stream);
 
 // ---------------------------------------------------------------- decode
 struct DecodeWorkspace {

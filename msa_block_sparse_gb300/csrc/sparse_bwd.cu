@@ -815,6 +815,16 @@ static int bwd_max_items(int T, int S, int max_seqlen) {
   return static_cast<int>(n < (1LL << 30) ? n : (1LL << 30));
 }
 
+msa_status_t launch_bwd_clear(const BwdWorkspace& ws, int Hkv, cudaStream_t stream) {
+  // the three accumulators and the item counters are carved back to back: one
+  // clear covers them
+  const size_t acc_bytes = reinterpret_cast<uint8_t*>(ws.item_ctr + Hkv) -
+                           reinterpret_cast<uint8_t*>(ws.dq_acc);
+  if (cudaMemsetAsync(ws.dq_acc, 0, acc_bytes, stream) != cudaSuccess)
+    return fail(MSA_ERR_CUDA, "workspace clear failed");
+  return MSA_OK;
+}
+
 BwdWorkspace carve_bwd_workspace(WsCursor& ws, int T, int S, int Hq, int Hkv, int max_seqlen) {
   BwdWorkspace w;
   w.max_items = bwd_max_items(T, S, max_seqlen);
@@ -838,7 +848,7 @@ msa_status_t launch_sparse_bwd(const void* q, const void* k, const void* v, cons
                                const void* dout, const float* lse, const int32_t* sel,
                                const int32_t* cu, int S, int T, int Hq, int Hkv, int max_seqlen,
                                float scale, const BwdWorkspace& ws, void* dq, void* dk, void* dv,
-                               cudaStream_t stream) {
+                               bool clear_acc, cudaStream_t stream) {
   const int G = Hq / Hkv;
   if (G != 16)
     return fail(MSA_ERR_UNSUPPORTED, "backward supports Hq/Hkv = 16 (got %d)", G);
@@ -861,12 +871,10 @@ msa_status_t launch_sparse_bwd(const void* q, const void* k, const void* v, cons
 
   const size_t nq = static_cast<size_t>(T) * Hq * kD;
   const size_t nkv = static_cast<size_t>(T) * Hkv * kD;
-  // the three accumulators and the item counters are carved back to back: one
-  // clear covers them
-  const size_t acc_bytes = reinterpret_cast<uint8_t*>(ws.item_ctr + Hkv) -
-                           reinterpret_cast<uint8_t*>(ws.dq_acc);
-  if (cudaMemsetAsync(ws.dq_acc, 0, acc_bytes, stream) != cudaSuccess)
-    return fail(MSA_ERR_CUDA, "workspace clear failed");
+  if (clear_acc) {
+    const msa_status_t e = launch_bwd_clear(ws, Hkv, stream);
+    if (e != MSA_OK) return e;
+  }
 
   const size_t rows = static_cast<size_t>(T) * Hq;
   {

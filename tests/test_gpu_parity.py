@@ -388,6 +388,44 @@ def test_sparse_bwd_small(m, name):
         assert r <= 1e-2, f"{name} {n}: rel-L2 {r:.3e}"
 
 
+def test_sparse_bwd_prepared_on_a_second_stream(m):
+    """msa_sparse_attn_bwd_prepare on another stream (ordered by an event) and
+    msa_sparse_attn_bwd_prepared give the oracle's gradients; the workspace is
+    dirty before the prepare (a previous backward ran in it)."""
+    name = "2seq-16q1kv"
+    shape = BWD_SMALL[name]
+    cpu, gpu = inputs(name, shape)
+    osel, _ = oracle_selection(name, shape, cpu)
+    sel = torch.from_numpy(osel.astype(np.int32)).to(DEV)
+    cu = gpu["cu_seqlens"]
+    L = shape.max_seqlen
+    o, lse = m.msa_sparse_attn_fwd(gpu["q"], gpu["k"], gpu["v"], sel, cu, L)
+    ws = torch.empty(m.workspace_bytes("sparse_attn_bwd", shape.T, shape.S, shape.hq, shape.hkv, L),
+                     dtype=torch.uint8, device=DEV)
+    ref = m.msa_sparse_attn_bwd(gpu["q"], gpu["k"], gpu["v"], o, gpu["do"], lse, sel, cu, L,
+                                workspace=ws)
+    side = torch.cuda.Stream(DEV)
+    ready, cleared = torch.cuda.Event(), torch.cuda.Event()
+    ready.record(torch.cuda.current_stream())
+    side.wait_event(ready)
+    m.msa_sparse_attn_bwd_prepare(gpu["q"], gpu["k"], cu, L, ws, stream=side)
+    cleared.record(side)
+    torch.cuda.current_stream().wait_event(cleared)
+    got = m.msa_sparse_attn_bwd(gpu["q"], gpu["k"], gpu["v"], o, gpu["do"], lse, sel, cu, L,
+                                workspace=ws, prepared=True)
+    m.msa_check_status()
+    rq, rk, rv = O.sparse_attn_bwd(f64(cpu["q"]), f64(cpu["k"]), f64(cpu["v"]), f64(cpu["do"]),
+                                   osel, cpu["cu_seqlens"].numpy(), SCALE)
+    for g_, r_, want, n in zip(got, ref, (rq, rk, rv), ("dq", "dk", "dv")):
+        assert rel_l2(f64(g_), want) <= 1e-2, n
+        # the same kernels on the same inputs: only the order of the fp32
+        # atomic additions may differ between the two runs
+        assert rel_l2(f64(g_), f64(r_)) <= 1e-3, n
+    with pytest.raises(ValueError):
+        m.msa_sparse_attn_bwd(gpu["q"], gpu["k"], gpu["v"], o, gpu["do"], lse, sel, cu, L,
+                              prepared=True)
+
+
 def bwd_sample_blocks(shape, seed):
     """(sequence, KV head, block) triples whose dk/dv a full-size backward test
     compares: for every sequence and KV head block 0 or 1 (selected by almost
