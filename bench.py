@@ -284,7 +284,9 @@ class SideClear:
 
     def __init__(self, dev):
         import torch
-        self.stream = torch.cuda.Stream(dev)
+        # high priority: the clear's blocks go ahead of the forward's once it
+        # has started, instead of waiting behind its persistent blocks
+        self.stream = torch.cuda.Stream(dev, priority=-1)
         self.after = torch.cuda.Event()
         self.cleared = torch.cuda.Event()
 
