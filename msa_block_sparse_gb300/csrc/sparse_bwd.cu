@@ -29,7 +29,9 @@
 //   compute (warps 2..9: warpgroup z takes the half-chunks u with u & 1 == z;
 //            thread = key row): P^T = exp2(S^T scale log2e - lse log2e),
 //            causally masked, packed to bf16 into TMEM; dS^T = P^T (dP^T -
-//            Delta) to shared memory; then the dQ^T rows are added into the
+//            Delta) to shared memory, with P^T read back from TMEM (the bf16
+//            values dV uses) and -Delta fetched from shared memory while dP^T
+//            is computed; then the dQ^T rows are added into the
 //            fp32 dQ accumulator with reductions straight from registers (a
 //            warp covers 32 consecutive floats of a row); at the end of an item
 //            warpgroup 0 adds dK, warpgroup 1 dV into their accumulators.
@@ -86,6 +88,10 @@ struct BwdSmem {
   uint32_t tmem_base;
 };
 static_assert(sizeof(BwdSmem) <= 232448, "backward shared memory above the 227 KB limit");
+
+__device__ __forceinline__ float2 unpack_bf16x2(uint32_t v) {
+  return make_float2(__uint_as_float(v << 16), __uint_as_float(v & 0xFFFF0000u));
+}
 
 __device__ __forceinline__ float ex2(float x) {
   float y;
@@ -705,29 +711,38 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
         tc_fence_before();
         mbar_arrive(&sm.p_full[z]);
+        // -Delta of the 64 columns, fetched while dP^T is computed (the dS step
+        // below then reads P^T back from TMEM and needs no shared-memory loads)
+        float4 ndl[kHc / 4];
+#pragma unroll
+        for (int q4 = 0; q4 < kHc / 4; ++q4)
+          ndl[q4] = *reinterpret_cast<const float4*>(ls + 32 * (q4 >> 2) + 16 + 4 * (q4 & 3));
 
         // ---- dS^T = P^T (dP^T - Delta) -> shared memory (K-major, rows = keys)
         if (!(ok = mbar_wait(&sm.dp_full[z], ph, status, 43))) break;
         __syncwarp();
         tc_fence_after();
-        {
-          uint32_t dv[kHc];
-          tmem_ld32(slot + kHc, dv);
-          tmem_ld32(slot + kHc + 32, dv + 32);
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+          uint32_t dv[32], pb[16];
+          tmem_ld32(slot + kHc + 32 * hf, dv);
+          tmem_ld16(slot + 16 * hf, pb);       // P^T of these 32 columns, bf16 pairs
           tmem_ld_wait();
 #pragma unroll
-          for (int c = 0; c < 8; ++c) {
+          for (int c = 4 * hf; c < 4 * hf + 4; ++c) {
             float x[8];
 #pragma unroll
             for (int e4 = 0; e4 < 2; ++e4) {
               const int c0 = 8 * c + 4 * e4;   // token c0 / 16, heads c0 % 16 ..
-              const float4 nd = *reinterpret_cast<const float4*>(ls + 32 * (c0 >> 4) + 16 + (c0 & 15));
-              const float2 t0 = fadd2(make_float2(__uint_as_float(dv[c0]), __uint_as_float(dv[c0 + 1])),
+              const int d0 = c0 - 32 * hf;
+              const float4 nd = ndl[c0 / 4];
+              const float2 t0 = fadd2(make_float2(__uint_as_float(dv[d0]), __uint_as_float(dv[d0 + 1])),
                                       make_float2(nd.x, nd.y));
-              const float2 t1 = fadd2(make_float2(__uint_as_float(dv[c0 + 2]), __uint_as_float(dv[c0 + 3])),
+              const float2 t1 = fadd2(make_float2(__uint_as_float(dv[d0 + 2]), __uint_as_float(dv[d0 + 3])),
                                       make_float2(nd.z, nd.w));
-              const float2 x0 = fmul2(make_float2(p[c0], p[c0 + 1]), t0);
-              const float2 x1 = fmul2(make_float2(p[c0 + 2], p[c0 + 3]), t1);
+              const float2 p01 = unpack_bf16x2(pb[d0 / 2]), p23 = unpack_bf16x2(pb[d0 / 2 + 1]);
+              const float2 x0 = fmul2(p01, t0);
+              const float2 x1 = fmul2(p23, t1);
               x[4 * e4] = x0.x;
               x[4 * e4 + 1] = x0.y;
               x[4 * e4 + 2] = x1.x;
