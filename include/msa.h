@@ -111,6 +111,8 @@ MSA_API msa_status_t msa_selftest_wait(msa_stream_t stream);
  *   position; channels >= rope_dim pass through.  rope_dim must be 64.
  * The four-tensor form runs q [T,Hq,128], k [T,Hkv,128], q_idx and k_idx
  * [T,Hi,128] with their own weights in one launch; same result as four calls.
+ * Head counts: 1 <= H <= 256 per tensor (MSA_ERR_INVALID_ARG below,
+ * MSA_ERR_UNSUPPORTED above; nothing is enqueued).
  */
 MSA_API msa_status_t msa_qk_norm_rope(const void* x, void* y, int T, int H, const void* w,
                                       const int32_t* cu_seqlens, int S, int rope_dim,
@@ -134,7 +136,8 @@ MSA_API msa_status_t msa_qk_norm_rope4(const void* q, void* q_out, int Hq, const
  *   dx = r (g - xh mean(g xh))          bf16 [T, H, 128]  (dx may be dy)
  *   dw = sum over tokens and heads of dz * xh     fp32 [128] (overwritten)
  * dw is summed in a fixed order (run to run identical).  Workspace from
- * msa_qk_norm_rope_bwd_workspace_size; other arguments as for msa_qk_norm_rope.
+ * msa_qk_norm_rope_bwd_workspace_size; other arguments (and the head-count
+ * limit 1 <= H <= 256) as for msa_qk_norm_rope.
  */
 MSA_API size_t msa_qk_norm_rope_bwd_workspace_size(int T, int H);
 

@@ -11,7 +11,12 @@
 // thread, so the rotation needs no shuffles; threads 8..15 hold the
 // pass-through channels 64..127.  Each thread keeps four rows in registers:
 // three rows' loads are in flight while the fourth is processed, and the first
-// rows' loads are issued before the angles are computed.
+// rows' loads are issued before the angles are computed.  The kernel is bound
+// by instruction issue as much as by memory, so the per-row work is kept
+// short: a cursor (tensor, row) walks the thread's rows without a table
+// lookup or a division per row, the token of a row is a multiply and a shift,
+// and the arithmetic runs on packed pairs of fp32 (two channels per
+// instruction).
 //
 // Angles avoid a large fp32 argument: the host turns each frequency f_i into
 // the 64-bit fixed-point fraction F_i = f_i / (2 pi) * 2^64 of a turn, so
@@ -35,14 +40,58 @@ struct PrologueArgs {
 constexpr int kProTokens = 16;
 constexpr int kProThreads = 256;             // decode-append kernel
 constexpr int kProSlots = kProThreads / 8;   // rows processed side by side
+constexpr int kProMaxH = 256;                // heads per tensor (token of a row = r * inv >> 20)
 // forward kernel: 128 threads, 8 rows side by side with 16 threads per row
 // (8 channels each: thread c < 8 holds the rotated pairs (4c + e, 4c + 32 + e),
 // c >= 8 the pass-through channels 64 + 8 (c - 8) ..); four rows per thread in
 // registers, so three rows' loads are in flight while the fourth is
-// normalised, rotated and stored (62 registers, 8 CTAs per SM)
+// normalised, rotated and stored (8 CTAs per SM)
 constexpr int kPfThreads = 128;
 constexpr int kPfLanes = 16;
 constexpr int kPfSlots = kPfThreads / kPfLanes;
+static_assert(kPfThreads == kProTokens * (kRopeDim / 8), "one thread per (token, 4 frequencies)");
+
+// the rows of one tensor that a CTA owns: rows [rowbase, rowbase + nrows) of
+// its [T * H, 128] view, row r of them belonging to the CTA's token r / H
+struct ProJobRows {
+  const __nv_bfloat16* x;
+  __nv_bfloat16* y;
+  int nrows;        // ntok * H (0: tensor absent)
+  int rowbase;      // t0 * H
+  uint32_t inv;     // ceil(2^20 / H): r / H == (r * inv) >> 20 for r < 16 H, H <= 256
+  int pad;
+};
+
+__device__ __forceinline__ float2 bf2_to_f2(uint32_t u) {
+  return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u));
+}
+
+// (cos, sin, -sin) of one token's frequencies 4g .. 4g + 3 (thread = (token, g)):
+// the token's position is found by a binary search over cu, the angle in
+// turns by the 64-bit fixed-point product described above
+__device__ __forceinline__ void rope_table_entry(float4 (*cs)[3][kRopeDim / 8], const RopeTurns& turns,
+                                                 const int32_t* __restrict__ cu, int S, int T,
+                                                 int t0, int tid) {
+  const int qt = tid >> 3, g = tid & 7;
+  const int t = t0 + qt;
+  float cv[4] = {1.f, 1.f, 1.f, 1.f}, sv[4] = {0.f, 0.f, 0.f, 0.f};
+  if (t < T) {
+    int lo = 0, hi = S;   // largest s with cu[s] <= t
+    while (hi - lo > 1) {
+      int mid = (lo + hi) >> 1;
+      if (__ldg(cu + mid) <= t) lo = mid; else hi = mid;
+    }
+    const unsigned long long pos = static_cast<unsigned long long>(t - __ldg(cu + lo));
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const long long ang = static_cast<long long>(pos * turns.f[4 * g + e]);
+      sincospif(static_cast<float>(ang) * 1.0842021724855044e-19f, &sv[e], &cv[e]);   // * 2^-63
+    }
+  }
+  cs[qt][0][g] = make_float4(cv[0], cv[1], cv[2], cv[3]);
+  cs[qt][1][g] = make_float4(sv[0], sv[1], sv[2], sv[3]);
+  cs[qt][2][g] = make_float4(-sv[0], -sv[1], -sv[2], -sv[3]);
+}
 
 __global__ void __launch_bounds__(kPfThreads, 8) prologue_kernel(const PrologueArgs args,
                                                                   const RopeTurns turns,
@@ -50,155 +99,146 @@ __global__ void __launch_bounds__(kPfThreads, 8) prologue_kernel(const PrologueA
                                                                   int S, int T, float eps,
                                                                   uint32_t* status) {
   pdl_enter();
-  __shared__ float2 cs[kProTokens][kRopeDim / 2];
+  __shared__ __align__(16) float4 cs[kProTokens][3][kRopeDim / 8];
   __shared__ __align__(16) float wsh[4][kD];
+  __shared__ ProJobRows js[4];
   const int t0 = blockIdx.x * kProTokens;
   const int tid = threadIdx.x;
-  const int hsum = args.hstart[4];
+  const int ntok = min(kProTokens, T - t0);
   const int c = tid & (kPfLanes - 1);     // channel group of the row
   const int slot = tid / kPfLanes;
   // channel offsets (elements) of this thread's two 4-channel pieces
   const int off0 = (c < 8) ? 4 * c : 64 + 8 * (c - 8);
   const int off1 = (c < 8) ? 4 * c + 32 : 64 + 8 * (c - 8) + 4;
-  // 1 + w of every job (read after the barrier below)
+  if (tid < 4) {
+    const int H = args.hstart[tid + 1] - args.hstart[tid];
+    ProJobRows r;
+    r.x = args.jobs[tid].x;
+    r.y = args.jobs[tid].y;
+    r.nrows = ntok * H;
+    r.rowbase = t0 * H;
+    r.inv = H > 0 ? ((1u << 20) + H - 1) / H : 0u;
+    r.pad = 0;
+    js[tid] = r;
+  }
+  __syncthreads();
+
+  // The thread's rows are the CTA's rows slot, slot + 8, slot + 16, ... taken
+  // tensor by tensor; the cursor (cj, cr) = (tensor, row within its CTA rows)
+  // and that tensor's fields stay in registers between rows.
+  int cj = 0, cr = slot, cnr = 0, crb = 0;
+  uint32_t cinv = 0;
+  const __nv_bfloat16* cx = nullptr;
+  auto next_tensor = [&]() {
+    while (cj < 4 && cr >= js[cj].nrows) {
+      cr -= js[cj].nrows;
+      ++cj;
+    }
+    if (cj < 4) {
+      cx = js[cj].x;
+      cnr = js[cj].nrows;
+      crb = js[cj].rowbase;
+      cinv = js[cj].inv;
+    }
+  };
+  next_tensor();
+  struct Rows {
+    uint2 xa, xb;
+    int g;     // row of the tensor's [T * H, 128] view
+    int jt;    // tensor | token of the CTA << 2; -1: none
+  };
+  Rows ra, rb, rc, rd;
+  auto load_row = [&](Rows& R) {
+    R.jt = -1;
+    R.g = 0;
+    R.xa = make_uint2(0, 0);
+    R.xb = R.xa;
+    if (cj < 4) {
+      const int g = crb + cr;
+      const __nv_bfloat16* src = cx + static_cast<size_t>(g) * kD;
+      R.xa = __ldcs(reinterpret_cast<const uint2*>(src + off0));
+      R.xb = __ldcs(reinterpret_cast<const uint2*>(src + off1));
+      R.g = g;
+      R.jt = cj | static_cast<int>((static_cast<uint32_t>(cr) * cinv) >> 20) << 2;
+      cr += kPfSlots;
+      if (cr >= cnr) next_tensor();
+    }
+  };
+  // the first rows' loads are in flight while the weights and angles are set up
+  load_row(ra);
+  load_row(rb);
+  load_row(rc);
   for (int k = tid; k < 4 * kD; k += blockDim.x) {
     const int j = k / kD;
     wsh[j][k % kD] = (args.hstart[j] < args.hstart[j + 1])
                          ? 1.f + __bfloat162float(args.jobs[j].w[k % kD]) : 0.f;
   }
-  const int ntok = min(kProTokens, T - t0);
-  const int rows = ntok * hsum;
-
-  // This thread's rows are slot, slot + 8, slot + 16, ...; (tl, k) = (token of
-  // the CTA, row within the token) advances by 8 rows per step without a
-  // division once hsum is known.
-  int tl = slot / hsum, k = slot - (slot / hsum) * hsum;
-  auto advance = [&]() {
-    k += kPfSlots;
-    while (k >= hsum) {
-      k -= hsum;
-      ++tl;
-    }
-  };
-  struct Rows {
-    uint2 xa, xb;
-    int rj, rtl;
-    size_t rrow;
-  };
-  Rows ra, rb, rc, rd;
-  // loads the thread's next row (rows are taken in order; r = the row index)
-  auto load_rows = [&](int r, Rows& R) {
-    R.rj = -1;
-    R.rtl = 0;
-    R.rrow = 0;
-    R.xa = make_uint2(0, 0);
-    R.xb = R.xa;
-    if (r < rows) {
-      const int j = (k >= args.hstart[1]) + (k >= args.hstart[2]) + (k >= args.hstart[3]);
-      const size_t row = static_cast<size_t>(t0 + tl) * args.jobs[j].H + (k - args.hstart[j]);
-      const __nv_bfloat16* src = args.jobs[j].x + row * kD;
-      R.xa = __ldcs(reinterpret_cast<const uint2*>(src + off0));
-      R.xb = __ldcs(reinterpret_cast<const uint2*>(src + off1));
-      R.rj = j;
-      R.rtl = tl;
-      R.rrow = row;
-      advance();
-    }
-  };
-  // the first rows' loads are in flight while the angles are computed
-  load_rows(slot, ra);
-  load_rows(kPfSlots + slot, rb);
-  load_rows(2 * kPfSlots + slot, rc);
-  // (cos, sin) for the CTA's tokens: thread = (token, frequency)
-  for (int q = tid; q < kProTokens * (kRopeDim / 2); q += blockDim.x) {
-    const int qt = q / (kRopeDim / 2), i = q % (kRopeDim / 2);
-    const int t = t0 + qt;
-    float cv = 1.f, sv = 0.f;
-    if (t < T) {
-      int lo = 0, hi = S;   // largest s with cu[s] <= t
-      while (hi - lo > 1) {
-        int mid = (lo + hi) >> 1;
-        if (__ldg(cu + mid) <= t) lo = mid; else hi = mid;
-      }
-      const unsigned long long pos = static_cast<unsigned long long>(t - __ldg(cu + lo));
-      const long long ang = static_cast<long long>(pos * turns.f[i]);
-      const float x = static_cast<float>(ang) * 1.0842021724855044e-19f;   // * 2^-63
-      sincospif(x, &sv, &cv);
-    }
-    cs[qt][i] = make_float2(cv, sv);
-  }
+  rope_table_entry(cs, turns, cu, S, T, t0, tid);
   __syncthreads();
 
   auto process = [&](const Rows& R) {
-    float x[8];
+    const int j = R.jt < 0 ? 0 : (R.jt & 3);
+    const int tl = R.jt < 0 ? 0 : (R.jt >> 2);
+    // x: channels off0 + {0,1}, off0 + {2,3}, off1 + {0,1}, off1 + {2,3}
+    float2 x[4] = {bf2_to_f2(R.xa.x), bf2_to_f2(R.xa.y), bf2_to_f2(R.xb.x), bf2_to_f2(R.xb.y)};
+    float2 s2 = __fmul2_rn(x[0], x[0]);
+#pragma unroll
+    for (int e = 1; e < 4; ++e) s2 = __ffma2_rn(x[e], x[e], s2);
+    float ss = s2.x + s2.y;
     {
-      const __nv_bfloat162* pa = reinterpret_cast<const __nv_bfloat162*>(&R.xa);
-      const __nv_bfloat162* pb = reinterpret_cast<const __nv_bfloat162*>(&R.xb);
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const float2 fa = __bfloat1622float2(pa[e]);
-        const float2 fb = __bfloat1622float2(pb[e]);
-        x[2 * e] = fa.x;
-        x[2 * e + 1] = fa.y;
-        x[4 + 2 * e] = fb.x;
-        x[4 + 2 * e + 1] = fb.y;
-      }
-    }
-    float s2[2] = {0.f, 0.f};
-#pragma unroll
-    for (int e = 0; e < 8; ++e) s2[e & 1] = fmaf(x[e], x[e], s2[e & 1]);
-    float ss = s2[0] + s2[1];
-#pragma unroll
-    for (int m = kPfLanes / 2; m >= 1; m >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, m);
-    const int j = R.rj < 0 ? 0 : R.rj;
-    const float rinv = rsqrtf(ss * (1.f / kD) + eps);
-    {
+      // x (1 + w) while the sum of squares is reduced
       const float4 w0 = *reinterpret_cast<const float4*>(&wsh[j][off0]);
       const float4 w1 = *reinterpret_cast<const float4*>(&wsh[j][off1]);
-      const float w[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
-#pragma unroll
-      for (int e = 0; e < 8; ++e) x[e] *= rinv * w[e];
+      x[0] = __fmul2_rn(x[0], make_float2(w0.x, w0.y));
+      x[1] = __fmul2_rn(x[1], make_float2(w0.z, w0.w));
+      x[2] = __fmul2_rn(x[2], make_float2(w1.x, w1.y));
+      x[3] = __fmul2_rn(x[3], make_float2(w1.z, w1.w));
     }
+#pragma unroll
+    for (int m = kPfLanes / 2; m >= 1; m >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, m);
     if (c < 8) {
-      // rotate channel 4c + e (x1) with 4c + 32 + e (x2), frequency 4c + e
-      const float4* cp = reinterpret_cast<const float4*>(&cs[R.rtl][4 * c]);
+      // rotate channel 4c + e (x1) with 4c + 32 + e (x2), frequency 4c + e:
+      // x1' = x1 cos - x2 sin, x2' = x2 cos + x1 sin (pairs e = 0,1 and 2,3)
+      const float4 cv = cs[tl][0][c], sv = cs[tl][1][c], nv = cs[tl][2][c];
+      const float2 c2[2] = {make_float2(cv.x, cv.y), make_float2(cv.z, cv.w)};
+      const float2 s2v[2] = {make_float2(sv.x, sv.y), make_float2(sv.z, sv.w)};
+      const float2 n2[2] = {make_float2(nv.x, nv.y), make_float2(nv.z, nv.w)};
 #pragma unroll
-      for (int e2 = 0; e2 < 2; ++e2) {
-        const float4 q = cp[e2];   // (cos, sin) of frequencies 2 e2, 2 e2 + 1
-        const float cc[2] = {q.x, q.z}, sn[2] = {q.y, q.w};
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int e = 2 * e2 + h;
-          const float x1 = x[e], x2 = x[4 + e];
-          x[e] = x1 * cc[h] - x2 * sn[h];
-          x[4 + e] = x2 * cc[h] + x1 * sn[h];
-        }
+      for (int h = 0; h < 2; ++h) {
+        const float2 x1 = x[h], x2 = x[2 + h];
+        x[h] = __ffma2_rn(x1, c2[h], __fmul2_rn(x2, n2[h]));
+        x[2 + h] = __ffma2_rn(x2, c2[h], __fmul2_rn(x1, s2v[h]));
       }
     }
-    if (R.rj >= 0) {
+    const float rinv = rsqrtf(ss * (1.f / kD) + eps);
+    const float2 rr = make_float2(rinv, rinv);
+    if (R.jt >= 0) {
       uint2 oa, ob;
-      oa.x = pack_bf16x2(x[0], x[1]);
-      oa.y = pack_bf16x2(x[2], x[3]);
-      ob.x = pack_bf16x2(x[4], x[5]);
-      ob.y = pack_bf16x2(x[6], x[7]);
-      __nv_bfloat16* dst = args.jobs[R.rj].y + R.rrow * kD;
+      const float2 y0 = __fmul2_rn(x[0], rr), y1 = __fmul2_rn(x[1], rr);
+      const float2 y2 = __fmul2_rn(x[2], rr), y3 = __fmul2_rn(x[3], rr);
+      oa.x = pack_bf16x2(y0.x, y0.y);
+      oa.y = pack_bf16x2(y1.x, y1.y);
+      ob.x = pack_bf16x2(y2.x, y2.y);
+      ob.y = pack_bf16x2(y3.x, y3.y);
+      __nv_bfloat16* dst = js[j].y + static_cast<size_t>(R.g) * kD;
       *reinterpret_cast<uint2*>(dst + off0) = oa;
       *reinterpret_cast<uint2*>(dst + off1) = ob;
     }
   };
   // the loop bound is uniform over the CTA: every lane reaches the shuffles;
   // three rows' loads are in flight while the fourth row is processed
+  const int rows = ntok * args.hstart[4];
   for (int base = 0; base < rows; base += 4 * kPfSlots) {
-    load_rows(base + 3 * kPfSlots + slot, rd);
+    load_row(rd);
     process(ra);
     if (base + kPfSlots >= rows) break;
-    load_rows(base + 4 * kPfSlots + slot, ra);
+    load_row(ra);
     process(rb);
     if (base + 2 * kPfSlots >= rows) break;
-    load_rows(base + 5 * kPfSlots + slot, rb);
+    load_row(rb);
     process(rc);
     if (base + 3 * kPfSlots >= rows) break;
-    load_rows(base + 6 * kPfSlots + slot, rc);
+    load_row(rc);
     process(rd);
   }
 }
@@ -206,6 +246,10 @@ __global__ void __launch_bounds__(kPfThreads, 8) prologue_kernel(const PrologueA
 msa_status_t launch_prologue(const PrologueJob* jobs, int njobs, const int32_t* cu, int S, int T,
                              float rope_base, float eps, cudaStream_t stream) {
   if (njobs < 1 || njobs > 4) return fail(MSA_ERR_INVALID_ARG, "prologue takes 1..4 tensors");
+  for (int j = 0; j < njobs; ++j)
+    if (jobs[j].H > kProMaxH)
+      return fail(MSA_ERR_UNSUPPORTED, "prologue: at most %d heads per tensor (got %d)", kProMaxH,
+                  jobs[j].H);
   PrologueArgs args{};
   int h = 0;
   for (int j = 0; j < 4; ++j) {
@@ -243,7 +287,9 @@ msa_status_t launch_prologue(const PrologueJob* jobs, int njobs, const int32_t* 
 // holding 8 channels each (thread c < 8: the rotated pairs (4c + e,
 // 4c + 32 + e); c >= 8: the pass-through channels 64 + 8 (c - 8) ..).  Each
 // thread keeps three rows in registers: two rows' loads are in flight while
-// the third is processed.  Few live values per thread keep 7 CTAs on an SM.
+// the third is processed.  Few live values per thread keep 7 CTAs on an SM;
+// the thread's 8 weights stay in registers, the token of a row is a multiply
+// and a shift, and the arithmetic runs on packed pairs of fp32.
 // Each thread sums dw for its 8 channels over its rows, the CTA adds its 8 row
 // slots into one partial row of dw_part, and prologue_bwd_sum_kernel adds the
 // partials in a fixed order (the result does not depend on scheduling).
@@ -257,18 +303,28 @@ __global__ void __launch_bounds__(kPbThreads, 7) prologue_bwd_kernel(
     const RopeTurns turns, const int32_t* __restrict__ cu, int S, int T, float eps,
     float* __restrict__ dw_part) {
   pdl_enter();
-  __shared__ float2 cs[kProTokens][kRopeDim / 2];
-  __shared__ __align__(16) float wsh[kD];
+  __shared__ __align__(16) float4 cs[kProTokens][3][kRopeDim / 8];
   __shared__ float red[kPbSlots][kD + 4];
   const int tid = threadIdx.x;
   const int c = tid & (kPbLanes - 1);
   const int slot = tid / kPbLanes;
   const int off0 = (c < 8) ? 4 * c : 64 + 8 * (c - 8);
   const int off1 = (c < 8) ? 4 * c + 32 : 64 + 8 * (c - 8) + 4;
-  for (int k = tid; k < kD; k += blockDim.x) wsh[k] = 1.f + __bfloat162float(w[k]);
-  float aw[8];
+  const uint32_t inv = ((1u << 20) + H - 1) / H;   // r / H == (r * inv) >> 20 (r < 16 H)
+  // 1 + w of the thread's 8 channels, and their dw sums over its rows
+  float2 w2[4];
+  {
+    const uint2 wa = __ldg(reinterpret_cast<const uint2*>(w + off0));
+    const uint2 wb = __ldg(reinterpret_cast<const uint2*>(w + off1));
+    const float2 one = make_float2(1.f, 1.f);
+    w2[0] = __fadd2_rn(bf2_to_f2(wa.x), one);
+    w2[1] = __fadd2_rn(bf2_to_f2(wa.y), one);
+    w2[2] = __fadd2_rn(bf2_to_f2(wb.x), one);
+    w2[3] = __fadd2_rn(bf2_to_f2(wb.y), one);
+  }
+  float2 aw[4];
 #pragma unroll
-  for (int e = 0; e < 8; ++e) aw[e] = 0.f;
+  for (int e = 0; e < 4; ++e) aw[e] = make_float2(0.f, 0.f);
   struct Rows {
     uint2 xa, xb, ga, gb;
     int r;                                 // row of the group, -1: none
@@ -293,108 +349,64 @@ __global__ void __launch_bounds__(kPbThreads, 7) prologue_bwd_kernel(
         R.r = r;
       }
     };
-    Rows ra, rb, rc, rd;
+    Rows ra, rb, rc;
     __syncthreads();                       // the previous group's angles are consumed
     load_rows(slot, ra);                   // in flight while the angles are computed
     load_rows(kPbSlots + slot, rb);
-    for (int q = tid; q < kProTokens * (kRopeDim / 2); q += blockDim.x) {
-      const int qt = q / (kRopeDim / 2), i = q % (kRopeDim / 2);
-      const int t = t0 + qt;
-      float cv = 1.f, sv = 0.f;
-      if (t < T) {
-        int lo = 0, hi = S;   // largest s with cu[s] <= t
-        while (hi - lo > 1) {
-          int mid = (lo + hi) >> 1;
-          if (__ldg(cu + mid) <= t) lo = mid; else hi = mid;
-        }
-        const unsigned long long pos = static_cast<unsigned long long>(t - __ldg(cu + lo));
-        const long long ang = static_cast<long long>(pos * turns.f[i]);
-        const float a = static_cast<float>(ang) * 1.0842021724855044e-19f;   // * 2^-63
-        sincospif(a, &sv, &cv);
-      }
-      cs[qt][i] = make_float2(cv, sv);
-    }
+    rope_table_entry(cs, turns, cu, S, T, t0, tid);
     __syncthreads();
 
     auto process = [&](const Rows& R) {
       const bool valid = R.r >= 0;
-      const int tl = valid ? R.r / H : 0;
-      float xv[8], dz[8];
-      {
-        const __nv_bfloat162* pa = reinterpret_cast<const __nv_bfloat162*>(&R.xa);
-        const __nv_bfloat162* pb = reinterpret_cast<const __nv_bfloat162*>(&R.xb);
-        const __nv_bfloat162* qa = reinterpret_cast<const __nv_bfloat162*>(&R.ga);
-        const __nv_bfloat162* qb = reinterpret_cast<const __nv_bfloat162*>(&R.gb);
+      const int tl = valid ? static_cast<int>((static_cast<uint32_t>(R.r) * inv) >> 20) : 0;
+      float2 xv[4] = {bf2_to_f2(R.xa.x), bf2_to_f2(R.xa.y), bf2_to_f2(R.xb.x), bf2_to_f2(R.xb.y)};
+      float2 dz[4] = {bf2_to_f2(R.ga.x), bf2_to_f2(R.ga.y), bf2_to_f2(R.gb.x), bf2_to_f2(R.gb.y)};
+      float2 s2 = __fmul2_rn(xv[0], xv[0]);
 #pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const float2 fa = __bfloat1622float2(pa[e]), fb = __bfloat1622float2(pb[e]);
-          const float2 da = __bfloat1622float2(qa[e]), db = __bfloat1622float2(qb[e]);
-          xv[2 * e] = fa.x;
-          xv[2 * e + 1] = fa.y;
-          xv[4 + 2 * e] = fb.x;
-          xv[4 + 2 * e + 1] = fb.y;
-          dz[2 * e] = da.x;
-          dz[2 * e + 1] = da.y;
-          dz[4 + 2 * e] = db.x;
-          dz[4 + 2 * e + 1] = db.y;
-        }
-      }
-      if (c < 8) {
-        // dz = R^T dy for the pairs (4c + e, 4c + 32 + e), frequency 4c + e
-        const float4* cp = reinterpret_cast<const float4*>(&cs[tl][4 * c]);
-#pragma unroll
-        for (int e2 = 0; e2 < 2; ++e2) {
-          const float4 q4 = cp[e2];
-          const float cc[2] = {q4.x, q4.z}, sn[2] = {q4.y, q4.w};
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const int e = 2 * e2 + h;
-            const float d1 = dz[e], d2 = dz[4 + e];
-            dz[e] = d1 * cc[h] + d2 * sn[h];
-            dz[4 + e] = d2 * cc[h] - d1 * sn[h];
-          }
-        }
-      }
-      float s2[2] = {0.f, 0.f};
-#pragma unroll
-      for (int e = 0; e < 8; ++e) s2[e & 1] = fmaf(xv[e], xv[e], s2[e & 1]);
-      float ss = s2[0] + s2[1];
+      for (int e = 1; e < 4; ++e) s2 = __ffma2_rn(xv[e], xv[e], s2);
+      float ss = s2.x + s2.y;
 #pragma unroll
       for (int m = kPbLanes / 2; m >= 1; m >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, m);
-      const float rinv = rsqrtf(ss * (1.f / kD) + eps);
-      float gw[8];
-      {
-        const float4 w0 = *reinterpret_cast<const float4*>(&wsh[off0]);
-        const float4 w1 = *reinterpret_cast<const float4*>(&wsh[off1]);
-        gw[0] = w0.x; gw[1] = w0.y; gw[2] = w0.z; gw[3] = w0.w;
-        gw[4] = w1.x; gw[5] = w1.y; gw[6] = w1.z; gw[7] = w1.w;
-      }
-      float d2[2] = {0.f, 0.f};
+      if (c < 8) {
+        // dz = R^T dy for the pairs (4c + e, 4c + 32 + e), frequency 4c + e:
+        // d1' = d1 cos + d2 sin, d2' = d2 cos - d1 sin
+        const float4 cv = cs[tl][0][c], sv = cs[tl][1][c], nv = cs[tl][2][c];
+        const float2 c2[2] = {make_float2(cv.x, cv.y), make_float2(cv.z, cv.w)};
+        const float2 s2v[2] = {make_float2(sv.x, sv.y), make_float2(sv.z, sv.w)};
+        const float2 n2[2] = {make_float2(nv.x, nv.y), make_float2(nv.z, nv.w)};
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        xv[e] *= rinv;                     // xh
-        gw[e] *= dz[e];                    // g = dz (1 + w)
-        d2[e & 1] = fmaf(gw[e], xv[e], d2[e & 1]);
+        for (int h = 0; h < 2; ++h) {
+          const float2 d1 = dz[h], d2 = dz[2 + h];
+          dz[h] = __ffma2_rn(d1, c2[h], __fmul2_rn(d2, s2v[h]));
+          dz[2 + h] = __ffma2_rn(d2, c2[h], __fmul2_rn(d1, n2[h]));
+        }
       }
-      float dot = d2[0] + d2[1];
+      const float rinv = rsqrtf(ss * (1.f / kD) + eps);
+      const float2 rr = make_float2(rinv, rinv);
+      float2 gw[4];
+      float2 d2 = make_float2(0.f, 0.f);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        xv[e] = __fmul2_rn(xv[e], rr);     // xh
+        gw[e] = __fmul2_rn(dz[e], w2[e]);  // g = dz (1 + w)
+        d2 = __ffma2_rn(gw[e], xv[e], d2);
+      }
+      float dot = d2.x + d2.y;
 #pragma unroll
       for (int m = kPbLanes / 2; m >= 1; m >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, m);
-      const float mean = dot * (1.f / kD);
+      const float nmean = dot * (-1.f / kD);
       if (valid) {
-        float o[8];
+        const float2 nm = make_float2(nmean, nmean);
+        uint32_t o[4];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          o[e] = rinv * (gw[e] - xv[e] * mean);
-          aw[e] = fmaf(dz[e], xv[e], aw[e]);
+        for (int e = 0; e < 4; ++e) {
+          const float2 v = __fmul2_rn(__ffma2_rn(xv[e], nm, gw[e]), rr);   // r (g - xh mean)
+          o[e] = pack_bf16x2(v.x, v.y);
+          aw[e] = __ffma2_rn(dz[e], xv[e], aw[e]);
         }
-        uint2 oa, ob;
-        oa.x = pack_bf16x2(o[0], o[1]);
-        oa.y = pack_bf16x2(o[2], o[3]);
-        ob.x = pack_bf16x2(o[4], o[5]);
-        ob.y = pack_bf16x2(o[6], o[7]);
         __nv_bfloat16* dr = dx + (row_base + R.r) * kD;
-        *reinterpret_cast<uint2*>(dr + off0) = oa;
-        *reinterpret_cast<uint2*>(dr + off1) = ob;
+        *reinterpret_cast<uint2*>(dr + off0) = make_uint2(o[0], o[1]);
+        *reinterpret_cast<uint2*>(dr + off1) = make_uint2(o[2], o[3]);
       }
     };
     // the loop bound is uniform over the CTA: every lane reaches the shuffles;
@@ -412,9 +424,11 @@ __global__ void __launch_bounds__(kPbThreads, 7) prologue_bwd_kernel(
   }
   // ---- dw: the CTA's 8 row slots -> one partial row
 #pragma unroll
-  for (int e = 0; e < 4; ++e) {
-    red[slot][off0 + e] = aw[e];
-    red[slot][off1 + e] = aw[4 + e];
+  for (int e = 0; e < 2; ++e) {
+    red[slot][off0 + 2 * e] = aw[e].x;
+    red[slot][off0 + 2 * e + 1] = aw[e].y;
+    red[slot][off1 + 2 * e] = aw[2 + e].x;
+    red[slot][off1 + 2 * e + 1] = aw[2 + e].y;
   }
   __syncthreads();
   for (int ch = tid; ch < kD; ch += blockDim.x) {
@@ -467,6 +481,8 @@ msa_status_t launch_prologue_bwd(const __nv_bfloat16* x, const __nv_bfloat16* dy
                                  __nv_bfloat16* dx, float* dw, const __nv_bfloat16* w, int H,
                                  const int32_t* cu, int S, int T, float rope_base, float eps,
                                  float* dw_part, cudaStream_t stream) {
+  if (H > kProMaxH)
+    return fail(MSA_ERR_UNSUPPORTED, "prologue backward: at most %d heads (got %d)", kProMaxH, H);
   RopeTurns turns;
   const double two_pi = 6.283185307179586476925286766559;
   for (int i = 0; i < kRopeDim / 2; ++i) {

@@ -211,6 +211,35 @@ def test_prologue_odd_head_counts(m, heads):
         assert rel_l2(f64(dw), want_dw) <= 1e-4, f"{heads} {n} dw"
 
 
+def test_prologue_head_limit(m):
+    """256 heads per tensor (the most the prologue kernels take: a CTA's rows of
+    one tensor reach 16 x 256) against the oracle, forward and backward, on a
+    ragged pack; 257 heads are refused with an error before anything runs."""
+    cu_cpu = torch.tensor([0, 3, 20, 21], dtype=torch.int32)
+    cun = cu_cpu.numpy()
+    T = int(cun[-1])
+    gen = torch.Generator().manual_seed(256)
+    x = torch.randn((T, 256, 128), generator=gen).to(torch.bfloat16)
+    w = (0.1 * torch.randn(128, generator=gen)).to(torch.bfloat16)
+    dy = torch.randn((T, 256, 128), generator=gen).to(torch.bfloat16)
+    cu = cu_cpu.to(DEV)
+    y = m.msa_qk_norm_rope(x.to(DEV), w.to(DEV), cu)
+    dx, dw = m.msa_qk_norm_rope_bwd(x.to(DEV), dy.to(DEV), w.to(DEV), cu)
+    m.msa_check_status()
+    assert_prologue_close(f64(y), O.qk_norm_rope(f64(x), f64(w), cun), "256 heads")
+    want_dx, want_dw = O.qk_norm_rope_bwd(f64(x), f64(w), f64(dy), cun)
+    off = np.abs(f64(dx) - want_dx)
+    tol = bf16_step(want_dx) * 1.0001 + 1e-5 * np.max(np.abs(want_dx), axis=-1, keepdims=True)
+    assert float(np.max(off - tol)) <= 0, "256 heads dx"
+    assert rel_l2(f64(dw), want_dw) <= 1e-4, "256 heads dw"
+    big = torch.zeros((T, 257, 128), dtype=torch.bfloat16, device=DEV)
+    with pytest.raises(m.MSAError):
+        m.msa_qk_norm_rope(big, w.to(DEV), cu)
+    with pytest.raises(m.MSAError):
+        m.msa_qk_norm_rope_bwd(big, big, w.to(DEV), cu)
+    m.msa_check_status()
+
+
 @pytest.mark.parametrize("name", ["tiny", "ragged"])
 def test_prologue_backward_matches_oracle(m, name):
     """dx (bf16) and dw (fp32) of the q and k prologues against the fp64 closed
