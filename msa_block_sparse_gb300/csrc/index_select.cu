@@ -13,7 +13,9 @@
 // SM, so that one's waits are covered by the other's work); warp 0 claims
 // units from a counter and passes each id to the others:
 //   TMA    : the unit's Q tile, then its K blocks (128 x 128 bf16, 128B
-//            swizzle) into a 2-stage ring that runs on across units
+//            swizzle), each as its two 64-channel halves, into a 4-stage ring
+//            of halves that runs on across units (a half is refilled once the
+//            four K-steps that read it are done)
 //   MMA    : S_b = Q K_b^T (M = N = K = 128) into one of two TMEM buffers
 //   epilogue (4 warps, thread = query row = TMEM lane): row max of S_b,
 //            then a register-resident insertion into a descending top-15
@@ -33,11 +35,12 @@ namespace msa {
 
 namespace {
 
-constexpr int kSelStages = 2;
+constexpr int kSelStages = 4;            // half-block stages (64 of the 128 channels)
 constexpr int kSelQBufs = 1;
 constexpr int kSelCtasPerSm = 2;
 constexpr int kSelThreads = 192;         // warp 0 TMA, warp 1 MMA, warps 2..5 epilogue
 constexpr int kTileBytes = 128 * 128 * 2;  // one 128 x 128 bf16 tile
+constexpr int kHalfBytes = kTileBytes / 2; // its 64-channel half (one 128B-swizzled box)
 constexpr uint32_t kSelIdesc = idesc_bf16(128, 128, false, false);
 constexpr int kUnitSlots = 4;
 constexpr int kUnitReaders = 1 + 4;      // the MMA thread and the 4 epilogue warps
@@ -46,7 +49,7 @@ constexpr int kPartKeys = 15 * 128;      // one chunk's lists: entry keys, [15][
 
 struct SelSmem {
   uint8_t q[kSelQBufs][kTileBytes];
-  uint8_t k[kSelStages][kTileBytes];
+  uint8_t k[kSelStages][kHalfBytes];
   uint64_t q_full[kSelQBufs], q_empty[kSelQBufs];
   uint64_t k_full[kSelStages];
   uint64_t k_empty[kSelStages];
@@ -378,15 +381,18 @@ __global__ void __launch_bounds__(kSelThreads, kSelCtasPerSm)
         ++nq;
         mbar_arrive_expect_tx(&sm.q_full[qbuf], kTileBytes);
         tma_load_3d(sm.q[qbuf], &tm_q, &sm.q_full[qbuf], 0, h, seq0 + qb * kBlock);
-        tma_load_3d(sm.q[qbuf] + kTileBytes / 2, &tm_q, &sm.q_full[qbuf], 64, h,
+        tma_load_3d(sm.q[qbuf] + kHalfBytes, &tm_q, &sm.q_full[qbuf], 64, h,
                     seq0 + qb * kBlock);
         bool ok = true;
-        for (int b = b0; b < b1; ++b, ++kb) {
-          const int st = kb % kSelStages;
-          if (!(ok = mbar_wait(&sm.k_empty[st], ((kb / kSelStages) & 1) ^ 1, status, 3))) break;
-          mbar_arrive_expect_tx(&sm.k_full[st], kTileBytes);
-          tma_load_3d(sm.k[st], &tm_k, &sm.k_full[st], 0, h, seq0 + b * kBlock);
-          tma_load_3d(sm.k[st] + kTileBytes / 2, &tm_k, &sm.k_full[st], 64, h, seq0 + b * kBlock);
+        // each K block as its two channel halves, one ring stage each: a half
+        // is reloaded as soon as the four K-steps that read it are done
+        for (int b = b0; ok && b < b1; ++b) {
+          for (int hf = 0; hf < 2; ++hf, ++kb) {
+            const int st = kb % kSelStages;
+            if (!(ok = mbar_wait(&sm.k_empty[st], ((kb / kSelStages) & 1) ^ 1, status, 3))) break;
+            mbar_arrive_expect_tx(&sm.k_full[st], kHalfBytes);
+            tma_load_3d(sm.k[st], &tm_k, &sm.k_full[st], 64 * hf, h, seq0 + b * kBlock);
+          }
         }
         if (!ok) break;
       }
@@ -394,7 +400,7 @@ __global__ void __launch_bounds__(kSelThreads, kSelCtasPerSm)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (elect_one()) {
-      uint32_t kb = 0, nq = 0;
+      uint32_t kb = 0, kh = 0, nq = 0;   // blocks (S buffers), K halves (ring stages), Q tiles
       bool ok = true;
       for (int ul = 0; ok; ++ul) {
         const int si = ul % kUnitSlots;
@@ -409,20 +415,23 @@ __global__ void __launch_bounds__(kSelThreads, kSelCtasPerSm)
         if (!(ok = mbar_wait(&sm.q_full[qbuf], (nq / kSelQBufs) & 1, status, 5))) break;
         ++nq;
         const uint32_t qa = smem_u32(sm.q[qbuf]);
-        for (int i = 0; i < nb; ++i, ++kb) {
-          const int st = kb % kSelStages, buf = kb & 1;
-          ok = mbar_wait(&sm.k_full[st], (kb / kSelStages) & 1, status, 6) &&
-               mbar_wait(&sm.s_empty[buf], ((kb >> 1) & 1) ^ 1, status, 7);
-          if (!ok) break;
-          tc_fence_after();
-          const uint32_t ka = smem_u32(sm.k[st]);
+        for (int i = 0; ok && i < nb; ++i, ++kb) {
+          const int buf = kb & 1;
+          if (!(ok = mbar_wait(&sm.s_empty[buf], ((kb >> 1) & 1) ^ 1, status, 7))) break;
+          // channels [64 hf, 64 hf + 64): four K-steps on each half of Q and K_b
+          for (int hf = 0; hf < 2; ++hf, ++kh) {
+            const int st = kh % kSelStages;
+            if (!(ok = mbar_wait(&sm.k_full[st], (kh / kSelStages) & 1, status, 6))) break;
+            tc_fence_after();
+            const uint32_t ka = smem_u32(sm.k[st]);
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
-            const uint32_t off = (kk >> 2) * (kTileBytes / 2) + (kk & 3) * 32;
-            umma_bf16(tmem + buf * 128, sdesc_sw128(qa + off, 16, 1024),
-                      sdesc_sw128(ka + off, 16, 1024), kSelIdesc, kk > 0);
+            for (int kk = 0; kk < 4; ++kk) {
+              umma_bf16(tmem + buf * 128, sdesc_sw128(qa + hf * kHalfBytes + kk * 32, 16, 1024),
+                        sdesc_sw128(ka + kk * 32, 16, 1024), kSelIdesc, (hf | kk) != 0);
+            }
+            umma_commit(&sm.k_empty[st]);
           }
-          umma_commit(&sm.k_empty[st]);
+          if (!ok) break;
           umma_commit(&sm.s_full[buf]);
         }
         umma_commit(&sm.q_empty[qbuf]);      // the Q tile is free once these MMAs are done
@@ -518,14 +527,22 @@ __global__ void __launch_bounds__(kSelThreads, kSelCtasPerSm)
 #pragma unroll
           for (int i = 0; i < 15; ++i) key[i] = entry_key(best[i], ids[i]);
           key[15] = 0ull;
-          for (int c = 0; c < nch; ++c) {
-            if (c == chunk) continue;
-            const unsigned long long* other = part + static_cast<size_t>(slot0 + c) * kPartKeys;
-            unsigned long long ok16[16];
+          // the other chunks' lists, three at a time: all their loads are in
+          // flight together, then they are merged in
+          for (int c0 = 0; c0 < nch; c0 += 3) {
+            unsigned long long ok16[3][16];
 #pragma unroll
-            for (int e = 0; e < 15; ++e) ok16[e] = ld_relaxed_gpu(other + e * 128 + r);
-            ok16[15] = 0ull;
-            merge_top16(key, ok16);
+            for (int j = 0; j < 3; ++j) {
+              const int c = c0 + j;
+              const unsigned long long* other = part + static_cast<size_t>(slot0 + c) * kPartKeys;
+#pragma unroll
+              for (int e = 0; e < 15; ++e)
+                ok16[j][e] = (c < nch && c != chunk) ? ld_relaxed_gpu(other + e * 128 + r) : 0ull;
+              ok16[j][15] = 0ull;
+            }
+#pragma unroll
+            for (int j = 0; j < 3; ++j)
+              if (c0 + j < nch && c0 + j != chunk) merge_top16(key, ok16[j]);
           }
 #pragma unroll
           for (int i = 0; i < 15; ++i) ids[i] = entry_id(key[i]);
