@@ -17,14 +17,16 @@
 //            of halves that runs on across units (a half is refilled once the
 //            four K-steps that read it are done)
 //   MMA    : S_b = Q K_b^T (M = N = K = 128) into one of two TMEM buffers
-//   epilogue (4 warps, thread = query row = TMEM lane): row max of S_b,
-//            then a register-resident insertion into a descending top-15
-//            list (strictly greater wins; blocks arrive in ascending order,
-//            so equal scores keep the lower id).
+//   epilogue (4 warps, thread = query row = TMEM lane): row max of S_b; a
+//            unit of at most 16 blocks keeps the maxima in a register shift
+//            line and sorts them once at its end, a longer one inserts each
+//            into a register-resident top-15 list as it arrives.  Both order
+//            by (score descending, block id ascending): equal scores keep the
+//            lower id, and an insertion moves the entries below it down in
+//            order.
 // A tile cut into several chunks leaves each chunk's list in the workspace;
 // the chunk that finishes last (arrival counter) merges the others into its
-// own, ordering by (score descending, block id ascending) -- the order the
-// single-chunk insertion keeps -- and writes the selection.
+// own in the same order and writes the selection.
 // With the init rule ("#4581", Kernel tuning; read as: the first n_init
 // blocks are always kept) blocks b < n_init enter the list with score +inf,
 // so they take the first places and the best others fill the rest.
@@ -111,6 +113,33 @@ __device__ __forceinline__ unsigned long long entry_key(float score, int id) {
 
 __device__ __forceinline__ int entry_id(unsigned long long key) {
   return static_cast<int>(0xffffffffu - static_cast<uint32_t>(key));
+}
+
+__device__ __forceinline__ float entry_score(unsigned long long key) {
+  uint32_t u = static_cast<uint32_t>(key >> 32);
+  u ^= (u & 0x80000000u) ? 0x80000000u : 0xffffffffu;
+  return __uint_as_float(u);
+}
+
+// k[0..15] sorted descending (bitonic sorting network)
+__device__ __forceinline__ void sort16_desc(unsigned long long* k) {
+#pragma unroll
+  for (int w = 2; w <= 16; w <<= 1) {
+#pragma unroll
+    for (int j = w >> 1; j > 0; j >>= 1) {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const int l = i ^ j;
+        if (l > i) {
+          const bool desc = (i & w) == 0;
+          const bool sw = desc ? (k[i] < k[l]) : (k[i] > k[l]);
+          const unsigned long long a = k[i], b = k[l];
+          k[i] = sw ? b : a;
+          k[l] = sw ? a : b;
+        }
+      }
+    }
+  }
 }
 
 // a[0..15] and b[0..15] sorted descending -> a[0..15] = the 16 largest of
@@ -467,9 +496,11 @@ __global__ void __launch_bounds__(kSelThreads, kSelCtasPerSm)
         ids[i] = -1;
       }
       bool ok = true;
-      for (int b = b0; b < b1; ++b, ++kb) {
+      // S_b of block b -> its row max (the S buffer is freed right after the read)
+      auto block_max = [&](int b) -> float {
         const int buf = kb & 1;
-        if (!(ok = mbar_wait(&sm.s_full[buf], (kb >> 1) & 1, status, 9))) break;
+        ++kb;
+        if (!(ok = mbar_wait(&sm.s_full[buf], ((kb - 1) >> 1) & 1, status, 9))) return 0.f;
         __syncwarp();
         tc_fence_after();
         // all 128 columns in flight at once, one wait, then the buffer is free
@@ -490,18 +521,51 @@ __global__ void __launch_bounds__(kSelThreads, kSelCtasPerSm)
             t = max3f(t, __uint_as_float(w[j]), __uint_as_float(w[j + 1]));
           m4[q] = fmaxf(t, __uint_as_float(w[31]));
         }
-        const float mx = (b < n_init) ? INFINITY : fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
-        float cv = mx;
-        int ci = b;
+        return (b < n_init) ? INFINITY : fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+      };
+      if (b1 - b0 <= 16) {
+        // A unit of at most 16 blocks keeps every block's score in a shift
+        // register (newest first) and sorts them once at its end.
+        float sc[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) sc[i] = -INFINITY;
+        for (int b = b0; ok && b < b1; ++b) {
+          const float mx = block_max(b);
+#pragma unroll
+          for (int i = 15; i > 0; --i) sc[i] = sc[i - 1];
+          sc[0] = mx;
+        }
+        // sc[i] is block b1 - 1 - i; (score descending, id ascending) is the
+        // order the insertion below keeps, and -inf / -1 fill unused places
+        unsigned long long key[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) key[i] = (i < b1 - b0) ? entry_key(sc[i], b1 - 1 - i) : 0ull;
+        sort16_desc(key);
 #pragma unroll
         for (int i = 0; i < 15; ++i) {
-          if (cv > best[i]) {
-            const float tv = best[i];
-            const int ti = ids[i];
-            best[i] = cv;
-            ids[i] = ci;
-            cv = tv;
-            ci = ti;
+          best[i] = key[i] ? entry_score(key[i]) : -INFINITY;
+          ids[i] = key[i] ? entry_id(key[i]) : -1;
+        }
+      } else {
+        // a longer unit inserts each block into the top-15 lists as it arrives:
+        // at the first place it beats (strictly: an equal score already held
+        // came from a lower block), and every later entry moves down one place
+        // in order, so equal scores stay in ascending block order
+        for (int b = b0; ok && b < b1; ++b) {
+          float cv = block_max(b);
+          int ci = b;
+          bool moving = false;
+#pragma unroll
+          for (int i = 0; i < 15; ++i) {
+            moving = moving || cv > best[i];
+            if (moving) {
+              const float tv = best[i];
+              const int ti = ids[i];
+              best[i] = cv;
+              ids[i] = ci;
+              cv = tv;
+              ci = ti;
+            }
           }
         }
       }

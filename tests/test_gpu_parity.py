@@ -323,6 +323,49 @@ def test_index_select_init_rule(m, n_init):
             assert np.all(np.any(g[keep] == i, axis=-1)), f"{name}: block {i} not kept"
 
 
+def test_index_select_exact_ties(m):
+    """Key blocks 0 .. 9 of each sequence copies of one block B, every later
+    one a copy of 2B (exact in bf16), so a token's earlier blocks score
+    exactly m or 2m (m > 0): by the selection rule (equal scores: lower block
+    first) a token with own block o keeps the lowest min(15, o - 10) of the 2B
+    blocks 10 .. o - 1, then the lowest B blocks 0 .. in the places left, and
+    o.  The larger scores arrive after the tied ones, so a list kept in
+    score order must move tied entries down without reordering them.  The
+    150-block sequence makes the pack's chunks longer than 16 blocks, so both
+    the sorted-at-the-end path (units of at most 16 blocks) and the
+    insert-as-they-come path run, and chunk lists with tied entries are
+    merged across CTAs."""
+    lens = (150 * 128, 300, 0, 2100)
+    cu_cpu = torch.tensor(np.concatenate([[0], np.cumsum(lens)]), dtype=torch.int32)
+    T = int(cu_cpu[-1])
+    gen = torch.Generator().manual_seed(77)
+    qi = torch.randn((T, 1, 128), generator=gen).to(torch.bfloat16)
+    blk = torch.randn((128, 1, 128), generator=gen).to(torch.bfloat16)
+    ki = torch.empty((T, 1, 128), dtype=torch.bfloat16)
+    k = 10
+    for s0, L in zip(cu_cpu[:-1].tolist(), lens):
+        for b in range((L + 127) // 128):
+            n = min(128, L - 128 * b)
+            ki[s0 + 128 * b:s0 + 128 * b + n] = blk[:n] * (2 if b >= k else 1)
+    # every token's block maximum over B must be positive for 2B to score higher
+    q64, b64 = f64(qi)[:, 0, :], f64(blk)[:, 0, :]
+    assert np.all((q64 @ b64.T).max(axis=1) > 0)
+    sel = m.msa_index_select(qi.to(DEV), ki.to(DEV), cu_cpu.to(DEV), max(lens))
+    m.msa_check_status()
+    got = sel.cpu().numpy()[:, 0, :]
+    own = O.positions(cu_cpu.numpy()) // 128
+    want = np.full((T, 16), -1, dtype=np.int64)
+    for t in range(T):
+        o = int(own[t])
+        hi = np.arange(k, o)[:15]                       # 2B blocks, lowest first
+        lo = np.arange(min(o, k))[:15 - hi.size]        # then B blocks, lowest first
+        row = np.sort(np.concatenate([hi, lo, [o]]))
+        want[t, :row.size] = row
+    bad = np.nonzero(np.any(got != want, axis=1))[0]
+    assert bad.size == 0, f"{bad.size} rows differ, first {bad[:4].tolist()}: " \
+                          f"{got[bad[0]].tolist()} != {want[bad[0]].tolist()}"
+
+
 # ------------------------------------------------------------------ forward
 
 @pytest.mark.parametrize("name", ["tiny", "ragged"])
