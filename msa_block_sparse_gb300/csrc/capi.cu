@@ -257,7 +257,39 @@ bool make_tmap_bf16_strided(CUtensorMap* map, const void* base, int rank, const 
 // One CTA.  nb(s) = ceil(len_s / tile) tiles per sequence; tiles are listed with
 // qb descending, s ascending.  cnt[q] = #{s : nb(s) > q}; start[q] = sum of
 // cnt[q'] for q' > q; thread q then appends (s, q) for every qualifying s in
-// order, so the list is deterministic.
+// order, so the list is deterministic.  Both suffix sums are block-wide scans
+// over the entries taken from the top (1024 per pass, a running carry between
+// passes); nb(s) is kept in shared memory when it fits beside them.
+__host__ __device__ constexpr bool plan_keeps_nb(int S, int max_nb) {
+  return (2 * (max_nb + 1) + S) * 4 <= 48 * 1024;
+}
+
+// inclusive scan of v over the CTA; *total = the sum over the CTA
+__device__ __forceinline__ int block_incl_scan(int v, int* warp_sums, int* total) {
+  const int lane = threadIdx.x & 31, wp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const int x = __shfl_up_sync(0xffffffffu, v, d);
+    if (lane >= d) v += x;
+  }
+  if (lane == 31) warp_sums[wp] = v;
+  __syncthreads();
+  if (wp == 0) {
+    int w = lane < nw ? warp_sums[lane] : 0;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int x = __shfl_up_sync(0xffffffffu, w, d);
+      if (lane >= d) w += x;
+    }
+    warp_sums[lane] = w;
+  }
+  __syncthreads();
+  v += wp > 0 ? warp_sums[wp - 1] : 0;
+  *total = warp_sums[nw - 1];
+  __syncthreads();                          // warp_sums may be reused
+  return v;
+}
+
 __global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ cu, int S,
                                                     int tile, int max_nb,
                                                     int2* __restrict__ tiles,
@@ -265,44 +297,53 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ 
                                                     uint32_t* status) {
   pdl_enter();
   extern __shared__ int sh[];
-  int* cnt = sh;                // [max_nb + 1]
-  int* start = sh + max_nb + 1; // [max_nb + 1]
+  int* cnt = sh;                     // [max_nb + 1]
+  int* start = sh + max_nb + 1;      // [max_nb + 1]
+  int* nbs = sh + 2 * (max_nb + 1);  // [S] when it fits
+  __shared__ int warp_sums[32];
   const int tid = threadIdx.x;
+  const bool keep = plan_keeps_nb(S, max_nb);
   for (int q = tid; q <= max_nb; q += blockDim.x) cnt[q] = 0;
   __syncthreads();
+  auto nb_of = [&](int s) {
+    const int len = cu[s + 1] - cu[s];
+    const int nb = (len + tile - 1) / tile;
+    return len < 0 ? 0 : (nb > max_nb ? max_nb : nb);
+  };
   for (int s = tid; s < S; s += blockDim.x) {
-    int len = cu[s + 1] - cu[s];
-    int nb = (len + tile - 1) / tile;
-    if (len < 0 || nb > max_nb) {
-      atomicOr(status, kStatusBounds);
-      nb = len < 0 ? 0 : max_nb;
-    }
+    const int len = cu[s + 1] - cu[s];
+    if (len < 0 || (len + tile - 1) / tile > max_nb) atomicOr(status, kStatusBounds);
+    const int nb = nb_of(s);
+    if (keep) nbs[s] = nb;
     if (nb > 0) atomicAdd(&cnt[nb - 1], 1);   // histogram of nb - 1
   }
   __syncthreads();
-  // cnt[q] <- #{s : nb(s) - 1 >= q} (suffix sum), start[q] <- sum_{q' > q} cnt[q'].
+  // entry i of a pass is q = max_nb - 1 - i: the running inclusive scan is the
+  // suffix sum cnt[q] = #{s : nb(s) - 1 >= q}; a second running scan of those,
+  // less the entry itself, is start[q] = sum_{q' > q} cnt[q']
+  int carry_c = 0, carry_s = 0;
+  for (int base = 0; base < max_nb; base += blockDim.x) {
+    const int q = max_nb - 1 - (base + tid);
+    int tot_c, tot_s;
+    const int c = carry_c + block_incl_scan(q >= 0 ? cnt[q] : 0, warp_sums, &tot_c);
+    const int st = carry_s + block_incl_scan(q >= 0 ? c : 0, warp_sums, &tot_s);
+    if (q >= 0) {
+      cnt[q] = c;
+      start[q] = st - c;
+    }
+    carry_c += tot_c;
+    carry_s += tot_s;
+  }
   if (tid == 0) {
-    int run = 0;
-    for (int q = max_nb - 1; q >= 0; --q) {
-      run += cnt[q];
-      cnt[q] = run;
-    }
-    int acc = 0;
-    for (int q = max_nb - 1; q >= 0; --q) {
-      start[q] = acc;
-      acc += cnt[q];
-    }
-    *num_tiles = acc < max_tiles ? acc : max_tiles;
-    if (acc > max_tiles) atomicOr(status, kStatusBounds);
+    *num_tiles = carry_s < max_tiles ? carry_s : max_tiles;
+    if (carry_s > max_tiles) atomicOr(status, kStatusBounds);
   }
   __syncthreads();
-  for (int q = tid; q < max_nb; q += blockDim.x) {
-    int pos = start[q];
+  for (int qq = tid; qq < max_nb; qq += blockDim.x) {
+    int pos = start[qq];
     for (int s = 0; s < S; ++s) {
-      int len = cu[s + 1] - cu[s];
-      int nb = (len + tile - 1) / tile;
-      if (nb > max_nb) nb = max_nb;
-      if (nb > q && pos < max_tiles) tiles[pos++] = make_int2(s, q);
+      const int nb = keep ? nbs[s] : nb_of(s);
+      if (nb > qq && pos < max_tiles) tiles[pos++] = make_int2(s, qq);
     }
   }
 }
@@ -319,7 +360,7 @@ Plan carve_plan(WsCursor& ws, int T, int S, int tile) {
 msa_status_t launch_plan(const Plan& plan, const int32_t* cu_seqlens, int S, int max_seqlen,
                          cudaStream_t stream) {
   int max_nb = (max_seqlen + plan.tile - 1) / plan.tile;
-  size_t smem = 2 * (max_nb + 1) * sizeof(int);
+  size_t smem = (2 * (max_nb + 1) + (plan_keeps_nb(S, max_nb) ? S : 0)) * sizeof(int);
   uint32_t* sw = nullptr;
   if (msa_status_t e = status_word(&sw); e != MSA_OK) return e;
   {

@@ -47,6 +47,11 @@ constexpr uint32_t kSelIdesc = idesc_bf16(128, 128, false, false);
 constexpr int kUnitSlots = 4;
 constexpr int kUnitReaders = 1 + 4;      // the MMA thread and the 4 epilogue warps
 constexpr int kMinChunk = 16;            // blocks
+// the plan keeps the sequences' tile starts in shared memory beside its
+// histogram when both fit in the default 48 KB
+__host__ __device__ constexpr bool sel_plan_keeps_ts(int S, int max_nb) {
+  return (max_nb + 1 + S + 1) * 4 <= 48 * 1024;
+}
 constexpr int kPartKeys = 15 * 128;      // one chunk's lists: entry keys, [15][128]
 
 struct SelSmem {
@@ -214,6 +219,9 @@ __global__ void __launch_bounds__(1024) select_plan_kernel(
     uint32_t* status) {
   pdl_enter();
   extern __shared__ int hist[];            // [max_nb + 1]: units by block count
+  // tile_start[0 .. S) is searched once per (tile, head): in shared memory
+  // (after hist) when it fits, else in the workspace
+  int* const ts = sel_plan_keeps_ts(S, max_nb) ? hist + max_nb + 1 : tile_start;
   __shared__ int warp_sums[32];
   __shared__ int carry;
   __shared__ unsigned long long wsum;
@@ -269,7 +277,7 @@ __global__ void __launch_bounds__(1024) select_plan_kernel(
       wloc += static_cast<unsigned long long>(nb) * (nb > 0 ? nb - 1 : 0) / 2;
     }
     const int off = scan(nb);
-    if (s < S) tile_start[s] = off;
+    if (s < S) ts[s] = off;
   }
   const int ntiles = min(carry, max_tiles);
   if (tid == 0 && carry > max_tiles) atomicOr(status, kStatusBounds);
@@ -283,7 +291,7 @@ __global__ void __launch_bounds__(1024) select_plan_kernel(
   const int ncidx = ntiles * Hi;
   for (int ci = tid; ci < ncidx; ci += blockDim.x) {
     const int t = ci / Hi;
-    const int qb = t - tile_start[seq_of_tile(tile_start, S, t)];
+    const int qb = t - ts[seq_of_tile(ts, S, t)];
     const int nch = qb > 0 ? (qb + C - 1) / C : 1;
     for (int c = 0; c < nch; ++c) atomicAdd(&hist[max(0, min(C, qb - c * C))], 1);
     merge_ctr[ci] = 0;
@@ -310,8 +318,8 @@ __global__ void __launch_bounds__(1024) select_plan_kernel(
     int nch = 0, qb = 0, s = 0;
     if (ci < ncidx) {
       const int t = ci / Hi;
-      s = seq_of_tile(tile_start, S, t);
-      qb = t - tile_start[s];
+      s = seq_of_tile(ts, S, t);
+      qb = t - ts[s];
       nch = qb > 0 ? (qb + C - 1) / C : 1;
     }
     const int slot0 = scan(nch > 1 ? nch : 0);
@@ -660,7 +668,9 @@ msa_status_t launch_index_select(const void* q_idx, const void* k_idx, const int
   const int max_nb = (max_seqlen + kBlock - 1) / kBlock;
   {
     TraceScope trace_("select_plan_kernel", stream);
-    launch_pdl(select_plan_kernel, 1, 1024, static_cast<size_t>(max_nb + 1) * sizeof(int),
+    const size_t plan_smem =
+        static_cast<size_t>(max_nb + 1 + (sel_plan_keeps_ts(S, max_nb) ? S + 1 : 0)) * sizeof(int);
+    launch_pdl(select_plan_kernel, 1, 1024, plan_smem,
         stream, cu, S, Hi, max_nb, w.units, w.aux, w.num_units, w.claim, w.merge_ctr,
         w.tile_start, w.max_units, w.max_tiles, sw);
   }

@@ -111,6 +111,29 @@ def test_qsa_pack16k_sampled(m):
         assert rk_ <= 1e-2 and rv_ <= 1e-2, f"block {(s, g, b)}: dk {rk_:.3e} dv {rv_:.3e}"
 
 
+def test_qsa_long_sequence_sampled(m):
+    """A 12,001-token sequence: 1201 query tiles of 10 tokens, more than the
+    plan kernel scans in one pass (1024 entries per pass), beside a 5-token
+    and a 300-token one; o and lse on sampled rows, dq on a few."""
+    shape = W.QsaShape("qsa-long-12q1kv", (12001, 5, 300), 12, 1, 64)
+    cpu = W.make_qsa(shape, seed=3, device="cpu")
+    gpu = {k: v.to(DEV) for k, v in cpu.items()}
+    o, lse, dq, dk, dv = run(m, shape, gpu)
+    sel = cpu["sel"].numpy()
+    cu = cpu["cu_seqlens"].numpy()
+    q, k, v, do = (f64(cpu[n]) for n in ("q", "k", "v", "do"))
+    rng = np.random.default_rng(11)
+    toks = sorted(set(rng.integers(0, shape.T, 24).tolist())
+                  | {0, 10239, 10240, 11999, 12000, 12001, 12005, shape.T - 1})
+    oo, olse = O.sparse_attn_fwd(q, k, v, sel, cu, SCALE, tokens=toks, block=W.QSA_BLOCK)
+    assert_close(f64(o[toks]), oo, 2e-2, 1e-2, "long o")
+    assert_close(lse[toks].cpu().numpy().astype(np.float64), olse, 1e-3, 1e-4, "long lse")
+    ref = O.sparse_attn_bwd(q, k, v, do, sel, cu, SCALE, dq_tokens=toks[:8], dkv_blocks=[],
+                            block=W.QSA_BLOCK)
+    r = rel_l2(f64(dq[toks[:8]]), ref["dq"])
+    assert r <= 1e-2, f"long dq rel-L2 {r:.3e}"
+
+
 def test_qsa_rejects_bad_shapes(m):
     shape, cpu, gpu = inputs(0)
     q12 = gpu["q"][:, :11].contiguous()
