@@ -128,11 +128,13 @@ __device__ __forceinline__ uint32_t tile_bits(const uint32_t* mrow, int kt) {
 
 // One warp per (token, KV head) row, grid-striding: the bitmap of the row's
 // selected blocks.  An id beyond the token's own block sets the bounds bit and is
-// dropped; -1 entries are padding.
+// dropped; -1 entries are padding.  With vec (topk a multiple of 4, sel 16-byte
+// aligned) every lane reads its ids as 16-byte vectors, all of the row's loads
+// in flight at once.
 __global__ void __launch_bounds__(256) qsa_mask_kernel(const int32_t* __restrict__ sel,
                                                        const int32_t* __restrict__ cu, int S,
                                                        int T, int Hkv, int topk, int W,
-                                                       uint32_t* __restrict__ masks,
+                                                       uint32_t* __restrict__ masks, int vec,
                                                        uint32_t* status) {
   pdl_enter();
   __shared__ uint32_t rows[8][kQsaMaxWords];
@@ -151,14 +153,32 @@ __global__ void __launch_bounds__(256) qsa_mask_kernel(const int32_t* __restrict
     for (int w = lane; w < W; w += 32) row[w] = 0u;
     __syncwarp();
     const int32_t* src = sel + static_cast<size_t>(rr) * topk;
-    for (int j = lane; j < topk; j += 32) {
-      const int b = __ldg(src + j);
-      if (b < 0) continue;
+    auto mark = [&](int b) {
+      if (b < 0) return;
       if (b > own || b >= W * 32) {
         atomicOr(status, kStatusBounds);
-        continue;
+        return;
       }
       atomicOr(&row[b >> 5], 1u << (b & 31));
+    };
+    if (vec) {
+      constexpr int kV = kQsaMaxTopk / 128;     // 16-byte vectors per lane at most
+      const int4* src4 = reinterpret_cast<const int4*>(src);
+      int4 ids[kV];
+#pragma unroll
+      for (int i = 0; i < kV; ++i) {
+        const int j4 = lane + 32 * i;
+        ids[i] = (4 * j4 < topk) ? __ldg(src4 + j4) : make_int4(-1, -1, -1, -1);
+      }
+#pragma unroll
+      for (int i = 0; i < kV; ++i) {
+        mark(ids[i].x);
+        mark(ids[i].y);
+        mark(ids[i].z);
+        mark(ids[i].w);
+      }
+    } else {
+      for (int j = lane; j < topk; j += 32) mark(__ldg(src + j));
     }
     __syncwarp();
     uint32_t* dst = masks + static_cast<size_t>(rr) * W;
@@ -1389,7 +1409,8 @@ static msa_status_t launch_qsa_tilemap(const int32_t* sel, const int32_t* cu, in
   {
     TraceScope trace_("qsa_mask_kernel", stream);
     launch_pdl(qsa_mask_kernel, capped_blocks(static_cast<size_t>(T) * Hkv, 8, 8 * sms), 256, 0,
-        stream, sel, cu, S, T, Hkv, topk, fw.W, fw.masks, sw);
+        stream, sel, cu, S, T, Hkv, topk, fw.W, fw.masks,
+        (topk % 4 == 0 && (reinterpret_cast<uintptr_t>(sel) & 15) == 0) ? 1 : 0, sw);
   }
   QSA_TRY(check_launch("qsa_mask_kernel"));
   QSA_TRY(launch_plan(fw.plan, cu, S, max_seqlen, stream));
