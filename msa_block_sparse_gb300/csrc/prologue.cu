@@ -45,7 +45,8 @@ constexpr int kProMaxH = 256;                // heads per tensor (token of a row
 // (8 channels each: thread c < 8 holds the rotated pairs (4c + e, 4c + 32 + e),
 // c >= 8 the pass-through channels 64 + 8 (c - 8) ..); four rows per thread in
 // registers, so three rows' loads are in flight while the fourth is
-// normalised, rotated and stored (8 CTAs per SM)
+// normalised, rotated and stored; the thread's weights stay in registers
+// (66 registers, 7 CTAs per SM: a 16k pack's 1024 CTAs still run in one wave)
 constexpr int kPfThreads = 128;
 constexpr int kPfLanes = 16;
 constexpr int kPfSlots = kPfThreads / kPfLanes;
@@ -66,10 +67,10 @@ __device__ __forceinline__ float2 bf2_to_f2(uint32_t u) {
   return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u));
 }
 
-// (cos, sin, -sin) of one token's frequencies 4g .. 4g + 3 (thread = (token, g)):
+// (cos, sin) of one token's frequencies 4g .. 4g + 3 (thread = (token, g)):
 // the token's position is found by a binary search over cu, the angle in
 // turns by the 64-bit fixed-point product described above
-__device__ __forceinline__ void rope_table_entry(float4 (*cs)[3][kRopeDim / 8], const RopeTurns& turns,
+__device__ __forceinline__ void rope_table_entry(float4 (*cs)[2][kRopeDim / 8], const RopeTurns& turns,
                                                  const int32_t* __restrict__ cu, int S, int T,
                                                  int t0, int tid) {
   const int qt = tid >> 3, g = tid & 7;
@@ -90,16 +91,15 @@ __device__ __forceinline__ void rope_table_entry(float4 (*cs)[3][kRopeDim / 8], 
   }
   cs[qt][0][g] = make_float4(cv[0], cv[1], cv[2], cv[3]);
   cs[qt][1][g] = make_float4(sv[0], sv[1], sv[2], sv[3]);
-  cs[qt][2][g] = make_float4(-sv[0], -sv[1], -sv[2], -sv[3]);
 }
 
-__global__ void __launch_bounds__(kPfThreads, 8) prologue_kernel(const PrologueArgs args,
+__global__ void __launch_bounds__(kPfThreads, 7) prologue_kernel(const PrologueArgs args,
                                                                   const RopeTurns turns,
                                                                   const int32_t* __restrict__ cu,
                                                                   int S, int T, float eps,
                                                                   uint32_t* status) {
   pdl_enter();
-  __shared__ __align__(16) float4 cs[kProTokens][3][kRopeDim / 8];
+  __shared__ __align__(16) float4 cs[kProTokens][2][kRopeDim / 8];
   __shared__ __align__(16) float wsh[4][kD];
   __shared__ ProJobRows js[4];
   const int t0 = blockIdx.x * kProTokens;
@@ -176,37 +176,45 @@ __global__ void __launch_bounds__(kPfThreads, 8) prologue_kernel(const PrologueA
   rope_table_entry(cs, turns, cu, S, T, t0, tid);
   __syncthreads();
 
+  // 1 + w of the thread's 8 channels for tensor wj, in registers; reloaded
+  // when a row of another tensor comes up (three times per thread at most)
+  int wj = -1;
+  float2 w2[4];
   auto process = [&](const Rows& R) {
     const int j = R.jt < 0 ? 0 : (R.jt & 3);
     const int tl = R.jt < 0 ? 0 : (R.jt >> 2);
+    if (j != wj) {
+      const float4 w0 = *reinterpret_cast<const float4*>(&wsh[j][off0]);
+      const float4 w1 = *reinterpret_cast<const float4*>(&wsh[j][off1]);
+      w2[0] = make_float2(w0.x, w0.y);
+      w2[1] = make_float2(w0.z, w0.w);
+      w2[2] = make_float2(w1.x, w1.y);
+      w2[3] = make_float2(w1.z, w1.w);
+      wj = j;
+    }
     // x: channels off0 + {0,1}, off0 + {2,3}, off1 + {0,1}, off1 + {2,3}
     float2 x[4] = {bf2_to_f2(R.xa.x), bf2_to_f2(R.xa.y), bf2_to_f2(R.xb.x), bf2_to_f2(R.xb.y)};
     float2 s2 = __fmul2_rn(x[0], x[0]);
 #pragma unroll
     for (int e = 1; e < 4; ++e) s2 = __ffma2_rn(x[e], x[e], s2);
     float ss = s2.x + s2.y;
-    {
-      // x (1 + w) while the sum of squares is reduced
-      const float4 w0 = *reinterpret_cast<const float4*>(&wsh[j][off0]);
-      const float4 w1 = *reinterpret_cast<const float4*>(&wsh[j][off1]);
-      x[0] = __fmul2_rn(x[0], make_float2(w0.x, w0.y));
-      x[1] = __fmul2_rn(x[1], make_float2(w0.z, w0.w));
-      x[2] = __fmul2_rn(x[2], make_float2(w1.x, w1.y));
-      x[3] = __fmul2_rn(x[3], make_float2(w1.z, w1.w));
-    }
+    // x (1 + w) while the sum of squares is reduced
+#pragma unroll
+    for (int e = 0; e < 4; ++e) x[e] = __fmul2_rn(x[e], w2[e]);
 #pragma unroll
     for (int m = kPfLanes / 2; m >= 1; m >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, m);
     if (c < 8) {
       // rotate channel 4c + e (x1) with 4c + 32 + e (x2), frequency 4c + e:
       // x1' = x1 cos - x2 sin, x2' = x2 cos + x1 sin (pairs e = 0,1 and 2,3)
-      const float4 cv = cs[tl][0][c], sv = cs[tl][1][c], nv = cs[tl][2][c];
+      const float4 cv = cs[tl][0][c], sv = cs[tl][1][c];
       const float2 c2[2] = {make_float2(cv.x, cv.y), make_float2(cv.z, cv.w)};
       const float2 s2v[2] = {make_float2(sv.x, sv.y), make_float2(sv.z, sv.w)};
-      const float2 n2[2] = {make_float2(nv.x, nv.y), make_float2(nv.z, nv.w)};
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         const float2 x1 = x[h], x2 = x[2 + h];
-        x[h] = __ffma2_rn(x1, c2[h], __fmul2_rn(x2, n2[h]));
+        // x1 cos - x2 sin as x1 cos + (-x2) sin: the sign goes on the product's operand
+        const float2 nx2 = make_float2(-x2.x, -x2.y);
+        x[h] = __ffma2_rn(x1, c2[h], __fmul2_rn(nx2, s2v[h]));
         x[2 + h] = __ffma2_rn(x2, c2[h], __fmul2_rn(x1, s2v[h]));
       }
     }
@@ -303,7 +311,7 @@ __global__ void __launch_bounds__(kPbThreads, 7) prologue_bwd_kernel(
     const RopeTurns turns, const int32_t* __restrict__ cu, int S, int T, float eps,
     float* __restrict__ dw_part) {
   pdl_enter();
-  __shared__ __align__(16) float4 cs[kProTokens][3][kRopeDim / 8];
+  __shared__ __align__(16) float4 cs[kProTokens][2][kRopeDim / 8];
   __shared__ float red[kPbSlots][kD + 4];
   const int tid = threadIdx.x;
   const int c = tid & (kPbLanes - 1);
@@ -370,15 +378,15 @@ __global__ void __launch_bounds__(kPbThreads, 7) prologue_bwd_kernel(
       if (c < 8) {
         // dz = R^T dy for the pairs (4c + e, 4c + 32 + e), frequency 4c + e:
         // d1' = d1 cos + d2 sin, d2' = d2 cos - d1 sin
-        const float4 cv = cs[tl][0][c], sv = cs[tl][1][c], nv = cs[tl][2][c];
+        const float4 cv = cs[tl][0][c], sv = cs[tl][1][c];
         const float2 c2[2] = {make_float2(cv.x, cv.y), make_float2(cv.z, cv.w)};
         const float2 s2v[2] = {make_float2(sv.x, sv.y), make_float2(sv.z, sv.w)};
-        const float2 n2[2] = {make_float2(nv.x, nv.y), make_float2(nv.z, nv.w)};
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           const float2 d1 = dz[h], d2 = dz[2 + h];
+          const float2 nd1 = make_float2(-d1.x, -d1.y);
           dz[h] = __ffma2_rn(d1, c2[h], __fmul2_rn(d2, s2v[h]));
-          dz[2 + h] = __ffma2_rn(d2, c2[h], __fmul2_rn(d1, n2[h]));
+          dz[2 + h] = __ffma2_rn(d2, c2[h], __fmul2_rn(nd1, s2v[h]));
         }
       }
       const float rinv = rsqrtf(ss * (1.f / kD) + eps);
