@@ -580,6 +580,17 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     const uint32_t trow = static_cast<uint32_t>(subp * 32) << 16;
     const float sl2 = scale * kLog2e;
     uint32_t tcount = 0, bc = 0;
+    // the storing warp of each half: 1 + the Q buffer its last tile's output
+    // stores still read from (handed back after the next tile's first block)
+    int store_tb = 0;
+    auto release_stored = [&]() {
+      if (store_tb) {
+        bulk_wait_read_all();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.tile_empty[store_tb - 1]);
+        store_tb = 0;
+      }
+    };
     bool ok = true;
     for (;;) {
       const int tb = tcount & 1;
@@ -675,6 +686,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         tc_fence_before();
         mbar_arrive(&sm.p_full[h][bc & 1]);
         ++bc;
+        if (i == 0) release_stored();
       }
       if (!ok) break;
       // ---- epilogue: merge the two halves of every row
@@ -732,10 +744,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             tma_store_3d(&tm_o, stage + lane * kTokRows, 64 * h, g * kG,
                          t.seq0 + t.p0 + member_offset(t, lane));
             bulk_commit_group();
-            bulk_wait_read_all();             // the Q buffer may be reloaded after this
           }
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&sm.tile_empty[tb]);
+          // the Q buffer goes back to the producer once the stores have read
+          // it: after the next tile's first block, not here, so that this
+          // warp starts that tile without waiting for them
+          store_tb = tb + 1;
         }
         ok = okw;
       }
@@ -744,6 +757,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       tc_fence_before();
       ++tcount;
     }
+    release_stored();
+    bulk_wait_all();                           // this warp's output stores are complete
   }
   tc_fence_before();
   __syncthreads();
