@@ -24,8 +24,9 @@
 //            P_h is packed to bf16 into the S buffer it came from.  The
 //            epilogue merges the halves, o = (O_0 2^(m_0-m) + O_1 2^(m_1-m)) / l,
 //            stages the tile in its (finished) Q buffer and writes it with one
-//            tensor store per token and half; the next tile's first PV waits
-//            until both halves have read O_0 and O_1.
+//            tensor store per token and half, each warp storing the two tokens
+//            whose rows it holds; the next tile's first PV waits until both
+//            halves have read O_0 and O_1.
 #include "kernels.cuh"
 
 namespace msa {
@@ -338,7 +339,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   if (tid == 0) {
     for (int i = 0; i < 2; ++i) {
       mbar_init(&sm.tile_full[i], 1);
-      mbar_init(&sm.tile_empty[i], 2 + 2 + 1);
+      mbar_init(&sm.tile_empty[i], 2 + 8 + 1);
       mbar_init(&sm.k_full[i], 1);
       mbar_init(&sm.k_empty[i], 2);
       mbar_init(&sm.v_full[i], 1);
@@ -580,8 +581,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     const uint32_t trow = static_cast<uint32_t>(subp * 32) << 16;
     const float sl2 = scale * kLog2e;
     uint32_t tcount = 0, bc = 0;
-    // the storing warp of each half: 1 + the Q buffer its last tile's output
-    // stores still read from (handed back after the next tile's first block)
+    // 1 + the Q buffer this warp's last output stores still read from (handed
+    // back after the next tile's first block)
     int store_tb = 0;
     auto release_stored = [&]() {
       if (store_tb) {
@@ -732,24 +733,27 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       tc_fence_before();
       fence_proxy_async_smem();                // staged rows -> the tensor stores' reads
       mbar_arrive(&sm.o_done[h]);
+      __syncwarp();
+      {
+        // this warp's 32 rows are tokens 2 subp and 2 subp + 1 of the tile:
+        // it stores them itself, one tensor store each; the Q buffer goes back
+        // to the producer once they have read it, after the next tile's first
+        // block, so that the warp starts that tile without waiting for them
+        const int tk = 2 * subp + lane;
+        if (lane < 2 && tk < t.ntok) {
+          tma_store_3d(&tm_o, stage + tk * kTokRows, 64 * h, g * kG,
+                       t.seq0 + t.p0 + member_offset(t, tk));
+          bulk_commit_group();
+        }
+        store_tb = tb + 1;
+      }
       if (subp == kFirstHalfWarp % 4) {
-        // one warp per half: once all the half's rows are read and staged,
-        // release O, store each token's rows and hand the Q buffer back
+        // one warp per half: once all the half's threads have read O, release
+        // it to the next tile's PV
         bool okw = true;
         if (lane == 0) okw = mbar_wait(&sm.o_done[h], tcount & 1, status, 17);
         okw = __shfl_sync(0xffffffffu, okw ? 1 : 0, 0) != 0;
-        if (okw) {
-          if (lane == 0) mbar_arrive(&sm.o_free);
-          if (lane < t.ntok) {
-            tma_store_3d(&tm_o, stage + lane * kTokRows, 64 * h, g * kG,
-                         t.seq0 + t.p0 + member_offset(t, lane));
-            bulk_commit_group();
-          }
-          // the Q buffer goes back to the producer once the stores have read
-          // it: after the next tile's first block, not here, so that this
-          // warp starts that tile without waiting for them
-          store_tb = tb + 1;
-        }
+        if (okw && lane == 0) mbar_arrive(&sm.o_free);
         ok = okw;
       }
       if (!(ok = __all_sync(0xffffffffu, ok))) break;
