@@ -193,6 +193,21 @@ MSA_API msa_status_t msa_sparse_attn_fwd(const void* q, const void* k, const voi
                                  void* o, float* lse, void* workspace,
                                  size_t workspace_bytes, msa_stream_t stream);
 
+/* The forward of a training step: msa_sparse_attn_fwd that also zeroes the
+ * fp32 accumulators and item counters of `bwd_workspace` (sized by
+ * msa_sparse_attn_bwd_workspace_size for the same T, S, Hq, Hkv, max_seqlen)
+ * while it runs, by bulk copies from the forward's otherwise idle memory
+ * bandwidth.  It stands in for msa_sparse_attn_bwd_prepare: follow it with
+ * msa_sparse_attn_bwd_prepared on that workspace (same stream, or an event),
+ * writing nothing into the workspace in between. */
+MSA_API msa_status_t msa_sparse_attn_fwd_train(const void* q, const void* k, const void* v,
+                                               const int32_t* sel, const int32_t* cu_seqlens,
+                                               int S, int T, int Hq, int Hkv, int max_seqlen,
+                                               float scale, void* o, float* lse,
+                                               void* workspace, size_t workspace_bytes,
+                                               void* bwd_workspace, size_t bwd_workspace_bytes,
+                                               msa_stream_t stream);
+
 /* ------------------------------------------------------------------------
  * Block-sparse attention backward ("#4581", "Kernel tuning"; the selection
  * is constant: "MiniMax-M3.1-Flash", 5.4 "Notable quirks").

@@ -46,6 +46,9 @@ _SIGNATURES = {
     "msa_sparse_attn_fwd_workspace_size": (_c_size, [_c_int, _c_int, _c_int, _c_int, _c_int]),
     "msa_sparse_attn_fwd": (_c_int, [_vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int,
                                      _c_int, _c_float, _vp, _vp, _vp, _c_size, _vp]),
+    "msa_sparse_attn_fwd_train": (_c_int, [_vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int,
+                                           _c_int, _c_float, _vp, _vp, _vp, _c_size, _vp, _c_size,
+                                           _vp]),
     "msa_sparse_attn_bwd_workspace_size": (_c_size, [_c_int, _c_int, _c_int, _c_int, _c_int]),
     "msa_sparse_attn_bwd": (_c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _c_int, _c_int,
                                      _c_int, _c_int, _c_int, _c_float, _vp, _vp, _vp, _vp,
@@ -260,8 +263,12 @@ def msa_index_select(q_idx, k_idx, cu_seqlens, max_seqlen: int, topk: int = TOPK
 
 def msa_sparse_attn_fwd(q, k, v, sel, cu_seqlens, max_seqlen: int, scale: Optional[float] = None,
                         out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
-                        workspace: Optional[torch.Tensor] = None):
-    """Block-sparse attention forward: (o bf16 [T, Hq, 128], lse fp32 [T, Hq])."""
+                        workspace: Optional[torch.Tensor] = None,
+                        bwd_workspace: Optional[torch.Tensor] = None):
+    """Block-sparse attention forward: (o bf16 [T, Hq, 128], lse fp32 [T, Hq]).
+    With bwd_workspace (msa_sparse_attn_fwd_train): that backward workspace's
+    accumulators are zeroed while the forward runs, for a following
+    msa_sparse_attn_bwd(..., workspace=bwd_workspace, prepared=True)."""
     T, Hq, Hkv = q.shape[0], q.shape[1], k.shape[1]
     _req(q, "q", torch.bfloat16, (T, Hq, D))
     _req(k, "k", torch.bfloat16, (T, Hkv, D))
@@ -276,9 +283,17 @@ def msa_sparse_attn_fwd(q, k, v, sel, cu_seqlens, max_seqlen: int, scale: Option
     _req(lse, "lse", torch.float32, (T, Hq))
     size = lib().msa_sparse_attn_fwd_workspace_size(T, S, Hq, Hkv, max_seqlen)
     ws = _workspace(size, q.device, workspace)
-    _check(lib().msa_sparse_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(sel), _ptr(cu_seqlens), S,
-                                     T, Hq, Hkv, max_seqlen, scale, _ptr(out), _ptr(lse),
-                                     _ptr(ws), ws.numel(), _stream(q)))
+    if bwd_workspace is None:
+        _check(lib().msa_sparse_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(sel), _ptr(cu_seqlens),
+                                         S, T, Hq, Hkv, max_seqlen, scale, _ptr(out), _ptr(lse),
+                                         _ptr(ws), ws.numel(), _stream(q)))
+    else:
+        bsize = lib().msa_sparse_attn_bwd_workspace_size(T, S, Hq, Hkv, max_seqlen)
+        bws = _workspace(bsize, q.device, bwd_workspace)
+        _check(lib().msa_sparse_attn_fwd_train(_ptr(q), _ptr(k), _ptr(v), _ptr(sel),
+                                               _ptr(cu_seqlens), S, T, Hq, Hkv, max_seqlen, scale,
+                                               _ptr(out), _ptr(lse), _ptr(ws), ws.numel(),
+                                               _ptr(bws), bws.numel(), _stream(q)))
     return out, lse
 
 

@@ -636,10 +636,11 @@ size_t msa_sparse_attn_fwd_workspace_size(int T, int S, int Hq, int Hkv, int max
   return ws.used + 256;
 }
 
-msa_status_t msa_sparse_attn_fwd(const void* q, const void* k, const void* v, const int32_t* sel,
-                                 const int32_t* cu_seqlens, int S, int T, int Hq, int Hkv,
-                                 int max_seqlen, float scale, void* o, float* lse,
-                                 void* workspace, size_t workspace_bytes, msa_stream_t stream) {
+static msa_status_t sparse_attn_fwd(const void* q, const void* k, const void* v,
+                                    const int32_t* sel, const int32_t* cu_seqlens, int S, int T,
+                                    int Hq, int Hkv, int max_seqlen, float scale, void* o,
+                                    float* lse, void* workspace, size_t workspace_bytes,
+                                    const FwdClear& clear, msa_stream_t stream) {
   MSA_REQUIRE_PTR(q);
   MSA_REQUIRE_PTR(k);
   MSA_REQUIRE_PTR(v);
@@ -657,7 +658,41 @@ msa_status_t msa_sparse_attn_fwd(const void* q, const void* k, const void* v, co
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   MSA_TRY(launch_plan(fw.plan, cu_seqlens, S, max_seqlen, st));
   return launch_sparse_fwd(q, k, v, sel, cu_seqlens, S, T, Hq, Hkv, max_seqlen, scale, fw, o,
-                           lse, st);
+                           lse, clear, st);
+}
+
+msa_status_t msa_sparse_attn_fwd(const void* q, const void* k, const void* v, const int32_t* sel,
+                                 const int32_t* cu_seqlens, int S, int T, int Hq, int Hkv,
+                                 int max_seqlen, float scale, void* o, float* lse,
+                                 void* workspace, size_t workspace_bytes, msa_stream_t stream) {
+  return sparse_attn_fwd(q, k, v, sel, cu_seqlens, S, T, Hq, Hkv, max_seqlen, scale, o, lse,
+                         workspace, workspace_bytes, FwdClear{}, stream);
+}
+
+msa_status_t msa_sparse_attn_fwd_train(const void* q, const void* k, const void* v,
+                                       const int32_t* sel, const int32_t* cu_seqlens, int S,
+                                       int T, int Hq, int Hkv, int max_seqlen, float scale,
+                                       void* o, float* lse, void* workspace,
+                                       size_t workspace_bytes, void* bwd_workspace,
+                                       size_t bwd_workspace_bytes, msa_stream_t stream) {
+  MSA_REQUIRE_PTR(bwd_workspace);
+  MSA_TRY(check_heads(Hq, Hkv));
+  if (T < 1 || S < 1 || max_seqlen < 1)
+    return fail(MSA_ERR_INVALID_ARG, "bad sizes T=%d S=%d max_seqlen=%d", T, S, max_seqlen);
+  if (bwd_workspace_bytes < msa_sparse_attn_bwd_workspace_size(T, S, Hq, Hkv, max_seqlen))
+    return fail(MSA_ERR_INVALID_ARG, "backward workspace too small");
+  WsCursor bws(bwd_workspace);
+  const BwdWorkspace bw = carve_bwd_workspace(bws, T, S, Hq, Hkv, max_seqlen);
+  // the three fp32 accumulators are carved back to back (multiples of 16
+  // bytes); the item counters after them are cleared as ints
+  FwdClear clear;
+  clear.ptr = bw.dq_acc;
+  clear.bytes = reinterpret_cast<uint8_t*>(bw.dv_acc + static_cast<size_t>(T) * Hkv * kD) -
+                reinterpret_cast<uint8_t*>(bw.dq_acc);
+  clear.ints = bw.item_ctr;
+  clear.nints = Hkv;
+  return sparse_attn_fwd(q, k, v, sel, cu_seqlens, S, T, Hq, Hkv, max_seqlen, scale, o, lse,
+                         workspace, workspace_bytes, clear, stream);
 }
 
 // ---------------------------------------------------------------- sparse backward

@@ -64,10 +64,20 @@ struct FwdWorkspace {
   int* tile_ctr;       // [Hkv] next tile to claim, zeroed by fwd_union_kernel
 };
 FwdWorkspace carve_fwd_workspace(WsCursor& ws, int T, int S, int Hkv);
+// A region to zero while the forward runs (e.g. the backward's fp32
+// accumulators): `bytes` (a multiple of 16) from the 16-byte aligned `ptr`,
+// written by bulk copies from a zeroed shared-memory buffer, plus `nints`
+// ints at `ints`.  Empty: ptr null, nints 0.
+struct FwdClear {
+  void* ptr = nullptr;
+  size_t bytes = 0;
+  int* ints = nullptr;
+  int nints = 0;
+};
 msa_status_t launch_sparse_fwd(const void* q, const void* k, const void* v, const int32_t* sel,
                                const int32_t* cu, int S, int T, int Hq, int Hkv, int max_seqlen,
                                float scale, const FwdWorkspace& fw, void* o, float* lse,
-                               cudaStream_t stream);
+                               const FwdClear& clear, cudaStream_t stream);
 
 // ---------------------------------------------------------------- sparse backward
 // Work items of the KV-major backward: (sequence, key block, segment of

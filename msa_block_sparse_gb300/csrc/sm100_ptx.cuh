@@ -160,6 +160,30 @@ __device__ __forceinline__ void bulk_reduce_add_f32(float* dst, const void* src,
       : "memory");
 }
 
+// Untiled bulk copy shared -> global, tracked by the issuing thread's bulk
+// async-group; both addresses 16-byte aligned, bytes % 16 == 0.
+__device__ __forceinline__ void bulk_store(void* dst, const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst),
+               "r"(smem_u32(src)), "r"(bytes)
+               : "memory");
+}
+
+// As bulk_store, with an L2 cache-eviction policy (createpolicy) for the writes.
+__device__ __forceinline__ void bulk_store_hint(void* dst, const void* src, uint32_t bytes,
+                                                uint64_t policy) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group.L2::cache_hint [%0], [%1], %2, %3;" ::
+                   "l"(dst),
+               "r"(smem_u32(src)), "r"(bytes), "l"(policy)
+               : "memory");
+}
+
+// An L2 policy under which the lines written are the first to be evicted.
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
 // Untiled bulk copy global -> shared; both addresses 16-byte aligned, bytes % 16 == 0.
 __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes,
                                           uint64_t* bar) {

@@ -14,7 +14,11 @@
 //            beforehand by fwd_union_kernel, one warp per tile) into a
 //            double-buffered slot, loads its Q tile and streams K_b through a
 //            2-stage TMA ring; warp 10 streams V_b through its own 2-stage
-//            ring, so neither ring's release holds up the other
+//            ring, so neither ring's release holds up the other, and for the
+//            training forward zeroes a given region (the backward's fp32
+//            accumulators) by 16 KB bulk copies of a zeroed shared buffer,
+//            one after each V block, with the memory bandwidth the forward
+//            leaves idle
 //   MMA (warps 1 and 11, one per 64-key half h): S_h = Q K_b[64h, 64h+64)^T
 //            into one of two TMEM buffers of the half; then
 //            O_h += P_h V_b[64h, 64h+64) with P_h read from TMEM as the A operand
@@ -58,10 +62,13 @@ struct TileInfo {
   uint32_t offs[2];                 // byte i: offset in the block of the tile's i-th token
 };
 
+constexpr int kZeroBytes = 16384;          // zeroed source of the bulk clearing copies
+
 struct FwdSmem {
   uint8_t q[2][kTile];
   uint8_t k[2][kTile];
   uint8_t v[2][kTile];
+  alignas(16) uint8_t zero[kZeroBytes];
   int ublk[2][kTpt * kTopK];                 // union entries (block << 8) | token mask
   int n_union[2];
   int tile_id[2];                           // tile of the slot; -1: no tiles left
@@ -321,7 +328,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                       const __grid_constant__ CUtensorMap tm_o, const int* __restrict__ ulist,
                       int* __restrict__ tile_ctr, const int32_t* __restrict__ cu, const int2* __restrict__ tiles,
                       const int* __restrict__ num_tiles, int Hq, int Hkv, float scale,
-                      __nv_bfloat16* __restrict__ o, float* __restrict__ lse, uint32_t* status) {
+                      __nv_bfloat16* __restrict__ o, float* __restrict__ lse,
+                      uint4* __restrict__ clear, size_t clear_u16, int* __restrict__ clear_ints,
+                      int n_clear_ints, uint32_t* status) {
   pdl_enter();
   const int total = *num_tiles * kG;
   if (static_cast<int>(blockIdx.x) >= total) return;
@@ -355,6 +364,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     mbar_init(&sm.o_done[0], kHalfThreads);
     mbar_init(&sm.o_done[1], kHalfThreads);
     fence_mbar_init();
+  }
+  if (clear_u16 > 0) {
+    for (int i = tid; i < kZeroBytes / 16; i += blockDim.x)
+      reinterpret_cast<uint4*>(sm.zero)[i] = make_uint4(0u, 0u, 0u, 0u);
+    fence_proxy_async_smem();                  // the zeros -> the bulk copies' reads
   }
   if (warp == 1) {
     tmem_alloc(&sm.tmem_base, 512);
@@ -481,6 +495,28 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     // ------------------------------------------------------------ V producer
     if (lane == 0) {
       prefetch_tmap(&tm_v);
+      // This CTA's share of the region to clear (the CTAs that have tiles
+      // split it evenly), one 16 KB bulk copy of zeros after each V block,
+      // the rest after the last one.
+      const size_t ncta = static_cast<size_t>(min(static_cast<int>(gridDim.x), total)) * gridDim.y;
+      const size_t cid = static_cast<size_t>(blockIdx.y) * min(static_cast<int>(gridDim.x), total) +
+                         blockIdx.x;
+      const size_t share = (clear_u16 + ncta - 1) / ncta;
+      size_t zb = cid * share < clear_u16 ? cid * share : clear_u16;
+      const size_t ze = zb + share < clear_u16 ? zb + share : clear_u16;
+      // the zeros are written evict-first: they are not read before the
+      // backward and should not push the forward's K and V out of L2
+      const uint64_t zpol = l2_policy_evict_first();
+      auto zero_one = [&]() {
+        if (zb < ze) {
+          const size_t n = ze - zb < kZeroBytes / 16 ? ze - zb : kZeroBytes / 16;
+          bulk_store_hint(clear + zb, sm.zero, static_cast<uint32_t>(n * 16), zpol);
+          bulk_commit_group();
+          zb += n;
+        }
+      };
+      if (cid == 0)
+        for (int i = 0; i < n_clear_ints; ++i) clear_ints[i] = 0;
       uint32_t tcount = 0, vc = 0;
       bool alive = true;
       for (;;) {
@@ -498,11 +534,14 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           tma_load_3d(sm.v[st], &tm_v, &sm.v_full[st], 0, g, row);
           tma_load_3d(sm.v[st] + kHalf, &tm_v, &sm.v_full[st], 64, g, row);
           ++vc;
+          zero_one();
         }
         if (!alive) break;
         mbar_arrive(&sm.tile_empty[tb]);   // done reading the tile's union list
         ++tcount;
       }
+      while (zb < ze) zero_one();
+      bulk_wait_all();                     // the zeros are written before the CTA exits
     }
   } else if (warp == 1 || warp == kMmaWarp1) {
     // ------------------------------------------------------------ MMA issuers
@@ -773,7 +812,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 msa_status_t launch_sparse_fwd(const void* q, const void* k, const void* v, const int32_t* sel,
                                const int32_t* cu, int S, int T, int Hq, int Hkv, int max_seqlen,
                                float scale, const FwdWorkspace& fw, void* o, float* lse,
-                               cudaStream_t stream) {
+                               const FwdClear& clear, cudaStream_t stream) {
+  if ((clear.ptr == nullptr) != (clear.bytes == 0) || clear.bytes % 16 != 0 ||
+      (reinterpret_cast<uintptr_t>(clear.ptr) & 15) != 0 || clear.nints < 0 ||
+      (clear.nints > 0 && clear.ints == nullptr))
+    return fail(MSA_ERR_INVALID_ARG, "forward: bad region to clear");
   const Plan& plan = fw.plan;
   (void)S;
   if (Hq / Hkv != kG)
@@ -815,7 +858,8 @@ msa_status_t launch_sparse_fwd(const void* q, const void* k, const void* v, cons
     TraceScope trace_("sparse_fwd_kernel", stream);
     launch_pdl(sparse_fwd_kernel, grid, kFwdThreads, smem, stream,
         tq, tk, tv, to, fw.ulist, fw.tile_ctr, cu, plan.tiles, plan.num_tiles, Hq, Hkv, scale,
-        static_cast<__nv_bfloat16*>(o), lse, sw);
+        static_cast<__nv_bfloat16*>(o), lse, static_cast<uint4*>(clear.ptr), clear.bytes / 16,
+        clear.ints, clear.nints, sw);
   }
   return check_launch("sparse_fwd_kernel");
 }

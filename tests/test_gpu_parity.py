@@ -540,6 +540,36 @@ def check_bwd_sampled(cpu, dq, dk, dv, sel, shape, toks, blocks, what, q=None, k
           f"worst rel-L2 {worst:.2e}")
 
 
+@pytest.mark.parametrize("name", ["tiny", "ragged"])
+def test_sparse_fwd_train_clears_bwd_workspace(m, name):
+    """msa_sparse_attn_fwd_train zeroes the backward workspace's accumulators
+    while it runs: with the workspace first filled with NaN bytes, its o and
+    lse equal the plain forward's bit for bit and the prepared backward that
+    follows matches the oracle and the unprepared backward."""
+    shape = SMALL[name]
+    cpu, gpu = inputs(name, shape)
+    osel, _ = oracle_selection(name, shape, cpu)
+    sel = torch.from_numpy(osel.astype(np.int32)).to(DEV)
+    cu = gpu["cu_seqlens"]
+    L = shape.max_seqlen
+    o_ref, lse_ref = m.msa_sparse_attn_fwd(gpu["q"], gpu["k"], gpu["v"], sel, cu, L)
+    ref = m.msa_sparse_attn_bwd(gpu["q"], gpu["k"], gpu["v"], o_ref, gpu["do"], lse_ref, sel, cu,
+                                L)
+    ws = torch.full((m.workspace_bytes("sparse_attn_bwd", shape.T, shape.S, shape.hq, shape.hkv,
+                                       L),), 0xFF, dtype=torch.uint8, device=DEV)
+    o, lse = m.msa_sparse_attn_fwd(gpu["q"], gpu["k"], gpu["v"], sel, cu, L, bwd_workspace=ws)
+    got = m.msa_sparse_attn_bwd(gpu["q"], gpu["k"], gpu["v"], o, gpu["do"], lse, sel, cu, L,
+                                workspace=ws, prepared=True)
+    m.msa_check_status()
+    assert torch.equal(o, o_ref) and torch.equal(lse, lse_ref)
+    rq, rk, rv = O.sparse_attn_bwd(f64(cpu["q"]), f64(cpu["k"]), f64(cpu["v"]), f64(cpu["do"]),
+                                   osel, cpu["cu_seqlens"].numpy(), SCALE)
+    for g_, r_, want, n in zip(got, ref, (rq, rk, rv), ("dq", "dk", "dv")):
+        assert torch.isfinite(g_.float()).all(), n
+        assert rel_l2(f64(g_), want) <= 1e-2, n
+        assert rel_l2(f64(g_), f64(r_)) <= 1e-3, n
+
+
 @pytest.mark.parametrize("idx", [1, 4])
 def test_sparse_bwd_full_size(m, idx):
     """Full-size backward with the oracle's selection: dq on >= 256 sampled
