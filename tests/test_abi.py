@@ -91,6 +91,23 @@ def test_unsupported_shapes_are_rejected(lib):
     assert rc == 2 and "16" in _err(lib)
 
 
+def test_training_forward_and_head_limits_are_checked_on_the_host(lib):
+    # the training forward needs a backward workspace of the backward's size
+    rc = lib.msa_sparse_attn_fwd_train(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 100, 16, 1, 100, 0.1,
+                                       FAKE, FAKE, FAKE, 1 << 20, None, 1 << 30, None)
+    assert rc == 1 and "bwd_workspace" in _err(lib)
+    need = lib.msa_sparse_attn_bwd_workspace_size(100, 1, 16, 1, 100)
+    rc = lib.msa_sparse_attn_fwd_train(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 100, 16, 1, 100, 0.1,
+                                       FAKE, FAKE, FAKE, 1 << 20, FAKE, need - 1, None)
+    assert rc == 1 and "workspace" in _err(lib)
+    # the prologue kernels take at most 256 heads per tensor
+    rc = lib.msa_qk_norm_rope(FAKE, FAKE, 10, 257, FAKE, FAKE, 1, 64, 1e7, 1e-6, None)
+    assert rc == 2 and "256" in _err(lib)
+    rc = lib.msa_qk_norm_rope_bwd(FAKE, FAKE, FAKE, FAKE, 10, 257, FAKE, FAKE, 1, 64, 1e7, 1e-6,
+                                  FAKE, 1 << 30, None)
+    assert rc == 2 and "256" in _err(lib)
+
+
 def test_python_binding_refuses_cpu_tensors():
     import torch
     x = torch.zeros(4, 1, 128, dtype=torch.bfloat16)
