@@ -285,7 +285,7 @@ __global__ void __launch_bounds__(kBwdSegment) bwd_lists_kernel(
 // For query row (t, 16 g + j): lsd[32 (t Hkv + g) + j] = -lse log2 e and
 // lsd[32 (t Hkv + g) + 16 + j] = -sum_d dout o (= -Delta).  16 lanes per row
 // (16-byte loads), kDeltaRows rows per thread with all loads issued first.
-constexpr int kDeltaRows = 4;
+constexpr int kDeltaRows = 2;
 __global__ void __launch_bounds__(256) bwd_delta_kernel(
     const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* __restrict__ dout,
     const float* __restrict__ lse, float* __restrict__ lsd, size_t rows,
