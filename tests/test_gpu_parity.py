@@ -366,6 +366,34 @@ def test_index_select_exact_ties(m):
                           f"{got[bad[0]].tolist()} != {want[bad[0]].tolist()}"
 
 
+def test_index_select_max_seqlen(m):
+    """One sequence of the longest supported length (1024 blocks of 128 tokens)
+    beside a short one: the plans' largest histograms, chunks longer than 16
+    blocks (the insert-as-they-come path) and up to 1023 earlier blocks per
+    query tile; sampled rows against the oracle.  One token more is refused
+    before anything runs."""
+    L = 1024 * 128
+    cu_cpu = torch.tensor([0, L, L + 300], dtype=torch.int32)
+    T = L + 300
+    gen = torch.Generator().manual_seed(1024)
+    qi = torch.randn((T, 1, 128), generator=gen).to(torch.bfloat16)
+    ki = torch.randn((T, 1, 128), generator=gen).to(torch.bfloat16)
+    sel = m.msa_index_select(qi.to(DEV), ki.to(DEV), cu_cpu.to(DEV), L)
+    m.msa_check_status()
+    rng = np.random.default_rng(1024)
+    toks = sorted({0, 127, 128, 2047, 16383, 16384, 65535, 65536, L - 129, L - 128, L - 1, L,
+                   T - 1} | set(int(x) for x in rng.integers(0, T, 24)))
+    cun = cu_cpu.numpy()
+    osel, gap = O.index_select(f64(qi), f64(ki), cun, tokens=toks)
+    compare_selection(sel.cpu().numpy()[toks], osel, gap, "max seqlen",
+                      own_blocks({"cu_seqlens": cu_cpu}, toks),
+                      SC.prefill_scores_of(f64(qi), f64(ki), cun, toks))
+    cu2 = torch.tensor([0, L + 1, T], dtype=torch.int32, device=DEV)
+    with pytest.raises(m.MSAError):
+        m.msa_index_select(qi.to(DEV), ki.to(DEV), cu2, L + 1)
+    m.msa_check_status()
+
+
 # ------------------------------------------------------------------ forward
 
 @pytest.mark.parametrize("name", ["tiny", "ragged"])
