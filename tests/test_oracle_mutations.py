@@ -49,6 +49,29 @@ def _select_init_rescored(scores, own, topk=O.TOPK, n_init=0):
     return sel, np.full(n, np.inf)
 
 
+def _select_streaming_insert_skips_ties(scores, own, topk=O.TOPK, n_init=0):
+    # blocks taken in ascending order into a list kept by score, each new one
+    # placed where it first beats an entry and the displaced entries carried on
+    # with a strict comparison, so a displaced entry passes entries of equal
+    # score (ties then stay in block order only while nothing larger arrives)
+    n = scores.shape[0]
+    sel = np.full((n, topk), -1, dtype=np.int64)
+    for r in range(n):
+        o = int(own[r])
+        ni = min(n_init, o)
+        slots = topk - 1 - ni
+        best = [(-np.inf, -1)] * max(slots, 0)
+        for b in range(ni, o):
+            cv, ci = scores[r, b], b
+            for i in range(len(best)):
+                if cv > best[i][0]:
+                    best[i], (cv, ci) = (cv, ci), best[i]
+        keep = [b for _, b in best if b >= 0]
+        ids = np.sort(np.concatenate([np.arange(ni), np.array(keep, dtype=np.int64), [o]]))
+        sel[r, :len(ids)] = ids
+    return sel, _ORIG["select_from_scores"](scores, own, topk, n_init)[1]
+
+
 def _gap_variant(scores, own, topk, n_init, shift, denom):
     """select_from_scores with its near-tie gap taken between scored candidates
     `slots - 1 + shift` and `slots + shift`, relative to `denom` of the two."""
@@ -167,6 +190,8 @@ MUTATIONS = [
     ("gemma_rmsnorm", _norm_without_one, [P.test_gemma_rmsnorm_matches_torch_rms_norm]),
     ("gemma_rmsnorm", _norm_eps_outside, [P.test_gemma_rmsnorm_zero_weight_gives_unit_rms]),
     ("select_from_scores", _select_higher_id_on_tie, [P.test_selection_tie_prefers_lower_block]),
+    ("select_from_scores", _select_streaming_insert_skips_ties,
+     [P.test_selection_with_exact_ties_then_larger_scores]),
     ("select_from_scores", _select_own_not_forced, [P.test_selection_invariants]),
     ("select_from_scores", _select_init_rescored, [P.test_init_rule_by_enumeration]),
     ("select_from_scores", _gap_one_past_the_cut, [P.test_near_tie_gap_exact_values]),

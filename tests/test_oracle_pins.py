@@ -328,6 +328,31 @@ def test_selection_tie_prefers_lower_block():
     assert gap[0] == 0.0
 
 
+def test_selection_with_exact_ties_then_larger_scores():
+    """Key blocks 0 .. 9 copies of one block B, later ones copies of 2B: every
+    earlier block scores exactly m or 2m (m > 0 for these queries), so the
+    rule alone gives each row's selection: the lowest 2B blocks first, then
+    the lowest B blocks in the places left, then the own block."""
+    g = rng(9)
+    L = 20 * 128
+    blk = g.standard_normal((128, 1, 128))
+    ki = np.concatenate([blk * (2.0 if b >= 10 else 1.0) for b in range(20)], axis=0)
+    qi = g.standard_normal((L, 1, 128))
+    assert np.all((qi[:, 0] @ blk[:, 0].T).max(axis=1) > 0)
+    sel, gap = O.index_select(qi, ki, np.array([0, L]))
+    for t in range(L):
+        o = t // 128
+        hi = list(range(10, o))[:15]
+        lo = list(range(min(o, 10)))[:15 - len(hi)]
+        want = sorted(hi + lo + [o])
+        assert list(sel[t, 0, :len(want)]) == want and np.all(sel[t, 0, len(want):] == -1), t
+        # with more than 15 earlier blocks the cut falls between two equal
+        # scores (gap 0) except at o = 25, where it falls between the last of
+        # the fifteen 2m blocks and block 0 (gap (2m - m) / 2m = 1/2)
+        if o > 15:
+            assert gap[t, 0] == (0.5 if o == 25 else 0.0), t
+
+
 def test_near_tie_gap_exact_values():
     """The near-tie gap compares the last kept scored block with the first
     dropped one, relative to the larger magnitude of the two (the parity rule:
